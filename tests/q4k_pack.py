@@ -1,0 +1,35 @@
+"""Test-side helpers that BUILD Q4_K bytes from chosen values (the inverse direction of
+the oracle's decoder), so that a transposed index or a wrong bit field in the decoder
+shows up as a mismatch.  Written from the GGUF K-quant layout description: eight 6-bit
+sub-scales and eight 6-bit sub-mins packed into 12 bytes, sub-blocks 4..7 split into a
+low nibble (bytes 8..11) and two top bits (the spare top bits of bytes 0..7)."""
+import numpy as np
+
+
+def pack_scales(sc, m) -> np.ndarray:
+    sc = [int(v) for v in sc]
+    m = [int(v) for v in m]
+    assert len(sc) == 8 and len(m) == 8 and all(0 <= v < 64 for v in sc + m)
+    p = np.zeros(12, dtype=np.uint8)
+    for j in range(4):
+        p[j] = sc[j] | ((sc[j + 4] >> 4) << 6)
+        p[j + 4] = m[j] | ((m[j + 4] >> 4) << 6)
+        p[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    return p
+
+
+def pack_nibbles(codes) -> np.ndarray:
+    """256 codes (0..15) in element order -> 128 bytes: byte 32c+i holds element 64c+i
+    in its low half and element 64c+32+i in its high half."""
+    codes = np.asarray(codes, dtype=np.uint8).reshape(4, 2, 32)
+    assert codes.max() < 16
+    return (codes[:, 0, :] | (codes[:, 1, :] << 4)).reshape(128).astype(np.uint8)
+
+
+def super_block(d_f16: int, dmin_f16: int, sc, m, codes) -> np.ndarray:
+    b = np.zeros(144, dtype=np.uint8)
+    b[0:2] = np.array([d_f16], dtype=np.uint16).view(np.uint8)
+    b[2:4] = np.array([dmin_f16], dtype=np.uint16).view(np.uint8)
+    b[4:16] = pack_scales(sc, m)
+    b[16:] = pack_nibbles(codes)
+    return b
