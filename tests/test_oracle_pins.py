@@ -136,6 +136,13 @@ def test_hand_example_nontrivial_scale(golden_hand):
     assert d == as_ints(g["e2_d_f16"])[0] and s == as_ints(g["e2_s_f16"])[0]
 
 
+def test_hand_example_true_division(golden_hand):
+    g = golden_hand
+    _, d, s, q = _quant_one(as_floats(g["e5_x"]))
+    assert q == as_ints(g["e5_q"])
+    assert d == as_ints(g["e5_d_f16"])[0] and s == as_ints(g["e5_s_f16"])[0]
+
+
 def test_hand_example_q4_k_super_block(golden_hand):
     g = golden_hand
     xq1, _, _, _ = _quant_one(as_floats(g["e1_x"]))
