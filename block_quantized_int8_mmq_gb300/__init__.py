@@ -1,0 +1,162 @@
+"""Python binding of libmmq, the GB300 (sm_103a) block-quantized int8 matrix multiply.
+
+Each function has the name of the C entry point it calls (include/mmq.h) and only
+marshals arguments: torch tensors supply device memory and the current CUDA stream,
+every computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+libmmq.so is not built, importing this package raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmmq.so")
+
+QK, QK_K = 32, 256
+Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES = 36, 34, 144
+FMT = {"q8_0": 0, "q4_k": 1}
+PATH_AUTO, PATH_SMALL, PATH_TC = 0, 1, 2
+
+EXPORTED = (
+    "mmq_status_string", "mmq_q8_1_bytes", "mmq_weight_row_bytes", "mmq_quantize_q8_1",
+    "mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k",
+    "mmq_set_path", "mmq_last_path", "mmq_get_device_error",
+)
+
+
+class MMQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_lib.mmq_status_string(status).decode()} ({status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run `python block_quantized_int8_mmq_gb300/_build.py`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.mmq_status_string.argtypes = [I]
+    L.mmq_status_string.restype = ctypes.c_char_p
+    L.mmq_q8_1_bytes.argtypes = [I64, I64]
+    L.mmq_q8_1_bytes.restype = ctypes.c_size_t
+    L.mmq_weight_row_bytes.argtypes = [I, I64]
+    L.mmq_weight_row_bytes.restype = ctypes.c_size_t
+    L.mmq_quantize_q8_1.argtypes = [P, I64, I64, P, P]
+    for f in ("mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k"):
+        getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P]
+    L.mmq_set_path.argtypes = [I]
+    L.mmq_get_device_error.argtypes = [P]
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn, st):
+    if st != 0:
+        raise MMQError(fn, st)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def mmq_status_string(status: int) -> str:
+    return _lib.mmq_status_string(int(status)).decode()
+
+
+def mmq_q8_1_bytes(M: int, K: int) -> int:
+    return int(_lib.mmq_q8_1_bytes(M, K))
+
+
+def mmq_weight_row_bytes(fmt: str, K: int) -> int:
+    return int(_lib.mmq_weight_row_bytes(FMT[fmt], K))
+
+
+def mmq_quantize_q8_1(x, xq=None, stream=None):
+    """x: f32 [M, K] CUDA tensor -> uint8 [M, K/32*36] q8_1 blocks."""
+    import torch
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K // QK * Q8_1_BYTES), dtype=torch.uint8, device=x.device)
+    _check("mmq_quantize_q8_1", _lib.mmq_quantize_q8_1(_ptr(x), M, K, _ptr(xq), _stream(stream)))
+    return xq
+
+
+def _gemm(fn, xq, wq, M, N, K, out, stream):
+    import torch
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    _check(fn, getattr(_lib, fn)(_ptr(xq), _ptr(wq), M, N, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def mmq_gemm_q8_0(xq, wq, M, N, K, out=None, stream=None):
+    """q8_1 [M, K/32*36] x Q8_0 [N, K/32*34] -> f32 [M, N]."""
+    return _gemm("mmq_gemm_q8_0", xq, wq, M, N, K, out, stream)
+
+
+def mmq_gemm_q4_k(xq, wq, M, N, K, out=None, stream=None):
+    """q8_1 [M, K/32*36] x Q4_K [N, K/256*144] -> f32 [M, N]."""
+    return _gemm("mmq_gemm_q4_k", xq, wq, M, N, K, out, stream)
+
+
+def _dots(fn, xq, wq, M, N, K, dots, stream):
+    import torch
+    if dots is None:
+        dots = torch.empty((M, N, K // QK), dtype=torch.int32, device=xq.device)
+    _check(fn, getattr(_lib, fn)(_ptr(xq), _ptr(wq), M, N, K, _ptr(dots), _stream(stream)))
+    return dots
+
+
+def mmq_debug_block_dots_q8_0(xq, wq, M, N, K, dots=None, stream=None):
+    return _dots("mmq_debug_block_dots_q8_0", xq, wq, M, N, K, dots, stream)
+
+
+def mmq_debug_block_dots_q4_k(xq, wq, M, N, K, dots=None, stream=None):
+    return _dots("mmq_debug_block_dots_q4_k", xq, wq, M, N, K, dots, stream)
+
+
+def mmq_set_path(path: int) -> int:
+    prev = _lib.mmq_set_path(int(path))
+    if prev < 0:
+        raise MMQError("mmq_set_path", prev)
+    return prev
+
+
+def mmq_last_path() -> int:
+    return int(_lib.mmq_last_path())
+
+
+def mmq_get_device_error(stream=None) -> int:
+    return int(_lib.mmq_get_device_error(_stream(stream)))
+
+
+def gemm(fmt: str, xq, wq, M, N, K, out=None, stream=None):
+    return (mmq_gemm_q8_0 if fmt == "q8_0" else mmq_gemm_q4_k)(xq, wq, M, N, K, out, stream)
+
+
+def block_dots(fmt: str, xq, wq, M, N, K, dots=None, stream=None):
+    f = mmq_debug_block_dots_q8_0 if fmt == "q8_0" else mmq_debug_block_dots_q4_k
+    return f(xq, wq, M, N, K, dots, stream)
+
+
+def mmq_linear(x, wq, fmt: str, N: int, xq=None, out=None, stream=None):
+    """Quantize x (f32 [M, K]) to q8_1 and contract it with weights wq: f32 [M, N]."""
+    M, K = x.shape
+    xq = mmq_quantize_q8_1(x, xq, stream)
+    return gemm(fmt, xq, wq, M, N, K, out, stream)

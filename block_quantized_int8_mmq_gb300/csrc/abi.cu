@@ -1,0 +1,185 @@
+// C ABI of libmmq: argument checks, kernel selection and the error protocol.
+//
+// Error protocol ("13 . r7-r8 raw-byte MMQ kernel", sec. 3.3, the silent-failure
+// lesson): every call returns a status; a refused call launches nothing and prints one
+// stderr line; a failed launch is read with cudaGetLastError (which also clears it) and
+// reported, so a benchmark can never time a kernel that did not run.
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace mmq {
+
+void report(const char* fn, int status, const char* detail) {
+    fprintf(stderr, "libmmq: %s refused: %s (%s)\n", fn, mmq_status_string(status), detail);
+}
+
+int launch_status(const char* fn) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        fprintf(stderr, "libmmq: %s launch failed: %s\n", fn, cudaGetErrorString(e));
+        return MMQ_ERR_LAUNCH;
+    }
+    return MMQ_OK;
+}
+
+bool tc_available();
+
+namespace {
+
+std::atomic<int> g_path{-1};
+thread_local int t_last_path = 0;
+
+int current_path() {
+    int p = g_path.load();
+    if (p < 0) {
+        p = MMQ_PATH_AUTO;
+        const char* env = getenv("MMQ_FORCE_PATH");
+        if (env && strcmp(env, "small") == 0) p = MMQ_PATH_SMALL;
+        if (env && strcmp(env, "tc") == 0) p = MMQ_PATH_TC;
+        int expected = -1;
+        g_path.compare_exchange_strong(expected, p);
+        p = g_path.load();
+    }
+    return p;
+}
+
+constexpr int64_t LIMIT = (int64_t)1 << 40;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_mk(const char* fn, int64_t M, int64_t N, int64_t K, int64_t kmul) {
+    if (M < 1 || N < 1 || K < 1) {
+        report(fn, MMQ_ERR_SHAPE, "M, N and K must be >= 1");
+        return MMQ_ERR_SHAPE;
+    }
+    if (K % kmul != 0) {
+        report(fn, MMQ_ERR_K_MULTIPLE, kmul == 256 ? "K % 256 != 0" : "K % 32 != 0");
+        return MMQ_ERR_K_MULTIPLE;
+    }
+    if (M > LIMIT / K || N > LIMIT / K || M > LIMIT / N || K / QK > 0x7fffffff || N > 0x7fffffff ||
+        M > 0x7fffffff) {
+        report(fn, MMQ_ERR_SHAPE, "size product too large");
+        return MMQ_ERR_SHAPE;
+    }
+    return MMQ_OK;
+}
+
+int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
+                float* out, int32_t* dots, void* stream) {
+    int st = check_mk(fn, M, N, K, fmt == FMT_Q4_K ? QK_K : QK);
+    if (st) return st;
+    void* o = out ? static_cast<void*>(out) : static_cast<void*>(dots);
+    if (!xq || !wq || !o) {
+        report(fn, MMQ_ERR_NULL, "xq, wq and the output must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(o, 16)) {
+        report(fn, MMQ_ERR_ALIGN, "xq, wq and the output must be 16-byte aligned");
+        return MMQ_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int path = current_path();
+    const bool small = path == MMQ_PATH_SMALL || (path == MMQ_PATH_AUTO && (M <= 8 || !tc_available()));
+    if (small) {
+        st = small_launch(fmt, xq, wq, M, N, K, out, dots, s);
+        if (st == MMQ_OK) t_last_path = MMQ_PATH_SMALL;
+    } else {
+        st = tc_launch(fmt, xq, wq, M, N, K, out, dots, s);
+        if (st == MMQ_OK) t_last_path = MMQ_PATH_TC;
+    }
+    return st;
+}
+
+}  // namespace
+}  // namespace mmq
+
+using namespace mmq;
+
+extern "C" {
+
+const char* mmq_status_string(int status) {
+    switch (status) {
+        case MMQ_OK: return "MMQ_OK";
+        case MMQ_ERR_SHAPE: return "MMQ_ERR_SHAPE";
+        case MMQ_ERR_K_MULTIPLE: return "MMQ_ERR_K_MULTIPLE";
+        case MMQ_ERR_NULL: return "MMQ_ERR_NULL";
+        case MMQ_ERR_ALIGN: return "MMQ_ERR_ALIGN";
+        case MMQ_ERR_SMEM: return "MMQ_ERR_SMEM";
+        case MMQ_ERR_LAUNCH: return "MMQ_ERR_LAUNCH";
+        case MMQ_ERR_TIMEOUT: return "MMQ_ERR_TIMEOUT";
+        case MMQ_ERR_CUDA: return "MMQ_ERR_CUDA";
+        case MMQ_ERR_ARG: return "MMQ_ERR_ARG";
+        default: return "MMQ_ERR_UNKNOWN";
+    }
+}
+
+size_t mmq_q8_1_bytes(int64_t M, int64_t K) {
+    if (M < 0 || K < 0 || K % QK != 0) return 0;
+    return (size_t)M * (size_t)(K / QK) * Q8_1_BYTES;
+}
+
+size_t mmq_weight_row_bytes(int fmt, int64_t K) {
+    if (K < 0) return 0;
+    if (fmt == FMT_Q8_0 && K % QK == 0) return (size_t)(K / QK) * Q8_0_BYTES;
+    if (fmt == FMT_Q4_K && K % QK_K == 0) return (size_t)(K / QK_K) * Q4_K_BYTES;
+    return 0;
+}
+
+int mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, void* stream) {
+    const char* fn = "mmq_quantize_q8_1";
+    int st = check_mk(fn, M, 1, K, QK);
+    if (st) return st;
+    if (!x || !xq) {
+        report(fn, MMQ_ERR_NULL, "x and xq must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    if (!aligned(x, 16) || !aligned(xq, 4)) {
+        report(fn, MMQ_ERR_ALIGN, "x must be 16-byte and xq 4-byte aligned");
+        return MMQ_ERR_ALIGN;
+    }
+    return quantize_launch(x, M, K, xq, static_cast<cudaStream_t>(stream));
+}
+
+int mmq_gemm_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, void* stream) {
+    return contraction("mmq_gemm_q8_0", FMT_Q8_0, xq, wq, M, N, K, out, nullptr, stream);
+}
+
+int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, void* stream) {
+    return contraction("mmq_gemm_q4_k", FMT_Q4_K, xq, wq, M, N, K, out, nullptr, stream);
+}
+
+int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,
+                              void* stream) {
+    return contraction("mmq_debug_block_dots_q8_0", FMT_Q8_0, xq, wq, M, N, K, nullptr, dots, stream);
+}
+
+int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,
+                              void* stream) {
+    return contraction("mmq_debug_block_dots_q4_k", FMT_Q4_K, xq, wq, M, N, K, nullptr, dots, stream);
+}
+
+int mmq_set_path(int path) {
+    if (path != MMQ_PATH_AUTO && path != MMQ_PATH_SMALL && path != MMQ_PATH_TC) return MMQ_ERR_ARG;
+    const int prev = current_path();
+    g_path.store(path);
+    return prev;
+}
+
+int mmq_last_path(void) { return t_last_path; }
+
+int mmq_get_device_error(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        fprintf(stderr, "libmmq: mmq_get_device_error: %s\n", cudaGetErrorString(e));
+        return MMQ_ERR_CUDA;
+    }
+    const unsigned bits = tc_take_error();
+    return (bits & ERR_TIMEOUT) ? MMQ_ERR_TIMEOUT : MMQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Shared device/host helpers of libmmq (sm_103a).  Block-format constants follow the
+// q8_1 / Q8_0 / Q4_K layouts described in include/mmq.h.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mmq.h"
+
+namespace mmq {
+
+constexpr int QK = 32;           // values per q8_1 / Q8_0 block and per Q4_K sub-block
+constexpr int QK_K = 256;        // values per Q4_K super-block
+constexpr int Q8_1_BYTES = 36;   // f16 d, f16 s, int8 q[32]
+constexpr int Q8_0_BYTES = 34;   // f16 d, int8 q[32]
+constexpr int Q4_K_BYTES = 144;  // f16 d, f16 dmin, 12 scale bytes, 128 nibble bytes
+
+enum WeightFormat { FMT_Q8_0 = 0, FMT_Q4_K = 1 };
+
+// Error bits a kernel may set in its translation unit's device error word.
+constexpr unsigned ERR_TIMEOUT = 1u;
+
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
+    return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xffffu)));
+}
+
+// Q4_K: 6-bit sub-scale and sub-min of sub-block j (0..7) from the 12 packed scale
+// bytes, given as three little-endian words s0 = bytes 0..3, s1 = 4..7, s2 = 8..11.
+// Sub-blocks 0..3: low 6 bits of byte j (scale) and byte j+4 (min).  Sub-blocks 4..7:
+// low nibble / high nibble of byte j+4 (scale / min low bits) and the top two bits of
+// byte j-4 (scale) and byte j (min).
+__device__ __forceinline__ void q4_k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j,
+                                               int& sc, int& mn) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        mn = (s1 >> (8 * j)) & 63;
+    } else {
+        const int i = j - 4;
+        const uint32_t lo = (s2 >> (8 * i)) & 0xff;
+        sc = (lo & 15) | (((s0 >> (8 * i + 6)) & 3) << 4);
+        mn = (lo >> 4) | (((s1 >> (8 * i + 6)) & 3) << 4);
+    }
+}
+
+}  // namespace mmq
+
+// Host-side per-translation-unit hooks (defined in each .cu that owns kernels).
+namespace mmq {
+int quantize_launch(const float* x, int64_t M, int64_t K, void* xq, cudaStream_t s);
+int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                 int32_t* dots, cudaStream_t s);
+int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+              int32_t* dots, cudaStream_t s);
+unsigned tc_take_error();
+void report(const char* fn, int status, const char* detail);
+int launch_status(const char* fn);
+}  // namespace mmq

@@ -1,0 +1,147 @@
+/*
+ * mmq.h -- C ABI of the GB300 (sm_103a) block-quantized int8 matrix multiply library
+ * (libmmq.so).
+ *
+ * The operation: activations x (f32, M rows of K) are quantized to q8_1 blocks and
+ * contracted against block-quantized weights (Q8_0 or Q4_K, N rows of K):
+ *
+ *   out[m,n] = sum over 32-element blocks b of (xd[m,b] * wd[n,b]) * sum_{k in b} xq[m,k] * wq[n,k]
+ *
+ * with, for Q4_K, wd = d * sc_j of the block's 256-element super-block and an extra
+ * -dmin * m_j * xs[m,b] per block ("When the Product Won't Collapse: A Negative Result
+ * on int8 Tensor-Core MMQ", sec. "The obstruction: an opaque accumulator", display
+ * equation; "When Does a Kernel Win Surface?", sec. "Kept levers: Vulkan", the Q4_K x
+ * q8_1 affine identity).  The scale is applied at every 32-block boundary because the
+ * integer sum is only meaningful inside one constant-scale block.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named x, xq, wq, out, dots are DEVICE pointers owned by the caller.  The
+ *    library never frees or retains them and allocates no device memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call is
+ *    asynchronous on that stream; results are valid once the stream has reached them.
+ *  - Return value: MMQ_OK (0) or a negative mmq_status.  A call that returns an error
+ *    for its arguments launches nothing and writes nothing, and prints one line on
+ *    stderr.  A failed launch is reported (the CUDA error is cleared first), never
+ *    ignored: a call that returns MMQ_OK has enqueued the complete computation.
+ *  - Device-side bounded waits (pipeline barriers) that run out set a sticky device
+ *    error word instead of hanging; mmq_get_device_error() reads and clears it.
+ *  - Shapes: 1 <= M, N and K a positive multiple of 32 (q8_1, Q8_0) or of 256 (Q4_K);
+ *    all of M*K, N*K and M*N below 2^40.
+ *  - Finite inputs are required; NaN or Inf in x gives unspecified codes.
+ *
+ * Byte layouts (little-endian):
+ *  q8_1 block (36 B): f16 d @0, f16 s @2, int8 q[32] @4.  A quantized activation matrix
+ *    is [M][K/32] blocks, row-major, contiguous.  d = amax/127 (f32), q = rint(x/d)
+ *    (IEEE division, ties to even) clamped to [-127, 127], s = f16(f32(d) * sum(q)).
+ *  Q8_0 block (34 B): f16 d @0, int8 q[32] @2.  Weights are [N][K/32] blocks.
+ *  Q4_K super-block (144 B, 256 values): f16 d @0, f16 dmin @2, 12 bytes of eight 6-bit
+ *    sub-scales sc_j and eight 6-bit sub-mins m_j @4 (GGUF K-quant packing), 128 nibble
+ *    bytes @16 (byte 32c+i: low nibble = value 64c+i, high nibble = value 64c+32+i).
+ *    Weights are [N][K/256] super-blocks.  Value = d*sc_j*q - dmin*m_j, q in 0..15
+ *    ("13 . r7-r8 raw-byte MMQ kernel", sec. 2 and sec. 3.2).
+ *  out: f32 [M][N] row-major, fully overwritten (no accumulate mode).
+ */
+#ifndef MMQ_H
+#define MMQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mmq_status {
+    MMQ_OK = 0,
+    MMQ_ERR_SHAPE = -1,       /* M, N or K < 1, or a size product too large */
+    MMQ_ERR_K_MULTIPLE = -2,  /* K not a multiple of 32 (q8_1, Q8_0) or 256 (Q4_K) */
+    MMQ_ERR_NULL = -3,        /* a required pointer is NULL */
+    MMQ_ERR_ALIGN = -4,       /* a pointer breaks its alignment rule (see each call) */
+    MMQ_ERR_SMEM = -5,        /* the kernel's shared-memory request was refused */
+    MMQ_ERR_LAUNCH = -6,      /* the kernel launch failed (CUDA error cleared) */
+    MMQ_ERR_TIMEOUT = -7,     /* a device-side bounded wait ran out (device error word) */
+    MMQ_ERR_CUDA = -8,        /* another CUDA runtime error (device query, tensor map) */
+    MMQ_ERR_ARG = -9          /* an argument outside its documented set */
+} mmq_status;
+
+/* Human-readable name of a status code.  Never NULL; the string is static. */
+const char* mmq_status_string(int status);
+
+/* Bytes of a q8_1 matrix of M rows of K values: M * (K/32) * 36.  0 if K % 32 != 0
+ * or a size is negative. */
+size_t mmq_q8_1_bytes(int64_t M, int64_t K);
+
+/* Bytes of one weight row of K values: K/32*34 (Q8_0) or K/256*144 (Q4_K).
+ * fmt: 0 = Q8_0, 1 = Q4_K.  0 for an invalid fmt or K. */
+size_t mmq_weight_row_bytes(int fmt, int64_t K);
+
+/*
+ * Quantize activations to q8_1 ("13 . r7-r8 raw-byte MMQ kernel", sec. 3.2, the
+ * quantize pass: block amax, scale, round, clamp, block sum; the q8_1 block keeps the
+ * f16 scale and the f16 block sum s = d * sum(q)).
+ *   x:  f32 [M][K] row-major, 16-byte aligned.
+ *   xq: output, mmq_q8_1_bytes(M, K) bytes, 4-byte aligned.
+ * Bit-exact: the same bytes as the definition evaluated with IEEE f32 arithmetic.
+ * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE (K % 32), MMQ_ERR_NULL, MMQ_ERR_ALIGN,
+ * MMQ_ERR_LAUNCH.
+ */
+int mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, void* stream);
+
+/*
+ * out = xq (q8_1, [M][K/32]) contracted with Q8_0 weights wq ([N][K/32] blocks)
+ * ("When the Product Won't Collapse", sec. "The obstruction", display equation).
+ *   xq: 16-byte aligned.  wq: 16-byte aligned.  out: f32 [M][N], 16-byte aligned.
+ * Accuracy: |out - exact| <= 1e-4 * sum_b |xd*wd*D_b| per entry, with the block dots
+ * D_b computed exactly.
+ * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE (K % 32), MMQ_ERR_NULL, MMQ_ERR_ALIGN,
+ * MMQ_ERR_SMEM, MMQ_ERR_LAUNCH.
+ */
+int mmq_gemm_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                  void* stream);
+
+/*
+ * out = xq (q8_1) contracted with Q4_K weights wq ([N][K/256] super-blocks), including
+ * the -dmin*m_j*s min term of every sub-block ("When Does a Kernel Win Surface?", sec.
+ * "Kept levers: Vulkan", affine identity; "13 . r7-r8 raw-byte MMQ kernel", sec. 3.1:
+ * whole super-blocks only, so K % 256 == 0).
+ *   Alignment and accuracy as mmq_gemm_q8_0 (the norm adds |dmin*m_j*xs| per block).
+ * Errors: as mmq_gemm_q8_0, with MMQ_ERR_K_MULTIPLE for K % 256.
+ */
+int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                  void* stream);
+
+/*
+ * Test hook: the per-block int32 dots D[m][n][b] (b < K/32) computed by the SAME data
+ * path as mmq_gemm_q8_0 / mmq_gemm_q4_k select for this M (same staging, same
+ * conversion, same MMA), written out instead of rescaled.  For Q4_K, D is the dot of
+ * the activation codes with the raw 4-bit codes (0..15), without sc_j.
+ *   dots: int32 [M][N][K/32], 16-byte aligned.  Bit-exact by definition.
+ */
+int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
+                              int32_t* dots, void* stream);
+int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
+                              int32_t* dots, void* stream);
+
+/* Kernel selection for the two contractions and their test hooks.
+ *   MMQ_PATH_AUTO  : by M (small-M warp kernel for M <= 8, tensor-core kernel above).
+ *   MMQ_PATH_SMALL : always the warp-level kernel (any M; slow for large M).
+ *   MMQ_PATH_TC    : always the tcgen05 tensor-core kernel.
+ * Process-wide; the environment variable MMQ_FORCE_PATH=auto|small|tc sets the initial
+ * value.  Returns the previous value, or MMQ_ERR_ARG. */
+enum { MMQ_PATH_AUTO = 0, MMQ_PATH_SMALL = 1, MMQ_PATH_TC = 2 };
+int mmq_set_path(int path);
+
+/* Path the last successful contraction or test-hook call on this thread took
+ * (MMQ_PATH_SMALL or MMQ_PATH_TC), or 0 before any. */
+int mmq_last_path(void);
+
+/* Synchronizes `stream`, then reads and clears the device error word of every kernel
+ * in the library.  Returns MMQ_OK, MMQ_ERR_TIMEOUT (a bounded wait ran out) or
+ * MMQ_ERR_CUDA (the synchronize itself failed). */
+int mmq_get_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMQ_H */

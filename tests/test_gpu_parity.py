@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same
+seeded operands.
+
+Acceptance (the method's own bar):
+  - q8_1 quantization: bit-exact bytes (codes, f16 d, f16 s);
+  - per-block int32 dots from the debug hook: bit-exact;
+  - f32 outputs: |gpu - oracle| <= TOL * sum_b |terms| per entry, TOL = 1e-4, where the
+    oracle is the fp64 contraction on the same quantized operands.
+Shapes: small ones the oracle computes in full (spanning several tiles plus ragged
+tails), and the full workload sizes checked on sampled entries.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+PATHS = ["small", "tc"]
+
+
+@pytest.fixture(scope="module")
+def mmq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_int8_mmq_gb300 as m
+    yield m
+    m.mmq_set_path(m.PATH_AUTO)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def set_path(mmq, path):
+    mmq.mmq_set_path({"auto": mmq.PATH_AUTO, "small": mmq.PATH_SMALL, "tc": mmq.PATH_TC}[path])
+
+
+def check_close(out, ref, norm, what=""):
+    out = np.asarray(out, dtype=np.float64)
+    err = np.abs(out - ref)
+    bad = err > TOL * norm
+    if bad.any():
+        i = np.argmax(np.where(norm > 0, err / np.maximum(norm, 1e-300), np.inf))
+        raise AssertionError(f"{what}: {bad.sum()} entries over tolerance; worst at flat index {i}: "
+                             f"gpu {out.flat[i]!r} oracle {ref.flat[i]!r} norm {norm.flat[i]!r}")
+
+
+# ------------------------------------------------------------------ quantize
+
+def tricky_activations(M=16, K=256):
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(M, K))
+    x[0] = 0.0                                                  # all-zero row
+    x[1, :32] = 3.25                                            # all-equal block
+    x[1, 32:64] = (np.arange(32) - 16) * 0.5                    # half-integer ties
+    x[2] *= 1e-3                                                # f16-subnormal scales
+    x[3] *= 1e-30                                               # tiny values
+    x[4] *= 3e3                                                 # large values
+    x[5, :32] = [127, 62.5, 2.5, 1.5, 0.5, -0.5, -1.5, -2.5] + [0] * 24
+    x[6, :32] = np.arange(32) - 16
+    x[7, ::7] = -0.0
+    x[8] = np.where(np.arange(K) % 32 == 3, 5.0, 0.0)           # one nonzero per block
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (17, 512), (64, 512), (512, 3584), (2048, 18944)])
+def test_quantize_bit_exact(mmq, M, K):
+    x = synth.activations(1000 + M, M, K, True)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    assert np.array_equal(xq.cpu().numpy(), oracle.quantize_q8_1(x))
+
+
+def test_quantize_edge_blocks_bit_exact(mmq):
+    x = tricky_activations()
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    assert np.array_equal(xq.cpu().numpy(), oracle.quantize_q8_1(x))
+
+
+def test_quantize_true_division_example(mmq):
+    # a block where x/d and x*(1/d) round to different codes (hand example E5)
+    from conftest import as_floats, read_golden
+    g = read_golden("hand_examples.txt")
+    x = np.array(as_floats(g["e5_x"]), dtype=np.float32)[None, :]
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    assert np.array_equal(xq.cpu().numpy(), oracle.quantize_q8_1(x))
+
+
+# ------------------------------------------------------------------ contractions, full compare
+
+SMALL_SHAPES = {
+    "q8_0": [(1, 1, 32), (3, 7, 64), (9, 33, 512), (64, 256, 512), (130, 200, 1024), (257, 129, 2304),
+             (8, 300, 3584)],
+    "q4_k": [(1, 1, 256), (3, 7, 256), (9, 33, 512), (64, 256, 512), (130, 200, 1024), (257, 129, 2304),
+             (8, 300, 3584)],
+}
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_gemm_parity_full(mmq, fmt, path):
+    set_path(mmq, path)
+    for (M, N, K) in SMALL_SHAPES[fmt]:
+        x = synth.activations(M * 7 + N, M, K, True)
+        w = synth.weights(fmt, M + N * 3, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        out = mmq.gemm(fmt, xq, dev(w), M, N, K)
+        assert mmq.mmq_last_path() == {"small": mmq.PATH_SMALL, "tc": mmq.PATH_TC}[path]
+        ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
+        check_close(out.cpu().numpy(), ref, norm, f"{fmt} {path} {M}x{N}x{K}")
+    assert mmq.mmq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_block_dots_bit_exact(mmq, fmt, path):
+    set_path(mmq, path)
+    for (M, N, K) in [(5, 9, 256), (70, 150, 512), (129, 257, 1024)]:
+        x = synth.activations(M + 11, M, K, True)
+        w = synth.weights(fmt, N + 13, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        dots = mmq.block_dots(fmt, xq, dev(w), M, N, K)
+        ref = oracle.block_dots(fmt, oracle.quantize_q8_1(x), w, M, N, K)
+        assert np.array_equal(dots.cpu().numpy(), ref), f"{fmt} {path} {M}x{N}x{K}"
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_extreme_codes_block_dots(mmq, path):
+    # |D| reaches 32*127*128 with all codes at the ends of their ranges
+    set_path(mmq, path)
+    M, N, K = 16, 16, 256
+    x = np.where(np.arange(M * K).reshape(M, K) % 3 == 0, -1.0, 1.0).astype(np.float32)
+    x[::2] = -1.0
+    w = np.zeros((N, K // 32, 34), dtype=np.uint8)
+    w[:, :, 0:2] = np.array([0.5], dtype=np.float16).view(np.uint8)
+    codes = np.where(np.arange(N * K).reshape(N, K // 32, 32) % 2 == 0, -128, 127).astype(np.int8)
+    codes[::3] = -128
+    w[:, :, 2:] = codes.view(np.uint8)
+    w = w.reshape(N, -1)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    dots = mmq.mmq_debug_block_dots_q8_0(xq, dev(w), M, N, K)
+    xq_ref = oracle.quantize_q8_1(x)
+    ref = oracle.block_dots("q8_0", xq_ref, w, M, N, K)
+    assert np.abs(ref).max() == 32 * 127 * 128
+    assert np.array_equal(dots.cpu().numpy(), ref)
+    out = mmq.mmq_gemm_q8_0(xq, dev(w), M, N, K)
+    r, nrm = oracle.gemm("q8_0", xq_ref, w, M, N, K)
+    check_close(out.cpu().numpy(), r, nrm, "extreme codes")
+
+
+# ------------------------------------------------------------------ full sizes, sampled
+
+def sample_entries(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    im = rng.integers(0, M, count)
+    inn = rng.integers(0, N, count)
+    edges_m = np.array([0, M - 1, min(M - 1, 127), min(M - 1, 128), M // 2])
+    edges_n = np.array([0, N - 1, min(N - 1, 255), min(N - 1, 256), N // 2])
+    em, en = np.meshgrid(edges_m, edges_n)
+    return np.concatenate([im, em.ravel()]), np.concatenate([inn, en.ravel()])
+
+
+@pytest.fixture(scope="module")
+def full_operands():
+    cache = {}
+
+    def get(index, M=None):
+        key = (index, M)
+        if key not in cache:
+            x, w, spec = synth.config_operands(index, M)
+            cache[key] = (x, w, spec, oracle.quantize_q8_1(x))
+        return cache[key]
+    return get
+
+
+@pytest.mark.parametrize("index", [0, 1, 2, 3])
+def test_config_sampled_parity(mmq, full_operands, index):
+    set_path(mmq, "auto")
+    x, w, spec, xq_ref = full_operands(index)
+    M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    out = torch.full((M, N), float("nan"), device="cuda")
+    mmq.gemm(fmt, xq, dev(w), M, N, K, out=out)
+    o = out.cpu().numpy()
+    assert not np.isnan(o).any(), "output not fully written"
+    im, inn = sample_entries(M, N, 3000, index)
+    ref, norm = oracle.gemm_at(fmt, xq_ref, w, M, N, K, im, inn)
+    check_close(o[im, inn], ref, norm, f"config {index}")
+    assert mmq.mmq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("M", synth.M_SWEEP)
+def test_m_sweep_sampled_parity(mmq, M):
+    set_path(mmq, "auto")
+    N = K = 3584
+    x = synth.activations(synth.substream(synth.BASE_SEED + 4, 7000 + M), M, K, True)
+    w = synth.layer_weights(0, "q", N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    out = mmq.mmq_gemm_q4_k(xq, dev(w), M, N, K).cpu().numpy()
+    xq_ref = oracle.quantize_q8_1(x)
+    im, inn = sample_entries(M, N, 1500, M)
+    ref, norm = oracle.gemm_at("q4_k", xq_ref, w, M, N, K, im, inn)
+    check_close(out[im, inn], ref, norm, f"M sweep {M}")
+
+
+# ------------------------------------------------------------------ protocol on the device
+
+def test_refused_call_leaves_output_untouched(mmq):
+    M, N, K = 8, 64, 256
+    x = synth.activations(3, M, K, True)
+    w = synth.q8_0_weights(4, N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    out = torch.full((M * N + 4,), float("nan"), device="cuda")
+    wd = dev(w)
+    lib = mmq.lib()
+    import ctypes
+    st = lib.mmq_gemm_q8_0(ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(wd.data_ptr()), M, N, K,
+                           ctypes.c_void_p(out.data_ptr() + 4), None)
+    assert st == -4
+    st = lib.mmq_gemm_q8_0(ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(wd.data_ptr()), M, N, K + 16,
+                           ctypes.c_void_p(out.data_ptr()), None)
+    assert st == -2
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()
+    with pytest.raises(mmq.MMQError):
+        mmq.mmq_gemm_q4_k(xq, wd, M, N, K + 32)
+
+
+def test_streams_and_device_error_word(mmq):
+    s = torch.cuda.Stream()
+    M, N, K = 33, 65, 512
+    x = synth.activations(9, M, K, True)
+    w = synth.q4_k_weights(10, N, K)
+    with torch.cuda.stream(s):
+        xd, wd = dev(x), dev(w)
+        xq = mmq.mmq_quantize_q8_1(xd, stream=s)
+        out = mmq.mmq_gemm_q4_k(xq, wd, M, N, K, stream=s)
+    assert mmq.mmq_get_device_error(s) == 0
+    ref, norm = oracle.gemm("q4_k", oracle.quantize_q8_1(x), w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, "side stream")
