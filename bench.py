@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-quantized int8 MMQ hot path on GB300.
+
+One step = one pass of the whole path over one batch: quantize the f32 activations to
+q8_1, then contract them with the block-quantized weights (f32 out).  Default workload:
+Q8_0 attention projection, M=512 tokens, N=K=3584 (the configuration the headline
+metric is quoted on).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c1|c2|c3|c3q]
+
+--impl reference times the CPU oracle (the plain C fp64 definition) on the host cores
+on a bounded sample of the same workload.  Multi-GPU runs (torchrun, one rank per GPU)
+are independent replicas of the single-GPU step (weak scaling, no collective on the
+data path); the timed region is bracketed by barriers and the max over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+L2_BYTES = 129 * 1024 * 1024
+
+WORKLOADS = {
+    "c1": dict(index=1, label="q8_0 MMQ attention-proj M=512 N=3584 K=3584 (quantize + GEMM)"),
+    "c2": dict(index=2, label="q4_k MMQ ffn-up M=2048 N=18944 K=3584 (quantize + GEMM)"),
+    "c3": dict(index=3, label="q4_k MMQ ffn-down M=2048 N=3584 K=18944 (quantize + GEMM)"),
+    "c3q": dict(index=3, label="q8_1 quantize alone M=2048 K=18944", quant_only=True),
+}
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "ptx.cuh", "common.cuh", "quantize.cu", "gemm_small.cu"):
+        with open(os.path.join(ROOT, "block_quantized_int8_mmq_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(f"{kernel}|{workload}")
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores, on a bounded sample of the workload."""
+    import oracle
+    wl = WORKLOADS[args.workload]
+    x, w, spec = synth.config_operands(wl["index"])
+    M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
+    # bounded sample: a band of output rows (all N columns) so that each step is well
+    # under a second of CPU work; the quantize of those rows is part of the step
+    rows = max(1, min(M, int(args.ref_rows)))
+    xs = np.ascontiguousarray(x[:rows])
+    cores = oracle.num_threads()
+    if wl.get("quant_only"):
+        xs = x
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        xq = oracle.quantize_q8_1(xs)
+        if not wl.get("quant_only"):
+            oracle.gemm(fmt, xq, w, rows, N, K)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    if wl.get("quant_only"):
+        value, unit = (xs.nbytes + xs.size // 32 * 36) / t / 1e9, "GB/s"
+        sample = f"full quantize M={M} K={K} per step"
+        metric = "q8_1 quantize GB/s"
+    else:
+        value, unit = 2.0 * rows * N * K / t / 1e12, "TOPS"
+        sample = f"rows 0..{rows - 1} of M={M} (all N={N} columns, full K={K}): quantize + contraction per step"
+        metric = "MMQ int8 TOPS (2*M*N*K per step: quantize + GEMM)"
+    return {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "none", "vs_baseline": None, "dtype": "int64 dots, f64 scales", "data": "synthetic",
+        "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt, "sampled_rows": rows},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline(workload: str, budget_s: float):
+    """Oracle on the host cores, on a band of rows sized to ~budget_s of CPU time."""
+    import oracle
+    wl = WORKLOADS[workload]
+    x, w, spec = synth.config_operands(wl["index"])
+    M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
+    if wl.get("quant_only"):
+        t0 = time.perf_counter()
+        oracle.quantize_q8_1(x)
+        dt = time.perf_counter() - t0
+        return {"value": (x.nbytes + M * K // 32 * 36) / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+                "kind": "oracle", "sample": f"full quantize M={M} K={K}, {dt:.2f} s"}
+    rows = 1
+    t0 = time.perf_counter()
+    xq = oracle.quantize_q8_1(x[:rows])
+    oracle.gemm(fmt, xq, w, rows, N, K)
+    dt = time.perf_counter() - t0
+    rows = int(max(1, min(M, rows * budget_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    xq = oracle.quantize_q8_1(np.ascontiguousarray(x[:rows]))
+    oracle.gemm(fmt, xq, w, rows, N, K)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TOPS", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"rows 0..{rows - 1} of M={M}, all N={N}, K={K}: quantize + contraction, "
+                                        f"{dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+    import block_quantized_int8_mmq_gb300 as mmq
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]
+    x, w, spec = synth.config_operands(wl["index"])
+    M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
+    quant_only = wl.get("quant_only", False)
+
+    xq_bytes = M * (K // 32) * 36
+    set_bytes = x.nbytes + (0 if quant_only else w.nbytes)
+    copies = max(2, -(-3 * L2_BYTES // set_bytes))
+    xs = [torch.from_numpy(x).to(dev)]
+    xs += [xs[0].clone() for _ in range(copies - 1)]
+    ws = []
+    if not quant_only:
+        ws = [torch.from_numpy(w).to(dev)]
+        ws += [ws[0].clone() for _ in range(copies - 1)]
+    xq = torch.empty(xq_bytes, dtype=torch.uint8, device=dev).view(M, -1)
+    out = torch.full((M, N), float("nan"), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    gemm = mmq.mmq_gemm_q8_0 if fmt == "q8_0" else mmq.mmq_gemm_q4_k
+
+    def step(i, evs=None):
+        j = i % copies
+        if evs is not None:
+            evs[0].record(stream)
+        mmq.mmq_quantize_q8_1(xs[j], xq, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        if not quant_only:
+            gemm(xq, ws[j], M, N, K, out, stream)
+            if evs is not None:
+                evs[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert mmq.mmq_get_device_error(stream) == 0
+    path = mmq.mmq_last_path()
+
+    # parity spot check of the warm-up result before timing (proves the kernels ran)
+    import oracle
+    xr = xq.cpu().numpy()
+    assert np.array_equal(xr, oracle.quantize_q8_1(x)), "q8_1 bytes differ from the oracle"
+    if not quant_only:
+        o = out.cpu().numpy()
+        assert not np.isnan(o).any(), "output not written"
+        rng = np.random.default_rng(0)
+        im, inn = rng.integers(0, M, 256), rng.integers(0, N, 256)
+        ref, norm = oracle.gemm_at(fmt, xr, w, M, N, K, im, inn)
+        assert np.all(np.abs(o[im, inn] - ref) <= 1e-4 * norm), "GEMM output differs from the oracle"
+        out.fill_(float("nan"))
+
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip().isdigit()]
+    clocks = ClockSampler(int(visible[local]) if local < len(visible) else local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [e[1].elapsed_time(e[2]) for e in evs] if not quant_only else []
+    if not quant_only:
+        assert not torch.isnan(out).any().item(), "timed steps did not write the output"
+    assert mmq.mmq_get_device_error(stream) == 0
+
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    ops = 2.0 * M * N * K
+    peaks = load_peaks()
+    if quant_only:
+        qbytes = x.nbytes + xq_bytes
+        value = qbytes * args.steps * world / (ms_max / 1e3) / 1e9
+        unit = "GB/s"
+        metric = "q8_1 quantize GB/s (algorithmic bytes: 4 B in + 1.125 B out per value)"
+        q_avg = sum(q_ms) / len(q_ms)
+        achieved = qbytes / (q_avg / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for("k_quantize_q8_1", args.workload),
+                "kernel": "k_quantize_q8_1", "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        value = ops * args.steps * world / (ms_max / 1e3) / 1e12
+        unit = "TOPS"
+        metric = "MMQ int8 TOPS (2*M*N*K per step: quantize + GEMM)"
+        g_avg = sum(g_ms) / len(g_ms)
+        achieved = ops / (g_avg / 1e3) / 1e12
+        kname = "k_mmq_tc" if path == mmq.PATH_TC else "k_mmq_small"
+        if path == mmq.PATH_TC:
+            peak = peaks["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic_for(kname, args.workload), "kernel": kname,
+                    "peak_source": f"{peaks['source']} bf16 burst (f16 tensor rate = bf16 rate)"}
+        else:
+            wbytes = w.nbytes + xq_bytes + M * N * 4
+            gbs = wbytes / (g_avg / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload), "kernel": kname,
+                    "peak_source": peaks["source"] + " hbm_gbs"}
+
+    # end to end through the public API: pinned host x -> device, step, out -> host
+    e2e = None
+    if not quant_only:
+        xh = torch.from_numpy(x).pin_memory()
+        oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(xs[0])
+        for i in range(3):
+            xd.copy_(xh, non_blocking=True)
+            mmq.mmq_linear(xd, ws[i % copies], fmt, N, xq=xq, out=out, stream=stream)
+            oh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            xd.copy_(xh, non_blocking=True)
+            mmq.mmq_linear(xd, ws[i % copies], fmt, N, xq=xq, out=out, stream=stream)
+            oh.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b)
+        e2e = {"value": ops * args.steps / (e_ms / 1e3) / 1e12, "unit": "TOPS",
+               "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": M * N * 4}
+
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 codes (exact on f16 tensor cores), f32 scales and output",
+        "data": "synthetic (seeded; 7B GQA projection shapes)",
+        "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"rotating {copies} operand copies ({copies * set_bytes / 2**20:.0f} MiB > 3x L2)"},
+        "roofline": roof,
+        "kernel_ms": {"quantize": sum(q_ms) / len(q_ms), "gemm": (sum(g_ms) / len(g_ms)) if g_ms else None},
+        "path": {mmq.PATH_TC: "tcgen05", mmq.PATH_SMALL: "warp-level"}.get(path, "quantize"),
+        "clocks": clk,
+        "gpu_launches": args.steps * (1 if quant_only else 2),
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-rows", type=int, default=32, help="rows per reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -84,7 +84,9 @@ int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int path = current_path();
-    const bool small = path == MMQ_PATH_SMALL || (path == MMQ_PATH_AUTO && (M <= 8 || !tc_available()));
+    // The tensor-core path stages 256-value k-tiles; other K go to the warp-level path.
+    const bool small =
+        path == MMQ_PATH_SMALL || (path == MMQ_PATH_AUTO && (M <= 8 || K % QK_K != 0 || !tc_available()));
     if (small) {
         st = small_launch(fmt, xq, wq, M, N, K, out, dots, s);
         if (st == MMQ_OK) t_last_path = MMQ_PATH_SMALL;

@@ -104,6 +104,8 @@ SMALL_SHAPES = {
 def test_gemm_parity_full(mmq, fmt, path):
     set_path(mmq, path)
     for (M, N, K) in SMALL_SHAPES[fmt]:
+        if path == "tc" and K % 256:
+            continue  # the tensor-core path stages 256-value k-tiles (refusal tested below)
         x = synth.activations(M * 7 + N, M, K, True)
         w = synth.weights(fmt, M + N * 3, N, K)
         xq = mmq.mmq_quantize_q8_1(dev(x))
@@ -112,6 +114,22 @@ def test_gemm_parity_full(mmq, fmt, path):
         ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
         check_close(out.cpu().numpy(), ref, norm, f"{fmt} {path} {M}x{N}x{K}")
     assert mmq.mmq_get_device_error() == 0
+
+
+def test_tc_path_refuses_partial_k_tiles_and_auto_routes_them(mmq):
+    M, N, K = 16, 40, 96
+    x = synth.activations(21, M, K, True)
+    w = synth.q8_0_weights(22, N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    set_path(mmq, "tc")
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_gemm_q8_0(xq, dev(w), M, N, K)
+    assert e.value.status == -2
+    set_path(mmq, "auto")
+    out = mmq.mmq_gemm_q8_0(xq, dev(w), M, N, K)
+    assert mmq.mmq_last_path() == mmq.PATH_SMALL
+    ref, norm = oracle.gemm("q8_0", oracle.quantize_q8_1(x), w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, "auto K % 256 != 0")
 
 
 @pytest.mark.parametrize("path", PATHS)
