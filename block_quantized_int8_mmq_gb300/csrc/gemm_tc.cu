@@ -64,11 +64,12 @@ static_assert(EPI_WARPS == 8 && BN == 128, "epilogue covers 4 lane quarters x 2 
 
 __host__ __device__ constexpr int b_row(int fmt) { return fmt == FMT_Q8_0 ? KT_BLOCKS * Q8_0_BYTES : Q4_K_BYTES; }
 
-// barrier indices
-constexpr int BAR_RAW_FULL = 0, BAR_RAW_EMPTY = BAR_RAW_FULL + RS, BAR_OP_FULL = BAR_RAW_EMPTY + RS,
-              BAR_OP_EMPTY = BAR_OP_FULL + FS, BAR_SC_FULL = BAR_OP_EMPTY + FS, BAR_SC_EMPTY = BAR_SC_FULL + FS,
-              BAR_D_FULL = BAR_SC_EMPTY + FS, BAR_D_EMPTY = BAR_D_FULL + DS, BAR_DRAIN = BAR_D_EMPTY + DS,
-              NBARS = BAR_DRAIN + 1;
+// barrier indices.  One slot holds the fp16 operands and the scales of one 32-block:
+// SLOT_FULL is arrived by every converter warp; SLOT_EMPTY by the MMA commit (operands
+// read) and by every epilogue warp (scales read).
+constexpr int BAR_RAW_FULL = 0, BAR_RAW_EMPTY = BAR_RAW_FULL + RS, BAR_SLOT_FULL = BAR_RAW_EMPTY + RS,
+              BAR_SLOT_EMPTY = BAR_SLOT_FULL + FS, BAR_D_FULL = BAR_SLOT_EMPTY + FS, BAR_D_EMPTY = BAR_D_FULL + DS,
+              BAR_DRAIN = BAR_D_EMPTY + DS, NBARS = BAR_DRAIN + 1;
 
 template <int FMT>
 struct Layout {
@@ -123,8 +124,9 @@ __device__ __forceinline__ uint2 u4x4_to_f16x4(uint32_t w) {
 }
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the wall
-// time limit ran out (then the error word and the abort flag are set).
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
+// time limit ran out (then the error word and the abort flag are set).  Inlined: a
+// call here costs the waiting warp more than the wait itself.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -151,13 +153,11 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity) {
     }
 }
 
-// All lanes of the warp take the same decision; lane 0 polls.
+// Every lane polls the same phase; the vote keeps the warp on one path (a phase that
+// one lane saw complete cannot be reused before this warp arrives on its partner).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    const bool ok = wait_bar(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
 }
 
 template <int FMT, bool DOTS>
@@ -183,10 +183,8 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             ptx::mbar_init(bar(BAR_RAW_EMPTY + s), CONV_WARPS);
         }
         for (int f = 0; f < FS; ++f) {
-            ptx::mbar_init(bar(BAR_OP_FULL + f), CONV_WARPS);
-            ptx::mbar_init(bar(BAR_OP_EMPTY + f), 1);
-            ptx::mbar_init(bar(BAR_SC_FULL + f), CONV_WARPS);
-            ptx::mbar_init(bar(BAR_SC_EMPTY + f), EPI_WARPS);
+            ptx::mbar_init(bar(BAR_SLOT_FULL + f), CONV_WARPS);
+            ptx::mbar_init(bar(BAR_SLOT_EMPTY + f), 1 + EPI_WARPS);
         }
         for (int t = 0; t < DS; ++t) {
             ptx::mbar_init(bar(BAR_D_FULL + t), 1);
@@ -231,14 +229,14 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             constexpr uint32_t idesc = make_idesc(BM, BN);
             for (int bi = 0; bi < nb; ++bi) {
                 const int f = bi % FS, t = bi % DS;
-                if (!wait_bar(bar(BAR_OP_FULL + f), (bi / FS) & 1, abort)) break;
+                if (!wait_bar(bar(BAR_SLOT_FULL + f), (bi / FS) & 1, abort)) break;
                 if (!wait_bar(bar(BAR_D_EMPTY + t), ((bi / DS) & 1) ^ 1, abort)) break;
                 ptx::tc_fence_after();
                 const uint32_t a = sbase + L::opA + f * OP_A, b = sbase + L::opB + f * OP_B;
                 const uint32_t d = tmem + (uint32_t)(t * BN);
                 ptx::umma_f16(d, sdesc(a), sdesc(b), idesc, 0u);
                 ptx::umma_f16(d, sdesc(a + 256), sdesc(b + 256), idesc, 1u);
-                ptx::umma_commit(bar(BAR_OP_EMPTY + f));
+                ptx::umma_commit(bar(BAR_SLOT_EMPTY + f));
                 ptx::umma_commit(bar(BAR_D_FULL + t));
             }
             ptx::umma_commit(bar(BAR_DRAIN));  // arrives once every MMA issued above is done
@@ -259,61 +257,63 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             const uint8_t* rB = smem + L::rawB + s * BN * BROW;
             for (int j = 0; j < KT_BLOCKS; ++j) {
                 const int bi = kt * KT_BLOCKS + j, f = bi % FS;
-                const uint32_t ph = ((bi / FS) & 1) ^ 1;
-                ok = warp_wait(bar(BAR_OP_EMPTY + f), ph, abort) && warp_wait(bar(BAR_SC_EMPTY + f), ph, abort);
+                ok = warp_wait(bar(BAR_SLOT_EMPTY + f), ((bi / FS) & 1) ^ 1, abort);
                 if (!ok) break;
                 uint8_t* oA = smem + L::opA + f * OP_A;
                 uint8_t* oB = smem + L::opB + f * OP_B;
                 float* sc = reinterpret_cast<float*>(smem + L::sc + f * SC_FLOATS * 4);
+                // All raw loads first (the stores below go to the same shared array, so
+                // the compiler would otherwise keep every load behind the previous store).
+                // Unit i: 8-row group g and a pair of 8-value k-groups; each lane takes
+                // one 4-code word = half of one core-matrix row.
+                uint32_t xa[8], wv[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    // unit u: 8-row group g and a pair of 8-value k-groups; each lane
-                    // converts one 4-code word (half of one core-matrix row)
                     const int u = i * CONV_WARPS + cw;
                     const int g = u >> 1, kg = (u & 1) * 2 + kgl, w = kg * 2 + half, r = g * 8 + r8;
-                    const int dst = g * 512 + kg * 128 + r8 * 16 + half * 8;
-                    const uint32_t xa = *reinterpret_cast<const uint32_t*>(rA + r * A_ROW + j * Q8_1_BYTES + 4 + w * 4);
-                    *reinterpret_cast<uint2*>(oA + dst) = i8x4_to_f16x4(xa);
+                    xa[i] = *reinterpret_cast<const uint32_t*>(rA + r * A_ROW + j * Q8_1_BYTES + 4 + w * 4);
                     if (FMT == FMT_Q8_0) {
-                        const uint8_t* p = rB + r * BROW + j * Q8_0_BYTES + 2 + w * 4;
-                        uint32_t wv;
-                        if (j & 1) {
-                            wv = *reinterpret_cast<const uint32_t*>(p);
-                        } else {  // codes start 2 bytes into an aligned word
-                            const uint32_t lo = *reinterpret_cast<const uint32_t*>(p - 2);
-                            const uint32_t hi = *reinterpret_cast<const uint32_t*>(p + 2);
-                            wv = __byte_perm(lo, hi, 0x5432);
-                        }
-                        *reinterpret_cast<uint2*>(oB + dst) = i8x4_to_f16x4(wv);
+                        // codes start at an odd half-word for even j: two aligned words
+                        // and a funnel shift (for odd j the second load is the first)
+                        const int off = r * BROW + j * Q8_0_BYTES + 2 + w * 4;
+                        const int sh = (off & 3) * 8;
+                        const uint32_t lo = *reinterpret_cast<const uint32_t*>(rB + (off & ~3));
+                        const uint32_t hi = *reinterpret_cast<const uint32_t*>(rB + (off & ~3) + (sh ? 4 : 0));
+                        wv[i] = __funnelshift_r(lo, hi, sh);
                     } else {
                         const uint32_t raw =
                             *reinterpret_cast<const uint32_t*>(rB + r * BROW + 16 + 32 * (j >> 1) + w * 4);
-                        const uint32_t nib = (j & 1) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
-                        *reinterpret_cast<uint2*>(oB + dst) = u4x4_to_f16x4(nib);
+                        wv[i] = (j & 1) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
                     }
                 }
-                {
-                    const uint32_t hd = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
-                    sc[ct] = f16_bits_to_f32(hd);
-                    sc[BM + ct] = f16_bits_to_f32(hd >> 16);
-                    if (FMT == FMT_Q8_0) {
-                        const uint32_t wd = *reinterpret_cast<const unsigned short*>(rB + ct * BROW + j * Q8_0_BYTES);
-                        sc[2 * BM + ct] = f16_bits_to_f32(wd);
-                        sc[2 * BM + BN + ct] = 0.f;
-                    } else {
-                        const uint32_t* p = reinterpret_cast<const uint32_t*>(rB + ct * BROW);
-                        int s6, m6;
-                        q4_k_scale_min(p[1], p[2], p[3], j, s6, m6);
-                        sc[2 * BM + ct] = f16_bits_to_f32(p[0]) * (float)s6;             // exact
-                        sc[2 * BM + BN + ct] = f16_bits_to_f32(p[0] >> 16) * (float)m6;  // exact
-                    }
+                const uint32_t hd = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
+                float wsc, wmn;
+                if (FMT == FMT_Q8_0) {
+                    wsc = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(rB + ct * BROW + j * Q8_0_BYTES));
+                    wmn = 0.f;
+                } else {
+                    const uint4 p = *reinterpret_cast<const uint4*>(rB + ct * BROW);
+                    int s6, m6;
+                    q4_k_scale_min(p.y, p.z, p.w, j, s6, m6);
+                    wsc = f16_bits_to_f32(p.x) * (float)s6;        // exact
+                    wmn = f16_bits_to_f32(p.x >> 16) * (float)m6;  // exact
                 }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int u = i * CONV_WARPS + cw;
+                    const int g = u >> 1, kg = (u & 1) * 2 + kgl;
+                    const int dst = g * 512 + kg * 128 + r8 * 16 + half * 8;
+                    *reinterpret_cast<uint2*>(oA + dst) = i8x4_to_f16x4(xa[i]);
+                    *reinterpret_cast<uint2*>(oB + dst) =
+                        FMT == FMT_Q8_0 ? i8x4_to_f16x4(wv[i]) : u4x4_to_f16x4(wv[i]);
+                }
+                sc[ct] = f16_bits_to_f32(hd);
+                sc[BM + ct] = f16_bits_to_f32(hd >> 16);
+                sc[2 * BM + ct] = wsc;
+                sc[2 * BM + BN + ct] = wmn;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(bar(BAR_OP_FULL + f));
-                    ptx::mbar_arrive(bar(BAR_SC_FULL + f));
-                }
+                if (lane == 0) ptx::mbar_arrive(bar(BAR_SLOT_FULL + f));
             }
             __syncwarp();
             if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_RAW_EMPTY + s));
@@ -330,7 +330,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         for (int bi = 0; bi < nb; ++bi) {
             const int t = bi % DS, f = bi % FS;
             if (!(warp_wait(bar(BAR_D_FULL + t), (bi / DS) & 1, abort) &&
-                  warp_wait(bar(BAR_SC_FULL + f), (bi / FS) & 1, abort)))
+                  warp_wait(bar(BAR_SLOT_FULL + f), (bi / FS) & 1, abort)))
                 break;
             ptx::tc_fence_after();
             const float* sc = reinterpret_cast<const float*>(smem + L::sc + f * SC_FLOATS * 4);
@@ -375,7 +375,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             __syncwarp();
             if (lane == 0) {
                 ptx::mbar_arrive(bar(BAR_D_EMPTY + t));
-                ptx::mbar_arrive(bar(BAR_SC_EMPTY + f));
+                ptx::mbar_arrive(bar(BAR_SLOT_EMPTY + f));
             }
         }
         if (!DOTS && mrow < M && !*abort) {
