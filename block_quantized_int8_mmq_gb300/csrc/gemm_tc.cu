@@ -12,22 +12,24 @@
 // block dot is an integer of magnitude <= 2^19, so an fp16 x fp16 -> f32 MMA over one
 // block computes D exactly.  That is the contraction used here.
 //
-// Warp roles (one 128 x 128 output tile per CTA, 448 threads):
+// Warp roles (one 128 x 128 output tile per CTA, 704 threads):
 //   warp 0     TMA producer: raw q8_1 rows (288 B per 256 values) and raw weight rows
 //              (Q8_0: 272 B, Q4_K: one 144 B super-block) for a 256-value k-tile, as
 //              2-D tensor copies into a 2-stage ring ("13 . r7-r8 raw-byte MMQ
 //              kernel", sec. 2: shared memory holds raw quant bytes; sec. 3.1: whole
 //              super-blocks, out-of-range rows zero-filled by the copy engine).
 //   warp 1     TMEM owner and MMA issuer: per 32-block, two K=16 MMAs (M=128, N=128)
-//              into one of four TMEM accumulators, then tcgen05.commit.
+//              into one of four TMEM accumulators; one tcgen05.commit per group of
+//              two blocks (barrier round trips cost more than the work between them).
 //   warps 2-5  converters: codes -> fp16 (sign-biased byte permute + one half2
 //              subtract, exact) into the canonical K-major no-swizzle UMMA layout, and
 //              the per-row / per-column block scales into a small scale ring
 //              (Q4_K: d*sc_j and dmin*m_j from the 12 packed bytes, computed once per
 //              (row, block) instead of per lane, as in sec. 3.2 of the same page).
-//   warps 6-13 epilogue: per 32-block, tcgen05.ld of the f32 block dots, then
-//              acc += (xd*wd) * D (Q4_K: wd = d*sc_j, and acc -= dmin*m_j*xs) in f32
-//              registers; at the end the tile is stored to out.
+//   warps 6-21 epilogue, 32 rows x 32 columns each: per 32-block, tcgen05.ld of the
+//              f32 block dots in 8-column chunks (the next loads while one is rescaled), then
+//              acc += (xd*wd) * D (Q4_K: wd = d*sc_j, and acc -= dmin*m_j*xs) with packed
+//              f32x2 multiply / FMA in registers; at the end the tile is stored to out.
 // Every wait is bounded by wall time; on expiry the kernel records ERR_TIMEOUT, lets
 // the other roles fall out, drains its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -46,10 +48,16 @@ constexpr int BM = 128;                 // activation rows per tile (TMEM lanes)
 constexpr int BN = 128;                 // weight rows per tile (MMA N, TMEM columns)
 constexpr int KT_BLOCKS = 8;            // 32-blocks per staged k-tile (256 values)
 constexpr int RS = 2;                   // raw k-tile stages
-constexpr int FS = 4;                   // fp16 operand / scale slots (one 32-block each)
+constexpr int FS = 4;                   // fp16 operand slots (one 32-block each)
+constexpr int SCN = 8;                  // scale slots (one 32-block each)
 constexpr int DS = 4;                   // TMEM accumulators (one 32-block each)
+constexpr int G = 2;                    // 32-blocks per barrier round trip (a "group")
+constexpr int SG = FS / G;              // operand slot groups in flight
+constexpr int SCG = SCN / G;            // scale slot groups in flight
+constexpr int DG = DS / G;              // TMEM groups in flight
 constexpr int CONV_WARPS = 4;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;
+constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // columns per epilogue warp (4 lane quarters)
 constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, WARP_EPI0 = WARP_CONV0 + CONV_WARPS;
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
 constexpr int TMEM_COLS = DS * BN;      // 512: the whole TMEM of the SM
@@ -57,19 +65,25 @@ constexpr int A_ROW = KT_BLOCKS * Q8_1_BYTES;  // 288
 constexpr int OP_A = BM * QK * 2;       // fp16 A tile of one block: 8 KiB
 constexpr int OP_B = BN * QK * 2;       // fp16 B tile of one block: 8 KiB
 constexpr int SC_FLOATS = 2 * BM + 2 * BN;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bound on any one wait
+constexpr uint32_t WAIT_SLEEP_NS = 100000;           // longest sleep inside one poll
 
-static_assert(BM == 32 * CONV_WARPS && BN == 32 * CONV_WARPS, "one scale row per converter thread");
-static_assert(EPI_WARPS == 8 && BN == 128, "epilogue covers 4 lane quarters x 2 column halves of 64");
+static_assert(BM == 32 * CONV_WARPS && BN == 32 * CONV_WARPS, "one activation and one weight scale row per converter thread");
+static_assert(32 % CONV_WARPS == 0, "32 conversion units per operand tile");
+static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 8 == 0, "epilogue covers 4 lane quarters x column groups");
 
 __host__ __device__ constexpr int b_row(int fmt) { return fmt == FMT_Q8_0 ? KT_BLOCKS * Q8_0_BYTES : Q4_K_BYTES; }
 
-// barrier indices.  One slot holds the fp16 operands and the scales of one 32-block:
-// SLOT_FULL is arrived by every converter warp; SLOT_EMPTY by the MMA commit (operands
-// read) and by every epilogue warp (scales read).
+// barrier indices.  A slot group holds the fp16 operands of G 32-blocks (SLOT_FULL:
+// every converter warp arrives; SLOT_EMPTY: the MMA commit).  The scales of a group sit
+// in a deeper ring of their own (SC_FULL: converters; SC_EMPTY: every epilogue warp), so
+// that operand slots come free as soon as their MMAs complete.  D_FULL / D_EMPTY guard
+// the G TMEM accumulators of a group.
 constexpr int BAR_RAW_FULL = 0, BAR_RAW_EMPTY = BAR_RAW_FULL + RS, BAR_SLOT_FULL = BAR_RAW_EMPTY + RS,
-              BAR_SLOT_EMPTY = BAR_SLOT_FULL + FS, BAR_D_FULL = BAR_SLOT_EMPTY + FS, BAR_D_EMPTY = BAR_D_FULL + DS,
-              BAR_DRAIN = BAR_D_EMPTY + DS, NBARS = BAR_DRAIN + 1;
+              BAR_SLOT_EMPTY = BAR_SLOT_FULL + SG, BAR_SC_FULL = BAR_SLOT_EMPTY + SG, BAR_SC_EMPTY = BAR_SC_FULL + SCG,
+              BAR_D_FULL = BAR_SC_EMPTY + SCG, BAR_D_EMPTY = BAR_D_FULL + DG, BAR_DRAIN = BAR_D_EMPTY + DG,
+              NBARS = BAR_DRAIN + 1;
+static_assert(KT_BLOCKS % G == 0 && FS % G == 0 && DS % G == 0 && SCN % G == 0, "groups tile the rings");
 
 template <int FMT>
 struct Layout {
@@ -78,7 +92,7 @@ struct Layout {
     static constexpr int opA = rawB + RS * BN * b_row(FMT);
     static constexpr int opB = opA + FS * OP_A;
     static constexpr int sc = opB + FS * OP_B;
-    static constexpr int bars = sc + FS * SC_FLOATS * 4;
+    static constexpr int bars = sc + SCN * SC_FLOATS * 4;
     static constexpr int tmem_slot = bars + NBARS * 8;
     static constexpr int total = tmem_slot + 16;
     static constexpr int alloc = total + 1024;  // slack to align the base to 1 KiB
@@ -129,15 +143,13 @@ __device__ __forceinline__ uint2 u4x4_to_f16x4(uint32_t w) {
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
-            if (*abort) return false;
-            if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                atomicOr(&g_tc_error, ERR_TIMEOUT);
-                *abort = 1;
-                return false;
-            }
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
+        if (*abort) return false;
+        if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(&g_tc_error, ERR_TIMEOUT);
+            *abort = 1;
+            return false;
         }
     }
 }
@@ -153,11 +165,12 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Every lane polls the same phase; the vote keeps the warp on one path (a phase that
-// one lane saw complete cannot be reused before this warp arrives on its partner).
+// Lane 0 polls (one shared-memory barrier access per poll instead of 32); the other
+// lanes take its answer, so the warp stays on one path.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    const bool ok = wait_bar(bar, parity, abort);
-    return __all_sync(0xffffffffu, ok);
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 template <int FMT, bool DOTS>
@@ -178,17 +191,21 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        for (int s = 0; s < RS; ++s) {
-            ptx::mbar_init(bar(BAR_RAW_FULL + s), 1);
-            ptx::mbar_init(bar(BAR_RAW_EMPTY + s), CONV_WARPS);
+        for (int i = 0; i < RS; ++i) {
+            ptx::mbar_init(bar(BAR_RAW_FULL + i), 1);
+            ptx::mbar_init(bar(BAR_RAW_EMPTY + i), CONV_WARPS);
         }
-        for (int f = 0; f < FS; ++f) {
-            ptx::mbar_init(bar(BAR_SLOT_FULL + f), CONV_WARPS);
-            ptx::mbar_init(bar(BAR_SLOT_EMPTY + f), 1 + EPI_WARPS);
+        for (int i = 0; i < SG; ++i) {
+            ptx::mbar_init(bar(BAR_SLOT_FULL + i), CONV_WARPS);
+            ptx::mbar_init(bar(BAR_SLOT_EMPTY + i), 1);
         }
-        for (int t = 0; t < DS; ++t) {
-            ptx::mbar_init(bar(BAR_D_FULL + t), 1);
-            ptx::mbar_init(bar(BAR_D_EMPTY + t), EPI_WARPS);
+        for (int i = 0; i < SCG; ++i) {
+            ptx::mbar_init(bar(BAR_SC_FULL + i), CONV_WARPS);
+            ptx::mbar_init(bar(BAR_SC_EMPTY + i), EPI_WARPS);
+        }
+        for (int i = 0; i < DG; ++i) {
+            ptx::mbar_init(bar(BAR_D_FULL + i), 1);
+            ptx::mbar_init(bar(BAR_D_EMPTY + i), EPI_WARPS);
         }
         ptx::mbar_init(bar(BAR_DRAIN), 1);
         ptx::fence_barrier_init();
@@ -205,6 +222,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::tmem_slot);
+    const int ng = nb / G;
 
     if (warp == WARP_TMA) {
         // ------------------------------------------------------------ producer
@@ -227,17 +245,21 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc(BM, BN);
-            for (int bi = 0; bi < nb; ++bi) {
-                const int f = bi % FS, t = bi % DS;
-                if (!wait_bar(bar(BAR_SLOT_FULL + f), (bi / FS) & 1, abort)) break;
-                if (!wait_bar(bar(BAR_D_EMPTY + t), ((bi / DS) & 1) ^ 1, abort)) break;
+            for (int gi = 0; gi < ng; ++gi) {
+                const int gs = gi % SG, gd = gi % DG;
+                if (!wait_bar(bar(BAR_SLOT_FULL + gs), (gi / SG) & 1, abort)) break;
+                if (!wait_bar(bar(BAR_D_EMPTY + gd), ((gi / DG) & 1) ^ 1, abort)) break;
                 ptx::tc_fence_after();
-                const uint32_t a = sbase + L::opA + f * OP_A, b = sbase + L::opB + f * OP_B;
-                const uint32_t d = tmem + (uint32_t)(t * BN);
-                ptx::umma_f16(d, sdesc(a), sdesc(b), idesc, 0u);
-                ptx::umma_f16(d, sdesc(a + 256), sdesc(b + 256), idesc, 1u);
-                ptx::umma_commit(bar(BAR_SLOT_EMPTY + f));
-                ptx::umma_commit(bar(BAR_D_FULL + t));
+#pragma unroll
+                for (int jj = 0; jj < G; ++jj) {
+                    const int bi = gi * G + jj, f = bi % FS, t = bi % DS;
+                    const uint32_t a = sbase + L::opA + f * OP_A, b = sbase + L::opB + f * OP_B;
+                    const uint32_t d = tmem + (uint32_t)(t * BN);
+                    ptx::umma_f16(d, sdesc(a), sdesc(b), idesc, 0u);
+                    ptx::umma_f16(d, sdesc(a + 256), sdesc(b + 256), idesc, 1u);
+                }
+                ptx::umma_commit(bar(BAR_SLOT_EMPTY + gs));
+                ptx::umma_commit(bar(BAR_D_FULL + gd));
             }
             ptx::umma_commit(bar(BAR_DRAIN));  // arrives once every MMA issued above is done
             drain_bar(bar(BAR_DRAIN), 0);
@@ -247,7 +269,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         // ------------------------------------------------------------ converters
         const int cw = warp - WARP_CONV0;
         const int ct = cw * 32 + lane;
-        const int r8 = lane & 7, half = (lane >> 3) & 1, kgl = lane >> 4;
+        const int r8 = lane & 7, half = (lane >> 3) & 1, hw = lane >> 4;
         bool ok = true;
         for (int kt = 0; kt < nkt && ok; ++kt) {
             const int s = kt % RS;
@@ -255,140 +277,198 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             if (!ok) break;
             const uint8_t* rA = smem + L::rawA + s * BM * A_ROW;
             const uint8_t* rB = smem + L::rawB + s * BN * BROW;
-            for (int j = 0; j < KT_BLOCKS; ++j) {
-                const int bi = kt * KT_BLOCKS + j, f = bi % FS;
-                ok = warp_wait(bar(BAR_SLOT_EMPTY + f), ((bi / FS) & 1) ^ 1, abort);
+            for (int gl = 0; gl < KT_BLOCKS / G; ++gl) {
+                const int gi = kt * (KT_BLOCKS / G) + gl, gs = gi % SG, gc = gi % SCG;
+                ok = warp_wait(bar(BAR_SLOT_EMPTY + gs), ((gi / SG) & 1) ^ 1, abort) &&
+                     warp_wait(bar(BAR_SC_EMPTY + gc), ((gi / SCG) & 1) ^ 1, abort);
                 if (!ok) break;
-                uint8_t* oA = smem + L::opA + f * OP_A;
-                uint8_t* oB = smem + L::opB + f * OP_B;
-                float* sc = reinterpret_cast<float*>(smem + L::sc + f * SC_FLOATS * 4);
-                // All raw loads first (the stores below go to the same shared array, so
-                // the compiler would otherwise keep every load behind the previous store).
-                // Unit i: 8-row group g and a pair of 8-value k-groups; each lane takes
-                // one 4-code word = half of one core-matrix row.
-                uint32_t xa[8], wv[8];
+#pragma unroll 1
+                for (int jj = 0; jj < G; ++jj) {
+                    const int j = gl * G + jj, bi = kt * KT_BLOCKS + j, f = bi % FS;
+                    uint8_t* oA = smem + L::opA + f * OP_A;
+                    uint8_t* oB = smem + L::opB + f * OP_B;
+                    float* sc = reinterpret_cast<float*>(smem + L::sc + (bi % SCN) * SC_FLOATS * 4);
+                    // All raw loads first (the stores below go to the same shared array,
+                    // so the compiler would otherwise keep every load behind the previous
+                    // store).  Unit i = (8-row group g, pass p), lane = (hw, half, r8):
+                    // row 8g + r8 takes k-group kg = 2*(p ^ (r8 / 4)) + hw, code word
+                    // w = 2*kg + half.  Rows r8 and r8 + 4 (same banks: rows are 72 words
+                    // apart) read different halves of the block, so a load touches 32
+                    // different banks; each half-warp stores rows 0-3 of one k-group and
+                    // rows 4-7 of another, two 64-byte runs in opposite bank halves.
+                    constexpr int UNITS = 32 / CONV_WARPS;
+                    uint32_t xa[UNITS], wv[UNITS];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int u = i * CONV_WARPS + cw;
-                    const int g = u >> 1, kg = (u & 1) * 2 + kgl, w = kg * 2 + half, r = g * 8 + r8;
-                    xa[i] = *reinterpret_cast<const uint32_t*>(rA + r * A_ROW + j * Q8_1_BYTES + 4 + w * 4);
-                    if (FMT == FMT_Q8_0) {
-                        // codes start at an odd half-word for even j: two aligned words
-                        // and a funnel shift (for odd j the second load is the first)
-                        const int off = r * BROW + j * Q8_0_BYTES + 2 + w * 4;
-                        const int sh = (off & 3) * 8;
-                        const uint32_t lo = *reinterpret_cast<const uint32_t*>(rB + (off & ~3));
-                        const uint32_t hi = *reinterpret_cast<const uint32_t*>(rB + (off & ~3) + (sh ? 4 : 0));
-                        wv[i] = __funnelshift_r(lo, hi, sh);
-                    } else {
-                        const uint32_t raw =
-                            *reinterpret_cast<const uint32_t*>(rB + r * BROW + 16 + 32 * (j >> 1) + w * 4);
-                        wv[i] = (j & 1) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
+                    for (int i = 0; i < UNITS; ++i) {
+                        const int u = i * CONV_WARPS + cw;
+                        const int g = u >> 1, w = 2 * (2 * ((u & 1) ^ (r8 >> 2)) + hw) + half, r = g * 8 + r8;
+                        xa[i] = *reinterpret_cast<const uint32_t*>(rA + r * A_ROW + j * Q8_1_BYTES + 4 + w * 4);
+                        if (FMT == FMT_Q8_0) {
+                            // codes start at an odd half-word for even j: two aligned
+                            // words and a funnel shift (for odd j both loads are the same)
+                            const int off = r * BROW + j * Q8_0_BYTES + 2 + w * 4;
+                            const int sh = (off & 3) * 8;
+                            const uint32_t lo = *reinterpret_cast<const uint32_t*>(rB + (off & ~3));
+                            const uint32_t hi = *reinterpret_cast<const uint32_t*>(rB + (off & ~3) + (sh ? 4 : 0));
+                            wv[i] = __funnelshift_r(lo, hi, sh);
+                        } else {
+                            const uint32_t raw =
+                                *reinterpret_cast<const uint32_t*>(rB + r * BROW + 16 + 32 * (j >> 1) + w * 4);
+                            wv[i] = (j & 1) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
+                        }
                     }
-                }
-                const uint32_t hd = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
-                float wsc, wmn;
-                if (FMT == FMT_Q8_0) {
-                    wsc = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(rB + ct * BROW + j * Q8_0_BYTES));
-                    wmn = 0.f;
-                } else {
-                    const uint4 p = *reinterpret_cast<const uint4*>(rB + ct * BROW);
-                    int s6, m6;
-                    q4_k_scale_min(p.y, p.z, p.w, j, s6, m6);
-                    wsc = f16_bits_to_f32(p.x) * (float)s6;        // exact
-                    wmn = f16_bits_to_f32(p.x >> 16) * (float)m6;  // exact
-                }
+                    // scales: converter thread ct takes activation row ct and weight row ct
+                    const uint32_t hd = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
+                    float wsc, wmn;
+                    if (FMT == FMT_Q8_0) {
+                        wsc = f16_bits_to_f32(
+                            *reinterpret_cast<const unsigned short*>(rB + ct * BROW + j * Q8_0_BYTES));
+                        wmn = 0.f;
+                    } else {
+                        const uint4 p = *reinterpret_cast<const uint4*>(rB + ct * BROW);
+                        int s6, m6;
+                        q4_k_scale_min(p.y, p.z, p.w, j, s6, m6);
+                        wsc = f16_bits_to_f32(p.x) * (float)s6;        // exact: d * sc_j
+                        wmn = f16_bits_to_f32(p.x >> 16) * (float)m6;  // exact: dmin * m_j
+                    }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int u = i * CONV_WARPS + cw;
-                    const int g = u >> 1, kg = (u & 1) * 2 + kgl;
-                    const int dst = g * 512 + kg * 128 + r8 * 16 + half * 8;
-                    *reinterpret_cast<uint2*>(oA + dst) = i8x4_to_f16x4(xa[i]);
-                    *reinterpret_cast<uint2*>(oB + dst) =
-                        FMT == FMT_Q8_0 ? i8x4_to_f16x4(wv[i]) : u4x4_to_f16x4(wv[i]);
+                    for (int i = 0; i < UNITS; ++i) {
+                        const int u = i * CONV_WARPS + cw;
+                        const int g = u >> 1, w = 2 * (2 * ((u & 1) ^ (r8 >> 2)) + hw) + half;
+                        const int dst = g * 512 + (w >> 1) * 128 + r8 * 16 + half * 8;
+                        *reinterpret_cast<uint2*>(oA + dst) = i8x4_to_f16x4(xa[i]);
+                        *reinterpret_cast<uint2*>(oB + dst) =
+                            FMT == FMT_Q8_0 ? i8x4_to_f16x4(wv[i]) : u4x4_to_f16x4(wv[i]);
+                    }
+                    // layout: xd[BM], -xs[BM], w[BN], wmin[BN]
+                    sc[ct] = f16_bits_to_f32(hd);
+                    sc[BM + ct] = -f16_bits_to_f32(hd >> 16);  // -xs, for the min term
+                    sc[2 * BM + ct] = wsc;
+                    sc[2 * BM + BN + ct] = wmn;
                 }
-                sc[ct] = f16_bits_to_f32(hd);
-                sc[BM + ct] = f16_bits_to_f32(hd >> 16);
-                sc[2 * BM + ct] = wsc;
-                sc[2 * BM + BN + ct] = wmn;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(BAR_SLOT_FULL + f));
+                if (lane == 0) {
+                    ptx::mbar_arrive(bar(BAR_SLOT_FULL + gs));
+                    ptx::mbar_arrive(bar(BAR_SC_FULL + gc));
+                }
             }
             __syncwarp();
             if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_RAW_EMPTY + s));
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;                    // TMEM lane quarter this warp may access
-        const int h = (warp - WARP_EPI0) >> 2;     // column half
-        const int mloc = 32 * q + lane;
-        const int mrow = m0 + mloc;
-        float acc[64];
+        // Warp (q = lane quarter, cg = column group) owns rows 32q..32q+31 and columns
+        // c0..c0+31 of the tile.  The block dots are read as two 16-lane x 32-column
+        // fragments: thread t holds rows 32q + t/4 + {0, 8, 16, 24} and columns
+        // c0 + 8k + 2*(t%4) + {0, 1}, k = 0..3, so it needs 4 row scales and 8 column
+        // scales per block (a one-row-per-thread layout would need all 32 column scales,
+        // each a broadcast read of shared memory).
+        const int q = warp & 3;
+        const int cg = (warp - WARP_EPI0) >> 2;
+        const int c0 = cg * EPI_COLS;
+        const int tr = lane >> 2, tc2 = 2 * (lane & 3);
+        const int rloc0 = 32 * q + tr;                 // rows rloc0 + 8*i, i = 0..3 (i = 2*half + i2)
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+        static_assert(EPI_COLS == 32, "one 16x256b.x4 fragment covers 32 columns");
+        unsigned long long acc[16];                    // [row i][col pair k] as packed pairs
 #pragma unroll
-        for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-        for (int bi = 0; bi < nb; ++bi) {
-            const int t = bi % DS, f = bi % FS;
-            if (!(warp_wait(bar(BAR_D_FULL + t), (bi / DS) & 1, abort) &&
-                  warp_wait(bar(BAR_SLOT_FULL + f), (bi / FS) & 1, abort)))
+        for (int c = 0; c < 16; ++c) acc[c] = 0ull;
+        for (int gi = 0; gi < ng; ++gi) {
+            const int gc = gi % SCG, gd = gi % DG;
+            if (!(warp_wait(bar(BAR_D_FULL + gd), (gi / DG) & 1, abort) &&
+                  warp_wait(bar(BAR_SC_FULL + gc), (gi / SCG) & 1, abort)))
                 break;
             ptx::tc_fence_after();
-            const float* sc = reinterpret_cast<const float*>(smem + L::sc + f * SC_FLOATS * 4);
-            const float xd = sc[mloc];
-            const float nxs = -sc[BM + mloc];
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t dv[32];
-                ptx::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(t * BN + 64 * h + 32 * c2), dv);
-                ptx::tmem_ld_wait(dv);
-                const int col0 = 64 * h + 32 * c2;
+#pragma unroll 1
+            for (int jj = 0; jj < G; ++jj) {
+                const int bi = gi * G + jj, t = bi % DS;
+                const float* sc = reinterpret_cast<const float*>(smem + L::sc + (bi % SCN) * SC_FLOATS * 4);
+                const uint32_t taddr = lane_base + (uint32_t)(t * BN);
                 if (DOTS) {
-                    if (mrow < M) {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t dv[16];
+                        ptx::tmem_ld16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16), dv);
+                        ptx::tmem_ld_wait(dv);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int n = n0 + col0 + c;
-                            if (n < N)
-                                dots[((long long)mrow * N + n) * nb + bi] = __float2int_rn(__uint_as_float(dv[c]));
+                        for (int i = 0; i < 2; ++i) {
+                            const int mrow = m0 + rloc0 + 16 * hh + 8 * i;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int n = n0 + c0 + 8 * k + tc2 + e;
+                                    if (mrow < M && n < N)
+                                        dots[((long long)mrow * N + n) * nb + bi] =
+                                            __float2int_rn(__uint_as_float(dv[4 * k + 2 * i + e]));
+                                }
                         }
                     }
                 } else {
+                    // column scales (and, for Q4_K, column min scales) of this thread
+                    unsigned long long w2[4], wm2[4];
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 w = *reinterpret_cast<const float4*>(sc + 2 * BM + col0 + 4 * c4);
-                        const float wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 4 * c4 + e;
-                            acc[32 * c2 + c] = fmaf(xd * wv[e], __uint_as_float(dv[c]), acc[32 * c2 + c]);
-                        }
-                        if (FMT == FMT_Q4_K) {
-                            const float4 mn = *reinterpret_cast<const float4*>(sc + 2 * BM + BN + col0 + 4 * c4);
-                            const float mv[4] = {mn.x, mn.y, mn.z, mn.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                acc[32 * c2 + 4 * c4 + e] = fmaf(mv[e], nxs, acc[32 * c2 + 4 * c4 + e]);
-                        }
+                    for (int k = 0; k < 4; ++k) {
+                        w2[k] = *reinterpret_cast<const unsigned long long*>(sc + 2 * BM + c0 + 8 * k + tc2);
+                        if (FMT == FMT_Q4_K)
+                            wm2[k] = *reinterpret_cast<const unsigned long long*>(sc + 2 * BM + BN + c0 + 8 * k + tc2);
                     }
+                    // acc[row i][pair k] += (xd_i * w_k) * D  (Q4_K: += -xs_i * wmin_k)
+                    auto rescale = [&](const uint32_t (&dv)[16], int hh) {
+#pragma unroll
+                        for (int i2 = 0; i2 < 2; ++i2) {
+                            const int i = 2 * hh + i2;
+                            const float xd = sc[rloc0 + 8 * i];
+                            const unsigned long long xd2 = ptx::f2_bits(xd, xd);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const unsigned long long dd = ptx::f2_bits(__uint_as_float(dv[4 * k + 2 * i2]),
+                                                                           __uint_as_float(dv[4 * k + 2 * i2 + 1]));
+                                acc[4 * i + k] = ptx::fma_f32x2(ptx::mul_f32x2(xd2, w2[k]), dd, acc[4 * i + k]);
+                            }
+                            if (FMT == FMT_Q4_K) {
+                                const float nxs = sc[BM + rloc0 + 8 * i];
+                                const unsigned long long nxs2 = ptx::f2_bits(nxs, nxs);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) acc[4 * i + k] = ptx::fma_f32x2(nxs2, wm2[k], acc[4 * i + k]);
+                            }
+                        }
+                    };
+                    // the two 16-lane halves one after the other (keeping both in flight
+                    // costs 16 more registers than the budget of 704 threads allows)
+                    uint32_t d0[16];
+                    ptx::tmem_ld16x256b_x4(taddr, d0);
+                    ptx::tmem_ld_wait(d0);
+                    rescale(d0, 0);
+                    ptx::tmem_ld16x256b_x4(taddr + (16u << 16), d0);
+                    ptx::tmem_ld_wait(d0);
+                    rescale(d0, 1);
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                ptx::mbar_arrive(bar(BAR_D_EMPTY + t));
-                ptx::mbar_arrive(bar(BAR_SLOT_EMPTY + f));
+                ptx::mbar_arrive(bar(BAR_D_EMPTY + gd));
+                ptx::mbar_arrive(bar(BAR_SC_EMPTY + gc));
             }
         }
-        if (!DOTS && mrow < M && !*abort) {
-            float* orow = out + (long long)mrow * N + n0 + 64 * h;
-            const int ncols = min(64, N - (n0 + 64 * h));
-            if (ncols == 64 && (N & 3) == 0) {
+        if (!DOTS && !*abort) {
 #pragma unroll
-                for (int c = 0; c < 64; c += 4)
-                    *reinterpret_cast<float4*>(orow + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-            } else {
+            for (int i = 0; i < 4; ++i) {
+                const int mrow = m0 + rloc0 + 8 * i;
+                if (mrow >= M) continue;
+                float* orow = out + (long long)mrow * N;
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < ncols) orow[c] = acc[c];
+                for (int k = 0; k < 4; ++k) {
+                    const int n = n0 + c0 + 8 * k + tc2;
+                    if (n + 1 < N && (N & 1) == 0) {
+                        *reinterpret_cast<unsigned long long*>(orow + n) = acc[4 * i + k];
+                    } else {
+                        if (n < N) orow[n] = __uint_as_float((uint32_t)acc[4 * i + k]);
+                        if (n + 1 < N) orow[n + 1] = __uint_as_float((uint32_t)(acc[4 * i + k] >> 32));
+                    }
+                }
             }
         }
     }
