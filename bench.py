@@ -7,7 +7,12 @@ Q8_0 attention projection, M=512 tokens, N=K=3584 (the configuration the headlin
 metric is quoted on).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c1|c2|c3|c3q]
+                  [--workload c1|c2|c3|c3q|layer|sweep]
+
+--workload layer: one 7B GQA transformer layer at 2K-token prefill, x28 layers (the four
+activation quantizes and the seven Q4_K projections; attention, norms and activations
+are not part of the path and are not timed).  --workload sweep: M in {1 .. 8192} on the
+3584x3584 Q4_K projection, one JSON line per M.
 
 --impl reference times the CPU oracle (the plain C fp64 definition) on the host cores
 on a bounded sample of the same workload.  Multi-GPU runs (torchrun, one rank per GPU)
@@ -371,13 +376,135 @@ def run_ours(args, rank, world, local):
     return line
 
 
+def _rotating(torch, dev, arr, copies):
+    t = torch.from_numpy(arr).to(dev)
+    return [t] + [t.clone() for _ in range(copies - 1)]
+
+
+def run_layer(args):
+    """28 layers x (4 quantizes + q, k, v, o, gate, up, down GEMMs) at M=2048, Q4_K.
+    Each layer uses its own device copy of the projection weights (the seven matrices are
+    generated once from their seeds and cloned per layer), so L2 holds none of them."""
+    import torch
+    import block_quantized_int8_mmq_gb300 as mmq
+    dev = torch.device("cuda", 0)
+    M, H, F = 2048, 3584, 18944
+    L = synth.LAYERS_7B
+    w_host = {name: synth.layer_weights(0, name, N, K) for (name, N, K) in synth.LAYER_7B}
+    w_dev = [{name: torch.from_numpy(w_host[name]).to(dev) for name in w_host} for _ in range(1)]
+    for _ in range(L - 1):
+        w_dev.append({name: t.clone() for name, t in w_dev[0].items()})
+    acts = [torch.from_numpy(synth.layer_activations(0, M, K, i)).to(dev) for i, K in enumerate((H, H, H, F))]
+    xq_h = torch.empty(M * (H // 32) * 36, dtype=torch.uint8, device=dev).view(M, -1)
+    xq_f = torch.empty(M * (F // 32) * 36, dtype=torch.uint8, device=dev).view(M, -1)
+    outs = {name: torch.empty((M, N), device=dev) for (name, N, K) in synth.LAYER_7B}
+    stream = torch.cuda.current_stream(dev)
+    q_ev = []
+
+    def layer(l, timed=False):
+        w = w_dev[l]
+        for i, names in enumerate((("q", "k", "v"), ("o",), ("gate", "up"), ("down",))):
+            K = F if i == 3 else H
+            xq = xq_f if i == 3 else xq_h
+            mmq.mmq_quantize_q8_1(acts[i], xq, stream)
+            for name in names:
+                N = outs[name].shape[1]
+                mmq.mmq_gemm_q4_k(xq, w[name], M, N, K, outs[name], stream)
+
+    for l in range(min(L, args.warmup)):
+        layer(l)
+    torch.cuda.synchronize(dev)
+    assert mmq.mmq_get_device_error(stream) == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, args.steps // 10)
+    clocks = ClockSampler(0)
+    clocks.start()
+    a.record(stream)
+    for _ in range(reps):
+        for l in range(L):
+            layer(l)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    assert mmq.mmq_get_device_error(stream) == 0
+    ms = a.elapsed_time(b) / reps
+    ops = 2.0 * M * sum(N * K for (_, N, K) in synth.LAYER_7B) * L
+    return {"metric": "7B-layer prefill ms @2K (28 layers: quantizes + Q4_K projections)", "value": ms,
+            "unit": "ms", "higher_is_better": False, "tok_per_s": M / (ms / 1e3), "tops": ops / (ms / 1e3) / 1e12,
+            "n_gpus": 1, "steps": reps, "warmup": args.warmup, "data": "synthetic (seeded, weights cloned per layer)",
+            "config": {"workload": "7B GQA layer x28 at M=2048, Q4_K (attention, norms, SiLU excluded)"},
+            "gpu_launches": reps * L * 11, "clocks": clk}
+
+
+def run_sweep(args):
+    """M sweep on the 3584x3584 Q4_K projection, plus M = 1 and 8 on the 18944x3584 and
+    3584x18944 projections: one line per case (quantize excluded: the GEMM is timed
+    alone, through CUDA events on the launching stream)."""
+    import torch
+    import block_quantized_int8_mmq_gb300 as mmq
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    lines = []
+    cases = [(M, 3584, 3584, "q") for M in synth.M_SWEEP]
+    # small M on the larger projections too: a 7 MB weight is below the size at which any
+    # kernel on this GPU streams at full HBM bandwidth
+    cases += [(M, 18944, 3584, "gate") for M in (1, 8)] + [(M, 3584, 18944, "down") for M in (1, 8)]
+    wcache = {}
+    for (M, N, K, proj) in cases:
+        if proj not in wcache:
+            wcache.clear()
+            wcache[proj] = synth.layer_weights(0, proj, N, K)
+        w = wcache[proj]
+        x = synth.activations(synth.substream(synth.BASE_SEED + 4, 7000 + M), M, K, True)
+        wbytes = w.nbytes
+        copies = max(2, -(-3 * L2_BYTES // (wbytes + x.nbytes)))
+        ws = _rotating(torch, dev, w, copies)
+        xd = torch.from_numpy(x).to(dev)
+        xq = mmq.mmq_quantize_q8_1(xd)
+        out = torch.empty((M, N), device=dev)
+        stream = torch.cuda.current_stream(dev)
+        iters = max(20, args.steps)
+        for i in range(args.warmup):
+            mmq.mmq_gemm_q4_k(xq, ws[i % copies], M, N, K, out, stream)
+        torch.cuda.synchronize(dev)
+        path = mmq.mmq_last_path()
+        # the timed launches are captured in one CUDA graph, so the gaps between
+        # back-to-back launches (comparable to a small-M kernel) are not counted
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(iters):
+                mmq.mmq_gemm_q4_k(xq, ws[i % copies], M, N, K, out)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        assert mmq.mmq_get_device_error(stream) == 0
+        ms = a.elapsed_time(b) / iters
+        ops = 2.0 * M * N * K
+        abytes = wbytes + xq.numel() + M * N * 4
+        gbs = abytes / (ms / 1e3) / 1e9
+        tops = ops / (ms / 1e3) / 1e12
+        lines.append({"M": M, "N": N, "K": K, "ms": ms, "tops": tops, "gbs": gbs, "tok_per_s": M / (ms / 1e3),
+                      "path": "tcgen05" if path == mmq.PATH_TC else "warp-level",
+                      "frac_hbm": gbs / peaks["hbm_gbs"], "frac_tensor": tops / peaks["bf16_tflops"],
+                      "algorithmic_bytes": abytes})
+        del ws
+    return {"metric": "Q4_K MMQ 3584x3584 M sweep (GEMM only)", "unit": "mixed", "lines": lines,
+            "data": "synthetic (seeded)", "peaks": peaks,
+            "config": {"workload": "3584x3584 Q4_K projection, M in " + str(synth.M_SWEEP),
+                       "l2": "rotating weight copies >= 3x L2", "cuda_graph": True}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c1")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["layer", "sweep"], default="c1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per reference-arm step")
@@ -387,11 +514,17 @@ def main():
     rank, world, local = dist_env()
 
     if args.impl == "reference":
+        if args.workload in ("layer", "sweep"):
+            args.workload = "c3" if args.workload == "layer" else "c1"
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args)), flush=True)
         return 0
 
+    if args.workload in ("layer", "sweep"):
+        if rank == 0:
+            print(json.dumps(run_layer(args) if args.workload == "layer" else run_sweep(args)), flush=True)
+        return 0
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")

@@ -180,7 +180,7 @@ int mmq_get_device_error(void* stream) {
         fprintf(stderr, "libmmq: mmq_get_device_error: %s\n", cudaGetErrorString(e));
         return MMQ_ERR_CUDA;
     }
-    const unsigned bits = tc_take_error();
+    const unsigned bits = tc_take_error() | small_take_error();
     return (bits & ERR_TIMEOUT) ? MMQ_ERR_TIMEOUT : MMQ_OK;
 }
 

@@ -53,6 +53,7 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
 int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
               int32_t* dots, cudaStream_t s);
 unsigned tc_take_error();
+unsigned small_take_error();
 void report(const char* fn, int status, const char* detail);
 int launch_status(const char* fn);
 }  // namespace mmq
