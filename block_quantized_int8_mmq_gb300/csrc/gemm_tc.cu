@@ -1,16 +1,26 @@
-// Tensor-core MMQ for sm_103a: tcgen05.mma into TMEM with a per-32-block drain.
+// Tensor-core MMQ for sm_103a: tcgen05.mma into TMEM, with the per-32-block scale
+// applied by one fused multiply-add per output element.
 //
 // The method applies a new f32 scale at every 32-value block boundary ("When the
 // Product Won't Collapse", sec. "The obstruction": int8 accumulation is only valid
-// inside one constant-scale block), so the int8 block dot D[m,n,b] must be formed
-// exactly, then rescaled in registers ("The viable route is per-backend anyway": apply
-// the scale in register, with no shared-memory round trip of the accumulator).
+// inside one constant-scale block), so the int8 block dot D[m,n,b] is formed exactly
+// and rescaled in registers ("The viable route is per-backend anyway": apply the scale
+// in register, with no shared-memory round trip of the accumulator).
 //
 // sm_103a has no integer tcgen05 MMA kind, and its int8 mma.sync rate is ~1/12 of the
-// fp16 tensor rate.  Every int8 code (and every Q4_K nibble) is an exact fp16 value,
-// each product is an integer of magnitude <= 2^14 and every partial sum of a 32-term
-// block dot is an integer of magnitude <= 2^19, so an fp16 x fp16 -> f32 MMA over one
-// block computes D exactly.  That is the contraction used here.
+// fp16 tensor rate.  Every int8 code (and every Q4_K nibble times its 6-bit sub-scale,
+// at most 945) is an exact fp16 value, each product is an integer below 2^17 and every
+// partial sum of a 32-term block dot an integer below 2^22, so an fp16 x fp16 -> f32
+// MMA over one block computes the block dot exactly.
+//
+// The scale of block b is the outer product S_b = xd[:,b] (x) w[:,b] of two vectors of
+// exact f16 values (Q8_0: w = wd; Q4_K: w = d of the super-block, the sub-scale sc_j
+// being folded into the weight codes).  A second, K=16 MMA whose operands carry xd and
+// w in column 0 (zeros elsewhere) writes S_b exactly into TMEM next to D_b, so the
+// epilogue is acc += S_b * D_b: one FMA per element, no scale reads.  The Q4_K min term
+// sum_j -dmin*m_j*xs_j of a super-block becomes a ninth item with D = sum_j xs_j*m_j
+// (K=16 MMA of the f16 sums s against the 6-bit mins) and S = 1 (x) (-dmin)
+// ("When Does a Kernel Win Surface?", sec. "Kept levers: Vulkan", affine identity).
 //
 // Warp roles (one 128 x 128 output tile per CTA, 704 threads):
 //   warp 0     TMA producer: raw q8_1 rows (288 B per 256 values) and raw weight rows
@@ -18,20 +28,18 @@
 //              2-D tensor copies into a 2-stage ring ("13 . r7-r8 raw-byte MMQ
 //              kernel", sec. 2: shared memory holds raw quant bytes; sec. 3.1: whole
 //              super-blocks, out-of-range rows zero-filled by the copy engine).
-//   warp 1     TMEM owner and MMA issuer: per 32-block, two K=16 MMAs (M=128, N=128)
-//              into one of four TMEM accumulators; one tcgen05.commit per group of
-//              two blocks (barrier round trips cost more than the work between them).
-//   warps 2-5  converters: codes -> fp16 (sign-biased byte permute + one half2
-//              subtract, exact) into the canonical K-major no-swizzle UMMA layout, and
-//              the per-row / per-column block scales into a small scale ring
-//              (Q4_K: d*sc_j and dmin*m_j from the 12 packed bytes, computed once per
-//              (row, block) instead of per lane, as in sec. 3.2 of the same page).
-//   warps 6-21 epilogue, 32 rows x 32 columns each: per 32-block, tcgen05.ld of the
-//              f32 block dots in 8-column chunks (the next loads while one is rescaled), then
-//              acc += (xd*wd) * D (Q4_K: wd = d*sc_j, and acc -= dmin*m_j*xs) with packed
-//              f32x2 multiply / FMA in registers; at the end the tile is stored to out.
+//   warp 1     TMEM owner and MMA issuer: per item, D (two K=16 MMAs; one for a min
+//              item) and S (one K=16 MMA) into one of two TMEM slots, then commits.
+//   warps 2-5  converters: codes -> exact fp16 (sign-biased byte permute and one half2
+//              subtract; Q4_K: half2 fused multiply by sc_j) in the canonical K-major
+//              no-swizzle UMMA layout, bank-conflict-free; the f16 scale vectors into
+//              column 0 of the scale operands.
+//   warps 6-21 epilogue, 32 rows x 32 columns each: per item, 16x256b TMEM fragments of
+//              D and S, acc += S * D with packed f32x2 FMA; at the end, 8-byte stores.
 // Every wait is bounded by wall time; on expiry the kernel records ERR_TIMEOUT, lets
 // the other roles fall out, drains its own copies and MMAs, frees TMEM and returns.
+// The block-dot test hook (DOTS) stages and multiplies the raw codes (no sc_j fold, no
+// min items) through the same pipeline and writes D.
 #include <cudaTypedefs.h>
 #include <stdio.h>
 #include <string.h>
@@ -45,58 +53,50 @@ namespace {
 __device__ unsigned int g_tc_error;
 
 constexpr int BM = 128;                 // activation rows per tile (TMEM lanes)
-constexpr int BN = 128;                 // weight rows per tile (MMA N, TMEM columns)
+constexpr int BN = 128;                 // weight rows per tile (MMA N)
 constexpr int KT_BLOCKS = 8;            // 32-blocks per staged k-tile (256 values)
 constexpr int RS = 2;                   // raw k-tile stages
-constexpr int FS = 4;                   // fp16 operand slots (one 32-block each)
-constexpr int SCN = 8;                  // scale slots (one 32-block each)
-constexpr int DS = 4;                   // TMEM accumulators (one 32-block each)
-constexpr int G = 2;                    // 32-blocks per barrier round trip (a "group")
-constexpr int SG = FS / G;              // operand slot groups in flight
-constexpr int SCG = SCN / G;            // scale slot groups in flight
-constexpr int DG = DS / G;              // TMEM groups in flight
+constexpr int FS = 3;                   // operand slots (one item each)
+constexpr int DS = 2;                   // TMEM slots (D and S of one item each)
 constexpr int CONV_WARPS = 4;
 constexpr int EPI_WARPS = 16;
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // columns per epilogue warp (4 lane quarters)
 constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, WARP_EPI0 = WARP_CONV0 + CONV_WARPS;
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
-constexpr int TMEM_COLS = DS * BN;      // 512: the whole TMEM of the SM
+constexpr int TMEM_COLS = DS * 2 * BN;  // 512: the whole TMEM of the SM
 constexpr int A_ROW = KT_BLOCKS * Q8_1_BYTES;  // 288
-constexpr int OP_A = BM * QK * 2;       // fp16 A tile of one block: 8 KiB
-constexpr int OP_B = BN * QK * 2;       // fp16 B tile of one block: 8 KiB
-constexpr int SC_FLOATS = 2 * BM + 2 * BN;
+constexpr int OP_MAIN = BM * QK * 2;    // fp16 tile of one block (K = 32): 8 KiB
+constexpr int OP_AUX = BM * 16 * 2;     // fp16 scale operand (K = 16, column 0 used): 4 KiB
+constexpr int SLOT = 2 * OP_MAIN + 2 * OP_AUX;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bound on any one wait
 constexpr uint32_t WAIT_SLEEP_NS = 100000;           // longest sleep inside one poll
 
-static_assert(BM == 32 * CONV_WARPS && BN == 32 * CONV_WARPS, "one activation and one weight scale row per converter thread");
-static_assert(32 % CONV_WARPS == 0, "32 conversion units per operand tile");
-static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 8 == 0, "epilogue covers 4 lane quarters x column groups");
+static_assert(BM == 32 * CONV_WARPS && BN == 32 * CONV_WARPS, "one activation and one weight row per converter thread");
+static_assert(EPI_COLS == 32, "one 16x256b.x4 fragment covers 32 columns");
 
 __host__ __device__ constexpr int b_row(int fmt) { return fmt == FMT_Q8_0 ? KT_BLOCKS * Q8_0_BYTES : Q4_K_BYTES; }
+// items per k-tile: 8 blocks, plus the min item of the super-block for Q4_K
+__host__ __device__ constexpr int items_per_kt(int fmt, bool dots) {
+    return KT_BLOCKS + (fmt == FMT_Q4_K && !dots ? 1 : 0);
+}
 
-// barrier indices.  A slot group holds the fp16 operands of G 32-blocks (SLOT_FULL:
-// every converter warp arrives; SLOT_EMPTY: the MMA commit).  The scales of a group sit
-// in a deeper ring of their own (SC_FULL: converters; SC_EMPTY: every epilogue warp), so
-// that operand slots come free as soon as their MMAs complete.  D_FULL / D_EMPTY guard
-// the G TMEM accumulators of a group.
+// barrier indices: raw stages, operand slots (converters -> MMA -> converters), TMEM
+// slots (MMA -> epilogue -> MMA), and a drain barrier for teardown
 constexpr int BAR_RAW_FULL = 0, BAR_RAW_EMPTY = BAR_RAW_FULL + RS, BAR_SLOT_FULL = BAR_RAW_EMPTY + RS,
-              BAR_SLOT_EMPTY = BAR_SLOT_FULL + SG, BAR_SC_FULL = BAR_SLOT_EMPTY + SG, BAR_SC_EMPTY = BAR_SC_FULL + SCG,
-              BAR_D_FULL = BAR_SC_EMPTY + SCG, BAR_D_EMPTY = BAR_D_FULL + DG, BAR_DRAIN = BAR_D_EMPTY + DG,
-              NBARS = BAR_DRAIN + 1;
-static_assert(KT_BLOCKS % G == 0 && FS % G == 0 && DS % G == 0 && SCN % G == 0, "groups tile the rings");
+              BAR_SLOT_EMPTY = BAR_SLOT_FULL + FS, BAR_D_FULL = BAR_SLOT_EMPTY + FS, BAR_D_EMPTY = BAR_D_FULL + DS,
+              BAR_DRAIN = BAR_D_EMPTY + DS, NBARS = BAR_DRAIN + 1;
 
 template <int FMT>
 struct Layout {
     static constexpr int rawA = 0;
     static constexpr int rawB = rawA + RS * BM * A_ROW;
-    static constexpr int opA = rawB + RS * BN * b_row(FMT);
-    static constexpr int opB = opA + FS * OP_A;
-    static constexpr int sc = opB + FS * OP_B;
-    static constexpr int bars = sc + SCN * SC_FLOATS * 4;
+    static constexpr int slots = rawB + RS * BN * b_row(FMT);
+    static constexpr int sctab = slots + FS * SLOT;  // Q4_K: per converter warp, (sc, -1024 sc) of its 64 rows x 8
+    static constexpr int bars = sctab + (FMT == FMT_Q4_K ? CONV_WARPS * 64 * 8 * 4 : 0);
     static constexpr int tmem_slot = bars + NBARS * 8;
     static constexpr int total = tmem_slot + 16;
     static constexpr int alloc = total + 1024;  // slack to align the base to 1 KiB
-    static_assert(rawB % 1024 == 0 && opA % 1024 == 0 && opB % 1024 == 0 && sc % 16 == 0, "alignment");
+    static_assert(rawB % 1024 == 0 && slots % 1024 == 0 && SLOT % 1024 == 0, "alignment");
 };
 
 // Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major.
@@ -106,35 +106,38 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
 
 // Shared-memory matrix descriptor, K-major, no swizzle: core matrices of 8 rows x 16 B
 // (8 fp16 along K) stored as 128 contiguous bytes; the next core matrix along K is
-// 128 B further (leading-dimension offset), the next 8-row group 512 B further
-// (stride-dimension offset: 4 core matrices cover the block's 32 values of K).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(512 >> 4) << 32) |
+// 128 B further (leading-dimension offset), the next 8-row group `sbo` bytes further
+// (512 for a K = 32 tile, 256 for a K = 16 tile).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
            (1ull << 46);
 }
 
-__device__ __forceinline__ uint32_t h2_sub_bits(uint32_t a, uint32_t b) {
-    __half2 x, y;
-    memcpy(&x, &a, 4);
-    memcpy(&y, &b, 4);
-    const __half2 r = __hsub2(x, y);
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) {
     uint32_t o;
-    memcpy(&o, &r, 4);
+    memcpy(&o, &h, 4);
     return o;
+}
+__device__ __forceinline__ __half2 bits_h2(uint32_t v) {
+    __half2 h;
+    memcpy(&h, &v, 4);
+    return h;
 }
 
 // Four signed int8 codes -> four exact fp16 values.  (x + 128) is placed in the low
 // mantissa byte of 1024.0 (bits 0x64xx), then 1152 = 1024 + 128 is subtracted.
 __device__ __forceinline__ uint2 i8x4_to_f16x4(uint32_t w) {
     const uint32_t u = w ^ 0x80808080u;
-    return make_uint2(h2_sub_bits(__byte_perm(u, 0x64646464u, 0x4140), 0x64806480u),
-                      h2_sub_bits(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u));
+    const __half2 bias = bits_h2(0x64806480u);
+    return make_uint2(h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4140)), bias)),
+                      h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4342)), bias)));
 }
 
-// Four codes 0..15 (one per byte) -> four exact fp16 values (1024 + q, minus 1024).
-__device__ __forceinline__ uint2 u4x4_to_f16x4(uint32_t w) {
-    return make_uint2(h2_sub_bits(__byte_perm(w, 0x64646464u, 0x4140), 0x64006400u),
-                      h2_sub_bits(__byte_perm(w, 0x64646464u, 0x4342), 0x64006400u));
+// Four codes q in 0..15 (one per byte) -> four exact fp16 values sc*q, from the bits of
+// 1024 + q and one fused (1024 + q)*sc - 1024*sc (exact: sc*q <= 945).
+__device__ __forceinline__ uint2 u4x4_scaled_f16x4(uint32_t w, __half2 sc2, __half2 nsc1024) {
+    return make_uint2(h2_bits(__hfma2(bits_h2(__byte_perm(w, 0x64646464u, 0x4140)), sc2, nsc1024)),
+                      h2_bits(__hfma2(bits_h2(__byte_perm(w, 0x64646464u, 0x4342)), sc2, nsc1024)));
 }
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the wall
@@ -173,12 +176,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Offset of (row r, k-group kg of 8 fp16) in a K-major no-swizzle tile with 8-row-group
+// stride sbo.
+__device__ __forceinline__ int core_off(int r, int kg, int sbo) { return (r >> 3) * sbo + kg * 128 + (r & 7) * 16; }
+
 template <int FMT, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int nb,
          float* __restrict__ out, int32_t* __restrict__ dots) {
     using L = Layout<FMT>;
     constexpr int BROW = b_row(FMT);
+    constexpr int IPK = items_per_kt(FMT, DOTS);
+    constexpr bool FOLD = FMT == FMT_Q4_K && !DOTS;  // sc_j folded into the weight codes
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -186,8 +195,10 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
     const int nkt = nb / KT_BLOCKS;
+    const int nitems = nkt * IPK;
     volatile int* abort = &s_abort;
     auto bar = [&](int i) -> uint32_t { return sbase + L::bars + 8 * i; };
+    auto slot_ptr = [&](int f) -> uint8_t* { return smem + L::slots + f * SLOT; };
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -195,21 +206,23 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             ptx::mbar_init(bar(BAR_RAW_FULL + i), 1);
             ptx::mbar_init(bar(BAR_RAW_EMPTY + i), CONV_WARPS);
         }
-        for (int i = 0; i < SG; ++i) {
+        for (int i = 0; i < FS; ++i) {
             ptx::mbar_init(bar(BAR_SLOT_FULL + i), CONV_WARPS);
             ptx::mbar_init(bar(BAR_SLOT_EMPTY + i), 1);
         }
-        for (int i = 0; i < SCG; ++i) {
-            ptx::mbar_init(bar(BAR_SC_FULL + i), CONV_WARPS);
-            ptx::mbar_init(bar(BAR_SC_EMPTY + i), EPI_WARPS);
-        }
-        for (int i = 0; i < DG; ++i) {
+        for (int i = 0; i < DS; ++i) {
             ptx::mbar_init(bar(BAR_D_FULL + i), 1);
             ptx::mbar_init(bar(BAR_D_EMPTY + i), EPI_WARPS);
         }
         ptx::mbar_init(bar(BAR_DRAIN), 1);
         ptx::fence_barrier_init();
     }
+    // the scale operands only ever hold column 0: zero all slots once
+    for (int i = threadIdx.x; i < FS * 2 * OP_AUX / 16; i += THREADS) {
+        const int f = i / (2 * OP_AUX / 16), o = i % (2 * OP_AUX / 16);
+        reinterpret_cast<uint4*>(slot_ptr(f) + 2 * OP_MAIN)[o] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    ptx::fence_proxy_async_smem();
     if (warp == WARP_MMA) {
         ptx::tmem_alloc(sbase + L::tmem_slot, TMEM_COLS);
         ptx::tmem_relinquish();
@@ -222,7 +235,6 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::tmem_slot);
-    const int ng = nb / G;
 
     if (warp == WARP_TMA) {
         // ------------------------------------------------------------ producer
@@ -245,21 +257,20 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc(BM, BN);
-            for (int gi = 0; gi < ng; ++gi) {
-                const int gs = gi % SG, gd = gi % DG;
-                if (!wait_bar(bar(BAR_SLOT_FULL + gs), (gi / SG) & 1, abort)) break;
-                if (!wait_bar(bar(BAR_D_EMPTY + gd), ((gi / DG) & 1) ^ 1, abort)) break;
+            for (int it = 0; it < nitems; ++it) {
+                const int f = it % FS, t = it % DS;
+                if (!wait_bar(bar(BAR_SLOT_FULL + f), (it / FS) & 1, abort)) break;
+                if (!wait_bar(bar(BAR_D_EMPTY + t), ((it / DS) & 1) ^ 1, abort)) break;
                 ptx::tc_fence_after();
-#pragma unroll
-                for (int jj = 0; jj < G; ++jj) {
-                    const int bi = gi * G + jj, f = bi % FS, t = bi % DS;
-                    const uint32_t a = sbase + L::opA + f * OP_A, b = sbase + L::opB + f * OP_B;
-                    const uint32_t d = tmem + (uint32_t)(t * BN);
-                    ptx::umma_f16(d, sdesc(a), sdesc(b), idesc, 0u);
-                    ptx::umma_f16(d, sdesc(a + 256), sdesc(b + 256), idesc, 1u);
-                }
-                ptx::umma_commit(bar(BAR_SLOT_EMPTY + gs));
-                ptx::umma_commit(bar(BAR_D_FULL + gd));
+                const uint32_t a = sbase + L::slots + f * SLOT, b = a + OP_MAIN;
+                const uint32_t as = b + OP_MAIN, bs = as + OP_AUX;
+                const uint32_t d = tmem + (uint32_t)(t * 2 * BN), sd = d + BN;
+                const bool min_item = IPK > KT_BLOCKS && (it % IPK) == KT_BLOCKS;
+                ptx::umma_f16(d, sdesc(a, 512), sdesc(b, 512), idesc, 0u);
+                if (!min_item) ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + 256, 512), idesc, 1u);
+                if (!DOTS) ptx::umma_f16(sd, sdesc(as, 256), sdesc(bs, 256), idesc, 0u);
+                ptx::umma_commit(bar(BAR_SLOT_EMPTY + f));
+                ptx::umma_commit(bar(BAR_D_FULL + t));
             }
             ptx::umma_commit(bar(BAR_DRAIN));  // arrives once every MMA issued above is done
             drain_bar(bar(BAR_DRAIN), 0);
@@ -268,26 +279,50 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     } else if (warp < WARP_EPI0) {
         // ------------------------------------------------------------ converters
         const int cw = warp - WARP_CONV0;
-        const int ct = cw * 32 + lane;
+        const int ct = cw * 32 + lane;          // the activation row and the weight row of this thread
         const int r8 = lane & 7, half = (lane >> 3) & 1, hw = lane >> 4;
+        // This warp converts the rows 8*(2i + cw/2) + r8, i = 0..7 (see the unit mapping
+        // below); its table of their sub-scales, [8*i + r8][sub-block], is private to it.
+        uint32_t* sct = reinterpret_cast<uint32_t*>(smem + L::sctab) + cw * 64 * 8;
         bool ok = true;
+        int it = 0;
         for (int kt = 0; kt < nkt && ok; ++kt) {
             const int s = kt % RS;
             ok = warp_wait(bar(BAR_RAW_FULL + s), (kt / RS) & 1, abort);
             if (!ok) break;
             const uint8_t* rA = smem + L::rawA + s * BM * A_ROW;
             const uint8_t* rB = smem + L::rawB + s * BN * BROW;
-            for (int gl = 0; gl < KT_BLOCKS / G; ++gl) {
-                const int gi = kt * (KT_BLOCKS / G) + gl, gs = gi % SG, gc = gi % SCG;
-                ok = warp_wait(bar(BAR_SLOT_EMPTY + gs), ((gi / SG) & 1) ^ 1, abort) &&
-                     warp_wait(bar(BAR_SC_EMPTY + gc), ((gi / SCG) & 1) ^ 1, abort);
+            uint4 whdr = make_uint4(0u, 0u, 0u, 0u);  // Q4_K: this thread's weight row super-block header
+            if (FMT == FMT_Q4_K) {
+                whdr = *reinterpret_cast<const uint4*>(rB + ct * BROW);
+                if (FOLD) {
+                    // lane l decodes the sub-scales of table rows 2l and 2l+1
+                    __syncwarp();  // this warp's reads of the previous k-tile's table are done
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tr = 2 * lane + e, row = 8 * (2 * (tr >> 3) + (cw >> 1)) + (tr & 7);
+                        const uint4 h = *reinterpret_cast<const uint4*>(rB + row * BROW);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            int s6, m6;
+                            q4_k_scale_min(h.y, h.z, h.w, j, s6, m6);
+                            sct[tr * 8 + j] = h2_bits(__halves2half2(__int2half_rn(s6), __int2half_rn(-1024 * s6)));
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            for (int ii = 0; ii < IPK && ok; ++ii, ++it) {
+                const int f = it % FS;
+                ok = warp_wait(bar(BAR_SLOT_EMPTY + f), ((it / FS) & 1) ^ 1, abort);
                 if (!ok) break;
-#pragma unroll 1
-                for (int jj = 0; jj < G; ++jj) {
-                    const int j = gl * G + jj, bi = kt * KT_BLOCKS + j, f = bi % FS;
-                    uint8_t* oA = smem + L::opA + f * OP_A;
-                    uint8_t* oB = smem + L::opB + f * OP_B;
-                    float* sc = reinterpret_cast<float*>(smem + L::sc + (bi % SCN) * SC_FLOATS * 4);
+                uint8_t* oA = slot_ptr(f);
+                uint8_t* oB = oA + OP_MAIN;
+                uint16_t* aS = reinterpret_cast<uint16_t*>(oB + OP_MAIN);   // column 0 of the scale operands
+                uint16_t* bS = reinterpret_cast<uint16_t*>(oB + OP_MAIN + OP_AUX);
+                const int aux0 = core_off(ct, 0, 256) / 2;                   // element index of (row ct, k 0)
+                if (ii < KT_BLOCKS) {
+                    const int j = ii;
                     // All raw loads first (the stores below go to the same shared array,
                     // so the compiler would otherwise keep every load behind the previous
                     // store).  Unit i = (8-row group g, pass p), lane = (hw, half, r8):
@@ -297,7 +332,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                     // different banks; each half-warp stores rows 0-3 of one k-group and
                     // rows 4-7 of another, two 64-byte runs in opposite bank halves.
                     constexpr int UNITS = 32 / CONV_WARPS;
-                    uint32_t xa[UNITS], wv[UNITS];
+                    uint32_t xa[UNITS], wv[UNITS], scv[UNITS];
 #pragma unroll
                     for (int i = 0; i < UNITS; ++i) {
                         const int u = i * CONV_WARPS + cw;
@@ -315,43 +350,55 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                             const uint32_t raw =
                                 *reinterpret_cast<const uint32_t*>(rB + r * BROW + 16 + 32 * (j >> 1) + w * 4);
                             wv[i] = (j & 1) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
+                            if (FOLD) scv[i] = sct[(i * 8 + r8) * 8 + j];  // table row 8i + r8 is row 8g + r8
                         }
                     }
-                    // scales: converter thread ct takes activation row ct and weight row ct
-                    const uint32_t hd = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
-                    float wsc, wmn;
-                    if (FMT == FMT_Q8_0) {
-                        wsc = f16_bits_to_f32(
-                            *reinterpret_cast<const unsigned short*>(rB + ct * BROW + j * Q8_0_BYTES));
-                        wmn = 0.f;
-                    } else {
-                        const uint4 p = *reinterpret_cast<const uint4*>(rB + ct * BROW);
-                        int s6, m6;
-                        q4_k_scale_min(p.y, p.z, p.w, j, s6, m6);
-                        wsc = f16_bits_to_f32(p.x) * (float)s6;        // exact: d * sc_j
-                        wmn = f16_bits_to_f32(p.x >> 16) * (float)m6;  // exact: dmin * m_j
-                    }
+                    // column 0 of the scale operands: xd of row ct, w of row ct
+                    const uint16_t xdh = *reinterpret_cast<const uint16_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
+                    const uint16_t wdh = FMT == FMT_Q8_0
+                                             ? *reinterpret_cast<const uint16_t*>(rB + ct * BROW + j * Q8_0_BYTES)
+                                             : (uint16_t)(whdr.x & 0xffffu);
 #pragma unroll
                     for (int i = 0; i < UNITS; ++i) {
                         const int u = i * CONV_WARPS + cw;
                         const int g = u >> 1, w = 2 * (2 * ((u & 1) ^ (r8 >> 2)) + hw) + half;
                         const int dst = g * 512 + (w >> 1) * 128 + r8 * 16 + half * 8;
                         *reinterpret_cast<uint2*>(oA + dst) = i8x4_to_f16x4(xa[i]);
-                        *reinterpret_cast<uint2*>(oB + dst) =
-                            FMT == FMT_Q8_0 ? i8x4_to_f16x4(wv[i]) : u4x4_to_f16x4(wv[i]);
+                        if (FMT == FMT_Q8_0)
+                            *reinterpret_cast<uint2*>(oB + dst) = i8x4_to_f16x4(wv[i]);
+                        else if (FOLD)
+                            *reinterpret_cast<uint2*>(oB + dst) = u4x4_scaled_f16x4(
+                                wv[i], __low2half2(bits_h2(scv[i])), __high2half2(bits_h2(scv[i])));
+                        else
+                            *reinterpret_cast<uint2*>(oB + dst) =
+                                u4x4_scaled_f16x4(wv[i], __float2half2_rn(1.f), __float2half2_rn(-1024.f));
                     }
-                    // layout: xd[BM], -xs[BM], w[BN], wmin[BN]
-                    sc[ct] = f16_bits_to_f32(hd);
-                    sc[BM + ct] = -f16_bits_to_f32(hd >> 16);  // -xs, for the min term
-                    sc[2 * BM + ct] = wsc;
-                    sc[2 * BM + BN + ct] = wmn;
+                    aS[aux0] = xdh;
+                    bS[aux0] = wdh;
+                } else {
+                    // Q4_K min item: A row m = (s of the 8 blocks, 0 x 8), B row n = (m_0..m_7,
+                    // 0 x 8); scale operands: A = 1, B = -dmin
+                    uint32_t sv[4], mv[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t s0 = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + (2 * jj) * Q8_1_BYTES);
+                        const uint32_t s1 = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + (2 * jj + 1) * Q8_1_BYTES);
+                        sv[jj] = (s0 >> 16) | (s1 & 0xffff0000u);
+                        int sc0, mn0, sc1, mn1;
+                        q4_k_scale_min(whdr.y, whdr.z, whdr.w, 2 * jj, sc0, mn0);
+                        q4_k_scale_min(whdr.y, whdr.z, whdr.w, 2 * jj + 1, sc1, mn1);
+                        mv[jj] = h2_bits(__halves2half2(__int2half_rn(mn0), __int2half_rn(mn1)));
+                    }
+                    *reinterpret_cast<uint4*>(oA + core_off(ct, 0, 512)) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
+                    *reinterpret_cast<uint4*>(oA + core_off(ct, 1, 512)) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(oB + core_off(ct, 0, 512)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
+                    *reinterpret_cast<uint4*>(oB + core_off(ct, 1, 512)) = make_uint4(0u, 0u, 0u, 0u);
+                    aS[aux0] = 0x3C00;                                     // 1.0
+                    bS[aux0] = (uint16_t)((whdr.x >> 16) ^ 0x8000u);       // -dmin
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(bar(BAR_SLOT_FULL + gs));
-                    ptx::mbar_arrive(bar(BAR_SC_FULL + gc));
-                }
+                if (lane == 0) ptx::mbar_arrive(bar(BAR_SLOT_FULL + f));
             }
             __syncwarp();
             if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_RAW_EMPTY + s));
@@ -359,99 +406,68 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     } else {
         // ------------------------------------------------------------ epilogue
         // Warp (q = lane quarter, cg = column group) owns rows 32q..32q+31 and columns
-        // c0..c0+31 of the tile.  The block dots are read as two 16-lane x 32-column
-        // fragments: thread t holds rows 32q + t/4 + {0, 8, 16, 24} and columns
-        // c0 + 8k + 2*(t%4) + {0, 1}, k = 0..3, so it needs 4 row scales and 8 column
-        // scales per block (a one-row-per-thread layout would need all 32 column scales,
-        // each a broadcast read of shared memory).
+        // c0..c0+31 of the tile.  D and S are read as 16-lane x 32-column fragments:
+        // thread t holds rows 32q + t/4 + {0, 8} (+16 for the second half) and columns
+        // c0 + 8k + 2*(t%4) + {0, 1}, k = 0..3; D and S have the same layout, so the
+        // rescale is an elementwise FMA on the fragments.
         const int q = warp & 3;
         const int cg = (warp - WARP_EPI0) >> 2;
         const int c0 = cg * EPI_COLS;
         const int tr = lane >> 2, tc2 = 2 * (lane & 3);
         const int rloc0 = 32 * q + tr;                 // rows rloc0 + 8*i, i = 0..3 (i = 2*half + i2)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
-        static_assert(EPI_COLS == 32, "one 16x256b.x4 fragment covers 32 columns");
         unsigned long long acc[16];                    // [row i][col pair k] as packed pairs
 #pragma unroll
         for (int c = 0; c < 16; ++c) acc[c] = 0ull;
-        for (int gi = 0; gi < ng; ++gi) {
-            const int gc = gi % SCG, gd = gi % DG;
-            if (!(warp_wait(bar(BAR_D_FULL + gd), (gi / DG) & 1, abort) &&
-                  warp_wait(bar(BAR_SC_FULL + gc), (gi / SCG) & 1, abort)))
-                break;
+        for (int it = 0; it < nitems; ++it) {
+            const int t = it % DS;
+            if (!warp_wait(bar(BAR_D_FULL + t), (it / DS) & 1, abort)) break;
             ptx::tc_fence_after();
+            const uint32_t taddr = lane_base + (uint32_t)(t * 2 * BN);
+            if (DOTS) {
+                const int bi = it;  // no min items in this mode
 #pragma unroll 1
-            for (int jj = 0; jj < G; ++jj) {
-                const int bi = gi * G + jj, t = bi % DS;
-                const float* sc = reinterpret_cast<const float*>(smem + L::sc + (bi % SCN) * SC_FLOATS * 4);
-                const uint32_t taddr = lane_base + (uint32_t)(t * BN);
-                if (DOTS) {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t dv[16];
-                        ptx::tmem_ld16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16), dv);
-                        ptx::tmem_ld_wait(dv);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t dv[16];
+                    ptx::tmem_ld16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16), dv);
+                    ptx::tmem_ld_wait(dv);
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const int mrow = m0 + rloc0 + 16 * hh + 8 * i;
+                    for (int i = 0; i < 2; ++i) {
+                        const int mrow = m0 + rloc0 + 16 * hh + 8 * i;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
+                        for (int k = 0; k < 4; ++k)
 #pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int n = n0 + c0 + 8 * k + tc2 + e;
-                                    if (mrow < M && n < N)
-                                        dots[((long long)mrow * N + n) * nb + bi] =
-                                            __float2int_rn(__uint_as_float(dv[4 * k + 2 * i + e]));
-                                }
-                        }
-                    }
-                } else {
-                    // column scales (and, for Q4_K, column min scales) of this thread
-                    unsigned long long w2[4], wm2[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        w2[k] = *reinterpret_cast<const unsigned long long*>(sc + 2 * BM + c0 + 8 * k + tc2);
-                        if (FMT == FMT_Q4_K)
-                            wm2[k] = *reinterpret_cast<const unsigned long long*>(sc + 2 * BM + BN + c0 + 8 * k + tc2);
-                    }
-                    // acc[row i][pair k] += (xd_i * w_k) * D  (Q4_K: += -xs_i * wmin_k)
-                    auto rescale = [&](const uint32_t (&dv)[16], int hh) {
-#pragma unroll
-                        for (int i2 = 0; i2 < 2; ++i2) {
-                            const int i = 2 * hh + i2;
-                            const float xd = sc[rloc0 + 8 * i];
-                            const unsigned long long xd2 = ptx::f2_bits(xd, xd);
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const unsigned long long dd = ptx::f2_bits(__uint_as_float(dv[4 * k + 2 * i2]),
-                                                                           __uint_as_float(dv[4 * k + 2 * i2 + 1]));
-                                acc[4 * i + k] = ptx::fma_f32x2(ptx::mul_f32x2(xd2, w2[k]), dd, acc[4 * i + k]);
+                            for (int e = 0; e < 2; ++e) {
+                                const int n = n0 + c0 + 8 * k + tc2 + e;
+                                if (mrow < M && n < N)
+                                    dots[((long long)mrow * N + n) * nb + bi] =
+                                        __float2int_rn(__uint_as_float(dv[4 * k + 2 * i + e]));
                             }
-                            if (FMT == FMT_Q4_K) {
-                                const float nxs = sc[BM + rloc0 + 8 * i];
-                                const unsigned long long nxs2 = ptx::f2_bits(nxs, nxs);
+                    }
+                }
+            } else {
 #pragma unroll
-                                for (int k = 0; k < 4; ++k) acc[4 * i + k] = ptx::fma_f32x2(nxs2, wm2[k], acc[4 * i + k]);
-                            }
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t dv[16], sv[16];
+                    ptx::tmem_ld16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16), dv);
+                    ptx::tmem_ld16x256b_x4(taddr + BN + ((uint32_t)(16 * hh) << 16), sv);
+                    ptx::tmem_ld_wait(dv);
+                    ptx::tmem_ld_wait(sv);
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int a = 4 * (2 * hh + i2) + k;
+                            acc[a] = ptx::fma_f32x2(
+                                ptx::f2_bits(__uint_as_float(sv[4 * k + 2 * i2]), __uint_as_float(sv[4 * k + 2 * i2 + 1])),
+                                ptx::f2_bits(__uint_as_float(dv[4 * k + 2 * i2]), __uint_as_float(dv[4 * k + 2 * i2 + 1])),
+                                acc[a]);
                         }
-                    };
-                    // the two 16-lane halves one after the other (keeping both in flight
-                    // costs 16 more registers than the budget of 704 threads allows)
-                    uint32_t d0[16];
-                    ptx::tmem_ld16x256b_x4(taddr, d0);
-                    ptx::tmem_ld_wait(d0);
-                    rescale(d0, 0);
-                    ptx::tmem_ld16x256b_x4(taddr + (16u << 16), d0);
-                    ptx::tmem_ld_wait(d0);
-                    rescale(d0, 1);
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bar(BAR_D_EMPTY + gd));
-                ptx::mbar_arrive(bar(BAR_SC_EMPTY + gc));
-            }
+            if (lane == 0) ptx::mbar_arrive(bar(BAR_D_EMPTY + t));
         }
         if (!DOTS && !*abort) {
 #pragma unroll
