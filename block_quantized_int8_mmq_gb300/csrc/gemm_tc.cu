@@ -22,7 +22,7 @@
 // (K=16 MMA of the f16 sums s against the 6-bit mins) and S = 1 (x) (-dmin)
 // ("When Does a Kernel Win Surface?", sec. "Kept levers: Vulkan", affine identity).
 //
-// Warp roles (one 128 x 128 output tile per CTA, 704 threads):
+// Warp roles (one 128 x 128 output tile per CTA, 832 threads):
 //   warp 0     TMA producer: raw q8_1 rows (288 B per 256 values) and raw weight rows
 //              (Q8_0: 272 B, Q4_K: one 144 B super-block) for a 256-value k-tile, as
 //              2-D tensor copies into a 2-stage ring ("13 . r7-r8 raw-byte MMQ
@@ -30,11 +30,11 @@
 //              super-blocks, out-of-range rows zero-filled by the copy engine).
 //   warp 1     TMEM owner and MMA issuer: per item, D (two K=16 MMAs; one for a min
 //              item) and S (one K=16 MMA) into one of two TMEM slots, then commits.
-//   warps 2-5  converters: codes -> exact fp16 (sign-biased byte permute and one half2
+//   warps 2-9  converters: codes -> exact fp16 (sign-biased byte permute and one half2
 //              subtract; Q4_K: half2 fused multiply by sc_j) in the canonical K-major
 //              no-swizzle UMMA layout, bank-conflict-free; the f16 scale vectors into
 //              column 0 of the scale operands.
-//   warps 6-21 epilogue, 32 rows x 32 columns each: per item, 16x256b TMEM fragments of
+//   warps 10-25 epilogue, 32 rows x 32 columns each: per item, 16x256b TMEM fragments of
 //              D and S, acc += S * D with packed f32x2 FMA; at the end, 8-byte stores.
 // Every wait is bounded by wall time; on expiry the kernel records ERR_TIMEOUT, lets
 // the other roles fall out, drains its own copies and MMAs, frees TMEM and returns.
@@ -58,7 +58,7 @@ constexpr int KT_BLOCKS = 8;            // 32-blocks per staged k-tile (256 valu
 constexpr int RS = 2;                   // raw k-tile stages
 constexpr int FS = 3;                   // operand slots (one item each)
 constexpr int DS = 2;                   // TMEM slots (D and S of one item each)
-constexpr int CONV_WARPS = 4;
+constexpr int CONV_WARPS = 8;
 constexpr int EPI_WARPS = 16;
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // columns per epilogue warp (4 lane quarters)
 constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, WARP_EPI0 = WARP_CONV0 + CONV_WARPS;
@@ -71,7 +71,7 @@ constexpr int SLOT = 2 * OP_MAIN + 2 * OP_AUX;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bound on any one wait
 constexpr uint32_t WAIT_SLEEP_NS = 100000;           // longest sleep inside one poll
 
-static_assert(BM == 32 * CONV_WARPS && BN == 32 * CONV_WARPS, "one activation and one weight row per converter thread");
+static_assert(BM + BN == 32 * CONV_WARPS, "one scale row (activation or weight) per converter thread");
 static_assert(EPI_COLS == 32, "one 16x256b.x4 fragment covers 32 columns");
 
 __host__ __device__ constexpr int b_row(int fmt) { return fmt == FMT_Q8_0 ? KT_BLOCKS * Q8_0_BYTES : Q4_K_BYTES; }
@@ -92,7 +92,7 @@ struct Layout {
     static constexpr int rawB = rawA + RS * BM * A_ROW;
     static constexpr int slots = rawB + RS * BN * b_row(FMT);
     static constexpr int sctab = slots + FS * SLOT;  // Q4_K: per converter warp, (sc, -1024 sc) of its 64 rows x 8
-    static constexpr int bars = sctab + (FMT == FMT_Q4_K ? CONV_WARPS * 64 * 8 * 4 : 0);
+    static constexpr int bars = sctab + (FMT == FMT_Q4_K ? CONV_WARPS * 32 * 8 * 4 : 0);
     static constexpr int tmem_slot = bars + NBARS * 8;
     static constexpr int total = tmem_slot + 16;
     static constexpr int alloc = total + 1024;  // slack to align the base to 1 KiB
@@ -279,11 +279,14 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     } else if (warp < WARP_EPI0) {
         // ------------------------------------------------------------ converters
         const int cw = warp - WARP_CONV0;
-        const int ct = cw * 32 + lane;          // the activation row and the weight row of this thread
+        const int ct = cw * 32 + lane;          // < BM: activation row ct; else weight row ct - BM
+        const bool arow = ct < BM;
+        const int srow = arow ? ct : ct - BM;
         const int r8 = lane & 7, half = (lane >> 3) & 1, hw = lane >> 4;
-        // This warp converts the rows 8*(2i + cw/2) + r8, i = 0..7 (see the unit mapping
-        // below); its table of their sub-scales, [8*i + r8][sub-block], is private to it.
-        uint32_t* sct = reinterpret_cast<uint32_t*>(smem + L::sctab) + cw * 64 * 8;
+        constexpr int UNITS = 32 / CONV_WARPS;   // conversion units per warp and operand
+        // Unit i of this warp: 8-row group g = 4i + cw/2, pass p = cw%2.  Its table of the
+        // sub-scales of those 32 rows, [8*i + r8][sub-block], is private to the warp.
+        uint32_t* sct = reinterpret_cast<uint32_t*>(smem + L::sctab) + cw * 32 * 8;
         bool ok = true;
         int it = 0;
         for (int kt = 0; kt < nkt && ok; ++kt) {
@@ -292,47 +295,38 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             if (!ok) break;
             const uint8_t* rA = smem + L::rawA + s * BM * A_ROW;
             const uint8_t* rB = smem + L::rawB + s * BN * BROW;
-            uint4 whdr = make_uint4(0u, 0u, 0u, 0u);  // Q4_K: this thread's weight row super-block header
+            uint4 whdr = make_uint4(0u, 0u, 0u, 0u);  // Q4_K: super-block header of weight row srow
             if (FMT == FMT_Q4_K) {
-                whdr = *reinterpret_cast<const uint4*>(rB + ct * BROW);
+                if (!arow) whdr = *reinterpret_cast<const uint4*>(rB + srow * BROW);
                 if (FOLD) {
-                    // lane l decodes the sub-scales of table rows 2l and 2l+1
                     __syncwarp();  // this warp's reads of the previous k-tile's table are done
+                    const int row = 8 * (UNITS * (lane >> 3) + (cw >> 1)) + (lane & 7);  // table row = lane
+                    const uint4 h = *reinterpret_cast<const uint4*>(rB + row * BROW);
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tr = 2 * lane + e, row = 8 * (2 * (tr >> 3) + (cw >> 1)) + (tr & 7);
-                        const uint4 h = *reinterpret_cast<const uint4*>(rB + row * BROW);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            int s6, m6;
-                            q4_k_scale_min(h.y, h.z, h.w, j, s6, m6);
-                            sct[tr * 8 + j] = h2_bits(__halves2half2(__int2half_rn(s6), __int2half_rn(-1024 * s6)));
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        int s6, m6;
+                        q4_k_scale_min(h.y, h.z, h.w, j, s6, m6);
+                        sct[lane * 8 + j] = h2_bits(__halves2half2(__int2half_rn(s6), __int2half_rn(-1024 * s6)));
                     }
                     __syncwarp();
                 }
             }
             for (int ii = 0; ii < IPK && ok; ++ii, ++it) {
                 const int f = it % FS;
-                ok = warp_wait(bar(BAR_SLOT_EMPTY + f), ((it / FS) & 1) ^ 1, abort);
-                if (!ok) break;
-                uint8_t* oA = slot_ptr(f);
-                uint8_t* oB = oA + OP_MAIN;
-                uint16_t* aS = reinterpret_cast<uint16_t*>(oB + OP_MAIN);   // column 0 of the scale operands
-                uint16_t* bS = reinterpret_cast<uint16_t*>(oB + OP_MAIN + OP_AUX);
-                const int aux0 = core_off(ct, 0, 256) / 2;                   // element index of (row ct, k 0)
-                if (ii < KT_BLOCKS) {
-                    const int j = ii;
-                    // All raw loads first (the stores below go to the same shared array,
-                    // so the compiler would otherwise keep every load behind the previous
-                    // store).  Unit i = (8-row group g, pass p), lane = (hw, half, r8):
-                    // row 8g + r8 takes k-group kg = 2*(p ^ (r8 / 4)) + hw, code word
-                    // w = 2*kg + half.  Rows r8 and r8 + 4 (same banks: rows are 72 words
-                    // apart) read different halves of the block, so a load touches 32
-                    // different banks; each half-warp stores rows 0-3 of one k-group and
-                    // rows 4-7 of another, two 64-byte runs in opposite bank halves.
-                    constexpr int UNITS = 32 / CONV_WARPS;
-                    uint32_t xa[UNITS], wv[UNITS], scv[UNITS];
+                const bool block_item = ii < KT_BLOCKS;
+                const int j = ii;
+                // Raw loads first, then the slot wait, then the stores: the wait's latency
+                // overlaps the loads, and no load sits behind a store to the same array.
+                // Unit i = (8-row group g, pass p), lane = (hw, half, r8): row 8g + r8
+                // takes k-group kg = 2*(p ^ (r8 / 4)) + hw, code word w = 2*kg + half.  Rows
+                // r8 and r8 + 4 (same banks: rows are 72 words apart) read different halves
+                // of the block, so a load touches 32 different banks; each half-warp stores
+                // rows 0-3 of one k-group and rows 4-7 of another, two 64-byte runs in
+                // opposite bank halves.
+                uint32_t xa[UNITS], wv[UNITS], scv[UNITS];
+                uint16_t scol = 0;        // column-0 value of this thread's scale-operand row
+                uint32_t mrow[4];         // min item: this thread's A or B row, k = 0..7
+                if (block_item) {
 #pragma unroll
                     for (int i = 0; i < UNITS; ++i) {
                         const int u = i * CONV_WARPS + cw;
@@ -353,11 +347,37 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                             if (FOLD) scv[i] = sct[(i * 8 + r8) * 8 + j];  // table row 8i + r8 is row 8g + r8
                         }
                     }
-                    // column 0 of the scale operands: xd of row ct, w of row ct
-                    const uint16_t xdh = *reinterpret_cast<const uint16_t*>(rA + ct * A_ROW + j * Q8_1_BYTES);
-                    const uint16_t wdh = FMT == FMT_Q8_0
-                                             ? *reinterpret_cast<const uint16_t*>(rB + ct * BROW + j * Q8_0_BYTES)
-                                             : (uint16_t)(whdr.x & 0xffffu);
+                    if (arow)
+                        scol = *reinterpret_cast<const uint16_t*>(rA + srow * A_ROW + j * Q8_1_BYTES);  // xd
+                    else if (FMT == FMT_Q8_0)
+                        scol = *reinterpret_cast<const uint16_t*>(rB + srow * BROW + j * Q8_0_BYTES);   // wd
+                    else
+                        scol = (uint16_t)(whdr.x & 0xffffu);                                            // d
+                } else {
+                    // Q4_K min item: A row m = (s of the 8 blocks, 0 x 8), B row n = (m_0..m_7,
+                    // 0 x 8); scale operands: A = 1, B = -dmin
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        if (arow) {
+                            const uint32_t s0 = *reinterpret_cast<const uint32_t*>(rA + srow * A_ROW + (2 * jj) * Q8_1_BYTES);
+                            const uint32_t s1 =
+                                *reinterpret_cast<const uint32_t*>(rA + srow * A_ROW + (2 * jj + 1) * Q8_1_BYTES);
+                            mrow[jj] = (s0 >> 16) | (s1 & 0xffff0000u);
+                        } else {
+                            int sc0, mn0, sc1, mn1;
+                            q4_k_scale_min(whdr.y, whdr.z, whdr.w, 2 * jj, sc0, mn0);
+                            q4_k_scale_min(whdr.y, whdr.z, whdr.w, 2 * jj + 1, sc1, mn1);
+                            mrow[jj] = h2_bits(__halves2half2(__int2half_rn(mn0), __int2half_rn(mn1)));
+                        }
+                    }
+                    scol = arow ? (uint16_t)0x3C00u : (uint16_t)((whdr.x >> 16) ^ 0x8000u);  // 1.0 / -dmin
+                }
+                ok = warp_wait(bar(BAR_SLOT_EMPTY + f), ((it / FS) & 1) ^ 1, abort);
+                if (!ok) break;
+                uint8_t* oA = slot_ptr(f);
+                uint8_t* oB = oA + OP_MAIN;
+                uint16_t* aux = reinterpret_cast<uint16_t*>(oB + OP_MAIN + (arow ? 0 : OP_AUX));
+                if (block_item) {
 #pragma unroll
                     for (int i = 0; i < UNITS; ++i) {
                         const int u = i * CONV_WARPS + cw;
@@ -373,29 +393,12 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                             *reinterpret_cast<uint2*>(oB + dst) =
                                 u4x4_scaled_f16x4(wv[i], __float2half2_rn(1.f), __float2half2_rn(-1024.f));
                     }
-                    aS[aux0] = xdh;
-                    bS[aux0] = wdh;
                 } else {
-                    // Q4_K min item: A row m = (s of the 8 blocks, 0 x 8), B row n = (m_0..m_7,
-                    // 0 x 8); scale operands: A = 1, B = -dmin
-                    uint32_t sv[4], mv[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const uint32_t s0 = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + (2 * jj) * Q8_1_BYTES);
-                        const uint32_t s1 = *reinterpret_cast<const uint32_t*>(rA + ct * A_ROW + (2 * jj + 1) * Q8_1_BYTES);
-                        sv[jj] = (s0 >> 16) | (s1 & 0xffff0000u);
-                        int sc0, mn0, sc1, mn1;
-                        q4_k_scale_min(whdr.y, whdr.z, whdr.w, 2 * jj, sc0, mn0);
-                        q4_k_scale_min(whdr.y, whdr.z, whdr.w, 2 * jj + 1, sc1, mn1);
-                        mv[jj] = h2_bits(__halves2half2(__int2half_rn(mn0), __int2half_rn(mn1)));
-                    }
-                    *reinterpret_cast<uint4*>(oA + core_off(ct, 0, 512)) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
-                    *reinterpret_cast<uint4*>(oA + core_off(ct, 1, 512)) = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(oB + core_off(ct, 0, 512)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
-                    *reinterpret_cast<uint4*>(oB + core_off(ct, 1, 512)) = make_uint4(0u, 0u, 0u, 0u);
-                    aS[aux0] = 0x3C00;                                     // 1.0
-                    bS[aux0] = (uint16_t)((whdr.x >> 16) ^ 0x8000u);       // -dmin
+                    uint8_t* o = arow ? oA : oB;
+                    *reinterpret_cast<uint4*>(o + core_off(srow, 0, 512)) = make_uint4(mrow[0], mrow[1], mrow[2], mrow[3]);
+                    *reinterpret_cast<uint4*>(o + core_off(srow, 1, 512)) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                aux[core_off(srow, 0, 256) / 2] = scol;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(BAR_SLOT_FULL + f));
