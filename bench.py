@@ -41,6 +41,9 @@ import synth  # noqa: E402
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 L2_BYTES = 129 * 1024 * 1024
+GRAPH_STEPS = 64          # steps per captured graph (rounded up to the operand copies)
+TARGET_TIMED_S = 2.0      # default timed region length (long enough for clock samples)
+E2E_STEPS = 1000          # end-to-end steps (host copies every step)
 
 WORKLOADS = {
     "c1": dict(index=1, label="q8_0 MMQ attention-proj M=512 N=3584 K=3584 (quantize + GEMM)"),
@@ -51,6 +54,10 @@ WORKLOADS = {
 
 
 # ---------------------------------------------------------------------------- helpers
+
+PATH_NAMES = {1: "warp-level", 2: "tcgen05, codes converted in shared memory",
+              3: "tcgen05, codes expanded once per call"}
+
 
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
@@ -70,9 +77,21 @@ def load_peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def auto_steps(step, warmup, stream, torch):
+    """Steps for about TARGET_TIMED_S of device time, from a short eager estimate."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(warmup):
+        step(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) / 1e3 / warmup
+    return int(min(200000, max(50, TARGET_TIMED_S / max(per, 1e-7))))
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "ptx.cuh", "common.cuh", "quantize.cu", "gemm_small.cu"):
+    for f in ("gemm_tc.cu", "gemm_expand.cu", "umma.cuh", "ptx.cuh", "common.cuh", "quantize.cu", "gemm_small.cu"):
         with open(os.path.join(ROOT, "block_quantized_int8_mmq_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -160,7 +179,8 @@ def run_reference(args):
     if wl.get("quant_only"):
         xs = x
     times = []
-    for i in range(args.warmup + args.steps):
+    ref_steps = args.steps if args.steps > 0 else 10
+    for i in range(args.warmup + ref_steps):
         t0 = time.perf_counter()
         xq = oracle.quantize_q8_1(xs)
         if not wl.get("quant_only"):
@@ -179,7 +199,7 @@ def run_reference(args):
         metric = "MMQ int8 TOPS (2*M*N*K per step: quantize + GEMM)"
     return {
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 0,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "steps": ref_steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
         "scaling": "none", "vs_baseline": None, "dtype": "int64 dots, f64 scales", "data": "synthetic",
         "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt, "sampled_rows": rows},
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
@@ -241,17 +261,11 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     gemm = mmq.mmq_gemm_q8_0 if fmt == "q8_0" else mmq.mmq_gemm_q4_k
 
-    def step(i, evs=None):
+    def step(i, stream=stream):
         j = i % copies
-        if evs is not None:
-            evs[0].record(stream)
         mmq.mmq_quantize_q8_1(xs[j], xq, stream)
-        if evs is not None:
-            evs[1].record(stream)
         if not quant_only:
             gemm(xq, ws[j], M, N, K, out, stream)
-            if evs is not None:
-                evs[2].record(stream)
 
     for i in range(args.warmup):
         step(i)
@@ -275,24 +289,55 @@ def run_ours(args, rank, world, local):
     barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
     visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip().isdigit()]
     clocks = ClockSampler(int(visible[local]) if local < len(visible) else local)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    # The K timed steps run as CUDA-graph replays (a step is 2 to 4 launches of tens of
+    # microseconds: launched one by one from Python the host, not the GPU, would set the
+    # pace).  One graph holds G steps, G a multiple of the operand copies so consecutive
+    # steps never reuse a copy; a second graph holds the K % G remaining steps.  The
+    # library's profiler records an event pair around every launch inside the graphs,
+    # so each kernel's duration is read from the last replay of the timed region.
+    steps = args.steps if args.steps > 0 else auto_steps(step, args.warmup, stream, torch)
+    G = min(steps, copies * max(1, -(-GRAPH_STEPS // copies)))
+    reps, tail = divmod(steps, G)
+    cap = torch.cuda.Stream(dev)
+    mmq.mmq_profile_read(reset=True)
+    prev_prof = mmq.mmq_profile_enable(True)
+    graphs = []
+    for count in ([G] if reps else []) + ([tail] if tail else []):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(count):
+                step(i, stream=cap)
+        graphs.append((g, count))
+    mmq.mmq_profile_enable(prev_prof)
+    for g, _ in graphs:  # upload and first run, untimed (the profile is read only after
+        g.replay()        # the timed region: captured launches are counted at one read)
+    torch.cuda.synchronize(dev)
+    out.fill_(float("nan"))
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     t_start.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i, evs[i])
+    for _ in range(reps):
+        graphs[0][0].replay()
+    if tail:
+        graphs[-1][0].replay()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
-    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    g_ms = [e[1].elapsed_time(e[2]) for e in evs] if not quant_only else []
+    prof = mmq.mmq_profile_read(reset=True)  # the last replay of each graph
     if not quant_only:
         assert not torch.isnan(out).any().item(), "timed steps did not write the output"
     assert mmq.mmq_get_device_error(stream) == 0
+    launches_per_step = sum(n for n, _ in prof.values()) / sum(c for _, c in graphs)
+    kernels = {k: {"launches_per_step": n / sum(c for _, c in graphs), "avg_ms": t / n} for k, (n, t) in prof.items()}
+    step_kernel_ms = sum(t for _, t in prof.values()) / sum(c for _, c in graphs)
+    for k, (n, t) in prof.items():
+        kernels[k]["share"] = (t / sum(c for _, c in graphs)) / step_kernel_ms
 
     ms_max = ms
     if world > 1:
@@ -304,29 +349,30 @@ def run_ours(args, rank, world, local):
     peaks = load_peaks()
     if quant_only:
         qbytes = x.nbytes + xq_bytes
-        value = qbytes * args.steps * world / (ms_max / 1e3) / 1e9
+        value = qbytes * steps * world / (ms_max / 1e3) / 1e9
         unit = "GB/s"
         metric = "q8_1 quantize GB/s (algorithmic bytes: 4 B in + 1.125 B out per value)"
-        q_avg = sum(q_ms) / len(q_ms)
-        achieved = qbytes / (q_avg / 1e3) / 1e9
+        kname = "k_quantize_q8_1"
+        achieved = qbytes / (kernels[kname]["avg_ms"] / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for("k_quantize_q8_1", args.workload),
-                "kernel": "k_quantize_q8_1", "peak_source": peaks["source"] + " hbm_gbs"}
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload),
+                "kernel": kname, "peak_source": peaks["source"] + " hbm_gbs"}
     else:
-        value = ops * args.steps * world / (ms_max / 1e3) / 1e12
+        value = ops * steps * world / (ms_max / 1e3) / 1e12
         unit = "TOPS"
         metric = "MMQ int8 TOPS (2*M*N*K per step: quantize + GEMM)"
-        g_avg = sum(g_ms) / len(g_ms)
-        achieved = ops / (g_avg / 1e3) / 1e12
-        kname = "k_mmq_tc" if path == mmq.PATH_TC else "k_mmq_small"
-        if path == mmq.PATH_TC:
+        gk = {k: v for k, v in kernels.items() if k.startswith("k_mmq")}
+        kname = max(gk, key=lambda k: gk[k]["avg_ms"] * gk[k]["launches_per_step"])
+        avg = gk[kname]["avg_ms"]
+        if kname in ("k_mmq_tc", "k_mmq_tcx"):
             peak = peaks["bf16_tflops"]
+            achieved = ops / (avg / 1e3) / 1e12
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic_for(kname, args.workload), "kernel": kname,
                     "peak_source": f"{peaks['source']} bf16 burst (f16 tensor rate = bf16 rate)"}
         else:
             wbytes = w.nbytes + xq_bytes + M * N * 4
-            gbs = wbytes / (g_avg / 1e3) / 1e9
+            gbs = wbytes / (avg / 1e3) / 1e9
             roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload), "kernel": kname,
                     "peak_source": peaks["source"] + " hbm_gbs"}
@@ -343,31 +389,33 @@ def run_ours(args, rank, world, local):
             oh.copy_(out, non_blocking=True)
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_steps = min(steps, E2E_STEPS)
         a.record(stream)
-        for i in range(args.steps):
+        for i in range(e_steps):
             xd.copy_(xh, non_blocking=True)
             mmq.mmq_linear(xd, ws[i % copies], fmt, N, xq=xq, out=out, stream=stream)
             oh.copy_(out, non_blocking=True)
         b.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = a.elapsed_time(b)
-        e2e = {"value": ops * args.steps / (e_ms / 1e3) / 1e12, "unit": "TOPS",
+        e2e = {"value": ops * e_steps / (e_ms / 1e3) / 1e12, "unit": "TOPS", "steps": e_steps,
                "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": M * N * 4}
 
     line = {
-        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 codes (exact on f16 tensor cores), f32 scales and output",
         "data": "synthetic (seeded; 7B GQA projection shapes)",
         "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"rotating {copies} operand copies ({copies * set_bytes / 2**20:.0f} MiB > 3x L2)"},
+                   "l2": f"rotating {copies} operand copies ({copies * set_bytes / 2**20:.0f} MiB > 3x L2)",
+                   "timing": f"CUDA graphs: {reps} replays of {G} steps" + (f" + {tail} steps" if tail else "")},
         "roofline": roof,
-        "kernel_ms": {"quantize": sum(q_ms) / len(q_ms), "gemm": (sum(g_ms) / len(g_ms)) if g_ms else None},
-        "path": {mmq.PATH_TC: "tcgen05", mmq.PATH_SMALL: "warp-level"}.get(path, "quantize"),
+        "kernels": kernels,
+        "path": PATH_NAMES.get(path, "quantize"),
         "clocks": clk,
-        "gpu_launches": args.steps * (1 if quant_only else 2),
+        "gpu_launches": int(round(launches_per_step * steps)),
     }
     if e2e:
         line["e2e"] = e2e
@@ -416,7 +464,7 @@ def run_layer(args):
     torch.cuda.synchronize(dev)
     assert mmq.mmq_get_device_error(stream) == 0
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(1, args.steps // 10)
+    reps = max(1, (args.steps if args.steps > 0 else 30) // 10)
     clocks = ClockSampler(0)
     clocks.start()
     a.record(stream)
@@ -488,7 +536,7 @@ def run_sweep(args):
         gbs = abytes / (ms / 1e3) / 1e9
         tops = ops / (ms / 1e3) / 1e12
         lines.append({"M": M, "N": N, "K": K, "ms": ms, "tops": tops, "gbs": gbs, "tok_per_s": M / (ms / 1e3),
-                      "path": "tcgen05" if path == mmq.PATH_TC else "warp-level",
+                      "path": PATH_NAMES.get(path, "?"),
                       "frac_hbm": gbs / peaks["hbm_gbs"], "frac_tensor": tops / peaks["bf16_tflops"],
                       "algorithmic_bytes": abytes})
         del ws
@@ -501,7 +549,7 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s of device time)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["layer", "sweep"], default="c1")

@@ -16,13 +16,18 @@ LIB_PATH = os.path.join(_HERE, "libmmq.so")
 QK, QK_K = 32, 256
 Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES = 36, 34, 144
 FMT = {"q8_0": 0, "q4_k": 1}
-PATH_AUTO, PATH_SMALL, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_SMALL, PATH_TC, PATH_EXPAND = 0, 1, 2, 3
 
 EXPORTED = (
     "mmq_status_string", "mmq_q8_1_bytes", "mmq_weight_row_bytes", "mmq_quantize_q8_1",
     "mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k",
-    "mmq_set_path", "mmq_last_path", "mmq_get_device_error",
+    "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
 )
+
+
+class KernelTime(ctypes.Structure):
+    """mmq_kernel_time: per-kernel launch count and total device time."""
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
 
 class MMQError(RuntimeError):
@@ -47,6 +52,8 @@ def _load():
         getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P]
     L.mmq_set_path.argtypes = [I]
     L.mmq_get_device_error.argtypes = [P]
+    L.mmq_profile_enable.argtypes = [I]
+    L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
     return L
 
 
@@ -73,6 +80,23 @@ def _check(fn, st):
 
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
+
+
+def mmq_profile_enable(on: bool) -> bool:
+    """Turn per-kernel event timing on or off; returns the previous state."""
+    return bool(_lib.mmq_profile_enable(1 if on else 0))
+
+
+def mmq_profile_read(reset: bool = False) -> dict:
+    """{kernel name: (launches, total device ms)} of the launches timed so far."""
+    n = _lib.mmq_profile_read(None, 0, 0)
+    if n < 0:
+        raise MMQError("mmq_profile_read", n)
+    buf = (KernelTime * max(n, 1))()
+    n = _lib.mmq_profile_read(buf, n, 1 if reset else 0)
+    if n < 0:
+        raise MMQError("mmq_profile_read", n)
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n)}
 
 
 def mmq_status_string(status: int) -> str:

@@ -41,6 +41,7 @@ int current_path() {
         const char* env = getenv("MMQ_FORCE_PATH");
         if (env && strcmp(env, "small") == 0) p = MMQ_PATH_SMALL;
         if (env && strcmp(env, "tc") == 0) p = MMQ_PATH_TC;
+        if (env && strcmp(env, "expand") == 0) p = MMQ_PATH_EXPAND;
         int expected = -1;
         g_path.compare_exchange_strong(expected, p);
         p = g_path.load();
@@ -83,17 +84,23 @@ int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t
         return MMQ_ERR_ALIGN;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int path = current_path();
-    // The tensor-core path stages 256-value k-tiles; other K go to the warp-level path.
-    const bool small =
-        path == MMQ_PATH_SMALL || (path == MMQ_PATH_AUTO && (M <= 8 || K % QK_K != 0 || !tc_available()));
-    if (small) {
-        st = small_launch(fmt, xq, wq, M, N, K, out, dots, s);
-        if (st == MMQ_OK) t_last_path = MMQ_PATH_SMALL;
-    } else {
-        st = tc_launch(fmt, xq, wq, M, N, K, out, dots, s);
-        if (st == MMQ_OK) t_last_path = MMQ_PATH_TC;
+    int path = current_path();
+    if (path == MMQ_PATH_AUTO) {
+        // The tensor-core paths stage 256-value groups; other K go to the warp-level path.
+        if (M <= 8 || K % QK_K != 0 || !tc_available())
+            path = MMQ_PATH_SMALL;
+        else if (M >= MMQ_EXPAND_MIN_M)
+            path = MMQ_PATH_EXPAND;
+        else
+            path = MMQ_PATH_TC;
     }
+    if (path == MMQ_PATH_SMALL)
+        st = small_launch(fmt, xq, wq, M, N, K, out, dots, s);
+    else if (path == MMQ_PATH_TC)
+        st = tc_launch(fmt, xq, wq, M, N, K, out, dots, s);
+    else
+        st = tcx_launch(fmt, xq, wq, M, N, K, out, dots, s);
+    if (st == MMQ_OK) t_last_path = path;
     return st;
 }
 
@@ -116,6 +123,7 @@ const char* mmq_status_string(int status) {
         case MMQ_ERR_TIMEOUT: return "MMQ_ERR_TIMEOUT";
         case MMQ_ERR_CUDA: return "MMQ_ERR_CUDA";
         case MMQ_ERR_ARG: return "MMQ_ERR_ARG";
+        case MMQ_ERR_NOMEM: return "MMQ_ERR_NOMEM";
         default: return "MMQ_ERR_UNKNOWN";
     }
 }
@@ -166,7 +174,8 @@ int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t
 }
 
 int mmq_set_path(int path) {
-    if (path != MMQ_PATH_AUTO && path != MMQ_PATH_SMALL && path != MMQ_PATH_TC) return MMQ_ERR_ARG;
+    if (path != MMQ_PATH_AUTO && path != MMQ_PATH_SMALL && path != MMQ_PATH_TC && path != MMQ_PATH_EXPAND)
+        return MMQ_ERR_ARG;
     const int prev = current_path();
     g_path.store(path);
     return prev;
@@ -180,7 +189,7 @@ int mmq_get_device_error(void* stream) {
         fprintf(stderr, "libmmq: mmq_get_device_error: %s\n", cudaGetErrorString(e));
         return MMQ_ERR_CUDA;
     }
-    const unsigned bits = tc_take_error() | small_take_error();
+    const unsigned bits = tc_take_error() | tcx_take_error() | small_take_error();
     return (bits & ERR_TIMEOUT) ? MMQ_ERR_TIMEOUT : MMQ_OK;
 }
 

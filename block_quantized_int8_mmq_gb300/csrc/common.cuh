@@ -52,8 +52,27 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
                  int32_t* dots, cudaStream_t s);
 int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
               int32_t* dots, cudaStream_t s);
+int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+               int32_t* dots, cudaStream_t s);
 unsigned tc_take_error();
+unsigned tcx_take_error();
 unsigned small_take_error();
 void report(const char* fn, int status, const char* detail);
 int launch_status(const char* fn);
+
+// Per-kernel timing (profile.cu): a ProfScope around a launch brackets it with two
+// events on `s` while profiling is enabled.
+bool profiling();
+int prof_begin(const char* name, cudaStream_t s);
+void prof_end(int slot, cudaStream_t s);
+struct ProfScope {
+    int slot = -1;
+    cudaStream_t s;
+    ProfScope(const char* name, cudaStream_t st) : s(st) {
+        if (profiling()) slot = prof_begin(name, st);
+    }
+    ~ProfScope() {
+        if (slot >= 0) prof_end(slot, s);
+    }
+};
 }  // namespace mmq

@@ -1,0 +1,636 @@
+// Tensor-core MMQ over codes expanded once per call (sm_103a).
+//
+// Every int8 code, and every Q4_K nibble times its 6-bit sub-scale, is an exact fp16
+// value, so the fp16 x fp16 -> f32 MMA over one 32-block computes the integer block dot
+// exactly ("When the Product Won't Collapse", sec. "The obstruction": one integer dot
+// per constant-scale block).  Because the scale changes at every block, the
+// accumulator is read out of TMEM after every block and rescaled in registers (same
+// page, sec. "The viable route is per-backend anyway"): out += xd[m,b] * w[n,b] * D_b.
+//
+// Measured on this GPU, one thread issues a kind::f16 MMA about every 128 cycles when
+// consecutive MMAs switch accumulators, while the tensor core finishes a 128 x 128 x 16
+// MMA in 64: so the 128 x 128 tiles here have two MMA-issuing warps (even and odd
+// blocks) and four 128-column TMEM slots, and the per-block readout of D, the
+// pipeline's critical resource, has four blocks of slack.  The codes reach shared
+// memory already in the MMA's layout: two streaming kernels convert every code once
+// per call into scratch,
+//
+//   k_expand_acts     q8_1 rows -> per (128-row tile, 32-block) an 8 KiB chunk of fp16
+//                     codes in the K-major no-swizzle core-matrix order; per (tile,
+//                     256-value group) the f32 row scales xd[c][row] of its blocks (row
+//                     c = 8: 1.0, the Q4_K min item) and, for Q4_K, the K = 16 operand
+//                     AM (column c = the f16 block sum s of block c);
+//   k_expand_weights  Q8_0 / Q4_K rows -> per (128-row tile, 32-block) the same chunks
+//                     (Q4_K: q * sc_j); per (tile, group) the f32 column scales w[c][n]
+//                     (Q8_0: wd; Q4_K: d, and -dmin for c = 8) and, for Q4_K, the K = 16
+//                     operand BMIN (column j = m_j) ("When Does a Kernel Win Surface?",
+//                     sec. "Kept levers: Vulkan", the Q4_K affine identity);
+//
+// and k_mmq_tcx copies whole chunks with 1-D bulk copies, issues the MMAs from two
+// threads and rescales in 16 epilogue warps.  The scale product s = xd * w is exact in
+// f32 (two f16 values), so each block adds one rounding: acc = fma(s, D, acc).  Rows
+// past M or N are zero in the scratch: they add nothing and are never stored.
+//
+// The price is scratch traffic: 2 bytes written and read back per code.  It pays when
+// M is large enough that converting each tile in shared memory, once per output tile
+// that uses it, costs more.
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace mmq {
+namespace {
+
+using namespace umma;
+
+__device__ unsigned int g_tcx_error;
+
+constexpr int BM = 128;                  // activation rows per tile (TMEM lanes)
+constexpr int BN = 128;                  // weight rows per tile (MMA N)
+constexpr int GB = 8;                    // 32-blocks per group (256 values)
+constexpr int CHUNK = BM * QK * 2;       // fp16 codes of one block, 128 rows: 8 KiB
+constexpr int TILE16 = BM * 16 * 2;      // a K = 16 operand, 128 rows: 4 KiB
+constexpr int NSTAGE = 8;                // blocks in flight (one block per stage)
+constexpr int STAGE = 2 * CHUNK;         // activation chunk, then weight chunk
+constexpr int GR = 2;                    // group-data slots
+constexpr int NMMA = 2;                  // MMA-issuing warps; warp e issues items e, e + 2, ...
+constexpr int DS = NMMA;                 // TMEM slots: slot e (D and S of one item) belongs to issuer e
+constexpr int OH = 4;                    // one-hot scale operand slots
+constexpr int EPI_WARPS = 16;            // warps 0..15: epilogue
+constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // 32 columns per epilogue warp
+constexpr int WARP_LOAD = EPI_WARPS, WARP_MMA0 = EPI_WARPS + 1, WARP_ONEHOT = WARP_MMA0 + NMMA;
+constexpr int THREADS = (WARP_ONEHOT + 1) * 32;  // 640
+constexpr int TMEM_COLS = DS * 2 * BN;           // 512
+constexpr int EXP_THREADS = 256;
+static_assert(TILE16 / 16 == EXP_THREADS, "one K = 16 tile piece per expansion thread");
+static_assert(OH % NMMA == 0, "each issuer sees its own one-hot slots");
+
+// Group data (scratch and shared memory).  Activation side: AS, the K = 16 operand whose
+// column c holds xd of block c (column 8: 1.0, the Q4_K min item), and for Q4_K AM
+// (column c = the f16 block sum s of block c).  Weight side: for Q4_K BMIN (column j =
+// m_j), then WS, the f16 column scales [item][128] (Q8_0: wd; Q4_K: d, and -dmin for
+// the min item).
+__host__ __device__ constexpr int xr(int fmt) { return fmt == FMT_Q4_K ? GB + 1 : GB; }
+__host__ __device__ constexpr int ga_bytes(int fmt) { return fmt == FMT_Q4_K ? 2 * TILE16 : TILE16; }
+__host__ __device__ constexpr int gw_bytes(int fmt) { return (fmt == FMT_Q4_K ? TILE16 : 0) + xr(fmt) * BN * 2; }
+__host__ __device__ constexpr int am_off(int fmt) { return TILE16; }
+__host__ __device__ constexpr int bmin_off(int fmt) { return ga_bytes(fmt); }
+__host__ __device__ constexpr int ws_off(int fmt) { return ga_bytes(fmt) + (fmt == FMT_Q4_K ? TILE16 : 0); }
+
+// u16 index of (row r, column c) in a K = 16 K-major no-swizzle tile (8-row groups 256 B apart)
+__device__ __forceinline__ int tile16_idx(int r, int c) {
+    return ((r >> 3) * 256 + (c >> 3) * 128 + (r & 7) * 16) / 2 + (c & 7);
+}
+
+__device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
+    return make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16), v[4] | ((uint32_t)v[5] << 16),
+                      v[6] | ((uint32_t)v[7] << 16));
+}
+
+// ---------------------------------------------------------------- expansion kernels
+// Piece p (0..511) of a chunk is the 16 bytes of row 8*(p/32) + p%8, values
+// 8*((p/8)%4) .. +7 of the block: offset p*16 is that row's core-matrix row, so the
+// pieces are written in order (coalesced).
+
+// One CTA per (128-row tile, 256-value group) of the q8_1 activations.
+template <int FMT>
+__global__ void __launch_bounds__(EXP_THREADS)
+k_expand_acts(const uint8_t* __restrict__ xq, int M, int nb, uint8_t* __restrict__ xa, uint8_t* __restrict__ ga) {
+    constexpr int ROW = GB * Q8_1_BYTES;  // 288 bytes of one row per group
+    constexpr int V = ROW / 16;           // 18
+    constexpr int SROW = 304;             // 76 words: the 64-bit reads below are conflict-free
+    __shared__ __align__(16) uint8_t sm[BM * SROW];
+    const int mt = blockIdx.x, g = blockIdx.y, ng = nb / GB;
+    const int m0 = mt * BM;
+    const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
+    for (int i = threadIdx.x; i < BM * V; i += EXP_THREADS) {
+        const int r = i / V, c = i % V;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (m0 + r < M) v = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)(m0 + r) * rowbytes + (size_t)g * ROW) + c);
+        *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
+    }
+    __syncthreads();
+    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * CHUNK;
+    for (int i = threadIdx.x; i < GB * (CHUNK / 16); i += EXP_THREADS) {
+        const int j = i / (CHUNK / 16), p = i % (CHUNK / 16);
+        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;
+        const uint8_t* src = sm + r * SROW + j * Q8_1_BYTES + 4 + 8 * kc;
+        const uint2 lo = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src));
+        const uint2 hi = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src + 4));
+        *reinterpret_cast<uint4*>(dst + (size_t)j * CHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    // AS [, AM]: thread t writes piece t = (row 8*(t/16) + t%8, columns 8*((t/8)%2) .. +7)
+    uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT);
+    const int t = threadIdx.x;
+    const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
+    uint16_t as[8], am[8];
+    if (kg == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {  // columns 0..7: the eight blocks of the group
+            const uint8_t* blk = sm + r * SROW + e * Q8_1_BYTES;
+            as[e] = *reinterpret_cast<const uint16_t*>(blk);
+            am[e] = *reinterpret_cast<const uint16_t*>(blk + 2);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {  // column 8: 1.0, the Q4_K min item's row scale
+            as[e] = (e == 0 && FMT == FMT_Q4_K) ? (uint16_t)0x3C00 : (uint16_t)0;
+            am[e] = 0;
+        }
+    }
+    *reinterpret_cast<uint4*>(gdst + t * 16) = pack8(as);
+    if (FMT == FMT_Q4_K) *reinterpret_cast<uint4*>(gdst + am_off(FMT) + t * 16) = pack8(am);
+}
+
+// One CTA per (128-row tile, 256-value group) of the weights.  FOLD: Q4_K codes are
+// q * sc_j (the contraction); without it, the raw nibbles (the block-dot test hook).
+template <int FMT, bool FOLD>
+__global__ void __launch_bounds__(EXP_THREADS)
+k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
+    constexpr int ROW = FMT == FMT_Q8_0 ? GB * Q8_0_BYTES : Q4_K_BYTES;  // 272 / 144 bytes per row per group
+    constexpr int V = ROW / 16;                                          // 17 / 9
+    constexpr int VP = V + 1;                                            // + one zero piece (Q8_0 reads 4 B past)
+    constexpr int SROW = FMT == FMT_Q8_0 ? 304 : 176;
+    static_assert(SROW >= VP * 16, "row pad");
+    __shared__ __align__(16) uint8_t sm[BN * SROW];
+    const int nt = blockIdx.x, g = blockIdx.y, ng = nb / GB;
+    const int n0 = nt * BN;
+    const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * Q4_K_BYTES;
+    for (int i = threadIdx.x; i < BN * VP; i += EXP_THREADS) {
+        const int r = i / VP, c = i % VP;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (c < V && n0 + r < N)
+            v = __ldg(reinterpret_cast<const uint4*>(wq + (size_t)(n0 + r) * rowbytes + (size_t)g * ROW) + c);
+        *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
+    }
+    __syncthreads();
+    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * CHUNK;
+    for (int i = threadIdx.x; i < GB * (CHUNK / 16); i += EXP_THREADS) {
+        const int j = i / (CHUNK / 16), p = i % (CHUNK / 16);
+        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;
+        const uint8_t* row = sm + r * SROW;
+        uint2 lo, hi;
+        if (FMT == FMT_Q8_0) {
+            // codes of block j start at byte 34j + 2: 2-byte aligned only
+            const int off = j * Q8_0_BYTES + 2 + 8 * kc;
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(row + (off & ~3));
+            const int sh = (off & 3) * 8;
+            const uint32_t a0 = w[0], a1 = w[1], a2 = w[2];
+            lo = i8x4_to_f16x4(__funnelshift_r(a0, a1, sh));
+            hi = i8x4_to_f16x4(__funnelshift_r(a1, a2, sh));
+        } else {
+            // value 32j + k of the super-block: byte 16 + 32*(j/2) + k, low nibble for even j
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 16 + 32 * (j >> 1) + 8 * kc);
+            uint32_t a0 = w[0], a1 = w[1];
+            if (j & 1) {
+                a0 >>= 4;
+                a1 >>= 4;
+            }
+            a0 &= 0x0F0F0F0Fu;
+            a1 &= 0x0F0F0F0Fu;
+            int sc = 1, mn;
+            if (FOLD) {
+                const uint32_t* h = reinterpret_cast<const uint32_t*>(row);
+                q4_k_scale_min(h[1], h[2], h[3], j, sc, mn);
+            }
+            const __half2 sc2 = __half2half2(__int2half_rn(sc));
+            const __half2 nsc = __half2half2(__int2half_rn(-1024 * sc));
+            lo = u4x4_scaled_f16x4(a0, sc2, nsc);
+            hi = u4x4_scaled_f16x4(a1, sc2, nsc);
+        }
+        *reinterpret_cast<uint4*>(dst + (size_t)j * CHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT);
+    const int t = threadIdx.x;
+    // WS[c][r]: piece t = rows 8*(t%16) .. +7 of column c = t/16
+    if (t < xr(FMT) * BN / 8) {
+        const int c = t >> 4, r0 = (t & 15) * 8;
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint16_t* hdr = reinterpret_cast<const uint16_t*>(sm + (r0 + e) * SROW);
+            if (FMT == FMT_Q8_0)
+                v[e] = *reinterpret_cast<const uint16_t*>(sm + (r0 + e) * SROW + c * Q8_0_BYTES);  // wd
+            else
+                v[e] = c < GB ? hdr[0] : (uint16_t)(hdr[1] ^ 0x8000u);  // d, or -dmin
+        }
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + t * 16) = pack8(v);
+    }
+    if (FMT == FMT_Q4_K) {
+        // BMIN: piece t = (row 8*(t/16) + t%8, columns 8*((t/8)%2) .. +7), column j = m_j
+        const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
+        const uint32_t* h = reinterpret_cast<const uint32_t*>(sm + r * SROW);
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            int sc, mn;
+            q4_k_scale_min(h[1], h[2], h[3], e, sc, mn);
+            v[e] = kg == 0 ? __half_as_ushort(__int2half_rn(mn)) : (uint16_t)0;
+        }
+        *reinterpret_cast<uint4*>(gdst + t * 16) = pack8(v);
+    }
+}
+
+// ---------------------------------------------------------------- GEMM kernel
+constexpr int BAR_ST_FULL = 0, BAR_ST_EMPTY = BAR_ST_FULL + NSTAGE, BAR_G_FULL = BAR_ST_EMPTY + NSTAGE,
+              BAR_G_EMPTY = BAR_G_FULL + GR, BAR_OH_FULL = BAR_G_EMPTY + GR, BAR_OH_EMPTY = BAR_OH_FULL + OH,
+              BAR_D_FULL = BAR_OH_EMPTY + OH, BAR_D_EMPTY = BAR_D_FULL + DS, BAR_DRAIN = BAR_D_EMPTY + DS,
+              NBARS = BAR_DRAIN + NMMA;
+
+template <int FMT>
+struct XLayout {
+    static constexpr int stages = 0;
+    static constexpr int gslot = (ga_bytes(FMT) + gw_bytes(FMT) + 1023) & ~1023;
+    static constexpr int groups = stages + NSTAGE * STAGE;
+    static constexpr int onehot = groups + GR * gslot;
+    static constexpr int bars = onehot + OH * TILE16;
+    static constexpr int tmem_slot = bars + NBARS * 8;
+    static constexpr int total = tmem_slot + 16;
+    static constexpr int alloc = total + 1024;  // slack to align the base to 1 KiB
+    static_assert(alloc <= 227 * 1024, "shared memory");
+};
+
+// Warps 0..15 own 32 rows each (their TMEM lane quarter, warp % 4) and 32 columns of
+// the 128 x 128 tile; warp 16 is the bulk-copy producer; warps 17 and 18 issue the MMAs
+// of the even and odd items, each into its own TMEM slot (D at column 256e, S at 256e +
+// 128); warp 19 writes each item's one-hot scale operand.  The scale MMA multiplies AS
+// (dense: column k = xd of block k) by the one-hot operand (only column c nonzero, = the
+// item's column scales), so S = xd_c (x) w_c exactly.  Each epilogue warp reads D and S
+// in two 16-column halves and hands the slot back before its last FMAs.
+template <int FMT, bool DOTS>
+__global__ void __launch_bounds__(THREADS, 1)
+k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const uint8_t* __restrict__ xb,
+          const uint8_t* __restrict__ gw, int M, int N, int nb, float* __restrict__ out, int32_t* __restrict__ dots) {
+    using L = XLayout<FMT>;
+    constexpr bool MIN = FMT == FMT_Q4_K && !DOTS;  // a min item closes every group
+    constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
+    constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT);
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_abort;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x, nt = blockIdx.y;
+    const int m0 = mt * BM, n0 = nt * BN;
+    const int ng = nb / GB;
+    const int nitems = ng * IPG;
+    volatile int* abort = &s_abort;
+    unsigned* err = &g_tcx_error;
+    auto bar = [&](int i) -> uint32_t { return sbase + L::bars + 8 * i; };
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < NSTAGE; ++i) {
+            ptx::mbar_init(bar(BAR_ST_FULL + i), 1);
+            ptx::mbar_init(bar(BAR_ST_EMPTY + i), 1);
+        }
+        for (int i = 0; i < GR; ++i) {
+            ptx::mbar_init(bar(BAR_G_FULL + i), 1);
+            ptx::mbar_init(bar(BAR_G_EMPTY + i), DOTS ? NMMA : NMMA + 1);  // MMA warps' commits (+ one-hot writer)
+        }
+        for (int i = 0; i < OH; ++i) {
+            ptx::mbar_init(bar(BAR_OH_FULL + i), 1);
+            ptx::mbar_init(bar(BAR_OH_EMPTY + i), 1);
+        }
+        for (int i = 0; i < DS; ++i) {
+            ptx::mbar_init(bar(BAR_D_FULL + i), 1);
+            ptx::mbar_init(bar(BAR_D_EMPTY + i), EPI_WARPS);
+        }
+        for (int i = 0; i < NMMA; ++i) ptx::mbar_init(bar(BAR_DRAIN + i), 1);
+        ptx::fence_barrier_init();
+    }
+    // one-hot operands start at zero; each item sets its column and clears the previous one
+    for (int i = threadIdx.x; i < OH * TILE16 / 16; i += THREADS)
+        reinterpret_cast<uint4*>(smem + L::onehot)[i] = make_uint4(0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+    if (warp == WARP_MMA0) {
+        ptx::tmem_alloc(sbase + L::tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::tmem_slot);
+
+    if (warp == WARP_LOAD) {
+        // ------------------------------------------------------------ bulk-copy producer
+        if (lane == 0) {
+            int st_issued = 0, g_issued = 0;
+            bool ok = true;
+            for (int g = 0; g < ng && ok; ++g) {
+                if (!DOTS) {
+                    const int gs = g % GR;
+                    if (!wait_bar(bar(BAR_G_EMPTY + gs), ((g / GR) & 1) ^ 1, abort, err)) break;
+                    const uint32_t dst = sbase + L::groups + gs * L::gslot;
+                    ptx::mbar_arrive_expect_tx(bar(BAR_G_FULL + gs), GA + GW);
+                    ptx::bulk_load(dst, ga + ((size_t)mt * ng + g) * GA, GA, bar(BAR_G_FULL + gs));
+                    ptx::bulk_load(dst + GA, gw + ((size_t)nt * ng + g) * GW, GW, bar(BAR_G_FULL + gs));
+                    g_issued = g + 1;
+                }
+                for (int j = 0; j < GB; ++j) {
+                    const int k = g * GB + j, s = k % NSTAGE;
+                    if (!wait_bar(bar(BAR_ST_EMPTY + s), ((k / NSTAGE) & 1) ^ 1, abort, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sbase + L::stages + s * STAGE;
+                    ptx::mbar_arrive_expect_tx(bar(BAR_ST_FULL + s), STAGE);
+                    ptx::bulk_load(dst, xa + ((size_t)mt * nb + k) * CHUNK, CHUNK, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst + CHUNK, xb + ((size_t)nt * nb + k) * CHUNK, CHUNK, bar(BAR_ST_FULL + s));
+                    st_issued = k + 1;
+                }
+            }
+            // copies of the last stages and groups may still be in flight after an abort
+            for (int k = st_issued - NSTAGE < 0 ? 0 : st_issued - NSTAGE; k < st_issued; ++k)
+                drain_bar(bar(BAR_ST_FULL + k % NSTAGE), (k / NSTAGE) & 1, err);
+            for (int g = g_issued - GR < 0 ? 0 : g_issued - GR; g < g_issued; ++g)
+                drain_bar(bar(BAR_G_FULL + g % GR), (g / GR) & 1, err);
+        }
+    } else if (warp >= WARP_MMA0 && warp < WARP_MMA0 + NMMA) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two issuing threads keep the tensor core busy although each switches between
+        // the D and S accumulators of its slot at every item.
+        const int e = warp - WARP_MMA0;
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, BN);
+            const uint32_t d = tmem + (uint32_t)(e * 2 * BN), sd = d + BN;
+            for (int it = e, n = 0; it < nitems; it += NMMA, ++n) {
+                const int g = it / IPG, c = it % IPG, gs = g % GR, o = it % OH;
+                const bool block = c < GB;
+                const int k = g * GB + c, s = k % NSTAGE;  // block index = stage sequence number
+                const uint32_t gbase = sbase + L::groups + gs * L::gslot;
+                if (!DOTS && !wait_bar(bar(BAR_G_FULL + gs), (g / GR) & 1, abort, err)) break;
+                if (block && !wait_bar(bar(BAR_ST_FULL + s), (k / NSTAGE) & 1, abort, err)) break;
+                if (!wait_bar(bar(BAR_D_EMPTY + e), (n & 1) ^ 1, abort, err)) break;
+                if (!DOTS && !wait_bar(bar(BAR_OH_FULL + o), (it / OH) & 1, abort, err)) break;
+                ptx::tc_fence_after();
+                if (block) {
+                    const uint32_t a = sbase + L::stages + s * STAGE, b = a + CHUNK;
+                    ptx::umma_f16(d, sdesc(a, 512), sdesc(b, 512), idesc, 0u);
+                    ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + 256, 512), idesc, 1u);
+                    ptx::umma_commit(bar(BAR_ST_EMPTY + s));
+                } else {
+                    // min item: AM x BMIN^T = sum_j s_j * m_j
+                    ptx::umma_f16(d, sdesc(gbase + am_off(FMT), 256), sdesc(gbase + bmin_off(FMT), 256), idesc, 0u);
+                }
+                if (!DOTS) {
+                    ptx::umma_f16(sd, sdesc(gbase, 256), sdesc(sbase + L::onehot + o * TILE16, 256), idesc, 0u);
+                    ptx::umma_commit(bar(BAR_OH_EMPTY + o));
+                    // this warp's last item of the group releases the group data
+                    if (it + NMMA >= (g + 1) * IPG || it + NMMA >= nitems) ptx::umma_commit(bar(BAR_G_EMPTY + gs));
+                }
+                ptx::umma_commit(bar(BAR_D_FULL + e));
+            }
+            ptx::umma_commit(bar(BAR_DRAIN + e));  // arrives once every MMA this thread issued is done
+            drain_bar(bar(BAR_DRAIN + e), 0, err);
+        }
+        __syncwarp();
+    } else if (warp == WARP_ONEHOT) {
+        // ------------------------------------------------------------ one-hot scale operands
+        if (!DOTS) {
+            int it = 0;
+            bool ok = true;
+            for (int g = 0; g < ng && ok; ++g) {
+                const int gs = g % GR;
+                if (!warp_wait(bar(BAR_G_FULL + gs), (g / GR) & 1, abort, err)) break;
+                const uint16_t* ws = reinterpret_cast<const uint16_t*>(smem + L::groups + gs * L::gslot + ws_off(FMT));
+                for (int c = 0; c < IPG; ++c, ++it) {
+                    const int o = it % OH;
+                    if (!warp_wait(bar(BAR_OH_EMPTY + o), ((it / OH) & 1) ^ 1, abort, err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint16_t* tile = reinterpret_cast<uint16_t*>(smem + L::onehot + o * TILE16);
+                    const int old = it >= OH ? (it - OH) % IPG : c;  // column the slot's last item used
+#pragma unroll
+                    for (int rr = 0; rr < BN / 32; ++rr) {
+                        const int r = lane + 32 * rr;
+                        if (old != c) tile[tile16_idx(r, old)] = 0;
+                        tile[tile16_idx(r, c)] = ws[c * BN + r];
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(BAR_OH_FULL + o));
+                }
+                __syncwarp();
+                if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_G_EMPTY + gs));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3, cg = warp >> 2;
+        const int c0 = cg * EPI_COLS;
+        const int mrow = m0 + 32 * q + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+        unsigned long long acc[EPI_COLS / 2];
+#pragma unroll
+        for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = 0ull;
+        for (int it = 0; it < nitems; ++it) {
+            const int e = it % DS;
+            if (!warp_wait(bar(BAR_D_FULL + e), (it / DS) & 1, abort, err)) break;
+            ptx::tc_fence_after();
+            const uint32_t taddr = lane_base + (uint32_t)(e * 2 * BN);
+            if (DOTS) {
+                uint32_t dv[EPI_COLS];
+                ptx::tmem_ld_cols(taddr, dv);
+                ptx::tmem_ld_wait(dv);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BAR_D_EMPTY + e));
+                if (mrow < M) {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; ++j) {
+                        const int n = n0 + c0 + j;
+                        if (n < N) dots[((long long)mrow * N + n) * nb + it] = __float2int_rn(__uint_as_float(dv[j]));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t dv[16], sv[16];
+                    ptx::tmem_ld_cols(taddr + 16 * h, dv);
+                    ptx::tmem_ld_cols(taddr + BN + 16 * h, sv);
+                    ptx::tmem_ld_wait(dv);
+                    ptx::tmem_ld_wait(sv);
+                    if (h == 1) {
+                        // the whole item is in registers: hand the TMEM slot back
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar(BAR_D_EMPTY + e));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[8 * h + j] =
+                            ptx::fma_f32x2(ptx::f2_bits(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
+                                           ptx::f2_bits(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1])),
+                                           acc[8 * h + j]);
+                }
+            }
+        }
+        if (!DOTS && !*abort && mrow < M) {
+            float* orow = out + (long long)mrow * N + n0 + c0;
+            const int ncols = N - (n0 + c0);  // columns of this warp's 32 that exist
+            if (ncols >= EPI_COLS && (N & 3) == 0) {
+#pragma unroll
+                for (int c = 0; c < EPI_COLS / 4; ++c)
+                    reinterpret_cast<ulonglong2*>(orow)[c] = make_ulonglong2(acc[2 * c], acc[2 * c + 1]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < EPI_COLS / 2; ++c) {
+                    if (2 * c < ncols) orow[2 * c] = __uint_as_float((uint32_t)acc[c]);
+                    if (2 * c + 1 < ncols) orow[2 * c + 1] = __uint_as_float((uint32_t)(acc[c] >> 32));
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+// Scratch comes from a library-owned stream-ordered pool per device: allocated and
+// freed on the call's stream, so calls on different streams never share bytes, and
+// kept cached between calls (release threshold = no limit).  Under stream capture the
+// same two calls are made on the device's default pool, which the graph turns into
+// allocation and free nodes.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[64];
+bool g_pool_tried[64];
+
+cudaMemPool_t scratch_pool(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pool_tried[dev]) {
+        g_pool_tried[dev] = true;
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) == cudaSuccess) {
+            uint64_t thr = ~0ull;
+            cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &thr);
+            g_pool[dev] = p;
+        } else {
+            cudaGetLastError();
+        }
+    }
+    return g_pool[dev];
+}
+
+template <typename Kern>
+bool set_smem(Kern k, int bytes, bool& done) {
+    if (done) return true;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done = true;
+    return true;
+}
+
+template <int FMT, bool DOTS>
+int launch_x(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
+             cudaStream_t s, const char* fn) {
+    const int nb = (int)(K / QK), ng = nb / GB;
+    const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
+    const size_t xa_b = (size_t)MT * nb * CHUNK, ga_b = (size_t)MT * ng * ga_bytes(FMT);
+    const size_t xb_b = (size_t)NT * nb * CHUNK, gw_b = (size_t)NT * ng * gw_bytes(FMT);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaGetDevice failed");
+        return MMQ_ERR_CUDA;
+    }
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool) {
+        report(fn, MMQ_ERR_CUDA, "scratch pool creation failed");
+        return MMQ_ERR_CUDA;
+    }
+    static bool attr_done = false;
+    if (!set_smem(k_mmq_tcx<FMT, DOTS>, XLayout<FMT>::alloc, attr_done)) {
+        report(fn, MMQ_ERR_SMEM, "shared-memory request refused");
+        return MMQ_ERR_SMEM;
+    }
+    // While `s` is being captured, the allocation and free below become graph memory
+    // nodes (graph-owned scratch); outside capture they come from the library's pool.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaStreamIsCapturing failed");
+        return MMQ_ERR_CUDA;
+    }
+    void* ws = nullptr;
+    const size_t bytes = xa_b + ga_b + xb_b + gw_b;
+    const cudaError_t ae = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(&ws, bytes, pool, s)
+                                                            : cudaMallocAsync(&ws, bytes, s);
+    if (ae != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_NOMEM, "scratch allocation failed");
+        return MMQ_ERR_NOMEM;
+    }
+    uint8_t* xa = static_cast<uint8_t*>(ws);
+    uint8_t* ga = xa + xa_b;
+    uint8_t* xb = ga + ga_b;
+    uint8_t* gw = xb + xb_b;
+    {
+        ProfScope ps("k_expand_acts", s);
+        k_expand_acts<FMT><<<dim3((unsigned)MT, (unsigned)ng), EXP_THREADS, 0, s>>>(
+            static_cast<const uint8_t*>(xq), (int)M, nb, xa, ga);
+    }
+    {
+        ProfScope ps("k_expand_weights", s);
+        k_expand_weights<FMT, !DOTS><<<dim3((unsigned)NT, (unsigned)ng), EXP_THREADS, 0, s>>>(
+            static_cast<const uint8_t*>(wq), (int)N, nb, xb, gw);
+    }
+    {
+        ProfScope ps("k_mmq_tcx", s);
+        k_mmq_tcx<FMT, DOTS><<<dim3((unsigned)MT, (unsigned)NT), THREADS, XLayout<FMT>::alloc, s>>>(
+            xa, ga, xb, gw, (int)M, (int)N, nb, out, dots);
+    }
+    const int st = launch_status(fn);
+    cudaFreeAsync(ws, s);  // stream-ordered: after the kernels above
+    return st;
+}
+
+}  // namespace
+
+int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
+               cudaStream_t s) {
+    const char* fn = fmt == FMT_Q8_0 ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
+                                     : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
+    if (K % QK_K != 0) {
+        report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
+        return MMQ_ERR_K_MULTIPLE;
+    }
+    if ((N + BN - 1) / BN > 65535 || K / QK_K > 65535) {
+        report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
+        return MMQ_ERR_SHAPE;
+    }
+    if (fmt == FMT_Q8_0)
+        return dots ? launch_x<FMT_Q8_0, true>(xq, wq, M, N, K, out, dots, s, fn)
+                    : launch_x<FMT_Q8_0, false>(xq, wq, M, N, K, out, dots, s, fn);
+    return dots ? launch_x<FMT_Q4_K, true>(xq, wq, M, N, K, out, dots, s, fn)
+                : launch_x<FMT_Q4_K, false>(xq, wq, M, N, K, out, dots, s, fn);
+}
+
+unsigned tcx_take_error() {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tcx_error, sizeof(v)) != cudaSuccess) return 0;
+    if (v) {
+        const unsigned zero = 0;
+        cudaMemcpyToSymbol(g_tcx_error, &zero, sizeof(zero));
+    }
+    return v;
+}
+
+}  // namespace mmq

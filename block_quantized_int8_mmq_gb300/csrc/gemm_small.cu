@@ -498,7 +498,10 @@ int launch_staged(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, in
         attr_done = true;
     }
     dim3 grid((unsigned)((N + 15) / 16), (unsigned)((M + 7) / 8));
-    k_mmq_small_staged<FMT><<<grid, ST_WARPS * 32, st_smem_bytes(FMT), s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
+    {
+        ProfScope ps("k_mmq_small_staged", s);
+        k_mmq_small_staged<FMT><<<grid, ST_WARPS * 32, st_smem_bytes(FMT), s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
+    }
     return launch_status(fn);
 }
 
@@ -529,6 +532,7 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
                                : launch_staged<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s);
     if (nb % 2 == 0) {
         dim3 g2((unsigned)((N + 15) / 16), (unsigned)((M + 7) / 8));
+        ProfScope ps("k_mmq_small_mma", s);
         if (fmt == FMT_Q8_0)
             k_mmq_small_mma<FMT_Q8_0><<<g2, MMA_WARPS * 32, 0, s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
         else
@@ -536,6 +540,7 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
         return launch_status(fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)");
     }
     dim3 grid((unsigned)((N + SMALL_WARPS - 1) / SMALL_WARPS), (unsigned)((M + SMALL_MT - 1) / SMALL_MT));
+    ProfScope ps("k_mmq_small", s);
     if (fmt == FMT_Q8_0)
         k_mmq_small<FMT_Q8_0><<<grid, SMALL_WARPS * 32, 0, s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
     else

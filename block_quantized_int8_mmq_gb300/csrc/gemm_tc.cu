@@ -46,9 +46,12 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "umma.cuh"
 
 namespace mmq {
 namespace {
+
+using namespace umma;
 
 __device__ unsigned int g_tc_error;
 
@@ -68,8 +71,6 @@ constexpr int A_ROW = KT_BLOCKS * Q8_1_BYTES;  // 288
 constexpr int OP_MAIN = BM * QK * 2;    // fp16 tile of one block (K = 32): 8 KiB
 constexpr int OP_AUX = BM * 16 * 2;     // fp16 scale operand (K = 16, column 0 used): 4 KiB
 constexpr int SLOT = 2 * OP_MAIN + 2 * OP_AUX;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bound on any one wait
-constexpr uint32_t WAIT_SLEEP_NS = 100000;           // longest sleep inside one poll
 
 static_assert(BM + BN == 32 * CONV_WARPS, "one scale row (activation or weight) per converter thread");
 static_assert(EPI_COLS == 32, "one 16x256b.x4 fragment covers 32 columns");
@@ -99,86 +100,13 @@ struct Layout {
     static_assert(rawB % 1024 == 0 && slots % 1024 == 0 && SLOT % 1024 == 0, "alignment");
 };
 
-// Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of 8 rows x 16 B
-// (8 fp16 along K) stored as 128 contiguous bytes; the next core matrix along K is
-// 128 B further (leading-dimension offset), the next 8-row group `sbo` bytes further
-// (512 for a K = 32 tile, 256 for a K = 16 tile).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t sbo) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
-           (1ull << 46);
-}
-
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) {
-    uint32_t o;
-    memcpy(&o, &h, 4);
-    return o;
-}
-__device__ __forceinline__ __half2 bits_h2(uint32_t v) {
-    __half2 h;
-    memcpy(&h, &v, 4);
-    return h;
-}
-
-// Four signed int8 codes -> four exact fp16 values.  (x + 128) is placed in the low
-// mantissa byte of 1024.0 (bits 0x64xx), then 1152 = 1024 + 128 is subtracted.
-__device__ __forceinline__ uint2 i8x4_to_f16x4(uint32_t w) {
-    const uint32_t u = w ^ 0x80808080u;
-    const __half2 bias = bits_h2(0x64806480u);
-    return make_uint2(h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4140)), bias)),
-                      h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4342)), bias)));
-}
-
-// Four codes q in 0..15 (one per byte) -> four exact fp16 values sc*q, from the bits of
-// 1024 + q and one fused (1024 + q)*sc - 1024*sc (exact: sc*q <= 945).
-__device__ __forceinline__ uint2 u4x4_scaled_f16x4(uint32_t w, __half2 sc2, __half2 nsc1024) {
-    return make_uint2(h2_bits(__hfma2(bits_h2(__byte_perm(w, 0x64646464u, 0x4140)), sc2, nsc1024)),
-                      h2_bits(__hfma2(bits_h2(__byte_perm(w, 0x64646464u, 0x4342)), sc2, nsc1024)));
-}
-
-// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the wall
-// time limit ran out (then the error word and the abort flag are set).  Inlined: a
-// call here costs the waiting warp more than the wait itself.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (;;) {
-        if (ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
-        if (*abort) return false;
-        if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-            atomicOr(&g_tc_error, ERR_TIMEOUT);
-            *abort = 1;
-            return false;
-        }
-    }
+    return umma::wait_bar(bar, parity, abort, &g_tc_error);
 }
-
-// Teardown wait: bounded by time only (used to drain in-flight copies and MMAs).
-__device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-            atomicOr(&g_tc_error, ERR_TIMEOUT);
-            return;
-        }
-    }
-}
-
-// Lane 0 polls (one shared-memory barrier access per poll instead of 32); the other
-// lanes take its answer, so the warp stays on one path.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) { umma::drain_bar(bar, parity, &g_tc_error); }
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort);
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    return umma::warp_wait(bar, parity, abort, &g_tc_error);
 }
-
-// Offset of (row r, k-group kg of 8 fp16) in a K-major no-swizzle tile with 8-row-group
-// stride sbo.
-__device__ __forceinline__ int core_off(int r, int kg, int sbo) { return (r >> 3) * sbo + kg * 128 + (r & 7) * 16; }
 
 template <int FMT, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -408,90 +336,9 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Warp (q = lane quarter, cg = column group) owns rows 32q..32q+31 and columns
-        // c0..c0+31 of the tile.  D and S are read as 16-lane x 32-column fragments:
-        // thread t holds rows 32q + t/4 + {0, 8} (+16 for the second half) and columns
-        // c0 + 8k + 2*(t%4) + {0, 1}, k = 0..3; D and S have the same layout, so the
-        // rescale is an elementwise FMA on the fragments.
-        const int q = warp & 3;
-        const int cg = (warp - WARP_EPI0) >> 2;
-        const int c0 = cg * EPI_COLS;
-        const int tr = lane >> 2, tc2 = 2 * (lane & 3);
-        const int rloc0 = 32 * q + tr;                 // rows rloc0 + 8*i, i = 0..3 (i = 2*half + i2)
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
-        unsigned long long acc[16];                    // [row i][col pair k] as packed pairs
-#pragma unroll
-        for (int c = 0; c < 16; ++c) acc[c] = 0ull;
-        for (int it = 0; it < nitems; ++it) {
-            const int t = it % DS;
-            if (!warp_wait(bar(BAR_D_FULL + t), (it / DS) & 1, abort)) break;
-            ptx::tc_fence_after();
-            const uint32_t taddr = lane_base + (uint32_t)(t * 2 * BN);
-            if (DOTS) {
-                const int bi = it;  // no min items in this mode
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t dv[16];
-                    ptx::tmem_ld16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16), dv);
-                    ptx::tmem_ld_wait(dv);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int mrow = m0 + rloc0 + 16 * hh + 8 * i;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int n = n0 + c0 + 8 * k + tc2 + e;
-                                if (mrow < M && n < N)
-                                    dots[((long long)mrow * N + n) * nb + bi] =
-                                        __float2int_rn(__uint_as_float(dv[4 * k + 2 * i + e]));
-                            }
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t dv[16], sv[16];
-                    ptx::tmem_ld16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16), dv);
-                    ptx::tmem_ld16x256b_x4(taddr + BN + ((uint32_t)(16 * hh) << 16), sv);
-                    ptx::tmem_ld_wait(dv);
-                    ptx::tmem_ld_wait(sv);
-#pragma unroll
-                    for (int i2 = 0; i2 < 2; ++i2)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int a = 4 * (2 * hh + i2) + k;
-                            acc[a] = ptx::fma_f32x2(
-                                ptx::f2_bits(__uint_as_float(sv[4 * k + 2 * i2]), __uint_as_float(sv[4 * k + 2 * i2 + 1])),
-                                ptx::f2_bits(__uint_as_float(dv[4 * k + 2 * i2]), __uint_as_float(dv[4 * k + 2 * i2 + 1])),
-                                acc[a]);
-                        }
-                }
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(BAR_D_EMPTY + t));
-        }
-        if (!DOTS && !*abort) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int mrow = m0 + rloc0 + 8 * i;
-                if (mrow >= M) continue;
-                float* orow = out + (long long)mrow * N;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int n = n0 + c0 + 8 * k + tc2;
-                    if (n + 1 < N && (N & 1) == 0) {
-                        *reinterpret_cast<unsigned long long*>(orow + n) = acc[4 * i + k];
-                    } else {
-                        if (n < N) orow[n] = __uint_as_float((uint32_t)acc[4 * i + k]);
-                        if (n + 1 < N) orow[n + 1] = __uint_as_float((uint32_t)(acc[4 * i + k] >> 32));
-                    }
-                }
-            }
-        }
+        epilogue_128x128<DOTS, DS, BN, false>(warp & 3, (warp - WARP_EPI0) >> 2, lane, tmem, nitems, bar(BAR_D_FULL),
+                                       bar(BAR_D_EMPTY), abort, &g_tc_error, M, N, m0, n0, nb, out, dots);
     }
-
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == WARP_MMA) {
@@ -552,7 +399,10 @@ int launch_t(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
         attr_done = true;
     }
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    k_mmq_tc<FMT, DOTS><<<grid, THREADS, smem, s>>>(ta, tb, (int)M, (int)N, nb, out, dots);
+    {
+        ProfScope ps("k_mmq_tc", s);
+        k_mmq_tc<FMT, DOTS><<<grid, THREADS, smem, s>>>(ta, tb, (int)M, (int)N, nb, out, dots);
+    }
     return launch_status(fn);
 }
 

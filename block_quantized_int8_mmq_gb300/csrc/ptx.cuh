@@ -45,6 +45,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of an mbarrier phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // As mbar_try_wait, but the thread may sleep in the instruction for up to `ns`
 // nanoseconds until the phase completes, instead of returning at once: waiting warps
 // then stop polling the barrier (every poll is a shared-memory access).
@@ -84,6 +95,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Generic-proxy shared-memory writes become visible to the async proxy (MMA reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ registers
+// Per-warpgroup register reallocation (all four warps of a warpgroup execute the same
+// one).  An increase waits until the CTA's pool (threads x registers at launch) has the
+// registers: the launching side checks that every split adds up.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -168,6 +192,11 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
                    "+r"(r[15]));
 }
+
+// 32 lanes x W consecutive 32-bit columns, W = 8, 16 or 32 (the array's length).
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[8]) { tmem_ld8(taddr, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
 
 // Packed f32 pairs (two IEEE round-to-nearest operations per instruction).
 __device__ __forceinline__ unsigned long long f2_bits(float lo, float hi) {

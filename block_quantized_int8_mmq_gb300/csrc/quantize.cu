@@ -86,7 +86,10 @@ int quantize_launch(const float* x, int64_t M, int64_t K, void* xq, cudaStream_t
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long cap = (long long)(sms > 0 ? sms : 152) * 16;
     if (grid > cap) grid = cap;
-    k_quantize_q8_1<<<(unsigned)grid, QUANT_THREADS, 0, s>>>(x, static_cast<uint8_t*>(xq), nblk);
+    {
+        ProfScope ps("k_quantize_q8_1", s);
+        k_quantize_q8_1<<<(unsigned)grid, QUANT_THREADS, 0, s>>>(x, static_cast<uint8_t*>(xq), nblk);
+    }
     return launch_status("mmq_quantize_q8_1");
 }
 

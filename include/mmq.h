@@ -16,7 +16,14 @@
  *
  * Conventions shared by every entry point:
  *  - Pointers named x, xq, wq, out, dots are DEVICE pointers owned by the caller.  The
- *    library never frees or retains them and allocates no device memory.
+ *    library never frees or retains them.
+ *  - Scratch: the expanded-code tensor-core path (MMQ_PATH_EXPAND) needs a scratch
+ *    buffer of about 2*K bytes per row of each operand (rows rounded up to 128).  It is
+ *    taken from a library-owned stream-ordered memory pool of the current device
+ *    (allocated and freed on the call's stream, cached between calls), so calls on
+ *    different streams never share scratch.  While `stream` is being captured into a
+ *    CUDA graph, the allocation and free are stream-ordered calls on the device's
+ *    default pool and become the graph's own memory nodes.  No other path allocates.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call is
  *    asynchronous on that stream; results are valid once the stream has reached them.
  *  - Return value: MMQ_OK (0) or a negative mmq_status.  A call that returns an error
@@ -61,7 +68,8 @@ typedef enum mmq_status {
     MMQ_ERR_LAUNCH = -6,      /* the kernel launch failed (CUDA error cleared) */
     MMQ_ERR_TIMEOUT = -7,     /* a device-side bounded wait ran out (device error word) */
     MMQ_ERR_CUDA = -8,        /* another CUDA runtime error (device query, tensor map) */
-    MMQ_ERR_ARG = -9          /* an argument outside its documented set */
+    MMQ_ERR_ARG = -9,         /* an argument outside its documented set */
+    MMQ_ERR_NOMEM = -10       /* the scratch allocation of the expanded path failed */
 } mmq_status;
 
 /* Human-readable name of a status code.  Never NULL; the string is static. */
@@ -93,8 +101,8 @@ int mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, void* stre
  *   xq: 16-byte aligned.  wq: 16-byte aligned.  out: f32 [M][N], 16-byte aligned.
  * Accuracy: |out - exact| <= 1e-4 * sum_b |xd*wd*D_b| per entry, with the block dots
  * D_b computed exactly.
- * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE (K % 32), MMQ_ERR_NULL, MMQ_ERR_ALIGN,
- * MMQ_ERR_SMEM, MMQ_ERR_LAUNCH.
+ * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE (K % 32; K % 256 on a forced tensor-core
+ * path), MMQ_ERR_NULL, MMQ_ERR_ALIGN, MMQ_ERR_SMEM, MMQ_ERR_NOMEM, MMQ_ERR_LAUNCH.
  */
 int mmq_gemm_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                   void* stream);
@@ -123,17 +131,41 @@ int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t
                               int32_t* dots, void* stream);
 
 /* Kernel selection for the two contractions and their test hooks.
- *   MMQ_PATH_AUTO  : by M (small-M warp kernel for M <= 8, tensor-core kernel above).
- *   MMQ_PATH_SMALL : always the warp-level kernel (any M; slow for large M).
- *   MMQ_PATH_TC    : always the tcgen05 tensor-core kernel.
- * Process-wide; the environment variable MMQ_FORCE_PATH=auto|small|tc sets the initial
- * value.  Returns the previous value, or MMQ_ERR_ARG. */
-enum { MMQ_PATH_AUTO = 0, MMQ_PATH_SMALL = 1, MMQ_PATH_TC = 2 };
+ *   MMQ_PATH_AUTO   : by shape: the warp-level kernel for M <= 8 or K % 256 != 0; else
+ *                     the expanded-code tensor-core path for M >= MMQ_EXPAND_MIN_M, the
+ *                     converter tensor-core kernel otherwise.
+ *   MMQ_PATH_SMALL  : always the warp-level kernel (any M; slow for large M).
+ *   MMQ_PATH_TC     : always the tcgen05 kernel that converts codes in shared memory
+ *                     (K % 256 == 0, no scratch).
+ *   MMQ_PATH_EXPAND : always the tcgen05 kernel over codes expanded to fp16 once per
+ *                     call into scratch (K % 256 == 0).
+ * Process-wide; the environment variable MMQ_FORCE_PATH=auto|small|tc|expand sets the
+ * initial value.  Returns the previous value, or MMQ_ERR_ARG. */
+enum { MMQ_PATH_AUTO = 0, MMQ_PATH_SMALL = 1, MMQ_PATH_TC = 2, MMQ_PATH_EXPAND = 3 };
+#define MMQ_EXPAND_MIN_M 64
 int mmq_set_path(int path);
 
 /* Path the last successful contraction or test-hook call on this thread took
- * (MMQ_PATH_SMALL or MMQ_PATH_TC), or 0 before any. */
+ * (MMQ_PATH_SMALL, MMQ_PATH_TC or MMQ_PATH_EXPAND), or 0 before any. */
 int mmq_last_path(void);
+
+/* Per-kernel device timing, for tests and benchmarks.  While enabled, every kernel the
+ * library launches is bracketed by two CUDA events on its stream.  On a stream being
+ * captured into a graph the two records become event-record nodes of the graph (their
+ * events then hold the times of the graph's latest launch and are never reused).
+ * mmq_profile_enable returns the previous state (0 or 1).  mmq_profile_read waits for
+ * every recorded launch to finish, adds it to its kernel's totals, writes up to
+ * `capacity` entries (kernels in name order; `out` may be NULL) and returns the number
+ * of kernels with at least one launch, or MMQ_ERR_CUDA if an event could not be read.
+ * A captured launch is counted once, at the first read after the graph has run.
+ * reset != 0 clears the totals afterwards.  Read outside timed regions. */
+typedef struct mmq_kernel_time {
+    char name[32];
+    int64_t launches;
+    double total_ms;
+} mmq_kernel_time;
+int mmq_profile_enable(int on);
+int mmq_profile_read(mmq_kernel_time* out, int capacity, int reset);
 
 /* Synchronizes `stream`, then reads and clears the device error word of every kernel
  * in the library.  Returns MMQ_OK, MMQ_ERR_TIMEOUT (a bounded wait ran out) or

@@ -36,7 +36,7 @@ def test_sizes():
 
 def test_status_strings():
     assert mmq.mmq_status_string(0) == "MMQ_OK"
-    for s in range(-9, 0):
+    for s in range(-10, 0):
         assert mmq.mmq_status_string(s).startswith("MMQ_ERR_")
     assert mmq.mmq_status_string(-1000) == "MMQ_ERR_UNKNOWN"
 
@@ -44,7 +44,8 @@ def test_status_strings():
 def test_path_selection_round_trip():
     prev = mmq.mmq_set_path(mmq.PATH_SMALL)
     assert mmq.mmq_set_path(mmq.PATH_TC) == mmq.PATH_SMALL
-    assert mmq.mmq_set_path(prev) == mmq.PATH_TC
+    assert mmq.mmq_set_path(mmq.PATH_EXPAND) == mmq.PATH_TC
+    assert mmq.mmq_set_path(prev) == mmq.PATH_EXPAND
     assert mmq.lib().mmq_set_path(7) == -9
 
 

@@ -19,7 +19,8 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-4
-PATHS = ["small", "tc"]
+PATHS = ["small", "tc", "expand"]
+PATH_IDS = {"small": 1, "tc": 2, "expand": 3}
 
 
 @pytest.fixture(scope="module")
@@ -36,7 +37,8 @@ def dev(a):
 
 
 def set_path(mmq, path):
-    mmq.mmq_set_path({"auto": mmq.PATH_AUTO, "small": mmq.PATH_SMALL, "tc": mmq.PATH_TC}[path])
+    mmq.mmq_set_path({"auto": mmq.PATH_AUTO, "small": mmq.PATH_SMALL, "tc": mmq.PATH_TC,
+                      "expand": mmq.PATH_EXPAND}[path])
 
 
 def check_close(out, ref, norm, what=""):
@@ -104,24 +106,25 @@ SMALL_SHAPES = {
 def test_gemm_parity_full(mmq, fmt, path):
     set_path(mmq, path)
     for (M, N, K) in SMALL_SHAPES[fmt]:
-        if path == "tc" and K % 256:
-            continue  # the tensor-core path stages 256-value k-tiles (refusal tested below)
+        if path != "small" and K % 256:
+            continue  # the tensor-core paths stage 256-value groups (refusal tested below)
         x = synth.activations(M * 7 + N, M, K, True)
         w = synth.weights(fmt, M + N * 3, N, K)
         xq = mmq.mmq_quantize_q8_1(dev(x))
         out = mmq.gemm(fmt, xq, dev(w), M, N, K)
-        assert mmq.mmq_last_path() == {"small": mmq.PATH_SMALL, "tc": mmq.PATH_TC}[path]
+        assert mmq.mmq_last_path() == PATH_IDS[path]
         ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
         check_close(out.cpu().numpy(), ref, norm, f"{fmt} {path} {M}x{N}x{K}")
     assert mmq.mmq_get_device_error() == 0
 
 
-def test_tc_path_refuses_partial_k_tiles_and_auto_routes_them(mmq):
-    M, N, K = 16, 40, 96
+@pytest.mark.parametrize("path", ["tc", "expand"])
+def test_tc_paths_refuse_partial_k_groups_and_auto_routes_them(mmq, path):
+    M, N, K = 80, 40, 96
     x = synth.activations(21, M, K, True)
     w = synth.q8_0_weights(22, N, K)
     xq = mmq.mmq_quantize_q8_1(dev(x))
-    set_path(mmq, "tc")
+    set_path(mmq, path)
     with pytest.raises(mmq.MMQError) as e:
         mmq.mmq_gemm_q8_0(xq, dev(w), M, N, K)
     assert e.value.status == -2
@@ -194,9 +197,10 @@ def full_operands():
     return get
 
 
-@pytest.mark.parametrize("index", [0, 1, 2, 3])
-def test_config_sampled_parity(mmq, full_operands, index):
-    set_path(mmq, "auto")
+@pytest.mark.parametrize("index,path", [(0, "auto"), (1, "auto"), (2, "auto"), (3, "auto"), (1, "tc"),
+                                        (3, "tc")])
+def test_config_sampled_parity(mmq, full_operands, index, path):
+    set_path(mmq, path)
     x, w, spec, xq_ref = full_operands(index)
     M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
     xq = mmq.mmq_quantize_q8_1(dev(x))
@@ -207,8 +211,10 @@ def test_config_sampled_parity(mmq, full_operands, index):
     assert not np.isnan(o).any(), "output not fully written"
     im, inn = sample_entries(M, N, 3000, index)
     ref, norm = oracle.gemm_at(fmt, xq_ref, w, M, N, K, im, inn)
-    check_close(o[im, inn], ref, norm, f"config {index}")
+    check_close(o[im, inn], ref, norm, f"config {index} {path}")
     assert mmq.mmq_get_device_error() == 0
+    if path == "auto":
+        assert mmq.mmq_last_path() == (mmq.PATH_EXPAND if M >= 64 else mmq.PATH_TC)
 
 
 @pytest.mark.parametrize("M", synth.M_SWEEP)
@@ -260,3 +266,82 @@ def test_streams_and_device_error_word(mmq):
     assert mmq.mmq_get_device_error(s) == 0
     ref, norm = oracle.gemm("q4_k", oracle.quantize_q8_1(x), w, M, N, K)
     check_close(out.cpu().numpy(), ref, norm, "side stream")
+
+
+def test_graph_capture_and_replay_with_scratch(mmq):
+    # under capture the expanded path's scratch becomes graph-owned memory; replaying the
+    # graph twice gives the eager result, and the profiler's event nodes time the replay
+    set_path(mmq, "auto")
+    M, N, K = 192, 160, 512
+    x = synth.activations(31, M, K, True)
+    w = synth.q8_0_weights(32, N, K)
+    xd, wd = dev(x), dev(w)
+    xq = mmq.mmq_quantize_q8_1(xd)
+    eager = mmq.mmq_gemm_q8_0(xq, wd, M, N, K)
+    assert mmq.mmq_last_path() == mmq.PATH_EXPAND
+    torch.cuda.synchronize()
+    mmq.mmq_profile_read(reset=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    out = torch.full((M, N), float("nan"), device="cuda")
+    prev = mmq.mmq_profile_enable(True)
+    try:
+        with torch.cuda.graph(g, stream=s):
+            mmq.mmq_gemm_q8_0(xq, wd, M, N, K, out=out, stream=s)
+        assert mmq.mmq_last_path() == mmq.PATH_EXPAND
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        prof = mmq.mmq_profile_read(reset=True)
+    finally:
+        mmq.mmq_profile_enable(prev)
+    assert set(prof) == {"k_expand_acts", "k_expand_weights", "k_mmq_tcx"}, prof
+    assert all(n == 1 and ms > 0 for n, ms in prof.values()), prof
+    ref, norm = oracle.gemm("q8_0", oracle.quantize_q8_1(x), w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, "captured")
+    check_close(eager.cpu().numpy(), ref, norm, "eager")
+    assert mmq.mmq_get_device_error() == 0
+
+
+def test_profile_counts_every_launch(mmq):
+    set_path(mmq, "auto")
+    torch.cuda.synchronize()
+    mmq.mmq_profile_read(reset=True)
+    prev = mmq.mmq_profile_enable(True)
+    try:
+        M, N, K = 100, 130, 512
+        x = synth.activations(61, M, K, True)
+        w = synth.q4_k_weights(62, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        mmq.mmq_gemm_q4_k(xq, dev(w), M, N, K)          # expanded path: three kernels
+        mmq.mmq_gemm_q4_k(xq[:4], dev(w), 4, N, K)      # M <= 8: warp-level kernel
+        prof = mmq.mmq_profile_read(reset=True)
+    finally:
+        mmq.mmq_profile_enable(prev)
+    assert prof["k_quantize_q8_1"][0] == 1
+    assert prof["k_expand_acts"][0] == prof["k_expand_weights"][0] == prof["k_mmq_tcx"][0] == 1
+    assert sum(n for k, (n, _) in prof.items() if k.startswith("k_mmq_small")) == 1
+    assert mmq.mmq_profile_read() == {}
+
+
+def test_expand_path_concurrent_streams(mmq):
+    # two streams in flight at once, each with its own stream-ordered scratch
+    set_path(mmq, "expand")
+    M, N, K = 256, 384, 1024
+    ops = []
+    for i in range(2):
+        x = synth.activations(40 + i, M, K, True)
+        w = synth.q4_k_weights(50 + i, N, K)
+        ops.append((x, w))
+    streams = [torch.cuda.Stream() for _ in ops]
+    outs = []
+    for (x, w), st in zip(ops, streams):
+        with torch.cuda.stream(st):
+            xq = mmq.mmq_quantize_q8_1(dev(x), stream=st)
+            outs.append(mmq.mmq_gemm_q4_k(xq, dev(w), M, N, K, stream=st))
+    torch.cuda.synchronize()
+    for (x, w), o in zip(ops, outs):
+        ref, norm = oracle.gemm("q4_k", oracle.quantize_q8_1(x), w, M, N, K)
+        check_close(o.cpu().numpy(), ref, norm, "concurrent streams")
+    assert mmq.mmq_get_device_error() == 0
