@@ -22,6 +22,7 @@ EXPORTED = (
     "mmq_status_string", "mmq_q8_1_bytes", "mmq_weight_row_bytes", "mmq_quantize_q8_1",
     "mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k",
     "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
+    "mmq_gemm_noalloc",
 )
 
 
@@ -52,6 +53,7 @@ def _load():
         getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P]
     L.mmq_set_path.argtypes = [I]
     L.mmq_get_device_error.argtypes = [P]
+    L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
     return L
@@ -137,6 +139,17 @@ def mmq_gemm_q8_0(xq, wq, M, N, K, out=None, stream=None):
 def mmq_gemm_q4_k(xq, wq, M, N, K, out=None, stream=None):
     """q8_1 [M, K/32*36] x Q4_K [N, K/256*144] -> f32 [M, N]."""
     return _gemm("mmq_gemm_q4_k", xq, wq, M, N, K, out, stream)
+
+
+def mmq_gemm_noalloc(fmt, xq, wq, M, N, K, out=None, stream=None):
+    """The contraction on the expanded tensor-core path with the library's fixed 64 MiB
+    device scratch: no device allocation.  fmt: "q8_0" / "q4_k" or 0 / 1."""
+    import torch
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    _check("mmq_gemm_noalloc", _lib.mmq_gemm_noalloc(f, _ptr(xq), _ptr(wq), M, N, K, _ptr(out), _stream(stream)))
+    return out
 
 
 def _dots(fn, xq, wq, M, N, K, dots, stream):

@@ -173,6 +173,28 @@ int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t
     return contraction("mmq_debug_block_dots_q4_k", FMT_Q4_K, xq, wq, M, N, K, nullptr, dots, stream);
 }
 
+int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                     void* stream) {
+    const char* fn = "mmq_gemm_noalloc";
+    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K) {
+        report(fn, MMQ_ERR_ARG, "fmt must be 0 (Q8_0) or 1 (Q4_K)");
+        return MMQ_ERR_ARG;
+    }
+    int st = check_mk(fn, M, N, K, fmt == FMT_Q4_K ? QK_K : QK);
+    if (st) return st;
+    if (!xq || !wq || !out) {
+        report(fn, MMQ_ERR_NULL, "xq, wq and out must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(out, 16)) {
+        report(fn, MMQ_ERR_ALIGN, "xq, wq and out must be 16-byte aligned");
+        return MMQ_ERR_ALIGN;
+    }
+    st = tcx_launch_noalloc(fmt, xq, wq, M, N, K, out, static_cast<cudaStream_t>(stream));
+    if (st == MMQ_OK) t_last_path = MMQ_PATH_EXPAND;
+    return st;
+}
+
 int mmq_set_path(int path) {
     if (path != MMQ_PATH_AUTO && path != MMQ_PATH_SMALL && path != MMQ_PATH_TC && path != MMQ_PATH_EXPAND)
         return MMQ_ERR_ARG;

@@ -538,50 +538,35 @@ bool set_smem(Kern k, int bytes, bool& done) {
     return true;
 }
 
+// Scratch bytes of one call: expanded activations, activation group data, expanded
+// weights, weight group data (each a multiple of 256 bytes).
+struct ScratchPlan {
+    size_t xa, ga, xb, gw;
+    size_t total() const { return xa + ga + xb + gw; }
+};
+ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K) {
+    const int64_t nb = K / QK, ng = nb / GB;
+    const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
+    return {(size_t)(MT * nb) * CHUNK, (size_t)(MT * ng) * ga_bytes(fmt), (size_t)(NT * nb) * CHUNK,
+            (size_t)(NT * ng) * gw_bytes(fmt)};
+}
+
+// The three launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K) bytes).
 template <int FMT, bool DOTS>
-int launch_x(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
-             cudaStream_t s, const char* fn) {
+int launch_on(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
+              uint8_t* ws, cudaStream_t s, const char* fn) {
     const int nb = (int)(K / QK), ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    const size_t xa_b = (size_t)MT * nb * CHUNK, ga_b = (size_t)MT * ng * ga_bytes(FMT);
-    const size_t xb_b = (size_t)NT * nb * CHUNK, gw_b = (size_t)NT * ng * gw_bytes(FMT);
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        report(fn, MMQ_ERR_CUDA, "cudaGetDevice failed");
-        return MMQ_ERR_CUDA;
-    }
-    cudaMemPool_t pool = scratch_pool(dev);
-    if (!pool) {
-        report(fn, MMQ_ERR_CUDA, "scratch pool creation failed");
-        return MMQ_ERR_CUDA;
-    }
+    const ScratchPlan sp = plan_scratch(FMT, M, N, K);
     static bool attr_done = false;
     if (!set_smem(k_mmq_tcx<FMT, DOTS>, XLayout<FMT>::alloc, attr_done)) {
         report(fn, MMQ_ERR_SMEM, "shared-memory request refused");
         return MMQ_ERR_SMEM;
     }
-    // While `s` is being captured, the allocation and free below become graph memory
-    // nodes (graph-owned scratch); outside capture they come from the library's pool.
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
-        cudaGetLastError();
-        report(fn, MMQ_ERR_CUDA, "cudaStreamIsCapturing failed");
-        return MMQ_ERR_CUDA;
-    }
-    void* ws = nullptr;
-    const size_t bytes = xa_b + ga_b + xb_b + gw_b;
-    const cudaError_t ae = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(&ws, bytes, pool, s)
-                                                            : cudaMallocAsync(&ws, bytes, s);
-    if (ae != cudaSuccess) {
-        cudaGetLastError();
-        report(fn, MMQ_ERR_NOMEM, "scratch allocation failed");
-        return MMQ_ERR_NOMEM;
-    }
-    uint8_t* xa = static_cast<uint8_t*>(ws);
-    uint8_t* ga = xa + xa_b;
-    uint8_t* xb = ga + ga_b;
-    uint8_t* gw = xb + xb_b;
+    uint8_t* xa = ws;
+    uint8_t* ga = xa + sp.xa;
+    uint8_t* xb = ga + sp.ga;
+    uint8_t* gw = xb + sp.xb;
     {
         ProfScope ps("k_expand_acts", s);
         k_expand_acts<FMT><<<dim3((unsigned)MT, (unsigned)ng), EXP_THREADS, 0, s>>>(
@@ -597,9 +582,67 @@ int launch_x(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
         k_mmq_tcx<FMT, DOTS><<<dim3((unsigned)MT, (unsigned)NT), THREADS, XLayout<FMT>::alloc, s>>>(
             xa, ga, xb, gw, (int)M, (int)N, nb, out, dots);
     }
-    const int st = launch_status(fn);
+    return launch_status(fn);
+}
+
+template <int FMT, bool DOTS>
+int launch_x(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
+             cudaStream_t s, const char* fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaGetDevice failed");
+        return MMQ_ERR_CUDA;
+    }
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool) {
+        report(fn, MMQ_ERR_CUDA, "scratch pool creation failed");
+        return MMQ_ERR_CUDA;
+    }
+    // While `s` is being captured, the allocation and free below become graph memory
+    // nodes (graph-owned scratch); outside capture they come from the library's pool.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaStreamIsCapturing failed");
+        return MMQ_ERR_CUDA;
+    }
+    void* ws = nullptr;
+    const size_t bytes = plan_scratch(FMT, M, N, K).total();
+    const cudaError_t ae = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(&ws, bytes, pool, s)
+                                                            : cudaMallocAsync(&ws, bytes, s);
+    if (ae != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_NOMEM, "scratch allocation failed");
+        return MMQ_ERR_NOMEM;
+    }
+    const int st = launch_on<FMT, DOTS>(xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), s, fn);
     cudaFreeAsync(ws, s);  // stream-ordered: after the kernels above
     return st;
+}
+
+// ---------------------------------------------------------------- fixed scratch
+// The scratch of mmq_gemm_noalloc: a fixed array in the module's device memory, one per
+// device, whose address is looked up once per device.  The expansion kernels write
+// every byte the GEMM kernel reads (rows past M or N included), so nothing in it has to
+// start at zero and nothing is cleared between calls.
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)64 << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_ptr[64];
+
+uint8_t* noalloc_scratch(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    return g_noalloc_ptr[dev];
 }
 
 }  // namespace
@@ -621,6 +664,36 @@ int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, in
                     : launch_x<FMT_Q8_0, false>(xq, wq, M, N, K, out, dots, s, fn);
     return dots ? launch_x<FMT_Q4_K, true>(xq, wq, M, N, K, out, dots, s, fn)
                 : launch_x<FMT_Q4_K, false>(xq, wq, M, N, K, out, dots, s, fn);
+}
+
+int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                       cudaStream_t s) {
+    const char* fn = "mmq_gemm_noalloc";
+    if (K % QK_K != 0) {
+        report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
+        return MMQ_ERR_K_MULTIPLE;
+    }
+    if ((N + BN - 1) / BN > 65535 || K / QK_K > 65535) {
+        report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
+        return MMQ_ERR_SHAPE;
+    }
+    if (plan_scratch(fmt, M, N, K).total() > NOALLOC_SCRATCH_BYTES) {
+        report(fn, MMQ_ERR_SHAPE, "the fixed 64 MiB scratch is too small for this shape");
+        return MMQ_ERR_SHAPE;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaGetDevice failed");
+        return MMQ_ERR_CUDA;
+    }
+    uint8_t* ws = noalloc_scratch(dev);
+    if (!ws) {
+        report(fn, MMQ_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed");
+        return MMQ_ERR_CUDA;
+    }
+    return fmt == FMT_Q8_0 ? launch_on<FMT_Q8_0, false>(xq, wq, M, N, K, out, nullptr, ws, s, fn)
+                           : launch_on<FMT_Q4_K, false>(xq, wq, M, N, K, out, nullptr, ws, s, fn);
 }
 
 unsigned tcx_take_error() {

@@ -130,6 +130,30 @@ int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t
 int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
                               int32_t* dots, void* stream);
 
+/*
+ * The contraction of mmq_gemm_q8_0 (fmt 0) or mmq_gemm_q4_k (fmt 1) on the expanded-code
+ * tensor-core path, with its scratch taken from a fixed 64 MiB array in the library's
+ * device memory (one per device) instead of an allocation: this call allocates no device
+ * memory and calls nothing that does.  The method's pages have no counterpart of this
+ * entry point; it exists for callers that may not allocate.
+ *  - Scratch need, in bytes, with MT = ceil(M/128), NT = ceil(N/128), nb = K/32,
+ *    ng = K/256:  MT*nb*8192 + MT*ng*GA + NT*nb*8192 + NT*ng*GW, where GA = 4096 and
+ *    GW = 2048 for Q8_0, GA = 8192 and GW = 6400 for Q4_K.  A shape that needs more
+ *    than 64 MiB is refused with MMQ_ERR_SHAPE (e.g. M = 512, N = K = 3584 Q8_0 needs
+ *    about 30 MiB).  K % 256 == 0 for both formats (MMQ_ERR_K_MULTIPLE otherwise).
+ *  - The array's address is looked up (cudaGetSymbolAddress) on the first call on each
+ *    device: make that first call outside any stream capture.
+ *  - There is one array per device: two calls whose kernels overlap in time on one
+ *    device (other streams, other host threads) race on it and give wrong results.
+ *    The caller orders them.
+ *  - Nothing in the array has to start at zero: the call writes every scratch byte it
+ *    reads before reading it.
+ *  - Arguments, alignment, accuracy and the other errors as mmq_gemm_q8_0 /
+ *    mmq_gemm_q4_k; MMQ_ERR_ARG for another fmt.
+ */
+int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                     void* stream);
+
 /* Kernel selection for the two contractions and their test hooks.
  *   MMQ_PATH_AUTO   : by shape: the warp-level kernel for M <= 8 or K % 256 != 0; else
  *                     the expanded-code tensor-core path for M >= MMQ_EXPAND_MIN_M, the
