@@ -363,10 +363,19 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                 const bool block = c < GB;
                 const int k = g * GB + c, s = k % NSTAGE;  // block index = stage sequence number
                 const uint32_t gbase = sbase + L::groups + gs * L::gslot;
-                if (!DOTS && !wait_bar(bar(BAR_G_FULL + gs), (g / GR) & 1, abort, err)) break;
-                if (block && !wait_bar(bar(BAR_ST_FULL + s), (k / NSTAGE) & 1, abort, err)) break;
-                if (!wait_bar(bar(BAR_D_EMPTY + e), (n & 1) ^ 1, abort, err)) break;
-                if (!DOTS && !wait_bar(bar(BAR_OH_FULL + o), (it / OH) & 1, abort, err)) break;
+                // a barrier probe costs ~100 cycles even when the phase is complete: the group
+                // barrier is probed at this warp's first item of the group only, and the
+                // item's three probes are issued together (the slow path waits one by one)
+                if (!DOTS && (it - NMMA < g * IPG) && !wait_bar(bar(BAR_G_FULL + gs), (g / GR) & 1, abort, err))
+                    break;
+                const bool r1 = !block || ptx::mbar_test_wait(bar(BAR_ST_FULL + s), (k / NSTAGE) & 1);
+                const bool r2 = ptx::mbar_test_wait(bar(BAR_D_EMPTY + e), (n & 1) ^ 1);
+                const bool r3 = DOTS || ptx::mbar_test_wait(bar(BAR_OH_FULL + o), (it / OH) & 1);
+                if (!(r1 && r2 && r3)) {
+                    if (block && !wait_bar(bar(BAR_ST_FULL + s), (k / NSTAGE) & 1, abort, err)) break;
+                    if (!wait_bar(bar(BAR_D_EMPTY + e), (n & 1) ^ 1, abort, err)) break;
+                    if (!DOTS && !wait_bar(bar(BAR_OH_FULL + o), (it / OH) & 1, abort, err)) break;
+                }
                 ptx::tc_fence_after();
                 if (block) {
                     const uint32_t a = sbase + L::stages + s * STAGE, b = a + CHUNK;
