@@ -65,8 +65,8 @@ constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // 32 columns per epilogue warp
 constexpr int WARP_LOAD = EPI_WARPS, WARP_MMA0 = EPI_WARPS + 1, WARP_ONEHOT = WARP_MMA0 + NMMA;
 constexpr int THREADS = (WARP_ONEHOT + 1) * 32;  // 640
 constexpr int TMEM_COLS = DS * 2 * BN;           // 512
-constexpr int EXP_THREADS = 256;
-static_assert(TILE16 / 16 == EXP_THREADS, "one K = 16 tile piece per expansion thread");
+constexpr int EXP_ROWS = 32;             // rows per expansion CTA (a quarter tile)
+constexpr int EXP_THREADS = 128;
 static_assert(OH % NMMA == 0, "each issuer sees its own one-hot slots");
 
 // Group data (scratch and shared memory).  Activation side: AS, the K = 16 operand whose
@@ -96,58 +96,58 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
 // 8*((p/8)%4) .. +7 of the block: offset p*16 is that row's core-matrix row, so the
 // pieces are written in order (coalesced).
 
-// One CTA per (128-row tile, 256-value group) of the q8_1 activations.
+// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the q8_1
+// activations: rows 32h..32h+31 of a tile are row groups 4h..4h+3, i.e. a contiguous
+// 2 KiB of every chunk and 1 KiB of every K = 16 tile.
 template <int FMT>
 __global__ void __launch_bounds__(EXP_THREADS)
 k_expand_acts(const uint8_t* __restrict__ xq, int M, int nb, uint8_t* __restrict__ xa, uint8_t* __restrict__ ga) {
     constexpr int ROW = GB * Q8_1_BYTES;  // 288 bytes of one row per group
     constexpr int V = ROW / 16;           // 18
     constexpr int SROW = 304;             // 76 words: the 64-bit reads below are conflict-free
-    __shared__ __align__(16) uint8_t sm[BM * SROW];
-    const int mt = blockIdx.x, g = blockIdx.y, ng = nb / GB;
-    const int m0 = mt * BM;
+    __shared__ __align__(16) uint8_t sm[EXP_ROWS * SROW];
+    const int mt = blockIdx.x >> 2, h = blockIdx.x & 3, g = blockIdx.y, ng = nb / GB;
+    const int m0 = mt * BM + h * EXP_ROWS;
     const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
-    for (int i = threadIdx.x; i < BM * V; i += EXP_THREADS) {
+    for (int i = threadIdx.x; i < EXP_ROWS * V; i += EXP_THREADS) {
         const int r = i / V, c = i % V;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (m0 + r < M) v = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)(m0 + r) * rowbytes + (size_t)g * ROW) + c);
         *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
     }
     __syncthreads();
-    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * CHUNK;
-    for (int i = threadIdx.x; i < GB * (CHUNK / 16); i += EXP_THREADS) {
-        const int j = i / (CHUNK / 16), p = i % (CHUNK / 16);
-        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;
+    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * CHUNK + h * (CHUNK / 4);
+    constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
+    for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
+        const int j = i / PIECES, p = i % PIECES;
+        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;  // row within the quarter
         const uint8_t* src = sm + r * SROW + j * Q8_1_BYTES + 4 + 8 * kc;
         const uint2 lo = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src));
         const uint2 hi = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src + 4));
         *reinterpret_cast<uint4*>(dst + (size_t)j * CHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
-    // AS [, AM]: thread t writes piece t = (row 8*(t/16) + t%8, columns 8*((t/8)%2) .. +7)
-    uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT);
-    const int t = threadIdx.x;
+    // AS [, AM]: quarter piece t (0..63) = (row 8*(t/16) + t%8, columns 8*((t/8)%2) .. +7)
+    uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT) + h * (TILE16 / 4);
+    const int t = threadIdx.x & 63;
+    const bool second = threadIdx.x >= 64;  // threads 64..127 write AM (Q4_K)
+    if (second && FMT != FMT_Q4_K) return;
     const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
-    uint16_t as[8], am[8];
+    uint16_t v[8];
     if (kg == 0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {  // columns 0..7: the eight blocks of the group
-            const uint8_t* blk = sm + r * SROW + e * Q8_1_BYTES;
-            as[e] = *reinterpret_cast<const uint16_t*>(blk);
-            am[e] = *reinterpret_cast<const uint16_t*>(blk + 2);
-        }
+        for (int e = 0; e < 8; ++e)  // columns 0..7: d (AS) or s (AM) of the eight blocks of the group
+            v[e] = *reinterpret_cast<const uint16_t*>(sm + r * SROW + e * Q8_1_BYTES + (second ? 2 : 0));
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {  // column 8: 1.0, the Q4_K min item's row scale
-            as[e] = (e == 0 && FMT == FMT_Q4_K) ? (uint16_t)0x3C00 : (uint16_t)0;
-            am[e] = 0;
-        }
+        for (int e = 0; e < 8; ++e)  // AS column 8: 1.0, the Q4_K min item's row scale
+            v[e] = (!second && e == 0 && FMT == FMT_Q4_K) ? (uint16_t)0x3C00 : (uint16_t)0;
     }
-    *reinterpret_cast<uint4*>(gdst + t * 16) = pack8(as);
-    if (FMT == FMT_Q4_K) *reinterpret_cast<uint4*>(gdst + am_off(FMT) + t * 16) = pack8(am);
+    *reinterpret_cast<uint4*>(gdst + (second ? am_off(FMT) : 0) + t * 16) = pack8(v);
 }
 
-// One CTA per (128-row tile, 256-value group) of the weights.  FOLD: Q4_K codes are
-// q * sc_j (the contraction); without it, the raw nibbles (the block-dot test hook).
+// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the weights.  FOLD:
+// Q4_K codes are q * sc_j (the contraction); without it, the raw nibbles (the block-dot
+// test hook).
 template <int FMT, bool FOLD>
 __global__ void __launch_bounds__(EXP_THREADS)
 k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
@@ -156,11 +156,11 @@ k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restr
     constexpr int VP = V + 1;                                            // + one zero piece (Q8_0 reads 4 B past)
     constexpr int SROW = FMT == FMT_Q8_0 ? 304 : 176;
     static_assert(SROW >= VP * 16, "row pad");
-    __shared__ __align__(16) uint8_t sm[BN * SROW];
-    const int nt = blockIdx.x, g = blockIdx.y, ng = nb / GB;
-    const int n0 = nt * BN;
+    __shared__ __align__(16) uint8_t sm[EXP_ROWS * SROW];
+    const int nt = blockIdx.x >> 2, h = blockIdx.x & 3, g = blockIdx.y, ng = nb / GB;
+    const int n0 = nt * BN + h * EXP_ROWS;
     const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * Q4_K_BYTES;
-    for (int i = threadIdx.x; i < BN * VP; i += EXP_THREADS) {
+    for (int i = threadIdx.x; i < EXP_ROWS * VP; i += EXP_THREADS) {
         const int r = i / VP, c = i % VP;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (c < V && n0 + r < N)
@@ -168,10 +168,11 @@ k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restr
         *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
     }
     __syncthreads();
-    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * CHUNK;
-    for (int i = threadIdx.x; i < GB * (CHUNK / 16); i += EXP_THREADS) {
-        const int j = i / (CHUNK / 16), p = i % (CHUNK / 16);
-        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;
+    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * CHUNK + h * (CHUNK / 4);
+    constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
+    for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
+        const int j = i / PIECES, p = i % PIECES;
+        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;  // row within the quarter
         const uint8_t* row = sm + r * SROW;
         uint2 lo, hi;
         if (FMT == FMT_Q8_0) {
@@ -194,8 +195,8 @@ k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restr
             a1 &= 0x0F0F0F0Fu;
             int sc = 1, mn;
             if (FOLD) {
-                const uint32_t* h = reinterpret_cast<const uint32_t*>(row);
-                q4_k_scale_min(h[1], h[2], h[3], j, sc, mn);
+                const uint32_t* hw = reinterpret_cast<const uint32_t*>(row);
+                q4_k_scale_min(hw[1], hw[2], hw[3], j, sc, mn);
             }
             const __half2 sc2 = __half2half2(__int2half_rn(sc));
             const __half2 nsc = __half2half2(__int2half_rn(-1024 * sc));
@@ -206,9 +207,9 @@ k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restr
     }
     uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT);
     const int t = threadIdx.x;
-    // WS[c][r]: piece t = rows 8*(t%16) .. +7 of column c = t/16
-    if (t < xr(FMT) * BN / 8) {
-        const int c = t >> 4, r0 = (t & 15) * 8;
+    // WS[c][r]: piece t = rows 32h + 8*(t%4) .. +7 of column c = t/4
+    if (t < xr(FMT) * EXP_ROWS / 8) {
+        const int c = t >> 2, r0 = (t & 3) * 8;
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -218,20 +219,22 @@ k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restr
             else
                 v[e] = c < GB ? hdr[0] : (uint16_t)(hdr[1] ^ 0x8000u);  // d, or -dmin
         }
-        *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + t * 16) = pack8(v);
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + (c * BN + h * EXP_ROWS + r0) * 2) = pack8(v);
     }
-    if (FMT == FMT_Q4_K) {
-        // BMIN: piece t = (row 8*(t/16) + t%8, columns 8*((t/8)%2) .. +7), column j = m_j
-        const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
-        const uint32_t* h = reinterpret_cast<const uint32_t*>(sm + r * SROW);
+    if (FMT == FMT_Q4_K && t >= 64) {
+        // BMIN: quarter piece u = t - 64 (0..63) = (row 8*(u/16) + u%8, columns 8*((u/8)%2)
+        // .. +7), column j = m_j
+        const int u = t - 64;
+        const int r = 8 * (u >> 4) + (u & 7), kg = (u >> 3) & 1;
+        const uint32_t* hw = reinterpret_cast<const uint32_t*>(sm + r * SROW);
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             int sc, mn;
-            q4_k_scale_min(h[1], h[2], h[3], e, sc, mn);
+            q4_k_scale_min(hw[1], hw[2], hw[3], e, sc, mn);
             v[e] = kg == 0 ? __half_as_ushort(__int2half_rn(mn)) : (uint16_t)0;
         }
-        *reinterpret_cast<uint4*>(gdst + t * 16) = pack8(v);
+        *reinterpret_cast<uint4*>(gdst + h * (TILE16 / 4) + u * 16) = pack8(v);
     }
 }
 
@@ -578,12 +581,12 @@ int launch_on(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, f
     uint8_t* gw = xb + sp.xb;
     {
         ProfScope ps("k_expand_acts", s);
-        k_expand_acts<FMT><<<dim3((unsigned)MT, (unsigned)ng), EXP_THREADS, 0, s>>>(
+        k_expand_acts<FMT><<<dim3((unsigned)(4 * MT), (unsigned)ng), EXP_THREADS, 0, s>>>(
             static_cast<const uint8_t*>(xq), (int)M, nb, xa, ga);
     }
     {
         ProfScope ps("k_expand_weights", s);
-        k_expand_weights<FMT, !DOTS><<<dim3((unsigned)NT, (unsigned)ng), EXP_THREADS, 0, s>>>(
+        k_expand_weights<FMT, !DOTS><<<dim3((unsigned)(4 * NT), (unsigned)ng), EXP_THREADS, 0, s>>>(
             static_cast<const uint8_t*>(wq), (int)N, nb, xb, gw);
     }
     {
