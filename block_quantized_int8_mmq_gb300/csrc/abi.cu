@@ -50,6 +50,24 @@ int current_path() {
 }
 
 constexpr int64_t LIMIT = (int64_t)1 << 40;
+constexpr int SM_COUNT = 152;  // GB300
+
+// Path choice for MMQ_PATH_AUTO from two measured cost models (GB300, microseconds):
+// the warp-level kernel streams the weights once per 8 activation rows; the expanded
+// tensor-core path pays the code expansion (about 3 bytes of traffic per weight byte)
+// plus, per wave of 128 x 128 tiles over the SMs, one tile's pass over K (~0.34 us per
+// 32-block; Q4_K adds one min item per 8 blocks).  The converter kernel is never the
+// faster of the two and is only used when asked for.
+int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
+    if (M <= 8 || K % QK_K != 0 || !tc_available()) return MMQ_PATH_SMALL;
+    const double wbytes = (double)N * (double)mmq_weight_row_bytes(fmt, K);
+    const double t_small = (double)((M + 7) / 8) * wbytes / 1.3e6 + 3.0;
+    const double tiles = (double)((M + 127) / 128) * (double)((N + 127) / 128);
+    const double waves = (double)(int64_t)((tiles + SM_COUNT - 1) / SM_COUNT);
+    const double items = (double)(K / QK) * (fmt == FMT_Q4_K ? 9.0 / 8.0 : 1.0);
+    const double t_expand = 3.0 * wbytes / 3.0e6 + waves * items * 0.34 + 8.0;
+    return t_small < t_expand ? MMQ_PATH_SMALL : MMQ_PATH_EXPAND;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -85,15 +103,7 @@ int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int path = current_path();
-    if (path == MMQ_PATH_AUTO) {
-        // The tensor-core paths stage 256-value groups; other K go to the warp-level path.
-        if (M <= 8 || K % QK_K != 0 || !tc_available())
-            path = MMQ_PATH_SMALL;
-        else if (M >= MMQ_EXPAND_MIN_M)
-            path = MMQ_PATH_EXPAND;
-        else
-            path = MMQ_PATH_TC;
-    }
+    if (path == MMQ_PATH_AUTO) path = auto_path(fmt, M, N, K);
     if (path == MMQ_PATH_SMALL)
         st = small_launch(fmt, xq, wq, M, N, K, out, dots, s);
     else if (path == MMQ_PATH_TC)

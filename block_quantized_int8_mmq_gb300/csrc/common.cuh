@@ -2,6 +2,7 @@
 // q8_1 / Q8_0 / Q4_K layouts described in include/mmq.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -59,6 +60,8 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
 unsigned tc_take_error();
 unsigned tcx_take_error();
 unsigned small_take_error();
+bool make_byte_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                   uint32_t box_rows, int elem_bytes);
 void report(const char* fn, int status, const char* detail);
 int launch_status(const char* fn);
 

@@ -314,108 +314,361 @@ k_mmq_small_mma(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, 
     }
 }
 
-// ---------------------------------------------------------------- staged variant
-// The 16 weight rows of a CTA, and the (at most 8) activation rows, are copied into
-// shared memory piece by piece (one bulk copy per row per piece: 2176 B of Q8_0 or
-// 2304 B of Q4_K weights), so the whole tile is requested from HBM
-// at once and its latency is paid once per piece; the math then reads shared memory.
+// ---------------------------------------------------------------- dp4a row kernel
+// k_mmq_dp4a_rows: for MT <= 2 activation rows, where a tensor-core tile would waste
+// most of its 8 token columns, every block dot is formed by dp4a on the raw codes (Q4_K
+// nibbles masked to bytes, Q8_0 codes as they are): about one instruction per weight at
+// one token.  The CTA first copies its MT activation rows into shared memory,
+// reorganised for aligned 16-byte reads (codes [t][b][32], f32 xd[t][b] and xs[t][b]).
+// Each warp then streams whole weight rows: Q4_K with 8 lanes per super-block (lane i
+// reads the 16 nibble bytes 16i..16i+15, i.e. 16 values of sub-block 2(i/2) in the low
+// nibbles and of sub-block 2(i/2)+1 in the high nibbles, plus the super-block header),
+// four super-blocks per warp-wide load; Q8_0 with one 34-byte block per lane, read as
+// aligned words and funnel-shifted.  Each lane applies the block scales to its partial
+// dots at once; the warp reduces with shuffles at the end of a row.
+constexpr int DR_WARPS = 16;
+__host__ __device__ constexpr int dr_act_bytes(int mt, int nb) { return mt * nb * (QK + 8); }
+
+template <int FMT, int MT>
+__global__ void __launch_bounds__(DR_WARPS * 32)
+k_mmq_dp4a_rows(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, int M, int N, int nb, int rw,
+                float* __restrict__ out, int32_t* __restrict__ dots) {
+    extern __shared__ __align__(16) uint8_t dr_smem[];
+    uint8_t* xcodes = dr_smem;                                         // [MT][nb][32]
+    float* xdv = reinterpret_cast<float*>(dr_smem + MT * nb * QK);      // [MT][nb]
+    float* xsv = xdv + MT * nb;                                         // [MT][nb]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * MT;
+    const int ntok = min(MT, M - m0);
+    // stage the activation rows (rows past M as zeros)
+    for (int e = threadIdx.x; e < MT * nb; e += DR_WARPS * 32) {
+        const int t = e / nb, b = e % nb;
+        uint32_t h = 0u, c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (t < ntok) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((long long)(m0 + t) * nb + b) * Q8_1_BYTES);
+            h = __ldg(src);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] = __ldg(src + 1 + i);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(xcodes + (size_t)e * QK);
+        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        xdv[e] = f16_bits_to_f32(h);
+        xsv[e] = f16_bits_to_f32(h >> 16);
+    }
+    __syncthreads();
+    for (int ri = 0; ri < rw; ++ri) {
+        const long long n = ((long long)blockIdx.x * rw + ri) * DR_WARPS + warp;
+        if (n >= N) break;  // uniform per warp
+        float acc[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+        if (FMT == FMT_Q4_K) {
+            const int nsb = nb >> 3;
+            const uint8_t* row = wq + n * (long long)nsb * Q4_K_BYTES;
+            const int grp = lane >> 3, i = lane & 7, c = i >> 1, k0 = 16 * (i & 1);
+            // two super-blocks per lane per iteration: both loads are issued before the math
+            for (int sb0 = grp; sb0 < nsb; sb0 += 8) {
+                uint4 hdrs[2], wvs[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int sb = sb0 + 4 * u;
+                    if (sb < nsb) {
+                        const uint8_t* sbk = row + (long long)sb * Q4_K_BYTES;
+                        hdrs[u] = __ldg(reinterpret_cast<const uint4*>(sbk));
+                        wvs[u] = __ldg(reinterpret_cast<const uint4*>(sbk + 16 + 16 * i));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int sb = sb0 + 4 * u;
+                    if (sb >= nsb) break;
+                    const uint4 hdr = hdrs[u], wv = wvs[u];
+                    int sc0, mn0, sc1, mn1;
+                    q4_k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, mn0);
+                    q4_k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, mn1);
+                    const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+                    const float ds0 = d * (float)sc0, ds1 = d * (float)sc1;        // exact
+                    const float dm0 = -dmin * (float)mn0, dm1 = -dmin * (float)mn1;  // exact
+                    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        lo[j] = w[j] & 0x0F0F0F0Fu;
+                        hi[j] = (w[j] >> 4) & 0x0F0F0F0Fu;
+                    }
+                    const int b0 = 8 * sb + 2 * c;  // sub-block 2c; 2c + 1 is b0 + 1
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xcodes + ((size_t)t * nb + b0) * QK + k0);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xcodes + ((size_t)t * nb + b0 + 1) * QK + k0);
+                        int D0 = 0, D1 = 0;
+                        D0 = __dp4a((int)lo[0], (int)xa.x, D0);
+                        D0 = __dp4a((int)lo[1], (int)xa.y, D0);
+                        D0 = __dp4a((int)lo[2], (int)xa.z, D0);
+                        D0 = __dp4a((int)lo[3], (int)xa.w, D0);
+                        D1 = __dp4a((int)hi[0], (int)xb.x, D1);
+                        D1 = __dp4a((int)hi[1], (int)xb.y, D1);
+                        D1 = __dp4a((int)hi[2], (int)xb.z, D1);
+                        D1 = __dp4a((int)hi[3], (int)xb.w, D1);
+                        if (dots) {
+                            // the other half of each sub-block's 32 values sits in lane i ^ 1 (same
+                            // 8-lane group, hence the same trip count: the mask names that group)
+                            const unsigned grp_mask = 0xFFu << (8 * grp);
+                            const int F0 = D0 + __shfl_xor_sync(grp_mask, D0, 1);
+                            const int F1 = D1 + __shfl_xor_sync(grp_mask, D1, 1);
+                            if ((i & 1) == 0 && t < ntok) {
+                                dots[((long long)(m0 + t) * N + n) * nb + b0] = F0;
+                                dots[((long long)(m0 + t) * N + n) * nb + b0 + 1] = F1;
+                            }
+                        } else {
+                            const float2 xd = *reinterpret_cast<const float2*>(xdv + (size_t)t * nb + b0);
+                            acc[t] = fmaf(ds0 * xd.x, (float)D0, acc[t]);
+                            acc[t] = fmaf(ds1 * xd.y, (float)D1, acc[t]);
+                            if ((i & 1) == 0) {  // one of the two lanes of a sub-block pair adds the min terms
+                                const float2 xs = *reinterpret_cast<const float2*>(xsv + (size_t)t * nb + b0);
+                                acc[t] = fmaf(dm0, xs.x, acc[t]);
+                                acc[t] = fmaf(dm1, xs.y, acc[t]);
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
+            const uint8_t* row = wq + n * (long long)nb * Q8_0_BYTES;
+            for (int b = lane; b < nb; b += 32) {
+                const uint8_t* blk = row + (long long)b * Q8_0_BYTES;
+                // 34 bytes at a 2-byte alignment, read as the 9 aligned words around them
+                // (in bounds: with K % 256 == 0 the matrix's last block starts 2 bytes into a
+                // word, so its window ends with the block).  sh = 16: window = [2 bytes of
+                // the previous block | wd | codes], code word j = word j + 1.  sh = 0:
+                // window = [wd | codes | 2 bytes of the next block], a 16-bit funnel shift.
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(blk) & ~(uintptr_t)3);
+                const bool sh = (reinterpret_cast<uintptr_t>(blk) & 3) != 0;
+                uint32_t t9[9];
+#pragma unroll
+                for (int j = 0; j < 9; ++j) t9[j] = __ldg(wp + j);
+                const float wd = f16_bits_to_f32(sh ? (t9[0] >> 16) : (t9[0] & 0xffffu));
+                uint32_t cw[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) cw[j] = sh ? t9[j + 1] : __funnelshift_r(t9[j], t9[j + 1], 16);
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    const uint4* xc = reinterpret_cast<const uint4*>(xcodes + ((size_t)t * nb + b) * QK);
+                    const uint4 xa = xc[0], xb = xc[1];
+                    int D = 0;
+                    D = __dp4a((int)cw[0], (int)xa.x, D);
+                    D = __dp4a((int)cw[1], (int)xa.y, D);
+                    D = __dp4a((int)cw[2], (int)xa.z, D);
+                    D = __dp4a((int)cw[3], (int)xa.w, D);
+                    D = __dp4a((int)cw[4], (int)xb.x, D);
+                    D = __dp4a((int)cw[5], (int)xb.y, D);
+                    D = __dp4a((int)cw[6], (int)xb.z, D);
+                    D = __dp4a((int)cw[7], (int)xb.w, D);
+                    if (dots) {
+                        if (t < ntok) dots[((long long)(m0 + t) * N + n) * nb + b] = D;
+                    } else {
+                        acc[t] = fmaf(wd * xdv[(size_t)t * nb + b], (float)D, acc[t]);
+                    }
+                }
+            }
+        }
+        if (!dots) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float v = acc[t];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0 && t < ntok) out[(long long)(m0 + t) * N + n] = v;
+            }
+        }
+    }
+}
+
+template <int FMT, int MT>
+int launch_dp4a_rows(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
+                     cudaStream_t s, const char* fn) {
+    const int smem = dr_act_bytes(MT, nb);
+    static int attr_bytes = 0;
+    if (smem > 48 * 1024 && smem > attr_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(k_mmq_dp4a_rows<FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
+            return MMQ_ERR_SMEM;
+        }
+        attr_bytes = smem;
+    }
+    // rows per warp: enough CTAs for two per SM, each staging its activations once
+    const int64_t rows_per_cta_min = DR_WARPS;
+    int rw = (int)(N / (rows_per_cta_min * 2 * 152));
+    rw = rw < 1 ? 1 : (rw > 4 ? 4 : rw);
+    dim3 grid((unsigned)((N + (int64_t)DR_WARPS * rw - 1) / ((int64_t)DR_WARPS * rw)), (unsigned)((M + MT - 1) / MT));
+    {
+        ProfScope ps("k_mmq_dp4a_rows", s);
+        k_mmq_dp4a_rows<FMT, MT><<<grid, DR_WARPS * 32, smem, s>>>(x8, w8, (int)M, (int)N, nb, rw, out, dots);
+    }
+    return launch_status(fn);
+}
+
+// ---------------------------------------------------------------- streaming kernel
+// k_mmq_gemv: one CTA per R weight rows (R = 16, 32 or 64, picked so that there are
+// enough CTAs for the GPU) and up to 8 activation rows (grid.y = ceil(M/8) passes).
+// The rows' weights stream through a 3-stage ring of pieces of 32 blocks (Q8_0: 1088 B
+// per row, Q4_K: 4 super-blocks = 576 B per row): one 2-D tensor copy brings all R rows
+// of a piece (the weight matrix viewed as 8-byte elements; rows past N and blocks past
+// K arrive as zeros), 1-D bulk copies the activation rows' q8_1 blocks, so HBM reads
+// run ahead of the math with two copy operations per piece.  The 8 warps split each piece's blocks (warp w takes blocks w, w+8, ...): a
+// warp converts a block's activation codes to fp16 B fragments once and reuses them
+// for all R/16 row tiles of its mma.sync m16n8k16 (16 weight rows x 8 tokens, k
+// permuted identically in both operands so that a thread's 8 values of a block are 8
+// contiguous bytes).  Q4_K sub-scales and sub-mins are decoded once per (row,
+// super-block) and piece into a shared table of f32 (d*sc, dmin*m).  Each warp holds
+// partial sums for all R rows; the warps reduce through shared memory at the end.
 // Needs K % 256 == 0 (whole 16-byte aligned pieces of both formats).
 
 __device__ unsigned int g_small_error;
 
-constexpr int ST_WARPS = 16;
-__host__ __device__ constexpr int st_piece_blocks(int fmt) {  // 32-blocks of K per piece
-    return fmt == FMT_Q8_0 ? 64 : 128;
+constexpr int GV_WARPS = 8;
+constexpr int GV_STAGES = 3;
+constexpr uint64_t GV_WAIT_LIMIT_NS = 2000000000ull;
+__host__ __device__ constexpr int gv_piece_blocks(int fmt) { return 32; }
+__host__ __device__ constexpr int gv_piece_bytes(int fmt) {  // weight bytes of one row per piece
+    return fmt == FMT_Q8_0 ? gv_piece_blocks(fmt) * Q8_0_BYTES : gv_piece_blocks(fmt) / 8 * Q4_K_BYTES;
 }
-constexpr uint64_t ST_WAIT_LIMIT_NS = 2000000000ull;
-
-__host__ __device__ constexpr int st_piece_bytes(int fmt) {
-    return fmt == FMT_Q8_0 ? st_piece_blocks(fmt) * Q8_0_BYTES : st_piece_blocks(fmt) / 8 * Q4_K_BYTES;
+// activation bytes per token per piece in shared memory, padded by 16 B so that the 8
+// token rows start in different banks
+__host__ __device__ constexpr int gv_act_stride(int fmt) { return gv_piece_blocks(fmt) * Q8_1_BYTES + 16; }
+__host__ __device__ constexpr int gv_stage_bytes(int fmt, int R) { return R * gv_piece_bytes(fmt) + 8 * gv_act_stride(fmt); }
+__host__ __device__ constexpr int gv_table_bytes(int fmt, int R) { return fmt == FMT_Q4_K ? R * gv_piece_blocks(fmt) * 8 : 0; }
+__host__ __device__ constexpr int gv_smem_bytes(int fmt, int R) {
+    return GV_STAGES * gv_stage_bytes(fmt, R) + gv_table_bytes(fmt, R) + GV_WARPS * R * 8 * 4 + 2 * GV_STAGES * 8 + 16;
 }
 
-// bytes of activation row data per token per piece in shared memory (padded by 16 B
-// so that the 8 token rows start in different banks)
-__host__ __device__ constexpr int st_act_stride(int fmt) { return st_piece_blocks(fmt) * Q8_1_BYTES + 16; }
-__host__ __device__ constexpr int st_smem_bytes(int fmt) {
-    return 16 * st_piece_bytes(fmt) + 8 * st_act_stride(fmt) + ST_WARPS * 16 * 8 * 4 + 16;
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(ST_WARPS * 32, 2)
-k_mmq_small_staged(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, int M, int N, int nb,
-                   float* __restrict__ out, int32_t* __restrict__ dots) {
-    constexpr int PB = st_piece_bytes(FMT);
-    constexpr int PBLK = st_piece_blocks(FMT);
-    constexpr int AS = st_act_stride(FMT);
-    extern __shared__ __align__(128) uint8_t st_smem[];
-    uint8_t* tile = st_smem;                                   // [16 rows][PB]
-    uint8_t* act = st_smem + 16 * PB;                          // [8 tokens][AS]
-    float(*red)[16][8] = reinterpret_cast<float(*)[16][8]>(act + 8 * AS);
-    const uint32_t bar = ptx::smem_u32(act + 8 * AS + ST_WARPS * 16 * 8 * 4);
+template <int FMT, int R>
+__global__ void __launch_bounds__(GV_WARPS * 32)
+k_mmq_gemv(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ xq, int M, int N, int nb,
+           float* __restrict__ out, int32_t* __restrict__ dots) {
+    constexpr int RT = R / 16;  // mma row tiles per warp
+    constexpr int PBLK = gv_piece_blocks(FMT), PB = gv_piece_bytes(FMT), AS = gv_act_stride(FMT);
+    constexpr int SB = gv_stage_bytes(FMT, R);
+    extern __shared__ __align__(128) uint8_t gv_smem[];
+    float2* table = reinterpret_cast<float2*>(gv_smem + GV_STAGES * SB);                    // [R][PBLK]
+    float(*red)[R][8] = reinterpret_cast<float(*)[R][8]>(gv_smem + GV_STAGES * SB + gv_table_bytes(FMT, R));
+    const uint32_t bar0 = ptx::smem_u32(gv_smem + GV_STAGES * SB + gv_table_bytes(FMT, R) + GV_WARPS * R * 8 * 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int n0 = blockIdx.x * 16, m0 = blockIdx.y * 8;
-    const int nrows = min(16, N - n0), ntok = min(8, M - m0);
-    const int t0 = 2 * q, t1 = t0 + 1;                         // D-fragment tokens (local)
-    const long long row_bytes = FMT == FMT_Q8_0 ? (long long)nb * Q8_0_BYTES : (long long)(nb >> 3) * Q4_K_BYTES;
+    const int n0 = blockIdx.x * R, m0 = blockIdx.y * 8;
+    const int nrows = min(R, N - n0), ntok = min(8, M - m0);
+    const int t0 = 2 * q, t1 = t0 + 1;  // D-fragment tokens (local)
     const long long xrow_bytes = (long long)nb * Q8_1_BYTES;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int npieces = (nb + PBLK - 1) / PBLK;
+    float acc[RT][4];
+#pragma unroll
+    for (int r = 0; r < RT; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+
+    auto issue = [&](int p) {  // thread 0: the copies of piece p into stage p % GV_STAGES
+        const int kb0 = p * PBLK, pb = min(PBLK, nb - kb0);
+        const uint32_t abytes = (uint32_t)pb * Q8_1_BYTES;
+        uint8_t* st = gv_smem + (p % GV_STAGES) * SB;
+        const uint32_t bar = bar0 + 8 * (p % GV_STAGES);
+        // the tensor copy counts its whole box, zero-filled parts included
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)(R * PB) + abytes * (uint32_t)ntok);
+        ptx::tma_load_2d(ptx::smem_u32(st), &tmW, bar, p * (PB / 8), n0);
+        for (int t = 0; t < ntok; ++t)
+            ptx::bulk_load(ptx::smem_u32(st + R * PB + t * AS),
+                           xq + (long long)(m0 + t) * xrow_bytes + (long long)kb0 * Q8_1_BYTES, abytes, bar);
+    };
+    int issued = 0;  // thread 0: pieces whose copies were issued
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar, 1);
+        ptx::tma_prefetch_desc(&tmW);
+        for (int i = 0; i < GV_STAGES; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
         ptx::fence_barrier_init();
+        for (; issued < GV_STAGES - 1 && issued < npieces; ++issued) issue(issued);
     }
     __syncthreads();
     bool ok = true;
-    const int npieces = (nb + PBLK - 1) / PBLK;
-    for (int p = 0; p < npieces && ok; ++p) {
-        const int kb0 = p * PBLK, pb = min(PBLK, nb - kb0);
-        const uint32_t bytes = FMT == FMT_Q8_0 ? (uint32_t)pb * Q8_0_BYTES : (uint32_t)(pb >> 3) * Q4_K_BYTES;
-        const long long off = FMT == FMT_Q8_0 ? (long long)kb0 * Q8_0_BYTES : (long long)(kb0 >> 3) * Q4_K_BYTES;
-        const uint32_t abytes = (uint32_t)pb * Q8_1_BYTES;
-        if (threadIdx.x == 0) {
-            ptx::mbar_arrive_expect_tx(bar, bytes * (uint32_t)nrows + abytes * (uint32_t)ntok);
-            for (int r = 0; r < nrows; ++r)
-                ptx::bulk_load(ptx::smem_u32(tile + r * PB), wq + (long long)(n0 + r) * row_bytes + off, bytes, bar);
-            for (int t = 0; t < ntok; ++t)
-                ptx::bulk_load(ptx::smem_u32(act + t * AS), xq + (long long)(m0 + t) * xrow_bytes + (long long)kb0 * Q8_1_BYTES,
-                               abytes, bar);
-        }
-        if (!ptx::mbar_try_wait(bar, p & 1)) {
+    for (int p = 0; p < npieces; ++p) {
+        // the stage of piece p + 2 was freed by the __syncthreads that ended piece p - 1
+        if (threadIdx.x == 0 && issued < npieces) issue(issued++);
+        const uint32_t bar = bar0 + 8 * (p % GV_STAGES);
+        const uint32_t parity = (p / GV_STAGES) & 1;
+        if (!ptx::mbar_try_wait(bar, parity)) {
             const uint64_t t_start = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(bar, p & 1)) {
-                if (ptx::globaltimer_ns() - t_start > ST_WAIT_LIMIT_NS) {
+            while (!ptx::mbar_try_wait(bar, parity)) {
+                if (ptx::globaltimer_ns() - t_start > GV_WAIT_LIMIT_NS) {
                     atomicOr(&g_small_error, ERR_TIMEOUT);
                     ok = false;
                     break;
                 }
             }
         }
-        if (!ok) break;
-        const int rg0 = min(g, nrows - 1), rg1 = min(g + 8, nrows - 1);  // rows past N read row nrows-1 (discarded)
-        for (int c = warp; 2 * c < pb; c += ST_WARPS) {
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* tile = gv_smem + (p % GV_STAGES) * SB;
+        const uint8_t* act = tile + R * PB;
+        const int kb0 = p * PBLK, pb = min(PBLK, nb - kb0);
+        if (FMT == FMT_Q4_K && !dots) {
+            // (d*sc_j, dmin*m_j) of every (row, sub-block) of the piece, once
+            for (int e = threadIdx.x; e < R * (PBLK / 8); e += GV_WARPS * 32) {
+                const int r = e / (PBLK / 8), sbi = e % (PBLK / 8);
+                if (8 * sbi >= pb) continue;
+                const uint4 h = *reinterpret_cast<const uint4*>(tile + r * PB + sbi * Q4_K_BYTES);
+                const float d = f16_bits_to_f32(h.x), dmin = f16_bits_to_f32(h.x >> 16);
 #pragma unroll
-            for (int sb = 0; sb < 2; ++sb) {
-                const int bl = 2 * c + sb, b = kb0 + bl;     // block within the piece / within the row
+                for (int j = 0; j < 8; ++j) {
+                    int sc, mn;
+                    q4_k_scale_min(h.y, h.z, h.w, j, sc, mn);
+                    table[r * PBLK + 8 * sbi + j] = make_float2(d * (float)sc, dmin * (float)mn);  // exact
+                }
+            }
+            __syncthreads();
+        }
+        for (int bl = warp; bl < pb; bl += GV_WARPS) {
+            const int b = kb0 + bl;  // block index within the row
+            // activation B fragments of token g (zeros past ntok), reused for every row tile
+            uint32_t xw0 = 0u, xw1 = 0u;
+            if (g < ntok) {
+                const uint32_t* xc = reinterpret_cast<const uint32_t*>(act + g * AS + bl * Q8_1_BYTES + 4 + 8 * q);
+                xw0 = xc[0];
+                xw1 = xc[1];
+            }
+            uint32_t b_lo0, b_lo1, b_hi0, b_hi1;
+            s8x4_h2(xw0, b_lo0, b_lo1);
+            s8x4_h2(xw1, b_hi0, b_hi1);
+            float xd0 = 0.f, xs0 = 0.f, xd1 = 0.f, xs1 = 0.f;
+            if (!dots) {
+                const uint32_t h0 = t0 < ntok ? *reinterpret_cast<const uint32_t*>(act + t0 * AS + bl * Q8_1_BYTES) : 0u;
+                const uint32_t h1 = t1 < ntok ? *reinterpret_cast<const uint32_t*>(act + t1 * AS + bl * Q8_1_BYTES) : 0u;
+                xd0 = f16_bits_to_f32(h0);
+                xs0 = f16_bits_to_f32(h0 >> 16);
+                xd1 = f16_bits_to_f32(h1);
+                xs1 = f16_bits_to_f32(h1 >> 16);
+            }
+#pragma unroll
+            for (int rt = 0; rt < RT; ++rt) {
                 uint32_t a_lo[4], a_hi[4];
                 float ws[2], wm[2];
-                const int rr[2] = {rg0, rg1};
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const uint8_t* rowp = tile + rr[i] * PB;
+                    const int r = 16 * rt + g + 8 * i;  // rows past N are zeros; their sums are never stored
+                    const uint8_t* rowp = tile + r * PB;
                     if (FMT == FMT_Q4_K) {
                         const uint8_t* sbk = rowp + (bl >> 3) * Q4_K_BYTES;
                         const uint2 wv = *reinterpret_cast<const uint2*>(sbk + 16 + 32 * ((bl >> 1) & 3) + 8 * q);
-                        const int shift = 4 * sb;
+                        const int shift = 4 * (bl & 1);
                         u4x4_h2((wv.x >> shift) & 0x0F0F0F0Fu, a_lo[i], a_lo[i + 2]);
                         u4x4_h2((wv.y >> shift) & 0x0F0F0F0Fu, a_hi[i], a_hi[i + 2]);
-                        const uint4 h = *reinterpret_cast<const uint4*>(sbk);
-                        int sc, mn;
-                        q4_k_scale_min(h.y, h.z, h.w, b & 7, sc, mn);
-                        ws[i] = f16_bits_to_f32(h.x) * (float)sc;
-                        wm[i] = f16_bits_to_f32(h.x >> 16) * (float)mn;
+                        if (!dots) {
+                            const float2 t = table[r * PBLK + bl];
+                            ws[i] = t.x;
+                            wm[i] = t.y;
+                        }
                     } else {
                         const uint8_t* blk = rowp + bl * Q8_0_BYTES;
-                        const int o = 2 + 8 * q + (bl & 1) * 2;     // byte offset of the codes, mod 4
+                        const int o = 2 + 8 * q + (bl & 1) * 2;  // byte offset of the codes, mod 4
                         const uint32_t* a = reinterpret_cast<const uint32_t*>(blk + 2 + 8 * q - (o & 2));
                         uint32_t w0 = a[0], w1 = a[1];
                         if (o & 2) {
@@ -425,71 +678,72 @@ k_mmq_small_staged(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ w
                         }
                         s8x4_h2(w0, a_lo[i], a_lo[i + 2]);
                         s8x4_h2(w1, a_hi[i], a_hi[i + 2]);
-                        ws[i] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(blk));
+                        ws[i] = dots ? 0.f : f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(blk));
                         wm[i] = 0.f;
                     }
                 }
-                uint32_t xw0 = 0u, xw1 = 0u;
-                if (g < ntok) {
-                    const uint32_t* xc = reinterpret_cast<const uint32_t*>(act + g * AS + bl * Q8_1_BYTES + 4 + 8 * q);
-                    xw0 = xc[0];
-                    xw1 = xc[1];
-                }
-                uint32_t b_lo0, b_lo1, b_hi0, b_hi1;
-                s8x4_h2(xw0, b_lo0, b_lo1);
-                s8x4_h2(xw1, b_hi0, b_hi1);
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
                 mma16816(d, a_lo, b_lo0, b_lo1);
                 mma16816(d, a_hi, b_hi0, b_hi1);
                 if (dots) {
-                    const int rw[2] = {n0 + g, n0 + g + 8}, tt[2] = {m0 + t0, m0 + t1};
+                    const int rw[2] = {n0 + 16 * rt + g, n0 + 16 * rt + g + 8}, tt[2] = {m0 + t0, m0 + t1};
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         if (rw[e >> 1] < N && tt[e & 1] < M)
                             dots[((long long)tt[e & 1] * N + rw[e >> 1]) * nb + b] = __float2int_rn(d[e]);
                 } else {
-                    const uint32_t h0 = t0 < ntok ? *reinterpret_cast<const uint32_t*>(act + t0 * AS + bl * Q8_1_BYTES) : 0u;
-                    const uint32_t h1 = t1 < ntok ? *reinterpret_cast<const uint32_t*>(act + t1 * AS + bl * Q8_1_BYTES) : 0u;
-                    const float xd0 = f16_bits_to_f32(h0), xs0 = f16_bits_to_f32(h0 >> 16);
-                    const float xd1 = f16_bits_to_f32(h1), xs1 = f16_bits_to_f32(h1 >> 16);
-                    acc[0] = fmaf(xd0 * ws[0], d[0], acc[0]);
-                    acc[1] = fmaf(xd1 * ws[0], d[1], acc[1]);
-                    acc[2] = fmaf(xd0 * ws[1], d[2], acc[2]);
-                    acc[3] = fmaf(xd1 * ws[1], d[3], acc[3]);
+                    acc[rt][0] = fmaf(xd0 * ws[0], d[0], acc[rt][0]);
+                    acc[rt][1] = fmaf(xd1 * ws[0], d[1], acc[rt][1]);
+                    acc[rt][2] = fmaf(xd0 * ws[1], d[2], acc[rt][2]);
+                    acc[rt][3] = fmaf(xd1 * ws[1], d[3], acc[rt][3]);
                     if (FMT == FMT_Q4_K) {
-                        acc[0] = fmaf(-wm[0], xs0, acc[0]);
-                        acc[1] = fmaf(-wm[0], xs1, acc[1]);
-                        acc[2] = fmaf(-wm[1], xs0, acc[2]);
-                        acc[3] = fmaf(-wm[1], xs1, acc[3]);
+                        acc[rt][0] = fmaf(-wm[0], xs0, acc[rt][0]);
+                        acc[rt][1] = fmaf(-wm[0], xs1, acc[rt][1]);
+                        acc[rt][2] = fmaf(-wm[1], xs0, acc[rt][2]);
+                        acc[rt][3] = fmaf(-wm[1], xs1, acc[rt][3]);
                     }
                 }
             }
         }
-        __syncthreads();  // every warp is done with the tile before the next piece lands
+        __syncthreads();  // every warp is done with the stage and the table
     }
-    if (dots || !ok) return;
-    red[warp][g][2 * q] = acc[0];
-    red[warp][g][2 * q + 1] = acc[1];
-    red[warp][g + 8][2 * q] = acc[2];
-    red[warp][g + 8][2 * q + 1] = acc[3];
+    if (!ok) {
+        // copies of the pieces still in flight must land before the CTA exits
+        if (threadIdx.x == 0)
+            for (int p = issued - GV_STAGES < 0 ? 0 : issued - GV_STAGES; p < issued; ++p) {
+                const uint64_t t_start = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(bar0 + 8 * (p % GV_STAGES), (p / GV_STAGES) & 1))
+                    if (ptx::globaltimer_ns() - t_start > GV_WAIT_LIMIT_NS) break;
+            }
+        return;
+    }
+    if (dots) return;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+        red[warp][16 * rt + g][t0] = acc[rt][0];
+        red[warp][16 * rt + g][t1] = acc[rt][1];
+        red[warp][16 * rt + g + 8][t0] = acc[rt][2];
+        red[warp][16 * rt + g + 8][t1] = acc[rt][3];
+    }
     __syncthreads();
-    if (threadIdx.x < 128) {
-        const int rr = threadIdx.x >> 3, tt = threadIdx.x & 7;
+    for (int e = threadIdx.x; e < R * 8; e += GV_WARPS * 32) {
+        const int rr = e >> 3, tt = e & 7;
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < ST_WARPS; ++w) v += red[w][rr][tt];
-        if (n0 + rr < N && m0 + tt < M) out[(long long)(m0 + tt) * N + n0 + rr] = v;
+        for (int w = 0; w < GV_WARPS; ++w) v += red[w][rr][tt];
+        if (rr < nrows && tt < ntok) out[(long long)(m0 + tt) * N + n0 + rr] = v;
     }
 }
 
-template <int FMT>
-int launch_staged(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
-                  cudaStream_t s) {
-    const char* fn = FMT == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
+static_assert(gv_smem_bytes(FMT_Q4_K, 64) <= 227 * 1024 && gv_smem_bytes(FMT_Q8_0, 32) <= 227 * 1024, "smem");
+
+template <int FMT, int R>
+int launch_gemv_r(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
+                  cudaStream_t s, const char* fn) {
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_small_staged<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             st_smem_bytes(FMT));
+        cudaError_t e = cudaFuncSetAttribute(k_mmq_gemv<FMT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             gv_smem_bytes(FMT, R));
         if (e != cudaSuccess) {
             cudaGetLastError();
             report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
@@ -497,12 +751,32 @@ int launch_staged(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, in
         }
         attr_done = true;
     }
-    dim3 grid((unsigned)((N + 15) / 16), (unsigned)((M + 7) / 8));
+    CUtensorMap tm;
+    const uint64_t row_bytes = FMT == FMT_Q8_0 ? (uint64_t)nb * Q8_0_BYTES : (uint64_t)(nb / 8) * Q4_K_BYTES;
+    if (!make_byte_map(&tm, w8, row_bytes, (uint64_t)N, gv_piece_bytes(FMT), R, 8)) {
+        report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
+        return MMQ_ERR_CUDA;
+    }
+    dim3 grid((unsigned)((N + R - 1) / R), (unsigned)((M + 7) / 8));
     {
-        ProfScope ps("k_mmq_small_staged", s);
-        k_mmq_small_staged<FMT><<<grid, ST_WARPS * 32, st_smem_bytes(FMT), s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
+        ProfScope ps("k_mmq_gemv", s);
+        k_mmq_gemv<FMT, R><<<grid, GV_WARPS * 32, gv_smem_bytes(FMT, R), s>>>(tm, x8, (int)M, (int)N, nb, out, dots);
     }
     return launch_status(fn);
+}
+
+// Rows per CTA: the most (fewest activation conversions per weight) that still gives
+// about two CTAs per SM.
+template <int FMT>
+int launch_gemv(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
+                cudaStream_t s) {
+    const char* fn = FMT == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
+    const int64_t passes = (M + 7) / 8;
+    // (Q8_0 pieces are twice as long: 64 rows of them would not fit three stages)
+    if (FMT == FMT_Q4_K && passes * ((N + 63) / 64) >= 2 * 152)
+        return launch_gemv_r<FMT, 64>(x8, w8, M, N, nb, out, dots, s, fn);
+    if (passes * ((N + 31) / 32) >= 2 * 152) return launch_gemv_r<FMT, 32>(x8, w8, M, N, nb, out, dots, s, fn);
+    return launch_gemv_r<FMT, 16>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
 }  // namespace
@@ -527,9 +801,19 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     }
     const uint8_t* x8 = static_cast<const uint8_t*>(xq);
     const uint8_t* w8 = static_cast<const uint8_t*>(wq);
+    // one or two activation rows: dp4a rows (a tensor tile would waste 6 of its 8 token
+    // columns); 3 to 8 rows: the tensor-core stream (measured crossover)
+    if (nb % 8 == 0 && M <= 2 && dr_act_bytes(2, nb) <= 200 * 1024) {
+        const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
+        if (fmt == FMT_Q8_0)
+            return M <= 1 ? launch_dp4a_rows<FMT_Q8_0, 1>(x8, w8, M, N, nb, out, dots, s, fn)
+                          : launch_dp4a_rows<FMT_Q8_0, 2>(x8, w8, M, N, nb, out, dots, s, fn);
+        return M <= 1 ? launch_dp4a_rows<FMT_Q4_K, 1>(x8, w8, M, N, nb, out, dots, s, fn)
+                      : launch_dp4a_rows<FMT_Q4_K, 2>(x8, w8, M, N, nb, out, dots, s, fn);
+    }
     if (nb % 8 == 0)
-        return fmt == FMT_Q8_0 ? launch_staged<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s)
-                               : launch_staged<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s);
+        return fmt == FMT_Q8_0 ? launch_gemv<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s)
+                               : launch_gemv<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s);
     if (nb % 2 == 0) {
         dim3 g2((unsigned)((N + 15) / 16), (unsigned)((M + 7) / 8));
         ProfScope ps("k_mmq_small_mma", s);
