@@ -77,6 +77,23 @@ def load_peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's timed-region length (the job's wall time): an all-reduce MAX
+    over the process group (NCCL on GPUs, gloo on the CPU), or ms itself for one rank."""
+    if world == 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, world: int, ms_max: float, scale: float) -> float:
+    """Units processed by all ranks (each rank a replica doing units_per_step per step)
+    divided by the slowest rank's time, in units of `scale` per second."""
+    return units_per_step * steps * world / (ms_max / 1e3) / scale
+
+
 def auto_steps(step, warmup, stream, torch):
     """Steps for about TARGET_TIMED_S of device time, from a short eager estimate."""
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -363,17 +380,13 @@ def run_ours(args, rank, world, local):
     for k, (n, t) in prof.items():
         kernels[k]["share"] = (t / sum(c for _, c in graphs)) / step_kernel_ms
 
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
 
     ops = 2.0 * M * N * K
     peaks = load_peaks()
     if quant_only:
         qbytes = x.nbytes + xq_bytes
-        value = qbytes * steps * world / (ms_max / 1e3) / 1e9
+        value = whole_job_rate(qbytes, steps, world, ms_max, 1e9)
         unit = "GB/s"
         metric = "q8_1 quantize GB/s (algorithmic bytes: 4 B in + 1.125 B out per value)"
         kname = "k_quantize_q8_1"
@@ -382,7 +395,7 @@ def run_ours(args, rank, world, local):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload),
                 "kernel": kname, "peak_source": peaks["source"] + " hbm_gbs"}
     else:
-        value = ops * steps * world / (ms_max / 1e3) / 1e12
+        value = whole_job_rate(ops, steps, world, ms_max, 1e12)
         unit = "TOPS"
         metric = "MMQ int8 TOPS (2*M*N*K per step: quantize + GEMM)"
         gk = {k: v for k, v in kernels.items() if k.startswith("k_mmq")}
