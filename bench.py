@@ -115,7 +115,7 @@ KERNEL_SOURCES = {
     "k_mmq_tcx": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
     "k_expand_acts": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
     "k_expand_weights": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
-    "k_mmq_dp4a_rows": ("gemm_small.cu",) + _COMMON_SRC,
+    "k_mmq_dp4a_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_gemv": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small_mma": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small": ("gemm_small.cu",) + _COMMON_SRC,
@@ -528,24 +528,28 @@ def run_layer(args):
 
 
 def run_sweep(args):
-    """M sweep on the 3584x3584 Q4_K projection, plus M = 1 and 8 on the 18944x3584 and
-    3584x18944 projections: one line per case (quantize excluded: the GEMM is timed
-    alone, through CUDA events on the launching stream)."""
+    """M sweep on the 3584x3584 Q4_K projection, plus the small-M cases (M = 1, 2, 4, 8)
+    on the 18944x3584 and 3584x18944 projections in both weight formats: one line per
+    case (quantize excluded: the GEMM is timed alone, through CUDA events on the
+    launching stream)."""
     import torch
     import block_quantized_int8_mmq_gb300 as mmq
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
     lines = []
-    cases = [(M, 3584, 3584, "q") for M in synth.M_SWEEP]
+    cases = [("q4_k", M, 3584, 3584, "q") for M in synth.M_SWEEP]
     # small M on the larger projections too: a 7 MB weight is below the size at which any
     # kernel on this GPU streams at full HBM bandwidth
-    cases += [(M, 18944, 3584, "gate") for M in (1, 8)] + [(M, 3584, 18944, "down") for M in (1, 8)]
+    for fmt in ("q4_k", "q8_0"):
+        cases += [(fmt, M, 18944, 3584, "gate") for M in (1, 2, 4, 8)]
+        cases += [(fmt, M, 3584, 18944, "down") for M in (1, 2, 4, 8)]
     wcache = {}
-    for (M, N, K, proj) in cases:
-        if proj not in wcache:
+    for (fmt, M, N, K, proj) in cases:
+        if (fmt, proj) not in wcache:
             wcache.clear()
-            wcache[proj] = synth.layer_weights(0, proj, N, K)
-        w = wcache[proj]
+            wcache[(fmt, proj)] = (synth.layer_weights(0, proj, N, K) if fmt == "q4_k"
+                                   else synth.weights(fmt, synth.substream(synth.BASE_SEED + 5, N + K), N, K))
+        w = wcache[(fmt, proj)]
         x = synth.activations(synth.substream(synth.BASE_SEED + 4, 7000 + M), M, K, True)
         wbytes = w.nbytes
         copies = max(2, -(-3 * L2_BYTES // (wbytes + x.nbytes)))
@@ -556,7 +560,7 @@ def run_sweep(args):
         stream = torch.cuda.current_stream(dev)
         iters = max(20, args.steps)
         for i in range(args.warmup):
-            mmq.mmq_gemm_q4_k(xq, ws[i % copies], M, N, K, out, stream)
+            mmq.gemm(fmt, xq, ws[i % copies], M, N, K, out, stream)
         torch.cuda.synchronize(dev)
         path = mmq.mmq_last_path()
         # the timed launches are captured in one CUDA graph, so the gaps between
@@ -564,7 +568,7 @@ def run_sweep(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(iters):
-                mmq.mmq_gemm_q4_k(xq, ws[i % copies], M, N, K, out)
+                mmq.gemm(fmt, xq, ws[i % copies], M, N, K, out)
         graph.replay()
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -578,14 +582,15 @@ def run_sweep(args):
         abytes = wbytes + xq.numel() + M * N * 4
         gbs = abytes / (ms / 1e3) / 1e9
         tops = ops / (ms / 1e3) / 1e12
-        lines.append({"M": M, "N": N, "K": K, "ms": ms, "tops": tops, "gbs": gbs, "tok_per_s": M / (ms / 1e3),
-                      "path": PATH_NAMES.get(path, "?"),
+        lines.append({"fmt": fmt, "M": M, "N": N, "K": K, "ms": ms, "tops": tops, "gbs": gbs,
+                      "tok_per_s": M / (ms / 1e3), "path": PATH_NAMES.get(path, "?"),
                       "frac_hbm": gbs / peaks["hbm_gbs"], "frac_tensor": tops / peaks["bf16_tflops"],
                       "algorithmic_bytes": abytes})
         del ws
-    return {"metric": "Q4_K MMQ 3584x3584 M sweep (GEMM only)", "unit": "mixed", "lines": lines,
+    return {"metric": "MMQ M sweep (GEMM only)", "unit": "mixed", "lines": lines,
             "data": "synthetic (seeded)", "peaks": peaks,
-            "config": {"workload": "3584x3584 Q4_K projection, M in " + str(synth.M_SWEEP),
+            "config": {"workload": "3584x3584 Q4_K projection, M in " + str(synth.M_SWEEP)
+                                   + "; M in [1, 2, 4, 8] on 18944x3584 and 3584x18944, Q4_K and Q8_0",
                        "l2": "rotating weight copies >= 3x L2", "cuda_graph": True}}
 
 

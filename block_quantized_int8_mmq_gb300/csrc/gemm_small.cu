@@ -25,6 +25,8 @@
 // of a batch of chunks (codes, scale headers, activation codes and scales) before any
 // math, so the DRAM latency is paid once per batch; the warps reduce through shared
 // memory at the end.
+#include <algorithm>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -314,35 +316,119 @@ k_mmq_small_mma(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, 
     }
 }
 
-// ---------------------------------------------------------------- dp4a row kernel
-// k_mmq_dp4a_rows: for MT <= 2 activation rows, where a tensor-core tile would waste
+// ---------------------------------------------------------------- dp4a stream kernel
+// k_mmq_dp4a_stream: for MT <= 2 activation rows, where a tensor-core tile would waste
 // most of its 8 token columns, every block dot is formed by dp4a on the raw codes (Q4_K
-// nibbles masked to bytes, Q8_0 codes as they are): about one instruction per weight at
-// one token.  The CTA first copies its MT activation rows into shared memory,
-// reorganised for aligned 16-byte reads (codes [t][b][32], f32 xd[t][b] and xs[t][b]).
-// Each warp then streams whole weight rows: Q4_K with 8 lanes per super-block (lane i
-// reads the 16 nibble bytes 16i..16i+15, i.e. 16 values of sub-block 2(i/2) in the low
-// nibbles and of sub-block 2(i/2)+1 in the high nibbles, plus the super-block header),
-// four super-blocks per warp-wide load; Q8_0 with one 34-byte block per lane, read as
-// aligned words and funnel-shifted.  Each lane applies the block scales to its partial
-// dots at once; the warp reduces with shuffles at the end of a row.
-constexpr int DR_WARPS = 16;
-__host__ __device__ constexpr int dr_act_bytes(int mt, int nb) { return mt * nb * (QK + 8); }
+// nibbles masked to bytes, Q8_0 codes as they are).  The kernel is a set of independent
+// weight streams, one per warp, sized so that all CTAs are resident at once: warp gw of
+// tw owns the rows gw, gw + tw, ..., and walks them in pieces of up to 16 Q4_K
+// super-blocks (2304 B) or 64 Q8_0 blocks (2176 B), each one 1-D bulk async copy into
+// the warp's own ring of four slots.  With 16 warps per SM that keeps about 64 copies
+// (~150 KB) in flight per SM, enough to cover the HBM latency ("When Does a Kernel Win
+// Surface?", sec. "A bottleneck taxonomy": the decode regime is bound by the weight
+// bytes); more, smaller copies per SM were measured to stream slower.
+//
+// A lane owns whole 32-blocks, so each block dot is complete in one lane and its scale
+// is applied right there (the per-32-block rescale in registers):
+//   Q4_K: lanes 2s and 2s + 1 take super-block s of the piece, halves h = 0 / 1, i.e.
+//         nibble chunks 2h and 2h + 1 (sub-blocks 4h .. 4h + 3).  The four 6-bit
+//         sub-scales and sub-mins of a half are unpacked byte-parallel from the 12 scale
+//         bytes (one word each), the nibbles masked to bytes, and each sub-block adds
+//         (d*sc_j * xd) * D - (dmin*m_j) * xs.
+//   Q8_0: lane l takes blocks 2l and 2l + 1 (68 bytes at a 4-byte aligned offset, read
+//         as 17 words; the first block's codes are funnel-shifted by 16 bits).
+// The CTA first copies its MT activation rows into shared memory with 16 bytes of
+// padding after every 4 blocks (block b at (b / 4) * 144 + (b % 4) * 32), so that the
+// 16-byte reads of lanes 4 or 2 blocks apart fall in distinct banks; f32 xd and xs are
+// stored beside them.  The warp reduces with shuffles at the end of a row.
+__device__ unsigned int g_small_error;
 
-template <int FMT, int MT>
-__global__ void __launch_bounds__(DR_WARPS * 32)
-k_mmq_dp4a_rows(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, int M, int N, int nb, int rw,
-                float* __restrict__ out, int32_t* __restrict__ dots) {
-    extern __shared__ __align__(16) uint8_t dr_smem[];
-    uint8_t* xcodes = dr_smem;                                         // [MT][nb][32]
-    float* xdv = reinterpret_cast<float*>(dr_smem + MT * nb * QK);      // [MT][nb]
-    float* xsv = xdv + MT * nb;                                         // [MT][nb]
+constexpr int DS_WARPS = 8;
+constexpr int DS_SLOT = 16 * Q4_K_BYTES;  // 2304 B; a Q8_0 piece is 64 * 34 = 2176 B
+constexpr uint64_t DS_WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint32_t DS_SLEEP_NS = 2000;    // suspend hint of one barrier poll
+__host__ __device__ constexpr int ds_piece_units(int fmt) { return fmt == FMT_Q4_K ? 16 : 64; }
+__host__ __device__ constexpr int ds_unit_bytes(int fmt) { return fmt == FMT_Q4_K ? Q4_K_BYTES : Q8_0_BYTES; }
+__host__ __device__ constexpr int ds_ring_bytes(int slots) { return DS_WARPS * slots * (DS_SLOT + 8); }
+// activation row stride in shared memory: 144 B per 4 blocks (nb % 8 == 0)
+__host__ __device__ constexpr int ds_xrow_bytes(int nb) { return nb / 4 * 144; }
+__host__ __device__ constexpr int ds_smem_bytes(int mt, int slots, int nb) {
+    return ds_ring_bytes(slots) + mt * (ds_xrow_bytes(nb) + 8 * nb);
+}
+static_assert(64 * Q8_0_BYTES <= DS_SLOT && (64 * Q8_0_BYTES) % 16 == 0 && DS_SLOT % 16 == 0, "slots");
+
+// All lanes of the warp poll the slot's barrier (sleeping in the poll); false on every
+// lane after the time limit, with the error recorded.
+__device__ __forceinline__ bool ds_wait(uint32_t bar, uint32_t parity) {
+    bool done = ptx::mbar_try_wait(bar, parity);
+    if (!done) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!(done = ptx::mbar_try_wait_sleep(bar, parity, DS_SLEEP_NS)))
+            if (ptx::globaltimer_ns() - t0 > DS_WAIT_LIMIT_NS) break;
+    }
+    done = __all_sync(0xffffffffu, done);
+    if (!done && (threadIdx.x & 31) == 0) atomicOr(&g_small_error, ERR_TIMEOUT);
+    return done;
+}
+
+// byte u of a word as an exact f32 (0..255): the byte placed in the low mantissa bits
+// of 2^23 (unit 1), then 2^23 subtracted; byte_f32_div16: the same under 2^19 (unit 1/16)
+__device__ __forceinline__ float byte_f32(uint32_t w, int u) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440 + u)) - 8388608.f;
+}
+__device__ __forceinline__ float byte_f32_div16(uint32_t w, int u) {
+    return __uint_as_float(__byte_perm(w, 0x49000000u, 0x7440 + u)) - 524288.f;
+}
+// dp4a with unsigned bytes in a and signed bytes in b
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// S: slots per warp; 4 CTAs per SM with 2 slots, 2 CTAs per SM with 4 (64 copies in flight per SM)
+template <int FMT, int MT, int S>
+__global__ void __launch_bounds__(DS_WARPS * 32, S == 2 ? 4 : 2)
+k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, int M, int N, int nb,
+                  float* __restrict__ out, int32_t* __restrict__ dots) {
+    constexpr int PU = ds_piece_units(FMT), UB = ds_unit_bytes(FMT);
+    extern __shared__ __align__(128) uint8_t ds_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = ds_smem + warp * S * DS_SLOT;  // this warp's slots
+    const uint32_t bar0 = ptx::smem_u32(ds_smem + DS_WARPS * S * DS_SLOT) + 8 * warp * S;
+    const int xrow = ds_xrow_bytes(nb);
+    uint8_t* xcodes = ds_smem + ds_ring_bytes(S);                         // [MT][nb/4][144]
+    float* xdv = reinterpret_cast<float*>(xcodes + MT * xrow);           // [MT][nb]
+    float* xsv = xdv + MT * nb;                                          // [MT][nb]
     const int m0 = blockIdx.y * MT;
     const int ntok = min(MT, M - m0);
-    // stage the activation rows (rows past M as zeros)
-    for (int e = threadIdx.x; e < MT * nb; e += DR_WARPS * 32) {
-        const int t = e / nb, b = e % nb;
+    const int tw = gridDim.x * DS_WARPS, gw = blockIdx.x * DS_WARPS + warp;
+    const int units = FMT == FMT_Q4_K ? nb >> 3 : nb;  // super-blocks or blocks per row
+    const int ppr = (units + PU - 1) / PU;             // pieces per row
+    const long long row_bytes = (long long)units * UB;
+    const int nrows = gw < N ? (N - 1 - gw) / tw + 1 : 0;
+    const int total = nrows * ppr;  // pieces of this warp
+
+    auto issue = [&](int q) {  // lane 0: the copy of piece q into slot q % S
+        const int r = q / ppr, p = q - r * ppr;
+        const long long n = gw + (long long)r * tw;
+        const int u0 = p * PU, nu = min(PU, units - u0);
+        const uint32_t bar = bar0 + 8 * (q % S);
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nu * UB));
+        ptx::bulk_load(ptx::smem_u32(ring + (q % S) * DS_SLOT), wq + n * row_bytes + (long long)u0 * UB,
+                       (uint32_t)(nu * UB), bar);
+    };
+    int issued = 0;  // pieces whose copies were issued (kept by every lane)
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncwarp();
+    for (; issued < S && issued < total; ++issued)
+        if (lane == 0) issue(issued);
+    // stage the activation rows (rows past M as zeros) while the first pieces arrive
+    for (int e = threadIdx.x; e < MT * nb; e += DS_WARPS * 32) {
+        const int t = e / nb, b = e - t * nb;
         uint32_t h = 0u, c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (t < ntok) {
             const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((long long)(m0 + t) * nb + b) * Q8_1_BYTES);
@@ -350,129 +436,142 @@ k_mmq_dp4a_rows(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, 
 #pragma unroll
             for (int i = 0; i < 8; ++i) c[i] = __ldg(src + 1 + i);
         }
-        uint4* dst = reinterpret_cast<uint4*>(xcodes + (size_t)e * QK);
+        uint4* dst = reinterpret_cast<uint4*>(xcodes + t * xrow + (b >> 2) * 144 + (b & 3) * QK);
         dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
         dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
         xdv[e] = f16_bits_to_f32(h);
         xsv[e] = f16_bits_to_f32(h >> 16);
     }
     __syncthreads();
-    for (int ri = 0; ri < rw; ++ri) {
-        const long long n = ((long long)blockIdx.x * rw + ri) * DR_WARPS + warp;
-        if (n >= N) break;  // uniform per warp
+
+    bool ok = true;
+    int q = 0;  // pieces consumed
+    for (int r = 0; r < nrows && ok; ++r) {
+        const long long n = gw + (long long)r * tw;
         float acc[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) acc[t] = 0.f;
-        if (FMT == FMT_Q4_K) {
-            const int nsb = nb >> 3;
-            const uint8_t* row = wq + n * (long long)nsb * Q4_K_BYTES;
-            const int grp = lane >> 3, i = lane & 7, c = i >> 1, k0 = 16 * (i & 1);
-            // two super-blocks per lane per iteration: both loads are issued before the math
-            for (int sb0 = grp; sb0 < nsb; sb0 += 8) {
-                uint4 hdrs[2], wvs[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int sb = sb0 + 4 * u;
-                    if (sb < nsb) {
-                        const uint8_t* sbk = row + (long long)sb * Q4_K_BYTES;
-                        hdrs[u] = __ldg(reinterpret_cast<const uint4*>(sbk));
-                        wvs[u] = __ldg(reinterpret_cast<const uint4*>(sbk + 16 + 16 * i));
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int sb = sb0 + 4 * u;
-                    if (sb >= nsb) break;
-                    const uint4 hdr = hdrs[u], wv = wvs[u];
-                    int sc0, mn0, sc1, mn1;
-                    q4_k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, mn0);
-                    q4_k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, mn1);
+        for (int p = 0; p < ppr; ++p, ++q) {
+            if (!ds_wait(bar0 + 8 * (q % S), (q / S) & 1)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* pc = ring + (q % S) * DS_SLOT;
+            const int u0 = p * PU, nu = min(PU, units - u0);
+            if (FMT == FMT_Q4_K) {
+                const int sl = lane >> 1, h = lane & 1;  // super-block of the piece, half
+                if (sl < nu) {
+                    const uint8_t* sbk = pc + sl * Q4_K_BYTES;
+                    const uint4 hdr = *reinterpret_cast<const uint4*>(sbk);
+                    // sub-blocks 4h + u, u = 0..3: 6-bit scale and min, one per byte
+                    const uint32_t sc4 = h ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
+                    const uint32_t mn4 =
+                        h ? (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u)) : (hdr.z & 0x3F3F3F3Fu);
                     const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
-                    const float ds0 = d * (float)sc0, ds1 = d * (float)sc1;        // exact
-                    const float dm0 = -dmin * (float)mn0, dm1 = -dmin * (float)mn1;  // exact
-                    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                    uint32_t lo[4], hi[4];
+                    // sc_j as f32, divided by 16 for the high-nibble sub-blocks (their dot is
+                    // formed on the nibble in place, i.e. 16x the code); m_j as f32 (all exact)
+                    float scf[4], mnf[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        lo[j] = w[j] & 0x0F0F0F0Fu;
-                        hi[j] = (w[j] >> 4) & 0x0F0F0F0Fu;
+                    for (int u = 0; u < 4; ++u) {
+                        scf[u] = (u & 1) ? byte_f32_div16(sc4, u) : byte_f32(sc4, u);
+                        mnf[u] = byte_f32(mn4, u);
                     }
-                    const int b0 = 8 * sb + 2 * c;  // sub-block 2c; 2c + 1 is b0 + 1
+                    const int b0 = 8 * (u0 + sl) + 4 * h;  // first block (sub-block 4h) in the row
+                    // nibble chunks 2h and 2h + 1: bytes 64h .. 64h + 63 after the header
+                    const uint4* wc = reinterpret_cast<const uint4*>(sbk + 16 + 64 * h);
+                    const uint4 w0 = wc[0], w1 = wc[1], w2 = wc[2], w3 = wc[3];
+                    const uint32_t wv[2][8] = {{w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w},
+                                               {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w}};
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
-                        const uint4 xa = *reinterpret_cast<const uint4*>(xcodes + ((size_t)t * nb + b0) * QK + k0);
-                        const uint4 xb = *reinterpret_cast<const uint4*>(xcodes + ((size_t)t * nb + b0 + 1) * QK + k0);
-                        int D0 = 0, D1 = 0;
-                        D0 = __dp4a((int)lo[0], (int)xa.x, D0);
-                        D0 = __dp4a((int)lo[1], (int)xa.y, D0);
-                        D0 = __dp4a((int)lo[2], (int)xa.z, D0);
-                        D0 = __dp4a((int)lo[3], (int)xa.w, D0);
-                        D1 = __dp4a((int)hi[0], (int)xb.x, D1);
-                        D1 = __dp4a((int)hi[1], (int)xb.y, D1);
-                        D1 = __dp4a((int)hi[2], (int)xb.z, D1);
-                        D1 = __dp4a((int)hi[3], (int)xb.w, D1);
-                        if (dots) {
-                            // the other half of each sub-block's 32 values sits in lane i ^ 1 (same
-                            // 8-lane group, hence the same trip count: the mask names that group)
-                            const unsigned grp_mask = 0xFFu << (8 * grp);
-                            const int F0 = D0 + __shfl_xor_sync(grp_mask, D0, 1);
-                            const int F1 = D1 + __shfl_xor_sync(grp_mask, D1, 1);
-                            if ((i & 1) == 0 && t < ntok) {
-                                dots[((long long)(m0 + t) * N + n) * nb + b0] = F0;
-                                dots[((long long)(m0 + t) * N + n) * nb + b0 + 1] = F1;
-                            }
-                        } else {
-                            const float2 xd = *reinterpret_cast<const float2*>(xdv + (size_t)t * nb + b0);
-                            acc[t] = fmaf(ds0 * xd.x, (float)D0, acc[t]);
-                            acc[t] = fmaf(ds1 * xd.y, (float)D1, acc[t]);
-                            if ((i & 1) == 0) {  // one of the two lanes of a sub-block pair adds the min terms
-                                const float2 xs = *reinterpret_cast<const float2*>(xsv + (size_t)t * nb + b0);
-                                acc[t] = fmaf(dm0, xs.x, acc[t]);
-                                acc[t] = fmaf(dm1, xs.y, acc[t]);
+                        const uint8_t* xb = xcodes + t * xrow + (b0 >> 2) * 144;  // blocks b0 .. b0 + 3
+                        const float4 xd = *reinterpret_cast<const float4*>(xdv + t * nb + b0);
+                        const float4 xs = *reinterpret_cast<const float4*>(xsv + t * nb + b0);
+                        const float xdu[4] = {xd.x, xd.y, xd.z, xd.w}, xsu[4] = {xs.x, xs.y, xs.z, xs.w};
+                        float sacc = 0.f, macc = 0.f;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {  // sub-block 4h + u: chunk u / 2, low (u even) or high nibbles
+                            const uint4 xa = *reinterpret_cast<const uint4*>(xb + u * QK);
+                            const uint4 xc = *reinterpret_cast<const uint4*>(xb + u * QK + 16);
+                            const uint32_t* cw = wv[u >> 1];
+                            const uint32_t mask = (u & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+                            int D = 0;  // the block dot, times 16 for the high nibbles
+                            D = dp4a_us(cw[0] & mask, xa.x, D);
+                            D = dp4a_us(cw[1] & mask, xa.y, D);
+                            D = dp4a_us(cw[2] & mask, xa.z, D);
+                            D = dp4a_us(cw[3] & mask, xa.w, D);
+                            D = dp4a_us(cw[4] & mask, xc.x, D);
+                            D = dp4a_us(cw[5] & mask, xc.y, D);
+                            D = dp4a_us(cw[6] & mask, xc.z, D);
+                            D = dp4a_us(cw[7] & mask, xc.w, D);
+                            if (dots) {
+                                if (t < ntok) dots[((long long)(m0 + t) * N + n) * nb + b0 + u] = (u & 1) ? D >> 4 : D;
+                            } else {
+                                sacc = fmaf(scf[u], xdu[u] * (float)D, sacc);
+                                macc = fmaf(mnf[u], xsu[u], macc);
                             }
                         }
+                        // (d * sc_j * xd) * D - (dmin * m_j) * xs summed over the half's 4 sub-blocks
+                        acc[t] = fmaf(d, sacc, acc[t]);
+                        acc[t] = fmaf(-dmin, macc, acc[t]);
                     }
                 }
-            }
-        } else {
-            const uint8_t* row = wq + n * (long long)nb * Q8_0_BYTES;
-            for (int b = lane; b < nb; b += 32) {
-                const uint8_t* blk = row + (long long)b * Q8_0_BYTES;
-                // 34 bytes at a 2-byte alignment, read as the 9 aligned words around them
-                // (in bounds: with K % 256 == 0 the matrix's last block starts 2 bytes into a
-                // word, so its window ends with the block).  sh = 16: window = [2 bytes of
-                // the previous block | wd | codes], code word j = word j + 1.  sh = 0:
-                // window = [wd | codes | 2 bytes of the next block], a 16-bit funnel shift.
-                const uint32_t* wp = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(blk) & ~(uintptr_t)3);
-                const bool sh = (reinterpret_cast<uintptr_t>(blk) & 3) != 0;
-                uint32_t t9[9];
+            } else if (2 * lane < nu) {
+                // blocks 2l and 2l + 1 of the piece: 68 bytes at offset 68l (4-byte aligned) =
+                // [wd0 | 32 codes | wd1 | 32 codes]; nu is even (K % 256 == 0)
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(pc + lane * 2 * Q8_0_BYTES);
+                uint32_t w[17];
 #pragma unroll
-                for (int j = 0; j < 9; ++j) t9[j] = __ldg(wp + j);
-                const float wd = f16_bits_to_f32(sh ? (t9[0] >> 16) : (t9[0] & 0xffffu));
-                uint32_t cw[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) cw[j] = sh ? t9[j + 1] : __funnelshift_r(t9[j], t9[j + 1], 16);
+                for (int e = 0; e < 17; ++e) w[e] = wp[e];
+                const float wd0 = f16_bits_to_f32(w[0]), wd1 = f16_bits_to_f32(w[8] >> 16);
+                const int b0 = u0 + 2 * lane;
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
-                    const uint4* xc = reinterpret_cast<const uint4*>(xcodes + ((size_t)t * nb + b) * QK);
-                    const uint4 xa = xc[0], xb = xc[1];
-                    int D = 0;
-                    D = __dp4a((int)cw[0], (int)xa.x, D);
-                    D = __dp4a((int)cw[1], (int)xa.y, D);
-                    D = __dp4a((int)cw[2], (int)xa.z, D);
-                    D = __dp4a((int)cw[3], (int)xa.w, D);
-                    D = __dp4a((int)cw[4], (int)xb.x, D);
-                    D = __dp4a((int)cw[5], (int)xb.y, D);
-                    D = __dp4a((int)cw[6], (int)xb.z, D);
-                    D = __dp4a((int)cw[7], (int)xb.w, D);
+                    const uint8_t* xb = xcodes + t * xrow + (b0 >> 2) * 144 + (b0 & 3) * QK;  // blocks b0, b0 + 1
+                    const uint4 xa0 = *reinterpret_cast<const uint4*>(xb);
+                    const uint4 xa1 = *reinterpret_cast<const uint4*>(xb + 16);
+                    const uint4 xb0 = *reinterpret_cast<const uint4*>(xb + 32);
+                    const uint4 xb1 = *reinterpret_cast<const uint4*>(xb + 48);
+                    int D0 = 0, D1 = 0;
+                    D0 = __dp4a((int)__funnelshift_r(w[0], w[1], 16), (int)xa0.x, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[1], w[2], 16), (int)xa0.y, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[2], w[3], 16), (int)xa0.z, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[3], w[4], 16), (int)xa0.w, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[4], w[5], 16), (int)xa1.x, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[5], w[6], 16), (int)xa1.y, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[6], w[7], 16), (int)xa1.z, D0);
+                    D0 = __dp4a((int)__funnelshift_r(w[7], w[8], 16), (int)xa1.w, D0);
+                    D1 = __dp4a((int)w[9], (int)xb0.x, D1);
+                    D1 = __dp4a((int)w[10], (int)xb0.y, D1);
+                    D1 = __dp4a((int)w[11], (int)xb0.z, D1);
+                    D1 = __dp4a((int)w[12], (int)xb0.w, D1);
+                    D1 = __dp4a((int)w[13], (int)xb1.x, D1);
+                    D1 = __dp4a((int)w[14], (int)xb1.y, D1);
+                    D1 = __dp4a((int)w[15], (int)xb1.z, D1);
+                    D1 = __dp4a((int)w[16], (int)xb1.w, D1);
                     if (dots) {
-                        if (t < ntok) dots[((long long)(m0 + t) * N + n) * nb + b] = D;
+                        if (t < ntok) {
+                            dots[((long long)(m0 + t) * N + n) * nb + b0] = D0;
+                            dots[((long long)(m0 + t) * N + n) * nb + b0 + 1] = D1;
+                        }
                     } else {
-                        acc[t] = fmaf(wd * xdv[(size_t)t * nb + b], (float)D, acc[t]);
+                        const float2 xd = *reinterpret_cast<const float2*>(xdv + t * nb + b0);
+                        acc[t] = fmaf(wd0 * xd.x, (float)D0, acc[t]);
+                        acc[t] = fmaf(wd1 * xd.y, (float)D1, acc[t]);
                     }
                 }
             }
+            // every lane is done with the slot: refill it with the piece S ahead
+            __syncwarp();
+            if (issued < total) {
+                if (lane == 0) {
+                    ptx::fence_proxy_async_smem();
+                    issue(issued);
+                }
+                ++issued;
+            }
         }
+        if (!ok) break;
         if (!dots) {
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
@@ -483,15 +582,47 @@ k_mmq_dp4a_rows(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, 
             }
         }
     }
+    if (!ok && lane == 0) {
+        // copies still in flight must land before the CTA exits
+        for (int k = q; k < issued; ++k) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar0 + 8 * (k % S), (k / S) & 1))
+                if (ptx::globaltimer_ns() - t0 > DS_WAIT_LIMIT_NS) break;
+        }
+    }
 }
 
-template <int FMT, int MT>
-int launch_dp4a_rows(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
-                     cudaStream_t s, const char* fn) {
-    const int smem = dr_act_bytes(MT, nb);
+// SM count and shared memory per SM of the current device (cached per device)
+struct DeviceShape {
+    int sms = 0, smem_per_sm = 0;
+};
+DeviceShape device_shape() {
+    static DeviceShape cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return DeviceShape{152, 233472};
+    }
+    if (cache[dev].sms == 0) {
+        DeviceShape d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return DeviceShape{152, 233472};
+        }
+        cache[dev] = d;
+    }
+    return cache[dev];
+}
+
+template <int FMT, int MT, int S>
+int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
+                         int32_t* dots, cudaStream_t s, const char* fn) {
+    const int smem = ds_smem_bytes(MT, S, nb);
     static int attr_bytes = 0;
     if (smem > 48 * 1024 && smem > attr_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_dp4a_rows<FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(k_mmq_dp4a_stream<FMT, MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             cudaGetLastError();
             report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
@@ -499,16 +630,29 @@ int launch_dp4a_rows(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
         }
         attr_bytes = smem;
     }
-    // rows per warp: enough CTAs for two per SM, each staging its activations once
-    const int64_t rows_per_cta_min = DR_WARPS;
-    int rw = (int)(N / (rows_per_cta_min * 2 * 152));
-    rw = rw < 1 ? 1 : (rw > 4 ? 4 : rw);
-    dim3 grid((unsigned)((N + (int64_t)DR_WARPS * rw - 1) / ((int64_t)DR_WARPS * rw)), (unsigned)((M + MT - 1) / MT));
+    // every CTA resident at once (as many per SM as the launch bounds and shared memory
+    // allow), and the rows dealt out evenly: rows per warp = ceil(N / warps that fit),
+    // then only as many CTAs as that needs
+    const DeviceShape ds = device_shape();
+    const int per_sm = std::max(1, std::min(S == 2 ? 4 : 2, ds.smem_per_sm / (smem + 1024)));
+    const int64_t max_warps = (int64_t)ds.sms * per_sm * DS_WARPS;
+    const int64_t rpw = (N + max_warps - 1) / max_warps;
+    const int64_t ctas = (N + DS_WARPS * rpw - 1) / (DS_WARPS * rpw);
+    dim3 grid((unsigned)ctas, (unsigned)((M + MT - 1) / MT));
     {
-        ProfScope ps("k_mmq_dp4a_rows", s);
-        k_mmq_dp4a_rows<FMT, MT><<<grid, DR_WARPS * 32, smem, s>>>(x8, w8, (int)M, (int)N, nb, rw, out, dots);
+        ProfScope ps("k_mmq_dp4a_stream", s);
+        k_mmq_dp4a_stream<FMT, MT, S><<<grid, DS_WARPS * 32, smem, s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
     }
     return launch_status(fn);
+}
+
+// Two slots and four CTAs per SM (more warps to hide the math) for one activation row;
+// four slots and two CTAs per SM for two (measured best for each).
+template <int FMT>
+int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
+                       int32_t* dots, cudaStream_t s, const char* fn) {
+    return M <= 1 ? launch_dp4a_stream_s<FMT, 1, 2>(x8, w8, M, N, nb, out, dots, s, fn)
+                  : launch_dp4a_stream_s<FMT, 2, 4>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
 // ---------------------------------------------------------------- streaming kernel
@@ -526,8 +670,6 @@ int launch_dp4a_rows(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
 // super-block) and piece into a shared table of f32 (d*sc, dmin*m).  Each warp holds
 // partial sums for all R rows; the warps reduce through shared memory at the end.
 // Needs K % 256 == 0 (whole 16-byte aligned pieces of both formats).
-
-__device__ unsigned int g_small_error;
 
 constexpr int GV_WARPS = 8;
 constexpr int GV_STAGES = 3;
@@ -803,13 +945,10 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     const uint8_t* w8 = static_cast<const uint8_t*>(wq);
     // one or two activation rows: dp4a rows (a tensor tile would waste 6 of its 8 token
     // columns); 3 to 8 rows: the tensor-core stream (measured crossover)
-    if (nb % 8 == 0 && M <= 2 && dr_act_bytes(2, nb) <= 200 * 1024) {
+    if (nb % 8 == 0 && M <= 2 && ds_smem_bytes(2, 4, nb) <= 200 * 1024) {
         const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
-        if (fmt == FMT_Q8_0)
-            return M <= 1 ? launch_dp4a_rows<FMT_Q8_0, 1>(x8, w8, M, N, nb, out, dots, s, fn)
-                          : launch_dp4a_rows<FMT_Q8_0, 2>(x8, w8, M, N, nb, out, dots, s, fn);
-        return M <= 1 ? launch_dp4a_rows<FMT_Q4_K, 1>(x8, w8, M, N, nb, out, dots, s, fn)
-                      : launch_dp4a_rows<FMT_Q4_K, 2>(x8, w8, M, N, nb, out, dots, s, fn);
+        return fmt == FMT_Q8_0 ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, fn)
+                               : launch_dp4a_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, fn);
     }
     if (nb % 8 == 0)
         return fmt == FMT_Q8_0 ? launch_gemv<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s)

@@ -148,6 +148,30 @@ def test_block_dots_bit_exact(mmq, fmt, path):
         assert np.array_equal(dots.cpu().numpy(), ref), f"{fmt} {path} {M}x{N}x{K}"
 
 
+# one and two activation rows on the small path: weight rows dealt out to warps (several
+# rows per warp when N exceeds the resident warps), rows of 1 to 10 pieces with a partial
+# last piece, and N = 1
+STREAM_SHAPES = [(1, 1, 256), (2, 7, 2304), (1, 300, 3584), (2, 77, 18944), (1, 40000, 256), (2, 9000, 512)]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_one_two_row_stream_parity_and_dots(mmq, fmt):
+    set_path(mmq, "small")
+    for (M, N, K) in STREAM_SHAPES:
+        x = synth.activations(M * 5 + N, M, K, True)
+        w = synth.weights(fmt, N * 7 + K, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        xq_ref = oracle.quantize_q8_1(x)
+        out = mmq.gemm(fmt, xq, dev(w), M, N, K)
+        ref, norm = oracle.gemm(fmt, xq_ref, w, M, N, K)
+        check_close(out.cpu().numpy(), ref, norm, f"{fmt} stream {M}x{N}x{K}")
+        if N * K <= 300 * 18944:
+            dots = mmq.block_dots(fmt, xq, dev(w), M, N, K)
+            assert np.array_equal(dots.cpu().numpy(), oracle.block_dots(fmt, xq_ref, w, M, N, K)), \
+                f"{fmt} stream dots {M}x{N}x{K}"
+    assert mmq.mmq_get_device_error() == 0
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_extreme_codes_block_dots(mmq, path):
     # |D| reaches 32*127*128 with all codes at the ends of their ranges
