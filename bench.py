@@ -543,6 +543,11 @@ def run_sweep(args):
     for fmt in ("q4_k", "q8_0"):
         cases += [(fmt, M, 18944, 3584, "gate") for M in (1, 2, 4, 8)]
         cases += [(fmt, M, 3584, 18944, "down") for M in (1, 2, 4, 8)]
+    if args.only:  # one case, "fmt:M:N:K" (for profiling a single kernel)
+        f, m, n, k = args.only.split(":")
+        cases = [c for c in cases if c[:4] == (f, int(m), int(n), int(k))]
+        if not cases:
+            raise SystemExit(f"--only {args.only}: not a sweep case")
     wcache = {}
     for (fmt, M, N, K, proj) in cases:
         if (fmt, proj) not in wcache:
@@ -604,6 +609,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per reference-arm step")
+    ap.add_argument("--only", default="", help="sweep: run the one case fmt:M:N:K")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

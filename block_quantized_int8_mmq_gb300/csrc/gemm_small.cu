@@ -651,8 +651,10 @@ int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_
 template <int FMT>
 int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                        int32_t* dots, cudaStream_t s, const char* fn) {
-    return M <= 1 ? launch_dp4a_stream_s<FMT, 1, 2>(x8, w8, M, N, nb, out, dots, s, fn)
-                  : launch_dp4a_stream_s<FMT, 2, 4>(x8, w8, M, N, nb, out, dots, s, fn);
+    if (M <= 1) return launch_dp4a_stream_s<FMT, 1, 2>(x8, w8, M, N, nb, out, dots, s, fn);
+    if (M <= 2) return launch_dp4a_stream_s<FMT, 2, 4>(x8, w8, M, N, nb, out, dots, s, fn);
+    if (M <= 4) return launch_dp4a_stream_s<FMT, 4, 4>(x8, w8, M, N, nb, out, dots, s, fn);
+    return launch_dp4a_stream_s<FMT, 8, 4>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
 // ---------------------------------------------------------------- streaming kernel
@@ -943,9 +945,10 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     }
     const uint8_t* x8 = static_cast<const uint8_t*>(xq);
     const uint8_t* w8 = static_cast<const uint8_t*>(wq);
-    // one or two activation rows: dp4a rows (a tensor tile would waste 6 of its 8 token
-    // columns); 3 to 8 rows: the tensor-core stream (measured crossover)
-    if (nb % 8 == 0 && M <= 2 && ds_smem_bytes(2, 4, nb) <= 200 * 1024) {
+    // measured: the dp4a weight streams beat the tensor-core stream up to 4 rows in both
+    // formats and up to 8 for Q8_0; Q4_K at 5 to 8 rows goes to the tensor-core stream
+    const int64_t dp4a_max_m = fmt == FMT_Q8_0 ? 8 : 4;
+    if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8, 4, nb) <= 220 * 1024) {
         const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
         return fmt == FMT_Q8_0 ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, fn)
                                : launch_dp4a_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, fn);

@@ -155,9 +155,12 @@ int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t
                      void* stream);
 
 /* Kernel selection for the two contractions and their test hooks.
- *   MMQ_PATH_AUTO   : by shape: the warp-level kernel for M <= 8 or K % 256 != 0; else
- *                     the expanded-code tensor-core path for M >= MMQ_EXPAND_MIN_M, the
- *                     converter tensor-core kernel otherwise.
+ *   MMQ_PATH_AUTO   : by shape: the warp-level kernels for M <= 8 or K % 256 != 0;
+ *                     otherwise whichever of the warp-level kernels and the
+ *                     expanded-code tensor-core path a cost model (weight bytes per
+ *                     8-row pass against tiles per wave and 32-blocks per tile, with
+ *                     constants measured on GB300) predicts to be faster.  The
+ *                     converter kernel is only taken when forced.
  *   MMQ_PATH_SMALL  : always the warp-level kernel (any M; slow for large M).
  *   MMQ_PATH_TC     : always the tcgen05 kernel that converts codes in shared memory
  *                     (K % 256 == 0, no scratch).
@@ -166,7 +169,6 @@ int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t
  * Process-wide; the environment variable MMQ_FORCE_PATH=auto|small|tc|expand sets the
  * initial value.  Returns the previous value, or MMQ_ERR_ARG. */
 enum { MMQ_PATH_AUTO = 0, MMQ_PATH_SMALL = 1, MMQ_PATH_TC = 2, MMQ_PATH_EXPAND = 3 };
-#define MMQ_EXPAND_MIN_M 64
 int mmq_set_path(int path);
 
 /* Path the last successful contraction or test-hook call on this thread took

@@ -148,14 +148,15 @@ def test_block_dots_bit_exact(mmq, fmt, path):
         assert np.array_equal(dots.cpu().numpy(), ref), f"{fmt} {path} {M}x{N}x{K}"
 
 
-# one and two activation rows on the small path: weight rows dealt out to warps (several
+# one to eight activation rows on the small path: weight rows dealt out to warps (several
 # rows per warp when N exceeds the resident warps), rows of 1 to 10 pieces with a partial
-# last piece, and N = 1
-STREAM_SHAPES = [(1, 1, 256), (2, 7, 2304), (1, 300, 3584), (2, 77, 18944), (1, 40000, 256), (2, 9000, 512)]
+# last piece, N = 1, and token counts that leave part of a 4- or 8-row pass empty
+STREAM_SHAPES = [(1, 1, 256), (2, 7, 2304), (1, 300, 3584), (2, 77, 18944), (1, 40000, 256), (2, 9000, 512),
+                 (3, 77, 2304), (4, 300, 3584), (5, 9000, 512), (8, 513, 3584), (7, 40, 7168)]
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
-def test_one_two_row_stream_parity_and_dots(mmq, fmt):
+def test_few_row_stream_parity_and_dots(mmq, fmt):
     set_path(mmq, "small")
     for (M, N, K) in STREAM_SHAPES:
         x = synth.activations(M * 5 + N, M, K, True)
