@@ -110,11 +110,10 @@ def auto_steps(step, warmup, stream, torch):
 # these files are unchanged
 _COMMON_SRC = ("ptx.cuh", "common.cuh")
 KERNEL_SOURCES = {
-    "k_quantize_q8_1": ("quantize.cu",) + _COMMON_SRC,
+    "k_quantize_q8_1": ("quantize.cu", "quant_block.cuh") + _COMMON_SRC,
     "k_mmq_tc": ("gemm_tc.cu", "umma.cuh") + _COMMON_SRC,
     "k_mmq_tcx": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
-    "k_expand_acts": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
-    "k_expand_weights": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
+    "k_expand": ("gemm_expand.cu", "quant_block.cuh", "umma.cuh") + _COMMON_SRC,
     "k_mmq_dp4a_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_gemv": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small_mma": ("gemm_small.cu",) + _COMMON_SRC,
@@ -300,13 +299,14 @@ def run_ours(args, rank, world, local):
     xq = torch.empty(xq_bytes, dtype=torch.uint8, device=dev).view(M, -1)
     out = torch.full((M, N), float("nan"), device=dev)
     stream = torch.cuda.current_stream(dev)
-    gemm = mmq.mmq_gemm_q8_0 if fmt == "q8_0" else mmq.mmq_gemm_q4_k
-
     def step(i, stream=stream):
+        # quantize + contraction: one call (on the expanded tensor-core path the quantize is
+        # fused into the activation expansion; xq still receives the q8_1 bytes)
         j = i % copies
-        mmq.mmq_quantize_q8_1(xs[j], xq, stream)
-        if not quant_only:
-            gemm(xq, ws[j], M, N, K, out, stream)
+        if quant_only:
+            mmq.mmq_quantize_q8_1(xs[j], xq, stream)
+        else:
+            mmq.mmq_linear(xs[j], ws[j], fmt, N, xq=xq, out=out, stream=stream)
 
     for i in range(args.warmup):
         step(i)

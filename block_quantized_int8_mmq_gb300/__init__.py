@@ -22,7 +22,7 @@ EXPORTED = (
     "mmq_status_string", "mmq_q8_1_bytes", "mmq_weight_row_bytes", "mmq_quantize_q8_1",
     "mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k",
     "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
-    "mmq_gemm_noalloc",
+    "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k",
 )
 
 
@@ -54,6 +54,8 @@ def _load():
     L.mmq_set_path.argtypes = [I]
     L.mmq_get_device_error.argtypes = [P]
     L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
+    for f in ("mmq_linear_q8_0", "mmq_linear_q4_k"):
+        getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
     return L
@@ -193,7 +195,14 @@ def block_dots(fmt: str, xq, wq, M, N, K, dots=None, stream=None):
 
 
 def mmq_linear(x, wq, fmt: str, N: int, xq=None, out=None, stream=None):
-    """Quantize x (f32 [M, K]) to q8_1 and contract it with weights wq: f32 [M, N]."""
+    """Quantize x (f32 [M, K]) to q8_1 (into xq) and contract it with weights wq in one
+    call (mmq_linear_q8_0 / mmq_linear_q4_k): f32 [M, N]."""
+    import torch
     M, K = x.shape
-    xq = mmq_quantize_q8_1(x, xq, stream)
-    return gemm(fmt, xq, wq, M, N, K, out, stream)
+    if xq is None:
+        xq = torch.empty((M, K // QK * Q8_1_BYTES), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    fn = "mmq_linear_q8_0" if fmt == "q8_0" else "mmq_linear_q4_k"
+    _check(fn, getattr(_lib, fn)(_ptr(x), M, K, _ptr(wq), N, _ptr(xq), _ptr(out), _stream(stream)))
+    return out

@@ -114,6 +114,36 @@ int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t
     return st;
 }
 
+// Quantize + contraction in one call.  On the expanded-code path the quantization is
+// fused into the activation expansion (one pass over x writes both xq and the fp16
+// operand); on the other paths it is the quantize kernel followed by the contraction.
+int linear(const char* fn, int fmt, const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq,
+           float* out, void* stream) {
+    int st = check_mk(fn, M, N, K, fmt == FMT_Q4_K ? QK_K : QK);
+    if (st) return st;
+    if (!x || !xq || !wq || !out) {
+        report(fn, MMQ_ERR_NULL, "x, xq, wq and out must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    if (!aligned(x, 16) || !aligned(xq, 16) || !aligned(wq, 16) || !aligned(out, 16)) {
+        report(fn, MMQ_ERR_ALIGN, "x, xq, wq and out must be 16-byte aligned");
+        return MMQ_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int path = current_path();
+    if (path == MMQ_PATH_AUTO) path = auto_path(fmt, M, N, K);
+    if (path == MMQ_PATH_EXPAND) {
+        st = tcx_linear_launch(fmt, x, xq, wq, M, N, K, out, s);
+    } else {
+        st = quantize_launch(x, M, K, xq, s);
+        if (st == MMQ_OK)
+            st = path == MMQ_PATH_SMALL ? small_launch(fmt, xq, wq, M, N, K, out, nullptr, s)
+                                        : tc_launch(fmt, xq, wq, M, N, K, out, nullptr, s);
+    }
+    if (st == MMQ_OK) t_last_path = path;
+    return st;
+}
+
 }  // namespace
 }  // namespace mmq
 
@@ -171,6 +201,16 @@ int mmq_gemm_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
 
 int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, void* stream) {
     return contraction("mmq_gemm_q4_k", FMT_Q4_K, xq, wq, M, N, K, out, nullptr, stream);
+}
+
+int mmq_linear_q8_0(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream) {
+    return linear("mmq_linear_q8_0", FMT_Q8_0, x, M, K, wq, N, xq, out, stream);
+}
+
+int mmq_linear_q4_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream) {
+    return linear("mmq_linear_q4_k", FMT_Q4_K, x, M, K, wq, N, xq, out, stream);
 }
 
 int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,

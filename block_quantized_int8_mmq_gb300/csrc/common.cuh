@@ -55,6 +55,8 @@ int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int
               int32_t* dots, cudaStream_t s);
 int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                int32_t* dots, cudaStream_t s);
+int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                      cudaStream_t s);
 int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                        cudaStream_t s);
 unsigned tc_take_error();

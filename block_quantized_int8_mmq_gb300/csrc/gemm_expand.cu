@@ -10,26 +10,26 @@
 // Measured on this GPU, one thread issues a kind::f16 MMA about every 128 cycles when
 // consecutive MMAs switch accumulators, while the tensor core finishes a 128 x 128 x 16
 // MMA in 64: so the 128 x 128 tiles here have two MMA-issuing warps (even and odd
-// blocks) and four 128-column TMEM slots, and the per-block readout of D, the
-// pipeline's critical resource, has four blocks of slack.  The codes reach shared
-// memory already in the MMA's layout: two streaming kernels convert every code once
-// per call into scratch,
+// items), each with its own TMEM slot of 256 columns (D, then the scale products S).
+// The codes reach shared memory already in the MMA's layout: one streaming kernel,
+// k_expand, converts every code once per call into scratch, its CTAs split between
 //
-//   k_expand_acts     q8_1 rows -> per (128-row tile, 32-block) an 8 KiB chunk of fp16
-//                     codes in the K-major no-swizzle core-matrix order; per (tile,
-//                     256-value group) the f32 row scales xd[c][row] of its blocks (row
-//                     c = 8: 1.0, the Q4_K min item) and, for Q4_K, the K = 16 operand
-//                     AM (column c = the f16 block sum s of block c);
-//   k_expand_weights  Q8_0 / Q4_K rows -> per (128-row tile, 32-block) the same chunks
-//                     (Q4_K: q * sc_j); per (tile, group) the f32 column scales w[c][n]
-//                     (Q8_0: wd; Q4_K: d, and -dmin for c = 8) and, for Q4_K, the K = 16
-//                     operand BMIN (column j = m_j) ("When Does a Kernel Win Surface?",
-//                     sec. "Kept levers: Vulkan", the Q4_K affine identity);
+//   activations  q8_1 rows (or f32 rows, quantized on the way) -> per (128-row tile,
+//                32-block) an 8 KiB chunk of fp16 codes in the K-major no-swizzle
+//                core-matrix order; per (tile, 256-value group) the K = 16 operand AS
+//                (column c = xd of block c; column 8 = 1.0, the Q4_K min item) and, for
+//                Q4_K, AM (column c = the f16 block sum s of block c);
+//   weights      Q8_0 / Q4_K rows -> per (128-row tile, 32-block) the same chunks (Q4_K:
+//                q * sc_j); per (tile, group) the f16 column scales WS (Q8_0: wd; Q4_K: d,
+//                and -dmin for the min item) and, for Q4_K, the K = 16 operand BMIN
+//                (column j = m_j) ("When Does a Kernel Win Surface?", sec. "Kept levers:
+//                Vulkan", the Q4_K affine identity);
 //
-// and k_mmq_tcx copies whole chunks with 1-D bulk copies, issues the MMAs from two
-// threads and rescales in 16 epilogue warps.  The scale product s = xd * w is exact in
-// f32 (two f16 values), so each block adds one rounding: acc = fma(s, D, acc).  Rows
-// past M or N are zero in the scratch: they add nothing and are never stored.
+// and k_mmq_tcx copies whole chunks with 1-D bulk copies, issues two K = 16 MMAs per
+// block (the exact block dot D) and one K = 16 MMA of AS against a one-hot operand built
+// from WS (the scale products S = xd * w, exact in f32) per item, and rescales in 16
+// epilogue warps: acc = fma(S, D, acc), one rounding per block.  Rows past M or N are
+// zero in the scratch: they add nothing and are never stored.
 //
 // The price is scratch traffic: 2 bytes written and read back per code.  It pays when
 // M is large enough that converting each tile in shared memory, once per output tile
@@ -40,6 +40,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "quant_block.cuh"
 #include "umma.cuh"
 
 namespace mmq {
@@ -96,24 +97,61 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
 // 8*((p/8)%4) .. +7 of the block: offset p*16 is that row's core-matrix row, so the
 // pieces are written in order (coalesced).
 
-// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the q8_1
-// activations: rows 32h..32h+31 of a tile are row groups 4h..4h+3, i.e. a contiguous
-// 2 KiB of every chunk and 1 KiB of every K = 16 tile.
-template <int FMT>
-__global__ void __launch_bounds__(EXP_THREADS)
-k_expand_acts(const uint8_t* __restrict__ xq, int M, int nb, uint8_t* __restrict__ xa, uint8_t* __restrict__ ga) {
+// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the activations:
+// rows 32h..32h+31 of a tile are row groups 4h..4h+3, i.e. a contiguous 2 KiB of every
+// chunk and 1 KiB of every K = 16 tile.  The quarter's q8_1 rows are first gathered into
+// shared memory (row stride EXP_SROW): copied from xq, or (FROM_X) quantized here from
+// the f32 rows of x by the same per-block arithmetic as k_quantize_q8_1, the q8_1 bytes
+// also written to xq for the caller.
+constexpr int EXP_SROW = 304;  // 76 words: the 64-bit reads below are conflict-free
+
+template <int FMT, bool FROM_X>
+__device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __restrict__ x,
+                                                 const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
+                                                 int M, int nb, uint8_t* __restrict__ xa, uint8_t* __restrict__ ga,
+                                                 uint8_t* __restrict__ sm) {
     constexpr int ROW = GB * Q8_1_BYTES;  // 288 bytes of one row per group
     constexpr int V = ROW / 16;           // 18
-    constexpr int SROW = 304;             // 76 words: the 64-bit reads below are conflict-free
-    __shared__ __align__(16) uint8_t sm[EXP_ROWS * SROW];
-    const int mt = blockIdx.x >> 2, h = blockIdx.x & 3, g = blockIdx.y, ng = nb / GB;
+    constexpr int SROW = EXP_SROW;
+    const int mt = bx >> 2, h = bx & 3, ng = nb / GB;
     const int m0 = mt * BM + h * EXP_ROWS;
     const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
-    for (int i = threadIdx.x; i < EXP_ROWS * V; i += EXP_THREADS) {
-        const int r = i / V, c = i % V;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m0 + r < M) v = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)(m0 + r) * rowbytes + (size_t)g * ROW) + c);
-        *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
+    if (FROM_X) {
+        // 32 rows x 8 blocks, four lanes per block: a warp quantizes the 8 blocks (1 KiB of
+        // x) of one row per pass
+        const int part = threadIdx.x & 3;
+        for (int pass = 0; pass < EXP_ROWS * GB / (EXP_THREADS / 4); ++pass) {
+            const int blk = pass * (EXP_THREADS / 4) + (threadIdx.x >> 2);
+            const int r = blk / GB, j = blk % GB, m = m0 + r;
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (m < M) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(x + (size_t)m * nb * QK + (size_t)(g * GB + j) * QK + part * 8);
+                const float4 a = __ldcs(src), b = __ldcs(src + 1);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+            uint32_t w0, w1, hdr;
+            quantize_q8_1_part(v, w0, w1, hdr);
+            uint8_t* sb = sm + r * SROW + j * Q8_1_BYTES;
+            if (part == 0) *reinterpret_cast<uint32_t*>(sb) = hdr;
+            *reinterpret_cast<uint32_t*>(sb + 4 + 8 * part) = w0;
+            *reinterpret_cast<uint32_t*>(sb + 8 + 8 * part) = w1;
+            if (m < M) {
+                uint8_t* gb = xq_out + (size_t)m * rowbytes + (size_t)(g * GB + j) * Q8_1_BYTES;
+                if (part == 0) *reinterpret_cast<uint32_t*>(gb) = hdr;
+                *reinterpret_cast<uint32_t*>(gb + 4 + 8 * part) = w0;
+                *reinterpret_cast<uint32_t*>(gb + 8 + 8 * part) = w1;
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < EXP_ROWS * V; i += EXP_THREADS) {
+            const int r = i / V, c = i % V;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (m0 + r < M)
+                v = __ldg(reinterpret_cast<const uint4*>(xq_in + (size_t)(m0 + r) * rowbytes + (size_t)g * ROW) + c);
+            *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
+        }
     }
     __syncthreads();
     uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * CHUNK + h * (CHUNK / 4);
@@ -149,15 +187,15 @@ k_expand_acts(const uint8_t* __restrict__ xq, int M, int nb, uint8_t* __restrict
 // Q4_K codes are q * sc_j (the contraction); without it, the raw nibbles (the block-dot
 // test hook).
 template <int FMT, bool FOLD>
-__global__ void __launch_bounds__(EXP_THREADS)
-k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
+__device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
+                                                    uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
+                                                    uint8_t* __restrict__ sm) {
     constexpr int ROW = FMT == FMT_Q8_0 ? GB * Q8_0_BYTES : Q4_K_BYTES;  // 272 / 144 bytes per row per group
     constexpr int V = ROW / 16;                                          // 17 / 9
     constexpr int VP = V + 1;                                            // + one zero piece (Q8_0 reads 4 B past)
     constexpr int SROW = FMT == FMT_Q8_0 ? 304 : 176;
-    static_assert(SROW >= VP * 16, "row pad");
-    __shared__ __align__(16) uint8_t sm[EXP_ROWS * SROW];
-    const int nt = blockIdx.x >> 2, h = blockIdx.x & 3, g = blockIdx.y, ng = nb / GB;
+    static_assert(SROW >= VP * 16 && SROW <= EXP_SROW, "row pad");
+    const int nt = bx >> 2, h = bx & 3, ng = nb / GB;
     const int n0 = nt * BN + h * EXP_ROWS;
     const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * Q4_K_BYTES;
     for (int i = threadIdx.x; i < EXP_ROWS * VP; i += EXP_THREADS) {
@@ -236,6 +274,21 @@ k_expand_weights(const uint8_t* __restrict__ wq, int N, int nb, uint8_t* __restr
         }
         *reinterpret_cast<uint4*>(gdst + h * (TILE16 / 4) + u * 16) = pack8(v);
     }
+}
+
+// Both expansions in one launch: CTAs 0 .. acts_x - 1 (grid x) expand the activations,
+// the rest the weights; grid y = the 256-value group.  The two halves are independent, so
+// they run side by side instead of one after the other.
+template <int FMT, bool FROM_X, bool FOLD>
+__global__ void __launch_bounds__(EXP_THREADS)
+k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
+         const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
+         uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
+    __shared__ __align__(16) uint8_t sm[EXP_ROWS * EXP_SROW];
+    if ((int)blockIdx.x < acts_x)
+        expand_acts_body<FMT, FROM_X>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
+    else
+        expand_weights_body<FMT, FOLD>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
 }
 
 // ---------------------------------------------------------------- GEMM kernel
@@ -563,10 +616,12 @@ ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K) {
             (size_t)(NT * ng) * gw_bytes(fmt)};
 }
 
-// The three launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K) bytes).
+// The two launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K) bytes): both
+// expansions, then the contraction.  x != nullptr: the activations come as f32 rows and
+// are quantized by the expansion (q8_1 bytes written to xq); else xq is the input.
 template <int FMT, bool DOTS>
-int launch_on(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
-              uint8_t* ws, cudaStream_t s, const char* fn) {
+int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+              int32_t* dots, uint8_t* ws, cudaStream_t s, const char* fn) {
     const int nb = (int)(K / QK), ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
     const ScratchPlan sp = plan_scratch(FMT, M, N, K);
@@ -579,15 +634,17 @@ int launch_on(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, f
     uint8_t* ga = xa + sp.xa;
     uint8_t* xb = ga + sp.ga;
     uint8_t* gw = xb + sp.xb;
+    const dim3 eg((unsigned)(4 * MT + 4 * NT), (unsigned)ng);
     {
-        ProfScope ps("k_expand_acts", s);
-        k_expand_acts<FMT><<<dim3((unsigned)(4 * MT), (unsigned)ng), EXP_THREADS, 0, s>>>(
-            static_cast<const uint8_t*>(xq), (int)M, nb, xa, ga);
-    }
-    {
-        ProfScope ps("k_expand_weights", s);
-        k_expand_weights<FMT, !DOTS><<<dim3((unsigned)(4 * NT), (unsigned)ng), EXP_THREADS, 0, s>>>(
-            static_cast<const uint8_t*>(wq), (int)N, nb, xb, gw);
+        ProfScope ps("k_expand", s);
+        if (x && !DOTS)
+            k_expand<FMT, true, true><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, static_cast<uint8_t*>(const_cast<void*>(xq)),
+                                                                 static_cast<const uint8_t*>(wq), (int)M, (int)N, nb,
+                                                                 (int)(4 * MT), xa, ga, xb, gw);
+        else
+            k_expand<FMT, false, !DOTS><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq), nullptr,
+                                                                  static_cast<const uint8_t*>(wq), (int)M, (int)N, nb,
+                                                                  (int)(4 * MT), xa, ga, xb, gw);
     }
     {
         ProfScope ps("k_mmq_tcx", s);
@@ -598,8 +655,8 @@ int launch_on(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, f
 }
 
 template <int FMT, bool DOTS>
-int launch_x(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
-             cudaStream_t s, const char* fn) {
+int launch_x(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+             int32_t* dots, cudaStream_t s, const char* fn) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -628,7 +685,7 @@ int launch_x(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
         report(fn, MMQ_ERR_NOMEM, "scratch allocation failed");
         return MMQ_ERR_NOMEM;
     }
-    const int st = launch_on<FMT, DOTS>(xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), s, fn);
+    const int st = launch_on<FMT, DOTS>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), s, fn);
     cudaFreeAsync(ws, s);  // stream-ordered: after the kernels above
     return st;
 }
@@ -672,10 +729,25 @@ int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, in
         return MMQ_ERR_SHAPE;
     }
     if (fmt == FMT_Q8_0)
-        return dots ? launch_x<FMT_Q8_0, true>(xq, wq, M, N, K, out, dots, s, fn)
-                    : launch_x<FMT_Q8_0, false>(xq, wq, M, N, K, out, dots, s, fn);
-    return dots ? launch_x<FMT_Q4_K, true>(xq, wq, M, N, K, out, dots, s, fn)
-                : launch_x<FMT_Q4_K, false>(xq, wq, M, N, K, out, dots, s, fn);
+        return dots ? launch_x<FMT_Q8_0, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+                    : launch_x<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
+    return dots ? launch_x<FMT_Q4_K, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+                : launch_x<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
+}
+
+int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                      cudaStream_t s) {
+    const char* fn = fmt == FMT_Q8_0 ? "mmq_linear_q8_0" : "mmq_linear_q4_k";
+    if (K % QK_K != 0) {
+        report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
+        return MMQ_ERR_K_MULTIPLE;
+    }
+    if ((N + BN - 1) / BN > 65535 || K / QK_K > 65535) {
+        report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
+        return MMQ_ERR_SHAPE;
+    }
+    return fmt == FMT_Q8_0 ? launch_x<FMT_Q8_0, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
+                           : launch_x<FMT_Q4_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn);
 }
 
 int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
@@ -704,8 +776,8 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
         report(fn, MMQ_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed");
         return MMQ_ERR_CUDA;
     }
-    return fmt == FMT_Q8_0 ? launch_on<FMT_Q8_0, false>(xq, wq, M, N, K, out, nullptr, ws, s, fn)
-                           : launch_on<FMT_Q4_K, false>(xq, wq, M, N, K, out, nullptr, ws, s, fn);
+    return fmt == FMT_Q8_0 ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
+                           : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn);
 }
 
 unsigned tcx_take_error() {

@@ -7,12 +7,12 @@
 // (two 16-byte loads); amax and the code sum are reduced across the four lanes with
 // shuffles.  amax is exact under any association, so the tree order changes nothing.
 //
-// Bit-exact arithmetic: d = amax / 127 and each x / d are IEEE divisions (__fdiv_rn),
-// rounding to the nearest integer ties to even (__float2int_rn), s = f16(d * S) with
-// one f32 multiply.  Blocks whose d is 0 get all-zero codes, d and s.
+// The arithmetic of one block (bit-exact: IEEE divisions, ties to even, s = f16(d * S)) is
+// quantize_q8_1_part, shared with the fused quantize-and-expand kernel.
 #include <stdio.h>
 
 #include "common.cuh"
+#include "quant_block.cuh"
 
 namespace mmq {
 namespace {
@@ -22,7 +22,6 @@ constexpr int BLOCKS_PER_WARP = 8;  // 32 lanes / 4 lanes per block
 
 __global__ void __launch_bounds__(QUANT_THREADS)
 k_quantize_q8_1(const float* __restrict__ x, uint8_t* __restrict__ y, long long nblk) {
-    const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 2;   // block within the warp's group of 8
     const int part = lane & 3;   // which 8 values of the block
@@ -39,38 +38,14 @@ k_quantize_q8_1(const float* __restrict__ x, uint8_t* __restrict__ y, long long 
             b = __ldcs(src + 1);
         }
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
-        const float d = __fdiv_rn(amax, 127.0f);
-
-        int sum = 0;
-        uint32_t w[2] = {0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int q = 0;
-            if (d != 0.f) {
-                q = __float2int_rn(__fdiv_rn(v[i], d));
-                q = max(-127, min(127, q));
-            }
-            sum += q;
-            w[i >> 2] |= (uint32_t)(q & 0xff) << (8 * (i & 3));
-        }
-        sum += __shfl_xor_sync(FULL, sum, 1);
-        sum += __shfl_xor_sync(FULL, sum, 2);
-
+        uint32_t w0, w1, hdr;
+        quantize_q8_1_part(v, w0, w1, hdr);
         if (valid) {
             uint8_t* dst = y + g * Q8_1_BYTES;
-            if (part == 0) {
-                const uint32_t dh = __half_as_ushort(__float2half_rn(d));
-                const uint32_t sh = __half_as_ushort(__float2half_rn(__fmul_rn(d, (float)sum)));
-                *reinterpret_cast<uint32_t*>(dst) = dh | (sh << 16);
-            }
+            if (part == 0) *reinterpret_cast<uint32_t*>(dst) = hdr;
             uint32_t* q32 = reinterpret_cast<uint32_t*>(dst + 4 + part * 8);
-            q32[0] = w[0];
-            q32[1] = w[1];
+            q32[0] = w0;
+            q32[1] = w1;
         }
     }
 }

@@ -119,6 +119,24 @@ int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
                   void* stream);
 
 /*
+ * Quantize + contraction in one call: xq = q8_1 of x (the same bytes as
+ * mmq_quantize_q8_1) and out = xq contracted with Q8_0 (mmq_linear_q8_0) or Q4_K
+ * (mmq_linear_q4_k) weights, as mmq_gemm_q8_0 / mmq_gemm_q4_k would compute it.  On the
+ * expanded-code tensor-core path the quantization is fused into the expansion of the
+ * activations (x is read once; "13 . r7-r8 raw-byte MMQ kernel", sec. 3.2, names the
+ * quantize pass as the cost that grows once the contraction is fast); otherwise it is the
+ * quantize kernel followed by the contraction, on `stream`.
+ *   x: f32 [M][K] row-major, 16-byte aligned.  wq: weights as in the gemm calls,
+ *   16-byte aligned.  xq: output, mmq_q8_1_bytes(M, K) bytes, 16-byte aligned.
+ *   out: f32 [M][N], 16-byte aligned.
+ * Errors: as mmq_quantize_q8_1 and mmq_gemm_q8_0 / mmq_gemm_q4_k.
+ */
+int mmq_linear_q8_0(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream);
+int mmq_linear_q4_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream);
+
+/*
  * Test hook: the per-block int32 dots D[m][n][b] (b < K/32) computed by the SAME data
  * path as mmq_gemm_q8_0 / mmq_gemm_q4_k select for this M (same staging, same
  * conversion, same MMA), written out instead of rescaled.  For Q4_K, D is the dot of

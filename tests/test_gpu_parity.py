@@ -173,6 +173,59 @@ def test_few_row_stream_parity_and_dots(mmq, fmt):
     assert mmq.mmq_get_device_error() == 0
 
 
+# quantize + contraction in one call: on the expanded path the quantize is fused into the
+# activation expansion.  xq must hold the q8_1 bytes of x and out must equal the separate
+# quantize + gemm calls on the same path bit for bit (same kernels downstream of the
+# expanded operands), and the oracle within tolerance.
+@pytest.mark.parametrize("path", ["auto", "expand", "small", "tc"])
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_linear_matches_separate_calls(mmq, fmt, path):
+    set_path(mmq, path)
+    for (M, N, K) in [(300, 200, 1024), (129, 257, 2304), (4, 130, 512), (513, 64, 256)]:
+        x = synth.activations(M + 3 * N + K, M, K, True)
+        w = synth.weights(fmt, 2 * M + N, N, K)
+        xd, wd = dev(x), dev(w)
+        xq = torch.full((M, K // 32 * 36), 0xAB, dtype=torch.uint8, device="cuda")
+        out = mmq.mmq_linear(xd, wd, fmt, N, xq=xq)
+        taken = mmq.mmq_last_path()
+        xq_ref = oracle.quantize_q8_1(x)
+        assert np.array_equal(xq.cpu().numpy(), xq_ref), f"{fmt} {path} {M}x{N}x{K}: q8_1 bytes"
+        sep = mmq.gemm(fmt, mmq.mmq_quantize_q8_1(xd), wd, M, N, K)
+        assert mmq.mmq_last_path() == taken
+        assert torch.equal(out, sep), f"{fmt} {path} {M}x{N}x{K}: fused != separate"
+        ref, norm = oracle.gemm(fmt, xq_ref, w, M, N, K)
+        check_close(out.cpu().numpy(), ref, norm, f"{fmt} linear {path} {M}x{N}x{K}")
+    assert mmq.mmq_get_device_error() == 0
+
+
+def test_linear_graph_capture_two_kernels(mmq):
+    set_path(mmq, "expand")
+    M, N, K = 256, 384, 1024
+    x = synth.activations(91, M, K, True)
+    w = synth.q4_k_weights(92, N, K)
+    xd, wd = dev(x), dev(w)
+    xq = torch.empty((M, K // 32 * 36), dtype=torch.uint8, device="cuda")
+    out = torch.full((M, N), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    prev = mmq.mmq_profile_enable(True)
+    try:
+        with torch.cuda.graph(g, stream=s):
+            mmq.mmq_linear(xd, wd, "q4_k", N, xq=xq, out=out, stream=s)
+        g.replay()
+        torch.cuda.synchronize()
+        prof = mmq.mmq_profile_read(reset=True)
+    finally:
+        mmq.mmq_profile_enable(prev)
+    assert set(prof) == {"k_expand", "k_mmq_tcx"}, prof
+    xq_ref = oracle.quantize_q8_1(x)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    ref, norm = oracle.gemm("q4_k", xq_ref, w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, "captured linear")
+    assert mmq.mmq_get_device_error() == 0
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_extreme_codes_block_dots(mmq, path):
     # |D| reaches 32*127*128 with all codes at the ends of their ranges
@@ -240,6 +293,25 @@ def test_config_sampled_parity(mmq, full_operands, index, path):
     assert mmq.mmq_get_device_error() == 0
     if path == "auto":  # the converter kernel is never the automatic choice
         assert mmq.mmq_last_path() == (mmq.PATH_EXPAND if M >= 512 else mmq.PATH_SMALL)
+
+
+@pytest.mark.parametrize("index", [1, 2, 3])
+def test_config_linear_sampled_parity(mmq, full_operands, index):
+    """The fused quantize + contraction at the full workload sizes (the bench's step)."""
+    set_path(mmq, "auto")
+    x, w, spec, xq_ref = full_operands(index)
+    M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
+    xq = torch.empty((M, K // 32 * 36), dtype=torch.uint8, device="cuda")
+    out = torch.full((M, N), float("nan"), device="cuda")
+    mmq.mmq_linear(dev(x), dev(w), fmt, N, xq=xq, out=out)
+    assert mmq.mmq_last_path() == mmq.PATH_EXPAND
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    o = out.cpu().numpy()
+    assert not np.isnan(o).any(), "output not fully written"
+    im, inn = sample_entries(M, N, 3000, index + 10)
+    ref, norm = oracle.gemm_at(fmt, xq_ref, w, M, N, K, im, inn)
+    check_close(o[im, inn], ref, norm, f"config {index} linear")
+    assert mmq.mmq_get_device_error() == 0
 
 
 @pytest.mark.parametrize("M", synth.M_SWEEP)
@@ -321,7 +393,7 @@ def test_graph_capture_and_replay_with_scratch(mmq):
         prof = mmq.mmq_profile_read(reset=True)
     finally:
         mmq.mmq_profile_enable(prev)
-    assert set(prof) == {"k_expand_acts", "k_expand_weights", "k_mmq_tcx"}, prof
+    assert set(prof) == {"k_expand", "k_mmq_tcx"}, prof
     assert all(n == 1 and ms > 0 for n, ms in prof.values()), prof
     ref, norm = oracle.gemm("q8_0", oracle.quantize_q8_1(x), w, M, N, K)
     check_close(out.cpu().numpy(), ref, norm, "captured")
@@ -339,16 +411,16 @@ def test_profile_counts_every_launch(mmq):
         x = synth.activations(61, M, K, True)
         w = synth.q4_k_weights(62, N, K)
         xq = mmq.mmq_quantize_q8_1(dev(x))
-        mmq.mmq_gemm_q4_k(xq, dev(w), M, N, K)          # expanded path: three kernels
+        mmq.mmq_gemm_q4_k(xq, dev(w), M, N, K)          # expanded path: two kernels
         set_path(mmq, "auto")
         mmq.mmq_gemm_q4_k(xq[:4], dev(w), 4, N, K)      # M <= 8: warp-level kernel
         prof = mmq.mmq_profile_read(reset=True)
     finally:
         mmq.mmq_profile_enable(prev)
     assert prof["k_quantize_q8_1"][0] == 1
-    assert prof["k_expand_acts"][0] == prof["k_expand_weights"][0] == prof["k_mmq_tcx"][0] == 1
+    assert prof["k_expand"][0] == prof["k_mmq_tcx"][0] == 1
     small = {k: n for k, (n, _) in prof.items()
-             if k not in ("k_quantize_q8_1", "k_expand_acts", "k_expand_weights", "k_mmq_tcx")}
+             if k not in ("k_quantize_q8_1", "k_expand", "k_mmq_tcx")}
     assert sum(small.values()) == 1, prof  # one warp-level kernel for the M = 4 call
     assert mmq.mmq_profile_read() == {}
 
