@@ -334,15 +334,16 @@ def run_ours(args, rank, world, local):
     # The K timed steps run as CUDA-graph replays (a step is 2 to 4 launches of tens of
     # microseconds: launched one by one from Python the host, not the GPU, would set the
     # pace).  One graph holds G steps, G a multiple of the operand copies so consecutive
-    # steps never reuse a copy; a second graph holds the K % G remaining steps.  The
-    # library's profiler records an event pair around every launch inside the graphs,
-    # so each kernel's duration is read from the last replay of the timed region.
+    # steps never reuse a copy; a second graph holds the K % G remaining steps.  These
+    # graphs hold the kernels only.  A third graph, the same G steps captured with the
+    # library's profiler on (a CUDA-event pair around every launch), is replayed once
+    # right after the timed region: it gives each kernel's duration and the launches per
+    # step, without the event nodes slowing the timed steps.
     steps = args.steps if args.steps > 0 else auto_steps(step, args.warmup, stream, torch)
     G = min(steps, copies * max(1, -(-GRAPH_STEPS // copies)))
     reps, tail = divmod(steps, G)
     cap = torch.cuda.Stream(dev)
-    mmq.mmq_profile_read(reset=True)
-    prev_prof = mmq.mmq_profile_enable(True)
+    prev_prof = mmq.mmq_profile_enable(False)
     graphs = []
     for count in ([G] if reps else []) + ([tail] if tail else []):
         g = torch.cuda.CUDAGraph()
@@ -351,9 +352,16 @@ def run_ours(args, rank, world, local):
             for i in range(count):
                 step(i, stream=cap)
         graphs.append((g, count))
+    mmq.mmq_profile_read(reset=True)
+    mmq.mmq_profile_enable(True)
+    prof_graph = torch.cuda.CUDAGraph()
+    cap.wait_stream(stream)
+    with torch.cuda.graph(prof_graph, stream=cap):
+        for i in range(G):
+            step(i, stream=cap)
     mmq.mmq_profile_enable(prev_prof)
-    for g, _ in graphs:  # upload and first run, untimed (the profile is read only after
-        g.replay()        # the timed region: captured launches are counted at one read)
+    for g, _ in graphs:  # upload and first run, untimed
+        g.replay()
     torch.cuda.synchronize(dev)
     out.fill_(float("nan"))
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -370,15 +378,17 @@ def run_ours(args, rank, world, local):
     barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
-    prof = mmq.mmq_profile_read(reset=True)  # the last replay of each graph
     if not quant_only:
         assert not torch.isnan(out).any().item(), "timed steps did not write the output"
+    prof_graph.replay()  # the profiled pass: G steps, right after the timed region
+    torch.cuda.synchronize(dev)
+    prof = mmq.mmq_profile_read(reset=True)  # the profiled pass
     assert mmq.mmq_get_device_error(stream) == 0
-    launches_per_step = sum(n for n, _ in prof.values()) / sum(c for _, c in graphs)
-    kernels = {k: {"launches_per_step": n / sum(c for _, c in graphs), "avg_ms": t / n} for k, (n, t) in prof.items()}
-    step_kernel_ms = sum(t for _, t in prof.values()) / sum(c for _, c in graphs)
+    launches_per_step = sum(n for n, _ in prof.values()) / G
+    kernels = {k: {"launches_per_step": n / G, "avg_ms": t / n} for k, (n, t) in prof.items()}
+    step_kernel_ms = sum(t for _, t in prof.values()) / G
     for k, (n, t) in prof.items():
-        kernels[k]["share"] = (t / sum(c for _, c in graphs)) / step_kernel_ms
+        kernels[k]["share"] = (t / G) / step_kernel_ms
 
     ms_max = max_over_ranks(ms, world, dev)
 
@@ -447,7 +457,8 @@ def run_ours(args, rank, world, local):
         "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"rotating {copies} operand copies ({copies * set_bytes / 2**20:.0f} MiB > 3x L2)",
-                   "timing": f"CUDA graphs: {reps} replays of {G} steps" + (f" + {tail} steps" if tail else "")},
+                   "timing": f"CUDA graphs: {reps} replays of {G} steps" + (f" + {tail} steps" if tail else "")
+                             + "; kernel durations from one profiled replay of the step graph after the timed region"},
         "roofline": roof,
         "kernels": kernels,
         "path": PATH_NAMES.get(path, "quantize"),

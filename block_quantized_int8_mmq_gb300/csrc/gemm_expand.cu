@@ -118,30 +118,42 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
     if (FROM_X) {
         // 32 rows x 8 blocks, four lanes per block: a warp quantizes the 8 blocks (1 KiB of
-        // x) of one row per pass
+        // x) of one row per pass; the loads of four passes are issued before their math
+        constexpr int PASSES = EXP_ROWS * GB / (EXP_THREADS / 4);  // 8
+        constexpr int BATCH = 4;
         const int part = threadIdx.x & 3;
-        for (int pass = 0; pass < EXP_ROWS * GB / (EXP_THREADS / 4); ++pass) {
-            const int blk = pass * (EXP_THREADS / 4) + (threadIdx.x >> 2);
-            const int r = blk / GB, j = blk % GB, m = m0 + r;
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (m < M) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(x + (size_t)m * nb * QK + (size_t)(g * GB + j) * QK + part * 8);
-                const float4 a = __ldcs(src), b = __ldcs(src + 1);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+#pragma unroll
+        for (int p0 = 0; p0 < PASSES; p0 += BATCH) {
+            float4 va[BATCH], vb[BATCH];
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int blk = (p0 + u) * (EXP_THREADS / 4) + (threadIdx.x >> 2);
+                const int r = blk / GB, j = blk % GB, m = m0 + r;
+                va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (m < M) {
+                    const float4* src = reinterpret_cast<const float4*>(x + (size_t)m * nb * QK +
+                                                                        (size_t)(g * GB + j) * QK + part * 8);
+                    va[u] = __ldcs(src);
+                    vb[u] = __ldcs(src + 1);
+                }
             }
-            uint32_t w0, w1, hdr;
-            quantize_q8_1_part(v, w0, w1, hdr);
-            uint8_t* sb = sm + r * SROW + j * Q8_1_BYTES;
-            if (part == 0) *reinterpret_cast<uint32_t*>(sb) = hdr;
-            *reinterpret_cast<uint32_t*>(sb + 4 + 8 * part) = w0;
-            *reinterpret_cast<uint32_t*>(sb + 8 + 8 * part) = w1;
-            if (m < M) {
-                uint8_t* gb = xq_out + (size_t)m * rowbytes + (size_t)(g * GB + j) * Q8_1_BYTES;
-                if (part == 0) *reinterpret_cast<uint32_t*>(gb) = hdr;
-                *reinterpret_cast<uint32_t*>(gb + 4 + 8 * part) = w0;
-                *reinterpret_cast<uint32_t*>(gb + 8 + 8 * part) = w1;
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int blk = (p0 + u) * (EXP_THREADS / 4) + (threadIdx.x >> 2);
+                const int r = blk / GB, j = blk % GB, m = m0 + r;
+                const float v[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+                uint32_t w0, w1, hdr;
+                quantize_q8_1_part(v, w0, w1, hdr);
+                uint8_t* sb = sm + r * SROW + j * Q8_1_BYTES;
+                if (part == 0) *reinterpret_cast<uint32_t*>(sb) = hdr;
+                *reinterpret_cast<uint32_t*>(sb + 4 + 8 * part) = w0;
+                *reinterpret_cast<uint32_t*>(sb + 8 + 8 * part) = w1;
+                if (m < M) {
+                    uint8_t* gb = xq_out + (size_t)m * rowbytes + (size_t)(g * GB + j) * Q8_1_BYTES;
+                    if (part == 0) *reinterpret_cast<uint32_t*>(gb) = hdr;
+                    *reinterpret_cast<uint32_t*>(gb + 4 + 8 * part) = w0;
+                    *reinterpret_cast<uint32_t*>(gb + 8 + 8 * part) = w1;
+                }
             }
         }
     } else {
@@ -289,6 +301,9 @@ k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t
         expand_acts_body<FMT, FROM_X>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
     else
         expand_weights_body<FMT, FOLD>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+    // the contraction may start its set-up now; it reads the scratch only after this
+    // whole grid has completed (griddepcontrol.wait)
+    ptx::grid_dep_launch_dependents();
 }
 
 // ---------------------------------------------------------------- GEMM kernel
@@ -375,6 +390,9 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     if (warp == WARP_LOAD) {
         // ------------------------------------------------------------ bulk-copy producer
         if (lane == 0) {
+            // launched as a programmatic dependent of the expansion: everything above
+            // overlapped its tail; the scratch it wrote is read from here on
+            ptx::grid_dep_wait();
             int st_issued = 0, g_issued = 0;
             bool ok = true;
             for (int g = 0; g < ng && ok; ++g) {
@@ -647,9 +665,26 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
                                                                   (int)(4 * MT), xa, ga, xb, gw);
     }
     {
+        // a programmatic dependent launch: the contraction's CTAs may be scheduled while the
+        // expansion drains, their set-up (barriers, TMEM, one-hot operands) overlapping it
         ProfScope ps("k_mmq_tcx", s);
-        k_mmq_tcx<FMT, DOTS><<<dim3((unsigned)MT, (unsigned)NT), THREADS, XLayout<FMT>::alloc, s>>>(
-            xa, ga, xb, gw, (int)M, (int)N, nb, out, dots);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)MT, (unsigned)NT);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = XLayout<FMT>::alloc;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, DOTS>, (const uint8_t*)xa, (const uint8_t*)ga,
+                                                 (const uint8_t*)xb, (const uint8_t*)gw, (int)M, (int)N, nb, out, dots);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            report(fn, MMQ_ERR_LAUNCH, cudaGetErrorString(e));
+            return MMQ_ERR_LAUNCH;
+        }
     }
     return launch_status(fn);
 }
