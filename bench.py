@@ -478,7 +478,7 @@ def _rotating(torch, dev, arr, copies):
 
 
 def run_layer(args):
-    """28 layers x (4 quantizes + q, k, v, o, gate, up, down GEMMs) at M=2048, Q4_K.
+    """28 layers x (4 activation quantizes + q, k, v, o, gate, up, down GEMMs) at M=2048, Q4_K.
     Each layer uses its own device copy of the projection weights (the seven matrices are
     generated once from their seeds and cloned per layer), so L2 holds none of them."""
     import torch
@@ -495,15 +495,17 @@ def run_layer(args):
     xq_f = torch.empty(M * (F // 32) * 36, dtype=torch.uint8, device=dev).view(M, -1)
     outs = {name: torch.empty((M, N), device=dev) for (name, N, K) in synth.LAYER_7B}
     stream = torch.cuda.current_stream(dev)
-    q_ev = []
 
-    def layer(l, timed=False):
+    def layer(l, stream=stream):
+        # each activation is quantized once, by the fused call of its first projection
+        # (q, o, gate, down), whose q8_1 output the other projections reuse (k, v, up)
         w = w_dev[l]
         for i, names in enumerate((("q", "k", "v"), ("o",), ("gate", "up"), ("down",))):
             K = F if i == 3 else H
             xq = xq_f if i == 3 else xq_h
-            mmq.mmq_quantize_q8_1(acts[i], xq, stream)
-            for name in names:
+            first = names[0]
+            mmq.mmq_linear(acts[i], w[first], "q4_k", outs[first].shape[1], xq=xq, out=outs[first], stream=stream)
+            for name in names[1:]:
                 N = outs[name].shape[1]
                 mmq.mmq_gemm_q4_k(xq, w[name], M, N, K, outs[name], stream)
 
@@ -517,14 +519,26 @@ def run_layer(args):
     layer(0)
     mmq.mmq_profile_enable(prev)
     per_layer = sum(n for n, _ in mmq.mmq_profile_read(reset=True).values())
+    # the 28 layers as one CUDA graph (a layer is ~20 launches: launched one by one the
+    # host would add gaps between them)
+    prev = mmq.mmq_profile_enable(False)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for l in range(L):
+            layer(l, stream=cap)
+    mmq.mmq_profile_enable(prev)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    assert mmq.mmq_get_device_error(stream) == 0
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(1, (args.steps if args.steps > 0 else 30) // 10)
     clocks = ClockSampler(0)
     clocks.start()
     a.record(stream)
     for _ in range(reps):
-        for l in range(L):
-            layer(l)
+        graph.replay()
     b.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
@@ -534,7 +548,9 @@ def run_layer(args):
     return {"metric": "7B-layer prefill ms @2K (28 layers: quantizes + Q4_K projections)", "value": ms,
             "unit": "ms", "higher_is_better": False, "tok_per_s": M / (ms / 1e3), "tops": ops / (ms / 1e3) / 1e12,
             "n_gpus": 1, "steps": reps, "warmup": args.warmup, "data": "synthetic (seeded, weights cloned per layer)",
-            "config": {"workload": "7B GQA layer x28 at M=2048, Q4_K (attention, norms, SiLU excluded)"},
+            "config": {"workload": "7B GQA layer x28 at M=2048, Q4_K (attention, norms, SiLU excluded)",
+                       "timing": "the 28 layers captured in one CUDA graph; each activation quantized once, fused "
+                                 "into its first projection"},
             "gpu_launches": reps * L * per_layer, "clocks": clk}
 
 
