@@ -115,7 +115,7 @@ KERNEL_SOURCES = {
     "k_mmq_tcx": ("gemm_expand.cu", "umma.cuh") + _COMMON_SRC,
     "k_expand": ("gemm_expand.cu", "quant_block.cuh", "umma.cuh") + _COMMON_SRC,
     "k_mmq_dp4a_stream": ("gemm_small.cu",) + _COMMON_SRC,
-    "k_mmq_gemv": ("gemm_small.cu",) + _COMMON_SRC,
+    "k_mmq_i8_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small_mma": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small": ("gemm_small.cu",) + _COMMON_SRC,
 }

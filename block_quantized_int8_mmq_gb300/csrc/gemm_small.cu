@@ -653,274 +653,287 @@ int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
                        int32_t* dots, cudaStream_t s, const char* fn) {
     if (M <= 1) return launch_dp4a_stream_s<FMT, 1, 2>(x8, w8, M, N, nb, out, dots, s, fn);
     if (M <= 2) return launch_dp4a_stream_s<FMT, 2, 4>(x8, w8, M, N, nb, out, dots, s, fn);
-    if (M <= 4) return launch_dp4a_stream_s<FMT, 4, 4>(x8, w8, M, N, nb, out, dots, s, fn);
-    return launch_dp4a_stream_s<FMT, 8, 4>(x8, w8, M, N, nb, out, dots, s, fn);
+    return launch_dp4a_stream_s<FMT, 4, 4>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
-// ---------------------------------------------------------------- streaming kernel
-// k_mmq_gemv: one CTA per R weight rows (R = 16, 32 or 64, picked so that there are
-// enough CTAs for the GPU) and up to 8 activation rows (grid.y = ceil(M/8) passes).
-// The rows' weights stream through a 3-stage ring of pieces of 32 blocks (Q8_0: 1088 B
-// per row, Q4_K: 4 super-blocks = 576 B per row): one 2-D tensor copy brings all R rows
-// of a piece (the weight matrix viewed as 8-byte elements; rows past N and blocks past
-// K arrive as zeros), 1-D bulk copies the activation rows' q8_1 blocks, so HBM reads
-// run ahead of the math with two copy operations per piece.  The 8 warps split each piece's blocks (warp w takes blocks w, w+8, ...): a
-// warp converts a block's activation codes to fp16 B fragments once and reuses them
-// for all R/16 row tiles of its mma.sync m16n8k16 (16 weight rows x 8 tokens, k
-// permuted identically in both operands so that a thread's 8 values of a block are 8
-// contiguous bytes).  Q4_K sub-scales and sub-mins are decoded once per (row,
-// super-block) and piece into a shared table of f32 (d*sc, dmin*m).  Each warp holds
-// partial sums for all R rows; the warps reduce through shared memory at the end.
-// Needs K % 256 == 0 (whole 16-byte aligned pieces of both formats).
+// ---------------------------------------------------------------- int8 tensor-core stream
+// k_mmq_i8_stream: up to 8 activation rows (one pass; grid.y = ceil(M/8) passes) on the
+// int8 tensor cores with the pages' instruction, mma.sync m16n8k32 s8 x s8 -> s32 ("When the
+// Product Won't Collapse", sec. "The obstruction": one exact integer dot per 32-block; "13 .
+// r7-r8 raw-byte MMQ kernel", sec. 2): 16 weight rows x 8 tokens x one whole 32-block per
+// instruction, the raw codes as operands (Q8_0 codes as they are, Q4_K nibbles masked to
+// bytes 0..15), no conversion.  A CTA owns `tpc` consecutive 16-row tiles; its 8 warps split
+// each tile's K round-robin in pieces (warp w takes pieces w, w + 8, ...), a piece being 16
+// rows x one Q4_K super-block (2304 B) or x 8 Q8_0 blocks (4352 B), brought by one 2-D tensor
+// copy into the warp's own ring (rows past N arrive as zeros).  The activation codes (B
+// fragments) and scales are read from global memory (L2-resident q8_1 rows); k is permuted
+// identically in A and B (a thread's 8 values of a block are 8 contiguous bytes), which
+// leaves every block dot unchanged.  Each block's int32 dots are rescaled in registers at
+// once (Q4_K: per super-block, sum_j sc_j*xd*D_j and sum_j m_j*xs, then d and -dmin); the
+// warps' partial sums of a tile meet in shared memory at the end.  Needs K % 256 == 0.
+constexpr int IS_WARPS = 8;
 
-constexpr int GV_WARPS = 8;
-constexpr int GV_STAGES = 3;
-constexpr uint64_t GV_WAIT_LIMIT_NS = 2000000000ull;
-__host__ __device__ constexpr int gv_piece_blocks(int fmt) { return 32; }
-__host__ __device__ constexpr int gv_piece_bytes(int fmt) {  // weight bytes of one row per piece
-    return fmt == FMT_Q8_0 ? gv_piece_blocks(fmt) * Q8_0_BYTES : gv_piece_blocks(fmt) / 8 * Q4_K_BYTES;
+__host__ __device__ constexpr int is_row_bytes(int fmt) { return fmt == FMT_Q4_K ? Q4_K_BYTES : 8 * Q8_0_BYTES; }
+__host__ __device__ constexpr int is_slot_bytes(int fmt) { return 16 * is_row_bytes(fmt); }  // 2304 / 4352
+__host__ __device__ constexpr int is_slots(int fmt) { return fmt == FMT_Q4_K ? 4 : 2; }
+__host__ __device__ constexpr int is_smem_bytes(int fmt, int tpc) {
+    return IS_WARPS * is_slots(fmt) * (is_slot_bytes(fmt) + 8) + tpc * IS_WARPS * 16 * 8 * 4;
 }
-// activation bytes per token per piece in shared memory, padded by 16 B so that the 8
-// token rows start in different banks
-__host__ __device__ constexpr int gv_act_stride(int fmt) { return gv_piece_blocks(fmt) * Q8_1_BYTES + 16; }
-__host__ __device__ constexpr int gv_stage_bytes(int fmt, int R) { return R * gv_piece_bytes(fmt) + 8 * gv_act_stride(fmt); }
-__host__ __device__ constexpr int gv_table_bytes(int fmt, int R) { return fmt == FMT_Q4_K ? R * gv_piece_blocks(fmt) * 8 : 0; }
-__host__ __device__ constexpr int gv_smem_bytes(int fmt, int R) {
-    return GV_STAGES * gv_stage_bytes(fmt, R) + gv_table_bytes(fmt, R) + GV_WARPS * R * 8 * 4 + 2 * GV_STAGES * 8 + 16;
+constexpr int IS_MAX_TPC = 4;
+static_assert(is_smem_bytes(FMT_Q8_0, IS_MAX_TPC) <= 110 * 1024 && is_slot_bytes(FMT_Q4_K) % 128 == 0 &&
+                  is_slot_bytes(FMT_Q8_0) % 128 == 0,
+              "two CTAs per SM; 128-byte aligned slots");
+
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
 }
 
-template <int FMT, int R>
-__global__ void __launch_bounds__(GV_WARPS * 32)
-k_mmq_gemv(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ xq, int M, int N, int nb,
-           float* __restrict__ out, int32_t* __restrict__ dots) {
-    constexpr int RT = R / 16;  // mma row tiles per warp
-    constexpr int PBLK = gv_piece_blocks(FMT), PB = gv_piece_bytes(FMT), AS = gv_act_stride(FMT);
-    constexpr int SB = gv_stage_bytes(FMT, R);
-    extern __shared__ __align__(128) uint8_t gv_smem[];
-    float2* table = reinterpret_cast<float2*>(gv_smem + GV_STAGES * SB);                    // [R][PBLK]
-    float(*red)[R][8] = reinterpret_cast<float(*)[R][8]>(gv_smem + GV_STAGES * SB + gv_table_bytes(FMT, R));
-    const uint32_t bar0 = ptx::smem_u32(gv_smem + GV_STAGES * SB + gv_table_bytes(FMT, R) + GV_WARPS * R * 8 * 4);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int n0 = blockIdx.x * R, m0 = blockIdx.y * 8;
-    const int nrows = min(R, N - n0), ntok = min(8, M - m0);
-    const int t0 = 2 * q, t1 = t0 + 1;  // D-fragment tokens (local)
-    const long long xrow_bytes = (long long)nb * Q8_1_BYTES;
-    const int npieces = (nb + PBLK - 1) / PBLK;
-    float acc[RT][4];
-#pragma unroll
-    for (int r = 0; r < RT; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+template <int FMT>
+__global__ void __launch_bounds__(IS_WARPS * 32, 2)
+k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ xq, int M, int N, int nb,
+                int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
+    constexpr int S = is_slots(FMT), SLOT = is_slot_bytes(FMT), RB = is_row_bytes(FMT);
+    extern __shared__ __align__(128) uint8_t is_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    uint8_t* ring = is_smem + warp * S * SLOT;
+    const uint32_t bar0 = ptx::smem_u32(is_smem + IS_WARPS * S * SLOT) + 8 * S * warp;
+    float* red = reinterpret_cast<float*>(is_smem + IS_WARPS * S * (SLOT + 8));  // [tpc][IS_WARPS][16][8]
+    const int ntiles = (N + 15) / 16;
+    const int t0 = blockIdx.x * tpc, nt = min(tpc, ntiles - t0);
+    const int npieces = nb / 8;  // Q4_K super-blocks, or groups of 8 Q8_0 blocks
+    const int my = warp < npieces ? (npieces - 1 - warp) / IS_WARPS + 1 : 0;  // this warp's pieces per tile
+    const int total = nt * my;
+    const int m0 = blockIdx.y * 8;
+    const long long xrow = (long long)nb * Q8_1_BYTES;
+    // B fragment: token g's codes 8q .. 8q + 7 of a block; D fragment tokens 2q and 2q + 1
+    const bool bok = m0 + g < M, h0ok = m0 + 2 * q < M, h1ok = m0 + 2 * q + 1 < M;
+    const uint8_t* xb = xq + (long long)(bok ? m0 + g : 0) * xrow + 4 + 8 * q;
+    const uint8_t* xh0 = xq + (long long)(h0ok ? m0 + 2 * q : 0) * xrow;
+    const uint8_t* xh1 = xq + (long long)(h1ok ? m0 + 2 * q + 1 : 0) * xrow;
 
-    auto issue = [&](int p) {  // thread 0: the copies of piece p into stage p % GV_STAGES
-        const int kb0 = p * PBLK, pb = min(PBLK, nb - kb0);
-        const uint32_t abytes = (uint32_t)pb * Q8_1_BYTES;
-        uint8_t* st = gv_smem + (p % GV_STAGES) * SB;
-        const uint32_t bar = bar0 + 8 * (p % GV_STAGES);
-        // the tensor copy counts its whole box, zero-filled parts included
-        ptx::mbar_arrive_expect_tx(bar, (uint32_t)(R * PB) + abytes * (uint32_t)ntok);
-        ptx::tma_load_2d(ptx::smem_u32(st), &tmW, bar, p * (PB / 8), n0);
-        for (int t = 0; t < ntok; ++t)
-            ptx::bulk_load(ptx::smem_u32(st + R * PB + t * AS),
-                           xq + (long long)(m0 + t) * xrow_bytes + (long long)kb0 * Q8_1_BYTES, abytes, bar);
+    auto issue = [&](int i) {  // lane 0: the copy of this warp's piece i into slot i % S
+        const int k = i / nt, tl = i - k * nt;  // piece-major: a piece's activations serve all tiles
+        const int p = warp + k * IS_WARPS;
+        const uint32_t bar = bar0 + 8 * (i % S);
+        ptx::mbar_arrive_expect_tx(bar, SLOT);  // the whole box, zero-filled rows included
+        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, p * (RB / 8), (t0 + tl) * 16);
     };
-    int issued = 0;  // thread 0: pieces whose copies were issued
-    if (threadIdx.x == 0) {
+    // the piece's activation words: codes (B) of token g and f16 d|s headers of tokens 2q,
+    // 2q + 1, for its 8 blocks
+    auto load_acts = [&](int p, uint32_t (&bw)[8][2], uint32_t (&h0)[8], uint32_t (&h1)[8]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const long long bo = (long long)(8 * p + j) * Q8_1_BYTES;
+            bw[j][0] = bok ? __ldg(reinterpret_cast<const uint32_t*>(xb + bo)) : 0u;
+            bw[j][1] = bok ? __ldg(reinterpret_cast<const uint32_t*>(xb + bo + 4)) : 0u;
+            h0[j] = h0ok ? __ldg(reinterpret_cast<const uint32_t*>(xh0 + bo)) : 0u;
+            h1[j] = h1ok ? __ldg(reinterpret_cast<const uint32_t*>(xh1 + bo)) : 0u;
+        }
+    };
+    int issued = 0;
+    if (lane == 0) {
         ptx::tma_prefetch_desc(&tmW);
-        for (int i = 0; i < GV_STAGES; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
+        for (int i = 0; i < S; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
         ptx::fence_barrier_init();
-        for (; issued < GV_STAGES - 1 && issued < npieces; ++issued) issue(issued);
     }
-    __syncthreads();
+    __syncwarp();
+    for (; issued < S && issued < total; ++issued)
+        if (lane == 0) issue(issued);
+
     bool ok = true;
-    for (int p = 0; p < npieces; ++p) {
-        // the stage of piece p + 2 was freed by the __syncthreads that ended piece p - 1
-        if (threadIdx.x == 0 && issued < npieces) issue(issued++);
-        const uint32_t bar = bar0 + 8 * (p % GV_STAGES);
-        const uint32_t parity = (p / GV_STAGES) & 1;
-        if (!ptx::mbar_try_wait(bar, parity)) {
-            const uint64_t t_start = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(bar, parity)) {
-                if (ptx::globaltimer_ns() - t_start > GV_WAIT_LIMIT_NS) {
-                    atomicOr(&g_small_error, ERR_TIMEOUT);
-                    ok = false;
-                    break;
-                }
+    int i = 0;
+    float acc[IS_MAX_TPC][4];  // per tile: rows g, g + 8 x tokens 2q, 2q + 1
+#pragma unroll
+    for (int tl = 0; tl < IS_MAX_TPC; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
+    // Q8_0 loads the next piece's activations while computing this one (measured faster);
+    // for Q4_K the extra registers cost more than the overlap gains
+    constexpr bool PREFETCH = FMT == FMT_Q8_0;
+    uint32_t bw[8][2], h0[8], h1[8];
+    if (PREFETCH && my > 0) load_acts(warp, bw, h0, h1);
+    for (int k = 0; k < my && ok; ++k) {
+        const int p = warp + k * IS_WARPS;
+        const int b0 = 8 * p;  // first block of the piece
+        uint32_t nbw[8][2], nh0[8], nh1[8];
+        if (!PREFETCH) load_acts(p, bw, h0, h1);
+        else if (k + 1 < my) load_acts(p + IS_WARPS, nbw, nh0, nh1);
+#pragma unroll
+        for (int tl = 0; tl < IS_MAX_TPC; ++tl) {
+            if (tl >= nt) break;
+            const int n0 = (t0 + tl) * 16;
+            if (!ds_wait(bar0 + 8 * (i % S), (i / S) & 1)) {
+                ok = false;
+                break;
             }
-        }
-        if (__syncthreads_or(!ok)) {
-            ok = false;
-            break;
-        }
-        const uint8_t* tile = gv_smem + (p % GV_STAGES) * SB;
-        const uint8_t* act = tile + R * PB;
-        const int kb0 = p * PBLK, pb = min(PBLK, nb - kb0);
-        if (FMT == FMT_Q4_K && !dots) {
-            // (d*sc_j, dmin*m_j) of every (row, sub-block) of the piece, once
-            for (int e = threadIdx.x; e < R * (PBLK / 8); e += GV_WARPS * 32) {
-                const int r = e / (PBLK / 8), sbi = e % (PBLK / 8);
-                if (8 * sbi >= pb) continue;
-                const uint4 h = *reinterpret_cast<const uint4*>(tile + r * PB + sbi * Q4_K_BYTES);
-                const float d = f16_bits_to_f32(h.x), dmin = f16_bits_to_f32(h.x >> 16);
+            const uint8_t* sl = ring + (i % S) * SLOT;
+            if (FMT == FMT_Q4_K) {
+                const uint8_t* rg = sl + g * RB;
+                const uint8_t* rh = sl + (g + 8) * RB;
+                const uint4 hg = *reinterpret_cast<const uint4*>(rg), hh = *reinterpret_cast<const uint4*>(rh);
+                // 6-bit scales and mins of sub-blocks 0..3 / 4..7, one per byte
+                const uint32_t scg[2] = {hg.y & 0x3F3F3F3Fu, (hg.w & 0x0F0F0F0Fu) | ((hg.y >> 2) & 0x30303030u)};
+                const uint32_t mng[2] = {hg.z & 0x3F3F3F3Fu, ((hg.w >> 4) & 0x0F0F0F0Fu) | ((hg.z >> 2) & 0x30303030u)};
+                const uint32_t sch[2] = {hh.y & 0x3F3F3F3Fu, (hh.w & 0x0F0F0F0Fu) | ((hh.y >> 2) & 0x30303030u)};
+                const uint32_t mnh[2] = {hh.z & 0x3F3F3F3Fu, ((hh.w >> 4) & 0x0F0F0F0Fu) | ((hh.z >> 2) & 0x30303030u)};
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f}, macc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    int sc, mn;
-                    q4_k_scale_min(h.y, h.z, h.w, j, sc, mn);
-                    table[r * PBLK + 8 * sbi + j] = make_float2(d * (float)sc, dmin * (float)mn);  // exact
-                }
-            }
-            __syncthreads();
-        }
-        for (int bl = warp; bl < pb; bl += GV_WARPS) {
-            const int b = kb0 + bl;  // block index within the row
-            // activation B fragments of token g (zeros past ntok), reused for every row tile
-            uint32_t xw0 = 0u, xw1 = 0u;
-            if (g < ntok) {
-                const uint32_t* xc = reinterpret_cast<const uint32_t*>(act + g * AS + bl * Q8_1_BYTES + 4 + 8 * q);
-                xw0 = xc[0];
-                xw1 = xc[1];
-            }
-            uint32_t b_lo0, b_lo1, b_hi0, b_hi1;
-            s8x4_h2(xw0, b_lo0, b_lo1);
-            s8x4_h2(xw1, b_hi0, b_hi1);
-            float xd0 = 0.f, xs0 = 0.f, xd1 = 0.f, xs1 = 0.f;
-            if (!dots) {
-                const uint32_t h0 = t0 < ntok ? *reinterpret_cast<const uint32_t*>(act + t0 * AS + bl * Q8_1_BYTES) : 0u;
-                const uint32_t h1 = t1 < ntok ? *reinterpret_cast<const uint32_t*>(act + t1 * AS + bl * Q8_1_BYTES) : 0u;
-                xd0 = f16_bits_to_f32(h0);
-                xs0 = f16_bits_to_f32(h0 >> 16);
-                xd1 = f16_bits_to_f32(h1);
-                xs1 = f16_bits_to_f32(h1 >> 16);
-            }
-#pragma unroll
-            for (int rt = 0; rt < RT; ++rt) {
-                uint32_t a_lo[4], a_hi[4];
-                float ws[2], wm[2];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = 16 * rt + g + 8 * i;  // rows past N are zeros; their sums are never stored
-                    const uint8_t* rowp = tile + r * PB;
-                    if (FMT == FMT_Q4_K) {
-                        const uint8_t* sbk = rowp + (bl >> 3) * Q4_K_BYTES;
-                        const uint2 wv = *reinterpret_cast<const uint2*>(sbk + 16 + 32 * ((bl >> 1) & 3) + 8 * q);
-                        const int shift = 4 * (bl & 1);
-                        u4x4_h2((wv.x >> shift) & 0x0F0F0F0Fu, a_lo[i], a_lo[i + 2]);
-                        u4x4_h2((wv.y >> shift) & 0x0F0F0F0Fu, a_hi[i], a_hi[i + 2]);
-                        if (!dots) {
-                            const float2 t = table[r * PBLK + bl];
-                            ws[i] = t.x;
-                            wm[i] = t.y;
-                        }
-                    } else {
-                        const uint8_t* blk = rowp + bl * Q8_0_BYTES;
-                        const int o = 2 + 8 * q + (bl & 1) * 2;  // byte offset of the codes, mod 4
-                        const uint32_t* a = reinterpret_cast<const uint32_t*>(blk + 2 + 8 * q - (o & 2));
-                        uint32_t w0 = a[0], w1 = a[1];
-                        if (o & 2) {
-                            const uint32_t w2 = a[2];
-                            w0 = __funnelshift_r(w0, w1, 16);
-                            w1 = __funnelshift_r(w1, w2, 16);
-                        }
-                        s8x4_h2(w0, a_lo[i], a_lo[i + 2]);
-                        s8x4_h2(w1, a_hi[i], a_hi[i + 2]);
-                        ws[i] = dots ? 0.f : f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(blk));
-                        wm[i] = 0.f;
+                    const int sh = 4 * (j & 1), off = 16 + 32 * (j >> 1) + 8 * q;
+                    const uint2 wg = *reinterpret_cast<const uint2*>(rg + off);
+                    const uint2 wh = *reinterpret_cast<const uint2*>(rh + off);
+                    int D[4];
+                    mma_s8_16832(D, (wg.x >> sh) & 0x0F0F0F0Fu, (wh.x >> sh) & 0x0F0F0F0Fu, (wg.y >> sh) & 0x0F0F0F0Fu,
+                                 (wh.y >> sh) & 0x0F0F0F0Fu, bw[j][0], bw[j][1]);
+                    if (dots) {
+                        const int b = b0 + j;
+                        if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D[0];
+                        if (h1ok && n0 + g < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g) * nb + b] = D[1];
+                        if (h0ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q) * N + n0 + g + 8) * nb + b] = D[2];
+                        if (h1ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g + 8) * nb + b] = D[3];
+                        continue;
                     }
+                    const float xd0 = f16_bits_to_f32(h0[j]), xs0 = f16_bits_to_f32(h0[j] >> 16);
+                    const float xd1 = f16_bits_to_f32(h1[j]), xs1 = f16_bits_to_f32(h1[j] >> 16);
+                    const float sg = byte_f32(scg[j >> 2], j & 3), sh8 = byte_f32(sch[j >> 2], j & 3);
+                    const float mg = byte_f32(mng[j >> 2], j & 3), mh = byte_f32(mnh[j >> 2], j & 3);
+                    sacc[0] = fmaf(sg * xd0, (float)D[0], sacc[0]);
+                    sacc[1] = fmaf(sg * xd1, (float)D[1], sacc[1]);
+                    sacc[2] = fmaf(sh8 * xd0, (float)D[2], sacc[2]);
+                    sacc[3] = fmaf(sh8 * xd1, (float)D[3], sacc[3]);
+                    macc[0] = fmaf(mg, xs0, macc[0]);
+                    macc[1] = fmaf(mg, xs1, macc[1]);
+                    macc[2] = fmaf(mh, xs0, macc[2]);
+                    macc[3] = fmaf(mh, xs1, macc[3]);
                 }
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma16816(d, a_lo, b_lo0, b_lo1);
-                mma16816(d, a_hi, b_hi0, b_hi1);
-                if (dots) {
-                    const int rw[2] = {n0 + 16 * rt + g, n0 + 16 * rt + g + 8}, tt[2] = {m0 + t0, m0 + t1};
+                if (!dots) {
+                    const float dg = f16_bits_to_f32(hg.x), dmg = f16_bits_to_f32(hg.x >> 16);
+                    const float dh = f16_bits_to_f32(hh.x), dmh = f16_bits_to_f32(hh.x >> 16);
+                    acc[tl][0] = fmaf(-dmg, macc[0], fmaf(dg, sacc[0], acc[tl][0]));
+                    acc[tl][1] = fmaf(-dmg, macc[1], fmaf(dg, sacc[1], acc[tl][1]));
+                    acc[tl][2] = fmaf(-dmh, macc[2], fmaf(dh, sacc[2], acc[tl][2]));
+                    acc[tl][3] = fmaf(-dmh, macc[3], fmaf(dh, sacc[3], acc[tl][3]));
+                }
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (rw[e >> 1] < N && tt[e & 1] < M)
-                            dots[((long long)tt[e & 1] * N + rw[e >> 1]) * nb + b] = __float2int_rn(d[e]);
-                } else {
-                    acc[rt][0] = fmaf(xd0 * ws[0], d[0], acc[rt][0]);
-                    acc[rt][1] = fmaf(xd1 * ws[0], d[1], acc[rt][1]);
-                    acc[rt][2] = fmaf(xd0 * ws[1], d[2], acc[rt][2]);
-                    acc[rt][3] = fmaf(xd1 * ws[1], d[3], acc[rt][3]);
-                    if (FMT == FMT_Q4_K) {
-                        acc[rt][0] = fmaf(-wm[0], xs0, acc[rt][0]);
-                        acc[rt][1] = fmaf(-wm[0], xs1, acc[rt][1]);
-                        acc[rt][2] = fmaf(-wm[1], xs0, acc[rt][2]);
-                        acc[rt][3] = fmaf(-wm[1], xs1, acc[rt][3]);
+                for (int j = 0; j < 8; ++j) {
+                    // codes 8q .. 8q + 7 of block j of rows g and g + 8: 2-byte aligned, read as
+                    // aligned words and funnel-shifted (a third word only when the shift is 16)
+                    const int off = j * Q8_0_BYTES + 2 + 8 * q, sh = (off & 3) * 8;
+                    const uint32_t* pg = reinterpret_cast<const uint32_t*>(sl + g * RB + (off & ~3));
+                    const uint32_t* ph = reinterpret_cast<const uint32_t*>(sl + (g + 8) * RB + (off & ~3));
+                    const uint32_t g0 = pg[0], g1 = pg[1], g2 = sh ? pg[2] : 0u;
+                    const uint32_t e0 = ph[0], e1 = ph[1], e2 = sh ? ph[2] : 0u;
+                    int D[4];
+                    mma_s8_16832(D, __funnelshift_r(g0, g1, sh), __funnelshift_r(e0, e1, sh), __funnelshift_r(g1, g2, sh),
+                                 __funnelshift_r(e1, e2, sh), bw[j][0], bw[j][1]);
+                    if (dots) {
+                        const int b = b0 + j;
+                        if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D[0];
+                        if (h1ok && n0 + g < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g) * nb + b] = D[1];
+                        if (h0ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q) * N + n0 + g + 8) * nb + b] = D[2];
+                        if (h1ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g + 8) * nb + b] = D[3];
+                        continue;
                     }
+                    const float wg = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sl + g * RB + j * Q8_0_BYTES));
+                    const float wh =
+                        f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sl + (g + 8) * RB + j * Q8_0_BYTES));
+                    const float xd0 = f16_bits_to_f32(h0[j]), xd1 = f16_bits_to_f32(h1[j]);
+                    acc[tl][0] = fmaf(wg * xd0, (float)D[0], acc[tl][0]);
+                    acc[tl][1] = fmaf(wg * xd1, (float)D[1], acc[tl][1]);
+                    acc[tl][2] = fmaf(wh * xd0, (float)D[2], acc[tl][2]);
+                    acc[tl][3] = fmaf(wh * xd1, (float)D[3], acc[tl][3]);
                 }
             }
+            // every lane is done with the slot: refill it with the piece S ahead
+            __syncwarp();
+            if (issued < total) {
+                if (lane == 0) {
+                    ptx::fence_proxy_async_smem();
+                    issue(issued);
+                }
+                ++issued;
+            }
+            ++i;
         }
-        __syncthreads();  // every warp is done with the stage and the table
+        if (PREFETCH && k + 1 < my) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                bw[j][0] = nbw[j][0];
+                bw[j][1] = nbw[j][1];
+                h0[j] = nh0[j];
+                h1[j] = nh1[j];
+            }
+        }
     }
-    if (!ok) {
-        // copies of the pieces still in flight must land before the CTA exits
-        if (threadIdx.x == 0)
-            for (int p = issued - GV_STAGES < 0 ? 0 : issued - GV_STAGES; p < issued; ++p) {
-                const uint64_t t_start = ptx::globaltimer_ns();
-                while (!ptx::mbar_try_wait(bar0 + 8 * (p % GV_STAGES), (p / GV_STAGES) & 1))
-                    if (ptx::globaltimer_ns() - t_start > GV_WAIT_LIMIT_NS) break;
-            }
-        return;
+    if (ok && !dots && my > 0) {
+#pragma unroll
+        for (int tl = 0; tl < IS_MAX_TPC; ++tl) {
+            if (tl >= nt) break;
+            float* rw = red + (tl * IS_WARPS + warp) * 16 * 8;
+            rw[g * 8 + 2 * q] = acc[tl][0];
+            rw[g * 8 + 2 * q + 1] = acc[tl][1];
+            rw[(g + 8) * 8 + 2 * q] = acc[tl][2];
+            rw[(g + 8) * 8 + 2 * q + 1] = acc[tl][3];
+        }
+    }
+    if (!ok && lane == 0) {
+        // copies still in flight must land before the CTA exits
+        for (int k2 = i; k2 < issued; ++k2) {
+            const uint64_t tb = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar0 + 8 * (k2 % S), (k2 / S) & 1))
+                if (ptx::globaltimer_ns() - tb > DS_WAIT_LIMIT_NS) break;
+        }
     }
     if (dots) return;
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-        red[warp][16 * rt + g][t0] = acc[rt][0];
-        red[warp][16 * rt + g][t1] = acc[rt][1];
-        red[warp][16 * rt + g + 8][t0] = acc[rt][2];
-        red[warp][16 * rt + g + 8][t1] = acc[rt][3];
-    }
     __syncthreads();
-    for (int e = threadIdx.x; e < R * 8; e += GV_WARPS * 32) {
-        const int rr = e >> 3, tt = e & 7;
+    if (__syncthreads_or(!ok)) return;
+    const int nw = min(npieces, IS_WARPS);  // warps that hold partial sums
+    for (int e = threadIdx.x; e < nt * 16 * 8; e += IS_WARPS * 32) {
+        const int tl = e >> 7, r = (e >> 3) & 15, tok = e & 7;
         float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < GV_WARPS; ++w) v += red[w][rr][tt];
-        if (rr < nrows && tt < ntok) out[(long long)(m0 + tt) * N + n0 + rr] = v;
+        for (int w = 0; w < nw; ++w) v += red[((tl * IS_WARPS + w) * 16 + r) * 8 + tok];
+        const int n = (t0 + tl) * 16 + r;
+        if (n < N && m0 + tok < M) out[(long long)(m0 + tok) * N + n] = v;
     }
 }
 
-static_assert(gv_smem_bytes(FMT_Q4_K, 64) <= 227 * 1024 && gv_smem_bytes(FMT_Q8_0, 32) <= 227 * 1024, "smem");
-
-template <int FMT, int R>
-int launch_gemv_r(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
-                  cudaStream_t s, const char* fn) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_gemv<FMT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             gv_smem_bytes(FMT, R));
+template <int FMT>
+int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
+                     int32_t* dots, cudaStream_t s, const char* fn) {
+    const int64_t ntiles = (N + 15) / 16;
+    const DeviceShape dsh = device_shape();
+    // tiles per CTA: the fewest (at most IS_MAX_TPC) that keep the grid within the two
+    // CTAs per SM that are resident at once (no second, partial wave)
+    int64_t tpc = (ntiles + 2 * (int64_t)dsh.sms - 1) / (2 * (int64_t)dsh.sms);
+    tpc = tpc < 1 ? 1 : (tpc > IS_MAX_TPC ? IS_MAX_TPC : tpc);
+    const int smem = is_smem_bytes(FMT, (int)tpc);
+    static int attr_bytes = 0;
+    if (smem > 48 * 1024 && smem > attr_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(k_mmq_i8_stream<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             is_smem_bytes(FMT, IS_MAX_TPC));
         if (e != cudaSuccess) {
             cudaGetLastError();
             report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
             return MMQ_ERR_SMEM;
         }
-        attr_done = true;
+        attr_bytes = is_smem_bytes(FMT, IS_MAX_TPC);
     }
     CUtensorMap tm;
     const uint64_t row_bytes = FMT == FMT_Q8_0 ? (uint64_t)nb * Q8_0_BYTES : (uint64_t)(nb / 8) * Q4_K_BYTES;
-    if (!make_byte_map(&tm, w8, row_bytes, (uint64_t)N, gv_piece_bytes(FMT), R, 8)) {
+    if (!make_byte_map(&tm, w8, row_bytes, (uint64_t)N, is_row_bytes(FMT), 16, 8)) {
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
     }
-    dim3 grid((unsigned)((N + R - 1) / R), (unsigned)((M + 7) / 8));
+    dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
     {
-        ProfScope ps("k_mmq_gemv", s);
-        k_mmq_gemv<FMT, R><<<grid, GV_WARPS * 32, gv_smem_bytes(FMT, R), s>>>(tm, x8, (int)M, (int)N, nb, out, dots);
+        ProfScope ps("k_mmq_i8_stream", s);
+        k_mmq_i8_stream<FMT><<<grid, IS_WARPS * 32, smem, s>>>(tm, x8, (int)M, (int)N, nb, (int)tpc, out, dots);
     }
     return launch_status(fn);
-}
-
-// Rows per CTA: the most (fewest activation conversions per weight) that still gives
-// about two CTAs per SM.
-template <int FMT>
-int launch_gemv(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
-                cudaStream_t s) {
-    const char* fn = FMT == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
-    const int64_t passes = (M + 7) / 8;
-    // (Q8_0 pieces are twice as long: 64 rows of them would not fit three stages)
-    if (FMT == FMT_Q4_K && passes * ((N + 63) / 64) >= 2 * 152)
-        return launch_gemv_r<FMT, 64>(x8, w8, M, N, nb, out, dots, s, fn);
-    if (passes * ((N + 31) / 32) >= 2 * 152) return launch_gemv_r<FMT, 32>(x8, w8, M, N, nb, out, dots, s, fn);
-    return launch_gemv_r<FMT, 16>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
 }  // namespace
@@ -945,17 +958,16 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     }
     const uint8_t* x8 = static_cast<const uint8_t*>(xq);
     const uint8_t* w8 = static_cast<const uint8_t*>(wq);
-    // measured: the dp4a weight streams beat the tensor-core stream up to 4 rows in both
-    // formats and up to 8 for Q8_0; Q4_K at 5 to 8 rows goes to the tensor-core stream
-    const int64_t dp4a_max_m = fmt == FMT_Q8_0 ? 8 : 4;
-    if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8, 4, nb) <= 220 * 1024) {
-        const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
-        return fmt == FMT_Q8_0 ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, fn)
-                               : launch_dp4a_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, fn);
-    }
+    const char* sfn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
+    // measured crossovers: the dp4a weight streams for one or two rows (and Q4_K up to four),
+    // the int8 tensor-core stream beyond, one pass per 8 rows
+    const int64_t dp4a_max_m = fmt == FMT_Q4_K ? 4 : 2;
+    if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
+        return fmt == FMT_Q8_0 ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
+                               : launch_dp4a_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, sfn);
     if (nb % 8 == 0)
-        return fmt == FMT_Q8_0 ? launch_gemv<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s)
-                               : launch_gemv<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s);
+        return fmt == FMT_Q8_0 ? launch_i8_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
+                               : launch_i8_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, sfn);
     if (nb % 2 == 0) {
         dim3 g2((unsigned)((N + 15) / 16), (unsigned)((M + 7) / 8));
         ProfScope ps("k_mmq_small_mma", s);
