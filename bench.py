@@ -424,29 +424,58 @@ def run_ours(args, rank, world, local):
                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload), "kernel": kname,
                     "peak_source": peaks["source"] + " hbm_gbs"}
 
-    # end to end through the public API: pinned host x -> device, step, out -> host
+    # end to end through the public API: every step copies its input from pinned host memory
+    # to the device, runs the fused quantize + contraction and copies the result back to
+    # pinned host memory.  The three run on their own streams with two device buffers each
+    # way, ordered by events, so the copies of neighbouring steps overlap a step's compute
+    # (the way a serving loop feeds the GPU); throughput is taken over all steps.
     e2e = None
     if not quant_only:
         xh = torch.from_numpy(x).pin_memory()
         oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        xd = torch.empty_like(xs[0])
-        for i in range(3):
-            xd.copy_(xh, non_blocking=True)
-            mmq.mmq_linear(xd, ws[i % copies], fmt, N, xq=xq, out=out, stream=stream)
-            oh.copy_(out, non_blocking=True)
+        nbuf = 2
+        xd = [torch.empty_like(xs[0]) for _ in range(nbuf)]
+        od = [torch.empty((M, N), device=dev) for _ in range(nbuf)]
+        s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        in_done = [torch.cuda.Event() for _ in range(nbuf)]
+        comp_done = [torch.cuda.Event() for _ in range(nbuf)]
+        out_done = [torch.cuda.Event() for _ in range(nbuf)]
+
+        def e2e_steps(n):
+            for i in range(n):
+                bi = i % nbuf
+                if i >= nbuf:
+                    s_in.wait_event(comp_done[bi])   # the input buffer's last reader is done
+                with torch.cuda.stream(s_in):
+                    xd[bi].copy_(xh, non_blocking=True)
+                in_done[bi].record(s_in)
+                s_comp.wait_event(in_done[bi])
+                if i >= nbuf:
+                    s_comp.wait_event(out_done[bi])  # the output buffer's last copy is done
+                mmq.mmq_linear(xd[bi], ws[i % copies], fmt, N, xq=xq, out=od[bi], stream=s_comp)
+                comp_done[bi].record(s_comp)
+                s_out.wait_event(comp_done[bi])
+                with torch.cuda.stream(s_out):
+                    oh.copy_(od[bi], non_blocking=True)
+                out_done[bi].record(s_out)
+
+        for st in (s_in, s_comp, s_out):
+            st.wait_stream(stream)
+        e2e_steps(3)
         torch.cuda.synchronize(dev)
+        assert np.array_equal(oh.numpy(), od[2 % nbuf].cpu().numpy()), "e2e output not copied back"
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_steps = min(steps, E2E_STEPS)
-        a.record(stream)
-        for i in range(e_steps):
-            xd.copy_(xh, non_blocking=True)
-            mmq.mmq_linear(xd, ws[i % copies], fmt, N, xq=xq, out=out, stream=stream)
-            oh.copy_(out, non_blocking=True)
-        b.record(stream)
+        a.record(s_in)
+        s_comp.wait_event(a)
+        s_out.wait_event(a)
+        e2e_steps(e_steps)
+        b.record(s_out)
         torch.cuda.synchronize(dev)
         e_ms = a.elapsed_time(b)
         e2e = {"value": ops * e_steps / (e_ms / 1e3) / 1e12, "unit": "TOPS", "steps": e_steps,
-               "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": M * N * 4}
+               "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": M * N * 4,
+               "overlap": "copy-in, compute and copy-out on three streams, two buffers each way"}
 
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
