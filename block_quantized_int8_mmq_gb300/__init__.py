@@ -22,7 +22,7 @@ EXPORTED = (
     "mmq_status_string", "mmq_q8_1_bytes", "mmq_weight_row_bytes", "mmq_quantize_q8_1",
     "mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k",
     "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
-    "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k",
+    "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k",
 )
 
 
@@ -56,6 +56,8 @@ def _load():
     L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
     for f in ("mmq_linear_q8_0", "mmq_linear_q4_k"):
         getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
+    for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k"):
+        getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
     return L
@@ -192,6 +194,18 @@ def gemm(fmt: str, xq, wq, M, N, K, out=None, stream=None):
 def block_dots(fmt: str, xq, wq, M, N, K, dots=None, stream=None):
     f = mmq_debug_block_dots_q8_0 if fmt == "q8_0" else mmq_debug_block_dots_q4_k
     return f(xq, wq, M, N, K, dots, stream)
+
+
+def mmq_gemm_grouped(fmt: str, xq, row_expert, wq, E: int, N: int, K: int, out=None, stream=None):
+    """Expert-grouped contraction: row r of xq (q8_1 [R, K/32*36]) with expert
+    row_expert[r] (int32 [R]) of wq (E matrices stacked, [E*N, ...] blocks): f32 [R, N]."""
+    import torch
+    R = xq.shape[0]
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.float32, device=xq.device)
+    fn = "mmq_gemm_grouped_q8_0" if fmt == "q8_0" else "mmq_gemm_grouped_q4_k"
+    _check(fn, getattr(_lib, fn)(_ptr(xq), _ptr(row_expert), R, _ptr(wq), E, N, K, _ptr(out), _stream(stream)))
+    return out
 
 
 def mmq_linear(x, wq, fmt: str, N: int, xq=None, out=None, stream=None):

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmmq.so")
-SOURCES = ["abi.cu", "quantize.cu", "gemm_small.cu", "gemm_tc.cu", "gemm_expand.cu", "profile.cu"]
+SOURCES = ["abi.cu", "quantize.cu", "gemm_small.cu", "gemm_tc.cu", "gemm_expand.cu", "grouped.cu", "profile.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                 "-I", os.path.join(ROOT, "include")]

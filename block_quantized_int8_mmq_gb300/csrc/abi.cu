@@ -144,6 +144,33 @@ int linear(const char* fn, int fmt, const float* x, int64_t M, int64_t K, const 
     return st;
 }
 
+// Expert-grouped contraction: rows grouped by expert on the device, then the converter
+// tensor-core kernel over the tile list (needs tcgen05 and K % 256 == 0).
+int grouped(const char* fn, int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E,
+            int64_t N, int64_t K, float* out, void* stream) {
+    int st = check_mk(fn, R, N, K, QK_K);
+    if (st) return st;
+    if (E < 1 || E > (int64_t)1 << 20 || E * N > 0x7fffffff || E > LIMIT / N / (K / QK)) {
+        report(fn, MMQ_ERR_SHAPE, "E must be in 1 .. 2^20 and E*N rows below 2^31");
+        return MMQ_ERR_SHAPE;
+    }
+    if (!xq || !row_expert || !wq || !out) {
+        report(fn, MMQ_ERR_NULL, "xq, row_expert, wq and out must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(out, 16) || !aligned(row_expert, 4)) {
+        report(fn, MMQ_ERR_ALIGN, "xq, wq and out must be 16-byte aligned, row_expert 4-byte aligned");
+        return MMQ_ERR_ALIGN;
+    }
+    if (!tc_available()) {
+        report(fn, MMQ_ERR_LAUNCH, "the grouped contraction needs the tcgen05 tensor cores");
+        return MMQ_ERR_LAUNCH;
+    }
+    st = grouped_launch(fmt, xq, row_expert, R, wq, E, N, K, out, static_cast<cudaStream_t>(stream));
+    if (st == MMQ_OK) t_last_path = MMQ_PATH_TC;
+    return st;
+}
+
 }  // namespace
 }  // namespace mmq
 
@@ -211,6 +238,16 @@ int mmq_linear_q8_0(const float* x, int64_t M, int64_t K, const void* wq, int64_
 int mmq_linear_q4_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
                     void* stream) {
     return linear("mmq_linear_q4_k", FMT_Q4_K, x, M, K, wq, N, xq, out, stream);
+}
+
+int mmq_gemm_grouped_q8_0(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream) {
+    return grouped("mmq_gemm_grouped_q8_0", FMT_Q8_0, xq, row_expert, R, wq, E, N, K, out, stream);
+}
+
+int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream) {
+    return grouped("mmq_gemm_grouped_q4_k", FMT_Q4_K, xq, row_expert, R, wq, E, N, K, out, stream);
 }
 
 int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,

@@ -59,6 +59,13 @@ int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t
                       cudaStream_t s);
 int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                        cudaStream_t s);
+int tc_grouped_launch(int fmt, const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
+                      const int2* tiles, const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map,
+                      float* out, cudaStream_t s);
+int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                   int64_t K, float* out, cudaStream_t s);
+int scratch_alloc(size_t bytes, cudaStream_t s, void** p, const char* fn);
+void scratch_free(void* p, cudaStream_t s);
 unsigned tc_take_error();
 unsigned tcx_take_error();
 unsigned small_take_error();

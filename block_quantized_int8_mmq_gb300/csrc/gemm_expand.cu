@@ -692,36 +692,11 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
 template <int FMT, bool DOTS>
 int launch_x(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
              int32_t* dots, cudaStream_t s, const char* fn) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        report(fn, MMQ_ERR_CUDA, "cudaGetDevice failed");
-        return MMQ_ERR_CUDA;
-    }
-    cudaMemPool_t pool = scratch_pool(dev);
-    if (!pool) {
-        report(fn, MMQ_ERR_CUDA, "scratch pool creation failed");
-        return MMQ_ERR_CUDA;
-    }
-    // While `s` is being captured, the allocation and free below become graph memory
-    // nodes (graph-owned scratch); outside capture they come from the library's pool.
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
-        cudaGetLastError();
-        report(fn, MMQ_ERR_CUDA, "cudaStreamIsCapturing failed");
-        return MMQ_ERR_CUDA;
-    }
     void* ws = nullptr;
-    const size_t bytes = plan_scratch(FMT, M, N, K).total();
-    const cudaError_t ae = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(&ws, bytes, pool, s)
-                                                            : cudaMallocAsync(&ws, bytes, s);
-    if (ae != cudaSuccess) {
-        cudaGetLastError();
-        report(fn, MMQ_ERR_NOMEM, "scratch allocation failed");
-        return MMQ_ERR_NOMEM;
-    }
+    const int st0 = scratch_alloc(plan_scratch(FMT, M, N, K).total(), s, &ws, fn);
+    if (st0 != MMQ_OK) return st0;
     const int st = launch_on<FMT, DOTS>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), s, fn);
-    cudaFreeAsync(ws, s);  // stream-ordered: after the kernels above
+    scratch_free(ws, s);  // stream-ordered: after the kernels above
     return st;
 }
 
@@ -750,6 +725,43 @@ uint8_t* noalloc_scratch(int dev) {
 }
 
 }  // namespace
+
+// Stream-ordered scratch: from the library's pool of the current device, or, while `s`
+// is being captured, the device's default pool (the graph's own allocation and free
+// nodes).  Returns MMQ_OK, MMQ_ERR_CUDA or MMQ_ERR_NOMEM (reported).
+int scratch_alloc(size_t bytes, cudaStream_t s, void** p, const char* fn) {
+    *p = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaGetDevice failed");
+        return MMQ_ERR_CUDA;
+    }
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool) {
+        report(fn, MMQ_ERR_CUDA, "scratch pool creation failed");
+        return MMQ_ERR_CUDA;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaStreamIsCapturing failed");
+        return MMQ_ERR_CUDA;
+    }
+    const cudaError_t ae = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(p, bytes, pool, s)
+                                                            : cudaMallocAsync(p, bytes, s);
+    if (ae != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        report(fn, MMQ_ERR_NOMEM, "scratch allocation failed");
+        return MMQ_ERR_NOMEM;
+    }
+    return MMQ_OK;
+}
+
+void scratch_free(void* p, cudaStream_t s) {
+    if (p) cudaFreeAsync(p, s);
+}
 
 int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
                cudaStream_t s) {

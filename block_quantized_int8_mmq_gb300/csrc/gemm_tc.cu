@@ -108,10 +108,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return umma::warp_wait(bar, parity, abort, &g_tc_error);
 }
 
-template <int FMT, bool DOTS>
+// GROUPED (expert-grouped contraction): CTA (x, y) takes tile y of a device-built list,
+// tiles[y] = (first row in the expert-sorted activations, expert e); its weight rows are
+// e * N + n0 .. of the experts' stacked matrices (tmB), rows past row_end[e] belong to
+// another expert and are not stored, and row m of the sorted activations is stored to
+// output row row_map[m].  CTAs past *ntiles leave at once.
+template <int FMT, bool DOTS, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int nb,
-         float* __restrict__ out, int32_t* __restrict__ dots) {
+         float* __restrict__ out, int32_t* __restrict__ dots, const int2* __restrict__ tiles,
+         const int* __restrict__ ntiles, const int* __restrict__ row_end, const int* __restrict__ row_map) {
     using L = Layout<FMT>;
     constexpr int BROW = b_row(FMT);
     constexpr int IPK = items_per_kt(FMT, DOTS);
@@ -121,7 +127,15 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+    const int n0 = blockIdx.x * BN;
+    int m0 = blockIdx.y * BM, b0 = n0, mlimit = M;
+    if (GROUPED) {
+        if ((int)blockIdx.y >= *ntiles) return;  // uniform over the CTA: nothing set up yet
+        const int2 tl = tiles[blockIdx.y];
+        m0 = tl.x;
+        b0 = tl.y * N + n0;
+        mlimit = row_end[tl.y];
+    }
     const int nkt = nb / KT_BLOCKS;
     const int nitems = nkt * IPK;
     volatile int* abort = &s_abort;
@@ -174,7 +188,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                 if (!wait_bar(bar(BAR_RAW_EMPTY + s), ((kt / RS) & 1) ^ 1, abort)) break;
                 ptx::mbar_arrive_expect_tx(bar(BAR_RAW_FULL + s), bytes);
                 ptx::tma_load_2d(sbase + L::rawA + s * BM * A_ROW, &tmA, bar(BAR_RAW_FULL + s), kt * (A_ROW / 2), m0);
-                ptx::tma_load_2d(sbase + L::rawB + s * BN * BROW, &tmB, bar(BAR_RAW_FULL + s), kt * (BROW / 2), n0);
+                ptx::tma_load_2d(sbase + L::rawB + s * BN * BROW, &tmB, bar(BAR_RAW_FULL + s), kt * (BROW / 2), b0);
                 issued = kt + 1;
             }
             // the copies of the last RS k-tiles may still be in flight after an abort
@@ -337,7 +351,8 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     } else {
         // ------------------------------------------------------------ epilogue
         epilogue_128x128<DOTS, DS, BN, false>(warp & 3, (warp - WARP_EPI0) >> 2, lane, tmem, nitems, bar(BAR_D_FULL),
-                                       bar(BAR_D_EMPTY), abort, &g_tc_error, M, N, m0, n0, nb, out, dots);
+                                              bar(BAR_D_EMPTY), abort, &g_tc_error, mlimit, N, m0, n0, nb, out, dots,
+                                              GROUPED ? row_map : nullptr);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -366,7 +381,7 @@ int launch_t(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
     const int smem = Layout<FMT>::alloc;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_tc<FMT, DOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(k_mmq_tc<FMT, DOTS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             cudaGetLastError();
             report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
@@ -377,12 +392,58 @@ int launch_t(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
     {
         ProfScope ps("k_mmq_tc", s);
-        k_mmq_tc<FMT, DOTS><<<grid, THREADS, smem, s>>>(ta, tb, (int)M, (int)N, nb, out, dots);
+        k_mmq_tc<FMT, DOTS, false><<<grid, THREADS, smem, s>>>(ta, tb, (int)M, (int)N, nb, out, dots, nullptr, nullptr,
+                                                               nullptr, nullptr);
+    }
+    return launch_status(fn);
+}
+
+// The grouped contraction over the expert-sorted activations xs (R rows): grid (N tiles,
+// max_tiles), tiles / ntiles / row_end / row_map built on the device by the grouping
+// kernels (grouped.cu).
+template <int FMT>
+int launch_grouped_t(const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K, const int2* tiles,
+                     const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map, float* out,
+                     cudaStream_t s, const char* fn) {
+    const int nb = (int)(K / QK);
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, xs, (uint64_t)nb * Q8_1_BYTES, (uint64_t)R, A_ROW, BM) ||
+        !make_map(&tb, wq, (uint64_t)(FMT == FMT_Q8_0 ? nb * Q8_0_BYTES : nb / 8 * Q4_K_BYTES), (uint64_t)(E * N),
+                  b_row(FMT), BN)) {
+        report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
+        return MMQ_ERR_CUDA;
+    }
+    const int smem = Layout<FMT>::alloc;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_mmq_tc<FMT, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
+            return MMQ_ERR_SMEM;
+        }
+        attr_done = true;
+    }
+    dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)max_tiles);
+    {
+        ProfScope ps("k_mmq_tc_grouped", s);
+        k_mmq_tc<FMT, false, true><<<grid, THREADS, smem, s>>>(ta, tb, (int)R, (int)N, nb, out, nullptr, tiles, ntiles,
+                                                               row_end, row_map);
     }
     return launch_status(fn);
 }
 
 }  // namespace
+
+int tc_grouped_launch(int fmt, const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
+                      const int2* tiles, const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map,
+                      float* out, cudaStream_t s) {
+    const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_grouped_q8_0" : "mmq_gemm_grouped_q4_k";
+    return fmt == FMT_Q8_0 ? launch_grouped_t<FMT_Q8_0>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map,
+                                                        out, s, fn)
+                           : launch_grouped_t<FMT_Q4_K>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map,
+                                                        out, s, fn);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -106,12 +106,13 @@ __device__ __forceinline__ int core_off(int r, int kg, int sbo) { return (r >> 3
 // and S, two 16-column halves: 64 registers) are issued before one wait; otherwise one
 // half at a time (32 registers, two waits).  bar_full / bar_empty: the slots' barriers
 // (8 bytes apart); each warp arrives once on bar_empty per item.  DOTS: D of item it (=
-// block it) is written to dots[m][n][it] instead.
+// block it) is written to dots[m][n][it] instead.  row_map (optional): the tile's row m
+// (m < M) is stored to output row row_map[m].
 template <bool DOTS, int DS, int BN, bool WIDE>
 __device__ __forceinline__ void epilogue_128x128(int q, int cg, int lane, uint32_t tmem, int nitems, uint32_t bar_full,
                                                  uint32_t bar_empty, volatile int* abort, unsigned* err, int M, int N,
                                                  int m0, int n0, int nb, float* __restrict__ out,
-                                                 int32_t* __restrict__ dots) {
+                                                 int32_t* __restrict__ dots, const int* __restrict__ row_map = nullptr) {
     const int c0 = cg * 32;
     const int mrow = m0 + 32 * q + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
@@ -177,7 +178,7 @@ __device__ __forceinline__ void epilogue_128x128(int q, int cg, int lane, uint32
         if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * t);
     }
     if (!DOTS && !*abort && mrow < M) {
-        float* orow = out + (long long)mrow * N + n0 + c0;
+        float* orow = out + (long long)(row_map ? row_map[mrow] : mrow) * N + n0 + c0;
         const int ncols = N - (n0 + c0);  // columns of this warp's 32 that exist
         if (ncols >= 32 && (N & 3) == 0) {
 #pragma unroll

@@ -137,6 +137,27 @@ int mmq_linear_q4_k(const float* x, int64_t M, int64_t K, const void* wq, int64_
                     void* stream);
 
 /*
+ * Expert-grouped contraction (mixture-of-experts "mul_mat_id"): for every activation row
+ * r < R, out[r] = xq[r] contracted with the weights of expert row_expert[r] ("When Does a
+ * Kernel Win Surface?", sec. "Fused indexed-MoE prefill GEMM": rows counting-sorted by
+ * expert into tiles of at most 128 rows, each tile staging one expert's weights once).
+ * The grouping runs on the device (no host round trip; capturable).
+ *   xq: q8_1 [R][K/32] blocks, 16-byte aligned.  row_expert: int32 [R], 4-byte aligned.
+ *   wq: E weight matrices stacked expert-major, expert e at row e*N ([E*N][K/32] Q8_0
+ *   blocks or [E*N][K/256] Q4_K super-blocks), 16-byte aligned.  out: f32 [R][N], 16-byte
+ *   aligned, fully overwritten; a row whose expert id is outside [0, E) gets zeros.
+ * Accuracy as mmq_gemm_q8_0 / mmq_gemm_q4_k, per row.  Needs K % 256 == 0 and
+ * R / 128 + min(E, R) <= 65535.  Scratch about R*K*1.125 bytes (stream-ordered, as the
+ * expanded path).
+ * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE, MMQ_ERR_NULL, MMQ_ERR_ALIGN, MMQ_ERR_SMEM,
+ * MMQ_ERR_NOMEM, MMQ_ERR_LAUNCH.
+ */
+int mmq_gemm_grouped_q8_0(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream);
+int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream);
+
+/*
  * Test hook: the per-block int32 dots D[m][n][b] (b < K/32) computed by the SAME data
  * path as mmq_gemm_q8_0 / mmq_gemm_q4_k select for this M (same staging, same
  * conversion, same MMA), written out instead of rescaled.  For Q4_K, D is the dot of

@@ -445,3 +445,88 @@ def test_expand_path_concurrent_streams(mmq):
         ref, norm = oracle.gemm("q4_k", oracle.quantize_q8_1(x), w, M, N, K)
         check_close(o.cpu().numpy(), ref, norm, "concurrent streams")
     assert mmq.mmq_get_device_error() == 0
+
+
+# ------------------------------------------------------------------ expert-grouped contraction
+
+def grouped_reference(fmt, xq_ref, ids, w, E, N, K):
+    """out[r] = row r contracted with expert ids[r] (the oracle per expert); zeros for ids
+    outside [0, E).  Returns (ref, norm)."""
+    R = len(ids)
+    ref = np.zeros((R, N))
+    norm = np.zeros((R, N))
+    rows_w = w.reshape(E, N, -1)
+    for e in range(E):
+        rows = np.nonzero(ids == e)[0]
+        if len(rows) == 0:
+            continue
+        r_e, n_e = oracle.gemm(fmt, np.ascontiguousarray(xq_ref[rows]), np.ascontiguousarray(rows_w[e]), len(rows), N, K)
+        ref[rows] = r_e
+        norm[rows] = n_e
+    return ref, norm
+
+
+GROUPED_CASES = [  # (R, E, N, K, routing)
+    (300, 5, 200, 512, "uniform"),
+    (1000, 16, 130, 256, "uniform"),
+    (64, 128, 64, 256, "uniform"),      # more experts than rows: most experts empty
+    (700, 8, 96, 512, "hot"),           # every row to one expert: several full tiles
+    (257, 6, 136, 256, "invalid"),      # some ids out of range: zero rows
+]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("case", range(len(GROUPED_CASES)))
+def test_grouped_parity(mmq, fmt, case):
+    R, E, N, K, routing = GROUPED_CASES[case]
+    rng = np.random.default_rng(100 + case)
+    if routing == "hot":
+        ids = np.full(R, 3 % E, dtype=np.int32)
+    else:
+        ids = rng.integers(0, E, R).astype(np.int32)
+    if routing == "invalid":
+        ids[::7] = -1
+        ids[3::11] = E
+    x = synth.activations(200 + case, R, K, True)
+    w = synth.weights(fmt, 300 + case, E * N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    out = torch.full((R, N), float("nan"), device="cuda")
+    mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K, out=out)
+    again = mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K)
+    assert mmq.mmq_get_device_error() == 0
+    assert torch.equal(out, again), "grouped result depends on the run"
+    ref, norm = grouped_reference(fmt, oracle.quantize_q8_1(x), ids, w, E, N, K)
+    check_close(out.cpu().numpy(), ref, norm, f"grouped {fmt} {GROUPED_CASES[case]}")
+
+
+def test_grouped_graph_capture(mmq):
+    R, E, N, K = 500, 12, 160, 512
+    rng = np.random.default_rng(7)
+    ids = rng.integers(0, E, R).astype(np.int32)
+    x = synth.activations(401, R, K, True)
+    w = synth.weights("q4_k", 402, E * N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    idd, wd = dev(ids), dev(w)
+    out = torch.full((R, N), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mmq.mmq_gemm_grouped("q4_k", xq, idd, wd, E, N, K, out=out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    ref, norm = grouped_reference("q4_k", oracle.quantize_q8_1(x), ids, w, E, N, K)
+    check_close(out.cpu().numpy(), ref, norm, "captured grouped")
+    assert mmq.mmq_get_device_error() == 0
+
+
+def test_grouped_refusals(mmq):
+    xq = torch.zeros((4, 8 * 36), dtype=torch.uint8, device="cuda")
+    ids = torch.zeros(4, dtype=torch.int32, device="cuda")
+    w = torch.zeros((2 * 8, 144), dtype=torch.uint8, device="cuda")
+    with pytest.raises(mmq.MMQError) as e:  # K % 256
+        mmq.mmq_gemm_grouped("q4_k", xq, ids, w, 2, 8, 128)
+    assert e.value.status == -2
+    with pytest.raises(mmq.MMQError) as e:  # E < 1
+        mmq.mmq_gemm_grouped("q4_k", xq, ids, w, 0, 8, 256)
+    assert e.value.status == -1
