@@ -55,7 +55,7 @@ WORKLOADS = {
 
 # ---------------------------------------------------------------------------- helpers
 
-PATH_NAMES = {1: "warp-level", 2: "tcgen05, codes converted in shared memory",
+PATH_NAMES = {1: "small-M streams (dp4a; int8 mma.sync)", 2: "tcgen05, codes converted in shared memory",
               3: "tcgen05, codes expanded once per call"}
 
 

@@ -1,30 +1,33 @@
-// Warp-level MMQ for few activation rows (the decode-like regime, bound by the weight
-// bytes read from HBM: "When Does a Kernel Win Surface?", sec. "A bottleneck taxonomy",
-// bandwidth-roofline decode).
+// MMQ for few activation rows: the decode-like regime, bound by the weight bytes read
+// from HBM ("When Does a Kernel Win Surface?", sec. "A bottleneck taxonomy",
+// bandwidth-roofline decode).  Kernels, chosen by small_launch at the end of the file:
+//   k_mmq_dp4a_stream  one or two rows (Q4_K up to four): per-warp weight streams, dp4a;
+//   k_mmq_i8_stream    three to eight rows per pass: the int8 tensor cores (mma.sync
+//                      m16n8k32 s8) on the raw codes, per-warp rings of 2-D tensor copies;
+//   k_mmq_small_mma, k_mmq_small  shapes the streams do not take (K % 256 != 0).
+// Each kernel's own comment describes it.
 //
-// One warp owns one weight row n and up to MT activation rows.  Lane l walks the
-// 32-value blocks u = l, l+32, ... of the row: it loads the block's weight codes once
-// (Q8_0: 32 int8 at a 2-byte alignment, fetched as aligned words and funnel-shifted;
-// Q4_K: the 32 nibbles of sub-block j from the 16-byte aligned nibble chunk, masked to
-// 0..15), forms the exact int32 block dot with each activation row by dp4a, and applies
-// that block's scale right away in f32 -- the per-32-block rescale in registers.  The
-// partial sums are reduced across the warp with shuffles at the end.
+// The two fallbacks.  k_mmq_small: one warp owns one weight row n and up to MT activation
+// rows.  Lane l walks the 32-value blocks u = l, l+32, ... of the row: it loads the
+// block's weight codes once (Q8_0: 32 int8 at a 2-byte alignment, fetched as aligned words
+// and funnel-shifted; Q4_K: the 32 nibbles of sub-block j from the 16-byte aligned nibble
+// chunk, masked to 0..15), forms the exact int32 block dot with each activation row by
+// dp4a, and applies that block's scale right away in f32 -- the per-32-block rescale in
+// registers.  The partial sums are reduced across the warp with shuffles at the end.
 // Q4_K adds -dmin*m_j*xs per sub-block ("When Does a Kernel Win Surface?", sec. "Kept
 // levers: Vulkan", affine identity; the per-(row, chunk) scales d*sc and -dmin*m as in
 // "13 . r7-r8 raw-byte MMQ kernel", sec. 3.2).
 //
-// For K a multiple of 64 the contraction runs on the tensor cores instead
-// (k_mmq_small_mma): mma.sync m16n8k16 with 16 weight rows as the M side and up to 8
-// tokens as N, codes converted to exact fp16 in registers.  dp4a would need the whole
-// dp4a rate of an SM to keep pace with HBM at 8 tokens; the fp16 mma has 4x that.
-// Within one 32-value block the order of k does not change the dot product, so both
-// operands use the same permutation of k: thread (g = lane/4, q = lane%4) takes the 8
-// consecutive values 8q..8q+7 of the block, i.e. 8 contiguous bytes of a row (Q4_K: one
-// 8-byte load gives the low nibbles of sub-block 2c and the high nibbles of 2c+1).
-// The 16 warps of a CTA share one 16-row tile and split K; each warp issues every load
-// of a batch of chunks (codes, scale headers, activation codes and scales) before any
-// math, so the DRAM latency is paid once per batch; the warps reduce through shared
-// memory at the end.
+// For K a multiple of 64, k_mmq_small_mma runs on the tensor cores instead: mma.sync
+// m16n8k16 with 16 weight rows as the M side and up to 8 tokens as N, codes converted to
+// exact fp16 in registers.  Within one 32-value block the order of k does not change the
+// dot product, so both operands use the same permutation of k: thread (g = lane/4, q =
+// lane%4) takes the 8 consecutive values 8q..8q+7 of the block, i.e. 8 contiguous bytes of
+// a row (Q4_K: one 8-byte load gives the low nibbles of sub-block 2c and the high nibbles
+// of 2c+1).  The 16 warps of a CTA share one 16-row tile and split K; each warp issues
+// every load of a batch of chunks (codes, scale headers, activation codes and scales)
+// before any math, so the DRAM latency is paid once per batch; the warps reduce through
+// shared memory at the end.
 #include <algorithm>
 
 #include "common.cuh"

@@ -194,13 +194,15 @@ int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t
                      void* stream);
 
 /* Kernel selection for the two contractions and their test hooks.
- *   MMQ_PATH_AUTO   : by shape: the warp-level kernels for M <= 8 or K % 256 != 0;
- *                     otherwise whichever of the warp-level kernels and the
+ *   MMQ_PATH_AUTO   : by shape: the small-M kernels for M <= 8 or K % 256 != 0;
+ *                     otherwise whichever of the small-M kernels and the
  *                     expanded-code tensor-core path a cost model (weight bytes per
  *                     8-row pass against tiles per wave and 32-blocks per tile, with
  *                     constants measured on GB300) predicts to be faster.  The
  *                     converter kernel is only taken when forced.
- *   MMQ_PATH_SMALL  : always the warp-level kernel (any M; slow for large M).
+ *   MMQ_PATH_SMALL  : always the small-M kernels (dp4a weight streams for one or two
+ *                     rows, int8 tensor-core streams in passes of 8 rows beyond; any M,
+ *                     slow for large M).
  *   MMQ_PATH_TC     : always the tcgen05 kernel that converts codes in shared memory
  *                     (K % 256 == 0, no scratch).
  *   MMQ_PATH_EXPAND : always the tcgen05 kernel over codes expanded to fp16 once per

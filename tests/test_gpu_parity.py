@@ -413,7 +413,7 @@ def test_profile_counts_every_launch(mmq):
         xq = mmq.mmq_quantize_q8_1(dev(x))
         mmq.mmq_gemm_q4_k(xq, dev(w), M, N, K)          # expanded path: two kernels
         set_path(mmq, "auto")
-        mmq.mmq_gemm_q4_k(xq[:4], dev(w), 4, N, K)      # M <= 8: warp-level kernel
+        mmq.mmq_gemm_q4_k(xq[:4], dev(w), 4, N, K)      # M <= 8: one small-M kernel
         prof = mmq.mmq_profile_read(reset=True)
     finally:
         mmq.mmq_profile_enable(prev)
@@ -421,7 +421,7 @@ def test_profile_counts_every_launch(mmq):
     assert prof["k_expand"][0] == prof["k_mmq_tcx"][0] == 1
     small = {k: n for k, (n, _) in prof.items()
              if k not in ("k_quantize_q8_1", "k_expand", "k_mmq_tcx")}
-    assert sum(small.values()) == 1, prof  # one warp-level kernel for the M = 4 call
+    assert sum(small.values()) == 1, prof  # one small-M kernel for the M = 4 call
     assert mmq.mmq_profile_read() == {}
 
 
