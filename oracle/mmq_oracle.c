@@ -34,6 +34,12 @@
  *    64c+32+i in its high half (sub-block 2c+1).
  *  - Q4_K weight value = d*sc_j*q - dmin*m_j, q in [0, 15]; the min term of the
  *    contraction uses the stored f16 block sum s of the activation block.
+ *  - Q5_K ([P3] sec. "Architecture: three orthogonal axes" lists it among the wired GGUF
+ *    K-quants; its bytes are not on the pages, so the GGUF arrangement is the reading):
+ *    super-block = 176 bytes: f16 d @0, f16 dmin @2, the 12 scale bytes @4 packed as in
+ *    Q4_K, 32 high-bit bytes qh @16, 128 nibble bytes qs @48 laid out as the Q4_K nibbles.
+ *    Element 64c+i (i < 64) takes its low 4 bits from qs as in Q4_K and its fifth bit
+ *    from bit 2c + (i >= 32) of qh[i % 32]; value = d*sc_j*q - dmin*m_j, q in [0, 31].
  */
 #include <math.h>
 #include <stdint.h>
@@ -47,6 +53,7 @@
 #define Q8_1_BYTES 36
 #define Q8_0_BYTES 34
 #define Q4_K_BYTES 144
+#define Q5_K_BYTES 176
 
 /* ---------------------------------------------------------------- binary16 */
 
@@ -148,6 +155,13 @@ static int q4_code(const uint8_t* qs, int e) {
     return i < 32 ? (byte & 15) : (byte >> 4);
 }
 
+/* 5-bit code (0..31) of element e in 0..255 of a Q5_K super-block sbk. */
+static int q5_code(const uint8_t* sbk, int e) {
+    int c = e / 64, i = e % 64;
+    int hi = (sbk[16 + (i % 32)] >> (2 * c + (i >= 32))) & 1;
+    return q4_code(sbk + 48, e) | (hi << 4);
+}
+
 /* --------------------------------------------------------------- block dots */
 
 /* Integer dot of activation block (m, b) with weight block (n, b), exact. */
@@ -169,6 +183,16 @@ static int64_t dot_q4_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t
     return s;
 }
 
+static int64_t dot_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t n, int64_t nb, int64_t b) {
+    int64_t nsb = nb / 8;
+    const int8_t* xa = (const int8_t*)(xq + (m * nb + b) * Q8_1_BYTES + 4);
+    const uint8_t* sbk = wq + (n * nsb + b / 8) * Q5_K_BYTES;
+    int j = (int)(b % 8);
+    int64_t s = 0;
+    for (int k = 0; k < QK; ++k) s += (int64_t)xa[k] * (int64_t)q5_code(sbk, 32 * j + k);
+    return s;
+}
+
 /* dots: int32 [M][N][K/32].  D[m,n,b] = sum over the block of xq * wq. */
 void oracle_block_dots_q8_0(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K, int32_t* dots) {
     int64_t nb = K / QK;
@@ -187,6 +211,16 @@ void oracle_block_dots_q4_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int
         for (int64_t n = 0; n < N; ++n)
             for (int64_t b = 0; b < nb; ++b)
                 dots[(m * N + n) * nb + b] = (int32_t)dot_q4_k(xq, wq, m, n, nb, b);
+}
+
+/* dots: int32 [M][N][K/32].  D[m,n,b] = sum over the block of xq * q5 (codes 0..31). */
+void oracle_block_dots_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K, int32_t* dots) {
+    int64_t nb = K / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < nb; ++b)
+                dots[(m * N + n) * nb + b] = (int32_t)dot_q5_k(xq, wq, m, n, nb, b);
 }
 
 /* -------------------------------------------------------------- contractions */
@@ -233,6 +267,29 @@ static void entry_q4_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t 
     *norm = t;
 }
 
+/* Q5_K: the same affine identity as Q4_K, over 5-bit codes (j = b mod 8). */
+static void entry_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t n, int64_t K,
+                       double* out, double* norm) {
+    int64_t nb = K / QK, nsb = K / QK_K;
+    double acc = 0.0, t = 0.0;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t* xb = xq + (m * nb + b) * Q8_1_BYTES;
+        const uint8_t* sbk = wq + (n * nsb + b / 8) * Q5_K_BYTES;
+        double xd = oracle_f16_to_f64(rd16(xb));
+        double xs = oracle_f16_to_f64(rd16(xb + 2));
+        double d = oracle_f16_to_f64(rd16(sbk));
+        double dmin = oracle_f16_to_f64(rd16(sbk + 2));
+        int sc, mn;
+        oracle_q4_k_scale_min(sbk + 4, (int)(b % 8), &sc, &mn);
+        double t1 = xd * d * (double)sc * (double)dot_q5_k(xq, wq, m, n, nb, b);
+        double t2 = dmin * (double)mn * xs;
+        acc += t1 - t2;
+        t += fabs(t1) + fabs(t2);
+    }
+    *out = acc;
+    *norm = t;
+}
+
 /* Full contraction: out, norm double [M][N]. */
 void oracle_gemm_q8_0(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                       double* out, double* norm) {
@@ -248,6 +305,13 @@ void oracle_gemm_q4_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N
         for (int64_t n = 0; n < N; ++n) entry_q4_k(xq, wq, m, n, K, out + m * N + n, norm + m * N + n);
 }
 
+void oracle_gemm_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
+                      double* out, double* norm) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) entry_q5_k(xq, wq, m, n, K, out + m * N + n, norm + m * N + n);
+}
+
 /* Sampled contraction: entry i is (im[i], in[i]); out, norm double [cnt]. */
 void oracle_gemm_q8_0_at(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                          const int64_t* im, const int64_t* in, int64_t cnt, double* out, double* norm) {
@@ -261,6 +325,13 @@ void oracle_gemm_q4_k_at(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_
     (void)M; (void)N;
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < cnt; ++i) entry_q4_k(xq, wq, im[i], in[i], K, out + i, norm + i);
+}
+
+void oracle_gemm_q5_k_at(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
+                         const int64_t* im, const int64_t* in, int64_t cnt, double* out, double* norm) {
+    (void)M; (void)N;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < cnt; ++i) entry_q5_k(xq, wq, im[i], in[i], K, out + i, norm + i);
 }
 
 /* Threads an OpenMP region of this library would use (the CPU baseline's core count). */

@@ -33,6 +33,7 @@ QK_K = 256
 Q8_1_BYTES = 36
 Q8_0_BYTES = 34
 Q4_K_BYTES = 144
+Q5_K_BYTES = 176
 
 BASE_SEED = 0x4D4D51
 
@@ -108,16 +109,31 @@ def q4_k_weights(seed: int, N: int, K: int) -> np.ndarray:
     return blk.reshape(N, nsb * Q4_K_BYTES)
 
 
+def q5_k_weights(seed: int, N: int, K: int) -> np.ndarray:
+    """uint8 [N, K/256*176]: per super-block f16 d, f16 dmin, then 172 uniform bytes (12
+    scale bytes, 32 high-bit bytes, 128 nibble bytes: every byte pattern is valid)."""
+    assert K % QK_K == 0
+    nsb = K // QK_K
+    u = uniform01(substream(seed, 32), 2 * N * nsb)
+    dd = (1e-4 + u * (2e-3 - 1e-4)).astype(np.float16).reshape(-1, 2)
+    blk = np.empty((N * nsb, Q5_K_BYTES), dtype=np.uint8)
+    blk[:, 0:4] = dd.view(np.uint8).reshape(-1, 4)
+    blk[:, 4:] = random_bytes(substream(seed, 33), N * nsb * (Q5_K_BYTES - 4)).reshape(-1, Q5_K_BYTES - 4)
+    return blk.reshape(N, nsb * Q5_K_BYTES)
+
+
 def weights(fmt: str, seed: int, N: int, K: int) -> np.ndarray:
     if fmt == "q8_0":
         return q8_0_weights(seed, N, K)
     if fmt == "q4_k":
         return q4_k_weights(seed, N, K)
+    if fmt == "q5_k":
+        return q5_k_weights(seed, N, K)
     raise ValueError(f"unknown weight format {fmt!r}")
 
 
 def row_bytes(fmt: str, K: int) -> int:
-    return {"q8_0": K // QK * Q8_0_BYTES, "q4_k": K // QK_K * Q4_K_BYTES}[fmt]
+    return {"q8_0": K // QK * Q8_0_BYTES, "q4_k": K // QK_K * Q4_K_BYTES, "q5_k": K // QK_K * Q5_K_BYTES}[fmt]
 
 
 # The five workloads: (format, M, N, K).  Seeds are BASE_SEED + index.

@@ -33,3 +33,22 @@ def super_block(d_f16: int, dmin_f16: int, sc, m, codes) -> np.ndarray:
     b[4:16] = pack_scales(sc, m)
     b[16:] = pack_nibbles(codes)
     return b
+
+
+def q5_k_super_block(d_f16: int, dmin_f16: int, sc, m, codes) -> np.ndarray:
+    """Q5_K super-block (176 B, the GGUF arrangement): f16 d, f16 dmin, the 12 scale bytes
+    as Q4_K, 32 high-bit bytes, then the 128 nibble bytes of the low 4 bits.  Element
+    64c + 32h + i (h = 0, 1) keeps its fifth bit in bit 2c + h of high-bit byte i."""
+    codes = np.asarray(codes, dtype=np.int64).reshape(256)
+    assert codes.min() >= 0 and codes.max() < 32
+    b = np.zeros(176, dtype=np.uint8)
+    b[0:2] = np.array([d_f16], dtype=np.uint16).view(np.uint8)
+    b[2:4] = np.array([dmin_f16], dtype=np.uint16).view(np.uint8)
+    b[4:16] = pack_scales(sc, m)
+    qh = np.zeros(32, dtype=np.int64)
+    for c in range(4):
+        for h in range(2):
+            qh |= ((codes[64 * c + 32 * h: 64 * c + 32 * h + 32] >> 4) & 1) << (2 * c + h)
+    b[16:48] = qh.astype(np.uint8)
+    b[48:] = pack_nibbles(codes & 15)
+    return b

@@ -23,7 +23,7 @@ import pytest
 import oracle
 import synth
 from conftest import as_floats, as_ints
-from q4k_pack import pack_nibbles, pack_scales, super_block
+from q4k_pack import pack_nibbles, pack_scales, q5_k_super_block, super_block
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -158,6 +158,21 @@ def test_hand_example_q4_k_super_block(golden_hand):
     assert (dots == as_ints(g["e3_dot"])[0]).all()
     out, _ = oracle.gemm("q4_k", xq, blk[None, :], 1, 1, 256)
     assert out[0, 0] == as_floats(g["e3_out"])[0]
+
+
+def test_hand_example_q5_k_super_block(golden_hand):
+    g = golden_hand
+    xq1, _, _, _ = _quant_one(as_floats(g["e1_x"]))
+    xq = np.tile(xq1, (1, 8))
+    sc, m = as_ints(g["e3_sc"]), as_ints(g["e3_m"])
+    codes = np.repeat(as_ints(g["e6_codes"]), 32)
+    blk = q5_k_super_block(as_ints(g["e3_d_f16"])[0], as_ints(g["e3_dmin_f16"])[0], sc, m, codes)
+    assert (blk[16:48] == as_ints(g["e6_qh_byte"])[0]).all() and (blk[48:] == as_ints(g["e6_qs_byte"])[0]).all()
+    assert np.array_equal(blk[4:16], np.array(as_ints(g["e3_scale_bytes"]), dtype=np.uint8))
+    dots = oracle.block_dots("q5_k", xq, blk[None, :], 1, 1, 256)
+    assert dots.reshape(8).tolist() == as_ints(g["e6_dots"])
+    out, _ = oracle.gemm("q5_k", xq, blk[None, :], 1, 1, 256)
+    assert out[0, 0] == as_floats(g["e6_out"])[0]
 
 
 def test_hand_example_scale_top_bits(golden_hand):
@@ -372,6 +387,69 @@ def test_q4_k_equals_dequantized_fp64_matmul(M, N, K):
     scale = np.abs(xh) @ np.abs(wh).T + np.abs(sa) @ np.abs(mterm).T
     assert np.all(np.abs(out - ref) <= 1e-12 * scale)
     assert np.all(norm >= np.abs(out) * (1 - 1e-15))
+
+
+def _random_q5_k(rng, N, K):
+    nsb = K // 256
+    d = rng.uniform(1e-4, 2e-3, (N, nsb)).astype(np.float16)
+    dmin = rng.uniform(1e-4, 2e-3, (N, nsb)).astype(np.float16)
+    sc = rng.integers(0, 64, (N, nsb, 8))
+    mn = rng.integers(0, 64, (N, nsb, 8))
+    codes = rng.integers(0, 32, (N, nsb, 256))
+    w = np.stack([q5_k_super_block(int(d[n, s].view(np.uint16)), int(dmin[n, s].view(np.uint16)),
+                                   sc[n, s], mn[n, s], codes[n, s])
+                  for n in range(N) for s in range(nsb)]).reshape(N, nsb * 176)
+    return w, d.astype(np.float64), dmin.astype(np.float64), sc, mn, codes
+
+
+def test_block_dots_q5_k_brute_force_on_packed_codes():
+    # every code of every element position: the fifth bit and the nibble of each element
+    # land where the decoder looks for them
+    rng = np.random.default_rng(51)
+    M, N, K = 3, 5, 512
+    x = synth.activations(51, M, K, True)
+    xq = oracle.quantize_q8_1(x)
+    w, d, dmin, sc, mn, codes = _random_q5_k(rng, N, K)
+    dots = oracle.block_dots("q5_k", xq, w, M, N, K)
+    _, _, qa = split_q8_1(xq)
+    ref = np.einsum("mbk,nbk->mnb", qa, codes.reshape(N, K // 32, 32))
+    assert np.array_equal(dots, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (2, 3, 512), (4, 2, 768)])
+def test_q5_k_equals_dequantized_fp64_matmul(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K + 5)
+    x = synth.activations(60 + M, M, K, True)
+    xq = oracle.quantize_q8_1(x)
+    w, d, dmin, sc, mn, codes = _random_q5_k(rng, N, K)
+    out, norm = oracle.gemm("q5_k", xq, w, M, N, K)
+    nsb = K // 256
+    wsub = (d[:, :, None] * sc)[:, :, :, None] * codes.reshape(N, nsb, 8, 32) \
+        - (dmin[:, :, None] * mn)[:, :, :, None]
+    wh = wsub.reshape(N, K)
+    da, sa, qa = split_q8_1(xq)
+    xh = (da[:, :, None] * qa).reshape(M, K)
+    ref = xh @ wh.T
+    S = qa.sum(axis=2)
+    mterm = (dmin[:, :, None] * mn).reshape(N, nsb * 8)
+    ref += (da * S - sa) @ mterm.T
+    scale = np.abs(xh) @ np.abs(wh).T + np.abs(sa) @ np.abs(mterm).T
+    assert np.all(np.abs(out - ref) <= 1e-12 * scale)
+    assert np.all(norm >= np.abs(out) * (1 - 1e-15))
+
+
+def test_q5_k_with_no_fifth_bits_equals_q4_k():
+    # a Q5_K block whose high-bit bytes are zero is the Q4_K block with the same fields
+    rng = np.random.default_rng(53)
+    M, N, K = 2, 3, 512
+    xq = oracle.quantize_q8_1(synth.activations(53, M, K, True))
+    w4, d, dmin, sc, mn, codes = _random_q4_k(rng, N, K)
+    w5 = np.stack([q5_k_super_block(int(np.float16(d[n, s]).view(np.uint16)),
+                                    int(np.float16(dmin[n, s]).view(np.uint16)), sc[n, s], mn[n, s], codes[n, s])
+                   for n in range(N) for s in range(K // 256)]).reshape(N, -1)
+    o4, _ = oracle.gemm("q4_k", xq, w4, M, N, K)
+    o5, _ = oracle.gemm("q5_k", xq, w5, M, N, K)
+    assert np.array_equal(o4, o5)
 
 
 def test_q4_k_zero_sub_scales_leave_only_the_min_term():
