@@ -14,8 +14,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmmq.so")
 
 QK, QK_K = 32, 256
-Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES = 36, 34, 144
-FMT = {"q8_0": 0, "q4_k": 1}
+Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES, Q5_K_BYTES = 36, 34, 144, 176
+FMT = {"q8_0": 0, "q4_k": 1, "q5_k": 2}
 PATH_AUTO, PATH_SMALL, PATH_TC, PATH_EXPAND = 0, 1, 2, 3
 
 EXPORTED = (
@@ -23,6 +23,7 @@ EXPORTED = (
     "mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k",
     "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
     "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k",
+    "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
 )
 
 
@@ -49,12 +50,13 @@ def _load():
     L.mmq_weight_row_bytes.argtypes = [I, I64]
     L.mmq_weight_row_bytes.restype = ctypes.c_size_t
     L.mmq_quantize_q8_1.argtypes = [P, I64, I64, P, P]
-    for f in ("mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_debug_block_dots_q8_0", "mmq_debug_block_dots_q4_k"):
+    for f in ("mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_gemm_q5_k", "mmq_debug_block_dots_q8_0",
+              "mmq_debug_block_dots_q4_k", "mmq_debug_block_dots_q5_k"):
         getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P]
     L.mmq_set_path.argtypes = [I]
     L.mmq_get_device_error.argtypes = [P]
     L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
-    for f in ("mmq_linear_q8_0", "mmq_linear_q4_k"):
+    for f in ("mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_linear_q5_k"):
         getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
     for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k"):
         getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
@@ -187,12 +189,23 @@ def mmq_get_device_error(stream=None) -> int:
     return int(_lib.mmq_get_device_error(_stream(stream)))
 
 
+def mmq_gemm_q5_k(xq, wq, M, N, K, out=None, stream=None):
+    """q8_1 [M, K/32*36] x Q5_K [N, K/256*176] -> f32 [M, N]."""
+    return _gemm("mmq_gemm_q5_k", xq, wq, M, N, K, out, stream)
+
+
+def mmq_debug_block_dots_q5_k(xq, wq, M, N, K, dots=None, stream=None):
+    return _dots("mmq_debug_block_dots_q5_k", xq, wq, M, N, K, dots, stream)
+
+
 def gemm(fmt: str, xq, wq, M, N, K, out=None, stream=None):
-    return (mmq_gemm_q8_0 if fmt == "q8_0" else mmq_gemm_q4_k)(xq, wq, M, N, K, out, stream)
+    f = {"q8_0": mmq_gemm_q8_0, "q4_k": mmq_gemm_q4_k, "q5_k": mmq_gemm_q5_k}[fmt]
+    return f(xq, wq, M, N, K, out, stream)
 
 
 def block_dots(fmt: str, xq, wq, M, N, K, dots=None, stream=None):
-    f = mmq_debug_block_dots_q8_0 if fmt == "q8_0" else mmq_debug_block_dots_q4_k
+    f = {"q8_0": mmq_debug_block_dots_q8_0, "q4_k": mmq_debug_block_dots_q4_k,
+         "q5_k": mmq_debug_block_dots_q5_k}[fmt]
     return f(xq, wq, M, N, K, dots, stream)
 
 
@@ -217,6 +230,6 @@ def mmq_linear(x, wq, fmt: str, N: int, xq=None, out=None, stream=None):
         xq = torch.empty((M, K // QK * Q8_1_BYTES), dtype=torch.uint8, device=x.device)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    fn = "mmq_linear_q8_0" if fmt == "q8_0" else "mmq_linear_q4_k"
+    fn = "mmq_linear_" + fmt
     _check(fn, getattr(_lib, fn)(_ptr(x), M, K, _ptr(wq), N, _ptr(xq), _ptr(out), _stream(stream)))
     return out

@@ -1,7 +1,7 @@
 // Tensor-core MMQ over codes expanded once per call (sm_103a).
 //
-// Every int8 code, and every Q4_K nibble times its 6-bit sub-scale, is an exact fp16
-// value, so the fp16 x fp16 -> f32 MMA over one 32-block computes the integer block dot
+// Every int8 code, and every K-quant code (Q4_K: 4 bits, Q5_K: 5 bits) times its 6-bit
+// sub-scale, is an exact fp16 value, so the fp16 x fp16 -> f32 MMA over one 32-block computes the integer block dot
 // exactly ("When the Product Won't Collapse", sec. "The obstruction": one integer dot
 // per constant-scale block).  Because the scale changes at every block, the
 // accumulator is read out of TMEM after every block and rescaled in registers (same
@@ -17,13 +17,13 @@
 //   activations  q8_1 rows (or f32 rows, quantized on the way) -> per (128-row tile,
 //                32-block) an 8 KiB chunk of fp16 codes in the K-major no-swizzle
 //                core-matrix order; per (tile, 256-value group) the K = 16 operand AS
-//                (column c = xd of block c; column 8 = 1.0, the Q4_K min item) and, for
-//                Q4_K, AM (column c = the f16 block sum s of block c);
-//   weights      Q8_0 / Q4_K rows -> per (128-row tile, 32-block) the same chunks (Q4_K:
-//                q * sc_j); per (tile, group) the f16 column scales WS (Q8_0: wd; Q4_K: d,
-//                and -dmin for the min item) and, for Q4_K, the K = 16 operand BMIN
-//                (column j = m_j) ("When Does a Kernel Win Surface?", sec. "Kept levers:
-//                Vulkan", the Q4_K affine identity);
+//                (column c = xd of block c; column 8 = 1.0, the K-quant min item) and,
+//                for K-quants, AM (column c = the f16 block sum s of block c);
+//   weights      Q8_0 / Q4_K / Q5_K rows -> per (128-row tile, 32-block) the same chunks
+//                (K-quants: q * sc_j); per (tile, group) the f16 column scales WS (Q8_0: wd;
+//                K-quants: d, and -dmin for the min item) and, for K-quants, the K = 16
+//                operand BMIN (column j = m_j) ("When Does a Kernel Win Surface?", sec.
+//                "Kept levers: Vulkan", the Q4_K affine identity);
 //
 // and k_mmq_tcx copies whole chunks with 1-D bulk copies, issues two K = 16 MMAs per
 // block (the exact block dot D) and one K = 16 MMA of AS against a one-hot operand built
@@ -71,16 +71,16 @@ constexpr int EXP_THREADS = 128;
 static_assert(OH % NMMA == 0, "each issuer sees its own one-hot slots");
 
 // Group data (scratch and shared memory).  Activation side: AS, the K = 16 operand whose
-// column c holds xd of block c (column 8: 1.0, the Q4_K min item), and for Q4_K AM
-// (column c = the f16 block sum s of block c).  Weight side: for Q4_K BMIN (column j =
-// m_j), then WS, the f16 column scales [item][128] (Q8_0: wd; Q4_K: d, and -dmin for
-// the min item).
-__host__ __device__ constexpr int xr(int fmt) { return fmt == FMT_Q4_K ? GB + 1 : GB; }
-__host__ __device__ constexpr int ga_bytes(int fmt) { return fmt == FMT_Q4_K ? 2 * TILE16 : TILE16; }
-__host__ __device__ constexpr int gw_bytes(int fmt) { return (fmt == FMT_Q4_K ? TILE16 : 0) + xr(fmt) * BN * 2; }
+// column c holds xd of block c (column 8: 1.0, the K-quant min item), and for K-quants
+// AM (column c = the f16 block sum s of block c).  Weight side: for K-quants BMIN (column
+// j = m_j), then WS, the f16 column scales [item][128] (Q8_0: wd; K-quants: d, and -dmin
+// for the min item).
+__host__ __device__ constexpr int xr(int fmt) { return is_kquant(fmt) ? GB + 1 : GB; }
+__host__ __device__ constexpr int ga_bytes(int fmt) { return is_kquant(fmt) ? 2 * TILE16 : TILE16; }
+__host__ __device__ constexpr int gw_bytes(int fmt) { return (is_kquant(fmt) ? TILE16 : 0) + xr(fmt) * BN * 2; }
 __host__ __device__ constexpr int am_off(int fmt) { return TILE16; }
 __host__ __device__ constexpr int bmin_off(int fmt) { return ga_bytes(fmt); }
-__host__ __device__ constexpr int ws_off(int fmt) { return ga_bytes(fmt) + (fmt == FMT_Q4_K ? TILE16 : 0); }
+__host__ __device__ constexpr int ws_off(int fmt) { return ga_bytes(fmt) + (is_kquant(fmt) ? TILE16 : 0); }
 
 // u16 index of (row r, column c) in a K = 16 K-major no-swizzle tile (8-row groups 256 B apart)
 __device__ __forceinline__ int tile16_idx(int r, int c) {
@@ -180,7 +180,7 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT) + h * (TILE16 / 4);
     const int t = threadIdx.x & 63;
     const bool second = threadIdx.x >= 64;  // threads 64..127 write AM (Q4_K)
-    if (second && FMT != FMT_Q4_K) return;
+    if (second && !is_kquant(FMT)) return;
     const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
     uint16_t v[8];
     if (kg == 0) {
@@ -190,26 +190,26 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)  // AS column 8: 1.0, the Q4_K min item's row scale
-            v[e] = (!second && e == 0 && FMT == FMT_Q4_K) ? (uint16_t)0x3C00 : (uint16_t)0;
+            v[e] = (!second && e == 0 && is_kquant(FMT)) ? (uint16_t)0x3C00 : (uint16_t)0;
     }
     *reinterpret_cast<uint4*>(gdst + (second ? am_off(FMT) : 0) + t * 16) = pack8(v);
 }
 
 // One CTA per (32-row quarter of a 128-row tile, 256-value group) of the weights.  FOLD:
-// Q4_K codes are q * sc_j (the contraction); without it, the raw nibbles (the block-dot
+// K-quant codes are q * sc_j (the contraction); without it, the raw nibbles (the block-dot
 // test hook).
 template <int FMT, bool FOLD>
 __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
                                                     uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
                                                     uint8_t* __restrict__ sm) {
-    constexpr int ROW = FMT == FMT_Q8_0 ? GB * Q8_0_BYTES : Q4_K_BYTES;  // 272 / 144 bytes per row per group
-    constexpr int V = ROW / 16;                                          // 17 / 9
-    constexpr int VP = V + 1;                                            // + one zero piece (Q8_0 reads 4 B past)
-    constexpr int SROW = FMT == FMT_Q8_0 ? 304 : 176;
+    constexpr int ROW = FMT == FMT_Q8_0 ? GB * Q8_0_BYTES : kq_bytes(FMT);  // 272 / 144 / 176 bytes per row per group
+    constexpr int V = ROW / 16;                                             // 17 / 9 / 11
+    constexpr int VP = V + 1;                                               // + one zero piece (Q8_0 reads 4 B past)
+    constexpr int SROW = FMT == FMT_Q8_0 ? 304 : (FMT == FMT_Q4_K ? 176 : 208);
     static_assert(SROW >= VP * 16 && SROW <= EXP_SROW, "row pad");
     const int nt = bx >> 2, h = bx & 3, ng = nb / GB;
     const int n0 = nt * BN + h * EXP_ROWS;
-    const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * Q4_K_BYTES;
+    const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * kq_bytes(FMT);
     for (int i = threadIdx.x; i < EXP_ROWS * VP; i += EXP_THREADS) {
         const int r = i / VP, c = i % VP;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -234,8 +234,9 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
             lo = i8x4_to_f16x4(__funnelshift_r(a0, a1, sh));
             hi = i8x4_to_f16x4(__funnelshift_r(a1, a2, sh));
         } else {
-            // value 32j + k of the super-block: byte 16 + 32*(j/2) + k, low nibble for even j
-            const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 16 + 32 * (j >> 1) + 8 * kc);
+            // value 32j + k of the super-block: nibble byte 32*(j/2) + k, low nibble for even j
+            // (Q5_K: plus the fifth bit, bit j of high-bit byte k)
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(row + kq_qs_off(FMT) + 32 * (j >> 1) + 8 * kc);
             uint32_t a0 = w[0], a1 = w[1];
             if (j & 1) {
                 a0 >>= 4;
@@ -243,15 +244,30 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
             }
             a0 &= 0x0F0F0F0Fu;
             a1 &= 0x0F0F0F0Fu;
+            if (FMT == FMT_Q5_K) {
+                const uint32_t* qh = reinterpret_cast<const uint32_t*>(row + 16 + 8 * kc);
+                a0 |= ((qh[0] >> j) & 0x01010101u) << 4;
+                a1 |= ((qh[1] >> j) & 0x01010101u) << 4;
+            }
             int sc = 1, mn;
             if (FOLD) {
                 const uint32_t* hw = reinterpret_cast<const uint32_t*>(row);
                 q4_k_scale_min(hw[1], hw[2], hw[3], j, sc, mn);
             }
             const __half2 sc2 = __half2half2(__int2half_rn(sc));
-            const __half2 nsc = __half2half2(__int2half_rn(-1024 * sc));
-            lo = u4x4_scaled_f16x4(a0, sc2, nsc);
-            hi = u4x4_scaled_f16x4(a1, sc2, nsc);
+            if (FMT == FMT_Q5_K) {
+                // codes up to 31: (1024 + q) * sc could exceed the f16 range, so the codes
+                // are converted exactly first and then scaled (q * sc <= 1953, exact)
+                const __half2 one = __half2half2(__int2half_rn(1));
+                const __half2 n1024 = __half2half2(__int2half_rn(-1024));
+                const uint2 l = u4x4_scaled_f16x4(a0, one, n1024), h = u4x4_scaled_f16x4(a1, one, n1024);
+                lo = make_uint2(h2_bits(__hmul2(bits_h2(l.x), sc2)), h2_bits(__hmul2(bits_h2(l.y), sc2)));
+                hi = make_uint2(h2_bits(__hmul2(bits_h2(h.x), sc2)), h2_bits(__hmul2(bits_h2(h.y), sc2)));
+            } else {
+                const __half2 nsc = __half2half2(__int2half_rn(-1024 * sc));
+                lo = u4x4_scaled_f16x4(a0, sc2, nsc);
+                hi = u4x4_scaled_f16x4(a1, sc2, nsc);
+            }
         }
         *reinterpret_cast<uint4*>(dst + (size_t)j * CHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
@@ -271,7 +287,7 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
         }
         *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + (c * BN + h * EXP_ROWS + r0) * 2) = pack8(v);
     }
-    if (FMT == FMT_Q4_K && t >= 64) {
+    if (is_kquant(FMT) && t >= 64) {
         // BMIN: quarter piece u = t - 64 (0..63) = (row 8*(u/16) + u%8, columns 8*((u/8)%2)
         // .. +7), column j = m_j
         const int u = t - 64;
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const uint8_t* __restrict__ xb,
           const uint8_t* __restrict__ gw, int M, int N, int nb, float* __restrict__ out, int32_t* __restrict__ dots) {
     using L = XLayout<FMT>;
-    constexpr bool MIN = FMT == FMT_Q4_K && !DOTS;  // a min item closes every group
+    constexpr bool MIN = is_kquant(FMT) && !DOTS;  // a min item closes every group
     constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
     constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT);
     extern __shared__ uint8_t smem_raw[];
@@ -765,8 +781,9 @@ void scratch_free(void* p, cudaStream_t s) {
 
 int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
                cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0 ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
-                                     : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
+    const char* fn = fmt == FMT_Q8_0   ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
+                     : fmt == FMT_Q5_K ? (dots ? "mmq_debug_block_dots_q5_k" : "mmq_gemm_q5_k")
+                                       : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
     if (K % QK_K != 0) {
         report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
         return MMQ_ERR_K_MULTIPLE;
@@ -778,13 +795,16 @@ int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, in
     if (fmt == FMT_Q8_0)
         return dots ? launch_x<FMT_Q8_0, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
                     : launch_x<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
+    if (fmt == FMT_Q5_K)
+        return dots ? launch_x<FMT_Q5_K, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+                    : launch_x<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
     return dots ? launch_x<FMT_Q4_K, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
                 : launch_x<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
 }
 
 int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                       cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0 ? "mmq_linear_q8_0" : "mmq_linear_q4_k";
+    const char* fn = fmt == FMT_Q8_0 ? "mmq_linear_q8_0" : fmt == FMT_Q5_K ? "mmq_linear_q5_k" : "mmq_linear_q4_k";
     if (K % QK_K != 0) {
         report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
         return MMQ_ERR_K_MULTIPLE;
@@ -793,8 +813,9 @@ int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t
         report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
         return MMQ_ERR_SHAPE;
     }
-    return fmt == FMT_Q8_0 ? launch_x<FMT_Q8_0, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
-                           : launch_x<FMT_Q4_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn);
+    return fmt == FMT_Q8_0   ? launch_x<FMT_Q8_0, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
+           : fmt == FMT_Q5_K ? launch_x<FMT_Q5_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
+                             : launch_x<FMT_Q4_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn);
 }
 
 int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
@@ -823,8 +844,9 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
         report(fn, MMQ_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed");
         return MMQ_ERR_CUDA;
     }
-    return fmt == FMT_Q8_0 ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
-                           : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn);
+    return fmt == FMT_Q8_0   ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
+           : fmt == FMT_Q5_K ? launch_on<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
+                             : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn);
 }
 
 unsigned tcx_take_error() {

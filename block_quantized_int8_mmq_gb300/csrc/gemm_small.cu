@@ -347,18 +347,22 @@ k_mmq_small_mma(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, 
 __device__ unsigned int g_small_error;
 
 constexpr int DS_WARPS = 8;
-constexpr int DS_SLOT = 16 * Q4_K_BYTES;  // 2304 B; a Q8_0 piece is 64 * 34 = 2176 B
+// slot bytes: 16 Q4_K super-blocks (2304 B; a Q8_0 piece, 64 * 34 = 2176 B, fits), or 16
+// Q5_K super-blocks (2816 B)
+__host__ __device__ constexpr int ds_slot(int fmt) { return fmt == FMT_Q5_K ? 16 * Q5_K_BYTES : 16 * Q4_K_BYTES; }
 constexpr uint64_t DS_WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t DS_SLEEP_NS = 2000;    // suspend hint of one barrier poll
-__host__ __device__ constexpr int ds_piece_units(int fmt) { return fmt == FMT_Q4_K ? 16 : 64; }
-__host__ __device__ constexpr int ds_unit_bytes(int fmt) { return fmt == FMT_Q4_K ? Q4_K_BYTES : Q8_0_BYTES; }
-__host__ __device__ constexpr int ds_ring_bytes(int slots) { return DS_WARPS * slots * (DS_SLOT + 8); }
+__host__ __device__ constexpr int ds_piece_units(int fmt) { return is_kquant(fmt) ? 16 : 64; }
+__host__ __device__ constexpr int ds_unit_bytes(int fmt) { return is_kquant(fmt) ? kq_bytes(fmt) : Q8_0_BYTES; }
+__host__ __device__ constexpr int ds_ring_bytes(int fmt, int slots) { return DS_WARPS * slots * (ds_slot(fmt) + 8); }
 // activation row stride in shared memory: 144 B per 4 blocks (nb % 8 == 0)
 __host__ __device__ constexpr int ds_xrow_bytes(int nb) { return nb / 4 * 144; }
-__host__ __device__ constexpr int ds_smem_bytes(int mt, int slots, int nb) {
-    return ds_ring_bytes(slots) + mt * (ds_xrow_bytes(nb) + 8 * nb);
+__host__ __device__ constexpr int ds_smem_bytes(int fmt, int mt, int slots, int nb) {
+    return ds_ring_bytes(fmt, slots) + mt * (ds_xrow_bytes(nb) + 8 * nb);
 }
-static_assert(64 * Q8_0_BYTES <= DS_SLOT && (64 * Q8_0_BYTES) % 16 == 0 && DS_SLOT % 16 == 0, "slots");
+static_assert(64 * Q8_0_BYTES <= ds_slot(FMT_Q8_0) && (64 * Q8_0_BYTES) % 16 == 0 && ds_slot(FMT_Q4_K) % 16 == 0 &&
+                  ds_slot(FMT_Q5_K) % 16 == 0,
+              "slots");
 
 // All lanes of the warp poll the slot's barrier (sleeping in the poll); false on every
 // lane after the time limit, with the error recorded.
@@ -394,19 +398,19 @@ template <int FMT, int MT, int S>
 __global__ void __launch_bounds__(DS_WARPS * 32, S == 2 ? 4 : 2)
 k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, int M, int N, int nb,
                   float* __restrict__ out, int32_t* __restrict__ dots) {
-    constexpr int PU = ds_piece_units(FMT), UB = ds_unit_bytes(FMT);
+    constexpr int PU = ds_piece_units(FMT), UB = ds_unit_bytes(FMT), DS_SLOT = ds_slot(FMT);
     extern __shared__ __align__(128) uint8_t ds_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* ring = ds_smem + warp * S * DS_SLOT;  // this warp's slots
     const uint32_t bar0 = ptx::smem_u32(ds_smem + DS_WARPS * S * DS_SLOT) + 8 * warp * S;
     const int xrow = ds_xrow_bytes(nb);
-    uint8_t* xcodes = ds_smem + ds_ring_bytes(S);                         // [MT][nb/4][144]
+    uint8_t* xcodes = ds_smem + ds_ring_bytes(FMT, S);                         // [MT][nb/4][144]
     float* xdv = reinterpret_cast<float*>(xcodes + MT * xrow);           // [MT][nb]
     float* xsv = xdv + MT * nb;                                          // [MT][nb]
     const int m0 = blockIdx.y * MT;
     const int ntok = min(MT, M - m0);
     const int tw = gridDim.x * DS_WARPS, gw = blockIdx.x * DS_WARPS + warp;
-    const int units = FMT == FMT_Q4_K ? nb >> 3 : nb;  // super-blocks or blocks per row
+    const int units = is_kquant(FMT) ? nb >> 3 : nb;  // super-blocks or blocks per row
     const int ppr = (units + PU - 1) / PU;             // pieces per row
     const long long row_bytes = (long long)units * UB;
     const int nrows = gw < N ? (N - 1 - gw) / tw + 1 : 0;
@@ -461,30 +465,38 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
             }
             const uint8_t* pc = ring + (q % S) * DS_SLOT;
             const int u0 = p * PU, nu = min(PU, units - u0);
-            if (FMT == FMT_Q4_K) {
+            if (is_kquant(FMT)) {
                 const int sl = lane >> 1, h = lane & 1;  // super-block of the piece, half
                 if (sl < nu) {
-                    const uint8_t* sbk = pc + sl * Q4_K_BYTES;
+                    const uint8_t* sbk = pc + sl * UB;
                     const uint4 hdr = *reinterpret_cast<const uint4*>(sbk);
                     // sub-blocks 4h + u, u = 0..3: 6-bit scale and min, one per byte
                     const uint32_t sc4 = h ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
                     const uint32_t mn4 =
                         h ? (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u)) : (hdr.z & 0x3F3F3F3Fu);
                     const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
-                    // sc_j as f32, divided by 16 for the high-nibble sub-blocks (their dot is
-                    // formed on the nibble in place, i.e. 16x the code); m_j as f32 (all exact)
+                    // Q4_K: sc_j as f32, divided by 16 for the high-nibble sub-blocks (their dot
+                    // is formed on the nibble in place, i.e. 16x the code); Q5_K codes are built
+                    // whole (nibble | fifth bit << 4).  m_j as f32 (all exact)
                     float scf[4], mnf[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        scf[u] = (u & 1) ? byte_f32_div16(sc4, u) : byte_f32(sc4, u);
+                        scf[u] = (FMT == FMT_Q4_K && (u & 1)) ? byte_f32_div16(sc4, u) : byte_f32(sc4, u);
                         mnf[u] = byte_f32(mn4, u);
                     }
                     const int b0 = 8 * (u0 + sl) + 4 * h;  // first block (sub-block 4h) in the row
-                    // nibble chunks 2h and 2h + 1: bytes 64h .. 64h + 63 after the header
-                    const uint4* wc = reinterpret_cast<const uint4*>(sbk + 16 + 64 * h);
+                    // nibble chunks 2h and 2h + 1: bytes 64h .. 64h + 63 of the nibble bytes
+                    const uint4* wc = reinterpret_cast<const uint4*>(sbk + kq_qs_off(FMT) + 64 * h);
                     const uint4 w0 = wc[0], w1 = wc[1], w2 = wc[2], w3 = wc[3];
                     const uint32_t wv[2][8] = {{w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w},
                                                {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w}};
+                    uint32_t qhw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // Q5_K: high-bit bytes 0..31
+                    if (FMT == FMT_Q5_K) {
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(sbk + 16);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(sbk + 32);
+                        qhw[0] = q0.x, qhw[1] = q0.y, qhw[2] = q0.z, qhw[3] = q0.w;
+                        qhw[4] = q1.x, qhw[5] = q1.y, qhw[6] = q1.z, qhw[7] = q1.w;
+                    }
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
                         const uint8_t* xb = xcodes + t * xrow + (b0 >> 2) * 144;  // blocks b0 .. b0 + 3
@@ -497,18 +509,27 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
                             const uint4 xa = *reinterpret_cast<const uint4*>(xb + u * QK);
                             const uint4 xc = *reinterpret_cast<const uint4*>(xb + u * QK + 16);
                             const uint32_t* cw = wv[u >> 1];
-                            const uint32_t mask = (u & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
-                            int D = 0;  // the block dot, times 16 for the high nibbles
-                            D = dp4a_us(cw[0] & mask, xa.x, D);
-                            D = dp4a_us(cw[1] & mask, xa.y, D);
-                            D = dp4a_us(cw[2] & mask, xa.z, D);
-                            D = dp4a_us(cw[3] & mask, xa.w, D);
-                            D = dp4a_us(cw[4] & mask, xc.x, D);
-                            D = dp4a_us(cw[5] & mask, xc.y, D);
-                            D = dp4a_us(cw[6] & mask, xc.z, D);
-                            D = dp4a_us(cw[7] & mask, xc.w, D);
+                            uint32_t code[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                if (FMT == FMT_Q5_K)
+                                    code[k] = ((cw[k] >> (4 * (u & 1))) & 0x0F0F0F0Fu) |
+                                              (((qhw[k] >> (4 * h + u)) & 0x01010101u) << 4);
+                                else  // the block dot of a high-nibble sub-block comes out 16x
+                                    code[k] = cw[k] & ((u & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu);
+                            }
+                            int D = 0;
+                            D = dp4a_us(code[0], xa.x, D);
+                            D = dp4a_us(code[1], xa.y, D);
+                            D = dp4a_us(code[2], xa.z, D);
+                            D = dp4a_us(code[3], xa.w, D);
+                            D = dp4a_us(code[4], xc.x, D);
+                            D = dp4a_us(code[5], xc.y, D);
+                            D = dp4a_us(code[6], xc.z, D);
+                            D = dp4a_us(code[7], xc.w, D);
                             if (dots) {
-                                if (t < ntok) dots[((long long)(m0 + t) * N + n) * nb + b0 + u] = (u & 1) ? D >> 4 : D;
+                                const bool x16 = FMT == FMT_Q4_K && (u & 1);
+                                if (t < ntok) dots[((long long)(m0 + t) * N + n) * nb + b0 + u] = x16 ? D >> 4 : D;
                             } else {
                                 sacc = fmaf(scf[u], xdu[u] * (float)D, sacc);
                                 macc = fmaf(mnf[u], xsu[u], macc);
@@ -621,7 +642,7 @@ DeviceShape device_shape() {
 template <int FMT, int MT, int S>
 int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                          int32_t* dots, cudaStream_t s, const char* fn) {
-    const int smem = ds_smem_bytes(MT, S, nb);
+    const int smem = ds_smem_bytes(FMT, MT, S, nb);
     static int attr_bytes = 0;
     if (smem > 48 * 1024 && smem > attr_bytes) {
         cudaError_t e =
@@ -676,14 +697,15 @@ int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
 // warps' partial sums of a tile meet in shared memory at the end.  Needs K % 256 == 0.
 constexpr int IS_WARPS = 8;
 
-__host__ __device__ constexpr int is_row_bytes(int fmt) { return fmt == FMT_Q4_K ? Q4_K_BYTES : 8 * Q8_0_BYTES; }
+__host__ __device__ constexpr int is_row_bytes(int fmt) { return is_kquant(fmt) ? kq_bytes(fmt) : 8 * Q8_0_BYTES; }
 __host__ __device__ constexpr int is_slot_bytes(int fmt) { return 16 * is_row_bytes(fmt); }  // 2304 / 4352
-__host__ __device__ constexpr int is_slots(int fmt) { return fmt == FMT_Q4_K ? 4 : 2; }
+__host__ __device__ constexpr int is_slots(int fmt) { return is_kquant(fmt) ? 4 : 2; }
 __host__ __device__ constexpr int is_smem_bytes(int fmt, int tpc) {
     return IS_WARPS * is_slots(fmt) * (is_slot_bytes(fmt) + 8) + tpc * IS_WARPS * 16 * 8 * 4;
 }
 constexpr int IS_MAX_TPC = 4;
-static_assert(is_smem_bytes(FMT_Q8_0, IS_MAX_TPC) <= 110 * 1024 && is_slot_bytes(FMT_Q4_K) % 128 == 0 &&
+static_assert(is_smem_bytes(FMT_Q8_0, IS_MAX_TPC) <= 110 * 1024 && is_smem_bytes(FMT_Q5_K, IS_MAX_TPC) <= 110 * 1024 &&
+                  is_slot_bytes(FMT_Q4_K) % 128 == 0 && is_slot_bytes(FMT_Q5_K) % 128 == 0 &&
                   is_slot_bytes(FMT_Q8_0) % 128 == 0,
               "two CTAs per SM; 128-byte aligned slots");
 
@@ -773,9 +795,12 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restri
                 break;
             }
             const uint8_t* sl = ring + (i % S) * SLOT;
-            if (FMT == FMT_Q4_K) {
+            if (is_kquant(FMT)) {
                 const uint8_t* rg = sl + g * RB;
                 const uint8_t* rh = sl + (g + 8) * RB;
+                // Q5_K: high-bit bytes of values 8q .. 8q + 7 of rows g and g + 8 (bit j: block j)
+                const uint2 qg = FMT == FMT_Q5_K ? *reinterpret_cast<const uint2*>(rg + 16 + 8 * q) : make_uint2(0u, 0u);
+                const uint2 qh = FMT == FMT_Q5_K ? *reinterpret_cast<const uint2*>(rh + 16 + 8 * q) : make_uint2(0u, 0u);
                 const uint4 hg = *reinterpret_cast<const uint4*>(rg), hh = *reinterpret_cast<const uint4*>(rh);
                 // 6-bit scales and mins of sub-blocks 0..3 / 4..7, one per byte
                 const uint32_t scg[2] = {hg.y & 0x3F3F3F3Fu, (hg.w & 0x0F0F0F0Fu) | ((hg.y >> 2) & 0x30303030u)};
@@ -785,12 +810,19 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restri
                 float sacc[4] = {0.f, 0.f, 0.f, 0.f}, macc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int sh = 4 * (j & 1), off = 16 + 32 * (j >> 1) + 8 * q;
+                    const int sh = 4 * (j & 1), off = kq_qs_off(FMT) + 32 * (j >> 1) + 8 * q;
                     const uint2 wg = *reinterpret_cast<const uint2*>(rg + off);
                     const uint2 wh = *reinterpret_cast<const uint2*>(rh + off);
+                    uint32_t ag0 = (wg.x >> sh) & 0x0F0F0F0Fu, ah0 = (wh.x >> sh) & 0x0F0F0F0Fu;
+                    uint32_t ag1 = (wg.y >> sh) & 0x0F0F0F0Fu, ah1 = (wh.y >> sh) & 0x0F0F0F0Fu;
+                    if (FMT == FMT_Q5_K) {
+                        ag0 |= ((qg.x >> j) & 0x01010101u) << 4;
+                        ag1 |= ((qg.y >> j) & 0x01010101u) << 4;
+                        ah0 |= ((qh.x >> j) & 0x01010101u) << 4;
+                        ah1 |= ((qh.y >> j) & 0x01010101u) << 4;
+                    }
                     int D[4];
-                    mma_s8_16832(D, (wg.x >> sh) & 0x0F0F0F0Fu, (wh.x >> sh) & 0x0F0F0F0Fu, (wg.y >> sh) & 0x0F0F0F0Fu,
-                                 (wh.y >> sh) & 0x0F0F0F0Fu, bw[j][0], bw[j][1]);
+                    mma_s8_16832(D, ag0, ah0, ag1, ah1, bw[j][0], bw[j][1]);
                     if (dots) {
                         const int b = b0 + j;
                         if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D[0];
@@ -926,7 +958,7 @@ int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
         attr_bytes = is_smem_bytes(FMT, IS_MAX_TPC);
     }
     CUtensorMap tm;
-    const uint64_t row_bytes = FMT == FMT_Q8_0 ? (uint64_t)nb * Q8_0_BYTES : (uint64_t)(nb / 8) * Q4_K_BYTES;
+    const uint64_t row_bytes = FMT == FMT_Q8_0 ? (uint64_t)nb * Q8_0_BYTES : (uint64_t)(nb / 8) * kq_bytes(FMT);
     if (!make_byte_map(&tm, w8, row_bytes, (uint64_t)N, is_row_bytes(FMT), 16, 8)) {
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
@@ -961,16 +993,23 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     }
     const uint8_t* x8 = static_cast<const uint8_t*>(xq);
     const uint8_t* w8 = static_cast<const uint8_t*>(wq);
-    const char* sfn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)" : "mmq_gemm_q4_k (small-M)";
+    const char* sfn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)"
+                      : fmt == FMT_Q5_K ? "mmq_gemm_q5_k (small-M)" : "mmq_gemm_q4_k (small-M)";
     // measured crossovers: the dp4a weight streams for one or two rows (and Q4_K up to four),
     // the int8 tensor-core stream beyond, one pass per 8 rows
-    const int64_t dp4a_max_m = fmt == FMT_Q4_K ? 4 : 2;
-    if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
-        return fmt == FMT_Q8_0 ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
-                               : launch_dp4a_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, sfn);
+    const int64_t dp4a_max_m = is_kquant(fmt) ? 4 : 2;
+    if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(fmt, M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
+        return fmt == FMT_Q8_0   ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
+               : fmt == FMT_Q5_K ? launch_dp4a_stream<FMT_Q5_K>(x8, w8, M, N, nb, out, dots, s, sfn)
+                                 : launch_dp4a_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, sfn);
     if (nb % 8 == 0)
-        return fmt == FMT_Q8_0 ? launch_i8_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
-                               : launch_i8_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, sfn);
+        return fmt == FMT_Q8_0   ? launch_i8_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
+               : fmt == FMT_Q5_K ? launch_i8_stream<FMT_Q5_K>(x8, w8, M, N, nb, out, dots, s, sfn)
+                                 : launch_i8_stream<FMT_Q4_K>(x8, w8, M, N, nb, out, dots, s, sfn);
+    if (fmt == FMT_Q5_K) {  // K-quants come in whole super-blocks: nb % 8 == 0 always
+        report(sfn, MMQ_ERR_K_MULTIPLE, "Q5_K needs K % 256 == 0");
+        return MMQ_ERR_K_MULTIPLE;
+    }
     if (nb % 2 == 0) {
         dim3 g2((unsigned)((N + 15) / 16), (unsigned)((M + 7) / 8));
         ProfScope ps("k_mmq_small_mma", s);

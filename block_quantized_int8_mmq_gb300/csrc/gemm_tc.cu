@@ -479,8 +479,13 @@ bool tc_available() { return true; }
 
 int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
               cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0 ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
-                                     : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
+    const char* fn = fmt == FMT_Q8_0   ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
+                     : fmt == FMT_Q5_K ? (dots ? "mmq_debug_block_dots_q5_k" : "mmq_gemm_q5_k")
+                                       : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
+    if (fmt == FMT_Q5_K) {
+        report(fn, MMQ_ERR_ARG, "the converter tensor-core kernel takes Q8_0 and Q4_K (Q5_K: the expanded path)");
+        return MMQ_ERR_ARG;
+    }
     if (K % QK_K != 0) {
         report(fn, MMQ_ERR_K_MULTIPLE, "the tensor-core path stages 256-value k-tiles: K % 256 != 0");
         return MMQ_ERR_K_MULTIPLE;

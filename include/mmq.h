@@ -46,6 +46,12 @@
  *    bytes @16 (byte 32c+i: low nibble = value 64c+i, high nibble = value 64c+32+i).
  *    Weights are [N][K/256] super-blocks.  Value = d*sc_j*q - dmin*m_j, q in 0..15
  *    ("13 . r7-r8 raw-byte MMQ kernel", sec. 2 and sec. 3.2).
+ *  Q5_K super-block (176 B, 256 values; "When Does a Kernel Win Surface?", sec.
+ *    "Architecture: three orthogonal axes", lists it among the GGUF K-quants; the bytes
+ *    follow the GGUF arrangement): f16 d @0, f16 dmin @2, the 12 scale bytes @4 as Q4_K,
+ *    32 high-bit bytes @16, 128 nibble bytes @48 as the Q4_K nibbles.  Value 64c+32h+i
+ *    (h = 0, 1) takes its fifth bit from bit 2c+h of high-bit byte i; value =
+ *    d*sc_j*q - dmin*m_j, q in 0..31.
  *  out: f32 [M][N] row-major, fully overwritten (no accumulate mode).
  */
 #ifndef MMQ_H
@@ -119,6 +125,15 @@ int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
                   void* stream);
 
 /*
+ * out = xq (q8_1) contracted with Q5_K weights wq ([N][K/256] super-blocks of 176 B),
+ * including the -dmin*m_j*s min term of every sub-block; as mmq_gemm_q4_k otherwise
+ * (K % 256 == 0).  Runs on the expanded-code tensor-core path and the small-M streams; the
+ * converter kernel (MMQ_PATH_TC) refuses it with MMQ_ERR_ARG.
+ */
+int mmq_gemm_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                  void* stream);
+
+/*
  * Quantize + contraction in one call: xq = q8_1 of x (the same bytes as
  * mmq_quantize_q8_1) and out = xq contracted with Q8_0 (mmq_linear_q8_0) or Q4_K
  * (mmq_linear_q4_k) weights, as mmq_gemm_q8_0 / mmq_gemm_q4_k would compute it.  On the
@@ -134,6 +149,8 @@ int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
 int mmq_linear_q8_0(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
                     void* stream);
 int mmq_linear_q4_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream);
+int mmq_linear_q5_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
                     void* stream);
 
 /*
@@ -161,25 +178,28 @@ int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, 
  * Test hook: the per-block int32 dots D[m][n][b] (b < K/32) computed by the SAME data
  * path as mmq_gemm_q8_0 / mmq_gemm_q4_k select for this M (same staging, same
  * conversion, same MMA), written out instead of rescaled.  For Q4_K, D is the dot of
- * the activation codes with the raw 4-bit codes (0..15), without sc_j.
+ * the activation codes with the raw 4-bit codes (0..15), without sc_j; for Q5_K, with
+ * the raw 5-bit codes (0..31).
  *   dots: int32 [M][N][K/32], 16-byte aligned.  Bit-exact by definition.
  */
 int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
                               int32_t* dots, void* stream);
 int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
                               int32_t* dots, void* stream);
+int mmq_debug_block_dots_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
+                              int32_t* dots, void* stream);
 
 /*
- * The contraction of mmq_gemm_q8_0 (fmt 0) or mmq_gemm_q4_k (fmt 1) on the expanded-code
- * tensor-core path, with its scratch taken from a fixed 64 MiB array in the library's
- * device memory (one per device) instead of an allocation: this call allocates no device
- * memory and calls nothing that does.  The method's pages have no counterpart of this
+ * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1) or mmq_gemm_q5_k
+ * (fmt 2) on the expanded-code tensor-core path, with its scratch taken from a fixed
+ * 64 MiB array in the library's device memory (one per device) instead of an allocation:
+ * this call allocates no device memory and calls nothing that does.  The method's pages have no counterpart of this
  * entry point; it exists for callers that may not allocate.
  *  - Scratch need, in bytes, with MT = ceil(M/128), NT = ceil(N/128), nb = K/32,
  *    ng = K/256:  MT*nb*8192 + MT*ng*GA + NT*nb*8192 + NT*ng*GW, where GA = 4096 and
- *    GW = 2048 for Q8_0, GA = 8192 and GW = 6400 for Q4_K.  A shape that needs more
- *    than 64 MiB is refused with MMQ_ERR_SHAPE (e.g. M = 512, N = K = 3584 Q8_0 needs
- *    about 30 MiB).  K % 256 == 0 for both formats (MMQ_ERR_K_MULTIPLE otherwise).
+ *    GW = 2048 for Q8_0, GA = 8192 and GW = 6400 for Q4_K and Q5_K.  A shape that needs
+ *    more than 64 MiB is refused with MMQ_ERR_SHAPE (e.g. M = 512, N = K = 3584 Q8_0
+ *    needs about 30 MiB).  K % 256 == 0 for every format (MMQ_ERR_K_MULTIPLE otherwise).
  *  - The array's address is looked up (cudaGetSymbolAddress) on the first call on each
  *    device: make that first call outside any stream capture.
  *  - There is one array per device: two calls whose kernels overlap in time on one
@@ -188,7 +208,7 @@ int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t
  *  - Nothing in the array has to start at zero: the call writes every scratch byte it
  *    reads before reading it.
  *  - Arguments, alignment, accuracy and the other errors as mmq_gemm_q8_0 /
- *    mmq_gemm_q4_k; MMQ_ERR_ARG for another fmt.
+ *    mmq_gemm_q4_k / mmq_gemm_q5_k; MMQ_ERR_ARG for another fmt.
  */
 int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                      void* stream);

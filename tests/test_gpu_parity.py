@@ -99,11 +99,15 @@ SMALL_SHAPES = {
     "q4_k": [(1, 1, 256), (3, 7, 256), (9, 33, 512), (64, 256, 512), (130, 200, 1024), (257, 129, 2304),
              (8, 300, 3584)],
 }
+SMALL_SHAPES["q5_k"] = SMALL_SHAPES["q4_k"]
+FMTS = ["q8_0", "q4_k", "q5_k"]
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_parity_full(mmq, fmt, path):
+    if (fmt, path) == ("q5_k", "tc"):
+        pytest.skip("the converter kernel takes Q8_0 and Q4_K (refusal tested below)")
     set_path(mmq, path)
     for (M, N, K) in SMALL_SHAPES[fmt]:
         if path != "small" and K % 256:
@@ -136,8 +140,10 @@ def test_tc_paths_refuse_partial_k_groups_and_auto_routes_them(mmq, path):
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", FMTS)
 def test_block_dots_bit_exact(mmq, fmt, path):
+    if (fmt, path) == ("q5_k", "tc"):
+        pytest.skip("the converter kernel takes Q8_0 and Q4_K")
     set_path(mmq, path)
     for (M, N, K) in [(5, 9, 256), (70, 150, 512), (129, 257, 1024)]:
         x = synth.activations(M + 11, M, K, True)
@@ -155,7 +161,7 @@ STREAM_SHAPES = [(1, 1, 256), (2, 7, 2304), (1, 300, 3584), (2, 77, 18944), (1, 
                  (3, 77, 2304), (4, 300, 3584), (5, 9000, 512), (8, 513, 3584), (7, 40, 7168)]
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", FMTS)
 def test_few_row_stream_parity_and_dots(mmq, fmt):
     set_path(mmq, "small")
     for (M, N, K) in STREAM_SHAPES:
@@ -178,8 +184,10 @@ def test_few_row_stream_parity_and_dots(mmq, fmt):
 # quantize + gemm calls on the same path bit for bit (same kernels downstream of the
 # expanded operands), and the oracle within tolerance.
 @pytest.mark.parametrize("path", ["auto", "expand", "small", "tc"])
-@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", FMTS)
 def test_linear_matches_separate_calls(mmq, fmt, path):
+    if (fmt, path) == ("q5_k", "tc"):
+        pytest.skip("the converter kernel takes Q8_0 and Q4_K")
     set_path(mmq, path)
     for (M, N, K) in [(300, 200, 1024), (129, 257, 2304), (4, 130, 512), (513, 64, 256)]:
         x = synth.activations(M + 3 * N + K, M, K, True)
@@ -248,6 +256,33 @@ def test_extreme_codes_block_dots(mmq, path):
     out = mmq.mmq_gemm_q8_0(xq, dev(w), M, N, K)
     r, nrm = oracle.gemm("q8_0", xq_ref, w, M, N, K)
     check_close(out.cpu().numpy(), r, nrm, "extreme codes")
+
+
+def test_q5_k_refused_by_converter_kernel_auto_takes_it(mmq):
+    M, N, K = 600, 64, 512
+    x = synth.activations(31, M, K, True)
+    w = synth.q5_k_weights(32, N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    set_path(mmq, "tc")
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_gemm_q5_k(xq, dev(w), M, N, K)
+    assert e.value.status == -9  # MMQ_ERR_ARG
+    set_path(mmq, "auto")
+    out = mmq.mmq_gemm_q5_k(xq, dev(w), M, N, K)
+    assert mmq.mmq_last_path() in (mmq.PATH_SMALL, mmq.PATH_EXPAND)
+    ref, norm = oracle.gemm("q5_k", oracle.quantize_q8_1(x), w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, "q5_k auto")
+    # Q5_K codes at the ends of 0..31 with the largest 6-bit scale: (q * sc) up to 31 * 63
+    # and the min term at 63 * 63 on every sub-block
+    w2 = synth.q5_k_weights(33, N, K).reshape(N, K // 256, 176).copy()
+    w2[:, :, 4:16] = 0xFF
+    w2[:, :, 16:] = np.where(np.arange(160) % 3 == 0, 0xFF, 0x00).astype(np.uint8)
+    w2 = w2.reshape(N, -1)
+    for path in ("expand", "small"):
+        set_path(mmq, path)
+        dots = mmq.mmq_debug_block_dots_q5_k(xq, dev(w2), M, N, K)
+        assert np.array_equal(dots.cpu().numpy(), oracle.block_dots("q5_k", oracle.quantize_q8_1(x), w2, M, N, K))
+    assert mmq.mmq_get_device_error() == 0
 
 
 # ------------------------------------------------------------------ full sizes, sampled
@@ -326,6 +361,27 @@ def test_m_sweep_sampled_parity(mmq, M):
     im, inn = sample_entries(M, N, 1500, M)
     ref, norm = oracle.gemm_at("q4_k", xq_ref, w, M, N, K, im, inn)
     check_close(out[im, inn], ref, norm, f"M sweep {M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 18944, 3584), (1, 3584, 18944), (4, 18944, 3584), (8, 3584, 18944),
+                                   (512, 3584, 3584), (2048, 18944, 3584)])
+def test_q5_k_full_size_sampled_parity(mmq, M, N, K):
+    """Q5_K at the 7B-class projection sizes: the small-M streams and the expanded path."""
+    set_path(mmq, "auto")
+    x = synth.activations(synth.substream(synth.BASE_SEED + 5, M + N), M, K, True)
+    w = synth.q5_k_weights(synth.substream(synth.BASE_SEED + 6, N + K), N, K)
+    xq_ref = oracle.quantize_q8_1(x)
+    xq = torch.empty((M, K // 32 * 36), dtype=torch.uint8, device="cuda")
+    out = torch.full((M, N), float("nan"), device="cuda")
+    mmq.mmq_linear(dev(x), dev(w), "q5_k", N, xq=xq, out=out)
+    assert mmq.mmq_last_path() == (mmq.PATH_EXPAND if M >= 512 else mmq.PATH_SMALL)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    o = out.cpu().numpy()
+    assert not np.isnan(o).any(), "output not fully written"
+    im, inn = sample_entries(M, N, 1500, M + 5)
+    ref, norm = oracle.gemm_at("q5_k", xq_ref, w, M, N, K, im, inn)
+    check_close(o[im, inn], ref, norm, f"q5_k {M}x{N}x{K}")
+    assert mmq.mmq_get_device_error() == 0
 
 
 # ------------------------------------------------------------------ protocol on the device
