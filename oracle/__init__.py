@@ -20,7 +20,7 @@ _SRC = os.path.join(_HERE, "mmq_oracle.c")
 _LIB = os.path.join(_HERE, "libmmq_oracle.so")
 
 QK, QK_K = 32, 256
-Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES, Q5_K_BYTES = 36, 34, 144, 176
+Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES, Q5_K_BYTES, Q6_K_BYTES = 36, 34, 144, 176, 210
 
 
 def build(force: bool = False) -> str:
@@ -51,11 +51,13 @@ def lib():
         L.oracle_f64_to_f16.restype = ctypes.c_uint16
         L.oracle_quantize_q8_1.argtypes = [P, I64, I64, P]
         L.oracle_q4_k_scale_min.argtypes = [P, ctypes.c_int, P, P]
-        for f in ("oracle_block_dots_q8_0", "oracle_block_dots_q4_k", "oracle_block_dots_q5_k"):
+        for f in ("oracle_block_dots_q8_0", "oracle_block_dots_q4_k", "oracle_block_dots_q5_k",
+                  "oracle_block_dots_q6_k"):
             getattr(L, f).argtypes = [P, P, I64, I64, I64, P]
-        for f in ("oracle_gemm_q8_0", "oracle_gemm_q4_k", "oracle_gemm_q5_k"):
+        for f in ("oracle_gemm_q8_0", "oracle_gemm_q4_k", "oracle_gemm_q5_k", "oracle_gemm_q6_k"):
             getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P]
-        for f in ("oracle_gemm_q8_0_at", "oracle_gemm_q4_k_at", "oracle_gemm_q5_k_at"):
+        for f in ("oracle_gemm_q8_0_at", "oracle_gemm_q4_k_at", "oracle_gemm_q5_k_at",
+                  "oracle_gemm_q6_k_at"):
             getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P, I64, P, P]
         L.oracle_num_threads.restype = ctypes.c_int
         _lib = L
@@ -94,15 +96,17 @@ def q4_k_scale_min(p12: np.ndarray, j: int) -> tuple[int, int]:
 
 
 def _check(fmt, xq, wq, M, N, K):
-    assert fmt in ("q8_0", "q4_k", "q5_k")
+    assert fmt in ("q8_0", "q4_k", "q5_k", "q6_k")
     assert xq.dtype == np.uint8 and wq.dtype == np.uint8
     assert xq.size == M * (K // QK) * Q8_1_BYTES
-    rb = {"q8_0": K // QK * Q8_0_BYTES, "q4_k": K // QK_K * Q4_K_BYTES, "q5_k": K // QK_K * Q5_K_BYTES}[fmt]
+    rb = {"q8_0": K // QK * Q8_0_BYTES, "q4_k": K // QK_K * Q4_K_BYTES, "q5_k": K // QK_K * Q5_K_BYTES,
+          "q6_k": K // QK_K * Q6_K_BYTES}[fmt]
     assert wq.size == N * rb
 
 
 def block_dots(fmt: str, xq: np.ndarray, wq: np.ndarray, M: int, N: int, K: int) -> np.ndarray:
-    """int32 [M, N, K/32]: per-32-block integer dot products."""
+    """int32 [M, N, K/32]: per-32-block integer dot products (Q6_K: with the 16-element
+    sub-scales and the centring inside)."""
     xq, wq = np.ascontiguousarray(xq), np.ascontiguousarray(wq)
     _check(fmt, xq, wq, M, N, K)
     out = np.empty((M, N, K // QK), dtype=np.int32)

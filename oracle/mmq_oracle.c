@@ -40,6 +40,16 @@
  *    Q4_K, 32 high-bit bytes qh @16, 128 nibble bytes qs @48 laid out as the Q4_K nibbles.
  *    Element 64c+i (i < 64) takes its low 4 bits from qs as in Q4_K and its fifth bit
  *    from bit 2c + (i >= 32) of qh[i % 32]; value = d*sc_j*q - dmin*m_j, q in [0, 31].
+ *  - Q6_K ([P3] sec. "Architecture: three orthogonal axes" lists it; [P3] sec. "Unified
+ *    dp4a decode cores" fixes its 16-element scale groups and the centring q - 32; the
+ *    bytes are the GGUF arrangement): super-block = 210 bytes: 128 low-nibble bytes ql @0,
+ *    64 bytes of 2-bit high parts qh @128, 16 int8 sub-scales @192, f16 d @208.  Element
+ *    128h + 32t + l (h in 0..1, t in 0..3, l in 0..31) takes its low 4 bits from
+ *    ql[64h + 32(t mod 2) + l] (low nibble for t < 2, high nibble for t >= 2) and its top
+ *    2 bits from bits 2t, 2t+1 of qh[32h + l]; value = d * sc[e/16] * (q - 32), q in
+ *    [0, 63].  Its scale changes every 16 elements, inside a q8_1 block, so the block dot
+ *    of a 32-element block is taken with the sub-scales inside:
+ *    D = sum_k u_k * (q_k - 32) * sc[k/16], and out = sum_b xd * d * D.
  */
 #include <math.h>
 #include <stdint.h>
@@ -54,6 +64,7 @@
 #define Q8_0_BYTES 34
 #define Q4_K_BYTES 144
 #define Q5_K_BYTES 176
+#define Q6_K_BYTES 210
 
 /* ---------------------------------------------------------------- binary16 */
 
@@ -162,6 +173,18 @@ static int q5_code(const uint8_t* sbk, int e) {
     return q4_code(sbk + 48, e) | (hi << 4);
 }
 
+/* 6-bit code (0..63) of element e in 0..255 of a Q6_K super-block sbk, and the int8
+ * sub-scale of its 16-element group. */
+static int q6_code(const uint8_t* sbk, int e) {
+    int h = e / 128, t = (e % 128) / 32, l = e % 32;
+    uint8_t lo = sbk[64 * h + 32 * (t % 2) + l];
+    int low4 = t < 2 ? (lo & 15) : (lo >> 4);
+    int top2 = (sbk[128 + 32 * h + l] >> (2 * t)) & 3;
+    return low4 | (top2 << 4);
+}
+
+static int q6_scale(const uint8_t* sbk, int e) { return (int)(int8_t)sbk[192 + e / 16]; }
+
 /* --------------------------------------------------------------- block dots */
 
 /* Integer dot of activation block (m, b) with weight block (n, b), exact. */
@@ -193,6 +216,21 @@ static int64_t dot_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t
     return s;
 }
 
+/* Q6_K block b (elements 32j .. 32j+31 of super-block b/8, j = b mod 8), with the
+ * centring and the two 16-element sub-scales inside. */
+static int64_t dot_q6_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t n, int64_t nb, int64_t b) {
+    int64_t nsb = nb / 8;
+    const int8_t* xa = (const int8_t*)(xq + (m * nb + b) * Q8_1_BYTES + 4);
+    const uint8_t* sbk = wq + (n * nsb + b / 8) * Q6_K_BYTES;
+    int j = (int)(b % 8);
+    int64_t s = 0;
+    for (int k = 0; k < QK; ++k) {
+        int e = 32 * j + k;
+        s += (int64_t)xa[k] * (int64_t)(q6_code(sbk, e) - 32) * (int64_t)q6_scale(sbk, e);
+    }
+    return s;
+}
+
 /* dots: int32 [M][N][K/32].  D[m,n,b] = sum over the block of xq * wq. */
 void oracle_block_dots_q8_0(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K, int32_t* dots) {
     int64_t nb = K / QK;
@@ -221,6 +259,16 @@ void oracle_block_dots_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int
         for (int64_t n = 0; n < N; ++n)
             for (int64_t b = 0; b < nb; ++b)
                 dots[(m * N + n) * nb + b] = (int32_t)dot_q5_k(xq, wq, m, n, nb, b);
+}
+
+/* dots: int32 [M][N][K/32].  D[m,n,b] = sum over the block of xq * (q6 - 32) * sc. */
+void oracle_block_dots_q6_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K, int32_t* dots) {
+    int64_t nb = K / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < nb; ++b)
+                dots[(m * N + n) * nb + b] = (int32_t)dot_q6_k(xq, wq, m, n, nb, b);
 }
 
 /* -------------------------------------------------------------- contractions */
@@ -290,6 +338,24 @@ static void entry_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t 
     *norm = t;
 }
 
+/* Q6_K: out[m,n] = sum_b xd * d * D[m,n,b] (the weight value d * sc * (q - 32) summed
+ * against the activation value xd * u; the sub-scales are inside D). */
+static void entry_q6_k(const uint8_t* xq, const uint8_t* wq, int64_t m, int64_t n, int64_t K,
+                       double* out, double* norm) {
+    int64_t nb = K / QK, nsb = K / QK_K;
+    double acc = 0.0, t = 0.0;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t* sbk = wq + (n * nsb + b / 8) * Q6_K_BYTES;
+        double xd = oracle_f16_to_f64(rd16(xq + (m * nb + b) * Q8_1_BYTES));
+        double d = oracle_f16_to_f64(rd16(sbk + 208));
+        double term = xd * d * (double)dot_q6_k(xq, wq, m, n, nb, b);
+        acc += term;
+        t += fabs(term);
+    }
+    *out = acc;
+    *norm = t;
+}
+
 /* Full contraction: out, norm double [M][N]. */
 void oracle_gemm_q8_0(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                       double* out, double* norm) {
@@ -312,6 +378,13 @@ void oracle_gemm_q5_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N
         for (int64_t n = 0; n < N; ++n) entry_q5_k(xq, wq, m, n, K, out + m * N + n, norm + m * N + n);
 }
 
+void oracle_gemm_q6_k(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
+                      double* out, double* norm) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) entry_q6_k(xq, wq, m, n, K, out + m * N + n, norm + m * N + n);
+}
+
 /* Sampled contraction: entry i is (im[i], in[i]); out, norm double [cnt]. */
 void oracle_gemm_q8_0_at(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
                          const int64_t* im, const int64_t* in, int64_t cnt, double* out, double* norm) {
@@ -332,6 +405,13 @@ void oracle_gemm_q5_k_at(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_
     (void)M; (void)N;
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < cnt; ++i) entry_q5_k(xq, wq, im[i], in[i], K, out + i, norm + i);
+}
+
+void oracle_gemm_q6_k_at(const uint8_t* xq, const uint8_t* wq, int64_t M, int64_t N, int64_t K,
+                         const int64_t* im, const int64_t* in, int64_t cnt, double* out, double* norm) {
+    (void)M; (void)N;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < cnt; ++i) entry_q6_k(xq, wq, im[i], in[i], K, out + i, norm + i);
 }
 
 /* Threads an OpenMP region of this library would use (the CPU baseline's core count). */

@@ -34,6 +34,7 @@ Q8_1_BYTES = 36
 Q8_0_BYTES = 34
 Q4_K_BYTES = 144
 Q5_K_BYTES = 176
+Q6_K_BYTES = 210
 
 BASE_SEED = 0x4D4D51
 
@@ -122,6 +123,21 @@ def q5_k_weights(seed: int, N: int, K: int) -> np.ndarray:
     return blk.reshape(N, nsb * Q5_K_BYTES)
 
 
+def q6_k_weights(seed: int, N: int, K: int) -> np.ndarray:
+    """uint8 [N, K/256*210]: per super-block 208 uniform bytes (128 low-nibble bytes, 64
+    bytes of 2-bit high parts, 16 int8 sub-scales: every byte pattern is valid), then f16 d
+    of either sign, |d| in [1e-5, 1e-4]."""
+    assert K % QK_K == 0
+    nsb = K // QK_K
+    u = uniform01(substream(seed, 34), N * nsb)
+    sign = np.where(uniform01(substream(seed, 35), N * nsb) < 0.5, -1.0, 1.0)
+    d = (sign * (1e-5 + u * (1e-4 - 1e-5))).astype(np.float16)
+    blk = np.empty((N * nsb, Q6_K_BYTES), dtype=np.uint8)
+    blk[:, :208] = random_bytes(substream(seed, 36), N * nsb * 208).reshape(-1, 208)
+    blk[:, 208:] = d.view(np.uint8).reshape(-1, 2)
+    return blk.reshape(N, nsb * Q6_K_BYTES)
+
+
 def weights(fmt: str, seed: int, N: int, K: int) -> np.ndarray:
     if fmt == "q8_0":
         return q8_0_weights(seed, N, K)
@@ -129,11 +145,14 @@ def weights(fmt: str, seed: int, N: int, K: int) -> np.ndarray:
         return q4_k_weights(seed, N, K)
     if fmt == "q5_k":
         return q5_k_weights(seed, N, K)
+    if fmt == "q6_k":
+        return q6_k_weights(seed, N, K)
     raise ValueError(f"unknown weight format {fmt!r}")
 
 
 def row_bytes(fmt: str, K: int) -> int:
-    return {"q8_0": K // QK * Q8_0_BYTES, "q4_k": K // QK_K * Q4_K_BYTES, "q5_k": K // QK_K * Q5_K_BYTES}[fmt]
+    return {"q8_0": K // QK * Q8_0_BYTES, "q4_k": K // QK_K * Q4_K_BYTES, "q5_k": K // QK_K * Q5_K_BYTES,
+            "q6_k": K // QK_K * Q6_K_BYTES}[fmt]
 
 
 # The five workloads: (format, M, N, K).  Seeds are BASE_SEED + index.

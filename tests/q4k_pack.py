@@ -52,3 +52,26 @@ def q5_k_super_block(d_f16: int, dmin_f16: int, sc, m, codes) -> np.ndarray:
     b[16:48] = qh.astype(np.uint8)
     b[48:] = pack_nibbles(codes & 15)
     return b
+
+
+def q6_k_super_block(d_f16: int, sc, codes) -> np.ndarray:
+    """Q6_K super-block (210 B, the GGUF arrangement) from 16 int8 sub-scales and 256
+    codes (0..63) in element order: 128 bytes of low nibbles, 64 bytes of 2-bit high
+    parts, the 16 sub-scales, f16 d.  Element 128h + 32t + l (t = 0..3, l = 0..31) keeps
+    its low nibble in byte 64h + 32(t % 2) + l (the high half of the byte for t >= 2) and
+    its top two bits in bits 2t, 2t + 1 of high-part byte 32h + l."""
+    codes = np.asarray(codes, dtype=np.int64).reshape(2, 4, 32)   # [h][t][l]
+    sc = np.asarray(sc, dtype=np.int64).reshape(16)
+    assert codes.min() >= 0 and codes.max() < 64 and sc.min() >= -128 and sc.max() < 128
+    b = np.zeros(210, dtype=np.uint8)
+    for h in range(2):
+        for tp in range(2):
+            lo, hi = codes[h, tp] & 15, codes[h, tp + 2] & 15
+            b[64 * h + 32 * tp: 64 * h + 32 * tp + 32] = (lo | (hi << 4)).astype(np.uint8)
+        qh = np.zeros(32, dtype=np.int64)
+        for t in range(4):
+            qh |= (codes[h, t] >> 4) << (2 * t)
+        b[128 + 32 * h: 160 + 32 * h] = qh.astype(np.uint8)
+    b[192:208] = sc.astype(np.int8).view(np.uint8)
+    b[208:210] = np.array([d_f16], dtype=np.uint16).view(np.uint8)
+    return b

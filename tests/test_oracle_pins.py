@@ -23,7 +23,7 @@ import pytest
 import oracle
 import synth
 from conftest import as_floats, as_ints
-from q4k_pack import pack_nibbles, pack_scales, q5_k_super_block, super_block
+from q4k_pack import pack_nibbles, pack_scales, q5_k_super_block, q6_k_super_block, super_block
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -173,6 +173,21 @@ def test_hand_example_q5_k_super_block(golden_hand):
     assert dots.reshape(8).tolist() == as_ints(g["e6_dots"])
     out, _ = oracle.gemm("q5_k", xq, blk[None, :], 1, 1, 256)
     assert out[0, 0] == as_floats(g["e6_out"])[0]
+
+
+def test_hand_example_q6_k_super_block(golden_hand):
+    g = golden_hand
+    xq1, _, _, _ = _quant_one(as_floats(g["e2_x"]))
+    xq = np.tile(xq1, (1, 8))
+    codes = np.repeat(as_ints(g["e7_codes"]), 16)
+    blk = q6_k_super_block(as_ints(g["e7_d_f16"])[0], as_ints(g["e7_sc"]), codes)
+    assert blk[as_ints(g["e7_ql_at"])].tolist() == as_ints(g["e7_ql"])
+    assert blk[128 + np.array(as_ints(g["e7_qh_at"]))].tolist() == as_ints(g["e7_qh"])
+    dots = oracle.block_dots("q6_k", xq, blk[None, :], 1, 1, 256)
+    assert dots.reshape(8).tolist() == as_ints(g["e7_dots"])
+    out, norm = oracle.gemm("q6_k", xq, blk[None, :], 1, 1, 256)
+    assert out[0, 0] == as_floats(g["e7_out"])[0]
+    assert norm[0, 0] == sum(abs(v) for v in as_ints(g["e7_dots"])) * 129 / 2048
 
 
 def test_hand_example_scale_top_bits(golden_hand):
@@ -493,3 +508,66 @@ def test_sampled_entries_match_full_contraction():
         im, inn = rng.integers(0, M, 40), rng.integers(0, N, 40)
         o2, n2 = oracle.gemm_at(fmt, xq, wq, M, N, K, im, inn)
         assert np.array_equal(o2, out[im, inn]) and np.array_equal(n2, norm[im, inn])
+
+
+def _random_q6_k(rng, N, K):
+    nsb = K // 256
+    d = (rng.uniform(1e-5, 1e-4, (N, nsb)) * rng.choice([-1.0, 1.0], (N, nsb))).astype(np.float16)
+    sc = rng.integers(-128, 128, (N, nsb, 16))
+    codes = rng.integers(0, 64, (N, nsb, 256))
+    w = np.stack([q6_k_super_block(int(d[n, s].view(np.uint16)), sc[n, s], codes[n, s])
+                  for n in range(N) for s in range(nsb)]).reshape(N, nsb * 210)
+    return w, d.astype(np.float64), sc, codes
+
+
+def test_block_dots_q6_k_brute_force_on_packed_codes():
+    # every element's six bits and its group's sub-scale land where the decoder looks
+    rng = np.random.default_rng(61)
+    M, N, K = 3, 5, 512
+    xq = oracle.quantize_q8_1(synth.activations(61, M, K, True))
+    w, d, sc, codes = _random_q6_k(rng, N, K)
+    dots = oracle.block_dots("q6_k", xq, w, M, N, K)
+    _, _, qa = split_q8_1(xq)
+    wv = (codes - 32) * np.repeat(sc, 16, axis=2)                   # (q - 32) * sc per element
+    ref = np.einsum("mbk,nbk->mnb", qa, wv.reshape(N, K // 32, 32))
+    assert np.array_equal(dots, ref)
+    assert np.abs(ref).max() > 2 ** 17  # the sub-scales reach the dots (not only the codes)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (2, 3, 512), (4, 2, 768)])
+def test_q6_k_equals_dequantized_fp64_matmul(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K + 6)
+    xq = oracle.quantize_q8_1(synth.activations(70 + M, M, K, True))
+    w, d, sc, codes = _random_q6_k(rng, N, K)
+    out, norm = oracle.gemm("q6_k", xq, w, M, N, K)
+    nsb = K // 256
+    wh = (d[:, :, None] * (np.repeat(sc, 16, axis=2) * (codes - 32))).reshape(N, K)
+    da, _, qa = split_q8_1(xq)
+    xh = (da[:, :, None] * qa).reshape(M, K)
+    ref = xh @ wh.T
+    scale = np.abs(xh) @ np.abs(wh).T
+    assert np.all(np.abs(out - ref) <= 1e-12 * scale)
+    assert np.all(norm >= np.abs(out) * (1 - 1e-15))
+
+
+def test_q6_k_with_one_sub_scale_per_block_equals_q8_0():
+    # both 16-element groups of every block share a sub-scale s_j in -3..3: the block is
+    # the Q8_0 block with codes (q - 32) * s_j (|.| <= 96) and the super-block's d
+    rng = np.random.default_rng(63)
+    M, N, K = 2, 3, 512
+    nsb = K // 256
+    xq = oracle.quantize_q8_1(synth.activations(63, M, K, True))
+    d = rng.uniform(1e-3, 1e-2, (N, nsb)).astype(np.float16)
+    sj = rng.integers(-3, 4, (N, nsb, 8))
+    codes = rng.integers(0, 64, (N, nsb, 256))
+    w6 = np.stack([q6_k_super_block(int(d[n, s].view(np.uint16)), np.repeat(sj[n, s], 2), codes[n, s])
+                   for n in range(N) for s in range(nsb)]).reshape(N, -1)
+    c8 = ((codes.reshape(N, nsb, 8, 32) - 32) * sj[:, :, :, None]).astype(np.int8)
+    w8 = np.zeros((N, nsb, 8, 34), dtype=np.uint8)
+    w8[:, :, :, 0:2] = np.repeat(d[:, :, None], 8, axis=2).view(np.uint8).reshape(N, nsb, 8, 2)
+    w8[:, :, :, 2:] = c8.view(np.uint8)
+    w8 = w8.reshape(N, -1)
+    o6, n6 = oracle.gemm("q6_k", xq, w6, M, N, K)
+    o8, n8 = oracle.gemm("q8_0", xq, w8, M, N, K)
+    assert np.array_equal(o6, o8) and np.array_equal(n6, n8)
+    assert np.array_equal(oracle.block_dots("q6_k", xq, w6, M, N, K), oracle.block_dots("q8_0", xq, w8, M, N, K))
