@@ -663,10 +663,11 @@ def run_sweep(args):
     cases = [("q4_k", M, 3584, 3584, "q") for M in synth.M_SWEEP]
     # small M on the larger projections too: a 7 MB weight is below the size at which any
     # kernel on this GPU streams at full HBM bandwidth
-    for fmt in ("q4_k", "q8_0", "q5_k"):
+    for fmt in ("q4_k", "q8_0", "q5_k", "q6_k"):
         cases += [(fmt, M, 18944, 3584, "gate") for M in (1, 2, 4, 8)]
         cases += [(fmt, M, 3584, 18944, "down") for M in (1, 2, 4, 8)]
-    cases += [("q5_k", M, 3584, 3584, "q") for M in (512, 2048)]  # Q5_K on the expanded path
+    for fmt in ("q5_k", "q6_k"):  # on the expanded path
+        cases += [(fmt, M, 3584, 3584, "q") for M in (512, 2048)]
     if args.only:  # one case, "fmt:M:N:K" (for profiling a single kernel)
         f, m, n, k = args.only.split(":")
         cases = [c for c in cases if c[:4] == (f, int(m), int(n), int(k))]
@@ -719,8 +720,8 @@ def run_sweep(args):
     return {"metric": "MMQ M sweep (GEMM only)", "unit": "mixed", "lines": lines,
             "data": "synthetic (seeded)", "peaks": peaks,
             "config": {"workload": "3584x3584 Q4_K projection, M in " + str(synth.M_SWEEP)
-                                   + "; M in [1, 2, 4, 8] on 18944x3584 and 3584x18944, Q4_K, Q8_0 and Q5_K"
-                                   + "; Q5_K 3584x3584 at M = 512, 2048",
+                                   + "; M in [1, 2, 4, 8] on 18944x3584 and 3584x18944, Q4_K, Q8_0, Q5_K"
+                                   + " and Q6_K; Q5_K and Q6_K 3584x3584 at M = 512, 2048",
                        "l2": "rotating weight copies >= 3x L2", "cuda_graph": True}}
 
 

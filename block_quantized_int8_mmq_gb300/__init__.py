@@ -14,8 +14,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmmq.so")
 
 QK, QK_K = 32, 256
-Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES, Q5_K_BYTES = 36, 34, 144, 176
-FMT = {"q8_0": 0, "q4_k": 1, "q5_k": 2}
+Q8_1_BYTES, Q8_0_BYTES, Q4_K_BYTES, Q5_K_BYTES, Q6_K_BYTES = 36, 34, 144, 176, 210
+FMT = {"q8_0": 0, "q4_k": 1, "q5_k": 2, "q6_k": 3}
 PATH_AUTO, PATH_SMALL, PATH_TC, PATH_EXPAND = 0, 1, 2, 3
 
 EXPORTED = (
@@ -24,6 +24,7 @@ EXPORTED = (
     "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
     "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k",
     "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
+    "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k",
 )
 
 
@@ -50,13 +51,13 @@ def _load():
     L.mmq_weight_row_bytes.argtypes = [I, I64]
     L.mmq_weight_row_bytes.restype = ctypes.c_size_t
     L.mmq_quantize_q8_1.argtypes = [P, I64, I64, P, P]
-    for f in ("mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_gemm_q5_k", "mmq_debug_block_dots_q8_0",
-              "mmq_debug_block_dots_q4_k", "mmq_debug_block_dots_q5_k"):
+    for f in ("mmq_gemm_q8_0", "mmq_gemm_q4_k", "mmq_gemm_q5_k", "mmq_gemm_q6_k", "mmq_debug_block_dots_q8_0",
+              "mmq_debug_block_dots_q4_k", "mmq_debug_block_dots_q5_k", "mmq_debug_block_dots_q6_k"):
         getattr(L, f).argtypes = [P, P, I64, I64, I64, P, P]
     L.mmq_set_path.argtypes = [I]
     L.mmq_get_device_error.argtypes = [P]
     L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
-    for f in ("mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_linear_q5_k"):
+    for f in ("mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_linear_q5_k", "mmq_linear_q6_k"):
         getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
     for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k"):
         getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
@@ -149,7 +150,7 @@ def mmq_gemm_q4_k(xq, wq, M, N, K, out=None, stream=None):
 
 def mmq_gemm_noalloc(fmt, xq, wq, M, N, K, out=None, stream=None):
     """The contraction on the expanded tensor-core path with the library's fixed 64 MiB
-    device scratch: no device allocation.  fmt: "q8_0" / "q4_k" or 0 / 1."""
+    device scratch: no device allocation.  fmt: "q8_0", "q4_k", "q5_k", "q6_k" or 0 .. 3."""
     import torch
     f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
     if out is None:
@@ -198,14 +199,23 @@ def mmq_debug_block_dots_q5_k(xq, wq, M, N, K, dots=None, stream=None):
     return _dots("mmq_debug_block_dots_q5_k", xq, wq, M, N, K, dots, stream)
 
 
+def mmq_gemm_q6_k(xq, wq, M, N, K, out=None, stream=None):
+    """q8_1 [M, K/32*36] x Q6_K [N, K/256*210] -> f32 [M, N]."""
+    return _gemm("mmq_gemm_q6_k", xq, wq, M, N, K, out, stream)
+
+
+def mmq_debug_block_dots_q6_k(xq, wq, M, N, K, dots=None, stream=None):
+    return _dots("mmq_debug_block_dots_q6_k", xq, wq, M, N, K, dots, stream)
+
+
 def gemm(fmt: str, xq, wq, M, N, K, out=None, stream=None):
-    f = {"q8_0": mmq_gemm_q8_0, "q4_k": mmq_gemm_q4_k, "q5_k": mmq_gemm_q5_k}[fmt]
+    f = {"q8_0": mmq_gemm_q8_0, "q4_k": mmq_gemm_q4_k, "q5_k": mmq_gemm_q5_k, "q6_k": mmq_gemm_q6_k}[fmt]
     return f(xq, wq, M, N, K, out, stream)
 
 
 def block_dots(fmt: str, xq, wq, M, N, K, dots=None, stream=None):
     f = {"q8_0": mmq_debug_block_dots_q8_0, "q4_k": mmq_debug_block_dots_q4_k,
-         "q5_k": mmq_debug_block_dots_q5_k}[fmt]
+         "q5_k": mmq_debug_block_dots_q5_k, "q6_k": mmq_debug_block_dots_q6_k}[fmt]
     return f(xq, wq, M, N, K, dots, stream)
 
 
@@ -223,7 +233,7 @@ def mmq_gemm_grouped(fmt: str, xq, row_expert, wq, E: int, N: int, K: int, out=N
 
 def mmq_linear(x, wq, fmt: str, N: int, xq=None, out=None, stream=None):
     """Quantize x (f32 [M, K]) to q8_1 (into xq) and contract it with weights wq in one
-    call (mmq_linear_q8_0 / mmq_linear_q4_k): f32 [M, N]."""
+    call (mmq_linear_<fmt>): f32 [M, N]."""
     import torch
     M, K = x.shape
     if xq is None:

@@ -61,11 +61,14 @@ constexpr int SM_COUNT = 152;  // GB300
 int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
     if (M <= 8 || K % QK_K != 0 || !tc_available()) return MMQ_PATH_SMALL;
     const double wbytes = (double)N * (double)mmq_weight_row_bytes(fmt, K);
-    const double t_small = (double)((M + 7) / 8) * wbytes / 1.3e6 + 3.0;
+    // Q6_K's small-M stream takes 4 rows per pass, and its expansion writes two fp16
+    // planes (4 bytes per value against 0.82 read)
+    const bool q6 = fmt == FMT_Q6_K;
+    const double t_small = (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * wbytes / 1.3e6 + 3.0;
     const double tiles = (double)((M + 127) / 128) * (double)((N + 127) / 128);
     const double waves = (double)(int64_t)((tiles + SM_COUNT - 1) / SM_COUNT);
     const double items = (double)(K / QK) * (is_kquant(fmt) ? 9.0 / 8.0 : 1.0);
-    const double t_expand = 3.0 * wbytes / 3.0e6 + waves * items * 0.34 + 8.0;
+    const double t_expand = (q6 ? 10.0 : 3.0) * wbytes / 3.0e6 + waves * items * 0.34 + 8.0;
     return t_small < t_expand ? MMQ_PATH_SMALL : MMQ_PATH_EXPAND;
 }
 
@@ -90,7 +93,7 @@ int check_mk(const char* fn, int64_t M, int64_t N, int64_t K, int64_t kmul) {
 
 int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
                 float* out, int32_t* dots, void* stream) {
-    int st = check_mk(fn, M, N, K, is_kquant(fmt) ? QK_K : QK);
+    int st = check_mk(fn, M, N, K, is_superblock(fmt) ? QK_K : QK);
     if (st) return st;
     void* o = out ? static_cast<void*>(out) : static_cast<void*>(dots);
     if (!xq || !wq || !o) {
@@ -119,7 +122,7 @@ int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t
 // operand); on the other paths it is the quantize kernel followed by the contraction.
 int linear(const char* fn, int fmt, const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq,
            float* out, void* stream) {
-    int st = check_mk(fn, M, N, K, is_kquant(fmt) ? QK_K : QK);
+    int st = check_mk(fn, M, N, K, is_superblock(fmt) ? QK_K : QK);
     if (st) return st;
     if (!x || !xq || !wq || !out) {
         report(fn, MMQ_ERR_NULL, "x, xq, wq and out must be non-NULL");
@@ -205,6 +208,7 @@ size_t mmq_weight_row_bytes(int fmt, int64_t K) {
     if (fmt == FMT_Q8_0 && K % QK == 0) return (size_t)(K / QK) * Q8_0_BYTES;
     if (fmt == FMT_Q4_K && K % QK_K == 0) return (size_t)(K / QK_K) * Q4_K_BYTES;
     if (fmt == FMT_Q5_K && K % QK_K == 0) return (size_t)(K / QK_K) * Q5_K_BYTES;
+    if (fmt == FMT_Q6_K && K % QK_K == 0) return (size_t)(K / QK_K) * Q6_K_BYTES;
     return 0;
 }
 
@@ -245,6 +249,20 @@ int mmq_debug_block_dots_q5_k(const void* xq, const void* wq, int64_t M, int64_t
     return contraction("mmq_debug_block_dots_q5_k", FMT_Q5_K, xq, wq, M, N, K, nullptr, dots, stream);
 }
 
+int mmq_gemm_q6_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, void* stream) {
+    return contraction("mmq_gemm_q6_k", FMT_Q6_K, xq, wq, M, N, K, out, nullptr, stream);
+}
+
+int mmq_linear_q6_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream) {
+    return linear("mmq_linear_q6_k", FMT_Q6_K, x, M, K, wq, N, xq, out, stream);
+}
+
+int mmq_debug_block_dots_q6_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,
+                              void* stream) {
+    return contraction("mmq_debug_block_dots_q6_k", FMT_Q6_K, xq, wq, M, N, K, nullptr, dots, stream);
+}
+
 int mmq_linear_q8_0(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
                     void* stream) {
     return linear("mmq_linear_q8_0", FMT_Q8_0, x, M, K, wq, N, xq, out, stream);
@@ -278,11 +296,11 @@ int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t
 int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                      void* stream) {
     const char* fn = "mmq_gemm_noalloc";
-    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K && fmt != FMT_Q5_K) {
-        report(fn, MMQ_ERR_ARG, "fmt must be 0 (Q8_0), 1 (Q4_K) or 2 (Q5_K)");
+    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K && fmt != FMT_Q5_K && fmt != FMT_Q6_K) {
+        report(fn, MMQ_ERR_ARG, "fmt must be 0 (Q8_0), 1 (Q4_K), 2 (Q5_K) or 3 (Q6_K)");
         return MMQ_ERR_ARG;
     }
-    int st = check_mk(fn, M, N, K, is_kquant(fmt) ? QK_K : QK);
+    int st = check_mk(fn, M, N, K, is_superblock(fmt) ? QK_K : QK);
     if (st) return st;
     if (!xq || !wq || !out) {
         report(fn, MMQ_ERR_NULL, "xq, wq and out must be non-NULL");

@@ -17,12 +17,18 @@ constexpr int Q8_1_BYTES = 36;   // f16 d, f16 s, int8 q[32]
 constexpr int Q8_0_BYTES = 34;   // f16 d, int8 q[32]
 constexpr int Q4_K_BYTES = 144;  // f16 d, f16 dmin, 12 scale bytes, 128 nibble bytes
 constexpr int Q5_K_BYTES = 176;  // f16 d, f16 dmin, 12 scale bytes, 32 high-bit bytes, 128 nibble bytes
+constexpr int Q6_K_BYTES = 210;  // 128 low-nibble bytes, 64 bytes of 2-bit high parts, 16 int8 scales, f16 d
 
-enum WeightFormat { FMT_Q8_0 = 0, FMT_Q4_K = 1, FMT_Q5_K = 2 };
-// K-quant super-block formats (256 values, eight 32-value sub-blocks with 6-bit scales and
-// mins, a min term per sub-block): Q4_K and Q5_K
+enum WeightFormat { FMT_Q8_0 = 0, FMT_Q4_K = 1, FMT_Q5_K = 2, FMT_Q6_K = 3 };
+// K-quant super-block formats with mins (256 values, eight 32-value sub-blocks with 6-bit
+// scales and mins, a min term per sub-block): Q4_K and Q5_K
 __host__ __device__ constexpr bool is_kquant(int fmt) { return fmt == FMT_Q4_K || fmt == FMT_Q5_K; }
-__host__ __device__ constexpr int kq_bytes(int fmt) { return fmt == FMT_Q5_K ? Q5_K_BYTES : Q4_K_BYTES; }
+// every format stored in 256-value super-blocks (K % 256 == 0): the K-quants with mins and
+// Q6_K (sixteen 16-value groups with int8 scales, values centred on 32, no min term)
+__host__ __device__ constexpr bool is_superblock(int fmt) { return is_kquant(fmt) || fmt == FMT_Q6_K; }
+__host__ __device__ constexpr int kq_bytes(int fmt) {
+    return fmt == FMT_Q6_K ? Q6_K_BYTES : fmt == FMT_Q5_K ? Q5_K_BYTES : Q4_K_BYTES;
+}
 // byte offset of the 128 nibble bytes in a super-block (Q5_K: after the 32 high-bit bytes)
 __host__ __device__ constexpr int kq_qs_off(int fmt) { return fmt == FMT_Q5_K ? 48 : 16; }
 

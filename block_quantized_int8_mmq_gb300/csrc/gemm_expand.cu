@@ -56,7 +56,10 @@ constexpr int GB = 8;                    // 32-blocks per group (256 values)
 constexpr int CHUNK = BM * QK * 2;       // fp16 codes of one block, 128 rows: 8 KiB
 constexpr int TILE16 = BM * 16 * 2;      // a K = 16 operand, 128 rows: 4 KiB
 constexpr int NSTAGE = 8;                // blocks in flight (one block per stage)
-constexpr int STAGE = 2 * CHUNK;         // activation chunk, then weight chunk
+// weight bytes per (tile, block): one chunk of codes, or for Q6_K two planes whose sum is
+// the code times its sub-scale (see expand_weights_q6_k)
+__host__ __device__ constexpr int wchunk(int fmt) { return fmt == FMT_Q6_K ? 2 * CHUNK : CHUNK; }
+__host__ __device__ constexpr int stage_bytes(int fmt) { return CHUNK + wchunk(fmt); }  // activation chunk, then weights
 constexpr int GR = 2;                    // group-data slots
 constexpr int NMMA = 2;                  // MMA-issuing warps; warp e issues items e, e + 2, ...
 constexpr int DS = NMMA;                 // TMEM slots: slot e (D and S of one item) belongs to issuer e
@@ -304,6 +307,101 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
     }
 }
 
+// Q6_K weights: one CTA per (32-row quarter of a 128-row tile, 256-value group).  A
+// weight value is d * sc * (q - 32) with q in 0..63 and an int8 scale sc per 16 values
+// ("When Does a Kernel Win Surface?", sec. "Unified dp4a decode cores": 16-element scale
+// groups, the q - 32 centring).  The scale changes inside a 32-value block, so it is
+// folded into the codes; (q - 32) * sc can reach 4096, past the integers fp16 holds
+// exactly, so it is split into two planes that are each exact:
+//   P1 = (q - 32) * 2 * (sc >> 1)   (|.| <= 4096, always even)
+//   P2 = (q - 32) * (sc & 1)        (|.| <= 32)
+// and the contraction takes both planes into the same block dot, which then equals the
+// integer sum of u * (q - 32) * sc (|D| < 2^24, exact in f32).  The block's column scale
+// is d.  Rows are 2-byte aligned only (210-byte super-blocks): a row's super-block is
+// gathered as the 16-byte granules that hold it, and words are read from shared memory
+// at the 4-byte boundary below and funnel-shifted into place.
+constexpr int Q6_SROW = 240;  // 15 granules: a super-block at any even offset in its first granule
+static_assert(Q6_SROW <= EXP_SROW && Q6_SROW >= 16 + Q6_K_BYTES + 14, "row pad");
+
+__device__ __forceinline__ uint2 q6_read8(const uint8_t* p) {  // 8 bytes at an even address
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)3);
+    const int fs = (int)(reinterpret_cast<uintptr_t>(p) & 2) * 8;
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
+    return make_uint2(__funnelshift_r(w0, w1, fs), __funnelshift_r(w1, w2, fs));
+}
+
+__device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
+                                                    uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
+                                                    uint8_t* __restrict__ sm) {
+    constexpr int GRAN = Q6_SROW / 16;
+    const int nt = bx >> 2, h = bx & 3, ng = nb / GB;
+    const int n0 = nt * BN + h * EXP_ROWS;
+    const long long rowbytes = (long long)ng * Q6_K_BYTES, end = (long long)N * rowbytes;
+    for (int i = threadIdx.x; i < EXP_ROWS * GRAN; i += EXP_THREADS) {
+        const int r = i / GRAN, c = i % GRAN;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n0 + r < N) {
+            const long long a = (long long)(n0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
+            const long long ga = (a & ~15ll) + 16 * c;
+            if (ga < a + Q6_K_BYTES) {
+                if (ga + 16 <= end) {
+                    v = __ldg(reinterpret_cast<const uint4*>(wq + ga));
+                } else {  // the buffer's last bytes, past its last whole granule
+                    uint16_t u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    for (int e = 0; e < 8 && ga + 2 * e < end; ++e)
+                        u[e] = __ldg(reinterpret_cast<const uint16_t*>(wq + ga + 2 * e));
+                    v = pack8(u);
+                }
+            }
+        }
+        *reinterpret_cast<uint4*>(sm + r * Q6_SROW + c * 16) = v;
+    }
+    __syncthreads();
+    auto sblk = [&](int r) -> const uint8_t* {  // super-block of row r of the quarter
+        const long long a = (long long)(n0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
+        return sm + r * Q6_SROW + (int)(a & 15);
+    };
+    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * (2 * CHUNK) + h * (CHUNK / 4);
+    constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
+    const __half2 one = __half2half2(__int2half_rn(1));
+    const __half2 n1056 = __half2half2(__int2half_rn(-1056));  // 0x6400 | q = 1024 + q; minus 1056 = q - 32
+    for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
+        const int j = i / PIECES, p = i % PIECES;
+        const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;  // row within the quarter, values 8kc .. 8kc + 7
+        const uint8_t* sb = sblk(r);
+        const int hh = j >> 2, t = j & 3;  // value 32j + 8kc + e = 128 hh + 32 t + (8 kc + e)
+        const uint2 lq = q6_read8(sb + 64 * hh + 32 * (t & 1) + 8 * kc);
+        const uint2 hq = q6_read8(sb + 128 + 32 * hh + 8 * kc);
+        const int sh = 4 * (t >> 1);
+        const uint32_t q0 = ((lq.x >> sh) & 0x0F0F0F0Fu) | (((hq.x >> (2 * t)) & 0x03030303u) << 4);
+        const uint32_t q1 = ((lq.y >> sh) & 0x0F0F0F0Fu) | (((hq.y >> (2 * t)) & 0x03030303u) << 4);
+        const int sc = (int)(int8_t)sb[192 + 2 * j + (kc >> 1)];
+        const uint2 c0 = u4x4_scaled_f16x4(q0, one, n1056), c1 = u4x4_scaled_f16x4(q1, one, n1056);  // q - 32
+        const __half2 s1 = __half2half2(__int2half_rn(2 * (sc >> 1))), s2 = __half2half2(__int2half_rn(sc & 1));
+        const uint4 p1 = make_uint4(h2_bits(__hmul2(bits_h2(c0.x), s1)), h2_bits(__hmul2(bits_h2(c0.y), s1)),
+                                    h2_bits(__hmul2(bits_h2(c1.x), s1)), h2_bits(__hmul2(bits_h2(c1.y), s1)));
+        const uint4 p2 = make_uint4(h2_bits(__hmul2(bits_h2(c0.x), s2)), h2_bits(__hmul2(bits_h2(c0.y), s2)),
+                                    h2_bits(__hmul2(bits_h2(c1.x), s2)), h2_bits(__hmul2(bits_h2(c1.y), s2)));
+        *reinterpret_cast<uint4*>(dst + (size_t)j * (2 * CHUNK) + p * 16) = p1;
+        *reinterpret_cast<uint4*>(dst + (size_t)j * (2 * CHUNK) + CHUNK + p * 16) = p2;
+    }
+    // WS[c][r] = d of the row's super-block for every block c: piece t = rows 32h + 8*(t%4)
+    // .. +7 of column c = t/4
+    const int t = threadIdx.x;
+    if (t < GB * EXP_ROWS / 8) {
+        const int c = t >> 2, r0 = (t & 3) * 8;
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint8_t* sb = sblk(r0 + e);
+            v[e] = (uint16_t)(sb[208] | (sb[209] << 8));
+        }
+        uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT_Q6_K);
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT_Q6_K) - ga_bytes(FMT_Q6_K) + (c * BN + h * EXP_ROWS + r0) * 2) =
+            pack8(v);
+    }
+}
+
 // Both expansions in one launch: CTAs 0 .. acts_x - 1 (grid x) expand the activations,
 // the rest the weights; grid y = the 256-value group.  The two halves are independent, so
 // they run side by side instead of one after the other.
@@ -313,10 +411,14 @@ k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t
          const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
          uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
     __shared__ __align__(16) uint8_t sm[EXP_ROWS * EXP_SROW];
-    if ((int)blockIdx.x < acts_x)
+    if ((int)blockIdx.x < acts_x) {
         expand_acts_body<FMT, FROM_X>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
-    else
-        expand_weights_body<FMT, FOLD>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+    } else {
+        if constexpr (FMT == FMT_Q6_K)  // the sub-scales are always folded (they are inside the block dot)
+            expand_weights_q6_k(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+        else
+            expand_weights_body<FMT, FOLD>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+    }
     // the contraction may start its set-up now; it reads the scratch only after this
     // whole grid has completed (griddepcontrol.wait)
     ptx::grid_dep_launch_dependents();
@@ -332,7 +434,7 @@ template <int FMT>
 struct XLayout {
     static constexpr int stages = 0;
     static constexpr int gslot = (ga_bytes(FMT) + gw_bytes(FMT) + 1023) & ~1023;
-    static constexpr int groups = stages + NSTAGE * STAGE;
+    static constexpr int groups = stages + NSTAGE * stage_bytes(FMT);
     static constexpr int onehot = groups + GR * gslot;
     static constexpr int bars = onehot + OH * TILE16;
     static constexpr int tmem_slot = bars + NBARS * 8;
@@ -355,7 +457,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     using L = XLayout<FMT>;
     constexpr bool MIN = is_kquant(FMT) && !DOTS;  // a min item closes every group
     constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
-    constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT);
+    constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT), WCH = wchunk(FMT), STAGE = stage_bytes(FMT);
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -430,7 +532,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     const uint32_t dst = sbase + L::stages + s * STAGE;
                     ptx::mbar_arrive_expect_tx(bar(BAR_ST_FULL + s), STAGE);
                     ptx::bulk_load(dst, xa + ((size_t)mt * nb + k) * CHUNK, CHUNK, bar(BAR_ST_FULL + s));
-                    ptx::bulk_load(dst + CHUNK, xb + ((size_t)nt * nb + k) * CHUNK, CHUNK, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst + CHUNK, xb + ((size_t)nt * nb + k) * WCH, WCH, bar(BAR_ST_FULL + s));
                     st_issued = k + 1;
                 }
             }
@@ -471,6 +573,10 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     const uint32_t a = sbase + L::stages + s * STAGE, b = a + CHUNK;
                     ptx::umma_f16(d, sdesc(a, 512), sdesc(b, 512), idesc, 0u);
                     ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + 256, 512), idesc, 1u);
+                    if (FMT == FMT_Q6_K) {  // the second weight plane into the same block dot
+                        ptx::umma_f16(d, sdesc(a, 512), sdesc(b + CHUNK, 512), idesc, 1u);
+                        ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + CHUNK + 256, 512), idesc, 1u);
+                    }
                     ptx::umma_commit(bar(BAR_ST_EMPTY + s));
                 } else {
                     // min item: AM x BMIN^T = sum_j s_j * m_j
@@ -646,7 +752,7 @@ struct ScratchPlan {
 ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K) {
     const int64_t nb = K / QK, ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    return {(size_t)(MT * nb) * CHUNK, (size_t)(MT * ng) * ga_bytes(fmt), (size_t)(NT * nb) * CHUNK,
+    return {(size_t)(MT * nb) * CHUNK, (size_t)(MT * ng) * ga_bytes(fmt), (size_t)(NT * nb) * wchunk(fmt),
             (size_t)(NT * ng) * gw_bytes(fmt)};
 }
 
@@ -783,6 +889,7 @@ int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, in
                cudaStream_t s) {
     const char* fn = fmt == FMT_Q8_0   ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
                      : fmt == FMT_Q5_K ? (dots ? "mmq_debug_block_dots_q5_k" : "mmq_gemm_q5_k")
+                     : fmt == FMT_Q6_K ? (dots ? "mmq_debug_block_dots_q6_k" : "mmq_gemm_q6_k")
                                        : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
     if (K % QK_K != 0) {
         report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
@@ -798,13 +905,18 @@ int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, in
     if (fmt == FMT_Q5_K)
         return dots ? launch_x<FMT_Q5_K, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
                     : launch_x<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
+    if (fmt == FMT_Q6_K)
+        return dots ? launch_x<FMT_Q6_K, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+                    : launch_x<FMT_Q6_K, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
     return dots ? launch_x<FMT_Q4_K, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
                 : launch_x<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
 }
 
 int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                       cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0 ? "mmq_linear_q8_0" : fmt == FMT_Q5_K ? "mmq_linear_q5_k" : "mmq_linear_q4_k";
+    const char* fn = fmt == FMT_Q8_0   ? "mmq_linear_q8_0"
+                     : fmt == FMT_Q5_K ? "mmq_linear_q5_k"
+                     : fmt == FMT_Q6_K ? "mmq_linear_q6_k" : "mmq_linear_q4_k";
     if (K % QK_K != 0) {
         report(fn, MMQ_ERR_K_MULTIPLE, "the expanded tensor-core path works in 256-value groups: K % 256 != 0");
         return MMQ_ERR_K_MULTIPLE;
@@ -815,6 +927,7 @@ int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t
     }
     return fmt == FMT_Q8_0   ? launch_x<FMT_Q8_0, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
            : fmt == FMT_Q5_K ? launch_x<FMT_Q5_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
+           : fmt == FMT_Q6_K ? launch_x<FMT_Q6_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn)
                              : launch_x<FMT_Q4_K, false>(x, xq, wq, M, N, K, out, nullptr, s, fn);
 }
 
@@ -846,6 +959,7 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
     }
     return fmt == FMT_Q8_0   ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
            : fmt == FMT_Q5_K ? launch_on<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
+           : fmt == FMT_Q6_K ? launch_on<FMT_Q6_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
                              : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn);
 }
 

@@ -347,13 +347,16 @@ k_mmq_small_mma(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, 
 __device__ unsigned int g_small_error;
 
 constexpr int DS_WARPS = 8;
-// slot bytes: 16 Q4_K super-blocks (2304 B; a Q8_0 piece, 64 * 34 = 2176 B, fits), or 16
-// Q5_K super-blocks (2816 B)
-__host__ __device__ constexpr int ds_slot(int fmt) { return fmt == FMT_Q5_K ? 16 * Q5_K_BYTES : 16 * Q4_K_BYTES; }
+// slot bytes: 16 Q4_K super-blocks (2304 B; a Q8_0 piece, 64 * 34 = 2176 B, fits), 16
+// Q5_K super-blocks (2816 B), or 16 Q6_K super-blocks (3360 B) with room for the 16-byte
+// granules around them (their rows are only 2-byte aligned: see the copy below)
+__host__ __device__ constexpr int ds_slot(int fmt) {
+    return fmt == FMT_Q6_K ? 16 * Q6_K_BYTES + 32 : fmt == FMT_Q5_K ? 16 * Q5_K_BYTES : 16 * Q4_K_BYTES;
+}
 constexpr uint64_t DS_WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t DS_SLEEP_NS = 2000;    // suspend hint of one barrier poll
-__host__ __device__ constexpr int ds_piece_units(int fmt) { return is_kquant(fmt) ? 16 : 64; }
-__host__ __device__ constexpr int ds_unit_bytes(int fmt) { return is_kquant(fmt) ? kq_bytes(fmt) : Q8_0_BYTES; }
+__host__ __device__ constexpr int ds_piece_units(int fmt) { return is_superblock(fmt) ? 16 : 64; }
+__host__ __device__ constexpr int ds_unit_bytes(int fmt) { return is_superblock(fmt) ? kq_bytes(fmt) : Q8_0_BYTES; }
 __host__ __device__ constexpr int ds_ring_bytes(int fmt, int slots) { return DS_WARPS * slots * (ds_slot(fmt) + 8); }
 // activation row stride in shared memory: 144 B per 4 blocks (nb % 8 == 0)
 __host__ __device__ constexpr int ds_xrow_bytes(int nb) { return nb / 4 * 144; }
@@ -361,7 +364,7 @@ __host__ __device__ constexpr int ds_smem_bytes(int fmt, int mt, int slots, int 
     return ds_ring_bytes(fmt, slots) + mt * (ds_xrow_bytes(nb) + 8 * nb);
 }
 static_assert(64 * Q8_0_BYTES <= ds_slot(FMT_Q8_0) && (64 * Q8_0_BYTES) % 16 == 0 && ds_slot(FMT_Q4_K) % 16 == 0 &&
-                  ds_slot(FMT_Q5_K) % 16 == 0,
+                  ds_slot(FMT_Q5_K) % 16 == 0 && ds_slot(FMT_Q6_K) % 16 == 0,
               "slots");
 
 // All lanes of the warp poll the slot's barrier (sleeping in the poll); false on every
@@ -407,10 +410,13 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
     uint8_t* xcodes = ds_smem + ds_ring_bytes(FMT, S);                         // [MT][nb/4][144]
     float* xdv = reinterpret_cast<float*>(xcodes + MT * xrow);           // [MT][nb]
     float* xsv = xdv + MT * nb;                                          // [MT][nb]
+    // Q6_K keeps, in place of the block sums s, the integer code sums of each block's two
+    // 16-value halves (int16 pairs) for the centring term
+    uint32_t* xhs = reinterpret_cast<uint32_t*>(xsv);
     const int m0 = blockIdx.y * MT;
     const int ntok = min(MT, M - m0);
     const int tw = gridDim.x * DS_WARPS, gw = blockIdx.x * DS_WARPS + warp;
-    const int units = is_kquant(FMT) ? nb >> 3 : nb;  // super-blocks or blocks per row
+    const int units = is_superblock(FMT) ? nb >> 3 : nb;  // super-blocks or blocks per row
     const int ppr = (units + PU - 1) / PU;             // pieces per row
     const long long row_bytes = (long long)units * UB;
     const int nrows = gw < N ? (N - 1 - gw) / tw + 1 : 0;
@@ -421,6 +427,23 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
         const long long n = gw + (long long)r * tw;
         const int u0 = p * PU, nu = min(PU, units - u0);
         const uint32_t bar = bar0 + 8 * (q % S);
+        if (FMT == FMT_Q6_K) {
+            // 210-byte super-blocks leave rows 2-byte aligned: copy the 16-byte granules that
+            // hold the piece (the consumer starts at the piece's offset in the first one).
+            // The buffer's bytes past its last whole granule come by plain loads instead.
+            const long long a = n * row_bytes + (long long)u0 * UB, end = (long long)N * row_bytes;
+            const long long a0 = a & ~15ll, lim = end & ~15ll;
+            long long a1 = (a + (long long)nu * UB + 15) & ~15ll;
+            uint8_t* slot = ring + (q % S) * DS_SLOT;
+            if (a1 > lim) {
+                for (long long o = lim; o < end; o += 2)
+                    *reinterpret_cast<uint16_t*>(slot + (o - a0)) = __ldg(reinterpret_cast<const uint16_t*>(wq + o));
+                a1 = lim;
+            }
+            ptx::mbar_arrive_expect_tx(bar, (uint32_t)(a1 - a0));
+            ptx::bulk_load(ptx::smem_u32(slot), wq + a0, (uint32_t)(a1 - a0), bar);
+            return;
+        }
         ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nu * UB));
         ptx::bulk_load(ptx::smem_u32(ring + (q % S) * DS_SLOT), wq + n * row_bytes + (long long)u0 * UB,
                        (uint32_t)(nu * UB), bar);
@@ -447,7 +470,17 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
         dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
         dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
         xdv[e] = f16_bits_to_f32(h);
-        xsv[e] = f16_bits_to_f32(h >> 16);
+        if (FMT == FMT_Q6_K) {
+            int s0 = 0, s1 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s0 = __dp4a((int)c[i], 0x01010101, s0);
+                s1 = __dp4a((int)c[i + 4], 0x01010101, s1);
+            }
+            xhs[e] = ((uint32_t)s0 & 0xFFFFu) | ((uint32_t)s1 << 16);
+        } else {
+            xsv[e] = f16_bits_to_f32(h >> 16);
+        }
     }
     __syncthreads();
 
@@ -465,7 +498,83 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
             }
             const uint8_t* pc = ring + (q % S) * DS_SLOT;
             const int u0 = p * PU, nu = min(PU, units - u0);
-            if (is_kquant(FMT)) {
+            if (FMT == FMT_Q6_K) {
+                const int sl = lane >> 1, h = lane & 1;  // super-block of the piece, half
+                if (sl < nu) {
+                    // the super-block starts at an even byte of the slot: read 4-byte words from
+                    // the word boundary below it and funnel-shift by 0 or 16 bits
+                    const int bs = (int)((n * row_bytes + (long long)u0 * UB) & 15) + sl * Q6_K_BYTES;
+                    const uint32_t* wa = reinterpret_cast<const uint32_t*>(pc + (bs & ~3));
+                    const int fs = (bs & 2) * 8;
+                    // half h: low-nibble bytes 64h .. 64h + 63, high-part bytes 128 + 32h ..
+                    // 128 + 32h + 31, scales 192 + 8h .. 192 + 8h + 7
+                    uint32_t ql[16], qh[8], scw[2];
+                    {
+                        uint32_t prev = wa[16 * h];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t nx = wa[16 * h + i + 1];
+                            ql[i] = __funnelshift_r(prev, nx, fs);
+                            prev = nx;
+                        }
+                        prev = wa[32 + 8 * h];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t nx = wa[32 + 8 * h + i + 1];
+                            qh[i] = __funnelshift_r(prev, nx, fs);
+                            prev = nx;
+                        }
+                        prev = wa[48 + 2 * h];
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const uint32_t nx = wa[48 + 2 * h + i + 1];
+                            scw[i] = __funnelshift_r(prev, nx, fs);
+                            prev = nx;
+                        }
+                    }
+                    const float d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(pc + bs + 208));
+                    const int b0 = 8 * (u0 + sl) + 4 * h;  // first block of the half in the row
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        const uint8_t* xb = xcodes + t * xrow + (b0 >> 2) * 144;  // blocks b0 .. b0 + 3
+                        const float4 xd = *reinterpret_cast<const float4*>(xdv + t * nb + b0);
+                        const uint4 hs = *reinterpret_cast<const uint4*>(xhs + t * nb + b0);
+                        const float xdu[4] = {xd.x, xd.y, xd.z, xd.w};
+                        const uint32_t hsu[4] = {hs.x, hs.y, hs.z, hs.w};
+                        float sacc = 0.f;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {  // block 4h + u: value 128h + 32u + l
+                            const uint4 xa = *reinterpret_cast<const uint4*>(xb + u * QK);
+                            const uint4 xc = *reinterpret_cast<const uint4*>(xb + u * QK + 16);
+                            uint32_t code[8];  // 6-bit codes 0..63, four per word
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                code[k] = ((ql[8 * (u & 1) + k] >> (4 * (u >> 1))) & 0x0F0F0F0Fu) |
+                                          (((qh[k] >> (2 * u)) & 0x03030303u) << 4);
+                            int Da = 0, Db = 0;  // the two 16-value groups
+                            Da = dp4a_us(code[0], xa.x, Da);
+                            Da = dp4a_us(code[1], xa.y, Da);
+                            Da = dp4a_us(code[2], xa.z, Da);
+                            Da = dp4a_us(code[3], xa.w, Da);
+                            Db = dp4a_us(code[4], xc.x, Db);
+                            Db = dp4a_us(code[5], xc.y, Db);
+                            Db = dp4a_us(code[6], xc.z, Db);
+                            Db = dp4a_us(code[7], xc.w, Db);
+                            // centring as a bias term: sum (q - 32) u = dp4a(q, u) - 32 sum u
+                            Da -= 32 * (int)(int16_t)(hsu[u] & 0xFFFFu);
+                            Db -= 32 * ((int)hsu[u] >> 16);
+                            const uint32_t sw = scw[u >> 1] >> (16 * (u & 1));
+                            const int D = (int)(int8_t)(sw & 0xFFu) * Da + (int)(int8_t)((sw >> 8) & 0xFFu) * Db;
+                            if (dots) {
+                                if (t < ntok) dots[((long long)(m0 + t) * N + n) * nb + b0 + u] = D;
+                            } else {
+                                sacc = fmaf(xdu[u], (float)D, sacc);
+                            }
+                        }
+                        acc[t] = fmaf(d, sacc, acc[t]);
+                    }
+                }
+            } else if (is_kquant(FMT)) {
                 const int sl = lane >> 1, h = lane & 1;  // super-block of the piece, half
                 if (sl < nu) {
                     const uint8_t* sbk = pc + sl * UB;
@@ -993,8 +1102,24 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     }
     const uint8_t* x8 = static_cast<const uint8_t*>(xq);
     const uint8_t* w8 = static_cast<const uint8_t*>(wq);
-    const char* sfn = fmt == FMT_Q8_0 ? "mmq_gemm_q8_0 (small-M)"
-                      : fmt == FMT_Q5_K ? "mmq_gemm_q5_k (small-M)" : "mmq_gemm_q4_k (small-M)";
+    const char* sfn = fmt == FMT_Q8_0   ? "mmq_gemm_q8_0 (small-M)"
+                      : fmt == FMT_Q5_K ? "mmq_gemm_q5_k (small-M)"
+                      : fmt == FMT_Q6_K ? "mmq_gemm_q6_k (small-M)" : "mmq_gemm_q4_k (small-M)";
+    if (fmt == FMT_Q6_K) {
+        // the dp4a weight stream, 1, 2 or 4 activation rows per pass (one row per pass when
+        // four rows' activations do not fit in shared memory next to the ring)
+        if (nb % 8 != 0) {
+            report(sfn, MMQ_ERR_K_MULTIPLE, "Q6_K needs K % 256 == 0");
+            return MMQ_ERR_K_MULTIPLE;
+        }
+        const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+        if (ds_smem_bytes(fmt, mt, mt == 1 ? 2 : 4, nb) <= 220 * 1024 && (M + mt - 1) / mt <= 65535)
+            return launch_dp4a_stream<FMT_Q6_K>(x8, w8, M, N, nb, out, dots, s, sfn);
+        if (ds_smem_bytes(fmt, 1, 2, nb) <= 220 * 1024 && M <= 65535)
+            return launch_dp4a_stream_s<FMT_Q6_K, 1, 2>(x8, w8, M, N, nb, out, dots, s, sfn);
+        report(sfn, MMQ_ERR_SHAPE, "K or M too large for the Q6_K small-M stream (the expanded path takes it)");
+        return MMQ_ERR_SHAPE;
+    }
     // measured crossovers: the dp4a weight streams for one or two rows (and Q4_K up to four),
     // the int8 tensor-core stream beyond, one pass per 8 rows
     const int64_t dp4a_max_m = is_kquant(fmt) ? 4 : 2;

@@ -481,9 +481,11 @@ int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int
               cudaStream_t s) {
     const char* fn = fmt == FMT_Q8_0   ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
                      : fmt == FMT_Q5_K ? (dots ? "mmq_debug_block_dots_q5_k" : "mmq_gemm_q5_k")
+                     : fmt == FMT_Q6_K ? (dots ? "mmq_debug_block_dots_q6_k" : "mmq_gemm_q6_k")
                                        : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
-    if (fmt == FMT_Q5_K) {
-        report(fn, MMQ_ERR_ARG, "the converter tensor-core kernel takes Q8_0 and Q4_K (Q5_K: the expanded path)");
+    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K) {
+        report(fn, MMQ_ERR_ARG,
+               "the converter tensor-core kernel takes Q8_0 and Q4_K (Q5_K and Q6_K: the expanded path)");
         return MMQ_ERR_ARG;
     }
     if (K % QK_K != 0) {

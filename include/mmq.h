@@ -3,7 +3,7 @@
  * (libmmq.so).
  *
  * The operation: activations x (f32, M rows of K) are quantized to q8_1 blocks and
- * contracted against block-quantized weights (Q8_0 or Q4_K, N rows of K):
+ * contracted against block-quantized weights (Q8_0, Q4_K, Q5_K or Q6_K, N rows of K):
  *
  *   out[m,n] = sum over 32-element blocks b of (xd[m,b] * wd[n,b]) * sum_{k in b} xq[m,k] * wq[n,k]
  *
@@ -11,8 +11,10 @@
  * -dmin * m_j * xs[m,b] per block ("When the Product Won't Collapse: A Negative Result
  * on int8 Tensor-Core MMQ", sec. "The obstruction: an opaque accumulator", display
  * equation; "When Does a Kernel Win Surface?", sec. "Kept levers: Vulkan", the Q4_K x
- * q8_1 affine identity).  The scale is applied at every 32-block boundary because the
- * integer sum is only meaningful inside one constant-scale block.
+ * q8_1 affine identity); Q5_K as Q4_K with 5-bit codes; for Q6_K, wd = d and the
+ * 16-value int8 sub-scales sit inside the block's integer sum (see mmq_gemm_q6_k).  The
+ * scale is applied at every 32-block boundary because the integer sum is only meaningful
+ * inside one constant-scale block.
  *
  * Conventions shared by every entry point:
  *  - Pointers named x, xq, wq, out, dots are DEVICE pointers owned by the caller.  The
@@ -32,7 +34,8 @@
  *    ignored: a call that returns MMQ_OK has enqueued the complete computation.
  *  - Device-side bounded waits (pipeline barriers) that run out set a sticky device
  *    error word instead of hanging; mmq_get_device_error() reads and clears it.
- *  - Shapes: 1 <= M, N and K a positive multiple of 32 (q8_1, Q8_0) or of 256 (Q4_K);
+ *  - Shapes: 1 <= M, N and K a positive multiple of 32 (q8_1, Q8_0) or of 256 (Q4_K,
+ *    Q5_K, Q6_K);
  *    all of M*K, N*K and M*N below 2^40.
  *  - Finite inputs are required; NaN or Inf in x gives unspecified codes.
  *
@@ -52,6 +55,14 @@
  *    32 high-bit bytes @16, 128 nibble bytes @48 as the Q4_K nibbles.  Value 64c+32h+i
  *    (h = 0, 1) takes its fifth bit from bit 2c+h of high-bit byte i; value =
  *    d*sc_j*q - dmin*m_j, q in 0..31.
+ *  Q6_K super-block (210 B, 256 values; listed in the same section, and "When Does a
+ *    Kernel Win Surface?", sec. "Unified dp4a decode cores", gives its 16-value scale
+ *    groups and the q - 32 centring; bytes in the GGUF arrangement): 128 low-nibble bytes
+ *    @0, 64 bytes of 2-bit high parts @128, 16 int8 sub-scales @192, f16 d @208.  Value
+ *    128h + 32t + l (h = 0, 1; t = 0..3; l = 0..31): low 4 bits from byte 64h + 32(t%2) + l
+ *    (low nibble for t < 2, high for t >= 2), top 2 bits from bits 2t, 2t+1 of byte
+ *    128 + 32h + l; value = d * sc[v/16] * (q - 32), q in 0..63.  Weights are [N][K/256]
+ *    super-blocks, so rows are only 2-byte aligned; wq itself must be 16-byte aligned.
  *  out: f32 [M][N] row-major, fully overwritten (no accumulate mode).
  */
 #ifndef MMQ_H
@@ -134,6 +145,19 @@ int mmq_gemm_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
                   void* stream);
 
 /*
+ * out = xq (q8_1) contracted with Q6_K weights wq ([N][K/256] super-blocks of 210 B):
+ *   out[m,n] = sum_b xd[m,b] * d * D[m,n,b],  D = sum_{k in b} xq[m,k] * (q[n,k] - 32) * sc
+ * with sc the int8 scale of k's 16-value group and d that of the block's super-block (no
+ * min term).  K % 256 == 0; alignment and accuracy as mmq_gemm_q8_0.  Runs on the
+ * expanded-code tensor-core path and the small-M stream (4 activation rows per pass); the
+ * converter kernel (MMQ_PATH_TC) refuses it with MMQ_ERR_ARG, and the small-M stream
+ * refuses (MMQ_ERR_SHAPE) a K whose activation rows do not fit in shared memory (above
+ * about 120000).
+ */
+int mmq_gemm_q6_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+                  void* stream);
+
+/*
  * Quantize + contraction in one call: xq = q8_1 of x (the same bytes as
  * mmq_quantize_q8_1) and out = xq contracted with Q8_0 (mmq_linear_q8_0) or Q4_K
  * (mmq_linear_q4_k) weights, as mmq_gemm_q8_0 / mmq_gemm_q4_k would compute it.  On the
@@ -151,6 +175,8 @@ int mmq_linear_q8_0(const float* x, int64_t M, int64_t K, const void* wq, int64_
 int mmq_linear_q4_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
                     void* stream);
 int mmq_linear_q5_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
+                    void* stream);
+int mmq_linear_q6_k(const float* x, int64_t M, int64_t K, const void* wq, int64_t N, void* xq, float* out,
                     void* stream);
 
 /*
@@ -179,7 +205,8 @@ int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, 
  * path as mmq_gemm_q8_0 / mmq_gemm_q4_k select for this M (same staging, same
  * conversion, same MMA), written out instead of rescaled.  For Q4_K, D is the dot of
  * the activation codes with the raw 4-bit codes (0..15), without sc_j; for Q5_K, with
- * the raw 5-bit codes (0..31).
+ * the raw 5-bit codes (0..31).  For Q6_K, whose scale changes inside a block, D is the
+ * block's integer sum of xq * (q - 32) * sc (the D of mmq_gemm_q6_k; |D| < 2^24).
  *   dots: int32 [M][N][K/32], 16-byte aligned.  Bit-exact by definition.
  */
 int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
@@ -188,16 +215,20 @@ int mmq_debug_block_dots_q4_k(const void* xq, const void* wq, int64_t M, int64_t
                               int32_t* dots, void* stream);
 int mmq_debug_block_dots_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
                               int32_t* dots, void* stream);
+int mmq_debug_block_dots_q6_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
+                              int32_t* dots, void* stream);
 
 /*
- * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1) or mmq_gemm_q5_k
- * (fmt 2) on the expanded-code tensor-core path, with its scratch taken from a fixed
- * 64 MiB array in the library's device memory (one per device) instead of an allocation:
- * this call allocates no device memory and calls nothing that does.  The method's pages have no counterpart of this
- * entry point; it exists for callers that may not allocate.
+ * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1), mmq_gemm_q5_k (fmt 2)
+ * or mmq_gemm_q6_k (fmt 3) on the expanded-code tensor-core path, with its scratch taken
+ * from a fixed 64 MiB array in the library's device memory (one per device) instead of an
+ * allocation: this call allocates no device memory and calls nothing that does.  The
+ * method's pages have no counterpart of this entry point; it exists for callers that may
+ * not allocate.
  *  - Scratch need, in bytes, with MT = ceil(M/128), NT = ceil(N/128), nb = K/32,
- *    ng = K/256:  MT*nb*8192 + MT*ng*GA + NT*nb*8192 + NT*ng*GW, where GA = 4096 and
- *    GW = 2048 for Q8_0, GA = 8192 and GW = 6400 for Q4_K and Q5_K.  A shape that needs
+ *    ng = K/256:  MT*nb*8192 + MT*ng*GA + NT*nb*WB + NT*ng*GW, where WB = 8192 (16384
+ *    for Q6_K), GA = 4096 and GW = 2048 for Q8_0 and Q6_K, GA = 8192 and GW = 6400 for
+ *    Q4_K and Q5_K.  A shape that needs
  *    more than 64 MiB is refused with MMQ_ERR_SHAPE (e.g. M = 512, N = K = 3584 Q8_0
  *    needs about 30 MiB).  K % 256 == 0 for every format (MMQ_ERR_K_MULTIPLE otherwise).
  *  - The array's address is looked up (cudaGetSymbolAddress) on the first call on each
@@ -208,7 +239,7 @@ int mmq_debug_block_dots_q5_k(const void* xq, const void* wq, int64_t M, int64_t
  *  - Nothing in the array has to start at zero: the call writes every scratch byte it
  *    reads before reading it.
  *  - Arguments, alignment, accuracy and the other errors as mmq_gemm_q8_0 /
- *    mmq_gemm_q4_k / mmq_gemm_q5_k; MMQ_ERR_ARG for another fmt.
+ *    mmq_gemm_q4_k / mmq_gemm_q5_k / mmq_gemm_q6_k; MMQ_ERR_ARG for another fmt.
  */
 int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                      void* stream);

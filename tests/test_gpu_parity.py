@@ -99,14 +99,15 @@ SMALL_SHAPES = {
     "q4_k": [(1, 1, 256), (3, 7, 256), (9, 33, 512), (64, 256, 512), (130, 200, 1024), (257, 129, 2304),
              (8, 300, 3584)],
 }
-SMALL_SHAPES["q5_k"] = SMALL_SHAPES["q4_k"]
-FMTS = ["q8_0", "q4_k", "q5_k"]
+SMALL_SHAPES["q5_k"] = SMALL_SHAPES["q6_k"] = SMALL_SHAPES["q4_k"]
+FMTS = ["q8_0", "q4_k", "q5_k", "q6_k"]
+NO_TC = ("q5_k", "q6_k")  # formats the converter kernel refuses
 
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_parity_full(mmq, fmt, path):
-    if (fmt, path) == ("q5_k", "tc"):
+    if fmt in NO_TC and path == "tc":
         pytest.skip("the converter kernel takes Q8_0 and Q4_K (refusal tested below)")
     set_path(mmq, path)
     for (M, N, K) in SMALL_SHAPES[fmt]:
@@ -142,7 +143,7 @@ def test_tc_paths_refuse_partial_k_groups_and_auto_routes_them(mmq, path):
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("fmt", FMTS)
 def test_block_dots_bit_exact(mmq, fmt, path):
-    if (fmt, path) == ("q5_k", "tc"):
+    if fmt in NO_TC and path == "tc":
         pytest.skip("the converter kernel takes Q8_0 and Q4_K")
     set_path(mmq, path)
     for (M, N, K) in [(5, 9, 256), (70, 150, 512), (129, 257, 1024)]:
@@ -186,7 +187,7 @@ def test_few_row_stream_parity_and_dots(mmq, fmt):
 @pytest.mark.parametrize("path", ["auto", "expand", "small", "tc"])
 @pytest.mark.parametrize("fmt", FMTS)
 def test_linear_matches_separate_calls(mmq, fmt, path):
-    if (fmt, path) == ("q5_k", "tc"):
+    if fmt in NO_TC and path == "tc":
         pytest.skip("the converter kernel takes Q8_0 and Q4_K")
     set_path(mmq, path)
     for (M, N, K) in [(300, 200, 1024), (129, 257, 2304), (4, 130, 512), (513, 64, 256)]:
@@ -258,20 +259,28 @@ def test_extreme_codes_block_dots(mmq, path):
     check_close(out.cpu().numpy(), r, nrm, "extreme codes")
 
 
-def test_q5_k_refused_by_converter_kernel_auto_takes_it(mmq):
+@pytest.mark.parametrize("fmt", NO_TC)
+def test_refused_by_converter_kernel_auto_takes_it(mmq, fmt):
     M, N, K = 600, 64, 512
     x = synth.activations(31, M, K, True)
-    w = synth.q5_k_weights(32, N, K)
+    w = synth.weights(fmt, 32, N, K)
     xq = mmq.mmq_quantize_q8_1(dev(x))
     set_path(mmq, "tc")
     with pytest.raises(mmq.MMQError) as e:
-        mmq.mmq_gemm_q5_k(xq, dev(w), M, N, K)
+        mmq.gemm(fmt, xq, dev(w), M, N, K)
     assert e.value.status == -9  # MMQ_ERR_ARG
     set_path(mmq, "auto")
-    out = mmq.mmq_gemm_q5_k(xq, dev(w), M, N, K)
+    out = mmq.gemm(fmt, xq, dev(w), M, N, K)
     assert mmq.mmq_last_path() in (mmq.PATH_SMALL, mmq.PATH_EXPAND)
-    ref, norm = oracle.gemm("q5_k", oracle.quantize_q8_1(x), w, M, N, K)
-    check_close(out.cpu().numpy(), ref, norm, "q5_k auto")
+    ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, f"{fmt} auto")
+    assert mmq.mmq_get_device_error() == 0
+
+
+def test_q5_k_extreme_codes_block_dots(mmq):
+    M, N, K = 600, 64, 512
+    x = synth.activations(31, M, K, True)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
     # Q5_K codes at the ends of 0..31 with the largest 6-bit scale: (q * sc) up to 31 * 63
     # and the min term at 63 * 63 on every sub-block
     w2 = synth.q5_k_weights(33, N, K).reshape(N, K // 256, 176).copy()
@@ -363,24 +372,53 @@ def test_m_sweep_sampled_parity(mmq, M):
     check_close(out[im, inn], ref, norm, f"M sweep {M}")
 
 
+def test_q6_k_extreme_codes_block_dots(mmq):
+    # |D| up to 32 * 127 * 32 * 128 = 16646144 (just under 2^24): activation codes +-127,
+    # weight codes 0 or 63 (q - 32 = -32 or 31), sub-scales -128 or 127
+    M, N, K = 130, 136, 512
+    xs = np.where(np.arange(M * K).reshape(M, K) % 5 == 0, -1.0, 1.0).astype(np.float32)
+    xs[::2] = -1.0
+    w = synth.q6_k_weights(41, N, K).reshape(N, K // 256, 210).copy()
+    w[:, :, :128] = np.where(np.arange(128) % 3 == 0, 0x00, 0xFF).astype(np.uint8)   # low nibbles 0 or 15
+    w[:, :, 128:192] = np.where(np.arange(64) % 3 == 0, 0x00, 0xFF).astype(np.uint8)  # top bits 0 or 3
+    w[:, :, 192:208] = np.where(np.arange(16) % 2 == 0, 0x80, 0x7F).astype(np.uint8)  # -128, 127
+    w[:4, :, 128:192] = 0x00  # rows 0..3: every code 0 or 15 -> q - 32 <= -17
+    w[4:8, :, :192] = 0x00    # rows 4..7: every code 0 -> D = -32 * sc * sum(u)
+    w[4:8, :, 192:208] = 0x80
+    w = w.reshape(N, -1)
+    xq = mmq.mmq_quantize_q8_1(dev(xs))
+    xq_ref = oracle.quantize_q8_1(xs)
+    ref = oracle.block_dots("q6_k", xq_ref, w, M, N, K)
+    assert np.abs(ref).max() == 32 * 127 * 32 * 128
+    for path in ("expand", "small"):
+        set_path(mmq, path)
+        dots = mmq.mmq_debug_block_dots_q6_k(xq, dev(w), M, N, K)
+        assert np.array_equal(dots.cpu().numpy(), ref), path
+        out = mmq.mmq_gemm_q6_k(xq, dev(w), M, N, K)
+        r, nrm = oracle.gemm("q6_k", xq_ref, w, M, N, K)
+        check_close(out.cpu().numpy(), r, nrm, f"q6_k extreme codes {path}")
+    assert mmq.mmq_get_device_error() == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 18944, 3584), (1, 3584, 18944), (4, 18944, 3584), (8, 3584, 18944),
                                    (512, 3584, 3584), (2048, 18944, 3584)])
-def test_q5_k_full_size_sampled_parity(mmq, M, N, K):
-    """Q5_K at the 7B-class projection sizes: the small-M streams and the expanded path."""
+@pytest.mark.parametrize("fmt", NO_TC)
+def test_k_quant_full_size_sampled_parity(mmq, fmt, M, N, K):
+    """Q5_K and Q6_K at the 7B-class projection sizes: the small-M streams and the expanded path."""
     set_path(mmq, "auto")
     x = synth.activations(synth.substream(synth.BASE_SEED + 5, M + N), M, K, True)
-    w = synth.q5_k_weights(synth.substream(synth.BASE_SEED + 6, N + K), N, K)
+    w = synth.weights(fmt, synth.substream(synth.BASE_SEED + 6, N + K), N, K)
     xq_ref = oracle.quantize_q8_1(x)
     xq = torch.empty((M, K // 32 * 36), dtype=torch.uint8, device="cuda")
     out = torch.full((M, N), float("nan"), device="cuda")
-    mmq.mmq_linear(dev(x), dev(w), "q5_k", N, xq=xq, out=out)
+    mmq.mmq_linear(dev(x), dev(w), fmt, N, xq=xq, out=out)
     assert mmq.mmq_last_path() == (mmq.PATH_EXPAND if M >= 512 else mmq.PATH_SMALL)
     assert np.array_equal(xq.cpu().numpy(), xq_ref)
     o = out.cpu().numpy()
     assert not np.isnan(o).any(), "output not fully written"
     im, inn = sample_entries(M, N, 1500, M + 5)
-    ref, norm = oracle.gemm_at("q5_k", xq_ref, w, M, N, K, im, inn)
-    check_close(o[im, inn], ref, norm, f"q5_k {M}x{N}x{K}")
+    ref, norm = oracle.gemm_at(fmt, xq_ref, w, M, N, K, im, inn)
+    check_close(o[im, inn], ref, norm, f"{fmt} {M}x{N}x{K}")
     assert mmq.mmq_get_device_error() == 0
 
 

@@ -32,7 +32,8 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-CASES = [("q4_k", 300, 520, 1024, 71), ("q8_0", 512, 3584, 3584, 72), ("q5_k", 130, 300, 512, 73)]
+CASES = [("q4_k", 300, 520, 1024, 71), ("q8_0", 512, 3584, 3584, 72), ("q5_k", 130, 300, 512, 73),
+         ("q6_k", 200, 260, 768, 74)]
 
 
 def test_two_consecutive_calls_match_the_allocating_path(mmq):
@@ -73,7 +74,7 @@ def test_refuses_shapes_beyond_the_fixed_scratch(mmq):
     st = lib.mmq_gemm_noalloc(0, ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(wq.data_ptr()), 64, 64, 3584 + 32,
                               ctypes.c_void_p(out.data_ptr()), None)
     assert st == -2
-    st = lib.mmq_gemm_noalloc(3, ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(wq.data_ptr()), 64, 64, 256,
+    st = lib.mmq_gemm_noalloc(4, ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(wq.data_ptr()), 64, 64, 256,
                               ctypes.c_void_p(out.data_ptr()), None)
     assert st == -9
     torch.cuda.synchronize()
