@@ -87,6 +87,35 @@ bool make_byte_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint6
 void report(const char* fn, int status, const char* detail);
 int launch_status(const char* fn);
 
+// Launch as a programmatic dependent of the previous kernel on the stream: the kernel may be
+// scheduled while that kernel drains, if that kernel allows it (griddepcontrol.launch_dependents);
+// the kernel itself must execute griddepcontrol.wait before it reads anything the previous
+// kernel may have written and before any global write.  Returns the launch's CUDA error.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// launch_status for a launch_pdl result: the error reported (and cleared) or MMQ_OK
+inline int pdl_status(cudaError_t e, const char* fn) {
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_LAUNCH, cudaGetErrorString(e));
+        return MMQ_ERR_LAUNCH;
+    }
+    return launch_status(fn);
+}
+
 // Per-kernel timing (profile.cu): a ProfScope around a launch brackets it with two
 // events on `s` while profiling is enabled.
 bool profiling();

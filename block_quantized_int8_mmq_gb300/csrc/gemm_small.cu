@@ -456,6 +456,12 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
     __syncwarp();
     for (; issued < S && issued < total; ++issued)
         if (lane == 0) issue(issued);
+    // Launched as a programmatic dependent: the weights (never written by a kernel of this
+    // library) start streaming while the previous kernel on the stream drains; the
+    // activations may be its output, so they are read, and anything is written, only after
+    // it has completed.  The next kernel may be scheduled from here on.
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
     // stage the activation rows (rows past M as zeros) while the first pieces arrive
     for (int e = threadIdx.x; e < MT * nb; e += DS_WARPS * 32) {
         const int t = e / nb, b = e - t * nb;
@@ -774,9 +780,10 @@ int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_
     dim3 grid((unsigned)ctas, (unsigned)((M + MT - 1) / MT));
     {
         ProfScope ps("k_mmq_dp4a_stream", s);
-        k_mmq_dp4a_stream<FMT, MT, S><<<grid, DS_WARPS * 32, smem, s>>>(x8, w8, (int)M, (int)N, nb, out, dots);
+        return pdl_status(launch_pdl(k_mmq_dp4a_stream<FMT, MT, S>, grid, dim3(DS_WARPS * 32), (size_t)smem, s, x8, w8,
+                                     (int)M, (int)N, nb, out, dots),
+                          fn);
     }
-    return launch_status(fn);
 }
 
 // Two slots and four CTAs per SM (more warps to hide the math) for one activation row;
@@ -878,6 +885,10 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restri
     __syncwarp();
     for (; issued < S && issued < total; ++issued)
         if (lane == 0) issue(issued);
+    // programmatic dependent: the weight pieces above are in flight; activations are read,
+    // and results written, only after the previous kernel on the stream has completed
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
 
     bool ok = true;
     int i = 0;
@@ -1075,9 +1086,10 @@ int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
     dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
     {
         ProfScope ps("k_mmq_i8_stream", s);
-        k_mmq_i8_stream<FMT><<<grid, IS_WARPS * 32, smem, s>>>(tm, x8, (int)M, (int)N, nb, (int)tpc, out, dots);
+        return pdl_status(launch_pdl(k_mmq_i8_stream<FMT>, grid, dim3(IS_WARPS * 32), (size_t)smem, s, tm, x8, (int)M,
+                                     (int)N, nb, (int)tpc, out, dots),
+                          fn);
     }
-    return launch_status(fn);
 }
 
 }  // namespace

@@ -12,6 +12,7 @@
 #include <stdio.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "quant_block.cuh"
 
 namespace mmq {
@@ -27,6 +28,9 @@ k_quantize_q8_1(const float* __restrict__ x, uint8_t* __restrict__ y, long long 
     const int part = lane & 3;   // which 8 values of the block
     const long long warp = ((long long)blockIdx.x * QUANT_THREADS + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * QUANT_THREADS) >> 5;
+    // programmatic dependent: x may be the previous kernel's output
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
 
     for (long long base = warp * BLOCKS_PER_WARP; base < nblk; base += nwarps * BLOCKS_PER_WARP) {
         const long long g = base + sub;
@@ -63,9 +67,10 @@ int quantize_launch(const float* x, int64_t M, int64_t K, void* xq, cudaStream_t
     if (grid > cap) grid = cap;
     {
         ProfScope ps("k_quantize_q8_1", s);
-        k_quantize_q8_1<<<(unsigned)grid, QUANT_THREADS, 0, s>>>(x, static_cast<uint8_t*>(xq), nblk);
+        return pdl_status(launch_pdl(k_quantize_q8_1, dim3((unsigned)grid), dim3(QUANT_THREADS), 0, s, x,
+                                     static_cast<uint8_t*>(xq), nblk),
+                          "mmq_quantize_q8_1");
     }
-    return launch_status("mmq_quantize_q8_1");
 }
 
 }  // namespace mmq

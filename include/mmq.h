@@ -34,6 +34,12 @@
  *    ignored: a call that returns MMQ_OK has enqueued the complete computation.
  *  - Device-side bounded waits (pipeline barriers) that run out set a sticky device
  *    error word instead of hanging; mmq_get_device_error() reads and clears it.
+ *  - The quantize kernel and the small-M contraction kernels are launched as programmatic
+ *    dependents of the previous kernel on the stream (CUDA programmatic dependent launch):
+ *    when that kernel allows it, they are scheduled while it drains.  They read the
+ *    activations and write any output only after it has completed, but the small-M
+ *    kernels start reading the WEIGHTS before: weights must not be written by a kernel
+ *    that allows its dependents to start early (no kernel of this library writes them).
  *  - Shapes: 1 <= M, N and K a positive multiple of 32 (q8_1, Q8_0) or of 256 (Q4_K,
  *    Q5_K, Q6_K);
  *    all of M*K, N*K and M*N below 2^40.
