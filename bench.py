@@ -668,6 +668,8 @@ def run_sweep(args):
         cases += [(fmt, M, 3584, 18944, "down") for M in (1, 2, 4, 8)]
     for fmt in ("q5_k", "q6_k"):  # on the expanded path
         cases += [(fmt, M, 3584, 3584, "q") for M in (512, 2048)]
+    for fmt in ("q4_k", "q8_0"):  # a few tens of rows
+        cases += [(fmt, M, 18944, 3584, "gate") for M in (16, 32, 64)]
     if args.only:  # one case, "fmt:M:N:K" (for profiling a single kernel)
         f, m, n, k = args.only.split(":")
         cases = [c for c in cases if c[:4] == (f, int(m), int(n), int(k))]

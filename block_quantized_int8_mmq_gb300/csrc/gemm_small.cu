@@ -787,11 +787,13 @@ int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_
 }
 
 // Two slots and four CTAs per SM (more warps to hide the math) for one activation row;
-// four slots and two CTAs per SM for two (measured best for each).
+// four slots and two CTAs per SM for two, and for Q6_K's one row (measured best for each).
 template <int FMT>
 int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                        int32_t* dots, cudaStream_t s, const char* fn) {
-    if (M <= 1) return launch_dp4a_stream_s<FMT, 1, 2>(x8, w8, M, N, nb, out, dots, s, fn);
+    if (M <= 1)  // Q6_K's slower math keeps more pieces in flight per warp
+        return FMT == FMT_Q6_K ? launch_dp4a_stream_s<FMT, 1, 4>(x8, w8, M, N, nb, out, dots, s, fn)
+                               : launch_dp4a_stream_s<FMT, 1, 2>(x8, w8, M, N, nb, out, dots, s, fn);
     if (M <= 2) return launch_dp4a_stream_s<FMT, 2, 4>(x8, w8, M, N, nb, out, dots, s, fn);
     return launch_dp4a_stream_s<FMT, 4, 4>(x8, w8, M, N, nb, out, dots, s, fn);
 }

@@ -180,6 +180,35 @@ def test_few_row_stream_parity_and_dots(mmq, fmt):
     assert mmq.mmq_get_device_error() == 0
 
 
+# three to a hundred rows on the small path (the int8 tensor-core stream, 8 rows per pass):
+# passes with rows past M, weight tiles with rows past N, one to hundreds of tiles
+TCS_SHAPES = [(3, 1, 256), (16, 129, 768), (17, 300, 2304), (32, 128, 512), (33, 3584, 256), (64, 200, 3584),
+              (100, 1000, 1024), (5, 18944, 512)]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
+def test_tens_of_rows_small_path_parity_and_dots(mmq, fmt):
+    set_path(mmq, "small")
+    for (M, N, K) in TCS_SHAPES:
+        x = synth.activations(M * 11 + N, M, K, True)
+        w = synth.weights(fmt, N * 5 + K, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        xq_ref = oracle.quantize_q8_1(x)
+        out = torch.full((M, N), float("nan"), device="cuda")
+        mmq.gemm(fmt, xq, dev(w), M, N, K, out=out)
+        o = out.cpu().numpy()
+        assert not np.isnan(o).any(), f"{fmt} {M}x{N}x{K}: output not fully written"
+        ref, norm = oracle.gemm(fmt, xq_ref, w, M, N, K)
+        check_close(o, ref, norm, f"{fmt} small {M}x{N}x{K}")
+        again = mmq.gemm(fmt, xq, dev(w), M, N, K)
+        assert torch.equal(again, out), f"{fmt} {M}x{N}x{K}: repeat differs"
+        if M * N * K <= 64 * 1000 * 3584:
+            dots = mmq.block_dots(fmt, xq, dev(w), M, N, K)
+            assert np.array_equal(dots.cpu().numpy(), oracle.block_dots(fmt, xq_ref, w, M, N, K)), \
+                f"{fmt} small dots {M}x{N}x{K}"
+    assert mmq.mmq_get_device_error() == 0
+
+
 # quantize + contraction in one call: on the expanded path the quantize is fused into the
 # activation expansion.  xq must hold the q8_1 bytes of x and out must equal the separate
 # quantize + gemm calls on the same path bit for bit (same kernels downstream of the
