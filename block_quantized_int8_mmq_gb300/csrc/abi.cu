@@ -53,18 +53,19 @@ constexpr int64_t LIMIT = (int64_t)1 << 40;
 constexpr int SM_COUNT = 152;  // GB300
 
 // Path choice for MMQ_PATH_AUTO from two measured cost models (GB300, microseconds):
-// the warp-level kernel streams the weights once per 8 activation rows; the expanded
-// tensor-core path pays the code expansion (about 3 bytes of traffic per weight byte)
-// plus, per wave of 128 x 128 tiles over the SMs, one tile's pass over K (~0.34 us per
-// 32-block; Q4_K adds one min item per 8 blocks).  The converter kernel is never the
+// the small-M streams take the weights once per pass of 8 activation rows (Q6_K: 4) at
+// about 4.2 (Q6_K: 2.7) million weight values per microsecond; the expanded tensor-core
+// path pays the code expansion (about 3 bytes of traffic per weight byte) plus, per wave
+// of 128 x 128 tiles over the SMs, one tile's pass over K (~0.34 us per 32-block; the
+// K-quants with mins add one min item per 8 blocks).  The converter kernel is never the
 // faster of the two and is only used when asked for.
 int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
     if (M <= 8 || K % QK_K != 0 || !tc_available()) return MMQ_PATH_SMALL;
     const double wbytes = (double)N * (double)mmq_weight_row_bytes(fmt, K);
-    // Q6_K's small-M stream takes 4 rows per pass, and its expansion writes two fp16
-    // planes (4 bytes per value against 0.82 read)
+    // Q6_K's expansion writes two fp16 planes (4 bytes per value against 0.82 read)
     const bool q6 = fmt == FMT_Q6_K;
-    const double t_small = (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * wbytes / 1.3e6 + 3.0;
+    const double t_small =
+        (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * (double)N * (double)K / (q6 ? 2.7e6 : 4.2e6) + 1.5;
     const double tiles = (double)((M + 127) / 128) * (double)((N + 127) / 128);
     const double waves = (double)(int64_t)((tiles + SM_COUNT - 1) / SM_COUNT);
     const double items = (double)(K / QK) * (is_kquant(fmt) ? 9.0 / 8.0 : 1.0);
