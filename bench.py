@@ -583,6 +583,84 @@ def run_layer(args):
             "gpu_launches": reps * L * per_layer, "clocks": clk}
 
 
+def run_decode(args):
+    """One-token decode through 28 7B layers (q, k, v, o, gate, up, down per layer), for each
+    weight format: each projection input quantized once by the fused call of its first
+    projection, the 28 layers captured in one CUDA graph.  Weights are per-layer device
+    copies (3.7 to 6.9 GB per format), so nothing is served from L2; the roofline is the
+    weight bytes per token over the measured HBM bandwidth."""
+    import torch
+    import block_quantized_int8_mmq_gb300 as mmq
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    M, H, F = 1, 3584, 18944
+    L = synth.LAYERS_7B
+    stream = torch.cuda.current_stream(dev)
+    acts = [torch.from_numpy(synth.layer_activations(0, M, K, i)).to(dev) for i, K in enumerate((H, H, H, F))]
+    xq_h = torch.empty((M, H // 32 * 36), dtype=torch.uint8, device=dev)
+    xq_f = torch.empty((M, F // 32 * 36), dtype=torch.uint8, device=dev)
+    outs = {name: torch.empty((M, N), device=dev) for (name, N, K) in synth.LAYER_7B}
+    lines = []
+    for fmt in ("q4_k", "q5_k", "q6_k", "q8_0"):
+        w0 = {name: torch.from_numpy(synth.layer_weights(0, name, N, K) if fmt == "q4_k" else
+                                     synth.weights(fmt, synth.substream(synth.BASE_SEED + 7, N + K), N, K)).to(dev)
+              for (name, N, K) in synth.LAYER_7B}
+        w_dev = [w0] + [{name: t.clone() for name, t in w0.items()} for _ in range(L - 1)]
+        wbytes = sum(t.numel() for t in w0.values()) * L
+
+        def layer(l, s):
+            w = w_dev[l]
+            for i, names in enumerate((("q", "k", "v"), ("o",), ("gate", "up"), ("down",))):
+                K = F if i == 3 else H
+                xq = xq_f if i == 3 else xq_h
+                mmq.mmq_linear(acts[i], w[names[0]], fmt, outs[names[0]].shape[1], xq=xq, out=outs[names[0]], stream=s)
+                for name in names[1:]:
+                    mmq.gemm(fmt, xq, w[name], M, outs[name].shape[1], K, outs[name], s)
+
+        for l in range(min(L, args.warmup)):
+            layer(l, stream)
+        torch.cuda.synchronize(dev)
+        assert mmq.mmq_get_device_error(stream) == 0
+        mmq.mmq_profile_read(reset=True)
+        prev = mmq.mmq_profile_enable(True)
+        layer(0, stream)
+        mmq.mmq_profile_enable(prev)
+        per_layer = sum(n for n, _ in mmq.mmq_profile_read(reset=True).values())
+        prev = mmq.mmq_profile_enable(False)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for l in range(L):
+                layer(l, cap)
+        mmq.mmq_profile_enable(prev)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(3, args.steps if args.steps > 0 else 50)
+        clocks = ClockSampler(0)
+        clocks.start()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        assert mmq.mmq_get_device_error(stream) == 0
+        ms = a.elapsed_time(b) / reps
+        gbs = wbytes / (ms / 1e3) / 1e9
+        lines.append({"fmt": fmt, "ms_per_token": ms, "tok_per_s": 1e3 / ms, "weight_bytes_per_token": wbytes,
+                      "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "launches_per_token": L * per_layer,
+                      "clocks": clk})
+        del w_dev, w0, graph
+        torch.cuda.empty_cache()
+    return {"metric": "7B one-token decode (28 layers of q, k, v, o, gate, up, down projections)", "unit": "mixed",
+            "lines": lines, "data": "synthetic (seeded, weights cloned per layer)", "peaks": peaks,
+            "config": {"workload": "7B GQA layer x28 at M=1 per weight format (attention, norms, SiLU excluded)",
+                       "timing": "28 layers in one CUDA graph, replayed back to back; each projection input "
+                                 "quantized once, fused into its first projection"}}
+
+
 def run_moe(args):
     """Expert-grouped contraction at a mixture-of-experts prefill shape: 2048 tokens, top-8
     of 128 experts (seeded, uniform: each token picks 8 distinct experts), expert matrices
@@ -733,7 +811,7 @@ def main():
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s of device time)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["layer", "sweep", "moe"], default="c1")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["layer", "sweep", "moe", "decode"], default="c1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per reference-arm step")
@@ -744,16 +822,16 @@ def main():
     rank, world, local = dist_env()
 
     if args.impl == "reference":
-        if args.workload in ("layer", "sweep", "moe"):
+        if args.workload in ("layer", "sweep", "moe", "decode"):
             args.workload = "c3" if args.workload == "layer" else "c1"
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args)), flush=True)
         return 0
 
-    if args.workload in ("layer", "sweep", "moe"):
+    if args.workload in ("layer", "sweep", "moe", "decode"):
         if rank == 0:
-            fn = {"layer": run_layer, "sweep": run_sweep, "moe": run_moe}[args.workload]
+            fn = {"layer": run_layer, "sweep": run_sweep, "moe": run_moe, "decode": run_decode}[args.workload]
             print(json.dumps(fn(args)), flush=True)
         return 0
     if world > 1:
