@@ -24,7 +24,7 @@ EXPORTED = (
     "mmq_set_path", "mmq_last_path", "mmq_get_device_error", "mmq_profile_enable", "mmq_profile_read",
     "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k",
     "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
-    "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k",
+    "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k", "mmq_gemm_grouped_q5_k",
 )
 
 
@@ -59,7 +59,7 @@ def _load():
     L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
     for f in ("mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_linear_q5_k", "mmq_linear_q6_k"):
         getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
-    for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k"):
+    for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k", "mmq_gemm_grouped_q5_k"):
         getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
@@ -226,7 +226,7 @@ def mmq_gemm_grouped(fmt: str, xq, row_expert, wq, E: int, N: int, K: int, out=N
     R = xq.shape[0]
     if out is None:
         out = torch.empty((R, N), dtype=torch.float32, device=xq.device)
-    fn = "mmq_gemm_grouped_q8_0" if fmt == "q8_0" else "mmq_gemm_grouped_q4_k"
+    fn = "mmq_gemm_grouped_" + fmt
     _check(fn, getattr(_lib, fn)(_ptr(xq), _ptr(row_expert), R, _ptr(wq), E, N, K, _ptr(out), _stream(stream)))
     return out
 

@@ -284,6 +284,11 @@ int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, 
     return grouped("mmq_gemm_grouped_q4_k", FMT_Q4_K, xq, row_expert, R, wq, E, N, K, out, stream);
 }
 
+int mmq_gemm_grouped_q5_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream) {
+    return grouped("mmq_gemm_grouped_q5_k", FMT_Q5_K, xq, row_expert, R, wq, E, N, K, out, stream);
+}
+
 int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,
                               void* stream) {
     return contraction("mmq_debug_block_dots_q8_0", FMT_Q8_0, xq, wq, M, N, K, nullptr, dots, stream);

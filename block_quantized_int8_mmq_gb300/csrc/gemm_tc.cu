@@ -8,30 +8,31 @@
 // in register, with no shared-memory round trip of the accumulator).
 //
 // sm_103a has no integer tcgen05 MMA kind, and its int8 mma.sync rate is ~1/12 of the
-// fp16 tensor rate.  Every int8 code (and every Q4_K nibble times its 6-bit sub-scale,
+// fp16 tensor rate.  Every int8 code (and every K-quant code times its 6-bit sub-scale,
 // at most 945) is an exact fp16 value, each product is an integer below 2^17 and every
 // partial sum of a 32-term block dot an integer below 2^22, so an fp16 x fp16 -> f32
 // MMA over one block computes the block dot exactly.
 //
 // The scale of block b is the outer product S_b = xd[:,b] (x) w[:,b] of two vectors of
-// exact f16 values (Q8_0: w = wd; Q4_K: w = d of the super-block, the sub-scale sc_j
+// exact f16 values (Q8_0: w = wd; Q4_K, Q5_K: w = d of the super-block, the sub-scale sc_j
 // being folded into the weight codes).  A second, K=16 MMA whose operands carry xd and
 // w in column 0 (zeros elsewhere) writes S_b exactly into TMEM next to D_b, so the
-// epilogue is acc += S_b * D_b: one FMA per element, no scale reads.  The Q4_K min term
+// epilogue is acc += S_b * D_b: one FMA per element, no scale reads.  The K-quant min term
 // sum_j -dmin*m_j*xs_j of a super-block becomes a ninth item with D = sum_j xs_j*m_j
 // (K=16 MMA of the f16 sums s against the 6-bit mins) and S = 1 (x) (-dmin)
 // ("When Does a Kernel Win Surface?", sec. "Kept levers: Vulkan", affine identity).
 //
 // Warp roles (one 128 x 128 output tile per CTA, 832 threads):
 //   warp 0     TMA producer: raw q8_1 rows (288 B per 256 values) and raw weight rows
-//              (Q8_0: 272 B, Q4_K: one 144 B super-block) for a 256-value k-tile, as
+//              (Q8_0: 272 B, Q4_K / Q5_K: one 144 / 176 B super-block) for a 256-value k-tile, as
 //              2-D tensor copies into a 2-stage ring ("13 . r7-r8 raw-byte MMQ
 //              kernel", sec. 2: shared memory holds raw quant bytes; sec. 3.1: whole
 //              super-blocks, out-of-range rows zero-filled by the copy engine).
 //   warp 1     TMEM owner and MMA issuer: per item, D (two K=16 MMAs; one for a min
 //              item) and S (one K=16 MMA) into one of two TMEM slots, then commits.
 //   warps 2-9  converters: codes -> exact fp16 (sign-biased byte permute and one half2
-//              subtract; Q4_K: half2 fused multiply by sc_j) in the canonical K-major
+//              subtract; Q4_K: half2 fused multiply by sc_j; Q5_K: the fifth bit OR'd in, exact
+//              conversion, then a multiply by sc_j) in the canonical K-major
 //              no-swizzle UMMA layout, bank-conflict-free; the f16 scale vectors into
 //              column 0 of the scale operands.
 //   warps 10-25 epilogue, 32 rows x 32 columns each: per item, 16x256b TMEM fragments of
@@ -75,10 +76,10 @@ constexpr int SLOT = 2 * OP_MAIN + 2 * OP_AUX;
 static_assert(BM + BN == 32 * CONV_WARPS, "one scale row (activation or weight) per converter thread");
 static_assert(EPI_COLS == 32, "one 16x256b.x4 fragment covers 32 columns");
 
-__host__ __device__ constexpr int b_row(int fmt) { return fmt == FMT_Q8_0 ? KT_BLOCKS * Q8_0_BYTES : Q4_K_BYTES; }
-// items per k-tile: 8 blocks, plus the min item of the super-block for Q4_K
+__host__ __device__ constexpr int b_row(int fmt) { return fmt == FMT_Q8_0 ? KT_BLOCKS * Q8_0_BYTES : kq_bytes(fmt); }
+// items per k-tile: 8 blocks, plus the min item of the super-block for Q4_K and Q5_K
 __host__ __device__ constexpr int items_per_kt(int fmt, bool dots) {
-    return KT_BLOCKS + (fmt == FMT_Q4_K && !dots ? 1 : 0);
+    return KT_BLOCKS + (is_kquant(fmt) && !dots ? 1 : 0);
 }
 
 // barrier indices: raw stages, operand slots (converters -> MMA -> converters), TMEM
@@ -92,12 +93,13 @@ struct Layout {
     static constexpr int rawA = 0;
     static constexpr int rawB = rawA + RS * BM * A_ROW;
     static constexpr int slots = rawB + RS * BN * b_row(FMT);
-    static constexpr int sctab = slots + FS * SLOT;  // Q4_K: per converter warp, (sc, -1024 sc) of its 64 rows x 8
-    static constexpr int bars = sctab + (FMT == FMT_Q4_K ? CONV_WARPS * 32 * 8 * 4 : 0);
+    static constexpr int sctab = slots + FS * SLOT;  // K-quants: per converter warp, sub-scale pairs of its 64 rows x 8
+    static constexpr int bars = sctab + (is_kquant(FMT) ? CONV_WARPS * 32 * 8 * 4 : 0);
     static constexpr int tmem_slot = bars + NBARS * 8;
     static constexpr int total = tmem_slot + 16;
     static constexpr int alloc = total + 1024;  // slack to align the base to 1 KiB
     static_assert(rawB % 1024 == 0 && slots % 1024 == 0 && SLOT % 1024 == 0, "alignment");
+    static_assert(alloc <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -121,7 +123,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     using L = Layout<FMT>;
     constexpr int BROW = b_row(FMT);
     constexpr int IPK = items_per_kt(FMT, DOTS);
-    constexpr bool FOLD = FMT == FMT_Q4_K && !DOTS;  // sc_j folded into the weight codes
+    constexpr bool FOLD = is_kquant(FMT) && !DOTS;  // sc_j folded into the weight codes
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -237,8 +239,8 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             if (!ok) break;
             const uint8_t* rA = smem + L::rawA + s * BM * A_ROW;
             const uint8_t* rB = smem + L::rawB + s * BN * BROW;
-            uint4 whdr = make_uint4(0u, 0u, 0u, 0u);  // Q4_K: super-block header of weight row srow
-            if (FMT == FMT_Q4_K) {
+            uint4 whdr = make_uint4(0u, 0u, 0u, 0u);  // K-quants: super-block header of weight row srow
+            if (is_kquant(FMT)) {
                 if (!arow) whdr = *reinterpret_cast<const uint4*>(rB + srow * BROW);
                 if (FOLD) {
                     __syncwarp();  // this warp's reads of the previous k-tile's table are done
@@ -248,7 +250,10 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                     for (int j = 0; j < 8; ++j) {
                         int s6, m6;
                         q4_k_scale_min(h.y, h.z, h.w, j, s6, m6);
-                        sct[lane * 8 + j] = h2_bits(__halves2half2(__int2half_rn(s6), __int2half_rn(-1024 * s6)));
+                        // Q4_K: (sc, -1024 sc) for one fused (1024 + q) * sc - 1024 sc; Q5_K: (sc, sc),
+                        // its 5-bit codes converted exactly first ((1024 + q) * sc would overflow)
+                        sct[lane * 8 + j] = h2_bits(__halves2half2(
+                            __int2half_rn(s6), __int2half_rn(FMT == FMT_Q5_K ? s6 : -1024 * s6)));
                     }
                     __syncwarp();
                 }
@@ -284,8 +289,12 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                             wv[i] = __funnelshift_r(lo, hi, sh);
                         } else {
                             const uint32_t raw =
-                                *reinterpret_cast<const uint32_t*>(rB + r * BROW + 16 + 32 * (j >> 1) + w * 4);
+                                *reinterpret_cast<const uint32_t*>(rB + r * BROW + kq_qs_off(FMT) + 32 * (j >> 1) + w * 4);
                             wv[i] = (j & 1) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
+                            if (FMT == FMT_Q5_K) {  // fifth bit of values 4w .. 4w + 3: bit j of high-bit bytes
+                                const uint32_t qh = *reinterpret_cast<const uint32_t*>(rB + r * BROW + 16 + w * 4);
+                                wv[i] |= ((qh >> j) & 0x01010101u) << 4;
+                            }
                             if (FOLD) scv[i] = sct[(i * 8 + r8) * 8 + j];  // table row 8i + r8 is row 8g + r8
                         }
                     }
@@ -296,7 +305,7 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                     else
                         scol = (uint16_t)(whdr.x & 0xffffu);                                            // d
                 } else {
-                    // Q4_K min item: A row m = (s of the 8 blocks, 0 x 8), B row n = (m_0..m_7,
+                    // K-quant min item: A row m = (s of the 8 blocks, 0 x 8), B row n = (m_0..m_7,
                     // 0 x 8); scale operands: A = 1, B = -dmin
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -328,7 +337,12 @@ k_mmq_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                         *reinterpret_cast<uint2*>(oA + dst) = i8x4_to_f16x4(xa[i]);
                         if (FMT == FMT_Q8_0)
                             *reinterpret_cast<uint2*>(oB + dst) = i8x4_to_f16x4(wv[i]);
-                        else if (FOLD)
+                        else if (FOLD && FMT == FMT_Q5_K) {
+                            const uint2 c = u4x4_scaled_f16x4(wv[i], __float2half2_rn(1.f), __float2half2_rn(-1024.f));
+                            const __half2 sc2 = __low2half2(bits_h2(scv[i]));
+                            *reinterpret_cast<uint2*>(oB + dst) =
+                                make_uint2(h2_bits(__hmul2(bits_h2(c.x), sc2)), h2_bits(__hmul2(bits_h2(c.y), sc2)));
+                        } else if (FOLD)
                             *reinterpret_cast<uint2*>(oB + dst) = u4x4_scaled_f16x4(
                                 wv[i], __low2half2(bits_h2(scv[i])), __high2half2(bits_h2(scv[i])));
                         else
@@ -373,7 +387,7 @@ int launch_t(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
     const int nb = (int)(K / QK);
     CUtensorMap ta, tb;
     if (!make_map(&ta, xq, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, A_ROW, BM) ||
-        !make_map(&tb, wq, (uint64_t)(FMT == FMT_Q8_0 ? nb * Q8_0_BYTES : nb / 8 * Q4_K_BYTES), (uint64_t)N,
+        !make_map(&tb, wq, (uint64_t)(FMT == FMT_Q8_0 ? nb * Q8_0_BYTES : nb / 8 * kq_bytes(FMT)), (uint64_t)N,
                   b_row(FMT), BN)) {
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
@@ -408,7 +422,7 @@ int launch_grouped_t(const void* xs, const void* wq, int64_t R, int64_t E, int64
     const int nb = (int)(K / QK);
     CUtensorMap ta, tb;
     if (!make_map(&ta, xs, (uint64_t)nb * Q8_1_BYTES, (uint64_t)R, A_ROW, BM) ||
-        !make_map(&tb, wq, (uint64_t)(FMT == FMT_Q8_0 ? nb * Q8_0_BYTES : nb / 8 * Q4_K_BYTES), (uint64_t)(E * N),
+        !make_map(&tb, wq, (uint64_t)(FMT == FMT_Q8_0 ? nb * Q8_0_BYTES : nb / 8 * kq_bytes(FMT)), (uint64_t)(E * N),
                   b_row(FMT), BN)) {
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
@@ -438,11 +452,13 @@ int launch_grouped_t(const void* xs, const void* wq, int64_t R, int64_t E, int64
 int tc_grouped_launch(int fmt, const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
                       const int2* tiles, const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map,
                       float* out, cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_grouped_q8_0" : "mmq_gemm_grouped_q4_k";
-    return fmt == FMT_Q8_0 ? launch_grouped_t<FMT_Q8_0>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map,
-                                                        out, s, fn)
-                           : launch_grouped_t<FMT_Q4_K>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map,
-                                                        out, s, fn);
+    const char* fn = fmt == FMT_Q8_0   ? "mmq_gemm_grouped_q8_0"
+                     : fmt == FMT_Q5_K ? "mmq_gemm_grouped_q5_k" : "mmq_gemm_grouped_q4_k";
+    if (fmt == FMT_Q8_0)
+        return launch_grouped_t<FMT_Q8_0>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map, out, s, fn);
+    if (fmt == FMT_Q5_K)
+        return launch_grouped_t<FMT_Q5_K>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map, out, s, fn);
+    return launch_grouped_t<FMT_Q4_K>(xs, wq, R, E, N, K, tiles, ntiles, max_tiles, row_end, row_map, out, s, fn);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -483,9 +499,8 @@ int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int
                      : fmt == FMT_Q5_K ? (dots ? "mmq_debug_block_dots_q5_k" : "mmq_gemm_q5_k")
                      : fmt == FMT_Q6_K ? (dots ? "mmq_debug_block_dots_q6_k" : "mmq_gemm_q6_k")
                                        : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
-    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K) {
-        report(fn, MMQ_ERR_ARG,
-               "the converter tensor-core kernel takes Q8_0 and Q4_K (Q5_K and Q6_K: the expanded path)");
+    if (fmt == FMT_Q6_K) {  // its 210-byte rows are not 16-byte strided: no 2-D tensor copies
+        report(fn, MMQ_ERR_ARG, "the converter tensor-core kernel takes Q8_0, Q4_K and Q5_K (Q6_K: the expanded path)");
         return MMQ_ERR_ARG;
     }
     if (K % QK_K != 0) {
@@ -499,6 +514,9 @@ int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int
     if (fmt == FMT_Q8_0)
         return dots ? launch_t<FMT_Q8_0, true>(xq, wq, M, N, K, out, dots, s, fn)
                     : launch_t<FMT_Q8_0, false>(xq, wq, M, N, K, out, dots, s, fn);
+    if (fmt == FMT_Q5_K)
+        return dots ? launch_t<FMT_Q5_K, true>(xq, wq, M, N, K, out, dots, s, fn)
+                    : launch_t<FMT_Q5_K, false>(xq, wq, M, N, K, out, dots, s, fn);
     return dots ? launch_t<FMT_Q4_K, true>(xq, wq, M, N, K, out, dots, s, fn)
                 : launch_t<FMT_Q4_K, false>(xq, wq, M, N, K, out, dots, s, fn);
 }

@@ -100,7 +100,8 @@ __global__ void k_group_scatter(const uint8_t* __restrict__ xq, const int32_t* _
 
 int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
                    int64_t K, float* out, cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0 ? "mmq_gemm_grouped_q8_0" : "mmq_gemm_grouped_q4_k";
+    const char* fn = fmt == FMT_Q8_0   ? "mmq_gemm_grouped_q8_0"
+                     : fmt == FMT_Q5_K ? "mmq_gemm_grouped_q5_k" : "mmq_gemm_grouped_q4_k";
     const int64_t nb = K / QK, row_bytes = nb * Q8_1_BYTES;
     const int64_t max_tiles = (R + GT - 1) / GT + (E < R ? E : R);  // each expert adds at most one partial tile
     if (max_tiles > 65535) {

@@ -144,8 +144,7 @@ int mmq_gemm_q4_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
 /*
  * out = xq (q8_1) contracted with Q5_K weights wq ([N][K/256] super-blocks of 176 B),
  * including the -dmin*m_j*s min term of every sub-block; as mmq_gemm_q4_k otherwise
- * (K % 256 == 0).  Runs on the expanded-code tensor-core path and the small-M streams; the
- * converter kernel (MMQ_PATH_TC) refuses it with MMQ_ERR_ARG.
+ * (K % 256 == 0).  Runs on every path.
  */
 int mmq_gemm_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                   void* stream);
@@ -193,9 +192,9 @@ int mmq_linear_q6_k(const float* x, int64_t M, int64_t K, const void* wq, int64_
  * The grouping runs on the device (no host round trip; capturable).
  *   xq: q8_1 [R][K/32] blocks, 16-byte aligned.  row_expert: int32 [R], 4-byte aligned.
  *   wq: E weight matrices stacked expert-major, expert e at row e*N ([E*N][K/32] Q8_0
- *   blocks or [E*N][K/256] Q4_K super-blocks), 16-byte aligned.  out: f32 [R][N], 16-byte
+ *   blocks or [E*N][K/256] Q4_K / Q5_K super-blocks), 16-byte aligned.  out: f32 [R][N], 16-byte
  *   aligned, fully overwritten; a row whose expert id is outside [0, E) gets zeros.
- * Accuracy as mmq_gemm_q8_0 / mmq_gemm_q4_k, per row.  Needs K % 256 == 0 and
+ * Accuracy as mmq_gemm_q8_0 / mmq_gemm_q4_k / mmq_gemm_q5_k, per row.  Needs K % 256 == 0 and
  * R / 128 + min(E, R) <= 65535.  Scratch about R*K*1.125 bytes (stream-ordered, as the
  * expanded path).
  * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE, MMQ_ERR_NULL, MMQ_ERR_ALIGN, MMQ_ERR_SMEM,
@@ -204,6 +203,8 @@ int mmq_linear_q6_k(const float* x, int64_t M, int64_t K, const void* wq, int64_
 int mmq_gemm_grouped_q8_0(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
                           int64_t K, float* out, void* stream);
 int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream);
+int mmq_gemm_grouped_q5_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
                           int64_t K, float* out, void* stream);
 
 /*

@@ -101,7 +101,7 @@ SMALL_SHAPES = {
 }
 SMALL_SHAPES["q5_k"] = SMALL_SHAPES["q6_k"] = SMALL_SHAPES["q4_k"]
 FMTS = ["q8_0", "q4_k", "q5_k", "q6_k"]
-NO_TC = ("q5_k", "q6_k")  # formats the converter kernel refuses
+NO_TC = ("q6_k",)  # formats the converter kernel refuses
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -316,7 +316,7 @@ def test_q5_k_extreme_codes_block_dots(mmq):
     w2[:, :, 4:16] = 0xFF
     w2[:, :, 16:] = np.where(np.arange(160) % 3 == 0, 0xFF, 0x00).astype(np.uint8)
     w2 = w2.reshape(N, -1)
-    for path in ("expand", "small"):
+    for path in ("expand", "small", "tc"):
         set_path(mmq, path)
         dots = mmq.mmq_debug_block_dots_q5_k(xq, dev(w2), M, N, K)
         assert np.array_equal(dots.cpu().numpy(), oracle.block_dots("q5_k", oracle.quantize_q8_1(x), w2, M, N, K))
@@ -431,7 +431,7 @@ def test_q6_k_extreme_codes_block_dots(mmq):
 
 @pytest.mark.parametrize("M,N,K", [(1, 18944, 3584), (1, 3584, 18944), (4, 18944, 3584), (8, 3584, 18944),
                                    (512, 3584, 3584), (2048, 18944, 3584)])
-@pytest.mark.parametrize("fmt", NO_TC)
+@pytest.mark.parametrize("fmt", ["q5_k", "q6_k"])
 def test_k_quant_full_size_sampled_parity(mmq, fmt, M, N, K):
     """Q5_K and Q6_K at the 7B-class projection sizes: the small-M streams and the expanded path."""
     set_path(mmq, "auto")
@@ -598,7 +598,7 @@ GROUPED_CASES = [  # (R, E, N, K, routing)
 ]
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
 @pytest.mark.parametrize("case", range(len(GROUPED_CASES)))
 def test_grouped_parity(mmq, fmt, case):
     R, E, N, K, routing = GROUPED_CASES[case]
