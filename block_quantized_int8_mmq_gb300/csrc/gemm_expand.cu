@@ -121,9 +121,9 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
     if (FROM_X) {
         // 32 rows x 8 blocks, four lanes per block: a warp quantizes the 8 blocks (1 KiB of
-        // x) of one row per pass; the loads of four passes are issued before their math
+        // x) of one row per pass; the loads of two passes are issued before their math
         constexpr int PASSES = EXP_ROWS * GB / (EXP_THREADS / 4);  // 8
-        constexpr int BATCH = 4;
+        constexpr int BATCH = 2;
         const int part = threadIdx.x & 3;
 #pragma unroll
         for (int p0 = 0; p0 < PASSES; p0 += BATCH) {
@@ -406,7 +406,7 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
 // the rest the weights; grid y = the 256-value group.  The two halves are independent, so
 // they run side by side instead of one after the other.
 template <int FMT, bool FROM_X, bool FOLD>
-__global__ void __launch_bounds__(EXP_THREADS)
+__global__ void __launch_bounds__(EXP_THREADS, 12)
 k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
          const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
          uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
