@@ -55,40 +55,39 @@ constexpr int BN = 128;                  // weight rows per tile (MMA N)
 constexpr int GB = 8;                    // 32-blocks per group (256 values)
 constexpr int CHUNK = BM * QK * 2;       // fp16 codes of one block, 128 rows: 8 KiB
 constexpr int TILE16 = BM * 16 * 2;      // a K = 16 operand, 128 rows: 4 KiB
-constexpr int NSTAGE = 8;                // blocks in flight (one block per stage)
+constexpr int NSTAGE = 8;                // blocks in flight (one block per stage; Q6_K: 6)
+// activation bytes per (tile, block): the fp16 codes, then AS_b, the K = 16 scale operand of
+// the block (column b % 8 = xd of the block, the other columns 0)
+constexpr int XCHUNK = CHUNK + TILE16;
 // weight bytes per (tile, block): one chunk of codes, or for Q6_K two planes whose sum is
 // the code times its sub-scale (see expand_weights_q6_k)
 __host__ __device__ constexpr int wchunk(int fmt) { return fmt == FMT_Q6_K ? 2 * CHUNK : CHUNK; }
-__host__ __device__ constexpr int stage_bytes(int fmt) { return CHUNK + wchunk(fmt); }  // activation chunk, then weights
+__host__ __device__ constexpr int stage_bytes(int fmt) { return XCHUNK + wchunk(fmt); }  // activations, then weights
+__host__ __device__ constexpr int nstage(int fmt) { return fmt == FMT_Q6_K ? 6 : NSTAGE; }
 constexpr int GR = 2;                    // group-data slots
 constexpr int NMMA = 2;                  // MMA-issuing warps; warp e issues items e, e + 2, ...
 constexpr int DS = NMMA;                 // TMEM slots: slot e (D and S of one item) belongs to issuer e
-constexpr int OH = 4;                    // one-hot scale operand slots
 constexpr int EPI_WARPS = 16;            // warps 0..15: epilogue
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // 32 columns per epilogue warp
-constexpr int WARP_LOAD = EPI_WARPS, WARP_MMA0 = EPI_WARPS + 1, WARP_ONEHOT = WARP_MMA0 + NMMA;
-constexpr int THREADS = (WARP_ONEHOT + 1) * 32;  // 640
-constexpr int TMEM_COLS = DS * 2 * BN;           // 512
+constexpr int WARP_LOAD = EPI_WARPS, WARP_MMA0 = EPI_WARPS + 1;
+constexpr int THREADS = (WARP_MMA0 + NMMA) * 32;  // 608
+constexpr int TMEM_COLS = DS * 2 * BN;            // 512
 constexpr int EXP_ROWS = 32;             // rows per expansion CTA (a quarter tile)
 constexpr int EXP_THREADS = 128;
-static_assert(OH % NMMA == 0, "each issuer sees its own one-hot slots");
 
-// Group data (scratch and shared memory).  Activation side: AS, the K = 16 operand whose
-// column c holds xd of block c (column 8: 1.0, the K-quant min item), and for K-quants
-// AM (column c = the f16 block sum s of block c).  Weight side: for K-quants BMIN (column
-// j = m_j), then WS, the f16 column scales [item][128] (Q8_0: wd; K-quants: d, and -dmin
-// for the min item).
+// Group data (scratch and shared memory), per 128-row tile and 256-value group.  Activation
+// side: for K-quants AM, the K = 16 operand of the min item (column c = the f16 block sum s
+// of block c).  Weight side: for K-quants BMIN (column j = m_j), then WS, the K = 16 operand
+// whose column c holds the column scales of item c (Q8_0: wd; K-quants and Q6_K: d; -dmin
+// for the min item, column 8).  The scale MMA of block item c multiplies AS_c (only column
+// c nonzero: xd) by WS, so S = xd_c (x) w_c exactly; the min item uses a constant AS whose
+// column 8 is 1.0.
 __host__ __device__ constexpr int xr(int fmt) { return is_kquant(fmt) ? GB + 1 : GB; }
-__host__ __device__ constexpr int ga_bytes(int fmt) { return is_kquant(fmt) ? 2 * TILE16 : TILE16; }
-__host__ __device__ constexpr int gw_bytes(int fmt) { return (is_kquant(fmt) ? TILE16 : 0) + xr(fmt) * BN * 2; }
-__host__ __device__ constexpr int am_off(int fmt) { return TILE16; }
-__host__ __device__ constexpr int bmin_off(int fmt) { return ga_bytes(fmt); }
+__host__ __device__ constexpr int ga_bytes(int fmt) { return is_kquant(fmt) ? TILE16 : 0; }
+__host__ __device__ constexpr int gw_bytes(int fmt) { return (is_kquant(fmt) ? TILE16 : 0) + TILE16; }
+__host__ __device__ constexpr int am_off(int fmt) { return 0; }
+__host__ __device__ constexpr int bmin_off(int fmt) { return ga_bytes(fmt); }  // in a group slot: GA, then GW
 __host__ __device__ constexpr int ws_off(int fmt) { return ga_bytes(fmt) + (is_kquant(fmt) ? TILE16 : 0); }
-
-// u16 index of (row r, column c) in a K = 16 K-major no-swizzle tile (8-row groups 256 B apart)
-__device__ __forceinline__ int tile16_idx(int r, int c) {
-    return ((r >> 3) * 256 + (c >> 3) * 128 + (r & 7) * 16) / 2 + (c & 7);
-}
 
 __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
     return make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16), v[4] | ((uint32_t)v[5] << 16),
@@ -169,7 +168,7 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
         }
     }
     __syncthreads();
-    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * CHUNK + h * (CHUNK / 4);
+    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * XCHUNK + h * (CHUNK / 4);
     constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
     for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
         const int j = i / PIECES, p = i % PIECES;
@@ -177,25 +176,31 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
         const uint8_t* src = sm + r * SROW + j * Q8_1_BYTES + 4 + 8 * kc;
         const uint2 lo = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src));
         const uint2 hi = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src + 4));
-        *reinterpret_cast<uint4*>(dst + (size_t)j * CHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        *reinterpret_cast<uint4*>(dst + (size_t)j * XCHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
-    // AS [, AM]: quarter piece t (0..63) = (row 8*(t/16) + t%8, columns 8*((t/8)%2) .. +7)
-    uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT) + h * (TILE16 / 4);
-    const int t = threadIdx.x & 63;
-    const bool second = threadIdx.x >= 64;  // threads 64..127 write AM (Q4_K)
-    if (second && !is_kquant(FMT)) return;
-    const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
-    uint16_t v[8];
-    if (kg == 0) {
+    // AS_j of each block (after its codes): quarter piece u (0..63) = (row 8*(u/16) + u%8,
+    // columns 8*((u/8)%2) .. +7); column j holds xd of block j, the others are 0
+    uint8_t* adst = xa + ((size_t)mt * nb + (size_t)g * GB) * XCHUNK + CHUNK + h * (TILE16 / 4);
+    for (int i = threadIdx.x; i < GB * 64; i += EXP_THREADS) {
+        const int j = i >> 6, u = i & 63;
+        const int r = 8 * (u >> 4) + (u & 7), kg = (u >> 3) & 1;
+        const uint16_t xd = *reinterpret_cast<const uint16_t*>(sm + r * SROW + j * Q8_1_BYTES);
+        uint16_t v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)  // columns 0..7: d (AS) or s (AM) of the eight blocks of the group
-            v[e] = *reinterpret_cast<const uint16_t*>(sm + r * SROW + e * Q8_1_BYTES + (second ? 2 : 0));
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)  // AS column 8: 1.0, the Q4_K min item's row scale
-            v[e] = (!second && e == 0 && is_kquant(FMT)) ? (uint16_t)0x3C00 : (uint16_t)0;
+        for (int e = 0; e < 8; ++e) v[e] = (kg == 0 && e == j) ? xd : (uint16_t)0;
+        *reinterpret_cast<uint4*>(adst + (size_t)j * XCHUNK + u * 16) = pack8(v);
     }
-    *reinterpret_cast<uint4*>(gdst + (second ? am_off(FMT) : 0) + t * 16) = pack8(v);
+    if (is_kquant(FMT) && threadIdx.x >= 64) {
+        // AM (group data): quarter piece u = t - 64, column c = s of block c of the group
+        uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT) + am_off(FMT) + h * (TILE16 / 4);
+        const int u = threadIdx.x - 64;
+        const int r = 8 * (u >> 4) + (u & 7), kg = (u >> 3) & 1;
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = kg == 0 ? *reinterpret_cast<const uint16_t*>(sm + r * SROW + e * Q8_1_BYTES + 2) : (uint16_t)0;
+        *reinterpret_cast<uint4*>(gdst + u * 16) = pack8(v);
+    }
 }
 
 // One CTA per (32-row quarter of a 128-row tile, 256-value group) of the weights.  FOLD:
@@ -276,19 +281,23 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
     }
     uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT);
     const int t = threadIdx.x;
-    // WS[c][r]: piece t = rows 32h + 8*(t%4) .. +7 of column c = t/4
-    if (t < xr(FMT) * EXP_ROWS / 8) {
-        const int c = t >> 2, r0 = (t & 3) * 8;
+    // WS (K = 16 operand): quarter piece t (0..63) = (row 8*(t/16) + t%8, columns
+    // 8*((t/8)%2) .. +7); column c = the scale of item c for that row
+    if (t < 64) {
+        const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
+        const uint16_t* hdr = reinterpret_cast<const uint16_t*>(sm + r * SROW);
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const uint16_t* hdr = reinterpret_cast<const uint16_t*>(sm + (r0 + e) * SROW);
-            if (FMT == FMT_Q8_0)
-                v[e] = *reinterpret_cast<const uint16_t*>(sm + (r0 + e) * SROW + c * Q8_0_BYTES);  // wd
+            const int c = 8 * kg + e;
+            if (c >= xr(FMT))
+                v[e] = 0;
+            else if (FMT == FMT_Q8_0)
+                v[e] = *reinterpret_cast<const uint16_t*>(sm + r * SROW + c * Q8_0_BYTES);  // wd
             else
                 v[e] = c < GB ? hdr[0] : (uint16_t)(hdr[1] ^ 0x8000u);  // d, or -dmin
         }
-        *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + (c * BN + h * EXP_ROWS + r0) * 2) = pack8(v);
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + h * (TILE16 / 4) + t * 16) = pack8(v);
     }
     if (is_kquant(FMT) && t >= 64) {
         // BMIN: quarter piece u = t - 64 (0..63) = (row 8*(u/16) + u%8, columns 8*((u/8)%2)
@@ -385,20 +394,18 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
         *reinterpret_cast<uint4*>(dst + (size_t)j * (2 * CHUNK) + p * 16) = p1;
         *reinterpret_cast<uint4*>(dst + (size_t)j * (2 * CHUNK) + CHUNK + p * 16) = p2;
     }
-    // WS[c][r] = d of the row's super-block for every block c: piece t = rows 32h + 8*(t%4)
-    // .. +7 of column c = t/4
+    // WS (K = 16 operand): quarter piece t (0..63) = (row 8*(t/16) + t%8, columns
+    // 8*((t/8)%2) .. +7); columns 0..7 = d of the row's super-block
     const int t = threadIdx.x;
-    if (t < GB * EXP_ROWS / 8) {
-        const int c = t >> 2, r0 = (t & 3) * 8;
+    if (t < 64) {
+        const int r = 8 * (t >> 4) + (t & 7), kg = (t >> 3) & 1;
+        const uint8_t* sb = sblk(r);
+        const uint16_t dd = (uint16_t)(sb[208] | (sb[209] << 8));
         uint16_t v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint8_t* sb = sblk(r0 + e);
-            v[e] = (uint16_t)(sb[208] | (sb[209] << 8));
-        }
+        for (int e = 0; e < 8; ++e) v[e] = kg == 0 ? dd : (uint16_t)0;
         uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT_Q6_K);
-        *reinterpret_cast<uint4*>(gdst + ws_off(FMT_Q6_K) - ga_bytes(FMT_Q6_K) + (c * BN + h * EXP_ROWS + r0) * 2) =
-            pack8(v);
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT_Q6_K) - ga_bytes(FMT_Q6_K) + h * (TILE16 / 4) + t * 16) = pack8(v);
     }
 }
 
@@ -426,17 +433,16 @@ k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t
 
 // ---------------------------------------------------------------- GEMM kernel
 constexpr int BAR_ST_FULL = 0, BAR_ST_EMPTY = BAR_ST_FULL + NSTAGE, BAR_G_FULL = BAR_ST_EMPTY + NSTAGE,
-              BAR_G_EMPTY = BAR_G_FULL + GR, BAR_OH_FULL = BAR_G_EMPTY + GR, BAR_OH_EMPTY = BAR_OH_FULL + OH,
-              BAR_D_FULL = BAR_OH_EMPTY + OH, BAR_D_EMPTY = BAR_D_FULL + DS, BAR_DRAIN = BAR_D_EMPTY + DS,
-              NBARS = BAR_DRAIN + NMMA;
+              BAR_G_EMPTY = BAR_G_FULL + GR, BAR_D_FULL = BAR_G_EMPTY + GR, BAR_D_EMPTY = BAR_D_FULL + DS,
+              BAR_DRAIN = BAR_D_EMPTY + DS, NBARS = BAR_DRAIN + NMMA;
 
 template <int FMT>
 struct XLayout {
     static constexpr int stages = 0;
     static constexpr int gslot = (ga_bytes(FMT) + gw_bytes(FMT) + 1023) & ~1023;
-    static constexpr int groups = stages + NSTAGE * stage_bytes(FMT);
-    static constexpr int onehot = groups + GR * gslot;
-    static constexpr int bars = onehot + OH * TILE16;
+    static constexpr int groups = stages + nstage(FMT) * stage_bytes(FMT);
+    static constexpr int asmin = groups + GR * gslot;  // the min item's constant AS (column 8 = 1.0)
+    static constexpr int bars = asmin + TILE16;
     static constexpr int tmem_slot = bars + NBARS * 8;
     static constexpr int total = tmem_slot + 16;
     static constexpr int alloc = total + 1024;  // slack to align the base to 1 KiB
@@ -446,10 +452,12 @@ struct XLayout {
 // Warps 0..15 own 32 rows each (their TMEM lane quarter, warp % 4) and 32 columns of
 // the 128 x 128 tile; warp 16 is the bulk-copy producer; warps 17 and 18 issue the MMAs
 // of the even and odd items, each into its own TMEM slot (D at column 256e, S at 256e +
-// 128); warp 19 writes each item's one-hot scale operand.  The scale MMA multiplies AS
-// (dense: column k = xd of block k) by the one-hot operand (only column c nonzero, = the
-// item's column scales), so S = xd_c (x) w_c exactly.  Each epilogue warp reads D and S
-// in two 16-column halves and hands the slot back before its last FMAs.
+// 128).  The scale MMA of block item c multiplies AS_c, which arrives with the block's codes
+// (only column c nonzero: xd), by the group's WS (column c = the item's column scales), so
+// S = xd_c (x) w_c exactly.  Measured on this GPU, the tensor core takes one tcgen05
+// instruction (MMA or commit) about every 120 cycles, one after the other: an item costs
+// three MMAs and two commits.  Each epilogue warp reads D and S in two 16-column halves and
+// hands the slot back before its last FMAs.
 template <int FMT, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const uint8_t* __restrict__ xb,
@@ -458,6 +466,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     constexpr bool MIN = is_kquant(FMT) && !DOTS;  // a min item closes every group
     constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
     constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT), WCH = wchunk(FMT), STAGE = stage_bytes(FMT);
+    constexpr int NS = nstage(FMT);
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -479,11 +488,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
         }
         for (int i = 0; i < GR; ++i) {
             ptx::mbar_init(bar(BAR_G_FULL + i), 1);
-            ptx::mbar_init(bar(BAR_G_EMPTY + i), DOTS ? NMMA : NMMA + 1);  // MMA warps' commits (+ one-hot writer)
-        }
-        for (int i = 0; i < OH; ++i) {
-            ptx::mbar_init(bar(BAR_OH_FULL + i), 1);
-            ptx::mbar_init(bar(BAR_OH_EMPTY + i), 1);
+            ptx::mbar_init(bar(BAR_G_EMPTY + i), NMMA);  // each MMA warp's commit after its last item of the group
         }
         for (int i = 0; i < DS; ++i) {
             ptx::mbar_init(bar(BAR_D_FULL + i), 1);
@@ -492,9 +497,12 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
         for (int i = 0; i < NMMA; ++i) ptx::mbar_init(bar(BAR_DRAIN + i), 1);
         ptx::fence_barrier_init();
     }
-    // one-hot operands start at zero; each item sets its column and clears the previous one
-    for (int i = threadIdx.x; i < OH * TILE16 / 16; i += THREADS)
-        reinterpret_cast<uint4*>(smem + L::onehot)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // the min item's AS: column 8 = 1.0 in every row (K = 16 no-swizzle core-matrix layout:
+    // columns 8..15 of row r are the 16 bytes at (r / 8) * 256 + 128 + (r % 8) * 16)
+    for (int i = threadIdx.x; i < TILE16 / 16; i += THREADS) {
+        const bool hi = ((i >> 3) & 1) != 0;  // the 16-byte piece holds columns 8..15
+        reinterpret_cast<uint4*>(smem + L::asmin)[i] = make_uint4(hi ? 0x3C00u : 0u, 0u, 0u, 0u);
+    }
     ptx::fence_proxy_async_smem();
     if (warp == WARP_MMA0) {
         ptx::tmem_alloc(sbase + L::tmem_slot, TMEM_COLS);
@@ -519,26 +527,26 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     if (!wait_bar(bar(BAR_G_EMPTY + gs), ((g / GR) & 1) ^ 1, abort, err)) break;
                     const uint32_t dst = sbase + L::groups + gs * L::gslot;
                     ptx::mbar_arrive_expect_tx(bar(BAR_G_FULL + gs), GA + GW);
-                    ptx::bulk_load(dst, ga + ((size_t)mt * ng + g) * GA, GA, bar(BAR_G_FULL + gs));
+                    if (GA > 0) ptx::bulk_load(dst, ga + ((size_t)mt * ng + g) * GA, GA, bar(BAR_G_FULL + gs));
                     ptx::bulk_load(dst + GA, gw + ((size_t)nt * ng + g) * GW, GW, bar(BAR_G_FULL + gs));
                     g_issued = g + 1;
                 }
                 for (int j = 0; j < GB; ++j) {
-                    const int k = g * GB + j, s = k % NSTAGE;
-                    if (!wait_bar(bar(BAR_ST_EMPTY + s), ((k / NSTAGE) & 1) ^ 1, abort, err)) {
+                    const int k = g * GB + j, s = k % NS;
+                    if (!wait_bar(bar(BAR_ST_EMPTY + s), ((k / NS) & 1) ^ 1, abort, err)) {
                         ok = false;
                         break;
                     }
                     const uint32_t dst = sbase + L::stages + s * STAGE;
                     ptx::mbar_arrive_expect_tx(bar(BAR_ST_FULL + s), STAGE);
-                    ptx::bulk_load(dst, xa + ((size_t)mt * nb + k) * CHUNK, CHUNK, bar(BAR_ST_FULL + s));
-                    ptx::bulk_load(dst + CHUNK, xb + ((size_t)nt * nb + k) * WCH, WCH, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst, xa + ((size_t)mt * nb + k) * XCHUNK, XCHUNK, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst + XCHUNK, xb + ((size_t)nt * nb + k) * WCH, WCH, bar(BAR_ST_FULL + s));
                     st_issued = k + 1;
                 }
             }
             // copies of the last stages and groups may still be in flight after an abort
-            for (int k = st_issued - NSTAGE < 0 ? 0 : st_issued - NSTAGE; k < st_issued; ++k)
-                drain_bar(bar(BAR_ST_FULL + k % NSTAGE), (k / NSTAGE) & 1, err);
+            for (int k = st_issued - NS < 0 ? 0 : st_issued - NS; k < st_issued; ++k)
+                drain_bar(bar(BAR_ST_FULL + k % NS), (k / NS) & 1, err);
             for (int g = g_issued - GR < 0 ? 0 : g_issued - GR; g < g_issued; ++g)
                 drain_bar(bar(BAR_G_FULL + g % GR), (g / GR) & 1, err);
         }
@@ -551,80 +559,48 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
             constexpr uint32_t idesc = make_idesc(BM, BN);
             const uint32_t d = tmem + (uint32_t)(e * 2 * BN), sd = d + BN;
             for (int it = e, n = 0; it < nitems; it += NMMA, ++n) {
-                const int g = it / IPG, c = it % IPG, gs = g % GR, o = it % OH;
+                const int g = it / IPG, c = it % IPG, gs = g % GR;
                 const bool block = c < GB;
-                const int k = g * GB + c, s = k % NSTAGE;  // block index = stage sequence number
+                const int k = g * GB + c, s = k % NS;  // block index = stage sequence number
                 const uint32_t gbase = sbase + L::groups + gs * L::gslot;
                 // a barrier probe costs ~100 cycles even when the phase is complete: the group
                 // barrier is probed at this warp's first item of the group only, and the
-                // item's three probes are issued together (the slow path waits one by one)
+                // item's probes are issued together (the slow path waits one by one)
                 if (!DOTS && (it - NMMA < g * IPG) && !wait_bar(bar(BAR_G_FULL + gs), (g / GR) & 1, abort, err))
                     break;
-                const bool r1 = !block || ptx::mbar_test_wait(bar(BAR_ST_FULL + s), (k / NSTAGE) & 1);
+                const bool r1 = !block || ptx::mbar_test_wait(bar(BAR_ST_FULL + s), (k / NS) & 1);
                 const bool r2 = ptx::mbar_test_wait(bar(BAR_D_EMPTY + e), (n & 1) ^ 1);
-                const bool r3 = DOTS || ptx::mbar_test_wait(bar(BAR_OH_FULL + o), (it / OH) & 1);
-                if (!(r1 && r2 && r3)) {
-                    if (block && !wait_bar(bar(BAR_ST_FULL + s), (k / NSTAGE) & 1, abort, err)) break;
+                if (!(r1 && r2)) {
+                    if (block && !wait_bar(bar(BAR_ST_FULL + s), (k / NS) & 1, abort, err)) break;
                     if (!wait_bar(bar(BAR_D_EMPTY + e), (n & 1) ^ 1, abort, err)) break;
-                    if (!DOTS && !wait_bar(bar(BAR_OH_FULL + o), (it / OH) & 1, abort, err)) break;
                 }
                 ptx::tc_fence_after();
+                const uint32_t a = sbase + L::stages + s * STAGE, b = a + XCHUNK;
                 if (block) {
-                    const uint32_t a = sbase + L::stages + s * STAGE, b = a + CHUNK;
                     ptx::umma_f16(d, sdesc(a, 512), sdesc(b, 512), idesc, 0u);
                     ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + 256, 512), idesc, 1u);
                     if (FMT == FMT_Q6_K) {  // the second weight plane into the same block dot
                         ptx::umma_f16(d, sdesc(a, 512), sdesc(b + CHUNK, 512), idesc, 1u);
                         ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + CHUNK + 256, 512), idesc, 1u);
                     }
-                    ptx::umma_commit(bar(BAR_ST_EMPTY + s));
                 } else {
                     // min item: AM x BMIN^T = sum_j s_j * m_j
                     ptx::umma_f16(d, sdesc(gbase + am_off(FMT), 256), sdesc(gbase + bmin_off(FMT), 256), idesc, 0u);
                 }
                 if (!DOTS) {
-                    ptx::umma_f16(sd, sdesc(gbase, 256), sdesc(sbase + L::onehot + o * TILE16, 256), idesc, 0u);
-                    ptx::umma_commit(bar(BAR_OH_EMPTY + o));
+                    // S = AS x WS^T: AS_c (with the block's codes) or the min item's constant AS
+                    const uint32_t as = block ? a + CHUNK : sbase + L::asmin;
+                    ptx::umma_f16(sd, sdesc(as, 256), sdesc(gbase + ws_off(FMT), 256), idesc, 0u);
                     // this warp's last item of the group releases the group data
                     if (it + NMMA >= (g + 1) * IPG || it + NMMA >= nitems) ptx::umma_commit(bar(BAR_G_EMPTY + gs));
                 }
+                if (block) ptx::umma_commit(bar(BAR_ST_EMPTY + s));  // the stage (codes and AS_c) is read
                 ptx::umma_commit(bar(BAR_D_FULL + e));
             }
             ptx::umma_commit(bar(BAR_DRAIN + e));  // arrives once every MMA this thread issued is done
             drain_bar(bar(BAR_DRAIN + e), 0, err);
         }
         __syncwarp();
-    } else if (warp == WARP_ONEHOT) {
-        // ------------------------------------------------------------ one-hot scale operands
-        if (!DOTS) {
-            int it = 0;
-            bool ok = true;
-            for (int g = 0; g < ng && ok; ++g) {
-                const int gs = g % GR;
-                if (!warp_wait(bar(BAR_G_FULL + gs), (g / GR) & 1, abort, err)) break;
-                const uint16_t* ws = reinterpret_cast<const uint16_t*>(smem + L::groups + gs * L::gslot + ws_off(FMT));
-                for (int c = 0; c < IPG; ++c, ++it) {
-                    const int o = it % OH;
-                    if (!warp_wait(bar(BAR_OH_EMPTY + o), ((it / OH) & 1) ^ 1, abort, err)) {
-                        ok = false;
-                        break;
-                    }
-                    uint16_t* tile = reinterpret_cast<uint16_t*>(smem + L::onehot + o * TILE16);
-                    const int old = it >= OH ? (it - OH) % IPG : c;  // column the slot's last item used
-#pragma unroll
-                    for (int rr = 0; rr < BN / 32; ++rr) {
-                        const int r = lane + 32 * rr;
-                        if (old != c) tile[tile16_idx(r, old)] = 0;
-                        tile[tile16_idx(r, c)] = ws[c * BN + r];
-                    }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(BAR_OH_FULL + o));
-                }
-                __syncwarp();
-                if (ok && lane == 0) ptx::mbar_arrive(bar(BAR_G_EMPTY + gs));
-            }
-        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3, cg = warp >> 2;
@@ -752,7 +728,7 @@ struct ScratchPlan {
 ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K) {
     const int64_t nb = K / QK, ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    return {(size_t)(MT * nb) * CHUNK, (size_t)(MT * ng) * ga_bytes(fmt), (size_t)(NT * nb) * wchunk(fmt),
+    return {(size_t)(MT * nb) * XCHUNK, (size_t)(MT * ng) * ga_bytes(fmt), (size_t)(NT * nb) * wchunk(fmt),
             (size_t)(NT * ng) * gw_bytes(fmt)};
 }
 

@@ -233,11 +233,11 @@ int mmq_debug_block_dots_q6_k(const void* xq, const void* wq, int64_t M, int64_t
  * method's pages have no counterpart of this entry point; it exists for callers that may
  * not allocate.
  *  - Scratch need, in bytes, with MT = ceil(M/128), NT = ceil(N/128), nb = K/32,
- *    ng = K/256:  MT*nb*8192 + MT*ng*GA + NT*nb*WB + NT*ng*GW, where WB = 8192 (16384
- *    for Q6_K), GA = 4096 and GW = 2048 for Q8_0 and Q6_K, GA = 8192 and GW = 6400 for
- *    Q4_K and Q5_K.  A shape that needs
+ *    ng = K/256:  MT*nb*12288 + MT*ng*GA + NT*nb*WB + NT*ng*GW, where WB = 8192 (16384
+ *    for Q6_K), GA = 0 and GW = 4096 for Q8_0 and Q6_K, GA = 4096 and GW = 8192 for Q4_K
+ *    and Q5_K.  A shape that needs
  *    more than 64 MiB is refused with MMQ_ERR_SHAPE (e.g. M = 512, N = K = 3584 Q8_0
- *    needs about 30 MiB).  K % 256 == 0 for every format (MMQ_ERR_K_MULTIPLE otherwise).
+ *    needs about 31 MiB).  K % 256 == 0 for every format (MMQ_ERR_K_MULTIPLE otherwise).
  *  - The array's address is looked up (cudaGetSymbolAddress) on the first call on each
  *    device: make that first call outside any stream capture.
  *  - There is one array per device: two calls whose kernels overlap in time on one
