@@ -1,34 +1,36 @@
 // Tensor-core MMQ over codes expanded once per call (sm_103a).
 //
 // Every int8 code, and every K-quant code (Q4_K: 4 bits, Q5_K: 5 bits) times its 6-bit
-// sub-scale, is an exact fp16 value, so the fp16 x fp16 -> f32 MMA over one 32-block computes the integer block dot
-// exactly ("When the Product Won't Collapse", sec. "The obstruction": one integer dot
+// sub-scale, is an exact fp16 value, so the fp16 x fp16 -> f32 MMA over one 32-block
+// computes the integer block dot exactly ("When the Product Won't Collapse", sec. "The obstruction": one integer dot
 // per constant-scale block).  Because the scale changes at every block, the
 // accumulator is read out of TMEM after every block and rescaled in registers (same
 // page, sec. "The viable route is per-backend anyway"): out += xd[m,b] * w[n,b] * D_b.
 //
-// Measured on this GPU, one thread issues a kind::f16 MMA about every 128 cycles when
-// consecutive MMAs switch accumulators, while the tensor core finishes a 128 x 128 x 16
-// MMA in 64: so the 128 x 128 tiles here have two MMA-issuing warps (even and odd
-// items), each with its own TMEM slot of 256 columns (D, then the scale products S).
+// Measured on this GPU, the tensor core takes one tcgen05 instruction (MMA or commit)
+// about every 120 cycles, one after the other, while it finishes a 128 x 128 x 16 MMA in
+// 64: an item (one 32-block of a 128 x 128 tile) costs what it issues, so each issues
+// three MMAs and two commits.  Two MMA-issuing warps (even and odd items) each own a TMEM
+// slot of 256 columns (D, then the scale products S).
 // The codes reach shared memory already in the MMA's layout: one streaming kernel,
 // k_expand, converts every code once per call into scratch, its CTAs split between
 //
 //   activations  q8_1 rows (or f32 rows, quantized on the way) -> per (128-row tile,
 //                32-block) an 8 KiB chunk of fp16 codes in the K-major no-swizzle
-//                core-matrix order; per (tile, 256-value group) the K = 16 operand AS
-//                (column c = xd of block c; column 8 = 1.0, the K-quant min item) and,
-//                for K-quants, AM (column c = the f16 block sum s of block c);
-//   weights      Q8_0 / Q4_K / Q5_K rows -> per (128-row tile, 32-block) the same chunks
-//                (K-quants: q * sc_j); per (tile, group) the f16 column scales WS (Q8_0: wd;
-//                K-quants: d, and -dmin for the min item) and, for K-quants, the K = 16
-//                operand BMIN (column j = m_j) ("When Does a Kernel Win Surface?", sec.
-//                "Kept levers: Vulkan", the Q4_K affine identity);
+//                core-matrix order followed by AS_b, the block's K = 16 scale operand
+//                (column b % 8 = xd, the other columns 0); per (tile, 256-value group), for
+//                K-quants, AM (column c = the f16 block sum s of block c);
+//   weights      Q8_0 / Q4_K / Q5_K / Q6_K rows -> per (128-row tile, 32-block) the same
+//                chunks (K-quants: q * sc_j; Q6_K: two planes); per (tile, group) WS, the
+//                K = 16 operand of the column scales (column c = wd of block c, or d; column
+//                8 = -dmin for the min item) and, for K-quants, BMIN (column j = m_j) ("When
+//                Does a Kernel Win Surface?", sec. "Kept levers: Vulkan", the Q4_K affine
+//                identity);
 //
 // and k_mmq_tcx copies whole chunks with 1-D bulk copies, issues two K = 16 MMAs per
-// block (the exact block dot D) and one K = 16 MMA of AS against a one-hot operand built
-// from WS (the scale products S = xd * w, exact in f32) per item, and rescales in 16
-// epilogue warps: acc = fma(S, D, acc), one rounding per block.  Rows past M or N are
+// block (the exact block dot D) and one K = 16 MMA of AS_b against WS (the scale products
+// S = xd (x) w, exact in f32: one nonzero term) per item, and rescales in 16 epilogue
+// warps: acc = fma(S, D, acc), one rounding per block.  Rows past M or N are
 // zero in the scratch: they add nothing and are never stored.
 //
 // The price is scratch traffic: 2 bytes written and read back per code.  It pays when
@@ -764,7 +766,7 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     }
     {
         // a programmatic dependent launch: the contraction's CTAs may be scheduled while the
-        // expansion drains, their set-up (barriers, TMEM, one-hot operands) overlapping it
+        // expansion drains, their set-up (barriers, TMEM, the constant scale operand) overlapping it
         ProfScope ps("k_mmq_tcx", s);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)MT, (unsigned)NT);
