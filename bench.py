@@ -748,6 +748,8 @@ def run_sweep(args):
         cases += [(fmt, M, 3584, 3584, "q") for M in (512, 2048)]
     for fmt in ("q4_k", "q8_0"):  # a few tens of rows
         cases += [(fmt, M, 18944, 3584, "gate") for M in (16, 32, 64)]
+    # tens to hundreds of rows on the long-K projection: few output tiles, K split
+    cases += [("q4_k", M, 3584, 18944, "down") for M in (64, 128, 256)]
     if args.only:  # one case, "fmt:M:N:K" (for profiling a single kernel)
         f, m, n, k = args.only.split(":")
         cases = [c for c in cases if c[:4] == (f, int(m), int(n), int(k))]

@@ -50,26 +50,31 @@ int current_path() {
 }
 
 constexpr int64_t LIMIT = (int64_t)1 << 40;
-constexpr int SM_COUNT = 152;  // GB300
 
-// Path choice for MMQ_PATH_AUTO from two measured cost models (GB300, microseconds):
-// the small-M streams take the weights once per pass of 8 activation rows (Q6_K: 4) at
-// about 4.2 (Q6_K: 2.7) million weight values per microsecond; the expanded tensor-core
-// path pays the code expansion (about 3 bytes of traffic per weight byte) plus, per wave
-// of 128 x 128 tiles over the SMs, one tile's pass over K (~0.34 us per 32-block; the
-// K-quants with mins add one min item per 8 blocks).  The converter kernel is never the
-// faster of the two and is only used when asked for.
+// Path choice for MMQ_PATH_AUTO from two cost models fitted to measurements on GB300
+// (microseconds, M from 8 to 384 on 512..18944 x 3584..18944 weights):
+// - the small-M streams take the weights once per pass of 8 activation rows (Q6_K: 4), at
+//   about 4.4 (Q6_K: 2.7) million weight values per microsecond, a quarter less when the
+//   weights are small (N * K below 32 M values: too little work per pass to fill the GPU);
+// - the expanded tensor-core path pays the code expansion (~0.6 us per million weight
+//   values; Q6_K, two planes: ~1.0) plus, per wave of 128 x 128 tiles (times their K
+//   splits) over the SMs, one CTA's pass over its share of K (~0.28 us per 32-block; the
+//   K-quants with mins add one min item per 8 blocks), plus fixed costs.
+// The converter kernel is never the faster of the two and is only used when asked for.
 int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
     if (M <= 8 || K % QK_K != 0 || !tc_available()) return MMQ_PATH_SMALL;
-    const double wbytes = (double)N * (double)mmq_weight_row_bytes(fmt, K);
-    // Q6_K's expansion writes two fp16 planes (4 bytes per value against 0.82 read)
     const bool q6 = fmt == FMT_Q6_K;
-    const double t_small =
-        (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * (double)N * (double)K / (q6 ? 2.7e6 : 4.2e6) + 1.5;
-    const double tiles = (double)((M + 127) / 128) * (double)((N + 127) / 128);
-    const double waves = (double)(int64_t)((tiles + SM_COUNT - 1) / SM_COUNT);
-    const double items = (double)(K / QK) * (is_kquant(fmt) ? 9.0 / 8.0 : 1.0);
-    const double t_expand = (q6 ? 10.0 : 3.0) * wbytes / 3.0e6 + waves * items * 0.34 + 8.0;
+    const double nk = (double)N * (double)K;
+    const double rate = (q6 ? 2.7e6 : 4.4e6) * (nk < 32e6 ? (q6 ? 0.82 : 0.77) : 1.0);
+    const double t_small = (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * nk / rate + 1.5;
+    // with K split S ways (small outputs), S times the CTAs each take 1/S of the groups,
+    // and a summing kernel follows
+    const int64_t S = tcx_splits(M, N, K), ng = K / QK_K;
+    const int64_t ctas = ((M + 127) / 128) * ((N + 127) / 128) * S;
+    const double waves = (double)((ctas + SM_COUNT - 1) / SM_COUNT);
+    const double items = (double)(8 * ((ng + S - 1) / S)) * (is_kquant(fmt) ? 9.0 / 8.0 : 1.0);
+    const double t_expand =
+        (q6 ? 1.0 : 0.6) * nk / 1e6 + 0.28 * waves * items + (q6 ? 5.0 : 8.0) + (S > 1 ? 1.0 : 0.0);
     return t_small < t_expand ? MMQ_PATH_SMALL : MMQ_PATH_EXPAND;
 }
 

@@ -72,6 +72,9 @@ int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t
                       cudaStream_t s);
 int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                        cudaStream_t s);
+// K splits the expanded path's contraction uses for an M x N x K call (1: none)
+int tcx_splits(int64_t M, int64_t N, int64_t K);
+constexpr int SM_COUNT = 152;  // GB300: 2 dies x 76 SMs
 int tc_grouped_launch(int fmt, const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
                       const int2* tiles, const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map,
                       float* out, cudaStream_t s);

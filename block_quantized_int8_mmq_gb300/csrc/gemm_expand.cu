@@ -7,11 +7,12 @@
 // accumulator is read out of TMEM after every block and rescaled in registers (same
 // page, sec. "The viable route is per-backend anyway"): out += xd[m,b] * w[n,b] * D_b.
 //
-// Measured on this GPU, the tensor core takes one tcgen05 instruction (MMA or commit)
-// about every 120 cycles, one after the other, while it finishes a 128 x 128 x 16 MMA in
-// 64: an item (one 32-block of a 128 x 128 tile) costs what it issues, so each issues
-// three MMAs and two commits.  Two MMA-issuing warps (even and odd items) each own a TMEM
-// slot of 256 columns (D, then the scale products S).
+// Measured on this GPU, one thread issuing 128 x 128 x 16 MMAs back to back into one
+// accumulator gets one every 64 cycles; an item here (one 32-block of a 128 x 128 tile:
+// two MMAs for D, one for S, two commits) takes about 750, the chain from issue through
+// the commits, the epilogue's TMEM reads and the slot's release, so every tcgen05
+// instruction saved per item counts.  Two MMA-issuing warps (even and odd items) each own
+// a TMEM slot of 256 columns (D, then the scale products S).
 // The codes reach shared memory already in the MMA's layout: one streaming kernel,
 // k_expand, converts every code once per call into scratch, its CTAs split between
 //
@@ -456,14 +457,17 @@ struct XLayout {
 // of the even and odd items, each into its own TMEM slot (D at column 256e, S at 256e +
 // 128).  The scale MMA of block item c multiplies AS_c, which arrives with the block's codes
 // (only column c nonzero: xd), by the group's WS (column c = the item's column scales), so
-// S = xd_c (x) w_c exactly.  Measured on this GPU, the tensor core takes one tcgen05
-// instruction (MMA or commit) about every 120 cycles, one after the other: an item costs
-// three MMAs and two commits.  Each epilogue warp reads D and S in two 16-column halves and
-// hands the slot back before its last FMAs.
+// S = xd_c (x) w_c exactly.  An item issues three MMAs and two commits (stage free; D and
+// S ready).  Epilogue warp 0 releases the
+// group data after each group's last item.  Each epilogue warp reads D and S in two
+// 16-column halves and hands the slot back before its last FMAs.  With K split over
+// gridDim.z CTAs per tile (small outputs), CTA z takes its share of the groups and writes
+// a partial tile.
 template <int FMT, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const uint8_t* __restrict__ xb,
-          const uint8_t* __restrict__ gw, int M, int N, int nb, float* __restrict__ out, int32_t* __restrict__ dots) {
+          const uint8_t* __restrict__ gw, int M, int N, int nb, float* __restrict__ out, int32_t* __restrict__ dots,
+          long long split_stride) {
     using L = XLayout<FMT>;
     constexpr bool MIN = is_kquant(FMT) && !DOTS;  // a min item closes every group
     constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
@@ -477,7 +481,12 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     const int mt = blockIdx.x, nt = blockIdx.y;
     const int m0 = mt * BM, n0 = nt * BN;
     const int ng = nb / GB;
-    const int nitems = ng * IPG;
+    // K split z of gridDim.z takes groups g0 .. g1 - 1 and writes its partial tile to
+    // out + z * split_stride (one split: the output itself); the indices below (items,
+    // stages, groups) count from g0
+    const int g0 = (int)((long long)blockIdx.z * ng / gridDim.z), g1 = (int)((long long)(blockIdx.z + 1) * ng / gridDim.z);
+    const int ngl = g1 - g0;
+    const int nitems = ngl * IPG;
     volatile int* abort = &s_abort;
     unsigned* err = &g_tcx_error;
     auto bar = [&](int i) -> uint32_t { return sbase + L::bars + 8 * i; };
@@ -490,7 +499,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
         }
         for (int i = 0; i < GR; ++i) {
             ptx::mbar_init(bar(BAR_G_FULL + i), 1);
-            ptx::mbar_init(bar(BAR_G_EMPTY + i), NMMA);  // each MMA warp's commit after its last item of the group
+            ptx::mbar_init(bar(BAR_G_EMPTY + i), 1);  // epilogue warp 0, once the group's last item is done
         }
         for (int i = 0; i < DS; ++i) {
             ptx::mbar_init(bar(BAR_D_FULL + i), 1);
@@ -523,26 +532,27 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
             ptx::grid_dep_wait();
             int st_issued = 0, g_issued = 0;
             bool ok = true;
-            for (int g = 0; g < ng && ok; ++g) {
+            for (int g = 0; g < ngl && ok; ++g) {
+                const int gg = g0 + g;  // the group's index in K
                 if (!DOTS) {
                     const int gs = g % GR;
                     if (!wait_bar(bar(BAR_G_EMPTY + gs), ((g / GR) & 1) ^ 1, abort, err)) break;
                     const uint32_t dst = sbase + L::groups + gs * L::gslot;
                     ptx::mbar_arrive_expect_tx(bar(BAR_G_FULL + gs), GA + GW);
-                    if (GA > 0) ptx::bulk_load(dst, ga + ((size_t)mt * ng + g) * GA, GA, bar(BAR_G_FULL + gs));
-                    ptx::bulk_load(dst + GA, gw + ((size_t)nt * ng + g) * GW, GW, bar(BAR_G_FULL + gs));
+                    if (GA > 0) ptx::bulk_load(dst, ga + ((size_t)mt * ng + gg) * GA, GA, bar(BAR_G_FULL + gs));
+                    ptx::bulk_load(dst + GA, gw + ((size_t)nt * ng + gg) * GW, GW, bar(BAR_G_FULL + gs));
                     g_issued = g + 1;
                 }
                 for (int j = 0; j < GB; ++j) {
-                    const int k = g * GB + j, s = k % NS;
+                    const int k = g * GB + j, s = k % NS, kk = gg * GB + j;
                     if (!wait_bar(bar(BAR_ST_EMPTY + s), ((k / NS) & 1) ^ 1, abort, err)) {
                         ok = false;
                         break;
                     }
                     const uint32_t dst = sbase + L::stages + s * STAGE;
                     ptx::mbar_arrive_expect_tx(bar(BAR_ST_FULL + s), STAGE);
-                    ptx::bulk_load(dst, xa + ((size_t)mt * nb + k) * XCHUNK, XCHUNK, bar(BAR_ST_FULL + s));
-                    ptx::bulk_load(dst + XCHUNK, xb + ((size_t)nt * nb + k) * WCH, WCH, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst, xa + ((size_t)mt * nb + kk) * XCHUNK, XCHUNK, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst + XCHUNK, xb + ((size_t)nt * nb + kk) * WCH, WCH, bar(BAR_ST_FULL + s));
                     st_issued = k + 1;
                 }
             }
@@ -593,10 +603,12 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     // S = AS x WS^T: AS_c (with the block's codes) or the min item's constant AS
                     const uint32_t as = block ? a + CHUNK : sbase + L::asmin;
                     ptx::umma_f16(sd, sdesc(as, 256), sdesc(gbase + ws_off(FMT), 256), idesc, 0u);
-                    // this warp's last item of the group releases the group data
-                    if (it + NMMA >= (g + 1) * IPG || it + NMMA >= nitems) ptx::umma_commit(bar(BAR_G_EMPTY + gs));
                 }
-                if (block) ptx::umma_commit(bar(BAR_ST_EMPTY + s));  // the stage (codes and AS_c) is read
+                // the stage (codes and AS_b) is free once these MMAs are done; the group data
+                // is released by the epilogue, which takes the items in order, after the
+                // group's last item (a commit per group and issuer costs the tensor core as
+                // much as an MMA)
+                if (block) ptx::umma_commit(bar(BAR_ST_EMPTY + s));
                 ptx::umma_commit(bar(BAR_D_FULL + e));
             }
             ptx::umma_commit(bar(BAR_DRAIN + e));  // arrives once every MMA this thread issued is done
@@ -616,6 +628,11 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
             const int e = it % DS;
             if (!warp_wait(bar(BAR_D_FULL + e), (it / DS) & 1, abort, err)) break;
             ptx::tc_fence_after();
+            if (!DOTS && warp == 0 && lane == 0 && it % IPG == IPG - 1) {
+                // every MMA of the group's last item and, since the items are taken in order,
+                // of all its earlier ones is done: the group data may be overwritten
+                ptx::mbar_arrive(bar(BAR_G_EMPTY + (it / IPG) % GR));
+            }
             const uint32_t taddr = lane_base + (uint32_t)(e * 2 * BN);
             if (DOTS) {
                 uint32_t dv[EPI_COLS];
@@ -628,7 +645,8 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
 #pragma unroll
                     for (int j = 0; j < EPI_COLS; ++j) {
                         const int n = n0 + c0 + j;
-                        if (n < N) dots[((long long)mrow * N + n) * nb + it] = __float2int_rn(__uint_as_float(dv[j]));
+                        if (n < N)
+                            dots[((long long)mrow * N + n) * nb + g0 * GB + it] = __float2int_rn(__uint_as_float(dv[j]));
                     }
                 }
             } else {
@@ -654,8 +672,10 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                 }
             }
         }
+        // the partial sums may now be read by a dependent launch once this grid is done
+        ptx::grid_dep_launch_dependents();
         if (!DOTS && !*abort && mrow < M) {
-            float* orow = out + (long long)mrow * N + n0 + c0;
+            float* orow = out + blockIdx.z * split_stride + (long long)mrow * N + n0 + c0;
             const int ncols = N - (n0 + c0);  // columns of this warp's 32 that exist
             if (ncols >= EPI_COLS && (N & 3) == 0) {
 #pragma unroll
@@ -676,6 +696,29 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     if (warp == WARP_MMA0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// The K splits of one output: element i of out is the sum of the splits' partial tiles in
+// the order z = 0, 1, ... (the same order at every call: deterministic).  Launched as a
+// programmatic dependent of the contraction.
+__global__ void __launch_bounds__(256) k_splitk_sum(const float* __restrict__ part, int splits, long long stride,
+                                                    long long n, float* __restrict__ out) {
+    ptx::grid_dep_wait();
+    const long long n4 = n >> 2;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+        float4 a = __ldcs(reinterpret_cast<const float4*>(part) + i);
+        for (int z = 1; z < splits; ++z) {
+            const float4 b = __ldcs(reinterpret_cast<const float4*>(part + z * stride) + i);
+            a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+        }
+        reinterpret_cast<float4*>(out)[i] = a;
+    }
+    const long long t = (n4 << 2) + blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (t < n && blockIdx.x * (long long)blockDim.x + threadIdx.x < 4) {
+        float a = part[t];
+        for (int z = 1; z < splits; ++z) a += part[z * stride + t];
+        out[t] = a;
     }
 }
 
@@ -722,16 +765,26 @@ bool set_smem(Kern k, int bytes, bool& done) {
 }
 
 // Scratch bytes of one call: expanded activations, activation group data, expanded
-// weights, weight group data (each a multiple of 256 bytes).
+// weights, weight group data (each a multiple of 256 bytes), and with K splits their f32
+// partial outputs (`splits` slabs of M x N, each padded to 256 bytes).
 struct ScratchPlan {
-    size_t xa, ga, xb, gw;
-    size_t total() const { return xa + ga + xb + gw; }
+    size_t xa, ga, xb, gw, part;
+    int splits;
+    long long split_stride;  // floats from one slab to the next
+    size_t total() const { return xa + ga + xb + gw + part; }
 };
-ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K) {
+ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K, bool allow_split = true) {
     const int64_t nb = K / QK, ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    return {(size_t)(MT * nb) * XCHUNK, (size_t)(MT * ng) * ga_bytes(fmt), (size_t)(NT * nb) * wchunk(fmt),
-            (size_t)(NT * ng) * gw_bytes(fmt)};
+    const int splits = allow_split ? tcx_splits(M, N, K) : 1;
+    const long long stride = ((long long)(M * N) + 63) & ~63LL;
+    return {(size_t)(MT * nb) * XCHUNK,
+            (size_t)(MT * ng) * ga_bytes(fmt),
+            (size_t)(NT * nb) * wchunk(fmt),
+            (size_t)(NT * ng) * gw_bytes(fmt),
+            splits > 1 ? (size_t)splits * (size_t)stride * 4 : 0,
+            splits,
+            stride};
 }
 
 // The two launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K) bytes): both
@@ -739,10 +792,9 @@ ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K) {
 // are quantized by the expansion (q8_1 bytes written to xq); else xq is the input.
 template <int FMT, bool DOTS>
 int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
-              int32_t* dots, uint8_t* ws, cudaStream_t s, const char* fn) {
+              int32_t* dots, uint8_t* ws, const ScratchPlan& sp, cudaStream_t s, const char* fn) {
     const int nb = (int)(K / QK), ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    const ScratchPlan sp = plan_scratch(FMT, M, N, K);
     static bool attr_done = false;
     if (!set_smem(k_mmq_tcx<FMT, DOTS>, XLayout<FMT>::alloc, attr_done)) {
         report(fn, MMQ_ERR_SMEM, "shared-memory request refused");
@@ -752,6 +804,10 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     uint8_t* ga = xa + sp.xa;
     uint8_t* xb = ga + sp.ga;
     uint8_t* gw = xb + sp.xb;
+    float* part = reinterpret_cast<float*>(gw + sp.gw);
+    // the block dots of each split go straight to their own places: only the f32 output
+    // needs the partial slabs
+    const bool summed = sp.splits > 1 && !DOTS;
     const dim3 eg((unsigned)(4 * MT + 4 * NT), (unsigned)ng);
     {
         ProfScope ps("k_expand", s);
@@ -769,7 +825,7 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         // expansion drains, their set-up (barriers, TMEM, the constant scale operand) overlapping it
         ProfScope ps("k_mmq_tcx", s);
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)MT, (unsigned)NT);
+        cfg.gridDim = dim3((unsigned)MT, (unsigned)NT, (unsigned)sp.splits);
         cfg.blockDim = dim3(THREADS);
         cfg.dynamicSmemBytes = XLayout<FMT>::alloc;
         cfg.stream = s;
@@ -778,8 +834,30 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, DOTS>, (const uint8_t*)xa, (const uint8_t*)ga,
-                                                 (const uint8_t*)xb, (const uint8_t*)gw, (int)M, (int)N, nb, out, dots);
+        const cudaError_t e =
+            cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, DOTS>, (const uint8_t*)xa, (const uint8_t*)ga, (const uint8_t*)xb,
+                               (const uint8_t*)gw, (int)M, (int)N, nb, summed ? part : out, dots,
+                               summed ? sp.split_stride : 0LL);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            report(fn, MMQ_ERR_LAUNCH, cudaGetErrorString(e));
+            return MMQ_ERR_LAUNCH;
+        }
+    }
+    if (summed) {
+        ProfScope ps("k_splitk_sum", s);
+        const long long n = (long long)M * N;
+        cudaLaunchConfig_t cfg = {};
+        const long long blocks = ((n >> 2) + 255) / 256;
+        cfg.gridDim = dim3((unsigned)(blocks < 1 ? 1 : blocks > 4 * SM_COUNT ? 4 * SM_COUNT : blocks));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_splitk_sum, (const float*)part, sp.splits, sp.split_stride, n, out);
         if (e != cudaSuccess) {
             cudaGetLastError();
             report(fn, MMQ_ERR_LAUNCH, cudaGetErrorString(e));
@@ -793,9 +871,10 @@ template <int FMT, bool DOTS>
 int launch_x(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
              int32_t* dots, cudaStream_t s, const char* fn) {
     void* ws = nullptr;
-    const int st0 = scratch_alloc(plan_scratch(FMT, M, N, K).total(), s, &ws, fn);
+    const ScratchPlan sp = plan_scratch(FMT, M, N, K);
+    const int st0 = scratch_alloc(sp.total(), s, &ws, fn);
     if (st0 != MMQ_OK) return st0;
-    const int st = launch_on<FMT, DOTS>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), s, fn);
+    const int st = launch_on<FMT, DOTS>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), sp, s, fn);
     scratch_free(ws, s);  // stream-ordered: after the kernels above
     return st;
 }
@@ -920,10 +999,13 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
         report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
         return MMQ_ERR_SHAPE;
     }
-    if (plan_scratch(fmt, M, N, K).total() > NOALLOC_SCRATCH_BYTES) {
+    if (plan_scratch(fmt, M, N, K, false).total() > NOALLOC_SCRATCH_BYTES) {
         report(fn, MMQ_ERR_SHAPE, "the fixed 64 MiB scratch is too small for this shape");
         return MMQ_ERR_SHAPE;
     }
+    // K splits only where their partial outputs fit in the fixed scratch too
+    ScratchPlan sp = plan_scratch(fmt, M, N, K);
+    if (sp.total() > NOALLOC_SCRATCH_BYTES) sp = plan_scratch(fmt, M, N, K, false);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -935,10 +1017,21 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
         report(fn, MMQ_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed");
         return MMQ_ERR_CUDA;
     }
-    return fmt == FMT_Q8_0   ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
-           : fmt == FMT_Q5_K ? launch_on<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
-           : fmt == FMT_Q6_K ? launch_on<FMT_Q6_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn)
-                             : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, s, fn);
+    return fmt == FMT_Q8_0   ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
+           : fmt == FMT_Q5_K ? launch_on<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
+           : fmt == FMT_Q6_K ? launch_on<FMT_Q6_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
+                             : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn);
+}
+
+// K splits of the contraction: only when the output has fewer 128 x 128 tiles than there
+// are SMs, as many as fill the SMs once (at most 8), each at least two 256-value groups.
+int tcx_splits(int64_t M, int64_t N, int64_t K) {
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t ng = K / QK_K;
+    int64_t sp = SM_COUNT / (tiles < 1 ? 1 : tiles);
+    if (sp > ng / 2) sp = ng / 2;
+    if (sp > 8) sp = 8;
+    return sp < 1 ? 1 : (int)sp;
 }
 
 unsigned tcx_take_error() {

@@ -20,7 +20,10 @@
  *  - Pointers named x, xq, wq, out, dots are DEVICE pointers owned by the caller.  The
  *    library never frees or retains them.
  *  - Scratch: the expanded-code tensor-core path (MMQ_PATH_EXPAND) needs a scratch
- *    buffer of about 2*K bytes per row of each operand (rows rounded up to 128).  It is
+ *    buffer of about 2*K bytes per row of each operand (rows rounded up to 128), plus,
+ *    when the output has fewer 128 x 128 tiles than the GPU has SMs and K is split
+ *    across S <= 8 CTAs per tile, S*M*N*4 bytes of partial outputs (summed in a fixed
+ *    order, so results are deterministic).  It is
  *    taken from a library-owned stream-ordered memory pool of the current device
  *    (allocated and freed on the call's stream, cached between calls), so calls on
  *    different streams never share scratch.  While `stream` is being captured into a
@@ -238,6 +241,8 @@ int mmq_debug_block_dots_q6_k(const void* xq, const void* wq, int64_t M, int64_t
  *    and Q5_K.  A shape that needs
  *    more than 64 MiB is refused with MMQ_ERR_SHAPE (e.g. M = 512, N = K = 3584 Q8_0
  *    needs about 31 MiB).  K % 256 == 0 for every format (MMQ_ERR_K_MULTIPLE otherwise).
+ *    The K splits of a small output (see Scratch above) are used only when their
+ *    partial outputs fit in the array as well.
  *  - The array's address is looked up (cudaGetSymbolAddress) on the first call on each
  *    device: make that first call outside any stream capture.
  *  - There is one array per device: two calls whose kernels overlap in time on one

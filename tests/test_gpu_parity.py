@@ -155,6 +155,31 @@ def test_block_dots_bit_exact(mmq, fmt, path):
         assert np.array_equal(dots.cpu().numpy(), ref), f"{fmt} {path} {M}x{N}x{K}"
 
 
+# Outputs with fewer 128 x 128 tiles than SMs: the expanded path splits K across up to 8
+# CTAs per tile (each at least two 256-value groups) and sums their partial tiles in a fixed
+# order; M * N not a multiple of 4 takes the summing kernel's scalar tail.
+SPLIT_SHAPES = [(7, 33, 2304), (130, 131, 4096), (1, 1, 1024), (128, 128, 512), (200, 300, 18944)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_split_k_parity_dots_and_determinism(mmq, fmt):
+    set_path(mmq, "expand")
+    for (M, N, K) in SPLIT_SHAPES:
+        x = synth.activations(M * 5 + K, M, K, True)
+        w = synth.weights(fmt, N * 7 + K, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        wd = dev(w)
+        out = mmq.gemm(fmt, xq, wd, M, N, K)
+        again = mmq.gemm(fmt, xq, wd, M, N, K)
+        assert torch.equal(out, again), f"{fmt} {M}x{N}x{K}: not deterministic"
+        ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
+        check_close(out.cpu().numpy(), ref, norm, f"{fmt} split {M}x{N}x{K}")
+        if M * N * K <= 130 * 131 * 4096:
+            dots = mmq.block_dots(fmt, xq, wd, M, N, K)
+            assert np.array_equal(dots.cpu().numpy(), oracle.block_dots(fmt, oracle.quantize_q8_1(x), w, M, N, K))
+    assert mmq.mmq_get_device_error() == 0
+
+
 # one to eight activation rows on the small path: weight rows dealt out to warps (several
 # rows per warp when N exceeds the resident warps), rows of 1 to 10 pieces with a partial
 # last piece, N = 1, and token counts that leave part of a 4- or 8-row pass empty
@@ -236,9 +261,12 @@ def test_linear_matches_separate_calls(mmq, fmt, path):
     assert mmq.mmq_get_device_error() == 0
 
 
-def test_linear_graph_capture_two_kernels(mmq):
+# 6 tiles: K = 512 (two groups) is not split, K = 1024 is split in two and summed
+@pytest.mark.parametrize("K,kernels", [(512, {"k_expand", "k_mmq_tcx"}),
+                                       (1024, {"k_expand", "k_mmq_tcx", "k_splitk_sum"})])
+def test_linear_graph_capture(mmq, K, kernels):
     set_path(mmq, "expand")
-    M, N, K = 256, 384, 1024
+    M, N = 256, 384
     x = synth.activations(91, M, K, True)
     w = synth.q4_k_weights(92, N, K)
     xd, wd = dev(x), dev(w)
@@ -256,7 +284,7 @@ def test_linear_graph_capture_two_kernels(mmq):
         prof = mmq.mmq_profile_read(reset=True)
     finally:
         mmq.mmq_profile_enable(prev)
-    assert set(prof) == {"k_expand", "k_mmq_tcx"}, prof
+    assert set(prof) == kernels and all(n == 1 for n, _ in prof.values()), prof
     xq_ref = oracle.quantize_q8_1(x)
     assert np.array_equal(xq.cpu().numpy(), xq_ref)
     ref, norm = oracle.gemm("q4_k", xq_ref, w, M, N, K)
