@@ -102,13 +102,19 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
 // 8*((p/8)%4) .. +7 of the block: offset p*16 is that row's core-matrix row, so the
 // pieces are written in order (coalesced).
 
-// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the activations:
-// rows 32h..32h+31 of a tile are row groups 4h..4h+3, i.e. a contiguous 2 KiB of every
-// chunk and 1 KiB of every K = 16 tile.  The quarter's q8_1 rows are first gathered into
-// shared memory (row stride EXP_SROW): copied from xq, or (FROM_X) quantized here from
-// the f32 rows of x by the same per-block arithmetic as k_quantize_q8_1, the q8_1 bytes
-// also written to xq for the caller.
+// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the activations, or,
+// when it quantizes them (FROM_X), per (quarter, 32-block): the quantization is the
+// heavier work, so it is spread over eight times as many CTAs (measured on 512 x 3584 x
+// 3584: 2 blocks per CTA 48.5 us per call, 1 block 47.5 us, 8 blocks 50.1 us).  Rows 32h..32h+31 of
+// a tile are row groups 4h..4h+3, i.e. a contiguous 2 KiB of every chunk and 1 KiB of
+// every K = 16 tile.  The CTA's q8_1 rows are first gathered into shared memory (row
+// stride EXP_SROW): copied from xq, or (FROM_X) quantized here from the f32 rows of x by
+// the same per-block arithmetic as k_quantize_q8_1, the q8_1 bytes also written to xq for
+// the caller.
 constexpr int EXP_SROW = 304;  // 76 words: the 64-bit reads below are conflict-free
+// 32-blocks per activation CTA (of a group's 8) and activation CTAs per (quarter, group)
+__host__ __device__ constexpr int acts_blocks(bool from_x) { return from_x ? 1 : GB; }
+__host__ __device__ constexpr int acts_split(bool from_x) { return GB / acts_blocks(from_x); }
 
 template <int FMT, bool FROM_X>
 __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __restrict__ x,
@@ -118,14 +124,18 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     constexpr int ROW = GB * Q8_1_BYTES;  // 288 bytes of one row per group
     constexpr int V = ROW / 16;           // 18
     constexpr int SROW = EXP_SROW;
-    const int mt = bx >> 2, h = bx & 3, ng = nb / GB;
+    constexpr int JB = acts_blocks(FROM_X), SPLIT = acts_split(FROM_X);
+    static_assert(SPLIT == 1 || JB <= 2, "columns of each AM piece");
+    const int mt = bx / (4 * SPLIT), h = (bx / SPLIT) & 3, j0 = (bx % SPLIT) * JB, ng = nb / GB;
     const int m0 = mt * BM + h * EXP_ROWS;
     const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
+    // shared memory: row r of the quarter, block j0 + jj at r * SROW + jj * 36
     if (FROM_X) {
-        // 32 rows x 8 blocks, four lanes per block: a warp quantizes the 8 blocks (1 KiB of
-        // x) of one row per pass; the loads of two passes are issued before their math
-        constexpr int PASSES = EXP_ROWS * GB / (EXP_THREADS / 4);  // 8
-        constexpr int BATCH = 2;
+        // 32 rows x JB blocks, four lanes per block (a pass covers 32 blocks); the loads of
+        // BATCH passes are issued before their math
+        constexpr int PASSES = EXP_ROWS * JB / (EXP_THREADS / 4);  // 1
+        constexpr int BATCH = PASSES < 2 ? PASSES : 2;
+        static_assert(PASSES % BATCH == 0, "passes");
         const int part = threadIdx.x & 3;
 #pragma unroll
         for (int p0 = 0; p0 < PASSES; p0 += BATCH) {
@@ -133,7 +143,7 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
                 const int blk = (p0 + u) * (EXP_THREADS / 4) + (threadIdx.x >> 2);
-                const int r = blk / GB, j = blk % GB, m = m0 + r;
+                const int r = blk / JB, j = j0 + blk % JB, m = m0 + r;
                 va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (m < M) {
                     const float4* src = reinterpret_cast<const float4*>(x + (size_t)m * nb * QK +
@@ -145,16 +155,16 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
                 const int blk = (p0 + u) * (EXP_THREADS / 4) + (threadIdx.x >> 2);
-                const int r = blk / GB, j = blk % GB, m = m0 + r;
+                const int r = blk / JB, jj = blk % JB, m = m0 + r;
                 const float v[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
                 uint32_t w0, w1, hdr;
                 quantize_q8_1_part(v, w0, w1, hdr);
-                uint8_t* sb = sm + r * SROW + j * Q8_1_BYTES;
+                uint8_t* sb = sm + r * SROW + jj * Q8_1_BYTES;
                 if (part == 0) *reinterpret_cast<uint32_t*>(sb) = hdr;
                 *reinterpret_cast<uint32_t*>(sb + 4 + 8 * part) = w0;
                 *reinterpret_cast<uint32_t*>(sb + 8 + 8 * part) = w1;
                 if (m < M) {
-                    uint8_t* gb = xq_out + (size_t)m * rowbytes + (size_t)(g * GB + j) * Q8_1_BYTES;
+                    uint8_t* gb = xq_out + (size_t)m * rowbytes + (size_t)(g * GB + j0 + jj) * Q8_1_BYTES;
                     if (part == 0) *reinterpret_cast<uint32_t*>(gb) = hdr;
                     *reinterpret_cast<uint32_t*>(gb + 4 + 8 * part) = w0;
                     *reinterpret_cast<uint32_t*>(gb + 8 + 8 * part) = w1;
@@ -171,38 +181,44 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
         }
     }
     __syncthreads();
-    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB) * XCHUNK + h * (CHUNK / 4);
+    uint8_t* dst = xa + ((size_t)mt * nb + (size_t)g * GB + j0) * XCHUNK + h * (CHUNK / 4);
     constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
-    for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
-        const int j = i / PIECES, p = i % PIECES;
+    for (int i = threadIdx.x; i < JB * PIECES; i += EXP_THREADS) {
+        const int jj = i / PIECES, p = i % PIECES;
         const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;  // row within the quarter
-        const uint8_t* src = sm + r * SROW + j * Q8_1_BYTES + 4 + 8 * kc;
+        const uint8_t* src = sm + r * SROW + jj * Q8_1_BYTES + 4 + 8 * kc;
         const uint2 lo = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src));
         const uint2 hi = i8x4_to_f16x4(*reinterpret_cast<const uint32_t*>(src + 4));
-        *reinterpret_cast<uint4*>(dst + (size_t)j * XCHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        *reinterpret_cast<uint4*>(dst + (size_t)jj * XCHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
     // AS_j of each block (after its codes): quarter piece u (0..63) = (row 8*(u/16) + u%8,
     // columns 8*((u/8)%2) .. +7); column j holds xd of block j, the others are 0
-    uint8_t* adst = xa + ((size_t)mt * nb + (size_t)g * GB) * XCHUNK + CHUNK + h * (TILE16 / 4);
-    for (int i = threadIdx.x; i < GB * 64; i += EXP_THREADS) {
-        const int j = i >> 6, u = i & 63;
+    uint8_t* adst = xa + ((size_t)mt * nb + (size_t)g * GB + j0) * XCHUNK + CHUNK + h * (TILE16 / 4);
+    for (int i = threadIdx.x; i < JB * 64; i += EXP_THREADS) {
+        const int jj = i >> 6, u = i & 63, j = j0 + jj;
         const int r = 8 * (u >> 4) + (u & 7), kg = (u >> 3) & 1;
-        const uint16_t xd = *reinterpret_cast<const uint16_t*>(sm + r * SROW + j * Q8_1_BYTES);
+        const uint16_t xd = *reinterpret_cast<const uint16_t*>(sm + r * SROW + jj * Q8_1_BYTES);
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = (kg == 0 && e == j) ? xd : (uint16_t)0;
-        *reinterpret_cast<uint4*>(adst + (size_t)j * XCHUNK + u * 16) = pack8(v);
+        *reinterpret_cast<uint4*>(adst + (size_t)jj * XCHUNK + u * 16) = pack8(v);
     }
     if (is_kquant(FMT) && threadIdx.x >= 64) {
         // AM (group data): quarter piece u = t - 64, column c = s of block c of the group
         uint8_t* gdst = ga + ((size_t)mt * ng + g) * ga_bytes(FMT) + am_off(FMT) + h * (TILE16 / 4);
         const int u = threadIdx.x - 64;
         const int r = 8 * (u >> 4) + (u & 7), kg = (u >> 3) & 1;
-        uint16_t v[8];
+        if (SPLIT == 1) {
+            uint16_t v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            v[e] = kg == 0 ? *reinterpret_cast<const uint16_t*>(sm + r * SROW + e * Q8_1_BYTES + 2) : (uint16_t)0;
-        *reinterpret_cast<uint4*>(gdst + u * 16) = pack8(v);
+            for (int e = 0; e < 8; ++e)
+                v[e] = kg == 0 ? *reinterpret_cast<const uint16_t*>(sm + r * SROW + e * Q8_1_BYTES + 2) : (uint16_t)0;
+            *reinterpret_cast<uint4*>(gdst + u * 16) = pack8(v);
+        } else if (kg == 0) {  // column j0 of the piece
+            *reinterpret_cast<uint16_t*>(gdst + u * 16 + 2 * j0) = *reinterpret_cast<const uint16_t*>(sm + r * SROW + 2);
+        } else if (j0 == 0) {  // columns 8..15 are zero
+            *reinterpret_cast<uint4*>(gdst + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 
@@ -808,17 +824,20 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     // the block dots of each split go straight to their own places: only the f32 output
     // needs the partial slabs
     const bool summed = sp.splits > 1 && !DOTS;
-    const dim3 eg((unsigned)(4 * MT + 4 * NT), (unsigned)ng);
+    // activation CTAs first: 4 per tile (one per quarter), times the block split when they
+    // also quantize
+    const int64_t acts_x = 4 * MT * ((x && !DOTS) ? acts_split(true) : 1);
+    const dim3 eg((unsigned)(acts_x + 4 * NT), (unsigned)ng);
     {
         ProfScope ps("k_expand", s);
         if (x && !DOTS)
             k_expand<FMT, true, true><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, static_cast<uint8_t*>(const_cast<void*>(xq)),
                                                                  static_cast<const uint8_t*>(wq), (int)M, (int)N, nb,
-                                                                 (int)(4 * MT), xa, ga, xb, gw);
+                                                                 (int)acts_x, xa, ga, xb, gw);
         else
             k_expand<FMT, false, !DOTS><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq), nullptr,
                                                                   static_cast<const uint8_t*>(wq), (int)M, (int)N, nb,
-                                                                  (int)(4 * MT), xa, ga, xb, gw);
+                                                                  (int)acts_x, xa, ga, xb, gw);
     }
     {
         // a programmatic dependent launch: the contraction's CTAs may be scheduled while the
