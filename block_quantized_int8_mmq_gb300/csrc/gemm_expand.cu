@@ -103,9 +103,11 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
 // pieces are written in order (coalesced).
 
 // One CTA per (32-row quarter of a 128-row tile, 256-value group) of the activations, or,
-// when it quantizes them (FROM_X), per (quarter, 32-block): the quantization is the
-// heavier work, so it is spread over eight times as many CTAs (measured on 512 x 3584 x
-// 3584: 2 blocks per CTA 48.5 us per call, 1 block 47.5 us, 8 blocks 50.1 us).  Rows 32h..32h+31 of
+// when it quantizes them (FROM_X) and SPLIT_A, per (quarter, 32-block): the quantization is
+// the heavier work, so where the activation tiles are few against the weight tiles it is
+// spread over eight times as many CTAs (measured on 512 x 3584 x 3584: 2 blocks per CTA
+// 48.5 us per call, 1 block 47.5 us, 8 blocks 50.1 us; on 2048 x 3584 x 18944, where the
+// activations are the larger operand, the split cost 1 %).  Rows 32h..32h+31 of
 // a tile are row groups 4h..4h+3, i.e. a contiguous 2 KiB of every chunk and 1 KiB of
 // every K = 16 tile.  The CTA's q8_1 rows are first gathered into shared memory (row
 // stride EXP_SROW): copied from xq, or (FROM_X) quantized here from the f32 rows of x by
@@ -113,10 +115,13 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
 // the caller.
 constexpr int EXP_SROW = 304;  // 76 words: the 64-bit reads below are conflict-free
 // 32-blocks per activation CTA (of a group's 8) and activation CTAs per (quarter, group)
-__host__ __device__ constexpr int acts_blocks(bool from_x) { return from_x ? 1 : GB; }
-__host__ __device__ constexpr int acts_split(bool from_x) { return GB / acts_blocks(from_x); }
+__host__ __device__ constexpr int acts_blocks(bool split) { return split ? 1 : GB; }
+__host__ __device__ constexpr int acts_split(bool split) { return GB / acts_blocks(split); }
+// the split is taken for the fused quantize when the weight tiles are at least four times
+// the activation tiles
+__host__ __device__ constexpr bool split_acts(bool from_x, int64_t MT, int64_t NT) { return from_x && NT >= 4 * MT; }
 
-template <int FMT, bool FROM_X>
+template <int FMT, bool FROM_X, bool SPLIT_A>
 __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __restrict__ x,
                                                  const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
                                                  int M, int nb, uint8_t* __restrict__ xa, uint8_t* __restrict__ ga,
@@ -124,7 +129,8 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     constexpr int ROW = GB * Q8_1_BYTES;  // 288 bytes of one row per group
     constexpr int V = ROW / 16;           // 18
     constexpr int SROW = EXP_SROW;
-    constexpr int JB = acts_blocks(FROM_X), SPLIT = acts_split(FROM_X);
+    static_assert(FROM_X || !SPLIT_A, "the split is for the quantizing expansion");
+    constexpr int JB = acts_blocks(SPLIT_A), SPLIT = acts_split(SPLIT_A);
     static_assert(SPLIT == 1 || JB <= 2, "columns of each AM piece");
     const int mt = bx / (4 * SPLIT), h = (bx / SPLIT) & 3, j0 = (bx % SPLIT) * JB, ng = nb / GB;
     const int m0 = mt * BM + h * EXP_ROWS;
@@ -431,14 +437,14 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
 // Both expansions in one launch: CTAs 0 .. acts_x - 1 (grid x) expand the activations,
 // the rest the weights; grid y = the 256-value group.  The two halves are independent, so
 // they run side by side instead of one after the other.
-template <int FMT, bool FROM_X, bool FOLD>
+template <int FMT, bool FROM_X, bool FOLD, bool SPLIT_A>
 __global__ void __launch_bounds__(EXP_THREADS, 12)
 k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
          const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
          uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
     __shared__ __align__(16) uint8_t sm[EXP_ROWS * EXP_SROW];
     if ((int)blockIdx.x < acts_x) {
-        expand_acts_body<FMT, FROM_X>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
+        expand_acts_body<FMT, FROM_X, SPLIT_A>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
     } else {
         if constexpr (FMT == FMT_Q6_K)  // the sub-scales are always folded (they are inside the block dot)
             expand_weights_q6_k(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
@@ -826,19 +832,25 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     const bool summed = sp.splits > 1 && !DOTS;
     // activation CTAs first: 4 per tile (one per quarter), times the block split when they
     // also quantize
-    const int64_t acts_x = 4 * MT * ((x && !DOTS) ? acts_split(true) : 1);
+    const bool split = split_acts(x && !DOTS, MT, NT);
+    const int64_t acts_x = 4 * MT * acts_split(split);
     const dim3 eg((unsigned)(acts_x + 4 * NT), (unsigned)ng);
     {
         ProfScope ps("k_expand", s);
-        if (x && !DOTS)
-            k_expand<FMT, true, true><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, static_cast<uint8_t*>(const_cast<void*>(xq)),
-                                                                 static_cast<const uint8_t*>(wq), (int)M, (int)N, nb,
-                                                                 (int)acts_x, xa, ga, xb, gw);
+        uint8_t* xq_out = static_cast<uint8_t*>(const_cast<void*>(xq));
+        const uint8_t* w8 = static_cast<const uint8_t*>(wq);
+        if (x && !DOTS && split)
+            k_expand<FMT, true, true, true><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
+                                                                       (int)acts_x, xa, ga, xb, gw);
+        else if (x && !DOTS)
+            k_expand<FMT, true, true, false><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
+                                                                        (int)acts_x, xa, ga, xb, gw);
         else
-            k_expand<FMT, false, !DOTS><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq), nullptr,
-                                                                  static_cast<const uint8_t*>(wq), (int)M, (int)N, nb,
-                                                                  (int)acts_x, xa, ga, xb, gw);
+            k_expand<FMT, false, !DOTS, false><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq),
+                                                                          nullptr, w8, (int)M, (int)N, nb,
+                                                                          (int)acts_x, xa, ga, xb, gw);
     }
+
     {
         // a programmatic dependent launch: the contraction's CTAs may be scheduled while the
         // expansion drains, their set-up (barriers, TMEM, the constant scale operand) overlapping it

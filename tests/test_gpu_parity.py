@@ -244,7 +244,9 @@ def test_linear_matches_separate_calls(mmq, fmt, path):
     if fmt in NO_TC and path == "tc":
         pytest.skip("the converter kernel takes Q8_0 and Q4_K")
     set_path(mmq, path)
-    for (M, N, K) in [(300, 200, 1024), (129, 257, 2304), (4, 130, 512), (513, 64, 256)]:
+    # (100, 600, 512): five weight tiles per activation tile, so the fused quantize is
+    # spread over one CTA per 32-block
+    for (M, N, K) in [(300, 200, 1024), (129, 257, 2304), (4, 130, 512), (513, 64, 256), (100, 600, 512)]:
         x = synth.activations(M + 3 * N + K, M, K, True)
         w = synth.weights(fmt, 2 * M + N, N, K)
         xd, wd = dev(x), dev(w)
