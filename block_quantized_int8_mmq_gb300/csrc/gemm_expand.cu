@@ -243,12 +243,22 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
     const int nt = bx >> 2, h = bx & 3, ng = nb / GB;
     const int n0 = nt * BN + h * EXP_ROWS;
     const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * kq_bytes(FMT);
-    for (int i = threadIdx.x; i < EXP_ROWS * VP; i += EXP_THREADS) {
-        const int r = i / VP, c = i % VP;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < V && n0 + r < N)
-            v = __ldg(reinterpret_cast<const uint4*>(wq + (size_t)(n0 + r) * rowbytes + (size_t)g * ROW) + c);
-        *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
+    {
+        // every load of a thread issued before its first store: one memory round trip
+        constexpr int TOTAL = EXP_ROWS * VP, NL = (TOTAL + EXP_THREADS - 1) / EXP_THREADS;
+        uint4 v[NL];
+#pragma unroll
+        for (int k = 0; k < NL; ++k) {
+            const int i = threadIdx.x + k * EXP_THREADS, r = i / VP, c = i % VP;
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < TOTAL && c < V && n0 + r < N)
+                v[k] = __ldg(reinterpret_cast<const uint4*>(wq + (size_t)(n0 + r) * rowbytes + (size_t)g * ROW) + c);
+        }
+#pragma unroll
+        for (int k = 0; k < NL; ++k) {
+            const int i = threadIdx.x + k * EXP_THREADS;
+            if (i < TOTAL) *reinterpret_cast<uint4*>(sm + (i / VP) * SROW + (i % VP) * 16) = v[k];
+        }
     }
     __syncthreads();
     uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * CHUNK + h * (CHUNK / 4);
