@@ -1134,9 +1134,12 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
         report(sfn, MMQ_ERR_SHAPE, "K or M too large for the Q6_K small-M stream (the expanded path takes it)");
         return MMQ_ERR_SHAPE;
     }
-    // measured crossovers: the dp4a weight streams for one or two rows (and Q4_K up to four),
-    // the int8 tensor-core stream beyond, one pass per 8 rows
-    const int64_t dp4a_max_m = is_kquant(fmt) ? 4 : 2;
+    // measured crossovers: the dp4a weight streams for one or two rows (and the K-quants up
+    // to four, unless there are at least two 16-row weight tiles per SM: at 3 or 4 rows of
+    // 18944 x 3584 the int8 stream takes 15.6 us against 17.4, while on 3584 x 18944 the
+    // dp4a stream is faster, 17.4 against 20.7), the int8 tensor-core stream beyond, one
+    // pass per 8 rows
+    const int64_t dp4a_max_m = is_kquant(fmt) && (N + 15) / 16 < 2 * (int64_t)device_shape().sms ? 4 : 2;
     if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(fmt, M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
         return fmt == FMT_Q8_0   ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
                : fmt == FMT_Q5_K ? launch_dp4a_stream<FMT_Q5_K>(x8, w8, M, N, nb, out, dots, s, sfn)

@@ -207,8 +207,10 @@ def test_few_row_stream_parity_and_dots(mmq, fmt):
 
 # three to a hundred rows on the small path (the int8 tensor-core stream, 8 rows per pass):
 # passes with rows past M, weight tiles with rows past N, one to hundreds of tiles
+# (3, 5000, 512) and (4, 18944, 768): three or four rows of a wide weight, which the K-quants
+# take on the int8 stream (one partly empty pass) rather than the dp4a stream
 TCS_SHAPES = [(3, 1, 256), (16, 129, 768), (17, 300, 2304), (32, 128, 512), (33, 3584, 256), (64, 200, 3584),
-              (100, 1000, 1024), (5, 18944, 512)]
+              (100, 1000, 1024), (5, 18944, 512), (3, 5000, 512), (4, 18944, 768)]
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
