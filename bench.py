@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -40,10 +41,10 @@ import synth  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-L2_BYTES = 129 * 1024 * 1024
-GRAPH_STEPS = 64          # steps per captured graph (rounded up to the operand copies)
-TARGET_TIMED_S = 2.0      # default timed region length (long enough for clock samples)
-E2E_STEPS = 1000          # end-to-end steps (host copies every step)
+L2_FALLBACK = 129 * 1024 * 1024  # when the device's L2 size cannot be queried
+MIN_TIMED_S = 1.0         # every timed region lasts at least this much device time (clock samples)
+MIN_REPLAYS, MAX_REPLAYS = 5, 200000
+E2E_MAX_STEPS = 20000
 
 WORKLOADS = {
     "c1": dict(index=1, label="q8_0 MMQ attention-proj M=512 N=3584 K=3584 (quantize + GEMM)"),
@@ -92,18 +93,6 @@ def whole_job_rate(units_per_step: float, steps: int, world: int, ms_max: float,
     """Units processed by all ranks (each rank a replica doing units_per_step per step)
     divided by the slowest rank's time, in units of `scale` per second."""
     return units_per_step * steps * world / (ms_max / 1e3) / scale
-
-
-def auto_steps(step, warmup, stream, torch):
-    """Steps for about TARGET_TIMED_S of device time, from a short eager estimate."""
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(warmup):
-        step(i)
-    b.record(stream)
-    torch.cuda.synchronize()
-    per = a.elapsed_time(b) / 1e3 / warmup
-    return int(min(200000, max(50, TARGET_TIMED_S / max(per, 1e-7))))
 
 
 # sources each kernel is built from: a kernel's committed DRAM counters stay valid while
@@ -276,20 +265,131 @@ def cpu_baseline(workload: str, budget_s: float):
 
 # ---------------------------------------------------------------------------- our arm
 
-def run_ours(args, rank, world, local):
+def oracle_single_core(budget_s: float = 6.0):
+    """The oracle on ONE host core (OMP_NUM_THREADS=1, a separate process): c0 in full and a
+    band of c1's rows (all N, full K), each quantize + contraction, in TOPS."""
+    code = r"""
+import json, sys, time
+sys.path.insert(0, ROOT)
+import numpy as np
+import oracle, synth
+res = {}
+for index, rows in ((0, None), (1, 4)):
+    x, w, spec = synth.config_operands(index)
+    M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
+    xs = np.ascontiguousarray(x if rows is None else x[:rows])
+    r = xs.shape[0]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.gemm(fmt, oracle.quantize_q8_1(xs), w, r, N, K)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt > BUDGET / 2 or n >= 50:
+            break
+    res["c%d" % index] = {"value": 2.0 * r * N * K * n / dt / 1e12, "unit": "TOPS", "cores": oracle.num_threads(),
+                          "sample": ("all M=%d rows" % M if rows is None else "rows 0..%d of M=%d" % (r - 1, M))
+                                    + ", all N=%d, K=%d, %d pass(es), %.2f s" % (N, K, n, dt)}
+print(json.dumps(res))
+"""
+    code = code.replace("ROOT", repr(ROOT)).replace("BUDGET", repr(budget_s))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=120)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": f"single-core oracle run failed: {e}"}
+
+
+def l2_bytes(torch, dev) -> int:
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size) or L2_FALLBACK
+    except (AttributeError, RuntimeError):
+        return L2_FALLBACK
+
+
+def timed_replays(step, copies, steps, stream, torch, dev, barrier, clocks, target_s):
+    """The K timed steps as CUDA-graph replays (a step is 2 to 4 launches of tens of
+    microseconds: launched one by one from Python the host, not the GPU, would set the
+    pace).  A graph holds exactly K steps; step i of graph r uses operand copy (r*K + i) %
+    copies, and the graphs are replayed in turn, so a copy is reused only after all the
+    others (more than 3x L2 between two uses).  The K-step replay is repeated until at
+    least `target_s` of device time has passed (and at least MIN_REPLAYS times), each replay
+    timed by its own CUDA events on the launching stream; the timed region is bracketed by
+    a barrier and a device synchronize on both sides and the clocks are sampled through it.
+    A further graph of the same K steps, captured with the library's profiler on and
+    replayed once after the timed region, gives each kernel's duration and the launches per
+    step without slowing the timed replays.  Returns (median ms per replay, all replay ms,
+    per-kernel profile)."""
+    import block_quantized_int8_mmq_gb300 as mmq
+    ng = copies // math.gcd(steps, copies)
+    cap = torch.cuda.Stream(dev)
+    prev_prof = mmq.mmq_profile_enable(False)
+    graphs = []
+    for r in range(ng):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(steps):
+                step((r * steps + i) % copies, cap)
+        graphs.append(g)
+    mmq.mmq_profile_read(reset=True)
+    mmq.mmq_profile_enable(True)
+    prof_graph = torch.cuda.CUDAGraph()
+    cap.wait_stream(stream)
+    with torch.cuda.graph(prof_graph, stream=cap):
+        for i in range(steps):
+            step(i % copies, cap)
+    mmq.mmq_profile_enable(prev_prof)
+    # upload and first run of every graph, untimed; the first also sizes the replay count
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for g in graphs:
+        g.replay()
+    b0.record(stream)
+    torch.cuda.synchronize(dev)
+    per = max(a0.elapsed_time(b0) / len(graphs), 1e-3)
+    reps = int(min(MAX_REPLAYS, max(MIN_REPLAYS, math.ceil(target_s * 1e3 / per))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for k in range(reps):
+        ev[k][0].record(stream)
+        graphs[k % ng].replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    prof_graph.replay()
+    torch.cuda.synchronize(dev)
+    prof = mmq.mmq_profile_read(reset=True)
+    return statistics.median(ms), ms, prof, clk, reps
+
+
+def kernel_table(prof, steps):
+    kernels = {k: {"launches_per_step": n / steps, "avg_ms": t / n} for k, (n, t) in prof.items()}
+    total = sum(t for _, t in prof.values()) / steps
+    for k, (n, t) in prof.items():
+        kernels[k]["share"] = (t / steps) / total
+    return kernels, sum(n for n, _ in prof.values()) / steps
+
+
+def measure_config(args, workload, rank, world, local, steps, with_e2e=True):
+    """One workload of BASELINE's configs: quantize + contraction per step (c1, c2, c3), or
+    the quantize alone (c3q).  Returns its bench entry."""
     import torch
     import block_quantized_int8_mmq_gb300 as mmq
-
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = WORKLOADS[args.workload]
+    wl = WORKLOADS[workload]
     x, w, spec = synth.config_operands(wl["index"])
     M, N, K, fmt = spec["M"], spec["N"], spec["K"], spec["fmt"]
     quant_only = wl.get("quant_only", False)
 
     xq_bytes = M * (K // 32) * 36
     set_bytes = x.nbytes + (0 if quant_only else w.nbytes)
-    copies = max(2, -(-3 * L2_BYTES // set_bytes))
+    L2 = l2_bytes(torch, dev)
+    copies = max(2, -(-3 * L2 // set_bytes))
     xs = [torch.from_numpy(x).to(dev)]
     xs += [xs[0].clone() for _ in range(copies - 1)]
     ws = []
@@ -299,17 +399,17 @@ def run_ours(args, rank, world, local):
     xq = torch.empty(xq_bytes, dtype=torch.uint8, device=dev).view(M, -1)
     out = torch.full((M, N), float("nan"), device=dev)
     stream = torch.cuda.current_stream(dev)
-    def step(i, stream=stream):
+
+    def step(j, s=stream):
         # quantize + contraction: one call (on the expanded tensor-core path the quantize is
         # fused into the activation expansion; xq still receives the q8_1 bytes)
-        j = i % copies
         if quant_only:
-            mmq.mmq_quantize_q8_1(xs[j], xq, stream)
+            mmq.mmq_quantize_q8_1(xs[j], xq, s)
         else:
-            mmq.mmq_linear(xs[j], ws[j], fmt, N, xq=xq, out=out, stream=stream)
+            mmq.mmq_linear(xs[j], ws[j], fmt, N, xq=xq, out=out, stream=s)
 
     for i in range(args.warmup):
-        step(i)
+        step(i % copies)
     torch.cuda.synchronize(dev)
     assert mmq.mmq_get_device_error(stream) == 0
     path = mmq.mmq_last_path()
@@ -330,67 +430,12 @@ def run_ours(args, rank, world, local):
     barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
     visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip().isdigit()]
     clocks = ClockSampler(int(visible[local]) if local < len(visible) else local)
-
-    # The K timed steps run as CUDA-graph replays (a step is 2 to 4 launches of tens of
-    # microseconds: launched one by one from Python the host, not the GPU, would set the
-    # pace).  One graph holds G steps, G a multiple of the operand copies so consecutive
-    # steps never reuse a copy; a second graph holds the K % G remaining steps.  These
-    # graphs hold the kernels only.  A third graph, the same G steps captured with the
-    # library's profiler on (a CUDA-event pair around every launch), is replayed once
-    # right after the timed region: it gives each kernel's duration and the launches per
-    # step, without the event nodes slowing the timed steps.
-    steps = args.steps if args.steps > 0 else auto_steps(step, args.warmup, stream, torch)
-    G = min(steps, copies * max(1, -(-GRAPH_STEPS // copies)))
-    reps, tail = divmod(steps, G)
-    cap = torch.cuda.Stream(dev)
-    prev_prof = mmq.mmq_profile_enable(False)
-    graphs = []
-    for count in ([G] if reps else []) + ([tail] if tail else []):
-        g = torch.cuda.CUDAGraph()
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(count):
-                step(i, stream=cap)
-        graphs.append((g, count))
-    mmq.mmq_profile_read(reset=True)
-    mmq.mmq_profile_enable(True)
-    prof_graph = torch.cuda.CUDAGraph()
-    cap.wait_stream(stream)
-    with torch.cuda.graph(prof_graph, stream=cap):
-        for i in range(G):
-            step(i, stream=cap)
-    mmq.mmq_profile_enable(prev_prof)
-    for g, _ in graphs:  # upload and first run, untimed
-        g.replay()
-    torch.cuda.synchronize(dev)
-    out.fill_(float("nan"))
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    t_start.record(stream)
-    for _ in range(reps):
-        graphs[0][0].replay()
-    if tail:
-        graphs[-1][0].replay()
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
+    med, all_ms, prof, clk, reps = timed_replays(step, copies, steps, stream, torch, dev, barrier, clocks, args.timed_s)
     if not quant_only:
         assert not torch.isnan(out).any().item(), "timed steps did not write the output"
-    prof_graph.replay()  # the profiled pass: G steps, right after the timed region
-    torch.cuda.synchronize(dev)
-    prof = mmq.mmq_profile_read(reset=True)  # the profiled pass
     assert mmq.mmq_get_device_error(stream) == 0
-    launches_per_step = sum(n for n, _ in prof.values()) / G
-    kernels = {k: {"launches_per_step": n / G, "avg_ms": t / n} for k, (n, t) in prof.items()}
-    step_kernel_ms = sum(t for _, t in prof.values()) / G
-    for k, (n, t) in prof.items():
-        kernels[k]["share"] = (t / G) / step_kernel_ms
-
-    ms_max = max_over_ranks(ms, world, dev)
+    kernels, launches_per_step = kernel_table(prof, steps)
+    ms_max = max_over_ranks(med, world, dev)
 
     ops = 2.0 * M * N * K
     peaks = load_peaks()
@@ -402,7 +447,7 @@ def run_ours(args, rank, world, local):
         kname = "k_quantize_q8_1"
         achieved = qbytes / (kernels[kname]["avg_ms"] / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(kname, workload),
                 "kernel": kname, "peak_source": peaks["source"] + " hbm_gbs"}
     else:
         value = whole_job_rate(ops, steps, world, ms_max, 1e12)
@@ -415,89 +460,137 @@ def run_ours(args, rank, world, local):
             peak = peaks["bf16_tflops"]
             achieved = ops / (avg / 1e3) / 1e12
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": traffic_for(kname, args.workload), "kernel": kname,
+                    "frac": achieved / peak, "traffic": traffic_for(kname, workload), "kernel": kname,
                     "peak_source": f"{peaks['source']} bf16 burst (f16 tensor rate = bf16 rate)"}
         else:
             wbytes = w.nbytes + xq_bytes + M * N * 4
             gbs = wbytes / (avg / 1e3) / 1e9
             roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for(kname, args.workload), "kernel": kname,
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for(kname, workload), "kernel": kname,
                     "peak_source": peaks["source"] + " hbm_gbs"}
 
-    # end to end through the public API: every step copies its input from pinned host memory
-    # to the device, runs the fused quantize + contraction and copies the result back to
-    # pinned host memory.  The three run on their own streams with two device buffers each
-    # way, ordered by events, so the copies of neighbouring steps overlap a step's compute
-    # (the way a serving loop feeds the GPU); throughput is taken over all steps.
     e2e = None
-    if not quant_only:
-        xh = torch.from_numpy(x).pin_memory()
-        oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        nbuf = 2
-        xd = [torch.empty_like(xs[0]) for _ in range(nbuf)]
-        od = [torch.empty((M, N), device=dev) for _ in range(nbuf)]
-        s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-        in_done = [torch.cuda.Event() for _ in range(nbuf)]
-        comp_done = [torch.cuda.Event() for _ in range(nbuf)]
-        out_done = [torch.cuda.Event() for _ in range(nbuf)]
+    if with_e2e:
+        e2e = measure_e2e(mmq, torch, dev, stream, x, ws, fmt, M, N, K, quant_only, xq, ops,
+                          ms_step=ms_max / steps, target_s=args.timed_s)
+    entry = {
+        "metric": metric, "value": value, "unit": unit, "ms_per_step": ms_max / steps,
+        "tok_per_s": M * steps * world / (ms_max / 1e3), "steps": steps,
+        "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt,
+                   "l2": f"rotating {copies} operand copies ({copies * set_bytes / 2**20:.0f} MiB > 3x the "
+                         f"{L2 / 2**20:.0f} MiB L2)",
+                   "timing": f"CUDA graphs of exactly {steps} steps, replayed {reps} times ({sum(all_ms):.0f} ms of "
+                             f"device time); value from the median replay ({min(all_ms):.3f} .. {max(all_ms):.3f} "
+                             "ms); kernel durations from one profiled replay after the timed region"},
+        "roofline": roof, "kernels": kernels, "path": PATH_NAMES.get(path, "quantize"), "clocks": clk,
+        "gpu_launches": int(round(launches_per_step * steps * reps)),
+        "gpu_launches_per_step": launches_per_step,
+    }
+    if e2e:
+        entry["e2e"] = e2e
+    return entry
 
-        def e2e_steps(n):
-            for i in range(n):
-                bi = i % nbuf
-                if i >= nbuf:
-                    s_in.wait_event(comp_done[bi])   # the input buffer's last reader is done
-                with torch.cuda.stream(s_in):
-                    xd[bi].copy_(xh, non_blocking=True)
-                in_done[bi].record(s_in)
-                s_comp.wait_event(in_done[bi])
-                if i >= nbuf:
-                    s_comp.wait_event(out_done[bi])  # the output buffer's last copy is done
+
+def measure_e2e(mmq, torch, dev, stream, x, ws, fmt, M, N, K, quant_only, xq, ops, ms_step, target_s):
+    """End to end through the public API: every step copies its input from pinned host
+    memory to the device, runs the fused quantize + contraction (or the quantize) and copies
+    the result back to pinned host memory.  The three run on their own streams with two
+    device buffers each way, ordered by events, so the copies of neighbouring steps overlap
+    a step's compute (the way a serving loop feeds the GPU); throughput over as many steps
+    as fill MIN_TIMED_S (the same length as the device-side timing)."""
+    xh = torch.from_numpy(x).pin_memory()
+    res_shape, res_dtype = ((M, K // 32 * 36), torch.uint8) if quant_only else ((M, N), torch.float32)
+    oh = torch.empty(res_shape, dtype=res_dtype).pin_memory()
+    nbuf = 2
+    xd = [torch.empty(x.shape, dtype=torch.float32, device=dev) for _ in range(nbuf)]
+    od = [torch.empty(res_shape, dtype=res_dtype, device=dev) for _ in range(nbuf)]
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    in_done = [torch.cuda.Event() for _ in range(nbuf)]
+    comp_done = [torch.cuda.Event() for _ in range(nbuf)]
+    out_done = [torch.cuda.Event() for _ in range(nbuf)]
+    copies = len(ws) if ws else 1
+
+    def run(n):
+        for i in range(n):
+            bi = i % nbuf
+            if i >= nbuf:
+                s_in.wait_event(comp_done[bi])   # the input buffer's last reader is done
+            with torch.cuda.stream(s_in):
+                xd[bi].copy_(xh, non_blocking=True)
+            in_done[bi].record(s_in)
+            s_comp.wait_event(in_done[bi])
+            if i >= nbuf:
+                s_comp.wait_event(out_done[bi])  # the output buffer's last copy is done
+            if quant_only:
+                mmq.mmq_quantize_q8_1(xd[bi], od[bi], s_comp)
+            else:
                 mmq.mmq_linear(xd[bi], ws[i % copies], fmt, N, xq=xq, out=od[bi], stream=s_comp)
-                comp_done[bi].record(s_comp)
-                s_out.wait_event(comp_done[bi])
-                with torch.cuda.stream(s_out):
-                    oh.copy_(od[bi], non_blocking=True)
-                out_done[bi].record(s_out)
+            comp_done[bi].record(s_comp)
+            s_out.wait_event(comp_done[bi])
+            with torch.cuda.stream(s_out):
+                oh.copy_(od[bi], non_blocking=True)
+            out_done[bi].record(s_out)
 
-        for st in (s_in, s_comp, s_out):
-            st.wait_stream(stream)
-        e2e_steps(3)
-        torch.cuda.synchronize(dev)
-        assert np.array_equal(oh.numpy(), od[2 % nbuf].cpu().numpy()), "e2e output not copied back"
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e_steps = min(steps, E2E_STEPS)
-        a.record(s_in)
-        s_comp.wait_event(a)
-        s_out.wait_event(a)
-        e2e_steps(e_steps)
-        b.record(s_out)
-        torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b)
-        e2e = {"value": ops * e_steps / (e_ms / 1e3) / 1e12, "unit": "TOPS", "steps": e_steps,
-               "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": M * N * 4,
-               "overlap": "copy-in, compute and copy-out on three streams, two buffers each way"}
+    for st in (s_in, s_comp, s_out):
+        st.wait_stream(stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    run(3)
+    b.record(s_out)
+    torch.cuda.synchronize(dev)
+    assert np.array_equal(oh.numpy(), od[2 % nbuf].cpu().numpy()), "e2e output not copied back"
+    per = max(a.elapsed_time(b) / 3, ms_step)
+    n = int(min(E2E_MAX_STEPS, max(20, math.ceil(target_s * 1e3 / per))))
+    a.record(s_in)
+    s_comp.wait_event(a)
+    s_out.wait_event(a)
+    run(n)
+    b.record(s_out)
+    torch.cuda.synchronize(dev)
+    e_ms = a.elapsed_time(b)
+    h2d, d2h = x.nbytes, oh.numel() * oh.element_size()
+    if quant_only:
+        val, unit = (x.nbytes + oh.numel()) * n / (e_ms / 1e3) / 1e9, "GB/s"
+    else:
+        val, unit = ops * n / (e_ms / 1e3) / 1e12, "TOPS"
+    return {"value": val, "unit": unit, "steps": n, "ms": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "copy-in, compute and copy-out on three streams, two buffers each way"}
 
+
+def run_ours(args, rank, world, local):
+    """The default line: c1 (the configuration the metric is quoted on) as `value`, and, on
+    one GPU, every other config of the metric in `per_config` (c2, c3, c3q, and the 7B
+    layer at 2K-token prefill x28)."""
+    import torch
+    torch.cuda.set_device(local)
+    steps = args.steps if args.steps > 0 else 20
+    main = measure_config(args, args.workload, rank, world, local, steps)
     line = {
-        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / steps, "higher_is_better": True,
+        "metric": main["metric"], "value": main["value"], "unit": main["unit"], "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 codes (exact on f16 tensor cores), f32 scales and output",
         "data": "synthetic (seeded; 7B GQA projection shapes)",
-        "config": {"workload": wl["label"], "M": M, "N": N, "K": K, "fmt": fmt,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"rotating {copies} operand copies ({copies * set_bytes / 2**20:.0f} MiB > 3x L2)",
-                   "timing": f"CUDA graphs: {reps} replays of {G} steps" + (f" + {tail} steps" if tail else "")
-                             + "; kernel durations from one profiled replay of the step graph after the timed region"},
-        "roofline": roof,
-        "kernels": kernels,
-        "path": PATH_NAMES.get(path, "quantize"),
-        "clocks": clk,
-        "gpu_launches": int(round(launches_per_step * steps)),
+        "config": dict(main["config"], parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "tok_per_s": main["tok_per_s"],
+        "roofline": main["roofline"], "kernels": main["kernels"], "path": main["path"], "clocks": main["clocks"],
+        "gpu_launches": main["gpu_launches"],
     }
-    if e2e:
-        line["e2e"] = e2e
+    if "e2e" in main:
+        line["e2e"] = main["e2e"]
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per = {}
+        for wlname in ("c2", "c3", "c3q"):
+            if wlname != args.workload:
+                e = measure_config(args, wlname, rank, world, local, steps)
+                e.pop("gpu_launches_per_step", None)
+                per[wlname] = e
+                torch.cuda.empty_cache()
+        per["layer"] = run_layer(args)
+        line["per_config"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+        line["cpu_baseline"]["single_core"] = oracle_single_core()
     return line
 
 
@@ -507,12 +600,15 @@ def _rotating(torch, dev, arr, copies):
 
 
 def run_layer(args):
-    """28 layers x (4 activation quantizes + q, k, v, o, gate, up, down GEMMs) at M=2048, Q4_K.
-    Each layer uses its own device copy of the projection weights (the seven matrices are
-    generated once from their seeds and cloned per layer), so L2 holds none of them."""
+    """28 layers x (4 activation quantizes + q, k, v, o, gate, up, down GEMMs) at M=2048, Q4_K:
+    the metric's "7B-layer prefill ms @2K".  Each layer uses its own device copy of the
+    projection weights (the seven matrices are generated once from their seeds and cloned
+    per layer), so L2 holds none of them.  The 28 layers are one CUDA graph, replayed until
+    at least MIN_TIMED_S of device time has passed; the value is the median replay."""
     import torch
     import block_quantized_int8_mmq_gb300 as mmq
     dev = torch.device("cuda", 0)
+    peaks = load_peaks()
     M, H, F = 2048, 3584, 18944
     L = synth.LAYERS_7B
     w_host = {name: synth.layer_weights(0, name, N, K) for (name, N, K) in synth.LAYER_7B}
@@ -542,45 +638,66 @@ def run_layer(args):
         layer(l)
     torch.cuda.synchronize(dev)
     assert mmq.mmq_get_device_error(stream) == 0
-    # launches per layer, counted by the library's profiler on one untimed layer
-    mmq.mmq_profile_read(reset=True)
-    prev = mmq.mmq_profile_enable(True)
-    layer(0)
-    mmq.mmq_profile_enable(prev)
-    per_layer = sum(n for n, _ in mmq.mmq_profile_read(reset=True).values())
     # the 28 layers as one CUDA graph (a layer is ~20 launches: launched one by one the
-    # host would add gaps between them)
-    prev = mmq.mmq_profile_enable(False)
+    # host would add gaps between them); a second copy captured with the profiler on
     cap = torch.cuda.Stream(dev)
+    prev = mmq.mmq_profile_enable(False)
     cap.wait_stream(stream)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cap):
         for l in range(L):
             layer(l, stream=cap)
+    mmq.mmq_profile_read(reset=True)
+    mmq.mmq_profile_enable(True)
+    cap.wait_stream(stream)
+    prof_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(prof_graph, stream=cap):
+        for l in range(L):
+            layer(l, stream=cap)
     mmq.mmq_profile_enable(prev)
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
     graph.replay()
+    b0.record(stream)
     torch.cuda.synchronize(dev)
     assert mmq.mmq_get_device_error(stream) == 0
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(1, (args.steps if args.steps > 0 else 30) // 10)
+    reps = int(min(MAX_REPLAYS, max(MIN_REPLAYS, math.ceil(args.timed_s * 1e3 / max(a0.elapsed_time(b0), 1e-3)))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     clocks = ClockSampler(0)
+    torch.cuda.synchronize(dev)
     clocks.start()
-    a.record(stream)
-    for _ in range(reps):
+    for a, b in ev:
+        a.record(stream)
         graph.replay()
-    b.record(stream)
+        b.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     assert mmq.mmq_get_device_error(stream) == 0
-    ms = a.elapsed_time(b) / reps
-    ops = 2.0 * M * sum(N * K for (_, N, K) in synth.LAYER_7B) * L
+    all_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.median(all_ms)
+    prof_graph.replay()
+    torch.cuda.synchronize(dev)
+    prof = mmq.mmq_profile_read(reset=True)
+    kernels, per_pass = kernel_table(prof, 1)
+    gemm_ops = 2.0 * M * sum(N * K for (_, N, K) in synth.LAYER_7B) * L
+    tcx = kernels.get("k_mmq_tcx")
+    roof = None
+    if tcx:
+        t_tcx = tcx["avg_ms"] * tcx["launches_per_step"]
+        achieved = gemm_ops / (t_tcx / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None, "kernel": "k_mmq_tcx",
+                "peak_source": f"{peaks['source']} bf16 sustained (a kernel timed inside a long step)",
+                "note": "all projections' 2MNK over the summed k_mmq_tcx time of one 28-layer pass"}
     return {"metric": "7B-layer prefill ms @2K (28 layers: quantizes + Q4_K projections)", "value": ms,
-            "unit": "ms", "higher_is_better": False, "tok_per_s": M / (ms / 1e3), "tops": ops / (ms / 1e3) / 1e12,
+            "unit": "ms", "higher_is_better": False, "tok_per_s": M / (ms / 1e3), "tops": gemm_ops / (ms / 1e3) / 1e12,
             "n_gpus": 1, "steps": reps, "warmup": args.warmup, "data": "synthetic (seeded, weights cloned per layer)",
             "config": {"workload": "7B GQA layer x28 at M=2048, Q4_K (attention, norms, SiLU excluded)",
-                       "timing": "the 28 layers captured in one CUDA graph; each activation quantized once, fused "
-                                 "into its first projection"},
-            "gpu_launches": reps * L * per_layer, "clocks": clk}
+                       "timing": f"the 28 layers captured in one CUDA graph, replayed {reps} times "
+                                 f"({sum(all_ms):.0f} ms); value = the median replay ({min(all_ms):.2f} .. "
+                                 f"{max(all_ms):.2f} ms); each activation quantized once, fused into its first "
+                                 "projection"},
+            "roofline": roof, "kernels": kernels, "gpu_launches": int(round(reps * per_pass)), "clocks": clk}
 
 
 def run_decode(args):
@@ -677,7 +794,7 @@ def run_moe(args):
     ids = np.stack([rng.permutation(E)[:TOPK] for _ in range(T)]).reshape(-1).astype(np.int32)
     x = synth.activations(synth.substream(synth.BASE_SEED + 6, 2), T, K, True)
     w = synth.weights("q4_k", synth.substream(synth.BASE_SEED + 6, 3), E * N, K)
-    copies = max(2, -(-3 * L2_BYTES // w.nbytes))
+    copies = max(2, -(-3 * l2_bytes(torch, dev) // w.nbytes))
     ws = _rotating(torch, dev, w, copies)
     xq_tok = mmq.mmq_quantize_q8_1(torch.from_numpy(x).to(dev))
     xq = xq_tok.repeat_interleave(TOPK, dim=0).contiguous()  # row t*8 + s: token t (slot s)
@@ -764,7 +881,7 @@ def run_sweep(args):
         w = wcache[(fmt, proj)]
         x = synth.activations(synth.substream(synth.BASE_SEED + 4, 7000 + M), M, K, True)
         wbytes = w.nbytes
-        copies = max(2, -(-3 * L2_BYTES // (wbytes + x.nbytes)))
+        copies = max(2, -(-3 * l2_bytes(torch, dev) // (wbytes + x.nbytes)))
         ws = _rotating(torch, dev, w, copies)
         xd = torch.from_numpy(x).to(dev)
         xq = mmq.mmq_quantize_q8_1(xd)
@@ -810,11 +927,15 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s of device time)")
+    ap.add_argument("--steps", type=int, default=0, help="steps per timed replay (0: 20)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["layer", "sweep", "moe", "decode"], default="c1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="only the main workload (no per_config entries)")
+    ap.add_argument("--timed-s", type=float, default=MIN_TIMED_S,
+                    help="device time each timed region lasts at least (replays of the K-step graph); 0: %d replays"
+                         % MIN_REPLAYS)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per reference-arm step")
     ap.add_argument("--only", default="", help="sweep: run the one case fmt:M:N:K")

@@ -25,6 +25,7 @@ EXPORTED = (
     "mmq_gemm_noalloc", "mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k",
     "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
     "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k", "mmq_gemm_grouped_q5_k",
+    "mmq_debug_product_dots", "mmq_debug_refuse_smem", "mmq_debug_set_wait_limit",
 )
 
 
@@ -61,6 +62,9 @@ def _load():
         getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
     for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k", "mmq_gemm_grouped_q5_k"):
         getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
+    L.mmq_debug_product_dots.argtypes = [I, P, P, I64, I64, I64, P, P]
+    L.mmq_debug_refuse_smem.argtypes = [I]
+    L.mmq_debug_set_wait_limit.argtypes = [I64]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
     return L
@@ -88,6 +92,11 @@ def _check(fn, st):
 
 
 def _ptr(t):
+    """Device address of a contiguous CUDA tensor (the library takes raw device pointers)."""
+    if not t.is_cuda:
+        raise ValueError("libmmq takes CUDA tensors (device memory); got a tensor on " + str(t.device))
+    if not t.is_contiguous():
+        raise ValueError("libmmq takes contiguous tensors")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -173,6 +182,29 @@ def mmq_debug_block_dots_q8_0(xq, wq, M, N, K, dots=None, stream=None):
 
 def mmq_debug_block_dots_q4_k(xq, wq, M, N, K, dots=None, stream=None):
     return _dots("mmq_debug_block_dots_q4_k", xq, wq, M, N, K, dots, stream)
+
+
+def mmq_debug_product_dots(fmt, xq, wq, M, N, K, dots=None, stream=None):
+    """The integer block dots of the expanded-path contraction as it forms them (K-quants:
+    the sub-scale folded into the weight codes): int32 [M, N, K/32]."""
+    import torch
+    if dots is None:
+        dots = torch.empty((M, N, K // QK), dtype=torch.int32, device=xq.device)
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check("mmq_debug_product_dots",
+           _lib.mmq_debug_product_dots(f, _ptr(xq), _ptr(wq), M, N, K, _ptr(dots), _stream(stream)))
+    return dots
+
+
+def mmq_debug_refuse_smem(on: bool) -> bool:
+    """Test switch: treat every shared-memory limit request as refused; returns the previous state."""
+    return bool(_lib.mmq_debug_refuse_smem(1 if on else 0))
+
+
+def mmq_debug_set_wait_limit(ns: int) -> None:
+    """Test switch: the bound of the expanded-path contraction's waits for its operand copies, in
+    ns (0: give up at the first such wait whose copy has not landed; < 0: the 2 s default)."""
+    _check("mmq_debug_set_wait_limit", _lib.mmq_debug_set_wait_limit(int(ns)))
 
 
 def mmq_set_path(path: int) -> int:

@@ -29,6 +29,55 @@ int launch_status(const char* fn) {
 
 bool tc_available();
 
+DeviceShape device_shape() {
+    static std::atomic<int> sms[MAX_DEVICES], smem[MAX_DEVICES], l2[MAX_DEVICES];
+    const DeviceShape fallback{152, 233472, 132 << 20};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return fallback;
+    }
+    if (sms[dev].load() == 0) {
+        int a = 0, b = 0, c = 0;
+        if (cudaDeviceGetAttribute(&a, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&b, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&c, cudaDevAttrL2CacheSize, dev) != cudaSuccess || a <= 0) {
+            cudaGetLastError();
+            return fallback;
+        }
+        smem[dev].store(b);
+        l2[dev].store(c);
+        sms[dev].store(a);
+    }
+    DeviceShape d;
+    d.sms = sms[dev].load();
+    d.smem_per_sm = smem[dev].load();
+    d.l2_bytes = l2[dev].load();
+    return d;
+}
+
+namespace {
+std::atomic<int> g_refuse_smem{0};  // test switch: every shared-memory request is refused
+}  // namespace
+
+int ensure_smem(const void* func, int bytes, SmemAttr& a) {
+    if (g_refuse_smem.load()) return MMQ_ERR_SMEM;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return MMQ_ERR_CUDA;
+    }
+    if (a.bytes[dev].load() >= bytes) return MMQ_OK;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_SMEM;
+    }
+    int cur = a.bytes[dev].load();
+    while (cur < bytes && !a.bytes[dev].compare_exchange_weak(cur, bytes)) {
+    }
+    return MMQ_OK;
+}
+
 namespace {
 
 std::atomic<int> g_path{-1};
@@ -57,9 +106,9 @@ constexpr int64_t LIMIT = (int64_t)1 << 40;
 //   about 4.4 (Q6_K: 2.7) million weight values per microsecond, a quarter less when the
 //   weights are small (N * K below 32 M values: too little work per pass to fill the GPU);
 // - the expanded tensor-core path pays the code expansion (~0.6 us per million weight
-//   values; Q6_K, two planes: ~1.0) plus, per wave of 128 x 128 tiles (times their K
-//   splits) over the SMs, one CTA's pass over its share of K (~0.28 us per 32-block; the
-//   K-quants with mins add one min item per 8 blocks), plus fixed costs.
+//   values; Q6_K, two planes: ~1.0) plus, per wave of output tiles (times their K splits)
+//   over the SMs, one CTA's pass over its share of K (~0.28 us per 32-block of a 128-wide
+//   tile; the K-quants with mins add one min item per 8 blocks), plus fixed costs.
 // The converter kernel is never the faster of the two and is only used when asked for.
 int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
     if (M <= 8 || K % QK_K != 0 || !tc_available()) return MMQ_PATH_SMALL;
@@ -69,10 +118,10 @@ int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
     const double t_small = (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * nk / rate + 1.5;
     // with K split S ways (small outputs), S times the CTAs each take 1/S of the groups,
     // and a summing kernel follows
-    const int64_t S = tcx_splits(M, N, K), ng = K / QK_K;
-    const int64_t ctas = ((M + 127) / 128) * ((N + 127) / 128) * S;
-    const double waves = (double)((ctas + SM_COUNT - 1) / SM_COUNT);
-    const double items = (double)(8 * ((ng + S - 1) / S)) * (is_kquant(fmt) ? 9.0 / 8.0 : 1.0);
+    const int64_t S = tcx_splits(fmt, M, N, K), ng = K / QK_K, bn = tcx_tile_n(fmt, M, N), sms = device_shape().sms;
+    const int64_t ctas = ((M + 127) / 128) * ((N + bn - 1) / bn) * S;
+    const double waves = (double)((ctas + sms - 1) / sms);
+    const double items = (double)(8 * ((ng + S - 1) / S)) * (is_kquant(fmt) ? 9.0 / 8.0 : 1.0) * (double)bn / 128.0;
     const double t_expand =
         (q6 ? 1.0 : 0.6) * nk / 1e6 + 0.28 * waves * items + (q6 ? 5.0 : 8.0) + (S > 1 ? 1.0 : 0.0);
     return t_small < t_expand ? MMQ_PATH_SMALL : MMQ_PATH_EXPAND;
@@ -118,7 +167,7 @@ int contraction(const char* fn, int fmt, const void* xq, const void* wq, int64_t
     else if (path == MMQ_PATH_TC)
         st = tc_launch(fmt, xq, wq, M, N, K, out, dots, s);
     else
-        st = tcx_launch(fmt, xq, wq, M, N, K, out, dots, s);
+        st = tcx_launch(fmt, xq, wq, M, N, K, out, dots, s, false);
     if (st == MMQ_OK) t_last_path = path;
     return st;
 }
@@ -324,6 +373,34 @@ int mmq_gemm_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t
     st = tcx_launch_noalloc(fmt, xq, wq, M, N, K, out, static_cast<cudaStream_t>(stream));
     if (st == MMQ_OK) t_last_path = MMQ_PATH_EXPAND;
     return st;
+}
+
+int mmq_debug_product_dots(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,
+                           void* stream) {
+    const char* fn = "mmq_debug_product_dots";
+    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K && fmt != FMT_Q5_K && fmt != FMT_Q6_K) {
+        report(fn, MMQ_ERR_ARG, "fmt must be 0 (Q8_0), 1 (Q4_K), 2 (Q5_K) or 3 (Q6_K)");
+        return MMQ_ERR_ARG;
+    }
+    int st = check_mk(fn, M, N, K, QK_K);
+    if (st) return st;
+    if (!xq || !wq || !dots) {
+        report(fn, MMQ_ERR_NULL, "xq, wq and dots must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(dots, 16)) {
+        report(fn, MMQ_ERR_ALIGN, "xq, wq and dots must be 16-byte aligned");
+        return MMQ_ERR_ALIGN;
+    }
+    st = tcx_launch(fmt, xq, wq, M, N, K, nullptr, dots, static_cast<cudaStream_t>(stream), true);
+    if (st == MMQ_OK) t_last_path = MMQ_PATH_EXPAND;
+    return st;
+}
+
+int mmq_debug_refuse_smem(int on) { return g_refuse_smem.exchange(on ? 1 : 0); }
+
+int mmq_debug_set_wait_limit(int64_t ns) {
+    return tcx_set_wait_limit(ns >= 0 ? (unsigned long long)ns : 2000000000ull);
 }
 
 int mmq_set_path(int path) {

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mmq.h"
 
 namespace mmq {
@@ -67,14 +69,32 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
 int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
               int32_t* dots, cudaStream_t s);
 int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
-               int32_t* dots, cudaStream_t s);
+               int32_t* dots, cudaStream_t s, bool fold);
 int tcx_linear_launch(int fmt, const float* x, void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                       cudaStream_t s);
 int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                        cudaStream_t s);
-// K splits the expanded path's contraction uses for an M x N x K call (1: none)
-int tcx_splits(int64_t M, int64_t N, int64_t K);
-constexpr int SM_COUNT = 152;  // GB300: 2 dies x 76 SMs
+// K splits and tile width (weight rows) the expanded path's contraction takes for M x N x K
+int tcx_splits(int fmt, int64_t M, int64_t N, int64_t K);
+int tcx_tile_n(int fmt, int64_t M, int64_t N);
+// bound of the expanded-path contraction's pipeline waits (device value; teardown drains
+// keep their own fixed bound)
+int tcx_set_wait_limit(unsigned long long ns);
+
+constexpr int MAX_DEVICES = 64;  // per-device host caches are indexed by the device ordinal
+// SM count, shared memory per SM and L2 bytes of the current device (queried once per
+// device; GB300 values if the query fails)
+struct DeviceShape {
+    int sms = 0, smem_per_sm = 0, l2_bytes = 0;
+};
+DeviceShape device_shape();
+// A kernel's dynamic shared-memory limit, raised once per device: cudaFuncSetAttribute
+// applies to the device current when it is called.  ensure_smem returns MMQ_OK,
+// MMQ_ERR_SMEM (refused, or refused on purpose by the test switch) or MMQ_ERR_CUDA.
+struct SmemAttr {
+    std::atomic<int> bytes[MAX_DEVICES];
+};
+int ensure_smem(const void* func, int bytes, SmemAttr& a);
 int tc_grouped_launch(int fmt, const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
                       const int2* tiles, const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map,
                       float* out, cudaStream_t s);

@@ -51,6 +51,7 @@ namespace {
 
 using namespace umma;
 
+__device__ unsigned long long g_tcx_wait_limit_ns = WAIT_LIMIT_NS;
 __device__ unsigned int g_tcx_error;
 
 constexpr int BM = 128;                  // activation rows per tile (TMEM lanes)
@@ -521,6 +522,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     const int nitems = ngl * IPG;
     volatile int* abort = &s_abort;
     unsigned* err = &g_tcx_error;
+    const uint64_t limit = g_tcx_wait_limit_ns;
     auto bar = [&](int i) -> uint32_t { return sbase + L::bars + 8 * i; };
 
     if (threadIdx.x == 0) {
@@ -615,7 +617,9 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                 const bool r1 = !block || ptx::mbar_test_wait(bar(BAR_ST_FULL + s), (k / NS) & 1);
                 const bool r2 = ptx::mbar_test_wait(bar(BAR_D_EMPTY + e), (n & 1) ^ 1);
                 if (!(r1 && r2)) {
-                    if (block && !wait_bar(bar(BAR_ST_FULL + s), (k / NS) & 1, abort, err)) break;
+                    // (the one wait with the run-time bound: the test setting of 0 makes the first
+                    // item's wait for a copy just started give up)
+                    if (block && !wait_bar_bounded(bar(BAR_ST_FULL + s), (k / NS) & 1, abort, err, limit)) break;
                     if (!wait_bar(bar(BAR_D_EMPTY + e), (n & 1) ^ 1, abort, err)) break;
                 }
                 ptx::tc_fence_after();
@@ -761,11 +765,11 @@ __global__ void __launch_bounds__(256) k_splitk_sum(const float* __restrict__ pa
 // same two calls are made on the device's default pool, which the graph turns into
 // allocation and free nodes.
 std::mutex g_pool_mu;
-cudaMemPool_t g_pool[64];
-bool g_pool_tried[64];
+cudaMemPool_t g_pool[MAX_DEVICES];
+bool g_pool_tried[MAX_DEVICES];
 
 cudaMemPool_t scratch_pool(int dev) {
-    if (dev < 0 || dev >= 64) return nullptr;
+    if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
     std::lock_guard<std::mutex> lk(g_pool_mu);
     if (!g_pool_tried[dev]) {
         g_pool_tried[dev] = true;
@@ -785,17 +789,6 @@ cudaMemPool_t scratch_pool(int dev) {
     return g_pool[dev];
 }
 
-template <typename Kern>
-bool set_smem(Kern k, int bytes, bool& done) {
-    if (done) return true;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    done = true;
-    return true;
-}
-
 // Scratch bytes of one call: expanded activations, activation group data, expanded
 // weights, weight group data (each a multiple of 256 bytes), and with K splits their f32
 // partial outputs (`splits` slabs of M x N, each padded to 256 bytes).
@@ -808,7 +801,7 @@ struct ScratchPlan {
 ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K, bool allow_split = true) {
     const int64_t nb = K / QK, ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    const int splits = allow_split ? tcx_splits(M, N, K) : 1;
+    const int splits = allow_split ? tcx_splits(fmt, M, N, K) : 1;
     const long long stride = ((long long)(M * N) + 63) & ~63LL;
     return {(size_t)(MT * nb) * XCHUNK,
             (size_t)(MT * ng) * ga_bytes(fmt),
@@ -822,15 +815,16 @@ ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K, bool allow_sp
 // The two launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K) bytes): both
 // expansions, then the contraction.  x != nullptr: the activations come as f32 rows and
 // are quantized by the expansion (q8_1 bytes written to xq); else xq is the input.
-template <int FMT, bool DOTS>
+template <int FMT, bool DOTS, bool FOLD = !DOTS>
 int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
               int32_t* dots, uint8_t* ws, const ScratchPlan& sp, cudaStream_t s, const char* fn) {
     const int nb = (int)(K / QK), ng = nb / GB;
     const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    static bool attr_done = false;
-    if (!set_smem(k_mmq_tcx<FMT, DOTS>, XLayout<FMT>::alloc, attr_done)) {
-        report(fn, MMQ_ERR_SMEM, "shared-memory request refused");
-        return MMQ_ERR_SMEM;
+    static SmemAttr attr;
+    const int st_attr = ensure_smem((const void*)k_mmq_tcx<FMT, DOTS>, XLayout<FMT>::alloc, attr);
+    if (st_attr != MMQ_OK) {
+        report(fn, st_attr, "shared-memory request refused");
+        return st_attr;
     }
     uint8_t* xa = ws;
     uint8_t* ga = xa + sp.xa;
@@ -856,7 +850,7 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
             k_expand<FMT, true, true, false><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
                                                                         (int)acts_x, xa, ga, xb, gw);
         else
-            k_expand<FMT, false, !DOTS, false><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq),
+            k_expand<FMT, false, FOLD, false><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq),
                                                                           nullptr, w8, (int)M, (int)N, nb,
                                                                           (int)acts_x, xa, ga, xb, gw);
     }
@@ -890,7 +884,8 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         const long long n = (long long)M * N;
         cudaLaunchConfig_t cfg = {};
         const long long blocks = ((n >> 2) + 255) / 256;
-        cfg.gridDim = dim3((unsigned)(blocks < 1 ? 1 : blocks > 4 * SM_COUNT ? 4 * SM_COUNT : blocks));
+        const long long cap = 4LL * device_shape().sms;
+        cfg.gridDim = dim3((unsigned)(blocks < 1 ? 1 : blocks > cap ? cap : blocks));
         cfg.blockDim = dim3(256);
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
@@ -908,14 +903,14 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     return launch_status(fn);
 }
 
-template <int FMT, bool DOTS>
+template <int FMT, bool DOTS, bool FOLD = !DOTS>
 int launch_x(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
              int32_t* dots, cudaStream_t s, const char* fn) {
     void* ws = nullptr;
     const ScratchPlan sp = plan_scratch(FMT, M, N, K);
     const int st0 = scratch_alloc(sp.total(), s, &ws, fn);
     if (st0 != MMQ_OK) return st0;
-    const int st = launch_on<FMT, DOTS>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), sp, s, fn);
+    const int st = launch_on<FMT, DOTS, FOLD>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), sp, s, fn);
     scratch_free(ws, s);  // stream-ordered: after the kernels above
     return st;
 }
@@ -928,10 +923,10 @@ int launch_x(const float* x, const void* xq, const void* wq, int64_t M, int64_t 
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)64 << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 std::mutex g_noalloc_mu;
-uint8_t* g_noalloc_ptr[64];
+uint8_t* g_noalloc_ptr[MAX_DEVICES];
 
 uint8_t* noalloc_scratch(int dev) {
-    if (dev < 0 || dev >= 64) return nullptr;
+    if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
         void* p = nullptr;
@@ -983,9 +978,12 @@ void scratch_free(void* p, cudaStream_t s) {
     if (p) cudaFreeAsync(p, s);
 }
 
+// The contraction (dots == nullptr) or the block-dot test hooks: `fold` selects the
+// product's expansion (K-quant codes times their sub-scales) for the hook.
 int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out, int32_t* dots,
-               cudaStream_t s) {
-    const char* fn = fmt == FMT_Q8_0   ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
+               cudaStream_t s, bool fold) {
+    const char* fn = dots && fold           ? "mmq_debug_product_dots"
+                     : fmt == FMT_Q8_0   ? (dots ? "mmq_debug_block_dots_q8_0" : "mmq_gemm_q8_0")
                      : fmt == FMT_Q5_K ? (dots ? "mmq_debug_block_dots_q5_k" : "mmq_gemm_q5_k")
                      : fmt == FMT_Q6_K ? (dots ? "mmq_debug_block_dots_q6_k" : "mmq_gemm_q6_k")
                                        : (dots ? "mmq_debug_block_dots_q4_k" : "mmq_gemm_q4_k");
@@ -997,6 +995,11 @@ int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, in
         report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
         return MMQ_ERR_SHAPE;
     }
+    if (dots && fold)
+        return fmt == FMT_Q8_0   ? launch_x<FMT_Q8_0, true, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+               : fmt == FMT_Q5_K ? launch_x<FMT_Q5_K, true, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+               : fmt == FMT_Q6_K ? launch_x<FMT_Q6_K, true, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
+                                 : launch_x<FMT_Q4_K, true, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
     if (fmt == FMT_Q8_0)
         return dots ? launch_x<FMT_Q8_0, true>(nullptr, xq, wq, M, N, K, out, dots, s, fn)
                     : launch_x<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, dots, s, fn);
@@ -1066,13 +1069,23 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
 
 // K splits of the contraction: only when the output has fewer 128 x 128 tiles than there
 // are SMs, as many as fill the SMs once (at most 8), each at least two 256-value groups.
-int tcx_splits(int64_t M, int64_t N, int64_t K) {
+int tcx_splits(int fmt, int64_t M, int64_t N, int64_t K) {
+    (void)fmt;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t ng = K / QK_K;
-    int64_t sp = SM_COUNT / (tiles < 1 ? 1 : tiles);
+    int64_t sp = device_shape().sms / (tiles < 1 ? 1 : tiles);
     if (sp > ng / 2) sp = ng / 2;
     if (sp > 8) sp = 8;
     return sp < 1 ? 1 : (int)sp;
+}
+
+int tcx_tile_n(int fmt, int64_t M, int64_t N) {
+    (void)fmt, (void)M, (void)N;
+    return BN;
+}
+
+int tcx_set_wait_limit(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_tcx_wait_limit_ns, &ns, sizeof(ns)) == cudaSuccess ? MMQ_OK : MMQ_ERR_CUDA;
 }
 
 unsigned tcx_take_error() {

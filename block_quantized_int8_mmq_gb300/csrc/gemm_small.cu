@@ -731,43 +731,17 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
     }
 }
 
-// SM count and shared memory per SM of the current device (cached per device)
-struct DeviceShape {
-    int sms = 0, smem_per_sm = 0;
-};
-DeviceShape device_shape() {
-    static DeviceShape cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        return DeviceShape{152, 233472};
-    }
-    if (cache[dev].sms == 0) {
-        DeviceShape d;
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return DeviceShape{152, 233472};
-        }
-        cache[dev] = d;
-    }
-    return cache[dev];
-}
-
 template <int FMT, int MT, int S>
 int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                          int32_t* dots, cudaStream_t s, const char* fn) {
     const int smem = ds_smem_bytes(FMT, MT, S, nb);
-    static int attr_bytes = 0;
-    if (smem > 48 * 1024 && smem > attr_bytes) {
-        cudaError_t e =
-            cudaFuncSetAttribute(k_mmq_dp4a_stream<FMT, MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
-            return MMQ_ERR_SMEM;
+    static SmemAttr attr;
+    if (smem > 48 * 1024) {
+        const int e = ensure_smem((const void*)k_mmq_dp4a_stream<FMT, MT, S>, smem, attr);
+        if (e != MMQ_OK) {
+            report(fn, e, "shared-memory request refused");
+            return e;
         }
-        attr_bytes = smem;
     }
     // every CTA resident at once (as many per SM as the launch bounds and shared memory
     // allow), and the rows dealt out evenly: rows per warp = ceil(N / warps that fit),
@@ -1068,16 +1042,13 @@ int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
     int64_t tpc = (ntiles + 2 * (int64_t)dsh.sms - 1) / (2 * (int64_t)dsh.sms);
     tpc = tpc < 1 ? 1 : (tpc > IS_MAX_TPC ? IS_MAX_TPC : tpc);
     const int smem = is_smem_bytes(FMT, (int)tpc);
-    static int attr_bytes = 0;
-    if (smem > 48 * 1024 && smem > attr_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_i8_stream<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             is_smem_bytes(FMT, IS_MAX_TPC));
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
-            return MMQ_ERR_SMEM;
+    static SmemAttr attr;
+    if (smem > 48 * 1024) {
+        const int e = ensure_smem((const void*)k_mmq_i8_stream<FMT>, is_smem_bytes(FMT, IS_MAX_TPC), attr);
+        if (e != MMQ_OK) {
+            report(fn, e, "shared-memory request refused");
+            return e;
         }
-        attr_bytes = is_smem_bytes(FMT, IS_MAX_TPC);
     }
     CUtensorMap tm;
     const uint64_t row_bytes = FMT == FMT_Q8_0 ? (uint64_t)nb * Q8_0_BYTES : (uint64_t)(nb / 8) * kq_bytes(FMT);

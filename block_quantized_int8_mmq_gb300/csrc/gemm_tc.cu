@@ -393,15 +393,11 @@ int launch_t(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, fl
         return MMQ_ERR_CUDA;
     }
     const int smem = Layout<FMT>::alloc;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_tc<FMT, DOTS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
-            return MMQ_ERR_SMEM;
-        }
-        attr_done = true;
+    static SmemAttr attr;
+    const int e_attr = ensure_smem((const void*)k_mmq_tc<FMT, DOTS, false>, smem, attr);
+    if (e_attr != MMQ_OK) {
+        report(fn, e_attr, "shared-memory request refused");
+        return e_attr;
     }
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
     {
@@ -428,15 +424,11 @@ int launch_grouped_t(const void* xs, const void* wq, int64_t R, int64_t E, int64
         return MMQ_ERR_CUDA;
     }
     const int smem = Layout<FMT>::alloc;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq_tc<FMT, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            report(fn, MMQ_ERR_SMEM, cudaGetErrorString(e));
-            return MMQ_ERR_SMEM;
-        }
-        attr_done = true;
+    static SmemAttr attr;
+    const int e_attr = ensure_smem((const void*)k_mmq_tc<FMT, false, true>, smem, attr);
+    if (e_attr != MMQ_OK) {
+        report(fn, e_attr, "shared-memory request refused");
+        return e_attr;
     }
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)max_tiles);
     {

@@ -74,6 +74,31 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// As wait_bar, with a run-time bound (a device variable the caller has read): for one
+// slow-path wait only, so that the hot waits keep their compile-time bound.  A bound of 0
+// (a test setting) gives up at once if the phase is not already complete.
+__device__ __forceinline__ bool wait_bar_bounded(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* err,
+                                                 uint64_t limit_ns) {
+    if (limit_ns == 0 && !ptx::mbar_test_wait(bar, parity)) {
+        atomicOr(err, ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+    }
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort) return false;
+            if (ptx::globaltimer_ns() - t0 > limit_ns) {
+                atomicOr(err, ERR_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Teardown wait: bounded by time only (used to drain in-flight copies and MMAs).
 static __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned* err) {
     const uint64_t t0 = ptx::globaltimer_ns();

@@ -105,8 +105,9 @@ const char* mmq_status_string(int status);
  * or a size is negative. */
 size_t mmq_q8_1_bytes(int64_t M, int64_t K);
 
-/* Bytes of one weight row of K values: K/32*34 (Q8_0) or K/256*144 (Q4_K).
- * fmt: 0 = Q8_0, 1 = Q4_K.  0 for an invalid fmt or K. */
+/* Bytes of one weight row of K values: K/32*34 (Q8_0), K/256*144 (Q4_K), K/256*176
+ * (Q5_K) or K/256*210 (Q6_K).  fmt: 0 = Q8_0, 1 = Q4_K, 2 = Q5_K, 3 = Q6_K.  0 for an
+ * invalid fmt, or a K that is not a multiple of 32 (Q8_0) or 256 (the others). */
 size_t mmq_weight_row_bytes(int fmt, int64_t K);
 
 /*
@@ -114,7 +115,8 @@ size_t mmq_weight_row_bytes(int fmt, int64_t K);
  * quantize pass: block amax, scale, round, clamp, block sum; the q8_1 block keeps the
  * f16 scale and the f16 block sum s = d * sum(q)).
  *   x:  f32 [M][K] row-major, 16-byte aligned.
- *   xq: output, mmq_q8_1_bytes(M, K) bytes, 4-byte aligned.
+ *   xq: output, mmq_q8_1_bytes(M, K) bytes, 4-byte aligned (this call); the contraction
+ *       and mmq_linear_* calls that take xq need it 16-byte aligned.
  * Bit-exact: the same bytes as the definition evaluated with IEEE f32 arithmetic.
  * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE (K % 32), MMQ_ERR_NULL, MMQ_ERR_ALIGN,
  * MMQ_ERR_LAUNCH.
@@ -211,12 +213,18 @@ int mmq_gemm_grouped_q5_k(const void* xq, const int32_t* row_expert, int64_t R, 
                           int64_t K, float* out, void* stream);
 
 /*
- * Test hook: the per-block int32 dots D[m][n][b] (b < K/32) computed by the SAME data
- * path as mmq_gemm_q8_0 / mmq_gemm_q4_k select for this M (same staging, same
- * conversion, same MMA), written out instead of rescaled.  For Q4_K, D is the dot of
- * the activation codes with the raw 4-bit codes (0..15), without sc_j; for Q5_K, with
- * the raw 5-bit codes (0..31).  For Q6_K, whose scale changes inside a block, D is the
- * block's integer sum of xq * (q - 32) * sc (the D of mmq_gemm_q6_k; |D| < 2^24).
+ * Test hook: the per-block int32 dots D[m][n][b] (b < K/32) of the integer block sums of
+ * the method ("When the Product Won't Collapse", sec. "The obstruction": the exact integer
+ * sum of one constant-scale block), from the contraction kernel that mmq_gemm_q8_0 /
+ * mmq_gemm_q4_k / mmq_gemm_q5_k / mmq_gemm_q6_k select for this M on the current path,
+ * written out instead of rescaled.  Q8_0: D = sum xq*wq, the product's own dot on every
+ * path.  Q4_K and Q5_K: D is the dot of the activation codes with the RAW weight codes
+ * (0..15, 0..31), without the sub-scale sc_j: on the small-M and converter paths this is
+ * the product's own dot (the kernels apply sc_j after it); the expanded-code path folds
+ * sc_j into its weight codes, so here it runs the same contraction kernel on an expansion
+ * of the raw codes, and mmq_debug_product_dots gives its folded dot.  Q6_K, whose scale
+ * changes inside a block: D = the block's integer sum of xq * (q - 32) * sc (the D of
+ * mmq_gemm_q6_k; |D| < 2^24), on every path.
  *   dots: int32 [M][N][K/32], 16-byte aligned.  Bit-exact by definition.
  */
 int mmq_debug_block_dots_q8_0(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
@@ -227,6 +235,42 @@ int mmq_debug_block_dots_q5_k(const void* xq, const void* wq, int64_t M, int64_t
                               int32_t* dots, void* stream);
 int mmq_debug_block_dots_q6_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t K,
                               int32_t* dots, void* stream);
+
+/*
+ * Test hook: the integer block dots exactly as the expanded-code tensor-core contraction
+ * (MMQ_PATH_EXPAND) forms them for its own arithmetic: the product's expansion, the
+ * product's contraction kernel and MMAs, with D written out instead of rescaled.
+ * fmt 0 (Q8_0): D = sum xq * wq.  fmt 1 (Q4_K) and 2 (Q5_K): D = sum xq * (q * sc_j), the
+ * sub-scale of the block's sub-block folded into the weight codes (|D| <= 32*127*31*63).
+ * fmt 3 (Q6_K): as mmq_debug_block_dots_q6_k.  The same integer sums the method defines
+ * ("When the Product Won't Collapse", sec. "The obstruction"), times sc_j for the
+ * K-quants; bit-exact.  Always runs the expanded path, whatever mmq_set_path says.
+ *   dots: int32 [M][N][K/32], 16-byte aligned.  K % 256 == 0.
+ * Errors: MMQ_ERR_ARG (fmt), MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE, MMQ_ERR_NULL,
+ * MMQ_ERR_ALIGN, MMQ_ERR_SMEM, MMQ_ERR_NOMEM, MMQ_ERR_LAUNCH.
+ */
+int mmq_debug_product_dots(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, int32_t* dots,
+                           void* stream);
+
+/*
+ * Test hooks for the two failure statuses a correct call never produces ("13 . r7-r8
+ * raw-byte MMQ kernel", sec. 3.3: a launch that silently did nothing was timed as a
+ * speed-up; every failure must come back as a status).
+ *  - mmq_debug_refuse_smem(on): while on, every request to raise a kernel's shared-memory
+ *    limit is treated as refused, so the calls that need one return MMQ_ERR_SMEM and
+ *    launch nothing (MMQ_PATH_EXPAND and MMQ_PATH_TC always need one).  Returns the
+ *    previous setting (0 or 1).  Process-wide.
+ *  - mmq_debug_set_wait_limit(ns): the wall-time bound of the expanded-path contraction
+ *    kernel's waits for its operand copies (default 2 s, the bound of every other wait;
+ *    ns < 0 restores it; 0 gives up at the first such wait whose copy has not already
+ *    landed).  A wait that runs out sets the kernel's device error word (read by
+ *    mmq_get_device_error as MMQ_ERR_TIMEOUT); the kernel then stops its pipeline, lets
+ *    its in-flight copies and MMAs finish (those drains keep the default bound), releases
+ *    its tensor memory and exits without storing.  Returns MMQ_OK or MMQ_ERR_CUDA.
+ *    Applies to the current device.
+ */
+int mmq_debug_refuse_smem(int on);
+int mmq_debug_set_wait_limit(int64_t ns);
 
 /*
  * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1), mmq_gemm_q5_k (fmt 2)

@@ -156,8 +156,9 @@ def test_hand_example_q4_k_super_block(golden_hand):
                       [as_ints(g["e3_nibble"])[0]] * 256)
     dots = oracle.block_dots("q4_k", xq, blk[None, :], 1, 1, 256)
     assert (dots == as_ints(g["e3_dot"])[0]).all()
-    out, _ = oracle.gemm("q4_k", xq, blk[None, :], 1, 1, 256)
+    out, norm = oracle.gemm("q4_k", xq, blk[None, :], 1, 1, 256)
     assert out[0, 0] == as_floats(g["e3_out"])[0]
+    assert norm[0, 0] == as_floats(g["e3_norm"])[0]
 
 
 def test_hand_example_q5_k_super_block(golden_hand):
@@ -171,8 +172,9 @@ def test_hand_example_q5_k_super_block(golden_hand):
     assert np.array_equal(blk[4:16], np.array(as_ints(g["e3_scale_bytes"]), dtype=np.uint8))
     dots = oracle.block_dots("q5_k", xq, blk[None, :], 1, 1, 256)
     assert dots.reshape(8).tolist() == as_ints(g["e6_dots"])
-    out, _ = oracle.gemm("q5_k", xq, blk[None, :], 1, 1, 256)
+    out, norm = oracle.gemm("q5_k", xq, blk[None, :], 1, 1, 256)
     assert out[0, 0] == as_floats(g["e6_out"])[0]
+    assert norm[0, 0] == as_floats(g["e6_norm"])[0]
 
 
 def test_hand_example_q6_k_super_block(golden_hand):

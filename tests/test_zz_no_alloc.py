@@ -6,6 +6,10 @@ same fixed scratch; each result must equal, bit for bit, the allocating entry po
 the same expanded-code path, and both must be within the parity tolerance of the oracle.
 """
 import ctypes
+import json
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -79,3 +83,47 @@ def test_refuses_shapes_beyond_the_fixed_scratch(mmq):
     assert st == -9
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
+
+
+# Run in a fresh process so that nothing earlier has grown a memory pool: with the CUDA
+# modules loaded eagerly (the fixed scratch array is part of the library's module image),
+# every tensor created first, free device memory is read before the first no-allocation
+# call and after two rounds of calls over every case, the split-K shape (q4_k 300 x 520 x
+# 1024, K split in two) included.  A call that allocated device memory, from the library's
+# pool or any other, would leave less free memory behind.
+CHILD = r"""
+import json, sys
+import numpy as np
+import torch
+sys.path.insert(0, ROOT)
+import block_quantized_int8_mmq_gb300 as mmq
+import synth
+cases = CASES
+ops = []
+for fmt, M, N, K, seed in cases:
+    x = torch.from_numpy(synth.activations(seed, M, K, True)).cuda()
+    w = torch.from_numpy(synth.weights(fmt, seed + 100, N, K)).cuda()
+    ops.append((fmt, M, N, K, mmq.mmq_quantize_q8_1(x), w, torch.empty((M, N), device="cuda")))
+torch.cuda.synchronize()
+free0 = torch.cuda.mem_get_info()[0]
+for _ in range(2):
+    for fmt, M, N, K, xq, w, out in ops:
+        mmq.mmq_gemm_noalloc(fmt, xq, w, M, N, K, out=out)
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+print(json.dumps({"free0": free0, "free1": free1, "err": mmq.mmq_get_device_error(),
+                  "finite": bool(all(torch.isfinite(o[6]).all().item() for o in ops))}))
+"""
+
+
+def test_calls_allocate_no_device_memory():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = CHILD.replace("ROOT", repr(root)).replace("CASES", repr(CASES))
+    env = dict(os.environ, CUDA_MODULE_LOADING="EAGER")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["err"] == 0 and res["finite"]
+    assert res["free1"] >= res["free0"], f"free device memory fell by {res['free0'] - res['free1']} bytes"
