@@ -867,6 +867,10 @@ def run_sweep(args):
         cases += [(fmt, M, 18944, 3584, "gate") for M in (16, 32, 64)]
     # tens to hundreds of rows on the long-K projection: few output tiles, K split
     cases += [("q4_k", M, 3584, 18944, "down") for M in (64, 128, 256)]
+    # three or four rows around 4864 weight rows (two 16-row tiles per SM), where the
+    # automatic small-M choice changes kernel for the K-quants
+    for fmt in ("q4_k", "q5_k"):
+        cases += [(fmt, M, N, 3584, "wide") for N in (4096, 4864, 5632) for M in (3, 4)]
     if args.only:  # one case, "fmt:M:N:K" (for profiling a single kernel)
         f, m, n, k = args.only.split(":")
         cases = [c for c in cases if c[:4] == (f, int(m), int(n), int(k))]
@@ -874,54 +878,77 @@ def run_sweep(args):
             raise SystemExit(f"--only {args.only}: not a sweep case")
     wcache = {}
     for (fmt, M, N, K, proj) in cases:
-        if (fmt, proj) not in wcache:
+        if (fmt, proj, N) not in wcache:
             wcache.clear()
-            wcache[(fmt, proj)] = (synth.layer_weights(0, proj, N, K) if fmt == "q4_k"
-                                   else synth.weights(fmt, synth.substream(synth.BASE_SEED + 5, N + K), N, K))
-        w = wcache[(fmt, proj)]
-        x = synth.activations(synth.substream(synth.BASE_SEED + 4, 7000 + M), M, K, True)
-        wbytes = w.nbytes
-        copies = max(2, -(-3 * l2_bytes(torch, dev) // (wbytes + x.nbytes)))
-        ws = _rotating(torch, dev, w, copies)
-        xd = torch.from_numpy(x).to(dev)
-        xq = mmq.mmq_quantize_q8_1(xd)
-        out = torch.empty((M, N), device=dev)
-        stream = torch.cuda.current_stream(dev)
-        iters = max(20, args.steps)
-        for i in range(args.warmup):
-            mmq.gemm(fmt, xq, ws[i % copies], M, N, K, out, stream)
-        torch.cuda.synchronize(dev)
-        path = mmq.mmq_last_path()
-        # the timed launches are captured in one CUDA graph, so the gaps between
-        # back-to-back launches (comparable to a small-M kernel) are not counted
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(iters):
-                mmq.gemm(fmt, xq, ws[i % copies], M, N, K, out)
-        graph.replay()
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        assert mmq.mmq_get_device_error(stream) == 0
-        ms = a.elapsed_time(b) / iters
-        ops = 2.0 * M * N * K
-        abytes = wbytes + xq.numel() + M * N * 4
-        gbs = abytes / (ms / 1e3) / 1e9
-        tops = ops / (ms / 1e3) / 1e12
-        lines.append({"fmt": fmt, "M": M, "N": N, "K": K, "ms": ms, "tops": tops, "gbs": gbs,
-                      "tok_per_s": M / (ms / 1e3), "path": PATH_NAMES.get(path, "?"),
-                      "frac_hbm": gbs / peaks["hbm_gbs"], "frac_tensor": tops / peaks["bf16_tflops"],
-                      "algorithmic_bytes": abytes})
-        del ws
+            wcache[(fmt, proj, N)] = (synth.layer_weights(0, proj, N, K) if fmt == "q4_k" and proj != "wide"
+                                      else synth.weights(fmt, synth.substream(synth.BASE_SEED + 5, N + K), N, K))
+        w = wcache[(fmt, proj, N)]
+        # up to eight rows of a K % 256 == 0 weight (not Q6_K): each small-M kernel that can
+        # take the shape, besides the automatic choice
+        routes = [("auto", mmq.SMALL_ROUTE_AUTO)]
+        if M <= 8 and fmt != "q6_k" and K % 256 == 0:
+            routes += ([("dp4a", mmq.SMALL_ROUTE_DP4A)] if M <= 4 else []) + [("mma", mmq.SMALL_ROUTE_MMA)]
+        for (route_name, route) in routes:
+            mmq.mmq_debug_small_route(route)
+            try:
+                lines.append(_sweep_line(mmq, torch, dev, peaks, fmt, M, N, K, w, args, route_name))
+            finally:
+                mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_AUTO)
     return {"metric": "MMQ M sweep (GEMM only)", "unit": "mixed", "lines": lines,
             "data": "synthetic (seeded)", "peaks": peaks,
             "config": {"workload": "3584x3584 Q4_K projection, M in " + str(synth.M_SWEEP)
                                    + "; M in [1, 2, 4, 8] on 18944x3584 and 3584x18944, Q4_K, Q8_0, Q5_K"
-                                   + " and Q6_K; Q5_K and Q6_K 3584x3584 at M = 512, 2048",
+                                   + " and Q6_K; Q5_K and Q6_K 3584x3584 at M = 512, 2048; Q4_K and Q5_K"
+                                   + " M = 3, 4 on N = 4096, 4864, 5632 (K = 3584); up to 8 rows: every"
+                                   + " small-M kernel that takes the shape (route) besides the automatic one",
                        "l2": "rotating weight copies >= 3x L2", "cuda_graph": True}}
+
+
+def _sweep_line(mmq, torch, dev, peaks, fmt, M, N, K, w, args, route_name):
+    """One sweep case: the GEMM alone, replayed from a CUDA graph, timed by CUDA events."""
+    x = synth.activations(synth.substream(synth.BASE_SEED + 4, 7000 + M), M, K, True)
+    wbytes = w.nbytes
+    copies = max(2, -(-3 * l2_bytes(torch, dev) // (wbytes + x.nbytes)))
+    ws = _rotating(torch, dev, w, copies)
+    xd = torch.from_numpy(x).to(dev)
+    xq = mmq.mmq_quantize_q8_1(xd)
+    out = torch.empty((M, N), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    iters = max(20, args.steps)
+    prev_prof = mmq.mmq_profile_enable(True)
+    mmq.mmq_profile_read(reset=True)
+    mmq.gemm(fmt, xq, ws[0], M, N, K, out, stream)
+    torch.cuda.synchronize(dev)
+    kernels = sorted(mmq.mmq_profile_read(reset=True))
+    mmq.mmq_profile_enable(prev_prof)
+    for i in range(args.warmup):
+        mmq.gemm(fmt, xq, ws[i % copies], M, N, K, out, stream)
+    torch.cuda.synchronize(dev)
+    path = mmq.mmq_last_path()
+    # the timed launches are captured in one CUDA graph, so the gaps between
+    # back-to-back launches (comparable to a small-M kernel) are not counted
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(iters):
+            mmq.gemm(fmt, xq, ws[i % copies], M, N, K, out)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    assert mmq.mmq_get_device_error(stream) == 0
+    ms = a.elapsed_time(b) / iters
+    ops = 2.0 * M * N * K
+    abytes = wbytes + xq.numel() + M * N * 4
+    gbs = abytes / (ms / 1e3) / 1e9
+    tops = ops / (ms / 1e3) / 1e12
+    del ws
+    return {"fmt": fmt, "M": M, "N": N, "K": K, "ms": ms, "tops": tops, "gbs": gbs,
+            "tok_per_s": M / (ms / 1e3), "path": PATH_NAMES.get(path, "?"), "route": route_name,
+            "kernels": kernels, "frac_hbm": gbs / peaks["hbm_gbs"], "frac_tensor": tops / peaks["bf16_tflops"],
+            "algorithmic_bytes": abytes}
 
 
 def main():

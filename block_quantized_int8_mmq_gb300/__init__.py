@@ -26,6 +26,7 @@ EXPORTED = (
     "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
     "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k", "mmq_gemm_grouped_q5_k",
     "mmq_debug_product_dots", "mmq_debug_refuse_smem", "mmq_debug_set_wait_limit",
+    "mmq_debug_small_route",
 )
 
 
@@ -64,6 +65,7 @@ def _load():
         getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
     L.mmq_debug_product_dots.argtypes = [I, P, P, I64, I64, I64, P, P]
     L.mmq_debug_refuse_smem.argtypes = [I]
+    L.mmq_debug_small_route.argtypes = [I]
     L.mmq_debug_set_wait_limit.argtypes = [I64]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
@@ -205,6 +207,18 @@ def mmq_debug_set_wait_limit(ns: int) -> None:
     """Test switch: the bound of the expanded-path contraction's waits for its operand copies, in
     ns (0: give up at the first such wait whose copy has not landed; < 0: the 2 s default)."""
     _check("mmq_debug_set_wait_limit", _lib.mmq_debug_set_wait_limit(int(ns)))
+
+
+SMALL_ROUTE_AUTO, SMALL_ROUTE_DP4A, SMALL_ROUTE_MMA = 0, 1, 2
+
+
+def mmq_debug_small_route(route: int) -> int:
+    """Which small-M kernel takes K % 256 == 0 shapes (0 measured choice, 1 dp4a stream up to four
+    rows, 2 tensor-core stream); returns the previous setting."""
+    prev = _lib.mmq_debug_small_route(int(route))
+    if prev < 0:
+        raise MMQError("mmq_debug_small_route", prev)
+    return prev
 
 
 def mmq_set_path(path: int) -> int:

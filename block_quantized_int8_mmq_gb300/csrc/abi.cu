@@ -399,6 +399,11 @@ int mmq_debug_product_dots(int fmt, const void* xq, const void* wq, int64_t M, i
 
 int mmq_debug_refuse_smem(int on) { return g_refuse_smem.exchange(on ? 1 : 0); }
 
+int mmq_debug_small_route(int route) {
+    if (route < SMALL_ROUTE_AUTO || route > SMALL_ROUTE_MMA) return MMQ_ERR_ARG;
+    return small_set_route(route);
+}
+
 int mmq_debug_set_wait_limit(int64_t ns) {
     return tcx_set_wait_limit(ns >= 0 ? (unsigned long long)ns : 2000000000ull);
 }

@@ -772,34 +772,58 @@ int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
     return launch_dp4a_stream_s<FMT, 4, 4>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
-// ---------------------------------------------------------------- int8 tensor-core stream
-// k_mmq_i8_stream: up to 8 activation rows (one pass; grid.y = ceil(M/8) passes) on the
-// int8 tensor cores with the pages' instruction, mma.sync m16n8k32 s8 x s8 -> s32 ("When the
-// Product Won't Collapse", sec. "The obstruction": one exact integer dot per 32-block; "13 .
-// r7-r8 raw-byte MMQ kernel", sec. 2): 16 weight rows x 8 tokens x one whole 32-block per
-// instruction, the raw codes as operands (Q8_0 codes as they are, Q4_K nibbles masked to
-// bytes 0..15), no conversion.  A CTA owns `tpc` consecutive 16-row tiles; its 8 warps split
-// each tile's K round-robin in pieces (warp w takes pieces w, w + 8, ...), a piece being 16
-// rows x one Q4_K super-block (2304 B) or x 8 Q8_0 blocks (4352 B), brought by one 2-D tensor
-// copy into the warp's own ring (rows past N arrive as zeros).  The activation codes (B
-// fragments) and scales are read from global memory (L2-resident q8_1 rows); k is permuted
+// ---------------------------------------------------------------- tensor-core streams
+// Two kernels for up to 8 activation rows per pass (grid.y = ceil(M/8) passes), both on the
+// tensor cores through mma.sync m16n8k32 ("When the Product Won't Collapse", sec. "The
+// obstruction": one exact integer dot per 32-block; "13 . r7-r8 raw-byte MMQ kernel", sec.
+// 2): 16 weight rows x 8 tokens x one whole 32-block per instruction, from the raw codes.
+//   k_mmq_i8_stream  Q8_0: s8 x s8 -> s32 on the codes as they are;
+//   k_mmq_kq_stream  Q4_K, Q5_K: e4m3 x e4m3 -> f32 (the fp8 form runs about twenty times
+//                    the int8 form's rate here, and is exact on these operands, below).
+// Common structure.  A CTA owns `tpc` consecutive 16-row tiles; its 8 warps split each
+// tile's K round-robin in pieces (warp w takes pieces w, w + 8, ...), a piece being 16 rows
+// x one super-block (2304 / 2816 B) or x 8 Q8_0 blocks (4352 B), brought by one 2-D tensor
+// copy into the warp's own ring (rows past N arrive as zeros).  The piece's activations (8
+// q8_1 rows x its 8 blocks, 2304 B; rows past M arrive as zeros) come by one more tensor
+// copy into the warp's activation slot and serve all of the CTA's tiles.  k is permuted
 // identically in A and B (a thread's 8 values of a block are 8 contiguous bytes), which
-// leaves every block dot unchanged.  Each block's int32 dots are rescaled in registers at
-// once (Q4_K: per super-block, sum_j sc_j*xd*D_j and sum_j m_j*xs, then d and -dmin); the
-// warps' partial sums of a tile meet in shared memory at the end.  Needs K % 256 == 0.
+// leaves every block dot unchanged.  The block dots are rescaled in registers as they come,
+// in packed f32 pairs; the warps' partial sums of a tile meet in shared memory at the end,
+// in each warp's weight ring (every copy into it consumed by then).  Needs K % 256 == 0.
 constexpr int IS_WARPS = 8;
-
-__host__ __device__ constexpr int is_row_bytes(int fmt) { return is_kquant(fmt) ? kq_bytes(fmt) : 8 * Q8_0_BYTES; }
-__host__ __device__ constexpr int is_slot_bytes(int fmt) { return 16 * is_row_bytes(fmt); }  // 2304 / 4352
-__host__ __device__ constexpr int is_slots(int fmt) { return is_kquant(fmt) ? 4 : 2; }
-__host__ __device__ constexpr int is_smem_bytes(int fmt, int tpc) {
-    return IS_WARPS * is_slots(fmt) * (is_slot_bytes(fmt) + 8) + tpc * IS_WARPS * 16 * 8 * 4;
-}
+constexpr int IS_XROW = 8 * Q8_1_BYTES;  // one activation row's 8 blocks: 288 B
+constexpr int IS_ASLOT = 8 * IS_XROW;    // a piece's activations, 8 rows: 2304 B
 constexpr int IS_MAX_TPC = 4;
-static_assert(is_smem_bytes(FMT_Q8_0, IS_MAX_TPC) <= 110 * 1024 && is_smem_bytes(FMT_Q5_K, IS_MAX_TPC) <= 110 * 1024 &&
-                  is_slot_bytes(FMT_Q4_K) % 128 == 0 && is_slot_bytes(FMT_Q5_K) % 128 == 0 &&
-                  is_slot_bytes(FMT_Q8_0) % 128 == 0,
-              "two CTAs per SM; 128-byte aligned slots");
+constexpr int IS_MAGIC = 0x4B400000;                                 // bit pattern of 1.5 * 2^23
+constexpr unsigned long long IS_NEG_MAGIC2 = 0xCB400000CB400000ull;  // (-1.5 * 2^23, -1.5 * 2^23)
+constexpr unsigned long long IS_NEG_2P23 = 0xCB000000CB000000ull;    // (-2^23, -2^23)
+
+// (a, b) as an exact f32 pair, for |a|, |b| < 2^22: an int32 v added to the bit pattern of
+// 1.5 * 2^23 is the float 1.5 * 2^23 + v, and subtracting 1.5 * 2^23 leaves v exactly
+// (no integer-to-float converter)
+__device__ __forceinline__ unsigned long long is_exact2(int a, int b) {
+    return ptx::add_f32x2(ptx::f2_bits(__int_as_float(a + IS_MAGIC), __int_as_float(b + IS_MAGIC)), IS_NEG_MAGIC2);
+}
+__device__ __forceinline__ unsigned long long is_splat2(float v) { return ptx::f2_bits(v, v); }
+// an f16 pair as an f32 pair
+__device__ __forceinline__ unsigned long long is_xd2(uint32_t h2) {
+    return ptx::f2_bits(f16_bits_to_f32(h2), f16_bits_to_f32(h2 >> 16));
+}
+// byte u of wa and of wb (0..255) as an exact f32 pair: each byte in the low mantissa bits
+// of 2^23, then 2^23 subtracted
+__device__ __forceinline__ unsigned long long is_bytes2(uint32_t wa, uint32_t wb, int u) {
+    return ptx::add_f32x2(ptx::f2_bits(__uint_as_float(__byte_perm(wa, 0x4B000000u, 0x7440 + u)),
+                                       __uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7440 + u))),
+                          IS_NEG_2P23);
+}
+// two bytes of w (0..63, picked by sel) as an exact f16 pair: with 0x64 above it a byte b is
+// the f16 1024 + b, and 1024 is subtracted
+__device__ __forceinline__ uint32_t is_byte_pair_f16(uint32_t w, uint32_t sel) {
+    const uint32_t h = __byte_perm(w, 0x64646464u, sel);
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0x64006400u));
+    return d;
+}
 
 __device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                              uint32_t b0, uint32_t b1) {
@@ -809,79 +833,134 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t 
         : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
 }
+// 16 x 8 x 32, e4m3 operands, f32 accumulation: from zero, and in place
+__device__ __forceinline__ void mma_e4m3_16832_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// 16 x 8 x 8, f16 operands, f32 result from zero: rows g / g + 8 x columns 2q, 2q + 1 in d
+__device__ __forceinline__ void mma_f16_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%7, %7, %7, %7};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0), "f"(0.f));
+}
 
-template <int FMT>
+// Per-warp pipeline bookkeeping shared by both kernels: the weight ring's copy schedule
+// (piece-major: a piece's activations serve all the CTA's tiles) without divisions.
+struct IsSchedule {
+    int k, tl;  // piece and tile of the next copy to issue
+};
+
+// ------------------------------------------ Q8_0: k_mmq_i8_stream
+// Two weight slots and two activation slots per warp.  A thread loads its piece's codes
+// (B) and the f16 xd of its two tokens into registers once per piece.  Each dot D (|D| <=
+// 32 * 127 * 128 < 2^22) is made an exact f32 as above and accumulated as acc += (d_w * xd)
+// * D, one pair per weight row and the thread's two tokens.
+constexpr int I8_SLOTS = 2, I8_ASLOTS = 2;
+constexpr int I8_SLOT = 16 * 8 * Q8_0_BYTES;  // 4352
+constexpr int I8_WARP_BYTES = I8_SLOTS * I8_SLOT + I8_ASLOTS * IS_ASLOT;
+constexpr int I8_SMEM = IS_WARPS * (I8_WARP_BYTES + 8 * (I8_SLOTS + I8_ASLOTS));
+static_assert(I8_SMEM <= 110 * 1024 && I8_SLOT % 128 == 0 && IS_ASLOT % 128 == 0, "two CTAs per SM");
+static_assert(IS_MAX_TPC * 16 * 8 * 4 <= I8_SLOTS * I8_SLOT, "a warp's partial sums fit in its weight ring");
+
+template <bool DOTS>
 __global__ void __launch_bounds__(IS_WARPS * 32, 2)
-k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ xq, int M, int N, int nb,
-                int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
-    constexpr int S = is_slots(FMT), SLOT = is_slot_bytes(FMT), RB = is_row_bytes(FMT);
+k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
+                int nb, int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
+    constexpr int S = I8_SLOTS, SA = I8_ASLOTS, SLOT = I8_SLOT, RB = 8 * Q8_0_BYTES, WB = I8_WARP_BYTES;
     extern __shared__ __align__(128) uint8_t is_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    uint8_t* ring = is_smem + warp * S * SLOT;
-    const uint32_t bar0 = ptx::smem_u32(is_smem + IS_WARPS * S * SLOT) + 8 * S * warp;
-    float* red = reinterpret_cast<float*>(is_smem + IS_WARPS * S * (SLOT + 8));  // [tpc][IS_WARPS][16][8]
+    uint8_t* ring = is_smem + warp * WB;  // S weight slots, then SA activation slots
+    uint8_t* aring = ring + S * SLOT;
+    const uint32_t bar0 = ptx::smem_u32(is_smem + IS_WARPS * WB) + 8 * (S + SA) * warp;
+    const uint32_t abar0 = bar0 + 8 * S;
     const int ntiles = (N + 15) / 16;
     const int t0 = blockIdx.x * tpc, nt = min(tpc, ntiles - t0);
-    const int npieces = nb / 8;  // Q4_K super-blocks, or groups of 8 Q8_0 blocks
+    const int npieces = nb / 8;  // groups of 8 blocks
     const int my = warp < npieces ? (npieces - 1 - warp) / IS_WARPS + 1 : 0;  // this warp's pieces per tile
     const int total = nt * my;
     const int m0 = blockIdx.y * 8;
-    const long long xrow = (long long)nb * Q8_1_BYTES;
-    // B fragment: token g's codes 8q .. 8q + 7 of a block; D fragment tokens 2q and 2q + 1
-    const bool bok = m0 + g < M, h0ok = m0 + 2 * q < M, h1ok = m0 + 2 * q + 1 < M;
-    const uint8_t* xb = xq + (long long)(bok ? m0 + g : 0) * xrow + 4 + 8 * q;
-    const uint8_t* xh0 = xq + (long long)(h0ok ? m0 + 2 * q : 0) * xrow;
-    const uint8_t* xh1 = xq + (long long)(h1ok ? m0 + 2 * q + 1 : 0) * xrow;
+    const bool h0ok = m0 + 2 * q < M, h1ok = m0 + 2 * q + 1 < M;  // the D fragment's tokens 2q, 2q + 1
 
-    auto issue = [&](int i) {  // lane 0: the copy of this warp's piece i into slot i % S
-        const int k = i / nt, tl = i - k * nt;  // piece-major: a piece's activations serve all tiles
-        const int p = warp + k * IS_WARPS;
+    IsSchedule next{0, 0};
+    auto issue = [&](int i) {  // lane 0: the copy of this warp's weight piece i into slot i % S
         const uint32_t bar = bar0 + 8 * (i % S);
         ptx::mbar_arrive_expect_tx(bar, SLOT);  // the whole box, zero-filled rows included
-        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, p * (RB / 8), (t0 + tl) * 16);
+        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, (warp + next.k * IS_WARPS) * (RB / 8),
+                         (t0 + next.tl) * 16);
     };
-    // the piece's activation words: codes (B) of token g and f16 d|s headers of tokens 2q,
-    // 2q + 1, for its 8 blocks
-    auto load_acts = [&](int p, uint32_t (&bw)[8][2], uint32_t (&h0)[8], uint32_t (&h1)[8]) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const long long bo = (long long)(8 * p + j) * Q8_1_BYTES;
-            bw[j][0] = bok ? __ldg(reinterpret_cast<const uint32_t*>(xb + bo)) : 0u;
-            bw[j][1] = bok ? __ldg(reinterpret_cast<const uint32_t*>(xb + bo + 4)) : 0u;
-            h0[j] = h0ok ? __ldg(reinterpret_cast<const uint32_t*>(xh0 + bo)) : 0u;
-            h1[j] = h1ok ? __ldg(reinterpret_cast<const uint32_t*>(xh1 + bo)) : 0u;
-        }
+    auto advance = [&]() {
+        if (++next.tl == nt) next.tl = 0, ++next.k;
     };
-    int issued = 0;
+    auto issue_acts = [&](int k) {  // lane 0: the activations of this warp's piece k into slot k % SA
+        const uint32_t bar = abar0 + 8 * (k % SA);
+        ptx::mbar_arrive_expect_tx(bar, IS_ASLOT);
+        ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), &tmX, bar, (warp + k * IS_WARPS) * (IS_XROW / 8),
+                         m0);
+    };
+    int issued = 0, aissued = 0;
     if (lane == 0) {
         ptx::tma_prefetch_desc(&tmW);
-        for (int i = 0; i < S; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
+        ptx::tma_prefetch_desc(&tmX);
+        for (int i = 0; i < S + SA; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
         ptx::fence_barrier_init();
     }
     __syncwarp();
-    for (; issued < S && issued < total; ++issued)
+    for (; issued < S && issued < total; ++issued, advance())
         if (lane == 0) issue(issued);
-    // programmatic dependent: the weight pieces above are in flight; activations are read,
-    // and results written, only after the previous kernel on the stream has completed
+    // programmatic dependent: the weight pieces above are in flight; the activations are
+    // read, and results written, only after the previous kernel on the stream has completed
     ptx::grid_dep_wait();
     ptx::grid_dep_launch_dependents();
+    for (; aissued < SA && aissued < my; ++aissued)
+        if (lane == 0) issue_acts(aissued);
 
     bool ok = true;
-    int i = 0;
-    float acc[IS_MAX_TPC][4];  // per tile: rows g, g + 8 x tokens 2q, 2q + 1
+    int i = 0, ka = 0;  // weight and activation slots consumed
+    unsigned long long acc[IS_MAX_TPC][2];  // per tile: rows g / g + 8, tokens (2q, 2q + 1)
 #pragma unroll
-    for (int tl = 0; tl < IS_MAX_TPC; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
-    // Q8_0 loads the next piece's activations while computing this one (measured faster);
-    // for Q4_K the extra registers cost more than the overlap gains
-    constexpr bool PREFETCH = FMT == FMT_Q8_0;
-    uint32_t bw[8][2], h0[8], h1[8];
-    if (PREFETCH && my > 0) load_acts(warp, bw, h0, h1);
+    for (int tl = 0; tl < IS_MAX_TPC; ++tl) acc[tl][0] = acc[tl][1] = 0ull;
     for (int k = 0; k < my && ok; ++k) {
-        const int p = warp + k * IS_WARPS;
-        const int b0 = 8 * p;  // first block of the piece
-        uint32_t nbw[8][2], nh0[8], nh1[8];
-        if (!PREFETCH) load_acts(p, bw, h0, h1);
-        else if (k + 1 < my) load_acts(p + IS_WARPS, nbw, nh0, nh1);
+        const int b0 = 8 * (warp + k * IS_WARPS);  // first block of the piece
+        if (!ds_wait(abar0 + 8 * (k % SA), (k / SA) & 1)) {
+            ok = false;
+            break;
+        }
+        ++ka;
+        // B fragments (codes 8q .. 8q + 7 of token g) and the f16 xd of tokens 2q, 2q + 1
+        const uint8_t* as = aring + (k % SA) * IS_ASLOT;
+        uint32_t bw[8][2], xh2[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t* cb = reinterpret_cast<const uint32_t*>(as + g * IS_XROW + j * Q8_1_BYTES + 4 + 8 * q);
+            bw[j][0] = cb[0];
+            bw[j][1] = cb[1];
+            const uint32_t e0 = *reinterpret_cast<const uint32_t*>(as + 2 * q * IS_XROW + j * Q8_1_BYTES);
+            const uint32_t e1 = *reinterpret_cast<const uint32_t*>(as + (2 * q + 1) * IS_XROW + j * Q8_1_BYTES);
+            xh2[j] = __byte_perm(e0, e1, 0x5410);
+        }
+        // every lane holds its copy: the slot takes the piece SA ahead
+        __syncwarp();
+        if (aissued < my) {
+            if (lane == 0) {
+                ptx::fence_proxy_async_smem();
+                issue_acts(aissued);
+            }
+            ++aissued;
+        }
 #pragma unroll
         for (int tl = 0; tl < IS_MAX_TPC; ++tl) {
             if (tl >= nt) break;
@@ -891,92 +970,327 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restri
                 break;
             }
             const uint8_t* sl = ring + (i % S) * SLOT;
-            if (is_kquant(FMT)) {
-                const uint8_t* rg = sl + g * RB;
-                const uint8_t* rh = sl + (g + 8) * RB;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                // codes 8q .. 8q + 7 of block j of rows g and g + 8: 2-byte aligned, read as
+                // aligned words and funnel-shifted (a third word only when the shift is 16)
+                const int off = j * Q8_0_BYTES + 2 + 8 * q, sh = (off & 3) * 8;
+                const uint32_t* pg = reinterpret_cast<const uint32_t*>(sl + g * RB + (off & ~3));
+                const uint32_t* ph = reinterpret_cast<const uint32_t*>(sl + (g + 8) * RB + (off & ~3));
+                const uint32_t g0 = pg[0], g1 = pg[1], g2 = sh ? pg[2] : 0u;
+                const uint32_t e0 = ph[0], e1 = ph[1], e2 = sh ? ph[2] : 0u;
+                int D[4];
+                mma_s8_16832(D, __funnelshift_r(g0, g1, sh), __funnelshift_r(e0, e1, sh), __funnelshift_r(g1, g2, sh),
+                             __funnelshift_r(e1, e2, sh), bw[j][0], bw[j][1]);
+                if constexpr (DOTS) {
+                    const int b = b0 + j;
+                    if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D[0];
+                    if (h1ok && n0 + g < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g) * nb + b] = D[1];
+                    if (h0ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q) * N + n0 + g + 8) * nb + b] = D[2];
+                    if (h1ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g + 8) * nb + b] = D[3];
+                    continue;
+                }
+                const float wg = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sl + g * RB + j * Q8_0_BYTES));
+                const float wh =
+                    f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sl + (g + 8) * RB + j * Q8_0_BYTES));
+                const unsigned long long xd = is_xd2(xh2[j]);
+                acc[tl][0] = ptx::fma_f32x2(is_exact2(D[0], D[1]), ptx::mul_f32x2(is_splat2(wg), xd), acc[tl][0]);
+                acc[tl][1] = ptx::fma_f32x2(is_exact2(D[2], D[3]), ptx::mul_f32x2(is_splat2(wh), xd), acc[tl][1]);
+            }
+            // every lane is done with the slot: refill it with the piece S ahead
+            __syncwarp();
+            if (issued < total) {
+                if (lane == 0) {
+                    ptx::fence_proxy_async_smem();
+                    issue(issued);
+                }
+                ++issued;
+                advance();
+            }
+            ++i;
+        }
+    }
+    if (!ok && lane == 0) {
+        // copies still in flight must land before the CTA exits
+        for (int k2 = i; k2 < issued; ++k2) {
+            const uint64_t tb = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar0 + 8 * (k2 % S), (k2 / S) & 1))
+                if (ptx::globaltimer_ns() - tb > DS_WAIT_LIMIT_NS) break;
+        }
+        for (int k2 = ka; k2 < aissued; ++k2) {
+            const uint64_t tb = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(abar0 + 8 * (k2 % SA), (k2 / SA) & 1))
+                if (ptx::globaltimer_ns() - tb > DS_WAIT_LIMIT_NS) break;
+        }
+    }
+    if (DOTS) return;
+    if (ok && my > 0) {
+        // this warp's partial sums, [tile][row][token], over its weight ring
+        float* rw = reinterpret_cast<float*>(ring);
+#pragma unroll
+        for (int tl = 0; tl < IS_MAX_TPC; ++tl) {
+            if (tl >= nt) break;
+            *reinterpret_cast<unsigned long long*>(rw + (tl * 16 + g) * 8 + 2 * q) = acc[tl][0];
+            *reinterpret_cast<unsigned long long*>(rw + (tl * 16 + g + 8) * 8 + 2 * q) = acc[tl][1];
+        }
+    }
+    if (__syncthreads_or(!ok)) return;
+    const int nw = min(npieces, IS_WARPS);  // warps that hold partial sums
+    for (int e = threadIdx.x; e < nt * 16 * 8; e += IS_WARPS * 32) {
+        const int tl = e >> 7, r = (e >> 3) & 15, tok = e & 7;
+        float v = 0.f;
+        for (int w = 0; w < nw; ++w) v += reinterpret_cast<const float*>(is_smem + w * WB)[e];
+        const int n = (t0 + tl) * 16 + r;
+        if (n < N && m0 + tok < M) out[(long long)(m0 + tok) * N + n] = v;
+    }
+}
+
+// ------------------------------------------ Q4_K, Q5_K: k_mmq_kq_stream
+// Each 32-block dot is two f16 MMAs (m16n8k16, f32 accumulation) on exact operands.  The
+// weight codes need no conversion: a code c <= 1023 in the low bits of an f16 half is the
+// subnormal c * 2^-24.  Masking a word of packed nibbles with 0x000F000F leaves two codes
+// of a sub-block j (j even) as an f16 pair; the high nibbles of the same bytes (j odd),
+// masked in place with 0x00F000F0, are 16 c * 2^-24, and the factor 16 goes into the
+// sub-scale (sc_j / 16); the other two bytes of the word take one shift.  Q5_K adds its
+// fifth bit in place (16 * 2^-24, or 256 * 2^-24 above a high nibble).  The int8
+// activation codes are f16 integers, formed once per piece (byte + 128 under the f16
+// 1024 bias, 1152 subtracted).  Every product is an integer times 2^-24 (2^-20 with the
+// factor 16), every partial sum below 2^24 units: the two MMAs give the block dot exactly
+// (measured exact on this part, subnormal operands included).  The k order inside a
+// block is permuted identically on both sides: thread (g, q) owns values 8q .. 8q + 7 of
+// the block, k slots (2q, 2q + 1) of the first MMA taking values (8q, 8q + 2), slots
+// (2q + 8, 2q + 9) values (8q + 1, 8q + 3), and the second MMA the same four higher.
+// Rescale, in packed f32 pairs over the thread's two tokens: S_row += (sc_j, sc_j) * (xd,
+// xd') * (D, D') per block, then per super-block acc += d * 2^24 * S - dmin * (sum_j m_j *
+// xs_j), the min term one m16n8k8 f16 MMA per tile (6-bit m_j and f16 xs_j are exact f16
+// operands, products exact, f32 accumulation).
+// A piece's activation codes and xd stay in registers for all of the CTA's tiles; the raw
+// q8_1 rows come by tensor copy into two slots per warp (the next piece's while this one
+// computes).  A weight copy brings BOXR = 32 rows (two tiles) x one super-block when there
+// are enough 32-row boxes to fill the GPU, else 16 rows: the copy engine streams 4.6 KB
+// boxes near the HBM rate and 2.3 KB boxes well below it (measured, 16 warps per SM,
+// nothing consuming).
+__host__ __device__ constexpr int ks_warps(int fmt, int boxr) { return boxr == 16 ? 8 : (fmt == FMT_Q4_K ? 8 : 7); }
+__host__ __device__ constexpr int ks_slots(int fmt, int boxr) { return boxr == 16 ? 3 : 2; }
+__host__ __device__ constexpr int ks_slot(int fmt, int boxr) { return boxr * kq_bytes(fmt); }
+__host__ __device__ constexpr int ks_max_boxes(int boxr) { return boxr == 16 ? 4 : 2; }  // per CTA
+constexpr int KS_ASLOTS = 2;
+__host__ __device__ constexpr int ks_warp_bytes(int fmt, int boxr) {
+    return ks_slots(fmt, boxr) * ks_slot(fmt, boxr) + KS_ASLOTS * IS_ASLOT;
+}
+__host__ __device__ constexpr int ks_smem_bytes(int fmt, int boxr) {
+    return ks_warps(fmt, boxr) * (ks_warp_bytes(fmt, boxr) + 8 * (ks_slots(fmt, boxr) + KS_ASLOTS));
+}
+constexpr int KS_SMEM_MAX = 113 * 1024;  // two CTAs per SM
+static_assert(ks_smem_bytes(FMT_Q4_K, 16) <= KS_SMEM_MAX && ks_smem_bytes(FMT_Q5_K, 16) <= KS_SMEM_MAX &&
+                  ks_smem_bytes(FMT_Q4_K, 32) <= KS_SMEM_MAX && ks_smem_bytes(FMT_Q5_K, 32) <= KS_SMEM_MAX,
+              "two CTAs per SM");
+static_assert(ks_slot(FMT_Q4_K, 16) % 128 == 0 && ks_slot(FMT_Q5_K, 16) % 128 == 0, "128-byte aligned slots");
+static_assert(4 * 16 * 8 * 4 <= 2 * ks_slot(FMT_Q4_K, 16), "a warp's partial sums fit in its weight ring");
+
+// 16 x 8 x 16, f16 operands, f32 accumulation: from zero, and in place
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// bytes (sel) of four int8 codes (u = codes ^ 0x80808080, i.e. code + 128) as an exact f16 pair
+__device__ __forceinline__ uint32_t ks_code_pair(uint32_t u, uint32_t sel) {
+    uint32_t h = __byte_perm(u, 0x64646464u, sel), d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0xE480E480u));  // - 1152
+    return d;
+}
+
+template <int FMT, int BOXR, bool DOTS>
+__global__ void __launch_bounds__(ks_warps(FMT, BOXR) * 32, 2)
+k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
+                int nb, int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
+    constexpr int W = ks_warps(FMT, BOXR), S = ks_slots(FMT, BOXR), SLOT = ks_slot(FMT, BOXR), RB = kq_bytes(FMT);
+    constexpr int SA = KS_ASLOTS, WB = ks_warp_bytes(FMT, BOXR), U = BOXR / 16, MB = ks_max_boxes(BOXR);
+    extern __shared__ __align__(128) uint8_t is_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    uint8_t* ring = is_smem + warp * WB;  // S weight slots, then SA activation slots
+    uint8_t* aring = ring + S * SLOT;
+    const uint32_t bar0 = ptx::smem_u32(is_smem + W * WB) + 8 * (S + SA) * warp;
+    const uint32_t abar0 = bar0 + 8 * S;
+    const int nboxes = (N + BOXR - 1) / BOXR;
+    const int t0 = blockIdx.x * tpc, nt = min(tpc, nboxes - t0);  // this CTA's boxes
+    const int npieces = nb / 8;  // super-blocks
+    const int my = warp < npieces ? (npieces - 1 - warp) / W + 1 : 0;  // this warp's pieces per box
+    const int total = nt * my;
+    const int m0 = blockIdx.y * 8;
+    const bool h0ok = m0 + 2 * q < M, h1ok = m0 + 2 * q + 1 < M;  // the D fragment's tokens 2q, 2q + 1
+
+    IsSchedule next{0, 0};
+    auto issue = [&](int i) {  // lane 0: the copy of this warp's weight piece i into slot i % S
+        const uint32_t bar = bar0 + 8 * (i % S);
+        ptx::mbar_arrive_expect_tx(bar, SLOT);  // the whole box, zero-filled rows included
+        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, (warp + next.k * W) * (RB / 8),
+                         (t0 + next.tl) * BOXR);
+    };
+    auto advance = [&]() {
+        if (++next.tl == nt) next.tl = 0, ++next.k;
+    };
+    auto issue_acts = [&](int k) {  // lane 0: the activations of this warp's piece k into slot k % SA
+        const uint32_t bar = abar0 + 8 * (k % SA);
+        ptx::mbar_arrive_expect_tx(bar, IS_ASLOT);
+        ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), &tmX, bar, (warp + k * W) * (IS_XROW / 8), m0);
+    };
+    int issued = 0, aissued = 0;
+    if (lane == 0) {
+        ptx::tma_prefetch_desc(&tmW);
+        ptx::tma_prefetch_desc(&tmX);
+        for (int i = 0; i < S + SA; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncwarp();
+    for (; issued < S && issued < total; ++issued, advance())
+        if (lane == 0) issue(issued);
+    // programmatic dependent: the weight pieces above are in flight; the activations are
+    // read, and results written, only after the previous kernel on the stream has completed
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
+    for (; aissued < SA && aissued < my; ++aissued)
+        if (lane == 0) issue_acts(aissued);
+
+    bool ok = true;
+    int i = 0, ka = 0;  // weight and activation copies consumed
+    // per box and tile of the box: rows g / g + 8, tokens (2q, 2q + 1)
+    unsigned long long acc[MB][U][2];
+#pragma unroll
+    for (int tl = 0; tl < MB; ++tl)
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[tl][u][0] = acc[tl][u][1] = 0ull;
+    const uint32_t msel = 0x4140u + 0x0202u * (q & 1);  // bytes 2(q & 1), 2(q & 1) + 1 of a scale word
+    for (int k = 0; k < my && ok; ++k) {
+        const int b0 = 8 * (warp + k * W);  // first block of the piece
+        if (!ds_wait(abar0 + 8 * (k % SA), (k / SA) & 1)) {
+            ok = false;
+            break;
+        }
+        ++ka;
+        // the piece's B operands (token g, values 8q .. 8q + 7 of each block, in the k order
+        // above), the f16 xd of tokens 2q, 2q + 1 per block, and the min MMA's B: the f16 xs of
+        // token g in blocks 2q and 2q + 1 (k = 2q, 2q + 1, n = g)
+        const uint8_t* as = aring + (k % SA) * IS_ASLOT;
+        uint32_t bx[8][4], xh2[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t* cb = reinterpret_cast<const uint32_t*>(as + g * IS_XROW + j * Q8_1_BYTES + 4 + 8 * q);
+            const uint32_t u0 = cb[0] ^ 0x80808080u, u1 = cb[1] ^ 0x80808080u;
+            bx[j][0] = ks_code_pair(u0, 0x4240u);
+            bx[j][1] = ks_code_pair(u0, 0x4341u);
+            bx[j][2] = ks_code_pair(u1, 0x4240u);
+            bx[j][3] = ks_code_pair(u1, 0x4341u);
+            const uint32_t e0 = *reinterpret_cast<const uint32_t*>(as + 2 * q * IS_XROW + j * Q8_1_BYTES);
+            const uint32_t e1 = *reinterpret_cast<const uint32_t*>(as + (2 * q + 1) * IS_XROW + j * Q8_1_BYTES);
+            xh2[j] = __byte_perm(e0, e1, 0x5410);
+        }
+        const uint32_t xsg = __byte_perm(*reinterpret_cast<const uint32_t*>(as + g * IS_XROW + 2 * q * Q8_1_BYTES),
+                                         *reinterpret_cast<const uint32_t*>(as + g * IS_XROW + (2 * q + 1) * Q8_1_BYTES),
+                                         0x7632);
+        // every lane holds its copy: the slot takes the piece SA ahead
+        __syncwarp();
+        if (aissued < my) {
+            if (lane == 0) {
+                ptx::fence_proxy_async_smem();
+                issue_acts(aissued);
+            }
+            ++aissued;
+        }
+#pragma unroll
+        for (int tl = 0; tl < MB; ++tl) {
+            if (tl >= nt) break;
+            if (!ds_wait(bar0 + 8 * (i % S), (i / S) & 1)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* sl = ring + (i % S) * SLOT;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int n0 = (t0 + tl) * BOXR + 16 * u;
+                const uint8_t* rg = sl + (16 * u + g) * RB;
+                const uint8_t* rh = rg + 8 * RB;
                 // Q5_K: high-bit bytes of values 8q .. 8q + 7 of rows g and g + 8 (bit j: block j)
                 const uint2 qg = FMT == FMT_Q5_K ? *reinterpret_cast<const uint2*>(rg + 16 + 8 * q) : make_uint2(0u, 0u);
                 const uint2 qh = FMT == FMT_Q5_K ? *reinterpret_cast<const uint2*>(rh + 16 + 8 * q) : make_uint2(0u, 0u);
                 const uint4 hg = *reinterpret_cast<const uint4*>(rg), hh = *reinterpret_cast<const uint4*>(rh);
-                // 6-bit scales and mins of sub-blocks 0..3 / 4..7, one per byte
+                // 6-bit sub-scales of sub-blocks 0..3 / 4..7, one per byte
                 const uint32_t scg[2] = {hg.y & 0x3F3F3F3Fu, (hg.w & 0x0F0F0F0Fu) | ((hg.y >> 2) & 0x30303030u)};
-                const uint32_t mng[2] = {hg.z & 0x3F3F3F3Fu, ((hg.w >> 4) & 0x0F0F0F0Fu) | ((hg.z >> 2) & 0x30303030u)};
                 const uint32_t sch[2] = {hh.y & 0x3F3F3F3Fu, (hh.w & 0x0F0F0F0Fu) | ((hh.y >> 2) & 0x30303030u)};
-                const uint32_t mnh[2] = {hh.z & 0x3F3F3F3Fu, ((hh.w >> 4) & 0x0F0F0F0Fu) | ((hh.z >> 2) & 0x30303030u)};
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f}, macc[4] = {0.f, 0.f, 0.f, 0.f};
+                unsigned long long sg = 0ull, sh = 0ull;  // sum_j sc_j * xd_j * D_j: rows g / g + 8
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int sh = 4 * (j & 1), off = kq_qs_off(FMT) + 32 * (j >> 1) + 8 * q;
+                    const int off = kq_qs_off(FMT) + 32 * (j >> 1) + 8 * q;
                     const uint2 wg = *reinterpret_cast<const uint2*>(rg + off);
                     const uint2 wh = *reinterpret_cast<const uint2*>(rh + off);
-                    uint32_t ag0 = (wg.x >> sh) & 0x0F0F0F0Fu, ah0 = (wh.x >> sh) & 0x0F0F0F0Fu;
-                    uint32_t ag1 = (wg.y >> sh) & 0x0F0F0F0Fu, ah1 = (wh.y >> sh) & 0x0F0F0F0Fu;
-                    if (FMT == FMT_Q5_K) {
-                        ag0 |= ((qg.x >> j) & 0x01010101u) << 4;
-                        ag1 |= ((qg.y >> j) & 0x01010101u) << 4;
-                        ah0 |= ((qh.x >> j) & 0x01010101u) << 4;
-                        ah1 |= ((qh.y >> j) & 0x01010101u) << 4;
+                    constexpr uint32_t MK = 0x000F000Fu;
+                    const uint32_t mk = (j & 1) ? MK << 4 : MK;
+                    // A: rows g (ag) and g + 8 (ah); [0], [1]: the first MMA's k slots (2q, 2q + 1)
+                    // and (2q + 8, 2q + 9); [2], [3]: the second MMA's
+                    uint32_t ag[4] = {wg.x & mk, (wg.x >> 8) & mk, wg.y & mk, (wg.y >> 8) & mk};
+                    uint32_t ah[4] = {wh.x & mk, (wh.x >> 8) & mk, wh.y & mk, (wh.y >> 8) & mk};
+                    if constexpr (FMT == FMT_Q5_K) {
+                        // the fifth bit: 16 units above a low nibble, 256 above a high one
+                        const int up = (j & 1) ? 8 : 4;
+                        const uint32_t bm = 0x00010001u << up;
+                        ag[0] |= ((qg.x >> j) << up) & bm;
+                        ag[1] |= ((qg.x >> (j + 8)) << up) & bm;
+                        ag[2] |= ((qg.y >> j) << up) & bm;
+                        ag[3] |= ((qg.y >> (j + 8)) << up) & bm;
+                        ah[0] |= ((qh.x >> j) << up) & bm;
+                        ah[1] |= ((qh.x >> (j + 8)) << up) & bm;
+                        ah[2] |= ((qh.y >> j) << up) & bm;
+                        ah[3] |= ((qh.y >> (j + 8)) << up) & bm;
                     }
-                    int D[4];
-                    mma_s8_16832(D, ag0, ah0, ag1, ah1, bw[j][0], bw[j][1]);
-                    if (dots) {
+                    float D[4];  // the block dot times 2^-24 (j even) or 2^-20 (j odd), exact
+                    mma_f16_16816_z(D, ag[0], ah[0], ag[1], ah[1], bx[j][0], bx[j][1]);
+                    mma_f16_16816(D, ag[2], ah[2], ag[3], ah[3], bx[j][2], bx[j][3]);
+                    if constexpr (DOTS) {
                         const int b = b0 + j;
-                        if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D[0];
-                        if (h1ok && n0 + g < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g) * nb + b] = D[1];
-                        if (h0ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q) * N + n0 + g + 8) * nb + b] = D[2];
-                        if (h1ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g + 8) * nb + b] = D[3];
+                        const float unit = (j & 1) ? 1048576.f : 16777216.f;
+                        const int D0 = __float2int_rn(D[0] * unit), D1 = __float2int_rn(D[1] * unit);
+                        const int D2 = __float2int_rn(D[2] * unit), D3 = __float2int_rn(D[3] * unit);
+                        if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D0;
+                        if (h1ok && n0 + g < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g) * nb + b] = D1;
+                        if (h0ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q) * N + n0 + g + 8) * nb + b] = D2;
+                        if (h1ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g + 8) * nb + b] = D3;
                         continue;
                     }
-                    const float xd0 = f16_bits_to_f32(h0[j]), xs0 = f16_bits_to_f32(h0[j] >> 16);
-                    const float xd1 = f16_bits_to_f32(h1[j]), xs1 = f16_bits_to_f32(h1[j] >> 16);
-                    const float sg = byte_f32(scg[j >> 2], j & 3), sh8 = byte_f32(sch[j >> 2], j & 3);
-                    const float mg = byte_f32(mng[j >> 2], j & 3), mh = byte_f32(mnh[j >> 2], j & 3);
-                    sacc[0] = fmaf(sg * xd0, (float)D[0], sacc[0]);
-                    sacc[1] = fmaf(sg * xd1, (float)D[1], sacc[1]);
-                    sacc[2] = fmaf(sh8 * xd0, (float)D[2], sacc[2]);
-                    sacc[3] = fmaf(sh8 * xd1, (float)D[3], sacc[3]);
-                    macc[0] = fmaf(mg, xs0, macc[0]);
-                    macc[1] = fmaf(mg, xs1, macc[1]);
-                    macc[2] = fmaf(mh, xs0, macc[2]);
-                    macc[3] = fmaf(mh, xs1, macc[3]);
+                    // (sc_j, sc_j) per row, sc_j / 16 for the high nibbles
+                    const float cg = (j & 1) ? byte_f32_div16(scg[j >> 2], j & 3) : byte_f32(scg[j >> 2], j & 3);
+                    const float ch = (j & 1) ? byte_f32_div16(sch[j >> 2], j & 3) : byte_f32(sch[j >> 2], j & 3);
+                    const unsigned long long xd = is_xd2(xh2[j]);
+                    sg = ptx::fma_f32x2(ptx::mul_f32x2(is_splat2(cg), xd), ptx::f2_bits(D[0], D[1]), sg);
+                    sh = ptx::fma_f32x2(ptx::mul_f32x2(is_splat2(ch), xd), ptx::f2_bits(D[2], D[3]), sh);
                 }
-                if (!dots) {
-                    const float dg = f16_bits_to_f32(hg.x), dmg = f16_bits_to_f32(hg.x >> 16);
-                    const float dh = f16_bits_to_f32(hh.x), dmh = f16_bits_to_f32(hh.x >> 16);
-                    acc[tl][0] = fmaf(-dmg, macc[0], fmaf(dg, sacc[0], acc[tl][0]));
-                    acc[tl][1] = fmaf(-dmg, macc[1], fmaf(dg, sacc[1], acc[tl][1]));
-                    acc[tl][2] = fmaf(-dmh, macc[2], fmaf(dh, sacc[2], acc[tl][2]));
-                    acc[tl][3] = fmaf(-dmh, macc[3], fmaf(dh, sacc[3], acc[tl][3]));
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // codes 8q .. 8q + 7 of block j of rows g and g + 8: 2-byte aligned, read as
-                    // aligned words and funnel-shifted (a third word only when the shift is 16)
-                    const int off = j * Q8_0_BYTES + 2 + 8 * q, sh = (off & 3) * 8;
-                    const uint32_t* pg = reinterpret_cast<const uint32_t*>(sl + g * RB + (off & ~3));
-                    const uint32_t* ph = reinterpret_cast<const uint32_t*>(sl + (g + 8) * RB + (off & ~3));
-                    const uint32_t g0 = pg[0], g1 = pg[1], g2 = sh ? pg[2] : 0u;
-                    const uint32_t e0 = ph[0], e1 = ph[1], e2 = sh ? ph[2] : 0u;
-                    int D[4];
-                    mma_s8_16832(D, __funnelshift_r(g0, g1, sh), __funnelshift_r(e0, e1, sh), __funnelshift_r(g1, g2, sh),
-                                 __funnelshift_r(e1, e2, sh), bw[j][0], bw[j][1]);
-                    if (dots) {
-                        const int b = b0 + j;
-                        if (h0ok && n0 + g < N) dots[((long long)(m0 + 2 * q) * N + n0 + g) * nb + b] = D[0];
-                        if (h1ok && n0 + g < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g) * nb + b] = D[1];
-                        if (h0ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q) * N + n0 + g + 8) * nb + b] = D[2];
-                        if (h1ok && n0 + g + 8 < N) dots[((long long)(m0 + 2 * q + 1) * N + n0 + g + 8) * nb + b] = D[3];
-                        continue;
-                    }
-                    const float wg = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sl + g * RB + j * Q8_0_BYTES));
-                    const float wh =
-                        f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sl + (g + 8) * RB + j * Q8_0_BYTES));
-                    const float xd0 = f16_bits_to_f32(h0[j]), xd1 = f16_bits_to_f32(h1[j]);
-                    acc[tl][0] = fmaf(wg * xd0, (float)D[0], acc[tl][0]);
-                    acc[tl][1] = fmaf(wg * xd1, (float)D[1], acc[tl][1]);
-                    acc[tl][2] = fmaf(wh * xd0, (float)D[2], acc[tl][2]);
-                    acc[tl][3] = fmaf(wh * xd1, (float)D[3], acc[tl][3]);
+                if constexpr (!DOTS) {
+                    // min term: A = m_j of rows g, g + 8 for j = 2q, 2q + 1 (sub-blocks 0..3 from
+                    // the low 6 bits of scale bytes 4..7, 4..7 from bytes 8..11 and 0..3)
+                    const uint32_t mwg = (q & 2) ? (((hg.w >> 4) & 0x0F0F0F0Fu) | ((hg.z >> 2) & 0x30303030u))
+                                                 : (hg.z & 0x3F3F3F3Fu);
+                    const uint32_t mwh = (q & 2) ? (((hh.w >> 4) & 0x0F0F0F0Fu) | ((hh.z >> 2) & 0x30303030u))
+                                                 : (hh.z & 0x3F3F3F3Fu);
+                    float mn[4];
+                    mma_f16_1688(mn, is_byte_pair_f16(mwg, msel), is_byte_pair_f16(mwh, msel), xsg);
+                    // d carries the 2^24 that undoes the weight operands' unit 2^-24
+                    const float dg = f16_bits_to_f32(hg.x) * 16777216.f, ndmg = f16_bits_to_f32((hg.x >> 16) ^ 0x8000u);
+                    const float dh = f16_bits_to_f32(hh.x) * 16777216.f, ndmh = f16_bits_to_f32((hh.x >> 16) ^ 0x8000u);
+                    acc[tl][u][0] = ptx::fma_f32x2(is_splat2(ndmg), ptx::f2_bits(mn[0], mn[1]),
+                                                   ptx::fma_f32x2(is_splat2(dg), sg, acc[tl][u][0]));
+                    acc[tl][u][1] = ptx::fma_f32x2(is_splat2(ndmh), ptx::f2_bits(mn[2], mn[3]),
+                                                   ptx::fma_f32x2(is_splat2(dh), sh, acc[tl][u][1]));
                 }
             }
             // every lane is done with the slot: refill it with the piece S ahead
@@ -987,28 +1301,9 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restri
                     issue(issued);
                 }
                 ++issued;
+                advance();
             }
             ++i;
-        }
-        if (PREFETCH && k + 1 < my) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                bw[j][0] = nbw[j][0];
-                bw[j][1] = nbw[j][1];
-                h0[j] = nh0[j];
-                h1[j] = nh1[j];
-            }
-        }
-    }
-    if (ok && !dots && my > 0) {
-#pragma unroll
-        for (int tl = 0; tl < IS_MAX_TPC; ++tl) {
-            if (tl >= nt) break;
-            float* rw = red + (tl * IS_WARPS + warp) * 16 * 8;
-            rw[g * 8 + 2 * q] = acc[tl][0];
-            rw[g * 8 + 2 * q + 1] = acc[tl][1];
-            rw[(g + 8) * 8 + 2 * q] = acc[tl][2];
-            rw[(g + 8) * 8 + 2 * q + 1] = acc[tl][3];
         }
     }
     if (!ok && lane == 0) {
@@ -1018,51 +1313,116 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restri
             while (!ptx::mbar_try_wait(bar0 + 8 * (k2 % S), (k2 / S) & 1))
                 if (ptx::globaltimer_ns() - tb > DS_WAIT_LIMIT_NS) break;
         }
+        for (int k2 = ka; k2 < aissued; ++k2) {
+            const uint64_t tb = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(abar0 + 8 * (k2 % SA), (k2 / SA) & 1))
+                if (ptx::globaltimer_ns() - tb > DS_WAIT_LIMIT_NS) break;
+        }
     }
-    if (dots) return;
-    __syncthreads();
+    if (DOTS) return;
+    if (ok && my > 0) {
+        // this warp's partial sums, [box][row][token], over its weight ring
+        float* rw = reinterpret_cast<float*>(ring);
+#pragma unroll
+        for (int tl = 0; tl < MB; ++tl) {
+            if (tl >= nt) break;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                *reinterpret_cast<unsigned long long*>(rw + (tl * BOXR + 16 * u + g) * 8 + 2 * q) = acc[tl][u][0];
+                *reinterpret_cast<unsigned long long*>(rw + (tl * BOXR + 16 * u + g + 8) * 8 + 2 * q) = acc[tl][u][1];
+            }
+        }
+    }
     if (__syncthreads_or(!ok)) return;
-    const int nw = min(npieces, IS_WARPS);  // warps that hold partial sums
-    for (int e = threadIdx.x; e < nt * 16 * 8; e += IS_WARPS * 32) {
-        const int tl = e >> 7, r = (e >> 3) & 15, tok = e & 7;
+    const int nw = min(npieces, W);  // warps that hold partial sums
+    for (int e = threadIdx.x; e < nt * BOXR * 8; e += W * 32) {
+        const int tl = e / (BOXR * 8), r = (e >> 3) % BOXR, tok = e & 7;
         float v = 0.f;
-        for (int w = 0; w < nw; ++w) v += red[((tl * IS_WARPS + w) * 16 + r) * 8 + tok];
-        const int n = (t0 + tl) * 16 + r;
+        for (int w = 0; w < nw; ++w) v += reinterpret_cast<const float*>(is_smem + w * WB)[e];
+        const int n = (t0 + tl) * BOXR + r;
         if (n < N && m0 + tok < M) out[(long long)(m0 + tok) * N + n] = v;
     }
+}
+
+// boxes per CTA: the fewest (at most max_boxes) that keep the grid within the two CTAs per
+// SM that are resident at once (no second, partial wave)
+inline int64_t stream_tpc(int64_t nboxes, int max_boxes) {
+    const int64_t per_wave = 2 * (int64_t)device_shape().sms;
+    const int64_t tpc = (nboxes + per_wave - 1) / per_wave;
+    return tpc < 1 ? 1 : (tpc > max_boxes ? max_boxes : tpc);
+}
+
+int launch_i8_stream_q8_0(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
+                          int32_t* dots, cudaStream_t s, const char* fn) {
+    const int64_t ntiles = (N + 15) / 16;
+    const int64_t tpc = stream_tpc(ntiles, IS_MAX_TPC);
+    static SmemAttr attr, attr_d;
+    const int e = dots ? ensure_smem((const void*)k_mmq_i8_stream<true>, I8_SMEM, attr_d)
+                       : ensure_smem((const void*)k_mmq_i8_stream<false>, I8_SMEM, attr);
+    if (e != MMQ_OK) {
+        report(fn, e, "shared-memory request refused");
+        return e;
+    }
+    CUtensorMap tw, tx;
+    if (!make_byte_map(&tw, w8, (uint64_t)nb * Q8_0_BYTES, (uint64_t)N, 8 * Q8_0_BYTES, 16, 8) ||
+        !make_byte_map(&tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, 8, 8)) {
+        report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
+        return MMQ_ERR_CUDA;
+    }
+    dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
+    ProfScope ps("k_mmq_i8_stream", s);
+    return pdl_status(dots ? launch_pdl(k_mmq_i8_stream<true>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx,
+                                        (int)M, (int)N, nb, (int)tpc, out, dots)
+                           : launch_pdl(k_mmq_i8_stream<false>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx,
+                                        (int)M, (int)N, nb, (int)tpc, out, dots),
+                      fn);
+}
+
+template <int FMT, int BOXR>
+int launch_kq_stream_b(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
+                       int32_t* dots, cudaStream_t s, const char* fn) {
+    const int64_t nboxes = (N + BOXR - 1) / BOXR;
+    const int64_t tpc = stream_tpc(nboxes, ks_max_boxes(BOXR));
+    constexpr int smem = ks_smem_bytes(FMT, BOXR);
+    static SmemAttr attr, attr_d;
+    const int e = dots ? ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, true>, smem, attr_d)
+                       : ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, false>, smem, attr);
+    if (e != MMQ_OK) {
+        report(fn, e, "shared-memory request refused");
+        return e;
+    }
+    CUtensorMap tw, tx;
+    if (!make_byte_map(&tw, w8, (uint64_t)(nb / 8) * kq_bytes(FMT), (uint64_t)N, kq_bytes(FMT), BOXR, 8) ||
+        !make_byte_map(&tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, 8, 8)) {
+        report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
+        return MMQ_ERR_CUDA;
+    }
+    dim3 grid((unsigned)((nboxes + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
+    const dim3 block(ks_warps(FMT, BOXR) * 32);
+    ProfScope ps("k_mmq_kq_stream", s);
+    return pdl_status(dots ? launch_pdl(k_mmq_kq_stream<FMT, BOXR, true>, grid, block, (size_t)smem, s, tw, tx, (int)M,
+                                        (int)N, nb, (int)tpc, out, dots)
+                           : launch_pdl(k_mmq_kq_stream<FMT, BOXR, false>, grid, block, (size_t)smem, s, tw, tx,
+                                        (int)M, (int)N, nb, (int)tpc, out, dots),
+                      fn);
+}
+
+// 32-row boxes when there are at least two of them per SM, else 16-row boxes
+template <int FMT>
+int launch_kq_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
+                     cudaStream_t s, const char* fn) {
+    if ((N + 31) / 32 >= 2 * (int64_t)device_shape().sms)
+        return launch_kq_stream_b<FMT, 32>(x8, w8, M, N, nb, out, dots, s, fn);
+    return launch_kq_stream_b<FMT, 16>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
 template <int FMT>
 int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                      int32_t* dots, cudaStream_t s, const char* fn) {
-    const int64_t ntiles = (N + 15) / 16;
-    const DeviceShape dsh = device_shape();
-    // tiles per CTA: the fewest (at most IS_MAX_TPC) that keep the grid within the two
-    // CTAs per SM that are resident at once (no second, partial wave)
-    int64_t tpc = (ntiles + 2 * (int64_t)dsh.sms - 1) / (2 * (int64_t)dsh.sms);
-    tpc = tpc < 1 ? 1 : (tpc > IS_MAX_TPC ? IS_MAX_TPC : tpc);
-    const int smem = is_smem_bytes(FMT, (int)tpc);
-    static SmemAttr attr;
-    if (smem > 48 * 1024) {
-        const int e = ensure_smem((const void*)k_mmq_i8_stream<FMT>, is_smem_bytes(FMT, IS_MAX_TPC), attr);
-        if (e != MMQ_OK) {
-            report(fn, e, "shared-memory request refused");
-            return e;
-        }
-    }
-    CUtensorMap tm;
-    const uint64_t row_bytes = FMT == FMT_Q8_0 ? (uint64_t)nb * Q8_0_BYTES : (uint64_t)(nb / 8) * kq_bytes(FMT);
-    if (!make_byte_map(&tm, w8, row_bytes, (uint64_t)N, is_row_bytes(FMT), 16, 8)) {
-        report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
-        return MMQ_ERR_CUDA;
-    }
-    dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
-    {
-        ProfScope ps("k_mmq_i8_stream", s);
-        return pdl_status(launch_pdl(k_mmq_i8_stream<FMT>, grid, dim3(IS_WARPS * 32), (size_t)smem, s, tm, x8, (int)M,
-                                     (int)N, nb, (int)tpc, out, dots),
-                          fn);
-    }
+    if constexpr (is_kquant(FMT))
+        return launch_kq_stream<FMT>(x8, w8, M, N, nb, out, dots, s, fn);
+    else
+        return launch_i8_stream_q8_0(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
 }  // namespace
@@ -1076,6 +1436,10 @@ unsigned small_take_error() {
     }
     return v;
 }
+
+std::atomic<int> g_small_route{SMALL_ROUTE_AUTO};
+
+int small_set_route(int route) { return g_small_route.exchange(route); }
 
 int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                  int32_t* dots, cudaStream_t s) {
@@ -1110,7 +1474,10 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
     // 18944 x 3584 the int8 stream takes 15.6 us against 17.4, while on 3584 x 18944 the
     // dp4a stream is faster, 17.4 against 20.7), the int8 tensor-core stream beyond, one
     // pass per 8 rows
-    const int64_t dp4a_max_m = is_kquant(fmt) && (N + 15) / 16 < 2 * (int64_t)device_shape().sms ? 4 : 2;
+    const int route = g_small_route.load();
+    const int64_t dp4a_max_m = route == SMALL_ROUTE_DP4A   ? 4
+                               : route == SMALL_ROUTE_MMA ? 0
+                               : is_kquant(fmt) && (N + 15) / 16 < 2 * (int64_t)device_shape().sms ? 4 : 2;
     if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(fmt, M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
         return fmt == FMT_Q8_0   ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
                : fmt == FMT_Q5_K ? launch_dp4a_stream<FMT_Q5_K>(x8, w8, M, N, nb, out, dots, s, sfn)

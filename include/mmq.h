@@ -273,6 +273,20 @@ int mmq_debug_refuse_smem(int on);
 int mmq_debug_set_wait_limit(int64_t ns);
 
 /*
+ * Which small-M kernel takes a shape on MMQ_PATH_SMALL (or on MMQ_PATH_AUTO when the
+ * automatic choice is the small path), for K % 256 == 0 and every format but Q6_K:
+ *   0  the measured choice (default): the dp4a weight stream for one or two rows (the
+ *      K-quants up to four unless the weight has at least two 16-row tiles per SM), the
+ *      tensor-core stream beyond;
+ *   1  the dp4a weight stream for up to four rows, the tensor-core stream beyond;
+ *   2  the tensor-core stream for every row count.
+ * For measuring the two kernels on the same shape; results are within the same tolerance
+ * either way, block dots bit-exact.  Returns the previous setting, or MMQ_ERR_ARG for a
+ * route outside 0..2 (nothing changed).  Process-wide.
+ */
+int mmq_debug_small_route(int route);
+
+/*
  * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1), mmq_gemm_q5_k (fmt 2)
  * or mmq_gemm_q6_k (fmt 3) on the expanded-code tensor-core path, with its scratch taken
  * from a fixed 64 MiB array in the library's device memory (one per device) instead of an

@@ -49,6 +49,15 @@ def test_path_selection_round_trip():
     assert mmq.lib().mmq_set_path(7) == -9
 
 
+def test_small_route_round_trip():
+    prev = mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_DP4A)
+    assert mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_MMA) == mmq.SMALL_ROUTE_DP4A
+    assert mmq.mmq_debug_small_route(prev) == mmq.SMALL_ROUTE_MMA
+    assert mmq.lib().mmq_debug_small_route(3) == -9
+    assert mmq.lib().mmq_debug_small_route(-1) == -9
+    assert mmq.mmq_debug_small_route(prev) == prev
+
+
 L = mmq.lib()
 V = ctypes.c_void_p
 

@@ -187,9 +187,20 @@ STREAM_SHAPES = [(1, 1, 256), (2, 7, 2304), (1, 300, 3584), (2, 77, 18944), (1, 
                  (3, 77, 2304), (4, 300, 3584), (5, 9000, 512), (8, 513, 3584), (7, 40, 7168)]
 
 
+@pytest.mark.parametrize("route", ["auto", "mma"])
 @pytest.mark.parametrize("fmt", FMTS)
-def test_few_row_stream_parity_and_dots(mmq, fmt):
+def test_few_row_stream_parity_and_dots(mmq, fmt, route):
+    if route == "mma" and fmt == "q6_k":
+        pytest.skip("Q6_K has no tensor-core stream")
     set_path(mmq, "small")
+    mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_MMA if route == "mma" else mmq.SMALL_ROUTE_AUTO)
+    try:
+        few_row_cases(mmq, fmt)
+    finally:
+        mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_AUTO)
+
+
+def few_row_cases(mmq, fmt):
     for (M, N, K) in STREAM_SHAPES:
         x = synth.activations(M * 5 + N, M, K, True)
         w = synth.weights(fmt, N * 7 + K, N, K)
@@ -318,6 +329,32 @@ def test_extreme_codes_block_dots(mmq, path):
     out = mmq.mmq_gemm_q8_0(xq, dev(w), M, N, K)
     r, nrm = oracle.gemm("q8_0", xq_ref, w, M, N, K)
     check_close(out.cpu().numpy(), r, nrm, "extreme codes")
+
+
+# Every K-quant code and 6-bit scale at its maximum, activation blocks all +127 or all -127:
+# the int8 stream's integer product sc_j * D_j then reaches 63 * 32 * 127 * 15 (Q4_K, the
+# largest value it converts exactly) and Q5_K's dot 32 * 127 * 31.  (8, 300, 1024) is one
+# full pass with a ragged last tile; (3, 5000, 512) a partly empty pass on a wide weight.
+@pytest.mark.parametrize("M,N,K", [(8, 300, 1024), (3, 5000, 512)])
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k"])
+def test_k_quant_extreme_scales_int8_stream(mmq, fmt, M, N, K):
+    set_path(mmq, "small")
+    sb = 144 if fmt == "q4_k" else 176
+    sign = np.where((np.arange(M)[:, None] + np.arange(K // 32)[None, :]) % 2 == 0, 1.0, -1.0)
+    x = np.repeat(sign, 32, axis=1).astype(np.float32)
+    w = synth.weights(fmt, 11, N, K).reshape(N, K // 256, sb).copy()
+    w[:, :, 4:] = 0xFF  # scales and mins 63, every code 15 (Q4_K) / 31 (Q5_K)
+    w = w.reshape(N, -1)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    xq_ref = oracle.quantize_q8_1(x)
+    dots = mmq.block_dots(fmt, xq, dev(w), M, N, K).cpu().numpy()
+    ref_dots = oracle.block_dots(fmt, xq_ref, w, M, N, K)
+    assert np.abs(ref_dots).min() == np.abs(ref_dots).max() == 32 * 127 * (15 if fmt == "q4_k" else 31)
+    assert np.array_equal(dots, ref_dots)
+    out = mmq.gemm(fmt, xq, dev(w), M, N, K)
+    ref, norm = oracle.gemm(fmt, xq_ref, w, M, N, K)
+    check_close(out.cpu().numpy(), ref, norm, f"{fmt} extreme scales {M}x{N}x{K}")
+    assert mmq.mmq_get_device_error() == 0
 
 
 @pytest.mark.parametrize("fmt", NO_TC)
