@@ -878,7 +878,8 @@ static_assert(IS_MAX_TPC * 16 * 8 * 4 <= I8_SLOTS * I8_SLOT, "a warp's partial s
 
 template <bool DOTS>
 __global__ void __launch_bounds__(IS_WARPS * 32, 2)
-k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
+k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmXl, int M, int N,
                 int nb, int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
     constexpr int S = I8_SLOTS, SA = I8_ASLOTS, SLOT = I8_SLOT, RB = 8 * Q8_0_BYTES, WB = I8_WARP_BYTES;
     extern __shared__ __align__(128) uint8_t is_smem[];
@@ -905,16 +906,21 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     auto advance = [&]() {
         if (++next.tl == nt) next.tl = 0, ++next.k;
     };
+    // the pass's activation rows: a box of min(8, M - m0) rows (rows past M are not copied;
+    // their slot rows only ever reach outputs that are not stored)
+    const bool lastp = blockIdx.y == gridDim.y - 1;
+    const uint32_t abytes = (uint32_t)min(M - m0, 8) * IS_XROW;
     auto issue_acts = [&](int k) {  // lane 0: the activations of this warp's piece k into slot k % SA
         const uint32_t bar = abar0 + 8 * (k % SA);
-        ptx::mbar_arrive_expect_tx(bar, IS_ASLOT);
-        ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), &tmX, bar, (warp + k * IS_WARPS) * (IS_XROW / 8),
-                         m0);
+        ptx::mbar_arrive_expect_tx(bar, abytes);
+        ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), lastp ? &tmXl : &tmX, bar,
+                         (warp + k * IS_WARPS) * (IS_XROW / 8), m0);
     };
     int issued = 0, aissued = 0;
     if (lane == 0) {
         ptx::tma_prefetch_desc(&tmW);
         ptx::tma_prefetch_desc(&tmX);
+        ptx::tma_prefetch_desc(&tmXl);
         for (int i = 0; i < S + SA; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
         ptx::fence_barrier_init();
     }
@@ -1114,7 +1120,8 @@ __device__ __forceinline__ uint32_t ks_code_pair(uint32_t u, uint32_t sel) {
 
 template <int FMT, int BOXR, bool DOTS>
 __global__ void __launch_bounds__(ks_warps(FMT, BOXR) * 32, 2)
-k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
+k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmXl, int M, int N,
                 int nb, int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
     constexpr int W = ks_warps(FMT, BOXR), S = ks_slots(FMT, BOXR), SLOT = ks_slot(FMT, BOXR), RB = kq_bytes(FMT);
     constexpr int SA = KS_ASLOTS, WB = ks_warp_bytes(FMT, BOXR), U = BOXR / 16, MB = ks_max_boxes(BOXR);
@@ -1142,27 +1149,41 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     auto advance = [&]() {
         if (++next.tl == nt) next.tl = 0, ++next.k;
     };
+    // the pass's activation rows: a box of min(8, M - m0) rows (rows past M are not copied;
+    // their slot rows only ever reach outputs that are not stored)
+    const bool lastp = blockIdx.y == gridDim.y - 1;
+    const uint32_t abytes = (uint32_t)min(M - m0, 8) * IS_XROW;
     auto issue_acts = [&](int k) {  // lane 0: the activations of this warp's piece k into slot k % SA
         const uint32_t bar = abar0 + 8 * (k % SA);
-        ptx::mbar_arrive_expect_tx(bar, IS_ASLOT);
-        ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), &tmX, bar, (warp + k * W) * (IS_XROW / 8), m0);
+        ptx::mbar_arrive_expect_tx(bar, abytes);
+        ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), lastp ? &tmXl : &tmX, bar,
+                         (warp + k * W) * (IS_XROW / 8), m0);
     };
     int issued = 0, aissued = 0;
     if (lane == 0) {
         ptx::tma_prefetch_desc(&tmW);
         ptx::tma_prefetch_desc(&tmX);
+        ptx::tma_prefetch_desc(&tmXl);
         for (int i = 0; i < S + SA; ++i) ptx::mbar_init(bar0 + 8 * i, 1);
         ptx::fence_barrier_init();
     }
     __syncwarp();
-    for (; issued < S && issued < total; ++issued, advance())
+    // programmatic dependent: weight pieces are requested before the previous kernel on the
+    // stream has completed; the activations are read, and results written, only after.
+    // Every copy queues behind the ones this SM requested before it (about 3 us deep once
+    // the rings are full), and no weight piece is of use before its activations: a warp with
+    // one or two pieces requests one weight piece, then its activations, then the rest; a
+    // warp with more fills its weight ring first (its later pieces need the deeper ring more
+    // than its first needs the earlier activations; both measured).
+    const int pre = my <= 2 ? 1 : S;
+    for (; issued < pre && issued < total; ++issued, advance())
         if (lane == 0) issue(issued);
-    // programmatic dependent: the weight pieces above are in flight; the activations are
-    // read, and results written, only after the previous kernel on the stream has completed
     ptx::grid_dep_wait();
     ptx::grid_dep_launch_dependents();
     for (; aissued < SA && aissued < my; ++aissued)
         if (lane == 0) issue_acts(aissued);
+    for (; issued < S && issued < total; ++issued, advance())
+        if (lane == 0) issue(issued);
 
     bool ok = true;
     int i = 0, ka = 0;  // weight and activation copies consumed
@@ -1344,6 +1365,15 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
 }
 
+// the activation maps of the streams: 8-row boxes for the full passes, and for the last pass
+// a box of its own rows (M - 8 (passes - 1)); copying rows past M as the copy engine's
+// zero fill was measured to slow a one-row pass down by a third
+inline bool make_act_maps(CUtensorMap* tx, CUtensorMap* txl, const uint8_t* x8, int64_t M, int nb) {
+    const uint32_t last = (uint32_t)(M - 8 * ((M - 1) / 8));
+    return make_byte_map(tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, 8, 8) &&
+           make_byte_map(txl, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, last, 8);
+}
+
 // boxes per CTA: the fewest (at most max_boxes) that keep the grid within the two CTAs per
 // SM that are resident at once (no second, partial wave)
 inline int64_t stream_tpc(int64_t nboxes, int max_boxes) {
@@ -1363,17 +1393,17 @@ int launch_i8_stream_q8_0(const uint8_t* x8, const uint8_t* w8, int64_t M, int64
         report(fn, e, "shared-memory request refused");
         return e;
     }
-    CUtensorMap tw, tx;
+    CUtensorMap tw, tx, txl;
     if (!make_byte_map(&tw, w8, (uint64_t)nb * Q8_0_BYTES, (uint64_t)N, 8 * Q8_0_BYTES, 16, 8) ||
-        !make_byte_map(&tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, 8, 8)) {
+        !make_act_maps(&tx, &txl, x8, M, nb)) {
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
     }
     dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
     ProfScope ps("k_mmq_i8_stream", s);
-    return pdl_status(dots ? launch_pdl(k_mmq_i8_stream<true>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx,
+    return pdl_status(dots ? launch_pdl(k_mmq_i8_stream<true>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx, txl,
                                         (int)M, (int)N, nb, (int)tpc, out, dots)
-                           : launch_pdl(k_mmq_i8_stream<false>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx,
+                           : launch_pdl(k_mmq_i8_stream<false>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx, txl,
                                         (int)M, (int)N, nb, (int)tpc, out, dots),
                       fn);
 }
@@ -1391,18 +1421,18 @@ int launch_kq_stream_b(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
         report(fn, e, "shared-memory request refused");
         return e;
     }
-    CUtensorMap tw, tx;
+    CUtensorMap tw, tx, txl;
     if (!make_byte_map(&tw, w8, (uint64_t)(nb / 8) * kq_bytes(FMT), (uint64_t)N, kq_bytes(FMT), BOXR, 8) ||
-        !make_byte_map(&tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, 8, 8)) {
+        !make_act_maps(&tx, &txl, x8, M, nb)) {
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
     }
     dim3 grid((unsigned)((nboxes + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
     const dim3 block(ks_warps(FMT, BOXR) * 32);
     ProfScope ps("k_mmq_kq_stream", s);
-    return pdl_status(dots ? launch_pdl(k_mmq_kq_stream<FMT, BOXR, true>, grid, block, (size_t)smem, s, tw, tx, (int)M,
+    return pdl_status(dots ? launch_pdl(k_mmq_kq_stream<FMT, BOXR, true>, grid, block, (size_t)smem, s, tw, tx, txl, (int)M,
                                         (int)N, nb, (int)tpc, out, dots)
-                           : launch_pdl(k_mmq_kq_stream<FMT, BOXR, false>, grid, block, (size_t)smem, s, tw, tx,
+                           : launch_pdl(k_mmq_kq_stream<FMT, BOXR, false>, grid, block, (size_t)smem, s, tw, tx, txl,
                                         (int)M, (int)N, nb, (int)tpc, out, dots),
                       fn);
 }
@@ -1469,15 +1499,19 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
         report(sfn, MMQ_ERR_SHAPE, "K or M too large for the Q6_K small-M stream (the expanded path takes it)");
         return MMQ_ERR_SHAPE;
     }
-    // measured crossovers: the dp4a weight streams for one or two rows (and the K-quants up
-    // to four, unless there are at least two 16-row weight tiles per SM: at 3 or 4 rows of
-    // 18944 x 3584 the int8 stream takes 15.6 us against 17.4, while on 3584 x 18944 the
-    // dp4a stream is faster, 17.4 against 20.7), the int8 tensor-core stream beyond, one
-    // pass per 8 rows
+    // measured crossovers (GEMM alone, back-to-back graph launches, 7B projections): the dp4a
+    // weight stream for one row (Q4_K 18944 x 3584: 8.7 us against 9.9); for two rows when
+    // the tensor-core stream would run one 16-row tile per CTA through a long K (3584 x
+    // 18944: 12.0 us against 16.1) or for Q5_K (12.9 against 13.9); for three or four rows
+    // only Q5_K on such a long K (18.7 against 20.4); the tensor-core streams otherwise (Q4_K
+    // 4 x 18944 x 3584: 10.1 us against 17.8)
     const int route = g_small_route.load();
-    const int64_t dp4a_max_m = route == SMALL_ROUTE_DP4A   ? 4
-                               : route == SMALL_ROUTE_MMA ? 0
-                               : is_kquant(fmt) && (N + 15) / 16 < 2 * (int64_t)device_shape().sms ? 4 : 2;
+    const bool long_narrow = (N + 15) / 16 <= 2 * (int64_t)device_shape().sms && nb / 8 >= 32;
+    const int64_t auto_max = M <= 1                                  ? 1
+                             : (fmt == FMT_Q5_K || long_narrow) && M <= 2 ? 2
+                             : fmt == FMT_Q5_K && long_narrow         ? 4
+                                                                      : 0;
+    const int64_t dp4a_max_m = route == SMALL_ROUTE_DP4A ? 4 : route == SMALL_ROUTE_MMA ? 0 : auto_max;
     if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(fmt, M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
         return fmt == FMT_Q8_0   ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)
                : fmt == FMT_Q5_K ? launch_dp4a_stream<FMT_Q5_K>(x8, w8, M, N, nb, out, dots, s, sfn)

@@ -275,9 +275,10 @@ int mmq_debug_set_wait_limit(int64_t ns);
 /*
  * Which small-M kernel takes a shape on MMQ_PATH_SMALL (or on MMQ_PATH_AUTO when the
  * automatic choice is the small path), for K % 256 == 0 and every format but Q6_K:
- *   0  the measured choice (default): the dp4a weight stream for one or two rows (the
- *      K-quants up to four unless the weight has at least two 16-row tiles per SM), the
- *      tensor-core stream beyond;
+ *   0  the measured choice (default): the dp4a weight stream for one row; for two rows
+ *      when the weight has at most two 16-row tiles per SM and K >= 8192 (a long K through
+ *      few tiles), or for Q5_K; for three or four rows only Q5_K with such a long K; the
+ *      tensor-core stream otherwise;
  *   1  the dp4a weight stream for up to four rows, the tensor-core stream beyond;
  *   2  the tensor-core stream for every row count.
  * For measuring the two kernels on the same shape; results are within the same tolerance
