@@ -1,9 +1,10 @@
 // MMQ for few activation rows: the decode-like regime, bound by the weight bytes read
 // from HBM ("When Does a Kernel Win Surface?", sec. "A bottleneck taxonomy",
 // bandwidth-roofline decode).  Kernels, chosen by small_launch at the end of the file:
-//   k_mmq_dp4a_stream  one or two rows (Q4_K up to four): per-warp weight streams, dp4a;
-//   k_mmq_i8_stream    three to eight rows per pass: the int8 tensor cores (mma.sync
-//                      m16n8k32 s8) on the raw codes, per-warp rings of 2-D tensor copies;
+//   k_mmq_dp4a_stream  one row (two for Q5_K and long K, up to four in a few cases, see
+//                      small_launch): per-warp weight streams, dp4a;
+//   k_mmq_i8_stream,   up to eight rows per pass on the tensor cores through mma.sync (Q8_0
+//   k_mmq_kq_stream    on s8, the K-quants on f16), per-warp rings of 2-D tensor copies;
 //   k_mmq_small_mma, k_mmq_small  shapes the streams do not take (K % 256 != 0).
 // Each kernel's own comment describes it.
 //
@@ -774,29 +775,29 @@ int launch_dp4a_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
 
 // ---------------------------------------------------------------- tensor-core streams
 // Two kernels for up to 8 activation rows per pass (grid.y = ceil(M/8) passes), both on the
-// tensor cores through mma.sync m16n8k32 ("When the Product Won't Collapse", sec. "The
-// obstruction": one exact integer dot per 32-block; "13 . r7-r8 raw-byte MMQ kernel", sec.
-// 2): 16 weight rows x 8 tokens x one whole 32-block per instruction, from the raw codes.
-//   k_mmq_i8_stream  Q8_0: s8 x s8 -> s32 on the codes as they are;
-//   k_mmq_kq_stream  Q4_K, Q5_K: e4m3 x e4m3 -> f32 (the fp8 form runs about twenty times
-//                    the int8 form's rate here, and is exact on these operands, below).
-// Common structure.  A CTA owns `tpc` consecutive 16-row tiles; its 8 warps split each
-// tile's K round-robin in pieces (warp w takes pieces w, w + 8, ...), a piece being 16 rows
-// x one super-block (2304 / 2816 B) or x 8 Q8_0 blocks (4352 B), brought by one 2-D tensor
-// copy into the warp's own ring (rows past N arrive as zeros).  The piece's activations (8
-// q8_1 rows x its 8 blocks, 2304 B; rows past M arrive as zeros) come by one more tensor
-// copy into the warp's activation slot and serve all of the CTA's tiles.  k is permuted
-// identically in A and B (a thread's 8 values of a block are 8 contiguous bytes), which
-// leaves every block dot unchanged.  The block dots are rescaled in registers as they come,
-// in packed f32 pairs; the warps' partial sums of a tile meet in shared memory at the end,
-// in each warp's weight ring (every copy into it consumed by then).  Needs K % 256 == 0.
+// tensor cores through mma.sync ("When the Product Won't Collapse", sec. "The obstruction":
+// one exact integer dot per 32-block; "13 . r7-r8 raw-byte MMQ kernel", sec. 2), 16 weight
+// rows x 8 tokens x one whole 32-block at a time, from the raw codes:
+//   k_mmq_i8_stream  Q8_0: m16n8k32 s8 x s8 -> s32 on the codes as they are;
+//   k_mmq_kq_stream  Q4_K, Q5_K: two m16n8k16 f16 MMAs per block on exact f16 operands
+//                    (on this part the s8 form runs at 69 cycles per MMA per SM sub-
+//                    partition, the f16 form at 9 per k16 half; both measured).
+// Common structure.  A CTA owns `tpc` consecutive weight boxes (16 rows; 32 for the K-quant
+// kernel when there are enough); its warps split each box's K round-robin in pieces (warp w
+// takes pieces w, w + W, ...), a piece being the box's rows x one super-block or x 8 Q8_0
+// blocks, brought by one 2-D tensor copy into the warp's own ring (rows past N arrive as
+// zeros).  The piece's activations (the pass's q8_1 rows x its 8 blocks) come by one more
+// tensor copy into the warp's activation slots and serve all of the CTA's boxes.  k is
+// permuted identically in A and B, which leaves every block dot unchanged.  The block dots
+// are rescaled in registers as they come, in packed f32 pairs; the warps' partial sums of
+// a box meet in shared memory at the end, in each warp's weight ring (every copy into it
+// consumed by then).  Needs K % 256 == 0.
 constexpr int IS_WARPS = 8;
 constexpr int IS_XROW = 8 * Q8_1_BYTES;  // one activation row's 8 blocks: 288 B
 constexpr int IS_ASLOT = 8 * IS_XROW;    // a piece's activations, 8 rows: 2304 B
 constexpr int IS_MAX_TPC = 4;
 constexpr int IS_MAGIC = 0x4B400000;                                 // bit pattern of 1.5 * 2^23
 constexpr unsigned long long IS_NEG_MAGIC2 = 0xCB400000CB400000ull;  // (-1.5 * 2^23, -1.5 * 2^23)
-constexpr unsigned long long IS_NEG_2P23 = 0xCB000000CB000000ull;    // (-2^23, -2^23)
 
 // (a, b) as an exact f32 pair, for |a|, |b| < 2^22: an int32 v added to the bit pattern of
 // 1.5 * 2^23 is the float 1.5 * 2^23 + v, and subtracting 1.5 * 2^23 leaves v exactly
@@ -808,13 +809,6 @@ __device__ __forceinline__ unsigned long long is_splat2(float v) { return ptx::f
 // an f16 pair as an f32 pair
 __device__ __forceinline__ unsigned long long is_xd2(uint32_t h2) {
     return ptx::f2_bits(f16_bits_to_f32(h2), f16_bits_to_f32(h2 >> 16));
-}
-// byte u of wa and of wb (0..255) as an exact f32 pair: each byte in the low mantissa bits
-// of 2^23, then 2^23 subtracted
-__device__ __forceinline__ unsigned long long is_bytes2(uint32_t wa, uint32_t wb, int u) {
-    return ptx::add_f32x2(ptx::f2_bits(__uint_as_float(__byte_perm(wa, 0x4B000000u, 0x7440 + u)),
-                                       __uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7440 + u))),
-                          IS_NEG_2P23);
 }
 // two bytes of w (0..63, picked by sel) as an exact f16 pair: with 0x64 above it a byte b is
 // the f16 1024 + b, and 1024 is subtracted
@@ -832,23 +826,6 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t 
         "{%10, %10, %10, %10};"
         : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
-}
-// 16 x 8 x 32, e4m3 operands, f32 accumulation: from zero, and in place
-__device__ __forceinline__ void mma_e4m3_16832_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                                 uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%10, %10, %10, %10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-}
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // 16 x 8 x 8, f16 operands, f32 result from zero: rows g / g + 8 x columns 2q, 2q + 1 in d
 __device__ __forceinline__ void mma_f16_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
