@@ -105,6 +105,7 @@ KERNEL_SOURCES = {
     "k_expand": ("gemm_expand.cu", "quant_block.cuh", "umma.cuh") + _COMMON_SRC,
     "k_mmq_dp4a_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_i8_stream": ("gemm_small.cu",) + _COMMON_SRC,
+    "k_mmq_kq_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small_mma": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small": ("gemm_small.cu",) + _COMMON_SRC,
 }
@@ -587,11 +588,44 @@ def run_ours(args, rank, world, local):
                 per[wlname] = e
                 torch.cuda.empty_cache()
         per["layer"] = run_layer(args)
+        per["small_m"] = run_small_m(args)
         line["per_config"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
         line["cpu_baseline"]["single_core"] = oracle_single_core()
     return line
+
+
+SMALL_M_CASES = [("q4_k", 1), ("q4_k", 2), ("q4_k", 8), ("q5_k", 1), ("q5_k", 8), ("q6_k", 1), ("q8_0", 1),
+                 ("q8_0", 8)]
+
+
+def run_small_m(args):
+    """The metric's small-M half: the GEMM alone (quantize excluded) at M = 1..8 on the 7B
+    ffn-up projection (N = 18944, K = 3584) in each weight format, on the automatic path;
+    per line the dominant kernel's HBM roofline (weight + activation + output bytes)."""
+    import torch
+    import block_quantized_int8_mmq_gb300 as mmq
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    N, K = 18944, 3584
+    lines = []
+    for fmt in ("q4_k", "q5_k", "q6_k", "q8_0"):
+        w = (synth.layer_weights(0, "gate", N, K) if fmt == "q4_k"
+             else synth.weights(fmt, synth.substream(synth.BASE_SEED + 5, N + K), N, K))
+        for (f, M) in SMALL_M_CASES:
+            if f != fmt:
+                continue
+            ln = _sweep_line(mmq, torch, dev, peaks, fmt, M, N, K, w, args, "auto")
+            kname = ln["kernels"][0] if ln["kernels"] else None
+            ln["roofline"] = {"bound": "hbm", "achieved": ln["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": ln["frac_hbm"], "kernel": kname,
+                              "traffic": traffic_for(kname, f"sweep {fmt} M={M} N={N} K={K}") if kname else None}
+            lines.append(ln)
+        torch.cuda.empty_cache()
+    return {"metric": "MMQ GEMM alone at M <= 8, 18944 x 3584", "unit": "GB/s", "lines": lines,
+            "config": {"workload": "7B ffn-up projection N=18944 K=3584, M in 1..8, each weight format",
+                       "l2": "rotating weight copies >= 3x L2", "cuda_graph": True}}
 
 
 def _rotating(torch, dev, arr, copies):
