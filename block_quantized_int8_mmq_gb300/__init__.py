@@ -26,7 +26,7 @@ EXPORTED = (
     "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
     "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k", "mmq_gemm_grouped_q5_k",
     "mmq_debug_product_dots", "mmq_debug_refuse_smem", "mmq_debug_set_wait_limit",
-    "mmq_debug_small_route",
+    "mmq_debug_small_route", "mmq_debug_expand_tiling",
 )
 
 
@@ -66,6 +66,8 @@ def _load():
     L.mmq_debug_product_dots.argtypes = [I, P, P, I64, I64, I64, P, P]
     L.mmq_debug_refuse_smem.argtypes = [I]
     L.mmq_debug_small_route.argtypes = [I]
+    L.mmq_debug_expand_tiling.argtypes = [I, I64, I64, I64, ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32)]
     L.mmq_debug_set_wait_limit.argtypes = [I64]
     L.mmq_profile_enable.argtypes = [I]
     L.mmq_profile_read.argtypes = [ctypes.POINTER(KernelTime), I, I]
@@ -219,6 +221,16 @@ def mmq_debug_small_route(route: int) -> int:
     if prev < 0:
         raise MMQError("mmq_debug_small_route", prev)
     return prev
+
+
+def mmq_debug_expand_tiling(fmt, M: int, N: int, K: int) -> tuple:
+    """(tile_n, splits): the weight rows per output tile and the K splits per tile the
+    expanded tensor-core path takes for this shape on the current device (host-only query)."""
+    tn, sp = ctypes.c_int32(0), ctypes.c_int32(0)
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check("mmq_debug_expand_tiling", _lib.mmq_debug_expand_tiling(f, int(M), int(N), int(K), ctypes.byref(tn),
+                                                                    ctypes.byref(sp)))
+    return tn.value, sp.value
 
 
 def mmq_set_path(path: int) -> int:

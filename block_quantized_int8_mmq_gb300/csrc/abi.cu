@@ -404,6 +404,23 @@ int mmq_debug_small_route(int route) {
     return small_set_route(route);
 }
 
+int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* splits) {
+    const char* fn = "mmq_debug_expand_tiling";
+    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K && fmt != FMT_Q5_K && fmt != FMT_Q6_K) {
+        report(fn, MMQ_ERR_ARG, "fmt must be 0 (Q8_0), 1 (Q4_K), 2 (Q5_K) or 3 (Q6_K)");
+        return MMQ_ERR_ARG;
+    }
+    const int st = check_mk(fn, M, N, K, QK_K);
+    if (st) return st;
+    if (!tile_n || !splits) {
+        report(fn, MMQ_ERR_NULL, "tile_n and splits must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    *tile_n = tcx_tile_n(fmt, M, N);
+    *splits = tcx_splits(fmt, M, N, K);
+    return MMQ_OK;
+}
+
 int mmq_debug_set_wait_limit(int64_t ns) {
     return tcx_set_wait_limit(ns >= 0 ? (unsigned long long)ns : 2000000000ull);
 }

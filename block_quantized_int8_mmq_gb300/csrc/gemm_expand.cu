@@ -55,7 +55,7 @@ __device__ unsigned long long g_tcx_wait_limit_ns = WAIT_LIMIT_NS;
 __device__ unsigned int g_tcx_error;
 
 constexpr int BM = 128;                  // activation rows per tile (TMEM lanes)
-constexpr int BN = 128;                  // weight rows per tile (MMA N)
+constexpr int BN = 128;                  // weight rows per tile (MMA N); the contraction also has 96 (tcx_tile_n)
 constexpr int GB = 8;                    // 32-blocks per group (256 values)
 constexpr int CHUNK = BM * QK * 2;       // fp16 codes of one block, 128 rows: 8 KiB
 constexpr int TILE16 = BM * 16 * 2;      // a K = 16 operand, 128 rows: 4 KiB
@@ -65,18 +65,19 @@ constexpr int NSTAGE = 8;                // blocks in flight (one block per stag
 constexpr int XCHUNK = CHUNK + TILE16;
 // weight bytes per (tile, block): one chunk of codes, or for Q6_K two planes whose sum is
 // the code times its sub-scale (see expand_weights_q6_k)
-__host__ __device__ constexpr int wchunk(int fmt) { return fmt == FMT_Q6_K ? 2 * CHUNK : CHUNK; }
-__host__ __device__ constexpr int stage_bytes(int fmt) { return XCHUNK + wchunk(fmt); }  // activations, then weights
+__host__ __device__ constexpr int wchunk(int fmt, int bn) { return (fmt == FMT_Q6_K ? 2 : 1) * bn * QK * 2; }
+__host__ __device__ constexpr int stage_bytes(int fmt, int bn) { return XCHUNK + wchunk(fmt, bn); }  // activations, then weights
 __host__ __device__ constexpr int nstage(int fmt) { return fmt == FMT_Q6_K ? 6 : NSTAGE; }
 constexpr int GR = 2;                    // group-data slots
 constexpr int NMMA = 2;                  // MMA-issuing warps; warp e issues items e, e + 2, ...
 constexpr int DS = NMMA;                 // TMEM slots: slot e (D and S of one item) belongs to issuer e
 constexpr int EPI_WARPS = 16;            // warps 0..15: epilogue
-constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // 32 columns per epilogue warp
 constexpr int WARP_LOAD = EPI_WARPS, WARP_MMA0 = EPI_WARPS + 1;
 constexpr int THREADS = (WARP_MMA0 + NMMA) * 32;  // 608
-constexpr int TMEM_COLS = DS * 2 * BN;            // 512
-constexpr int EXP_ROWS = 32;             // rows per expansion CTA (a quarter tile)
+constexpr int TMEM_COLS = DS * 2 * BN;            // 512: D at 256e, S at 256e + 128 for either tile width
+constexpr int EXP_ROWS = 32;             // rows per expansion CTA (a quarter of a 128-row tile)
+constexpr int QCHUNK = EXP_ROWS * QK * 2;     // a chunk's bytes of 32 rows: 2 KiB (whatever the tile's rows)
+constexpr int QTILE16 = EXP_ROWS * 16 * 2;    // a K = 16 operand's bytes of 32 rows: 1 KiB
 constexpr int EXP_THREADS = 128;
 
 // Group data (scratch and shared memory), per 128-row tile and 256-value group.  Activation
@@ -88,10 +89,11 @@ constexpr int EXP_THREADS = 128;
 // column 8 is 1.0.
 __host__ __device__ constexpr int xr(int fmt) { return is_kquant(fmt) ? GB + 1 : GB; }
 __host__ __device__ constexpr int ga_bytes(int fmt) { return is_kquant(fmt) ? TILE16 : 0; }
-__host__ __device__ constexpr int gw_bytes(int fmt) { return (is_kquant(fmt) ? TILE16 : 0) + TILE16; }
+__host__ __device__ constexpr int tile16(int rows) { return rows * 16 * 2; }
+__host__ __device__ constexpr int gw_bytes(int fmt, int bn) { return (is_kquant(fmt) ? tile16(bn) : 0) + tile16(bn); }
 __host__ __device__ constexpr int am_off(int fmt) { return 0; }
 __host__ __device__ constexpr int bmin_off(int fmt) { return ga_bytes(fmt); }  // in a group slot: GA, then GW
-__host__ __device__ constexpr int ws_off(int fmt) { return ga_bytes(fmt) + (is_kquant(fmt) ? TILE16 : 0); }
+__host__ __device__ constexpr int ws_off(int fmt, int bn) { return ga_bytes(fmt) + (is_kquant(fmt) ? tile16(bn) : 0); }
 
 __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
     return make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16), v[4] | ((uint32_t)v[5] << 16),
@@ -229,10 +231,10 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
     }
 }
 
-// One CTA per (32-row quarter of a 128-row tile, 256-value group) of the weights.  FOLD:
+// One CTA per (32-row quarter of a BNT-row tile, 256-value group) of the weights.  FOLD:
 // K-quant codes are q * sc_j (the contraction); without it, the raw nibbles (the block-dot
 // test hook).
-template <int FMT, bool FOLD>
+template <int FMT, bool FOLD, int BNT>
 __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
                                                     uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
                                                     uint8_t* __restrict__ sm) {
@@ -241,8 +243,9 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
     constexpr int VP = V + 1;                                               // + one zero piece (Q8_0 reads 4 B past)
     constexpr int SROW = FMT == FMT_Q8_0 ? 304 : (FMT == FMT_Q4_K ? 176 : 208);
     static_assert(SROW >= VP * 16 && SROW <= EXP_SROW, "row pad");
-    const int nt = bx >> 2, h = bx & 3, ng = nb / GB;
-    const int n0 = nt * BN + h * EXP_ROWS;
+    constexpr int QPT = BNT / EXP_ROWS, WCH = wchunk(FMT, BNT);  // quarters per tile, bytes per (tile, block)
+    const int nt = bx / QPT, h = bx % QPT, ng = nb / GB;
+    const int n0 = nt * BNT + h * EXP_ROWS;
     const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * kq_bytes(FMT);
     {
         // every load of a thread issued before its first store: one memory round trip
@@ -262,8 +265,8 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
         }
     }
     __syncthreads();
-    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * CHUNK + h * (CHUNK / 4);
-    constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
+    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * WCH + h * QCHUNK;
+    constexpr int PIECES = QCHUNK / 16;  // 128 16-byte pieces per block per quarter
     for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
         const int j = i / PIECES, p = i % PIECES;
         const int r = 8 * (p >> 5) + (p & 7), kc = (p >> 3) & 3;  // row within the quarter
@@ -313,9 +316,9 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
                 hi = u4x4_scaled_f16x4(a1, sc2, nsc);
             }
         }
-        *reinterpret_cast<uint4*>(dst + (size_t)j * CHUNK + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        *reinterpret_cast<uint4*>(dst + (size_t)j * WCH + p * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
-    uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT);
+    uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT, BNT);
     const int t = threadIdx.x;
     // WS (K = 16 operand): quarter piece t (0..63) = (row 8*(t/16) + t%8, columns
     // 8*((t/8)%2) .. +7); column c = the scale of item c for that row
@@ -333,7 +336,7 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
             else
                 v[e] = c < GB ? hdr[0] : (uint16_t)(hdr[1] ^ 0x8000u);  // d, or -dmin
         }
-        *reinterpret_cast<uint4*>(gdst + ws_off(FMT) - ga_bytes(FMT) + h * (TILE16 / 4) + t * 16) = pack8(v);
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT, BNT) - ga_bytes(FMT) + h * QTILE16 + t * 16) = pack8(v);
     }
     if (is_kquant(FMT) && t >= 64) {
         // BMIN: quarter piece u = t - 64 (0..63) = (row 8*(u/16) + u%8, columns 8*((u/8)%2)
@@ -348,7 +351,7 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
             q4_k_scale_min(hw[1], hw[2], hw[3], e, sc, mn);
             v[e] = kg == 0 ? __half_as_ushort(__int2half_rn(mn)) : (uint16_t)0;
         }
-        *reinterpret_cast<uint4*>(gdst + h * (TILE16 / 4) + u * 16) = pack8(v);
+        *reinterpret_cast<uint4*>(gdst + h * QTILE16 + u * 16) = pack8(v);
     }
 }
 
@@ -375,12 +378,14 @@ __device__ __forceinline__ uint2 q6_read8(const uint8_t* p) {  // 8 bytes at an 
     return make_uint2(__funnelshift_r(w0, w1, fs), __funnelshift_r(w1, w2, fs));
 }
 
+template <int BNT>
 __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
                                                     uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
                                                     uint8_t* __restrict__ sm) {
     constexpr int GRAN = Q6_SROW / 16;
-    const int nt = bx >> 2, h = bx & 3, ng = nb / GB;
-    const int n0 = nt * BN + h * EXP_ROWS;
+    constexpr int QPT = BNT / EXP_ROWS, PLANE = BNT * QK * 2, WCH = wchunk(FMT_Q6_K, BNT);  // two planes
+    const int nt = bx / QPT, h = bx % QPT, ng = nb / GB;
+    const int n0 = nt * BNT + h * EXP_ROWS;
     const long long rowbytes = (long long)ng * Q6_K_BYTES, end = (long long)N * rowbytes;
     for (int i = threadIdx.x; i < EXP_ROWS * GRAN; i += EXP_THREADS) {
         const int r = i / GRAN, c = i % GRAN;
@@ -406,8 +411,8 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
         const long long a = (long long)(n0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
         return sm + r * Q6_SROW + (int)(a & 15);
     };
-    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * (2 * CHUNK) + h * (CHUNK / 4);
-    constexpr int PIECES = CHUNK / 4 / 16;  // 128 16-byte pieces per block per quarter
+    uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * WCH + h * QCHUNK;
+    constexpr int PIECES = QCHUNK / 16;  // 128 16-byte pieces per block per quarter
     const __half2 one = __half2half2(__int2half_rn(1));
     const __half2 n1056 = __half2half2(__int2half_rn(-1056));  // 0x6400 | q = 1024 + q; minus 1056 = q - 32
     for (int i = threadIdx.x; i < GB * PIECES; i += EXP_THREADS) {
@@ -427,8 +432,8 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
                                     h2_bits(__hmul2(bits_h2(c1.x), s1)), h2_bits(__hmul2(bits_h2(c1.y), s1)));
         const uint4 p2 = make_uint4(h2_bits(__hmul2(bits_h2(c0.x), s2)), h2_bits(__hmul2(bits_h2(c0.y), s2)),
                                     h2_bits(__hmul2(bits_h2(c1.x), s2)), h2_bits(__hmul2(bits_h2(c1.y), s2)));
-        *reinterpret_cast<uint4*>(dst + (size_t)j * (2 * CHUNK) + p * 16) = p1;
-        *reinterpret_cast<uint4*>(dst + (size_t)j * (2 * CHUNK) + CHUNK + p * 16) = p2;
+        *reinterpret_cast<uint4*>(dst + (size_t)j * WCH + p * 16) = p1;
+        *reinterpret_cast<uint4*>(dst + (size_t)j * WCH + PLANE + p * 16) = p2;
     }
     // WS (K = 16 operand): quarter piece t (0..63) = (row 8*(t/16) + t%8, columns
     // 8*((t/8)%2) .. +7); columns 0..7 = d of the row's super-block
@@ -440,15 +445,15 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = kg == 0 ? dd : (uint16_t)0;
-        uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT_Q6_K);
-        *reinterpret_cast<uint4*>(gdst + ws_off(FMT_Q6_K) - ga_bytes(FMT_Q6_K) + h * (TILE16 / 4) + t * 16) = pack8(v);
+        uint8_t* gdst = gw + ((size_t)nt * ng + g) * gw_bytes(FMT_Q6_K, BNT);
+        *reinterpret_cast<uint4*>(gdst + ws_off(FMT_Q6_K, BNT) - ga_bytes(FMT_Q6_K) + h * QTILE16 + t * 16) = pack8(v);
     }
 }
 
 // Both expansions in one launch: CTAs 0 .. acts_x - 1 (grid x) expand the activations,
 // the rest the weights; grid y = the 256-value group.  The two halves are independent, so
 // they run side by side instead of one after the other.
-template <int FMT, bool FROM_X, bool FOLD, bool SPLIT_A>
+template <int FMT, bool FROM_X, bool FOLD, bool SPLIT_A, int BNT>
 __global__ void __launch_bounds__(EXP_THREADS, 12)
 k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
          const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
@@ -458,9 +463,9 @@ k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t
         expand_acts_body<FMT, FROM_X, SPLIT_A>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
     } else {
         if constexpr (FMT == FMT_Q6_K)  // the sub-scales are always folded (they are inside the block dot)
-            expand_weights_q6_k(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+            expand_weights_q6_k<BNT>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
         else
-            expand_weights_body<FMT, FOLD>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+            expand_weights_body<FMT, FOLD, BNT>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
     }
     // the contraction may start its set-up now; it reads the scratch only after this
     // whole grid has completed (griddepcontrol.wait)
@@ -472,11 +477,11 @@ constexpr int BAR_ST_FULL = 0, BAR_ST_EMPTY = BAR_ST_FULL + NSTAGE, BAR_G_FULL =
               BAR_G_EMPTY = BAR_G_FULL + GR, BAR_D_FULL = BAR_G_EMPTY + GR, BAR_D_EMPTY = BAR_D_FULL + DS,
               BAR_DRAIN = BAR_D_EMPTY + DS, NBARS = BAR_DRAIN + NMMA;
 
-template <int FMT>
+template <int FMT, int BNT>
 struct XLayout {
     static constexpr int stages = 0;
-    static constexpr int gslot = (ga_bytes(FMT) + gw_bytes(FMT) + 1023) & ~1023;
-    static constexpr int groups = stages + nstage(FMT) * stage_bytes(FMT);
+    static constexpr int gslot = (ga_bytes(FMT) + gw_bytes(FMT, BNT) + 1023) & ~1023;
+    static constexpr int groups = stages + nstage(FMT) * stage_bytes(FMT, BNT);
     static constexpr int asmin = groups + GR * gslot;  // the min item's constant AS (column 8 = 1.0)
     static constexpr int bars = asmin + TILE16;
     static constexpr int tmem_slot = bars + NBARS * 8;
@@ -485,26 +490,29 @@ struct XLayout {
     static_assert(alloc <= 227 * 1024, "shared memory");
 };
 
-// Warps 0..15 own 32 rows each (their TMEM lane quarter, warp % 4) and 32 columns of
-// the 128 x 128 tile; warp 16 is the bulk-copy producer; warps 17 and 18 issue the MMAs
+// Warps 0..15 own 32 rows each (their TMEM lane quarter, warp % 4) and a quarter of the
+// tile's columns (32 of a 128 x 128 tile, 24 of a 128 x 96 one); warp 16 is the bulk-copy producer; warps 17 and 18 issue the MMAs
 // of the even and odd items, each into its own TMEM slot (D at column 256e, S at 256e +
 // 128).  The scale MMA of block item c multiplies AS_c, which arrives with the block's codes
 // (only column c nonzero: xd), by the group's WS (column c = the item's column scales), so
 // S = xd_c (x) w_c exactly.  An item issues three MMAs and two commits (stage free; D and
 // S ready).  Epilogue warp 0 releases the
 // group data after each group's last item.  Each epilogue warp reads D and S in two
-// 16-column halves and hands the slot back before its last FMAs.  With K split over
+// loads (16 columns, then the other 16 or 8) and hands the slot back before its last FMAs.  With K split over
 // gridDim.z CTAs per tile (small outputs), CTA z takes its share of the groups and writes
 // a partial tile.
-template <int FMT, bool DOTS>
+template <int FMT, bool DOTS, int BNT>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const uint8_t* __restrict__ xb,
           const uint8_t* __restrict__ gw, int M, int N, int nb, float* __restrict__ out, int32_t* __restrict__ dots,
           long long split_stride) {
-    using L = XLayout<FMT>;
+    using L = XLayout<FMT, BNT>;
     constexpr bool MIN = is_kquant(FMT) && !DOTS;  // a min item closes every group
     constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
-    constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT), WCH = wchunk(FMT), STAGE = stage_bytes(FMT);
+    constexpr int GA = ga_bytes(FMT), GW = gw_bytes(FMT, BNT), WCH = wchunk(FMT, BNT), STAGE = stage_bytes(FMT, BNT);
+    constexpr int EPI_COLS = BNT / (EPI_WARPS / 4);  // columns per epilogue warp: 32 (or 24)
+    constexpr int H1 = EPI_COLS - 16;               // the second TMEM load's columns: 16 (or 8)
+    static_assert(BNT == 128 || (BNT == 96 && !DOTS), "96-wide tiles for the contraction only");
     constexpr int NS = nstage(FMT);
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
@@ -512,7 +520,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x, nt = blockIdx.y;
-    const int m0 = mt * BM, n0 = nt * BN;
+    const int m0 = mt * BM, n0 = nt * BNT;
     const int ng = nb / GB;
     // K split z of gridDim.z takes groups g0 .. g1 - 1 and writes its partial tile to
     // out + z * split_stride (one split: the output itself); the indices below (items,
@@ -602,7 +610,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
         // the D and S accumulators of its slot at every item.
         const int e = warp - WARP_MMA0;
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(BM, BN);
+            constexpr uint32_t idesc = make_idesc(BM, BNT);
             const uint32_t d = tmem + (uint32_t)(e * 2 * BN), sd = d + BN;
             for (int it = e, n = 0; it < nitems; it += NMMA, ++n) {
                 const int g = it / IPG, c = it % IPG, gs = g % GR;
@@ -628,8 +636,8 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     ptx::umma_f16(d, sdesc(a, 512), sdesc(b, 512), idesc, 0u);
                     ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + 256, 512), idesc, 1u);
                     if (FMT == FMT_Q6_K) {  // the second weight plane into the same block dot
-                        ptx::umma_f16(d, sdesc(a, 512), sdesc(b + CHUNK, 512), idesc, 1u);
-                        ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + CHUNK + 256, 512), idesc, 1u);
+                        ptx::umma_f16(d, sdesc(a, 512), sdesc(b + BNT * QK * 2, 512), idesc, 1u);
+                        ptx::umma_f16(d, sdesc(a + 256, 512), sdesc(b + BNT * QK * 2 + 256, 512), idesc, 1u);
                     }
                 } else {
                     // min item: AM x BMIN^T = sum_j s_j * m_j
@@ -638,7 +646,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                 if (!DOTS) {
                     // S = AS x WS^T: AS_c (with the block's codes) or the min item's constant AS
                     const uint32_t as = block ? a + CHUNK : sbase + L::asmin;
-                    ptx::umma_f16(sd, sdesc(as, 256), sdesc(gbase + ws_off(FMT), 256), idesc, 0u);
+                    ptx::umma_f16(sd, sdesc(as, 256), sdesc(gbase + ws_off(FMT, BNT), 256), idesc, 0u);
                 }
                 // the stage (codes and AS_b) is free once these MMAs are done; the group data
                 // is released by the epilogue, which takes the items in order, after the
@@ -670,7 +678,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                 ptx::mbar_arrive(bar(BAR_G_EMPTY + (it / IPG) % GR));
             }
             const uint32_t taddr = lane_base + (uint32_t)(e * 2 * BN);
-            if (DOTS) {
+            if constexpr (DOTS) {
                 uint32_t dv[EPI_COLS];
                 ptx::tmem_ld_cols(taddr, dv);
                 ptx::tmem_ld_wait(dv);
@@ -686,25 +694,34 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     }
                 }
             } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                {
                     uint32_t dv[16], sv[16];
-                    ptx::tmem_ld_cols(taddr + 16 * h, dv);
-                    ptx::tmem_ld_cols(taddr + BN + 16 * h, sv);
+                    ptx::tmem_ld_cols(taddr, dv);
+                    ptx::tmem_ld_cols(taddr + BN, sv);
                     ptx::tmem_ld_wait(dv);
                     ptx::tmem_ld_wait(sv);
-                    if (h == 1) {
-                        // the whole item is in registers: hand the TMEM slot back
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(bar(BAR_D_EMPTY + e));
-                    }
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        acc[8 * h + j] =
+                        acc[j] = ptx::fma_f32x2(ptx::f2_bits(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
+                                                ptx::f2_bits(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1])),
+                                                acc[j]);
+                }
+                {
+                    uint32_t dv[H1], sv[H1];
+                    ptx::tmem_ld_cols(taddr + 16, dv);
+                    ptx::tmem_ld_cols(taddr + BN + 16, sv);
+                    ptx::tmem_ld_wait(dv);
+                    ptx::tmem_ld_wait(sv);
+                    // the whole item is in registers: hand the TMEM slot back
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(BAR_D_EMPTY + e));
+#pragma unroll
+                    for (int j = 0; j < H1 / 2; ++j)
+                        acc[8 + j] =
                             ptx::fma_f32x2(ptx::f2_bits(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
                                            ptx::f2_bits(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1])),
-                                           acc[8 * h + j]);
+                                           acc[8 + j]);
                 }
             }
         }
@@ -712,7 +729,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
         ptx::grid_dep_launch_dependents();
         if (!DOTS && !*abort && mrow < M) {
             float* orow = out + blockIdx.z * split_stride + (long long)mrow * N + n0 + c0;
-            const int ncols = N - (n0 + c0);  // columns of this warp's 32 that exist
+            const int ncols = N - (n0 + c0);  // columns of this warp's EPI_COLS that exist
             if (ncols >= EPI_COLS && (N & 3) == 0) {
 #pragma unroll
                 for (int c = 0; c < EPI_COLS / 4; ++c)
@@ -798,30 +815,31 @@ struct ScratchPlan {
     long long split_stride;  // floats from one slab to the next
     size_t total() const { return xa + ga + xb + gw + part; }
 };
-ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K, bool allow_split = true) {
+ScratchPlan plan_scratch(int fmt, int64_t M, int64_t N, int64_t K, int bn, bool allow_split = true) {
     const int64_t nb = K / QK, ng = nb / GB;
-    const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
+    const int64_t MT = (M + BM - 1) / BM, NT = (N + bn - 1) / bn;
     const int splits = allow_split ? tcx_splits(fmt, M, N, K) : 1;
     const long long stride = ((long long)(M * N) + 63) & ~63LL;
     return {(size_t)(MT * nb) * XCHUNK,
             (size_t)(MT * ng) * ga_bytes(fmt),
-            (size_t)(NT * nb) * wchunk(fmt),
-            (size_t)(NT * ng) * gw_bytes(fmt),
+            (size_t)(NT * nb) * wchunk(fmt, bn),
+            (size_t)(NT * ng) * gw_bytes(fmt, bn),
             splits > 1 ? (size_t)splits * (size_t)stride * 4 : 0,
             splits,
             stride};
 }
 
-// The two launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K) bytes): both
-// expansions, then the contraction.  x != nullptr: the activations come as f32 rows and
-// are quantized by the expansion (q8_1 bytes written to xq); else xq is the input.
-template <int FMT, bool DOTS, bool FOLD = !DOTS>
+// The two launches of the path on scratch `ws` (plan_scratch(FMT, M, N, K, BNT) bytes):
+// both expansions, then the contraction, in BNT-wide weight tiles.  x != nullptr: the
+// activations come as f32 rows and are quantized by the expansion (q8_1 bytes written to
+// xq); else xq is the input.
+template <int FMT, bool DOTS, bool FOLD, int BNT>
 int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
               int32_t* dots, uint8_t* ws, const ScratchPlan& sp, cudaStream_t s, const char* fn) {
     const int nb = (int)(K / QK), ng = nb / GB;
-    const int64_t MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
+    const int64_t MT = (M + BM - 1) / BM, NT = (N + BNT - 1) / BNT;
     static SmemAttr attr;
-    const int st_attr = ensure_smem((const void*)k_mmq_tcx<FMT, DOTS>, XLayout<FMT>::alloc, attr);
+    const int st_attr = ensure_smem((const void*)k_mmq_tcx<FMT, DOTS, BNT>, XLayout<FMT, BNT>::alloc, attr);
     if (st_attr != MMQ_OK) {
         report(fn, st_attr, "shared-memory request refused");
         return st_attr;
@@ -838,19 +856,19 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     // also quantize
     const bool split = split_acts(x && !DOTS, MT, NT);
     const int64_t acts_x = 4 * MT * acts_split(split);
-    const dim3 eg((unsigned)(acts_x + 4 * NT), (unsigned)ng);
+    const dim3 eg((unsigned)(acts_x + (BNT / EXP_ROWS) * NT), (unsigned)ng);
     {
         ProfScope ps("k_expand", s);
         uint8_t* xq_out = static_cast<uint8_t*>(const_cast<void*>(xq));
         const uint8_t* w8 = static_cast<const uint8_t*>(wq);
         if (x && !DOTS && split)
-            k_expand<FMT, true, true, true><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
+            k_expand<FMT, true, true, true, BNT><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
                                                                        (int)acts_x, xa, ga, xb, gw);
         else if (x && !DOTS)
-            k_expand<FMT, true, true, false><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
+            k_expand<FMT, true, true, false, BNT><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
                                                                         (int)acts_x, xa, ga, xb, gw);
         else
-            k_expand<FMT, false, FOLD, false><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq),
+            k_expand<FMT, false, FOLD, false, BNT><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq),
                                                                           nullptr, w8, (int)M, (int)N, nb,
                                                                           (int)acts_x, xa, ga, xb, gw);
     }
@@ -862,7 +880,7 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)MT, (unsigned)NT, (unsigned)sp.splits);
         cfg.blockDim = dim3(THREADS);
-        cfg.dynamicSmemBytes = XLayout<FMT>::alloc;
+        cfg.dynamicSmemBytes = XLayout<FMT, BNT>::alloc;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -870,7 +888,7 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         const cudaError_t e =
-            cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, DOTS>, (const uint8_t*)xa, (const uint8_t*)ga, (const uint8_t*)xb,
+            cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, DOTS, BNT>, (const uint8_t*)xa, (const uint8_t*)ga, (const uint8_t*)xb,
                                (const uint8_t*)gw, (int)M, (int)N, nb, summed ? part : out, dots,
                                summed ? sp.split_stride : 0LL);
         if (e != cudaSuccess) {
@@ -903,14 +921,24 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
     return launch_status(fn);
 }
 
+// The launches in the tile width tcx_tile_n picks (the block-dot hooks: always 128).
+template <int FMT, bool DOTS, bool FOLD>
+int launch_bn(int bn, const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
+              int32_t* dots, uint8_t* ws, const ScratchPlan& sp, cudaStream_t s, const char* fn) {
+    if constexpr (!DOTS)
+        if (bn == 96) return launch_on<FMT, DOTS, FOLD, 96>(x, xq, wq, M, N, K, out, dots, ws, sp, s, fn);
+    return launch_on<FMT, DOTS, FOLD, BN>(x, xq, wq, M, N, K, out, dots, ws, sp, s, fn);
+}
+
 template <int FMT, bool DOTS, bool FOLD = !DOTS>
 int launch_x(const float* x, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
              int32_t* dots, cudaStream_t s, const char* fn) {
     void* ws = nullptr;
-    const ScratchPlan sp = plan_scratch(FMT, M, N, K);
+    const int bn = DOTS ? BN : tcx_tile_n(FMT, M, N);
+    const ScratchPlan sp = plan_scratch(FMT, M, N, K, bn);
     const int st0 = scratch_alloc(sp.total(), s, &ws, fn);
     if (st0 != MMQ_OK) return st0;
-    const int st = launch_on<FMT, DOTS, FOLD>(x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), sp, s, fn);
+    const int st = launch_bn<FMT, DOTS, FOLD>(bn, x, xq, wq, M, N, K, out, dots, static_cast<uint8_t*>(ws), sp, s, fn);
     scratch_free(ws, s);  // stream-ordered: after the kernels above
     return st;
 }
@@ -1043,13 +1071,16 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
         report(fn, MMQ_ERR_SHAPE, "N or K too large for the tile grid");
         return MMQ_ERR_SHAPE;
     }
-    if (plan_scratch(fmt, M, N, K, false).total() > NOALLOC_SCRATCH_BYTES) {
+    // the tile width the allocating call picks, unless only 128-wide tiles fit the fixed scratch
+    int bn = tcx_tile_n(fmt, M, N);
+    if (plan_scratch(fmt, M, N, K, bn, false).total() > NOALLOC_SCRATCH_BYTES) bn = BN;
+    if (plan_scratch(fmt, M, N, K, bn, false).total() > NOALLOC_SCRATCH_BYTES) {
         report(fn, MMQ_ERR_SHAPE, "the fixed 64 MiB scratch is too small for this shape");
         return MMQ_ERR_SHAPE;
     }
     // K splits only where their partial outputs fit in the fixed scratch too
-    ScratchPlan sp = plan_scratch(fmt, M, N, K);
-    if (sp.total() > NOALLOC_SCRATCH_BYTES) sp = plan_scratch(fmt, M, N, K, false);
+    ScratchPlan sp = plan_scratch(fmt, M, N, K, bn);
+    if (sp.total() > NOALLOC_SCRATCH_BYTES) sp = plan_scratch(fmt, M, N, K, bn, false);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -1061,17 +1092,17 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
         report(fn, MMQ_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed");
         return MMQ_ERR_CUDA;
     }
-    return fmt == FMT_Q8_0   ? launch_on<FMT_Q8_0, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
-           : fmt == FMT_Q5_K ? launch_on<FMT_Q5_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
-           : fmt == FMT_Q6_K ? launch_on<FMT_Q6_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
-                             : launch_on<FMT_Q4_K, false>(nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn);
+    return fmt == FMT_Q8_0   ? launch_bn<FMT_Q8_0, false, true>(bn, nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
+           : fmt == FMT_Q5_K ? launch_bn<FMT_Q5_K, false, true>(bn, nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
+           : fmt == FMT_Q6_K ? launch_bn<FMT_Q6_K, false, true>(bn, nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn)
+                             : launch_bn<FMT_Q4_K, false, true>(bn, nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn);
 }
 
-// K splits of the contraction: only when the output has fewer 128 x 128 tiles than there
-// are SMs, as many as fill the SMs once (at most 8), each at least two 256-value groups.
+// K splits of the contraction: only when the output has fewer tiles than half the SMs,
+// as many as fill the SMs once (at most 8), each at least two 256-value groups.
 int tcx_splits(int fmt, int64_t M, int64_t N, int64_t K) {
-    (void)fmt;
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int bn = tcx_tile_n(fmt, M, N);
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
     const int64_t ng = K / QK_K;
     int64_t sp = device_shape().sms / (tiles < 1 ? 1 : tiles);
     if (sp > ng / 2) sp = ng / 2;
@@ -1079,9 +1110,18 @@ int tcx_splits(int fmt, int64_t M, int64_t N, int64_t K) {
     return sp < 1 ? 1 : (int)sp;
 }
 
+// Weight tile width of the contraction.  A CTA's time is about proportional to its
+// tile's width, so where the 128-wide tiles leave SMs idle in their last wave (and are
+// too many to split K), 96-wide ones are taken when their waves times 96 come to at most
+// 0.9 of the 128-wide waves times 128: on 512 x 3584, 152 tiles on the 152 SMs instead of
+// 112.
 int tcx_tile_n(int fmt, int64_t M, int64_t N) {
-    (void)fmt, (void)M, (void)N;
-    return BN;
+    (void)fmt;
+    const int64_t sms = device_shape().sms, MT = (M + BM - 1) / BM;
+    const int64_t t128 = MT * ((N + BN - 1) / BN), t96 = MT * ((N + 95) / 96);
+    if (2 * t128 <= sms) return BN;  // K splits fill the SMs instead
+    const int64_t w128 = (t128 + sms - 1) / sms, w96 = (t96 + sms - 1) / sms;
+    return 10 * w96 * 96 <= 9 * w128 * BN ? 96 : BN;
 }
 
 int tcx_set_wait_limit(unsigned long long ns) {

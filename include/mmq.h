@@ -273,6 +273,21 @@ int mmq_debug_refuse_smem(int on);
 int mmq_debug_set_wait_limit(int64_t ns);
 
 /*
+ * The tiling the expanded-code tensor-core path (MMQ_PATH_EXPAND) takes for an M x N x K
+ * contraction of format fmt (0..3 as for mmq_gemm_noalloc) on the current device, written
+ * to the caller's host ints: *tile_n, the weight rows per output tile (128, or 96 where
+ * 128-wide tiles would leave SMs idle in their last wave: there are more than half as many
+ * 128-wide tiles as SMs, and the 96-wide tiles' waves times 96 come to at most 0.9 of the
+ * 128-wide waves times 128), and *splits, the CTAs that share one tile's K (1, or up to 8
+ * where there are at most half as many tiles as SMs, each taking at least two 256-value
+ * groups).  The tile's rows are always 128 activation rows; the block-dot hooks always use
+ * 128-wide tiles.  Host-only: launches nothing and reads the device's SM count once (152
+ * if no device can be queried).  Returns MMQ_OK, MMQ_ERR_ARG (fmt), MMQ_ERR_SHAPE,
+ * MMQ_ERR_K_MULTIPLE (K % 256 != 0) or MMQ_ERR_NULL; nothing is written on an error.
+ */
+int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* splits);
+
+/*
  * Which small-M kernel takes a shape on MMQ_PATH_SMALL (or on MMQ_PATH_AUTO when the
  * automatic choice is the small path), for K % 256 == 0 and every format but Q6_K:
  *   0  the measured choice (default): the dp4a weight stream for one row; for two rows

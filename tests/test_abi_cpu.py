@@ -58,6 +58,39 @@ def test_small_route_round_trip():
     assert mmq.mmq_debug_small_route(prev) == prev
 
 
+def test_expand_tiling_rule():
+    """The expanded path's tile width and K splits (host-only query; with no device it
+    assumes 152 SMs, the count of the GPU the rule was measured on)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("checked against the device's own SM count in the GPU tests")
+    except ImportError:
+        pass
+    t = mmq.mmq_debug_expand_tiling
+    # 4 x 28 = 112 tiles 128 wide on 152 SMs; 4 x 38 = 152 tiles 96 wide
+    assert t("q8_0", 512, 3584, 3584) == (96, 1)
+    assert t("q4_k", 1024, 3584, 3584) == (96, 1)      # 2 waves either way: 2 x 96 < 0.9 x 2 x 128
+    assert t("q4_k", 300, 3301, 512) == (96, 1)        # 3 x 26 = 78 > 76 tiles, 105 in 96-wide ones
+    assert t("q4_k", 2048, 18944, 3584) == (128, 1)    # 16 x 148 tiles: 16 waves against 21 x 96 / 128
+    assert t("q6_k", 2048, 3584, 18944) == (128, 1)    # 448 tiles, 3 waves; 608 narrow ones take 4
+    # at most half as many tiles as SMs: 128 wide and K split to fill the SMs
+    assert t("q4_k", 128, 3584, 3584) == (128, 5)      # 28 tiles, 152 // 28 = 5 splits of 14 groups
+    assert t("q8_0", 256, 3584, 18944) == (128, 2)
+    assert t("q8_0", 64, 256, 512) == (128, 1)         # two groups: no split below two groups each
+    assert t("q5_k", 9, 33, 4096) == (128, 8)          # one tile: at most 8 splits
+    for M, N, K in [(1, 1, 256), (777, 5000, 2048), (4096, 3584, 3584), (640, 1000, 1024)]:
+        bn, sp = t("q4_k", M, N, K)
+        assert bn in (96, 128) and 1 <= sp <= 8
+        assert sp == 1 or bn == 128
+        assert sp * 2 <= K // 256 or sp == 1
+    with pytest.raises(mmq.MMQError):
+        t("q4_k", 8, 8, 100)
+    with pytest.raises(mmq.MMQError):
+        t(4, 8, 8, 256)
+    assert mmq.lib().mmq_debug_expand_tiling(1, 8, 8, 256, None, None) == -3  # MMQ_ERR_NULL
+
+
 L = mmq.lib()
 V = ctypes.c_void_p
 

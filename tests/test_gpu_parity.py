@@ -180,6 +180,34 @@ def test_split_k_parity_dots_and_determinism(mmq, fmt):
     assert mmq.mmq_get_device_error() == 0
 
 
+# 96-wide weight tiles (taken where the 128-wide ones would leave SMs idle): the last tile
+# cut inside an epilogue warp's 24 columns, N odd or not a multiple of 4 (scalar stores)
+NARROW_SHAPES = [(300, 3300, 512), (300, 3301, 512), (257, 3850, 768)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_narrow_tile_parity_and_determinism(mmq, fmt):
+    set_path(mmq, "expand")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for (M, N, K) in NARROW_SHAPES:
+        bn, splits = mmq.mmq_debug_expand_tiling(fmt, M, N, K)
+        if sms == 152:
+            assert (bn, splits) == (96, 1), f"{M}x{N}x{K}: tiling {bn}, {splits}"
+        x = synth.activations(M * 3 + N, M, K, True)
+        w = synth.weights(fmt, N * 5 + K, N, K)
+        xq = mmq.mmq_quantize_q8_1(dev(x))
+        wd = dev(w)
+        out = torch.full((M, N), float("nan"), device="cuda")
+        mmq.gemm(fmt, xq, wd, M, N, K, out=out)
+        again = mmq.gemm(fmt, xq, wd, M, N, K)
+        assert torch.equal(out, again), f"{fmt} {M}x{N}x{K}: not deterministic"
+        o = out.cpu().numpy()
+        assert not np.isnan(o).any(), "output not fully written"
+        ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
+        check_close(o, ref, norm, f"{fmt} narrow tiles {M}x{N}x{K}")
+    assert mmq.mmq_get_device_error() == 0
+
+
 # one to eight activation rows on the small path: weight rows dealt out to warps (several
 # rows per warp when N exceeds the resident warps), rows of 1 to 10 pieces with a partial
 # last piece, N = 1, and token counts that leave part of a 4- or 8-row pass empty
