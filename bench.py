@@ -815,19 +815,28 @@ def run_decode(args):
 def run_moe(args):
     """Expert-grouped contraction at a mixture-of-experts prefill shape: 2048 tokens, top-8
     of 128 experts (seeded, uniform: each token picks 8 distinct experts), expert matrices
-    N=768 x K=2048 in Q4_K, i.e. 16384 routed rows.  The grouping (count, scan, scatter)
-    and the contraction are timed together, in CUDA-graph replays over rotating weight
-    copies (> 3x L2)."""
+    N=768 x K=2048, i.e. 16384 routed rows.  The grouping (count, scan, scatter) and the
+    contraction are timed together, in CUDA-graph replays over rotating weight copies (> 3x
+    L2).  The main line is Q4_K on the default (expanded) path; "lines" adds Q4_K on the
+    converter kernel and Q6_K experts, with each line's per-kernel device times."""
     import torch
     import block_quantized_int8_mmq_gb300 as mmq
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
+    lines = [_moe_line(mmq, torch, dev, peaks, fmt, path, args)
+             for (fmt, path) in (("q4_k", "auto"), ("q4_k", "tc"), ("q6_k", "auto"))]
+    main = dict(lines[0])
+    main["lines"] = lines
+    return main
+
+
+def _moe_line(mmq, torch, dev, peaks, fmt, path, args):
     T, TOPK, E, N, K = 2048, 8, 128, 768, 2048
     R = T * TOPK
     rng = np.random.default_rng(synth.substream(synth.BASE_SEED + 6, 1))
     ids = np.stack([rng.permutation(E)[:TOPK] for _ in range(T)]).reshape(-1).astype(np.int32)
     x = synth.activations(synth.substream(synth.BASE_SEED + 6, 2), T, K, True)
-    w = synth.weights("q4_k", synth.substream(synth.BASE_SEED + 6, 3), E * N, K)
+    w = synth.weights(fmt, synth.substream(synth.BASE_SEED + 6, 3), E * N, K)
     copies = max(2, -(-3 * l2_bytes(torch, dev) // w.nbytes))
     ws = _rotating(torch, dev, w, copies)
     xq_tok = mmq.mmq_quantize_q8_1(torch.from_numpy(x).to(dev))
@@ -835,26 +844,38 @@ def run_moe(args):
     idd = torch.from_numpy(ids).to(dev)
     out = torch.empty((R, N), device=dev)
     stream = torch.cuda.current_stream(dev)
-    for i in range(args.warmup):
-        mmq.mmq_gemm_grouped("q4_k", xq, idd, ws[i % copies], E, N, K, out=out, stream=stream)
-    torch.cuda.synchronize(dev)
-    assert mmq.mmq_get_device_error(stream) == 0
-    # spot parity on a few rows against the oracle (the rows' own experts)
-    import oracle
-    xr = xq.cpu().numpy()
-    o = out.cpu().numpy()
-    for r in (0, 1, R // 2, R - 1):
-        e = int(ids[r])
-        ref, norm = oracle.gemm("q4_k", np.ascontiguousarray(xr[r:r + 1]), np.ascontiguousarray(w[e * N:(e + 1) * N]),
-                                1, N, K)
-        assert np.all(np.abs(o[r] - ref[0]) <= 1e-4 * norm[0]), f"grouped row {r} differs from the oracle"
-    iters = max(20, args.steps)
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        for i in range(iters):
-            mmq.mmq_gemm_grouped("q4_k", xq, idd, ws[i % copies], E, N, K, out=out, stream=cap)
+    prev_path = mmq.mmq_set_path(mmq.PATH_TC if path == "tc" else mmq.PATH_AUTO)
+    try:
+        for i in range(args.warmup):
+            mmq.mmq_gemm_grouped(fmt, xq, idd, ws[i % copies], E, N, K, out=out, stream=stream)
+        torch.cuda.synchronize(dev)
+        used = PATH_NAMES.get(mmq.mmq_last_path(), "?")
+        assert mmq.mmq_get_device_error(stream) == 0
+        # spot parity on a few rows against the oracle (the rows' own experts)
+        import oracle
+        xr = xq.cpu().numpy()
+        o = out.cpu().numpy()
+        for r in (0, 1, R // 2, R - 1):
+            e = int(ids[r])
+            ref, norm = oracle.gemm(fmt, np.ascontiguousarray(xr[r:r + 1]),
+                                    np.ascontiguousarray(w[e * N:(e + 1) * N]), 1, N, K)
+            assert np.all(np.abs(o[r] - ref[0]) <= 1e-4 * norm[0]), f"grouped row {r} differs from the oracle"
+        # per-kernel device times of one call (serialised by the profile's events)
+        prev_prof = mmq.mmq_profile_enable(True)
+        mmq.mmq_profile_read(reset=True)
+        mmq.mmq_gemm_grouped(fmt, xq, idd, ws[0], E, N, K, out=out, stream=stream)
+        torch.cuda.synchronize(dev)
+        kernels = {k: round(v[1] * 1e3, 2) for k, v in sorted(mmq.mmq_profile_read(reset=True).items())}
+        mmq.mmq_profile_enable(prev_prof)
+        iters = max(20, args.steps)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(iters):
+                mmq.mmq_gemm_grouped(fmt, xq, idd, ws[i % copies], E, N, K, out=out, stream=cap)
+    finally:
+        mmq.mmq_set_path(prev_path)
     graph.replay()
     torch.cuda.synchronize(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -869,11 +890,13 @@ def run_moe(args):
     ms = a.elapsed_time(b) / iters
     ops = 2.0 * R * N * K
     wbytes = w.nbytes
+    del ws
     return {"metric": "expert-grouped MMQ TOPS (2*R*N*K, R = routed rows)", "value": ops / (ms / 1e3) / 1e12,
-            "unit": "TOPS", "ms_per_call": ms, "higher_is_better": True,
+            "unit": "TOPS", "ms_per_call": ms, "higher_is_better": True, "fmt": fmt, "path": used,
+            "kernels_us": kernels,
             "weight_gbs": wbytes / (ms / 1e3) / 1e9, "frac_hbm_weights": wbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
             "n_gpus": 1, "steps": iters, "warmup": args.warmup, "data": "synthetic (seeded routing and weights)",
-            "config": {"workload": "MoE prefill: 2048 tokens x top-8 of 128 experts, Q4_K experts 768x2048",
+            "config": {"workload": f"MoE prefill: 2048 tokens x top-8 of 128 experts, {fmt.upper()} experts 768x2048",
                        "R": R, "E": E, "N": N, "K": K, "l2": f"rotating {copies} weight copies",
                        "cuda_graph": True},
             "clocks": clk}

@@ -26,7 +26,7 @@ EXPORTED = (
     "mmq_gemm_q5_k", "mmq_linear_q5_k", "mmq_debug_block_dots_q5_k",
     "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k", "mmq_gemm_grouped_q5_k",
     "mmq_debug_product_dots", "mmq_debug_refuse_smem", "mmq_debug_set_wait_limit",
-    "mmq_debug_small_route", "mmq_debug_expand_tiling",
+    "mmq_debug_small_route", "mmq_debug_expand_tiling", "mmq_gemm_grouped_q6_k",
 )
 
 
@@ -61,7 +61,7 @@ def _load():
     L.mmq_gemm_noalloc.argtypes = [I, P, P, I64, I64, I64, P, P]
     for f in ("mmq_linear_q8_0", "mmq_linear_q4_k", "mmq_linear_q5_k", "mmq_linear_q6_k"):
         getattr(L, f).argtypes = [P, I64, I64, P, I64, P, P, P]
-    for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k", "mmq_gemm_grouped_q5_k"):
+    for f in ("mmq_gemm_grouped_q8_0", "mmq_gemm_grouped_q4_k", "mmq_gemm_grouped_q5_k", "mmq_gemm_grouped_q6_k"):
         getattr(L, f).argtypes = [P, P, I64, P, I64, I64, I64, P, P]
     L.mmq_debug_product_dots.argtypes = [I, P, P, I64, I64, I64, P, P]
     L.mmq_debug_refuse_smem.argtypes = [I]

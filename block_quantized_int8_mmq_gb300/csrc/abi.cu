@@ -202,8 +202,9 @@ int linear(const char* fn, int fmt, const float* x, int64_t M, int64_t K, const 
     return st;
 }
 
-// Expert-grouped contraction: rows grouped by expert on the device, then the converter
-// tensor-core kernel over the tile list (needs tcgen05 and K % 256 == 0).
+// Expert-grouped contraction: rows grouped by expert on the device, then a tensor-core
+// contraction over the tile list (needs tcgen05 and K % 256 == 0): the converter kernel
+// when MMQ_PATH_TC is set (not Q6_K), else the expanded path.
 int grouped(const char* fn, int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E,
             int64_t N, int64_t K, float* out, void* stream) {
     int st = check_mk(fn, R, N, K, QK_K);
@@ -224,8 +225,13 @@ int grouped(const char* fn, int fmt, const void* xq, const int32_t* row_expert, 
         report(fn, MMQ_ERR_LAUNCH, "the grouped contraction needs the tcgen05 tensor cores");
         return MMQ_ERR_LAUNCH;
     }
-    st = grouped_launch(fmt, xq, row_expert, R, wq, E, N, K, out, static_cast<cudaStream_t>(stream));
-    if (st == MMQ_OK) t_last_path = MMQ_PATH_TC;
+    const bool use_tc = current_path() == MMQ_PATH_TC;
+    if (use_tc && fmt == FMT_Q6_K) {
+        report(fn, MMQ_ERR_ARG, "the converter tensor-core kernel takes Q8_0, Q4_K and Q5_K (Q6_K: the expanded path)");
+        return MMQ_ERR_ARG;
+    }
+    st = grouped_launch(fmt, xq, row_expert, R, wq, E, N, K, out, static_cast<cudaStream_t>(stream), use_tc);
+    if (st == MMQ_OK) t_last_path = use_tc ? MMQ_PATH_TC : MMQ_PATH_EXPAND;
     return st;
 }
 
@@ -336,6 +342,11 @@ int mmq_gemm_grouped_q8_0(const void* xq, const int32_t* row_expert, int64_t R, 
 int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
                           int64_t K, float* out, void* stream) {
     return grouped("mmq_gemm_grouped_q4_k", FMT_Q4_K, xq, row_expert, R, wq, E, N, K, out, stream);
+}
+
+int mmq_gemm_grouped_q6_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream) {
+    return grouped("mmq_gemm_grouped_q6_k", FMT_Q6_K, xq, row_expert, R, wq, E, N, K, out, stream);
 }
 
 int mmq_gemm_grouped_q5_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,

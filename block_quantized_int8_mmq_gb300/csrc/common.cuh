@@ -103,8 +103,15 @@ int ensure_smem(const void* func, int bytes, SmemAttr& a);
 int tc_grouped_launch(int fmt, const void* xs, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
                       const int2* tiles, const int* ntiles, int64_t max_tiles, const int* row_end, const int* row_map,
                       float* out, cudaStream_t s);
+// the expanded path's grouped contraction over the grouping (activation rows read from xq
+// through perm; offsets[e + 1] = expert e's end in the sorted order)
+int tcx_grouped_launch(int fmt, const void* xq, int64_t R, const void* wq, int64_t E, int64_t N, int64_t K,
+                       const int2* tiles, const int* ntiles, int64_t max_tiles, const int* offsets, const int* perm,
+                       float* out, cudaStream_t s, const char* fn);
+// expert-grouped call: the grouping kernels, then the converter kernel (use_tc) or the
+// expanded path
 int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
-                   int64_t K, float* out, cudaStream_t s);
+                   int64_t K, float* out, cudaStream_t s, bool use_tc);
 int scratch_alloc(size_t bytes, cudaStream_t s, void** p, const char* fn);
 void scratch_free(void* p, cudaStream_t s);
 unsigned tc_take_error();

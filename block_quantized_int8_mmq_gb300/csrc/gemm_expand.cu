@@ -100,6 +100,19 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
                       v[6] | ((uint32_t)v[7] << 16));
 }
 
+// The device-built row grouping of an expert-grouped call (the grouping kernels of
+// grouped.cu): activation tile t holds expert-sorted rows tiles[t].x .. of expert
+// tiles[t].y, up to offsets[e + 1] (the expert's end); sorted row m is row perm[m] of the
+// caller's activations and output; expert e's weight rows are e * N .. e * N + N - 1 of the
+// stacked matrices, in ntpe weight tiles.
+struct Grouping {
+    const int2* tiles;
+    const int* ntiles;
+    const int* offsets;
+    const int* perm;
+    int ntpe;
+};
+
 // ---------------------------------------------------------------- expansion kernels
 // Piece p (0..511) of a chunk is the 16 bytes of row 8*(p/32) + p%8, values
 // 8*((p/8)%4) .. +7 of the block: offset p*16 is that row's core-matrix row, so the
@@ -124,19 +137,28 @@ __host__ __device__ constexpr int acts_split(bool split) { return GB / acts_bloc
 // the activation tiles
 __host__ __device__ constexpr bool split_acts(bool from_x, int64_t MT, int64_t NT) { return from_x && NT >= 4 * MT; }
 
-template <int FMT, bool FROM_X, bool SPLIT_A>
+// GROUPED: the quarter's rows are those of activation tile mt of the grouping, read from
+// xq through the permutation (tiles past the grouping's count are left alone).
+template <int FMT, bool FROM_X, bool SPLIT_A, bool GROUPED>
 __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __restrict__ x,
                                                  const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
                                                  int M, int nb, uint8_t* __restrict__ xa, uint8_t* __restrict__ ga,
-                                                 uint8_t* __restrict__ sm) {
+                                                 uint8_t* __restrict__ sm, const Grouping& gp) {
     constexpr int ROW = GB * Q8_1_BYTES;  // 288 bytes of one row per group
     constexpr int V = ROW / 16;           // 18
     constexpr int SROW = EXP_SROW;
     static_assert(FROM_X || !SPLIT_A, "the split is for the quantizing expansion");
     constexpr int JB = acts_blocks(SPLIT_A), SPLIT = acts_split(SPLIT_A);
     static_assert(SPLIT == 1 || JB <= 2, "columns of each AM piece");
+    static_assert(!GROUPED || !FROM_X, "grouped rows come quantized");
     const int mt = bx / (4 * SPLIT), h = (bx / SPLIT) & 3, j0 = (bx % SPLIT) * JB, ng = nb / GB;
-    const int m0 = mt * BM + h * EXP_ROWS;
+    int m0 = mt * BM + h * EXP_ROWS;
+    if constexpr (GROUPED) {
+        if (mt >= *gp.ntiles) return;  // uniform over the CTA
+        const int2 tl = gp.tiles[mt];
+        m0 = tl.x + h * EXP_ROWS;
+        M = gp.offsets[tl.y + 1];
+    }
     const size_t rowbytes = (size_t)nb * Q8_1_BYTES;
     // shared memory: row r of the quarter, block j0 + jj at r * SROW + jj * 36
     if (FROM_X) {
@@ -184,8 +206,10 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
         for (int i = threadIdx.x; i < EXP_ROWS * V; i += EXP_THREADS) {
             const int r = i / V, c = i % V;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (m0 + r < M)
-                v = __ldg(reinterpret_cast<const uint4*>(xq_in + (size_t)(m0 + r) * rowbytes + (size_t)g * ROW) + c);
+            if (m0 + r < M) {
+                const int src = GROUPED ? gp.perm[m0 + r] : m0 + r;
+                v = __ldg(reinterpret_cast<const uint4*>(xq_in + (size_t)src * rowbytes + (size_t)g * ROW) + c);
+            }
             *reinterpret_cast<uint4*>(sm + r * SROW + c * 16) = v;
         }
     }
@@ -234,10 +258,12 @@ __device__ __forceinline__ void expand_acts_body(int bx, int g, const float* __r
 // One CTA per (32-row quarter of a BNT-row tile, 256-value group) of the weights.  FOLD:
 // K-quant codes are q * sc_j (the contraction); without it, the raw nibbles (the block-dot
 // test hook).
-template <int FMT, bool FOLD, int BNT>
+// GROUPED: weight tile nt is tile nt % ntpe of expert nt / ntpe (experts without rows
+// are skipped).
+template <int FMT, bool FOLD, int BNT, bool GROUPED>
 __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
                                                     uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
-                                                    uint8_t* __restrict__ sm) {
+                                                    uint8_t* __restrict__ sm, const Grouping& gp) {
     constexpr int ROW = FMT == FMT_Q8_0 ? GB * Q8_0_BYTES : kq_bytes(FMT);  // 272 / 144 / 176 bytes per row per group
     constexpr int V = ROW / 16;                                             // 17 / 9 / 11
     constexpr int VP = V + 1;                                               // + one zero piece (Q8_0 reads 4 B past)
@@ -245,7 +271,14 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
     static_assert(SROW >= VP * 16 && SROW <= EXP_SROW, "row pad");
     constexpr int QPT = BNT / EXP_ROWS, WCH = wchunk(FMT, BNT);  // quarters per tile, bytes per (tile, block)
     const int nt = bx / QPT, h = bx % QPT, ng = nb / GB;
-    const int n0 = nt * BNT + h * EXP_ROWS;
+    // the quarter's first row in wq, and how many of its 32 rows exist
+    int w0 = nt * BNT + h * EXP_ROWS, nrows = N - w0;
+    if constexpr (GROUPED) {
+        const int e = nt / gp.ntpe, local = (nt % gp.ntpe) * BNT + h * EXP_ROWS;
+        if (gp.offsets[e] == gp.offsets[e + 1]) return;  // uniform over the CTA
+        w0 = e * N + local;
+        nrows = N - local;
+    }
     const size_t rowbytes = FMT == FMT_Q8_0 ? (size_t)nb * Q8_0_BYTES : (size_t)ng * kq_bytes(FMT);
     {
         // every load of a thread issued before its first store: one memory round trip
@@ -255,8 +288,8 @@ __device__ __forceinline__ void expand_weights_body(int bx, int g, const uint8_t
         for (int k = 0; k < NL; ++k) {
             const int i = threadIdx.x + k * EXP_THREADS, r = i / VP, c = i % VP;
             v[k] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < TOTAL && c < V && n0 + r < N)
-                v[k] = __ldg(reinterpret_cast<const uint4*>(wq + (size_t)(n0 + r) * rowbytes + (size_t)g * ROW) + c);
+            if (i < TOTAL && c < V && r < nrows)
+                v[k] = __ldg(reinterpret_cast<const uint4*>(wq + (size_t)(w0 + r) * rowbytes + (size_t)g * ROW) + c);
         }
 #pragma unroll
         for (int k = 0; k < NL; ++k) {
@@ -378,20 +411,27 @@ __device__ __forceinline__ uint2 q6_read8(const uint8_t* p) {  // 8 bytes at an 
     return make_uint2(__funnelshift_r(w0, w1, fs), __funnelshift_r(w1, w2, fs));
 }
 
-template <int BNT>
+template <int BNT, bool GROUPED>
 __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t* __restrict__ wq, int N, int nb,
                                                     uint8_t* __restrict__ xb, uint8_t* __restrict__ gw,
-                                                    uint8_t* __restrict__ sm) {
+                                                    uint8_t* __restrict__ sm, const Grouping& gp, long long wrows) {
     constexpr int GRAN = Q6_SROW / 16;
     constexpr int QPT = BNT / EXP_ROWS, PLANE = BNT * QK * 2, WCH = wchunk(FMT_Q6_K, BNT);  // two planes
     const int nt = bx / QPT, h = bx % QPT, ng = nb / GB;
-    const int n0 = nt * BNT + h * EXP_ROWS;
-    const long long rowbytes = (long long)ng * Q6_K_BYTES, end = (long long)N * rowbytes;
+    // the quarter's first row in wq, and how many of its 32 rows exist (wq holds wrows rows)
+    int w0 = nt * BNT + h * EXP_ROWS, nrows = N - w0;
+    if constexpr (GROUPED) {
+        const int e = nt / gp.ntpe, local = (nt % gp.ntpe) * BNT + h * EXP_ROWS;
+        if (gp.offsets[e] == gp.offsets[e + 1]) return;  // uniform over the CTA
+        w0 = e * N + local;
+        nrows = N - local;
+    }
+    const long long rowbytes = (long long)ng * Q6_K_BYTES, end = wrows * rowbytes;
     for (int i = threadIdx.x; i < EXP_ROWS * GRAN; i += EXP_THREADS) {
         const int r = i / GRAN, c = i % GRAN;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n0 + r < N) {
-            const long long a = (long long)(n0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
+        if (r < nrows) {
+            const long long a = (long long)(w0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
             const long long ga = (a & ~15ll) + 16 * c;
             if (ga < a + Q6_K_BYTES) {
                 if (ga + 16 <= end) {
@@ -408,7 +448,7 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
     }
     __syncthreads();
     auto sblk = [&](int r) -> const uint8_t* {  // super-block of row r of the quarter
-        const long long a = (long long)(n0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
+        const long long a = (long long)(w0 + r) * rowbytes + (long long)g * Q6_K_BYTES;
         return sm + r * Q6_SROW + (int)(a & 15);
     };
     uint8_t* dst = xb + ((size_t)nt * nb + (size_t)g * GB) * WCH + h * QCHUNK;
@@ -453,19 +493,20 @@ __device__ __forceinline__ void expand_weights_q6_k(int bx, int g, const uint8_t
 // Both expansions in one launch: CTAs 0 .. acts_x - 1 (grid x) expand the activations,
 // the rest the weights; grid y = the 256-value group.  The two halves are independent, so
 // they run side by side instead of one after the other.
-template <int FMT, bool FROM_X, bool FOLD, bool SPLIT_A, int BNT>
+template <int FMT, bool FROM_X, bool FOLD, bool SPLIT_A, int BNT, bool GROUPED = false>
 __global__ void __launch_bounds__(EXP_THREADS, 12)
 k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t* __restrict__ xq_out,
          const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
-         uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw) {
+         uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw, Grouping gp, long long wrows) {
     __shared__ __align__(16) uint8_t sm[EXP_ROWS * EXP_SROW];
     if ((int)blockIdx.x < acts_x) {
-        expand_acts_body<FMT, FROM_X, SPLIT_A>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm);
+        expand_acts_body<FMT, FROM_X, SPLIT_A, GROUPED>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm,
+                                                        gp);
     } else {
         if constexpr (FMT == FMT_Q6_K)  // the sub-scales are always folded (they are inside the block dot)
-            expand_weights_q6_k<BNT>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+            expand_weights_q6_k<BNT, GROUPED>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm, gp, wrows);
         else
-            expand_weights_body<FMT, FOLD, BNT>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm);
+            expand_weights_body<FMT, FOLD, BNT, GROUPED>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm, gp);
     }
     // the contraction may start its set-up now; it reads the scratch only after this
     // whole grid has completed (griddepcontrol.wait)
@@ -501,11 +542,17 @@ struct XLayout {
 // loads (16 columns, then the other 16 or 8) and hands the slot back before its last FMAs.  With K split over
 // gridDim.z CTAs per tile (small outputs), CTA z takes its share of the groups and writes
 // a partial tile.
-template <int FMT, bool DOTS, int BNT>
+//
+// GROUPED (expert-grouped call): CTA (x, y) takes weight tile x of the expert of
+// activation tile y of the grouping (CTAs past its count leave at once): the CTAs of one
+// activation tile are consecutive, and so are the tiles of one expert, so both operands
+// are reused from L2.  Sorted row m of the tile is stored to output row perm[m]; rows of
+// the next expert are not stored.
+template <int FMT, bool DOTS, int BNT, bool GROUPED = false>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const uint8_t* __restrict__ xb,
           const uint8_t* __restrict__ gw, int M, int N, int nb, float* __restrict__ out, int32_t* __restrict__ dots,
-          long long split_stride) {
+          long long split_stride, Grouping gp) {
     using L = XLayout<FMT, BNT>;
     constexpr bool MIN = is_kquant(FMT) && !DOTS;  // a min item closes every group
     constexpr int IPG = GB + (MIN ? 1 : 0);         // items per group
@@ -513,14 +560,25 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
     constexpr int EPI_COLS = BNT / (EPI_WARPS / 4);  // columns per epilogue warp: 32 (or 24)
     constexpr int H1 = EPI_COLS - 16;               // the second TMEM load's columns: 16 (or 8)
     static_assert(BNT == 128 || (BNT == 96 && !DOTS), "96-wide tiles for the contraction only");
+    static_assert(!GROUPED || !DOTS, "grouped calls are contractions");
     constexpr int NS = nstage(FMT);
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, nt = blockIdx.y;
-    const int m0 = mt * BM, n0 = nt * BNT;
+    const int mt = GROUPED ? blockIdx.y : blockIdx.x, nt = GROUPED ? blockIdx.x : blockIdx.y;
+    const int n0 = nt * BNT;
+    int m0 = mt * BM, wt = nt;  // first activation row; weight tile
+    if constexpr (GROUPED) {
+        // the tile list was written before the expansion: read it once that has completed
+        ptx::grid_dep_wait();
+        if (mt >= *gp.ntiles) return;  // uniform over the CTA: nothing set up yet
+        const int2 tl = gp.tiles[mt];
+        m0 = tl.x;
+        M = gp.offsets[tl.y + 1];
+        wt = tl.y * gp.ntpe + nt;
+    }
     const int ng = nb / GB;
     // K split z of gridDim.z takes groups g0 .. g1 - 1 and writes its partial tile to
     // out + z * split_stride (one split: the output itself); the indices below (items,
@@ -582,7 +640,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     const uint32_t dst = sbase + L::groups + gs * L::gslot;
                     ptx::mbar_arrive_expect_tx(bar(BAR_G_FULL + gs), GA + GW);
                     if (GA > 0) ptx::bulk_load(dst, ga + ((size_t)mt * ng + gg) * GA, GA, bar(BAR_G_FULL + gs));
-                    ptx::bulk_load(dst + GA, gw + ((size_t)nt * ng + gg) * GW, GW, bar(BAR_G_FULL + gs));
+                    ptx::bulk_load(dst + GA, gw + ((size_t)wt * ng + gg) * GW, GW, bar(BAR_G_FULL + gs));
                     g_issued = g + 1;
                 }
                 for (int j = 0; j < GB; ++j) {
@@ -594,7 +652,7 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
                     const uint32_t dst = sbase + L::stages + s * STAGE;
                     ptx::mbar_arrive_expect_tx(bar(BAR_ST_FULL + s), STAGE);
                     ptx::bulk_load(dst, xa + ((size_t)mt * nb + kk) * XCHUNK, XCHUNK, bar(BAR_ST_FULL + s));
-                    ptx::bulk_load(dst + XCHUNK, xb + ((size_t)nt * nb + kk) * WCH, WCH, bar(BAR_ST_FULL + s));
+                    ptx::bulk_load(dst + XCHUNK, xb + ((size_t)wt * nb + kk) * WCH, WCH, bar(BAR_ST_FULL + s));
                     st_issued = k + 1;
                 }
             }
@@ -728,7 +786,8 @@ k_mmq_tcx(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ ga, const 
         // the partial sums may now be read by a dependent launch once this grid is done
         ptx::grid_dep_launch_dependents();
         if (!DOTS && !*abort && mrow < M) {
-            float* orow = out + blockIdx.z * split_stride + (long long)mrow * N + n0 + c0;
+            const int orow_i = GROUPED ? gp.perm[mrow] : mrow;
+            float* orow = out + blockIdx.z * split_stride + (long long)orow_i * N + n0 + c0;
             const int ncols = N - (n0 + c0);  // columns of this warp's EPI_COLS that exist
             if (ncols >= EPI_COLS && (N & 3) == 0) {
 #pragma unroll
@@ -863,14 +922,15 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         const uint8_t* w8 = static_cast<const uint8_t*>(wq);
         if (x && !DOTS && split)
             k_expand<FMT, true, true, true, BNT><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
-                                                                       (int)acts_x, xa, ga, xb, gw);
+                                                                            (int)acts_x, xa, ga, xb, gw, Grouping{}, N);
         else if (x && !DOTS)
-            k_expand<FMT, true, true, false, BNT><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N, nb,
-                                                                        (int)acts_x, xa, ga, xb, gw);
+            k_expand<FMT, true, true, false, BNT><<<eg, EXP_THREADS, 0, s>>>(x, nullptr, xq_out, w8, (int)M, (int)N,
+                                                                             nb, (int)acts_x, xa, ga, xb, gw, Grouping{},
+                                                                             N);
         else
-            k_expand<FMT, false, FOLD, false, BNT><<<eg, EXP_THREADS, 0, s>>>(nullptr, static_cast<const uint8_t*>(xq),
-                                                                          nullptr, w8, (int)M, (int)N, nb,
-                                                                          (int)acts_x, xa, ga, xb, gw);
+            k_expand<FMT, false, FOLD, false, BNT><<<eg, EXP_THREADS, 0, s>>>(
+                nullptr, static_cast<const uint8_t*>(xq), nullptr, w8, (int)M, (int)N, nb, (int)acts_x, xa, ga, xb, gw,
+                Grouping{}, N);
     }
 
     {
@@ -890,7 +950,7 @@ int launch_on(const float* x, const void* xq, const void* wq, int64_t M, int64_t
         const cudaError_t e =
             cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, DOTS, BNT>, (const uint8_t*)xa, (const uint8_t*)ga, (const uint8_t*)xb,
                                (const uint8_t*)gw, (int)M, (int)N, nb, summed ? part : out, dots,
-                               summed ? sp.split_stride : 0LL);
+                               summed ? sp.split_stride : 0LL, Grouping{});
         if (e != cudaSuccess) {
             cudaGetLastError();
             report(fn, MMQ_ERR_LAUNCH, cudaGetErrorString(e));
@@ -1098,6 +1158,67 @@ int tcx_launch_noalloc(int fmt, const void* xq, const void* wq, int64_t M, int64
                              : launch_bn<FMT_Q4_K, false, true>(bn, nullptr, xq, wq, M, N, K, out, nullptr, ws, sp, s, fn);
 }
 
+// The expert-grouped contraction on the expanded path, after the grouping kernels: one
+// expansion launch (the activation tiles gathered through the permutation from xq, and
+// the weights of every expert with rows) and the contraction over the tile list, 128-wide
+// weight tiles, no K split.
+template <int FMT>
+int launch_grouped_x(const void* xq, int64_t R, const void* wq, int64_t E, int64_t N, int64_t K, const int2* tiles,
+                     const int* ntiles, int64_t max_tiles, const int* offsets, const int* perm, float* out,
+                     cudaStream_t s, const char* fn) {
+    const int nb = (int)(K / QK), ng = nb / GB;
+    const int64_t NTe = (N + BN - 1) / BN;
+    static SmemAttr attr;
+    const int st_attr = ensure_smem((const void*)k_mmq_tcx<FMT, false, BN, true>, XLayout<FMT, BN>::alloc, attr);
+    if (st_attr != MMQ_OK) {
+        report(fn, st_attr, "shared-memory request refused");
+        return st_attr;
+    }
+    const size_t b_xa = (size_t)(max_tiles * nb) * XCHUNK, b_ga = (size_t)(max_tiles * ng) * ga_bytes(FMT),
+                 b_xb = (size_t)(E * NTe * nb) * wchunk(FMT, BN), b_gw = (size_t)(E * NTe * ng) * gw_bytes(FMT, BN);
+    void* ws = nullptr;
+    const int st0 = scratch_alloc(b_xa + b_ga + b_xb + b_gw, s, &ws, fn);
+    if (st0 != MMQ_OK) return st0;
+    uint8_t* xa = static_cast<uint8_t*>(ws);
+    uint8_t* ga = xa + b_xa;
+    uint8_t* xb = ga + b_ga;
+    uint8_t* gw = xb + b_xb;
+    const Grouping gp{tiles, ntiles, offsets, perm, (int)NTe};
+    const int64_t acts_x = 4 * max_tiles;
+    int st = MMQ_OK;
+    {
+        ProfScope ps("k_expand", s);
+        const dim3 eg((unsigned)(acts_x + 4 * E * NTe), (unsigned)ng);
+        k_expand<FMT, false, true, false, BN, true><<<eg, EXP_THREADS, 0, s>>>(
+            nullptr, static_cast<const uint8_t*>(xq), nullptr, static_cast<const uint8_t*>(wq), (int)R, (int)N, nb,
+            (int)acts_x, xa, ga, xb, gw, gp, E * N);
+    }
+    {
+        ProfScope ps("k_mmq_tcx", s);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)NTe, (unsigned)max_tiles, 1u);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = XLayout<FMT, BN>::alloc;
+        cfg.stream = s;
+        cudaLaunchAttribute la[1];
+        la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        la[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = la;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_mmq_tcx<FMT, false, BN, true>, (const uint8_t*)xa,
+                                                 (const uint8_t*)ga, (const uint8_t*)xb, (const uint8_t*)gw, (int)R,
+                                                 (int)N, nb, out, (int32_t*)nullptr, 0LL, gp);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            report(fn, MMQ_ERR_LAUNCH, cudaGetErrorString(e));
+            st = MMQ_ERR_LAUNCH;
+        }
+    }
+    if (st == MMQ_OK) st = launch_status(fn);
+    scratch_free(ws, s);  // stream-ordered: after the kernels above
+    return st;
+}
+
 // K splits of the contraction: only when the output has fewer tiles than half the SMs,
 // as many as fill the SMs once (at most 8), each at least two 256-value groups.
 int tcx_splits(int fmt, int64_t M, int64_t N, int64_t K) {
@@ -1122,6 +1243,21 @@ int tcx_tile_n(int fmt, int64_t M, int64_t N) {
     if (2 * t128 <= sms) return BN;  // K splits fill the SMs instead
     const int64_t w128 = (t128 + sms - 1) / sms, w96 = (t96 + sms - 1) / sms;
     return 10 * w96 * 96 <= 9 * w128 * BN ? 96 : BN;
+}
+
+int tcx_grouped_launch(int fmt, const void* xq, int64_t R, const void* wq, int64_t E, int64_t N, int64_t K,
+                       const int2* tiles, const int* ntiles, int64_t max_tiles, const int* offsets, const int* perm,
+                       float* out, cudaStream_t s, const char* fn) {
+    if (4 * (max_tiles + E * ((N + BN - 1) / BN)) > 0x7fffffff || max_tiles > 65535) {
+        report(fn, MMQ_ERR_SHAPE, "too many tiles for the expansion grid");
+        return MMQ_ERR_SHAPE;
+    }
+    return fmt == FMT_Q8_0 ? launch_grouped_x<FMT_Q8_0>(xq, R, wq, E, N, K, tiles, ntiles, max_tiles, offsets, perm, out, s, fn)
+           : fmt == FMT_Q5_K
+               ? launch_grouped_x<FMT_Q5_K>(xq, R, wq, E, N, K, tiles, ntiles, max_tiles, offsets, perm, out, s, fn)
+           : fmt == FMT_Q6_K
+               ? launch_grouped_x<FMT_Q6_K>(xq, R, wq, E, N, K, tiles, ntiles, max_tiles, offsets, perm, out, s, fn)
+               : launch_grouped_x<FMT_Q4_K>(xq, R, wq, E, N, K, tiles, ntiles, max_tiles, offsets, perm, out, s, fn);
 }
 
 int tcx_set_wait_limit(unsigned long long ns) {

@@ -6,15 +6,23 @@
 //
 // Everything runs on the device, in stream order, so the call is asynchronous and can be
 // captured in a graph:
-//   k_group_count    per-expert row counts (rows whose id is outside [0, E) are not counted);
-//   k_group_plan     one CTA: exclusive scans of the counts and of the tiles per expert
+//   k_group_count    per-expert row counts (rows whose id is outside [0, E) are not counted):
+//                    per-CTA histograms in shared memory, one global add per CTA and expert;
+//   k_group_plan     one CTA (which also counts the ids itself, in shared memory, for up to
+//                    PLAN_COUNT_ROWS rows and SMEM_EXPERTS experts: then no k_group_count and
+//                    no clearing of the counts): exclusive scans of the counts and of the tiles per expert
 //                    (ceil(count / 128)) -> row offsets of each expert in the sorted order,
 //                    the tile list (first sorted row, expert) and its length;
-//   k_group_scatter  one warp per row: takes the next sorted slot of its expert, records the
-//                    original row for the store, copies the q8_1 row there; rows with an
-//                    out-of-range id get an all-zero output row instead;
-// then the tensor-core contraction over the tile list (gemm_tc.cu, GROUPED), which stores
-// each sorted row to its original row.  The order of rows within an expert depends on the
+//   k_group_scatter  a CTA per 256 rows: ranks its rows within each expert in shared
+//                    memory, reserves one range of sorted slots per expert (a global add on
+//                    the expert's cursor) and records each row's original index at its slot;
+//                    rows with an out-of-range id get an all-zero output row instead;
+//   k_group_copy     (the converter kernel only) one warp per sorted slot: the q8_1 row
+//                    copied there;
+// then a tensor-core contraction over the tile list, which stores each sorted row to its
+// original row: the converter kernel (gemm_tc.cu, GROUPED) on the sorted copy, or the
+// expanded path (gemm_expand.cu), whose expansion gathers each tile's rows from xq
+// through the permutation and expands the weights of every expert that has rows.  The order of rows within an expert depends on the
 // atomics, but every row's result is computed by the same arithmetic wherever it lands, so
 // the output does not depend on it.
 #include "common.cuh"
@@ -24,25 +32,60 @@ namespace {
 
 constexpr int GT = 128;          // rows per tile (the contraction's BM)
 constexpr int PLAN_THREADS = 1024;
+constexpr int SMEM_EXPERTS = 8192;  // per-expert counters in shared memory up to this many experts
+constexpr int GROUP_THREADS = 256;  // rows per counting / ranking CTA (one per thread)
 
-__global__ void k_group_count(const int32_t* __restrict__ row_expert, int R, int E, int* __restrict__ counts) {
-    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < R; r += gridDim.x * blockDim.x) {
-        const int e = row_expert[r];
-        if (e >= 0 && e < E) atomicAdd(&counts[e], 1);
+// Per-CTA counts in shared memory (E <= SMEM_EXPERTS), else global adds per row.
+__global__ void __launch_bounds__(GROUP_THREADS)
+k_group_count(const int32_t* __restrict__ row_expert, int R, int E, int* __restrict__ counts) {
+    extern __shared__ int hist[];
+    const bool local = E <= SMEM_EXPERTS;
+    if (local) {
+        for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+    }
+    const int r = blockIdx.x * GROUP_THREADS + threadIdx.x;
+    const int e = r < R ? row_expert[r] : -1;
+    if (e >= 0 && e < E) atomicAdd(local ? &hist[e] : &counts[e], 1);
+    if (local) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < E; i += blockDim.x)
+            if (hist[i]) atomicAdd(&counts[i], hist[i]);
     }
 }
 
+constexpr int PLAN_COUNT_ROWS = 65536;
+
+// counts == nullptr: the CTA counts the R ids of row_expert itself (E <= SMEM_EXPERTS)
 __global__ void __launch_bounds__(PLAN_THREADS)
-k_group_plan(const int* __restrict__ counts, int E, int* __restrict__ offsets, int* __restrict__ cursor,
-             int2* __restrict__ tiles, int* __restrict__ ntiles) {
+k_group_plan(const int32_t* __restrict__ row_expert, int R, const int* __restrict__ counts, int E,
+             int* __restrict__ offsets, int* __restrict__ cursor, int2* __restrict__ tiles, int* __restrict__ ntiles) {
+    extern __shared__ int hist[];
     __shared__ int s_rows[PLAN_THREADS], s_tiles[PLAN_THREADS];
     __shared__ int carry_rows, carry_tiles;
     const int t = threadIdx.x;
     if (t == 0) carry_rows = carry_tiles = 0;
+    if (!counts) {
+        for (int i = t; i < E; i += PLAN_THREADS) hist[i] = 0;
+        __syncthreads();
+        // eight ids per thread loaded before their adds (one memory round trip per batch)
+        constexpr int B = 8;
+        for (int r0 = 0; r0 < R; r0 += B * PLAN_THREADS) {
+            int ids[B];
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int r = r0 + u * PLAN_THREADS + t;
+                ids[u] = r < R ? row_expert[r] : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < B; ++u)
+                if (ids[u] >= 0 && ids[u] < E) atomicAdd(&hist[ids[u]], 1);
+        }
+    }
     __syncthreads();
     for (int base = 0; base < E; base += PLAN_THREADS) {
         const int e = base + t;
-        const int c = e < E ? counts[e] : 0;
+        const int c = e < E ? (counts ? counts[e] : hist[e]) : 0;
         const int nt = (c + GT - 1) / GT;
         s_rows[t] = c;
         s_tiles[t] = nt;
@@ -73,25 +116,49 @@ k_group_plan(const int* __restrict__ counts, int E, int* __restrict__ offsets, i
     }
 }
 
-__global__ void k_group_scatter(const uint8_t* __restrict__ xq, const int32_t* __restrict__ row_expert, int R, int E,
-                                int row16, int N, int* __restrict__ cursor, int* __restrict__ perm,
-                                uint8_t* __restrict__ xs, float* __restrict__ out) {
+// CTA c takes rows 256c .. 256c + 255; with E <= SMEM_EXPERTS it ranks them per expert in
+// shared memory and reserves one range of slots per expert, else one global add per row.
+__global__ void __launch_bounds__(GROUP_THREADS)
+k_group_scatter(const int32_t* __restrict__ row_expert, int R, int E, int N, int* __restrict__ cursor,
+                int* __restrict__ perm, float* __restrict__ out) {
+    extern __shared__ int hist[];  // E counters
+    const bool local = E <= SMEM_EXPERTS;
+    if (local) {
+        for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+    }
+    const int r = blockIdx.x * GROUP_THREADS + threadIdx.x;
+    const int e = r < R ? row_expert[r] : -1;
+    const bool valid = e >= 0 && e < E;
+    // the row's rank within its expert in this CTA (or, without the shared counters, its slot)
+    const int rank = !valid ? -1 : local ? atomicAdd(&hist[e], 1) : atomicAdd(&cursor[e], 1);
+    if (local) {
+        __syncthreads();
+        // one range of slots per expert with rows here: hist[e] becomes its first slot
+        for (int i = threadIdx.x; i < E; i += blockDim.x)
+            if (hist[i]) hist[i] = atomicAdd(&cursor[i], hist[i]);
+        __syncthreads();
+    }
+    if (valid) perm[local ? hist[e] + rank : rank] = r;
+    // an out-of-range id: an all-zero output row (the warp's such rows, one after another)
     const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
-        const int e = row_expert[r];
-        if (e < 0 || e >= E) {  // no expert: an all-zero output row
-            for (int n = lane; n < N; n += 32) out[(long long)r * N + n] = 0.f;
-            continue;
-        }
-        int pos = 0;
-        if (lane == 0) {
-            pos = atomicAdd(&cursor[e], 1);
-            perm[pos] = r;
-        }
-        pos = __shfl_sync(0xffffffffu, pos, 0);
-        const uint4* src = reinterpret_cast<const uint4*>(xq) + (long long)r * row16;
-        uint4* dst = reinterpret_cast<uint4*>(xs) + (long long)pos * row16;
+    unsigned bad = __ballot_sync(0xffffffffu, r < R && !valid);
+    while (bad) {
+        const int i = __ffs(bad) - 1;
+        bad &= bad - 1;
+        const long long row = (long long)(r - lane + i);
+        for (int n = lane; n < N; n += 32) out[row * N + n] = 0.f;
+    }
+}
+
+// The converter kernel's input: sorted row p (p < rows) is q8_1 row perm[p] of xq.
+__global__ void k_group_copy(const uint8_t* __restrict__ xq, const int* __restrict__ perm, const int* __restrict__ rows,
+                             int R, int row16, uint8_t* __restrict__ xs) {
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5), n = min(R, *rows);
+    for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n; p += warps) {
+        const uint4* src = reinterpret_cast<const uint4*>(xq) + (long long)perm[p] * row16;
+        uint4* dst = reinterpret_cast<uint4*>(xs) + (long long)p * row16;
         for (int i = lane; i < row16; i += 32) dst[i] = __ldg(src + i);
     }
 }
@@ -99,20 +166,22 @@ __global__ void k_group_scatter(const uint8_t* __restrict__ xq, const int32_t* _
 }  // namespace
 
 int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
-                   int64_t K, float* out, cudaStream_t s) {
+                   int64_t K, float* out, cudaStream_t s, bool use_tc) {
     const char* fn = fmt == FMT_Q8_0   ? "mmq_gemm_grouped_q8_0"
-                     : fmt == FMT_Q5_K ? "mmq_gemm_grouped_q5_k" : "mmq_gemm_grouped_q4_k";
+                     : fmt == FMT_Q5_K ? "mmq_gemm_grouped_q5_k"
+                     : fmt == FMT_Q6_K ? "mmq_gemm_grouped_q6_k" : "mmq_gemm_grouped_q4_k";
     const int64_t nb = K / QK, row_bytes = nb * Q8_1_BYTES;
     const int64_t max_tiles = (R + GT - 1) / GT + (E < R ? E : R);  // each expert adds at most one partial tile
     if (max_tiles > 65535) {
         report(fn, MMQ_ERR_SHAPE, "too many row tiles for the grid (R / 128 + min(E, R) > 65535)");
         return MMQ_ERR_SHAPE;
     }
-    // scratch: counts[E], offsets[E + 1], cursor[E], ntiles, tiles[max_tiles], perm[R], xs[R][row_bytes]
+    // scratch: counts[E], offsets[E + 1], cursor[E], ntiles, tiles[max_tiles], perm[R], and for
+    // the converter kernel xs[R][row_bytes]
     auto up = [](size_t b) { return (b + 255) / 256 * 256; };
     const size_t b_counts = up((size_t)E * 4), b_offsets = up((size_t)(E + 1) * 4), b_cursor = up((size_t)E * 4),
                  b_ntiles = 256, b_tiles = up((size_t)max_tiles * 8), b_perm = up((size_t)R * 4),
-                 b_xs = up((size_t)R * row_bytes);
+                 b_xs = use_tc ? up((size_t)R * row_bytes) : 0;
     void* ws = nullptr;
     int st = scratch_alloc(b_counts + b_offsets + b_cursor + b_ntiles + b_tiles + b_perm + b_xs, s, &ws, fn);
     if (st != MMQ_OK) return st;
@@ -123,31 +192,41 @@ int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R
     int* ntiles = reinterpret_cast<int*>(p += b_cursor);
     int2* tiles = reinterpret_cast<int2*>(p += b_ntiles);
     int* perm = reinterpret_cast<int*>(p += b_tiles);
-    uint8_t* xs = p + b_perm;
-    if (cudaMemsetAsync(counts, 0, (size_t)E * 4, s) != cudaSuccess) {
-        cudaGetLastError();
-        scratch_free(ws, s);
-        report(fn, MMQ_ERR_CUDA, "cudaMemsetAsync failed");
-        return MMQ_ERR_CUDA;
-    }
-    const int cgrid = (int)((R + 255) / 256 < 1184 ? (R + 255) / 256 : 1184);
-    {
+    uint8_t* xs = use_tc ? p + b_perm : nullptr;
+    const size_t hist_bytes = E <= SMEM_EXPERTS ? (size_t)E * 4 : 0;
+    const unsigned rgrid = (unsigned)((R + GROUP_THREADS - 1) / GROUP_THREADS);
+    const bool count_in_plan = R <= PLAN_COUNT_ROWS && E <= SMEM_EXPERTS;
+    if (!count_in_plan) {
+        if (cudaMemsetAsync(counts, 0, (size_t)E * 4, s) != cudaSuccess) {
+            cudaGetLastError();
+            scratch_free(ws, s);
+            report(fn, MMQ_ERR_CUDA, "cudaMemsetAsync failed");
+            return MMQ_ERR_CUDA;
+        }
         ProfScope ps("k_group_count", s);
-        k_group_count<<<cgrid, 256, 0, s>>>(row_expert, (int)R, (int)E, counts);
+        k_group_count<<<rgrid, GROUP_THREADS, hist_bytes, s>>>(row_expert, (int)R, (int)E, counts);
     }
     {
         ProfScope ps("k_group_plan", s);
-        k_group_plan<<<1, PLAN_THREADS, 0, s>>>(counts, (int)E, offsets, cursor, tiles, ntiles);
+        k_group_plan<<<1, PLAN_THREADS, count_in_plan ? hist_bytes : 0, s>>>(
+            row_expert, (int)R, count_in_plan ? nullptr : counts, (int)E, offsets, cursor, tiles, ntiles);
     }
     {
         ProfScope ps("k_group_scatter", s);
-        const int sgrid = (int)((R + 7) / 8 < 1184 ? (R + 7) / 8 : 1184);
-        k_group_scatter<<<sgrid, 256, 0, s>>>(static_cast<const uint8_t*>(xq), row_expert, (int)R, (int)E,
-                                              (int)(row_bytes / 16), (int)N, cursor, perm, xs, out);
+        k_group_scatter<<<rgrid, GROUP_THREADS, hist_bytes, s>>>(row_expert, (int)R, (int)E, (int)N, cursor, perm,
+                                                                 out);
+    }
+    if (use_tc) {
+        ProfScope ps("k_group_copy", s);
+        const int64_t cg = (R + 7) / 8;
+        k_group_copy<<<(unsigned)(cg < 4736 ? cg : 4736), 256, 0, s>>>(static_cast<const uint8_t*>(xq), perm,
+                                                                       offsets + E, (int)R, (int)(row_bytes / 16), xs);
     }
     st = launch_status(fn);
-    if (st == MMQ_OK)
+    if (st == MMQ_OK && use_tc)
         st = tc_grouped_launch(fmt, xs, wq, R, E, N, K, tiles, ntiles, max_tiles, offsets + 1, perm, out, s);
+    else if (st == MMQ_OK)
+        st = tcx_grouped_launch(fmt, xq, R, wq, E, N, K, tiles, ntiles, max_tiles, offsets, perm, out, s, fn);
     scratch_free(ws, s);  // stream-ordered: after the kernels above
     return st;
 }

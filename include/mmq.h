@@ -194,15 +194,22 @@ int mmq_linear_q6_k(const float* x, int64_t M, int64_t K, const void* wq, int64_
  * r < R, out[r] = xq[r] contracted with the weights of expert row_expert[r] ("When Does a
  * Kernel Win Surface?", sec. "Fused indexed-MoE prefill GEMM": rows counting-sorted by
  * expert into tiles of at most 128 rows, each tile staging one expert's weights once).
- * The grouping runs on the device (no host round trip; capturable).
+ * The grouping runs on the device (no host round trip; capturable).  The contraction over
+ * the tiles is the expanded-code tensor-core path (the activation tiles gathered from xq
+ * in sorted order, the weights of every expert that has rows expanded once per call), or,
+ * when mmq_set_path(MMQ_PATH_TC) is in force, the converter kernel (Q8_0, Q4_K, Q5_K; Q6_K
+ * is then refused with MMQ_ERR_ARG).
  *   xq: q8_1 [R][K/32] blocks, 16-byte aligned.  row_expert: int32 [R], 4-byte aligned.
  *   wq: E weight matrices stacked expert-major, expert e at row e*N ([E*N][K/32] Q8_0
- *   blocks or [E*N][K/256] Q4_K / Q5_K super-blocks), 16-byte aligned.  out: f32 [R][N], 16-byte
- *   aligned, fully overwritten; a row whose expert id is outside [0, E) gets zeros.
- * Accuracy as mmq_gemm_q8_0 / mmq_gemm_q4_k / mmq_gemm_q5_k, per row.  Needs K % 256 == 0 and
- * R / 128 + min(E, R) <= 65535.  Scratch about R*K*1.125 bytes (stream-ordered, as the
- * expanded path).
- * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE, MMQ_ERR_NULL, MMQ_ERR_ALIGN, MMQ_ERR_SMEM,
+ *   blocks or [E*N][K/256] Q4_K / Q5_K / Q6_K super-blocks), 16-byte aligned.  out: f32
+ *   [R][N], 16-byte aligned, fully overwritten; a row whose expert id is outside [0, E)
+ *   gets zeros.
+ * Accuracy as mmq_gemm_q8_0 / mmq_gemm_q4_k / mmq_gemm_q5_k / mmq_gemm_q6_k, per row.  Needs
+ * K % 256 == 0 and R / 128 + min(E, R) <= 65535.  Scratch (stream-ordered, as the expanded
+ * path): about R*K*1.125 bytes on the converter kernel; on the expanded path 3 bytes per
+ * activation value of up to R + 128*min(E, R) rows plus 2.25 bytes per weight value of the
+ * E*N weight rows (Q6_K: 4.25).
+ * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE, MMQ_ERR_NULL, MMQ_ERR_ALIGN, MMQ_ERR_ARG, MMQ_ERR_SMEM,
  * MMQ_ERR_NOMEM, MMQ_ERR_LAUNCH.
  */
 int mmq_gemm_grouped_q8_0(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
@@ -210,6 +217,8 @@ int mmq_gemm_grouped_q8_0(const void* xq, const int32_t* row_expert, int64_t R, 
 int mmq_gemm_grouped_q4_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
                           int64_t K, float* out, void* stream);
 int mmq_gemm_grouped_q5_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                          int64_t K, float* out, void* stream);
+int mmq_gemm_grouped_q6_k(const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
                           int64_t K, float* out, void* stream);
 
 /*

@@ -692,12 +692,20 @@ GROUPED_CASES = [  # (R, E, N, K, routing)
     (64, 128, 64, 256, "uniform"),      # more experts than rows: most experts empty
     (700, 8, 96, 512, "hot"),           # every row to one expert: several full tiles
     (257, 6, 136, 256, "invalid"),      # some ids out of range: zero rows
+    (2500, 40, 64, 256, "uniform"),     # several grouping CTAs (1024 rows each)
+    (300, 9000, 32, 256, "invalid"),    # more experts than the shared-memory counters hold
+    (70000, 24, 32, 256, "invalid"),    # more ids than the planning CTA counts itself
 ]
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
+@pytest.mark.parametrize("path", ["expand", "tc"])
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("case", range(len(GROUPED_CASES)))
-def test_grouped_parity(mmq, fmt, case):
+def test_grouped_parity(mmq, fmt, case, path):
+    """Both contractions over the device-built grouping: the expanded path (the default)
+    and the converter kernel (MMQ_PATH_TC; not Q6_K, refused below)."""
+    if fmt in NO_TC and path == "tc":
+        pytest.skip("the converter kernel takes Q8_0, Q4_K and Q5_K")
     R, E, N, K, routing = GROUPED_CASES[case]
     rng = np.random.default_rng(100 + case)
     if routing == "hot":
@@ -711,15 +719,21 @@ def test_grouped_parity(mmq, fmt, case):
     w = synth.weights(fmt, 300 + case, E * N, K)
     xq = mmq.mmq_quantize_q8_1(dev(x))
     out = torch.full((R, N), float("nan"), device="cuda")
-    mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K, out=out)
-    again = mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K)
+    set_path(mmq, "tc" if path == "tc" else "auto")
+    try:
+        mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K, out=out)
+        assert mmq.mmq_last_path() == PATH_IDS[path]
+        again = mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K)
+    finally:
+        set_path(mmq, "auto")
     assert mmq.mmq_get_device_error() == 0
     assert torch.equal(out, again), "grouped result depends on the run"
     ref, norm = grouped_reference(fmt, oracle.quantize_q8_1(x), ids, w, E, N, K)
     check_close(out.cpu().numpy(), ref, norm, f"grouped {fmt} {GROUPED_CASES[case]}")
 
 
-def test_grouped_graph_capture(mmq):
+@pytest.mark.parametrize("path", ["expand", "tc"])
+def test_grouped_graph_capture(mmq, path):
     R, E, N, K = 500, 12, 160, 512
     rng = np.random.default_rng(7)
     ids = rng.integers(0, E, R).astype(np.int32)
@@ -731,8 +745,12 @@ def test_grouped_graph_capture(mmq):
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        mmq.mmq_gemm_grouped("q4_k", xq, idd, wd, E, N, K, out=out, stream=s)
+    set_path(mmq, "tc" if path == "tc" else "auto")
+    try:
+        with torch.cuda.graph(g, stream=s):
+            mmq.mmq_gemm_grouped("q4_k", xq, idd, wd, E, N, K, out=out, stream=s)
+    finally:
+        set_path(mmq, "auto")
     g.replay()
     torch.cuda.synchronize()
     ref, norm = grouped_reference("q4_k", oracle.quantize_q8_1(x), ids, w, E, N, K)
@@ -750,3 +768,13 @@ def test_grouped_refusals(mmq):
     with pytest.raises(mmq.MMQError) as e:  # E < 1
         mmq.mmq_gemm_grouped("q4_k", xq, ids, w, 0, 8, 256)
     assert e.value.status == -1
+    out = torch.full((4, 8), float("nan"), device="cuda")
+    wq6 = torch.zeros((2 * 8, 210), dtype=torch.uint8, device="cuda")
+    set_path(mmq, "tc")
+    try:
+        with pytest.raises(mmq.MMQError) as e:  # Q6_K on the converter kernel
+            mmq.mmq_gemm_grouped("q6_k", xq, ids, wq6, 2, 8, 256, out=out)
+        assert e.value.status == -9
+    finally:
+        set_path(mmq, "auto")
+    assert torch.isnan(out).all(), "a refused call writes nothing"
