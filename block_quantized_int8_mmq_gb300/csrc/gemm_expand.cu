@@ -499,6 +499,10 @@ k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t
          const uint8_t* __restrict__ wq, int M, int N, int nb, int acts_x, uint8_t* __restrict__ xa,
          uint8_t* __restrict__ ga, uint8_t* __restrict__ xb, uint8_t* __restrict__ gw, Grouping gp, long long wrows) {
     __shared__ __align__(16) uint8_t sm[EXP_ROWS * EXP_SROW];
+    // the contraction's CTAs may be scheduled once every CTA of this grid has started (its
+    // set-up then overlaps this grid's last wave); it reads the scratch only after this
+    // whole grid has completed and its writes are visible (griddepcontrol.wait)
+    ptx::grid_dep_launch_dependents();
     if ((int)blockIdx.x < acts_x) {
         expand_acts_body<FMT, FROM_X, SPLIT_A, GROUPED>(blockIdx.x, blockIdx.y, x, xq_in, xq_out, M, nb, xa, ga, sm,
                                                         gp);
@@ -508,9 +512,6 @@ k_expand(const float* __restrict__ x, const uint8_t* __restrict__ xq_in, uint8_t
         else
             expand_weights_body<FMT, FOLD, BNT, GROUPED>(blockIdx.x - acts_x, blockIdx.y, wq, N, nb, xb, gw, sm, gp);
     }
-    // the contraction may start its set-up now; it reads the scratch only after this
-    // whole grid has completed (griddepcontrol.wait)
-    ptx::grid_dep_launch_dependents();
 }
 
 // ---------------------------------------------------------------- GEMM kernel
