@@ -950,11 +950,13 @@ def run_sweep(args):
             wcache[(fmt, proj, N)] = (synth.layer_weights(0, proj, N, K) if fmt == "q4_k" and proj != "wide"
                                       else synth.weights(fmt, synth.substream(synth.BASE_SEED + 5, N + K), N, K))
         w = wcache[(fmt, proj, N)]
-        # up to eight rows of a K % 256 == 0 weight (not Q6_K): each small-M kernel that can
-        # take the shape, besides the automatic choice
+        # up to eight rows of a K % 256 == 0 weight: each small-M kernel that can take the
+        # shape, besides the automatic choice (Q6_K: the dp4a stream at any M, in passes of
+        # up to four rows)
         routes = [("auto", mmq.SMALL_ROUTE_AUTO)]
-        if M <= 8 and fmt != "q6_k" and K % 256 == 0:
-            routes += ([("dp4a", mmq.SMALL_ROUTE_DP4A)] if M <= 4 else []) + [("mma", mmq.SMALL_ROUTE_MMA)]
+        if M <= 8 and K % 256 == 0:
+            routes += ([("dp4a", mmq.SMALL_ROUTE_DP4A)] if M <= 4 or fmt == "q6_k" else []) + \
+                [("mma", mmq.SMALL_ROUTE_MMA)]
         for (route_name, route) in routes:
             mmq.mmq_debug_small_route(route)
             try:

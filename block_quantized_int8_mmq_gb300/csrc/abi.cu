@@ -102,9 +102,11 @@ constexpr int64_t LIMIT = (int64_t)1 << 40;
 
 // Path choice for MMQ_PATH_AUTO from two cost models fitted to measurements on GB300
 // (microseconds, M from 8 to 384 on 512..18944 x 3584..18944 weights):
-// - the small-M streams take the weights once per pass of 8 activation rows (Q6_K: 4), at
-//   about 4.4 (Q6_K: 2.7) million weight values per microsecond, a quarter less when the
-//   weights are small (N * K below 32 M values: too little work per pass to fill the GPU);
+// - the small-M streams take the weights once per pass of 8 activation rows, at about 4.4
+//   million weight values per microsecond, a quarter less when the weights are small (N * K
+//   below 32 M values: too little work per pass to fill the GPU); Q6_K: its tensor-core
+//   stream's own model (q6_stream_cost_us: waves of CTAs times chunks per CTA), or, for
+//   the shapes that stream does not take, 4 rows per pass at 2.7 (0.82 of it when small);
 // - the expanded tensor-core path pays the code expansion (~0.6 us per million weight
 //   values; Q6_K, two planes: ~1.0) plus, per wave of output tiles (times their K splits)
 //   over the SMs, one CTA's pass over its share of K (~0.28 us per 32-block of a 128-wide
@@ -114,8 +116,9 @@ int auto_path(int fmt, int64_t M, int64_t N, int64_t K) {
     if (M <= 8 || K % QK_K != 0 || !tc_available()) return MMQ_PATH_SMALL;
     const bool q6 = fmt == FMT_Q6_K;
     const double nk = (double)N * (double)K;
+    const double t_q6s = q6 ? q6_stream_cost_us(M, N, K) : -1.0;
     const double rate = (q6 ? 2.7e6 : 4.4e6) * (nk < 32e6 ? (q6 ? 0.82 : 0.77) : 1.0);
-    const double t_small = (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * nk / rate + 1.5;
+    const double t_small = t_q6s >= 0 ? t_q6s : (double)(q6 ? (M + 3) / 4 : (M + 7) / 8) * nk / rate + 1.5;
     // with K split S ways (small outputs), S times the CTAs each take 1/S of the groups,
     // and a summing kernel follows
     const int64_t S = tcx_splits(fmt, M, N, K), ng = K / QK_K, bn = tcx_tile_n(fmt, M, N), sms = device_shape().sms;

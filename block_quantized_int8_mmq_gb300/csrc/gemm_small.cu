@@ -1342,13 +1342,442 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
 }
 
+// ------------------------------------------ Q6_K: k_mmq_q6_stream
+// The tensor-core stream for Q6_K: the weights are read once, and every block dot is taken
+// exactly on the tensor cores before its scales are applied ("13 . r7-r8 raw-byte MMQ
+// kernel", sec. 2; "When the Product Won't Collapse", sec. "The obstruction").
+// Copies.  A Q6_K row is nb/8 x 210 bytes, never a multiple of 16, so single rows cannot
+// be the lines of a tensor copy; eight consecutive rows are (8 x 210 = 105 x 16).  The
+// matrix is viewed as N/8 lines of eight rows, and a copy 16 lines high at byte offset
+// b * row + 420 c brings, for one b in 0..7, rows b, b + 8, ..., b + 120 of a 128-row box:
+// chunk c (super-blocks 2c, 2c + 1) of each, from the 16-byte boundary at or before it
+// (the chunk starts 0, 4, 8 or 12 bytes into its line when K % 512 == 0).  Eight copies
+// bring the box's 128 rows x one chunk; the pass's q8_1 rows for the chunk come by one
+// more.  Three chunks are in flight.
+// Roles.  Warp 16 issues the copies.  Once a chunk has landed, each of the 16 compute warps
+// turns one of its 16 q8_1 blocks into the MMAs' B operands for all of them (the f16 codes
+// in the k order below, the f32 xd pairs, and the centring terms: each sub-block's code
+// sum by dp4a and two shuffles); after a hardware barrier of the 16 warps, warp w takes
+// tile t = w >> 1 of the chunk: half 0 of super-block w & 1 and half 1 of the other.  (One warp converting every block
+// for the others ran at a fraction of their rate and held them up: measured.)  Tile t is
+// the 16 rows t, t + 8, ..., t + 120 of the box (one copy's lines, so the lanes' rows are
+// 432 bytes apart: distinct banks); the two partial sums of a tile meet in shared memory
+// at the end.
+// Arithmetic.  Each 16-value sub-block is one m16n8k16 f16 MMA on exact operands.  A 6-bit
+// code c is put together in place in an f16 half, its nibble and its two high bits
+// masked and shifted into the low bits: the subnormal c x 2^-24 (for the high nibbles of
+// the 128 low-bit bytes, 16 c x 2^-24, the 16 going into the sub-scale).  The MMA's
+// accumulator starts from the centring term -32 x sum(u) of the sub-block's activation
+// codes in the same unit (x 16 for the high nibbles).  Every partial sum is an integer
+// below 2^24 units, so each sum((c - 32) u) comes out exact.  The k order inside a
+// sub-block: thread (g, q) holds values 4q .. 4q + 3, k slots (2q, 2q + 1) taking values
+// (4q, 4q + 2) and slots (2q + 8, 2q + 9) values (4q + 1, 4q + 3), on both sides.  Rescale
+// in f32 pairs over the thread's two tokens: S += (xd, xd') (sc_a D_a + sc_b D_b) per block, then per
+// super-block acc += d 2^24 S.  The odd super-block of a chunk starts 2 bytes past a
+// 4-byte boundary: its words are put together from two aligned ones.
+// Small outputs split K over the CTAs of a cluster (grid z); their partial tiles are
+// added in rank order through distributed shared memory.  Needs K % 512 == 0, N % 8 == 0.
+constexpr int Q6S_TILES = 8;                          // 16-row tiles per box: 128 rows
+constexpr int Q6S_LINES = 2 * Q6S_TILES;              // eight-row lines per box
+constexpr int Q6S_CW = 2 * Q6S_TILES;                 // consumer warps
+constexpr int Q6S_THREADS = (Q6S_CW + 1) * 32;        // + the copy warp
+constexpr int Q6S_SLOTS = 3;
+constexpr int Q6S_CHUNK = 2 * Q6_K_BYTES;             // a row's bytes in one chunk: 420
+constexpr int Q6S_LB = 432;                           // bytes per line of a copy: the chunk and up to 12 before it
+constexpr int Q6S_COPY = Q6S_LINES * Q6S_LB;          // 6912
+constexpr int Q6S_WBYTES = 8 * Q6S_COPY;              // 55296
+constexpr int Q6S_XROW = 2 * IS_XROW;                 // a token's 16 q8_1 blocks of one chunk: 576
+constexpr int Q6S_ABYTES = 8 * Q6S_XROW;              // 4608
+constexpr int Q6S_CBLK = 32 * 16 + 4 * 16 + 4 * 8 + 16;  // per block: B operands, centring terms, xd pairs, pad
+constexpr int Q6S_CBYTES = 16 * Q6S_CBLK;             // 9728
+constexpr int Q6S_SLOT = Q6S_WBYTES + Q6S_ABYTES + Q6S_CBYTES;
+constexpr int Q6S_SMEM = Q6S_SLOTS * Q6S_SLOT + 2 * 8 * Q6S_SLOTS;  // + the full / empty barriers
+static_assert(Q6S_COPY % 128 == 0 && Q6S_SLOT % 128 == 0 && (Q6S_WBYTES + Q6S_ABYTES) % 16 == 0 &&
+                  Q6S_CBLK % 16 == 0 && Q6S_LB % 16 == 0 && Q6S_LB >= Q6S_CHUNK + 12,
+              "aligned regions");
+static_assert(Q6S_SMEM <= 227 * 1024, "one CTA per SM");
+static_assert(2 * 8 * 128 * 4 <= Q6S_SLOT, "the partial tiles fit in a slot");
+
+// the word at byte x of a row whose base p is 4-byte aligned (MIS false) or 2 bytes past
+// a 4-byte boundary (MIS true)
+template <bool MIS>
+__device__ __forceinline__ uint32_t q6s_word(const uint8_t* p, int x) {
+    if constexpr (MIS) {
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(p + x - 2);
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(p + x + 2);
+        return __byte_perm(lo, hi, 0x5432);
+    } else {
+        return *reinterpret_cast<const uint32_t*>(p + x);
+    }
+}
+template <int SH>
+__device__ __forceinline__ uint32_t q6s_shift(uint32_t v) {
+    if constexpr (SH >= 0)
+        return v << SH;
+    else
+        return v >> (-SH);
+}
+// byte u of a word of int8 values made unsigned (+128) as the exact f32 of the int8 value
+// (SIXTEENTH: a sixteenth of it): the byte in the low mantissa bits of 2^23 (2^19), then
+// 2^23 + 128 (2^19 + 8) subtracted
+template <bool SIXTEENTH>
+__device__ __forceinline__ float q6s_scale(uint32_t w, int u) {
+    if constexpr (SIXTEENTH)
+        return __uint_as_float(__byte_perm(w, 0x49000000u, 0x7440 + u)) - 524296.f;
+    else
+        return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440 + u)) - 8388736.f;
+}
+
+// The A operands of the sub-block pair of block jj (0..3) of a 128-value half from the
+// thread's words of the low-bit bytes (w0: values 4q .., w1: 16 + 4q .. of the block's
+// bytes) and of the high-bit bytes (h0, h1 likewise): [sub-block][even / odd pair].
+template <int JJ>
+__device__ __forceinline__ void q6s_codes(uint32_t w0, uint32_t w1, uint32_t h0, uint32_t h1, uint32_t (&a)[2][2]) {
+    constexpr bool HI = JJ >= 2;                          // the high nibbles: 16 c in place
+    constexpr uint32_t MK = HI ? 0x00F000F0u : 0x000F000Fu;
+    constexpr int UP = HI ? 8 : 4;                        // where the two high bits go
+    constexpr uint32_t BM = 0x00030003u << UP;
+    a[0][0] = (w0 & MK) | (q6s_shift<UP - 2 * JJ>(h0) & BM);
+    a[0][1] = ((w0 >> 8) & MK) | (q6s_shift<UP - 2 * JJ - 8>(h0) & BM);
+    a[1][0] = (w1 & MK) | (q6s_shift<UP - 2 * JJ>(h1) & BM);
+    a[1][1] = ((w1 >> 8) & MK) | (q6s_shift<UP - 2 * JJ - 8>(h1) & BM);
+}
+
+// Block blk (0..15) of a landed chunk's activations (as: [token][16 blocks of q8_1]) turned
+// into the compute warps' operands, in the converted area after the raw rows: per lane (g,
+// q) token g's B operands of both sub-blocks (values 4q .. 4q + 3 and 16 + 4q ..); the
+// quad's dp4a code sums give token g's centring terms, stored (lanes q = 0, 1) where a
+// compute lane reads tokens 2q', 2q' + 1 together, as is token g's xd (lane q = 2); lane
+// q = 3 writes the pad (one store per lane, no branch).
+__device__ __forceinline__ void q6s_convert(uint8_t* as, int blk, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    const uint8_t* xb = as + g * Q6S_XROW + blk * Q8_1_BYTES;
+    const uint32_t c0w = *reinterpret_cast<const uint32_t*>(xb + 4 + 4 * q);
+    const uint32_t c1w = *reinterpret_cast<const uint32_t*>(xb + 20 + 4 * q);
+    const uint32_t xdw = *reinterpret_cast<const uint32_t*>(xb);
+    int s0 = __dp4a((int)c0w, 0x01010101, 0), s1 = __dp4a((int)c1w, 0x01010101, 0);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    const uint32_t u0 = c0w ^ 0x80808080u, u1 = c1w ^ 0x80808080u;
+    uint4 bf;
+    bf.x = ks_code_pair(u0, 0x4240u);
+    bf.y = ks_code_pair(u0, 0x4341u);
+    bf.z = ks_code_pair(u1, 0x4240u);
+    bf.w = ks_code_pair(u1, 0x4341u);
+    uint8_t* cb = as + Q6S_ABYTES + blk * Q6S_CBLK;
+    *reinterpret_cast<uint4*>(cb + 16 * lane) = bf;
+    // -32 x sum(u) in units of 2^-24 (x 16 for the high nibbles: blocks 2, 3 of each half)
+    const float unit = (blk & 2) ? -512.f / 16777216.f : -32.f / 16777216.f;
+    const float v = q == 2 ? f16_bits_to_f32(xdw) : (float)(q ? s1 : s0) * unit;
+    const int off = q < 2 ? 512 + 16 * (g >> 1) + 4 * (g & 1) + 8 * q
+                          : (q == 2 ? 576 + 8 * (g >> 1) + 4 * (g & 1) : 608 + 4 * (g & 3));
+    *reinterpret_cast<float*>(cb + off) = v;
+}
+
+// mma_f16_16816 without the volatile qualifier: a pure function of its operands, which the
+// compiler may schedule among the surrounding work (several blocks' MMAs in flight)
+__device__ __forceinline__ void q6s_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Half H (blocks 4H .. 4H + 3) of one super-block of one 16-row tile: the thread's A rows g
+// (bytes at pg; weight row ng) and g + 8 (ph; weight row ng + 64); cv: the converted
+// activations of the super-block's eight blocks.  Accumulates into accg / acch (tokens 2q,
+// 2q + 1), or, with DOTS, writes the integer block dots of blocks b0 + 4H .. b0 + 4H + 3.
+template <bool MIS, bool DOTS, int H>
+__device__ __forceinline__ void q6s_half(const uint8_t* pg, const uint8_t* ph, const uint8_t* cv, int lane,
+                                         unsigned long long& accg, unsigned long long& acch, int32_t* dots, int M,
+                                         int N, int nb, int m0, int ng, int b0) {
+    const int q = lane & 3;
+    uint32_t scg[2], sch[2];  // the half's 8 int8 sub-scales of each row, made unsigned
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        scg[i] = q6s_word<MIS>(pg, 192 + 8 * H + 4 * i) ^ 0x80808080u;
+        sch[i] = q6s_word<MIS>(ph, 192 + 8 * H + 4 * i) ^ 0x80808080u;
+    }
+    unsigned long long sg = 0ull, sh = 0ull;
+    const uint32_t hg0 = q6s_word<MIS>(pg, 128 + 32 * H + 4 * q), hg1 = q6s_word<MIS>(pg, 144 + 32 * H + 4 * q);
+    const uint32_t hh0 = q6s_word<MIS>(ph, 128 + 32 * H + 4 * q), hh1 = q6s_word<MIS>(ph, 144 + 32 * H + 4 * q);
+#pragma unroll
+    for (int jo = 0; jo < 2; ++jo) {
+        const uint32_t wg0 = q6s_word<MIS>(pg, 64 * H + 32 * jo + 4 * q);
+        const uint32_t wg1 = q6s_word<MIS>(pg, 64 * H + 32 * jo + 16 + 4 * q);
+        const uint32_t wh0 = q6s_word<MIS>(ph, 64 * H + 32 * jo + 4 * q);
+        const uint32_t wh1 = q6s_word<MIS>(ph, 64 * H + 32 * jo + 16 + 4 * q);
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+            const int jj = jo + 2 * hi, blk = 4 * H + jj;
+            uint32_t ag[2][2], ah[2][2];
+            if (jj == 0) {
+                q6s_codes<0>(wg0, wg1, hg0, hg1, ag);
+                q6s_codes<0>(wh0, wh1, hh0, hh1, ah);
+            } else if (jj == 1) {
+                q6s_codes<1>(wg0, wg1, hg0, hg1, ag);
+                q6s_codes<1>(wh0, wh1, hh0, hh1, ah);
+            } else if (jj == 2) {
+                q6s_codes<2>(wg0, wg1, hg0, hg1, ag);
+                q6s_codes<2>(wh0, wh1, hh0, hh1, ah);
+            } else {
+                q6s_codes<3>(wg0, wg1, hg0, hg1, ag);
+                q6s_codes<3>(wh0, wh1, hh0, hh1, ah);
+            }
+            const uint8_t* cb = cv + blk * Q6S_CBLK;
+            const uint4 bf = *reinterpret_cast<const uint4*>(cb + 16 * lane);
+            const float4 bz = *reinterpret_cast<const float4*>(cb + 512 + 16 * q);
+            float D0[4] = {bz.x, bz.y, bz.x, bz.y}, D1[4] = {bz.z, bz.w, bz.z, bz.w};
+            q6s_mma(D0, ag[0][0], ah[0][0], ag[0][1], ah[0][1], bf.x, bf.y);
+            q6s_mma(D1, ag[1][0], ah[1][0], ag[1][1], ah[1][1], bf.z, bf.w);
+            const int s0 = 2 * jj, s1 = 2 * jj + 1;  // the block's sub-blocks among the half's 8
+            if constexpr (DOTS) {
+                const float unit = hi ? 1048576.f : 16777216.f;
+                const int cg0 = (int)((scg[s0 >> 2] >> (8 * (s0 & 3))) & 0xFFu) - 128;
+                const int cg1 = (int)((scg[s1 >> 2] >> (8 * (s1 & 3))) & 0xFFu) - 128;
+                const int ch0 = (int)((sch[s0 >> 2] >> (8 * (s0 & 3))) & 0xFFu) - 128;
+                const int ch1 = (int)((sch[s1 >> 2] >> (8 * (s1 & 3))) & 0xFFu) - 128;
+                const int v[4] = {cg0 * __float2int_rn(D0[0] * unit) + cg1 * __float2int_rn(D1[0] * unit),
+                                  cg0 * __float2int_rn(D0[1] * unit) + cg1 * __float2int_rn(D1[1] * unit),
+                                  ch0 * __float2int_rn(D0[2] * unit) + ch1 * __float2int_rn(D1[2] * unit),
+                                  ch0 * __float2int_rn(D0[3] * unit) + ch1 * __float2int_rn(D1[3] * unit)};
+                const int b = b0 + blk;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = m0 + 2 * q + (e & 1), n = ng + 64 * (e >> 1);
+                    if (m < M && n < N) dots[((long long)m * N + n) * nb + b] = v[e];
+                }
+            } else {
+                const float cg0 = hi ? q6s_scale<true>(scg[s0 >> 2], s0 & 3) : q6s_scale<false>(scg[s0 >> 2], s0 & 3);
+                const float cg1 = hi ? q6s_scale<true>(scg[s1 >> 2], s1 & 3) : q6s_scale<false>(scg[s1 >> 2], s1 & 3);
+                const float ch0 = hi ? q6s_scale<true>(sch[s0 >> 2], s0 & 3) : q6s_scale<false>(sch[s0 >> 2], s0 & 3);
+                const float ch1 = hi ? q6s_scale<true>(sch[s1 >> 2], s1 & 3) : q6s_scale<false>(sch[s1 >> 2], s1 & 3);
+                const unsigned long long xd = *reinterpret_cast<const unsigned long long*>(cb + 576 + 8 * q);
+                const unsigned long long tg = ptx::fma_f32x2(
+                    is_splat2(cg1), ptx::f2_bits(D1[0], D1[1]), ptx::mul_f32x2(is_splat2(cg0), ptx::f2_bits(D0[0], D0[1])));
+                const unsigned long long th = ptx::fma_f32x2(
+                    is_splat2(ch1), ptx::f2_bits(D1[2], D1[3]), ptx::mul_f32x2(is_splat2(ch0), ptx::f2_bits(D0[2], D0[3])));
+                sg = ptx::fma_f32x2(xd, tg, sg);
+                sh = ptx::fma_f32x2(xd, th, sh);
+            }
+        }
+    }
+    if constexpr (!DOTS) {
+        // d carries the 2^24 that undoes the weight operands' unit 2^-24
+        const uint32_t dwg = MIS ? (*reinterpret_cast<const uint32_t*>(pg + 206) >> 16)
+                                 : *reinterpret_cast<const uint32_t*>(pg + 208);
+        const uint32_t dwh = MIS ? (*reinterpret_cast<const uint32_t*>(ph + 206) >> 16)
+                                 : *reinterpret_cast<const uint32_t*>(ph + 208);
+        accg = ptx::fma_f32x2(is_splat2(f16_bits_to_f32(dwg) * 16777216.f), sg, accg);
+        acch = ptx::fma_f32x2(is_splat2(f16_bits_to_f32(dwh) * 16777216.f), sh, acch);
+    }
+}
+
+// hardware barrier 1 of the CTA over the compute warps, returning whether any of them
+// arrived with p set (every warp sees the same answer)
+__device__ __forceinline__ bool q6s_bar_any(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred b, 1, %2, a;\n selp.u32 %0, 1, 0, b;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "n"(Q6S_CW * 32)
+        : "memory");
+    return r != 0;
+}
+// one thread's bounded wait on an mbarrier phase, backing off between polls
+__device__ __forceinline__ bool q6s_wait1(uint32_t bar, uint32_t parity) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        __nanosleep(128);
+        if (ptx::globaltimer_ns() - t0 > DS_WAIT_LIMIT_NS) {
+            atomicOr(&g_small_error, ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <bool DOTS>
+__global__ void __launch_bounds__(Q6S_THREADS, 1)
+k_mmq_q6_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmXl, int M, int N, int nb, unsigned stagger_ns,
+                float* __restrict__ out, int32_t* __restrict__ dots) {
+    extern __shared__ __align__(128) uint8_t is_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const uint32_t full0 = ptx::smem_u32(is_smem + Q6S_SLOTS * Q6S_SLOT);
+    const uint32_t empty0 = full0 + 8 * Q6S_SLOTS;
+    const int nsb = nb / 8, nch = nsb / 2;
+    const long long rowb = (long long)nsb * Q6_K_BYTES;  // bytes per weight row
+    const int box = blockIdx.x, m0 = blockIdx.y * 8;
+    const int splits = gridDim.z, z = blockIdx.z;
+    const int c0 = (int)((long long)z * nch / splits), nmy = (int)((long long)(z + 1) * nch / splits) - c0;
+    const bool lastp = blockIdx.y == gridDim.y - 1;
+    const uint32_t abytes = (uint32_t)min(M - m0, 8) * Q6S_XROW;
+    const int CP = Q6S_CW;  // the copy warp
+    auto issue_w = [&](int i) {  // lane 0 of the copy warp: the weights of chunk c0 + i
+        const int sl = i % Q6S_SLOTS;
+        const uint32_t dst = ptx::smem_u32(is_smem + sl * Q6S_SLOT), bar = full0 + 8 * sl;
+        const long long cb = (long long)Q6S_CHUNK * (c0 + i);
+#pragma unroll 1
+        for (int b = 0; b < 8; ++b)
+            ptx::tma_load_2d(dst + b * Q6S_COPY, &tmW, bar, (int)(((b * rowb + cb) & ~15ll) >> 3), box * Q6S_LINES);
+    };
+    auto issue_x = [&](int i) {  // the pass's activation rows of chunk c0 + i
+        const int sl = i % Q6S_SLOTS;
+        ptx::tma_load_2d(ptx::smem_u32(is_smem + sl * Q6S_SLOT + Q6S_WBYTES), lastp ? &tmXl : &tmX, full0 + 8 * sl,
+                         (c0 + i) * (Q6S_XROW / 8), m0);
+    };
+    const int pre = min(nmy, Q6S_SLOTS);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Q6S_SLOTS; ++i) {
+            ptx::mbar_init(full0 + 8 * i, 1);
+            ptx::mbar_init(empty0 + 8 * i, Q6S_CW);
+        }
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    // programmatic dependent: the first weight chunk is requested before the previous kernel
+    // on the stream has completed; activations are read, and results written, after
+    uint64_t t_first = 0;
+    if (warp == CP && lane == 0) {
+        ptx::tma_prefetch_desc(&tmW);
+        ptx::tma_prefetch_desc(&tmX);
+        ptx::tma_prefetch_desc(&tmXl);
+        if (nmy > 0) {
+            ptx::mbar_arrive_expect_tx(full0, Q6S_WBYTES + abytes);
+            issue_w(0);
+            t_first = ptx::globaltimer_ns();
+        }
+    }
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
+
+    bool ok = true;
+    unsigned long long accg = 0ull, acch = 0ull;  // rows g / g + 8 of the warp's tile, tokens (2q, 2q + 1)
+    if (warp == CP) {
+        if (lane == 0) {
+            // the ring's first chunks one stagger apart (about one chunk's transfer time at
+            // the GPU's bandwidth share of this CTA), or as soon as the one before has landed:
+            // requested together, they arrive interleaved and the first lands only with the last
+            if (nmy > 0) issue_x(0);
+            for (int i = 1; i < pre; ++i) {
+                const uint64_t due = t_first + (uint64_t)i * stagger_ns;
+                while (ptx::globaltimer_ns() < due && !ptx::mbar_test_wait(full0 + 8 * (i - 1), 0)) __nanosleep(64);
+                ptx::mbar_arrive_expect_tx(full0 + 8 * i, Q6S_WBYTES + abytes);
+                issue_w(i);
+                issue_x(i);
+            }
+            int issued = pre;
+            for (int i = pre; i < nmy; ++i, ++issued) {
+                const int sl = i % Q6S_SLOTS;
+                if (!q6s_wait1(empty0 + 8 * sl, (i / Q6S_SLOTS - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive_expect_tx(full0 + 8 * sl, Q6S_WBYTES + abytes);
+                issue_w(i);
+                issue_x(i);
+            }
+            if (!ok) {
+            // copies still in flight must land before the CTA exits
+                for (int k = max(0, issued - Q6S_SLOTS); k < issued; ++k) {
+                    const uint64_t tb = ptx::globaltimer_ns();
+                    while (!ptx::mbar_try_wait(full0 + 8 * (k % Q6S_SLOTS), (k / Q6S_SLOTS) & 1))
+                        if (ptx::globaltimer_ns() - tb > DS_WAIT_LIMIT_NS) break;
+                }
+            }
+        }
+    } else {
+        const int t = warp >> 1, j = warp & 1;
+        const int ng = box * 128 + 8 * g + t;  // the weight row of the thread's first A row
+        // where the tile's rows start in their lines: (t * row + 420 c) mod 16, 0, 4, 8 or 12
+        const int rb16 = (int)(rowb & 15);
+        for (int i = 0; i < nmy; ++i) {
+            const int sl = i % Q6S_SLOTS;
+            // each compute warp converts one block of the landed chunk; the barrier then has
+            // every block converted, and tells every warp whether any wait ran out (a lone
+            // warp leaving the loop would leave the others at the barrier)
+            const bool landed = ds_wait(full0 + 8 * sl, (i / Q6S_SLOTS) & 1);
+            if (landed) q6s_convert(is_smem + sl * Q6S_SLOT + Q6S_WBYTES, warp, lane);
+            if (q6s_bar_any(!landed)) {
+                ok = false;
+                break;
+            }
+            const int c = c0 + i;
+            const uint8_t* slot = is_smem + sl * Q6S_SLOT;
+            const int o = (t * rb16 + 4 * c) & 15;
+            // super-block 0 of the chunk (4-byte aligned) and super-block 1 (2 bytes past):
+            // warp j takes half 0 of super-block j and half 1 of the other, so that every
+            // warp does one aligned and one misaligned half (equal work at the barrier)
+            const uint8_t* p0 = slot + t * Q6S_COPY + g * Q6S_LB + o;
+            const uint8_t* p1 = p0 + Q6_K_BYTES;
+            const uint8_t* cv0 = slot + Q6S_WBYTES + Q6S_ABYTES;
+            const uint8_t* cv1 = cv0 + 8 * Q6S_CBLK;
+            const int b00 = 16 * c, b01 = 16 * c + 8;
+            const int L8 = 8 * Q6S_LB;
+            if (j) {
+                q6s_half<true, DOTS, 0>(p1, p1 + L8, cv1, lane, accg, acch, dots, M, N, nb, m0, ng, b01);
+                q6s_half<false, DOTS, 1>(p0, p0 + L8, cv0, lane, accg, acch, dots, M, N, nb, m0, ng, b00);
+            } else {
+                q6s_half<false, DOTS, 0>(p0, p0 + L8, cv0, lane, accg, acch, dots, M, N, nb, m0, ng, b00);
+                q6s_half<true, DOTS, 1>(p1, p1 + L8, cv1, lane, accg, acch, dots, M, N, nb, m0, ng, b01);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty0 + 8 * sl);
+        }
+    }
+    const bool bad = __syncthreads_or(!ok);
+    // the tile's two partial sums ([super-block parity][token][128 rows] over slot 0), then
+    // their sum in place; every copy has landed by now
+    float* red = reinterpret_cast<float*>(is_smem);
+    if (!DOTS && !bad && warp < Q6S_CW) {
+        const int t = warp >> 1, j = warp & 1, r = 8 * g + t;  // box rows r and r + 64
+        float* rj = red + j * 1024;
+        rj[(2 * q) * 128 + r] = __uint_as_float((uint32_t)accg);
+        rj[(2 * q + 1) * 128 + r] = __uint_as_float((uint32_t)(accg >> 32));
+        rj[(2 * q) * 128 + r + 64] = __uint_as_float((uint32_t)acch);
+        rj[(2 * q + 1) * 128 + r + 64] = __uint_as_float((uint32_t)(acch >> 32));
+    }
+    __syncthreads();
+    if (!DOTS && !bad)
+        for (int e = threadIdx.x; e < 1024; e += Q6S_THREADS) red[e] += red[1024 + e];
+    if (splits > 1) {
+        // the cluster's CTAs (ranks 0 .. splits - 1 in K order) hold partial tiles; rank 0
+        // adds them in rank order and stores; nobody leaves while its tile may be read
+        ptx::cluster_sync();
+        if (!DOTS && !bad && ptx::cluster_ctarank() == 0) {
+            const uint32_t base = ptx::smem_u32(red);
+            for (int e = threadIdx.x; e < 1024; e += Q6S_THREADS) {
+                const int tok = e >> 7, n = box * 128 + (e & 127);
+                float v = 0.f;
+                for (int r = 0; r < splits; ++r) v += ptx::ld_cluster_f32(ptx::cluster_map(base + 4 * e, r));
+                if (n < N && m0 + tok < M) out[(long long)(m0 + tok) * N + n] = v;
+            }
+        }
+        ptx::cluster_sync();
+    } else {
+        __syncthreads();
+        if (!DOTS && !bad)
+            for (int e = threadIdx.x; e < 1024; e += Q6S_THREADS) {
+                const int tok = e >> 7, n = box * 128 + (e & 127);
+                if (n < N && m0 + tok < M) out[(long long)(m0 + tok) * N + n] = red[e];
+            }
+    }
+}
+
 // the activation maps of the streams: 8-row boxes for the full passes, and for the last pass
 // a box of its own rows (M - 8 (passes - 1)); copying rows past M as the copy engine's
 // zero fill was measured to slow a one-row pass down by a third
-inline bool make_act_maps(CUtensorMap* tx, CUtensorMap* txl, const uint8_t* x8, int64_t M, int nb) {
+inline bool make_act_maps(CUtensorMap* tx, CUtensorMap* txl, const uint8_t* x8, int64_t M, int nb,
+                          uint32_t box_bytes = IS_XROW) {
     const uint32_t last = (uint32_t)(M - 8 * ((M - 1) / 8));
-    return make_byte_map(tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, 8, 8) &&
-           make_byte_map(txl, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, IS_XROW, last, 8);
+    return make_byte_map(tx, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, box_bytes, 8, 8) &&
+           make_byte_map(txl, x8, (uint64_t)nb * Q8_1_BYTES, (uint64_t)M, box_bytes, last, 8);
 }
 
 // boxes per CTA: the fewest (at most max_boxes) that keep the grid within the two CTAs per
@@ -1423,6 +1852,54 @@ int launch_kq_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
     return launch_kq_stream_b<FMT, 16>(x8, w8, M, N, nb, out, dots, s, fn);
 }
 
+// the Q6_K tensor-core stream takes K % 512 == 0 (chunks of two super-blocks start 4-byte
+// aligned), N % 8 == 0 (the matrix as lines of eight rows) and lines below 2 GB
+bool q6_stream_fits(int64_t N, int nb) {
+    return nb % 16 == 0 && N % 8 == 0 && (int64_t)(nb / 8) * 8 * Q6_K_BYTES < ((int64_t)1 << 31);
+}
+
+// K split over clusters of 2, 4 or 8 CTAs while the grid still fits the SMs at one CTA each
+// (powers of two: clusters pack into the GPCs without leaving SMs over)
+int q6_stream_splits(int64_t boxes, int64_t passes, int64_t nch) {
+    int S = 1;
+    while (S < 8 && 2 * S <= nch && boxes * passes * 2 * S <= (int64_t)device_shape().sms) S *= 2;
+    return S;
+}
+
+template <bool DOTS>
+int launch_q6_stream_t(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
+                       int32_t* dots, cudaStream_t s, const char* fn) {
+    const int64_t nsb = nb / 8, nch = nsb / 2, boxes = (N + 127) / 128, passes = (M + 7) / 8;
+    const int S = q6_stream_splits(boxes, passes, nch);
+    static SmemAttr attr;
+    const int e = ensure_smem((const void*)k_mmq_q6_stream<DOTS>, Q6S_SMEM, attr);
+    if (e != MMQ_OK) {
+        report(fn, e, "shared-memory request refused");
+        return e;
+    }
+    CUtensorMap tw, tx, txl;
+    if (!make_byte_map(&tw, w8, (uint64_t)nsb * 8 * Q6_K_BYTES, (uint64_t)(N / 8), Q6S_LB, Q6S_LINES, 8) ||
+        !make_act_maps(&tx, &txl, x8, M, nb, Q6S_XROW)) {
+        report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
+        return MMQ_ERR_CUDA;
+    }
+    const dim3 grid((unsigned)boxes, (unsigned)passes, (unsigned)S);
+    // one chunk's transfer at this CTA's share of about 6 TB/s (bytes / (bytes per ns));
+    // at most 2 us (a bounded wait)
+    const int64_t ctas = std::min<int64_t>(boxes * passes * S, device_shape().sms);
+    const unsigned stagger = (unsigned)std::min<int64_t>(2000, (int64_t)(Q6S_WBYTES + 8 * Q6S_XROW) * ctas / 6000);
+    ProfScope ps("k_mmq_q6_stream", s);
+    return pdl_status(launch_pdl_zcluster(k_mmq_q6_stream<DOTS>, grid, dim3(Q6S_THREADS), (size_t)Q6S_SMEM, s,
+                                          (unsigned)S, tw, tx, txl, (int)M, (int)N, nb, stagger, out, dots),
+                      fn);
+}
+
+int launch_q6_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
+                     cudaStream_t s, const char* fn) {
+    return dots ? launch_q6_stream_t<true>(x8, w8, M, N, nb, out, dots, s, fn)
+                : launch_q6_stream_t<false>(x8, w8, M, N, nb, out, dots, s, fn);
+}
+
 template <int FMT>
 int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                      int32_t* dots, cudaStream_t s, const char* fn) {
@@ -1433,6 +1910,15 @@ int launch_i8_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N,
 }
 
 }  // namespace
+
+double q6_stream_cost_us(int64_t M, int64_t N, int64_t K) {
+    const int nb = (int)(K / QK);
+    if (K % QK_K != 0 || !q6_stream_fits(N, nb)) return -1.0;
+    const int64_t nch = nb / 16, boxes = (N + 127) / 128, passes = (M + 7) / 8, sms = device_shape().sms;
+    const int64_t S = q6_stream_splits(boxes, passes, nch);
+    const int64_t waves = (boxes * passes * S + sms - 1) / sms;
+    return (double)(waves * ((nch + S - 1) / S)) * 1.9 + 3.5;
+}
 
 unsigned small_take_error() {
     unsigned v = 0;
@@ -1462,12 +1948,16 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
                       : fmt == FMT_Q5_K ? "mmq_gemm_q5_k (small-M)"
                       : fmt == FMT_Q6_K ? "mmq_gemm_q6_k (small-M)" : "mmq_gemm_q4_k (small-M)";
     if (fmt == FMT_Q6_K) {
-        // the dp4a weight stream, 1, 2 or 4 activation rows per pass (one row per pass when
-        // four rows' activations do not fit in shared memory next to the ring)
         if (nb % 8 != 0) {
             report(sfn, MMQ_ERR_K_MULTIPLE, "Q6_K needs K % 256 == 0");
             return MMQ_ERR_K_MULTIPLE;
         }
+        // the tensor-core stream from two rows on (where its shape rules hold); else the
+        // dp4a weight stream, 1, 2 or 4 activation rows per pass (one row per pass when four
+        // rows' activations do not fit in shared memory next to the ring)
+        const int route = g_small_route.load();
+        if (q6_stream_fits(N, nb) && route != SMALL_ROUTE_DP4A && (M >= 2 || route == SMALL_ROUTE_MMA))
+            return launch_q6_stream(x8, w8, M, N, nb, out, dots, s, sfn);
         const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
         if (ds_smem_bytes(fmt, mt, mt == 1 ? 2 : 4, nb) <= 220 * 1024 && (M + mt - 1) / mt <= 65535)
             return launch_dp4a_stream<FMT_Q6_K>(x8, w8, M, N, nb, out, dots, s, sfn);

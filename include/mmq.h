@@ -298,13 +298,16 @@ int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* t
 
 /*
  * Which small-M kernel takes a shape on MMQ_PATH_SMALL (or on MMQ_PATH_AUTO when the
- * automatic choice is the small path), for K % 256 == 0 and every format but Q6_K:
+ * automatic choice is the small path), for K % 256 == 0:
  *   0  the measured choice (default): the dp4a weight stream for one row; for two rows
  *      when the weight has at most two 16-row tiles per SM and K >= 8192 (a long K through
  *      few tiles), or for Q5_K; for three or four rows only Q5_K with such a long K; the
- *      tensor-core stream otherwise;
- *   1  the dp4a weight stream for up to four rows, the tensor-core stream beyond;
+ *      tensor-core stream otherwise (Q6_K: from two rows on);
+ *   1  the dp4a weight stream for up to four rows, the tensor-core stream beyond (Q6_K:
+ *      the dp4a stream at every row count, four rows per pass);
  *   2  the tensor-core stream for every row count.
+ * Q6_K's tensor-core stream needs K % 512 == 0 and N % 8 == 0; other Q6_K shapes take the
+ * dp4a stream under every setting.
  * For measuring the two kernels on the same shape; results are within the same tolerance
  * either way, block dots bit-exact.  Returns the previous setting, or MMQ_ERR_ARG for a
  * route outside 0..2 (nothing changed).  Process-wide.

@@ -218,8 +218,6 @@ STREAM_SHAPES = [(1, 1, 256), (2, 7, 2304), (1, 300, 3584), (2, 77, 18944), (1, 
 @pytest.mark.parametrize("route", ["auto", "mma"])
 @pytest.mark.parametrize("fmt", FMTS)
 def test_few_row_stream_parity_and_dots(mmq, fmt, route):
-    if route == "mma" and fmt == "q6_k":
-        pytest.skip("Q6_K has no tensor-core stream")
     set_path(mmq, "small")
     mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_MMA if route == "mma" else mmq.SMALL_ROUTE_AUTO)
     try:
@@ -241,6 +239,48 @@ def few_row_cases(mmq, fmt):
             dots = mmq.block_dots(fmt, xq, dev(w), M, N, K)
             assert np.array_equal(dots.cpu().numpy(), oracle.block_dots(fmt, xq_ref, w, M, N, K)), \
                 f"{fmt} stream dots {M}x{N}x{K}"
+    assert mmq.mmq_get_device_error() == 0
+
+
+# the Q6_K tensor-core stream (K % 512 == 0, N % 8 == 0): 128-row boxes with rows past N
+# (8, 136, 1000, 4104 rows), one to eight rows and passes with rows past M, K split over
+# clusters of 1, 2, 4 and 8 CTAs (the split is chosen from the boxes and the K chunks:
+# S = 1 for 8 x 512, 2 for 136 x 1024, 4 for 1000 x 2048 and 3584 x 3584, 8 for 128 x 7168),
+# several passes (17 and 13 rows), and the one-row case the tensor-core route forces
+Q6S_SHAPES = [(1, 8, 512), (2, 136, 1024), (3, 1000, 2048), (8, 128, 7168), (5, 3584, 3584), (8, 4104, 4096),
+              (13, 264, 1536), (17, 64, 1024), (8, 18944, 512), (6, 2048, 18944)]
+
+
+@pytest.mark.parametrize("route", ["auto", "mma"])
+def test_q6_k_tensor_core_stream_parity_and_dots(mmq, route):
+    set_path(mmq, "small")
+    mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_MMA if route == "mma" else mmq.SMALL_ROUTE_AUTO)
+    try:
+        for (M, N, K) in Q6S_SHAPES:
+            x = synth.activations(M * 13 + N, M, K, True)
+            w = synth.weights("q6_k", N * 3 + K, N, K)
+            xq = mmq.mmq_quantize_q8_1(dev(x))
+            xq_ref = oracle.quantize_q8_1(x)
+            wd = dev(w)
+            out = torch.full((M, N), float("nan"), device="cuda")
+            mmq.gemm("q6_k", xq, wd, M, N, K, out=out)
+            again = mmq.gemm("q6_k", xq, wd, M, N, K)
+            assert torch.equal(out, again), f"{M}x{N}x{K}: not deterministic"
+            o = out.cpu().numpy()
+            assert not np.isnan(o).any(), f"{M}x{N}x{K}: output not fully written"
+            if M * N * K <= 2e9:
+                ref, norm = oracle.gemm("q6_k", xq_ref, w, M, N, K)
+                check_close(o, ref, norm, f"q6_k tensor-core stream {M}x{N}x{K}")
+            else:
+                im, inn = sample_entries(M, N, 1500, M + N)
+                ref, norm = oracle.gemm_at("q6_k", xq_ref, w, M, N, K, im, inn)
+                check_close(o[im, inn], ref, norm, f"q6_k tensor-core stream {M}x{N}x{K}")
+            if N * K <= 4200 * 4096:
+                dots = mmq.block_dots("q6_k", xq, wd, M, N, K)
+                assert np.array_equal(dots.cpu().numpy(), oracle.block_dots("q6_k", xq_ref, w, M, N, K)), \
+                    f"q6_k tensor-core stream dots {M}x{N}x{K}"
+    finally:
+        mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_AUTO)
     assert mmq.mmq_get_device_error() == 0
 
 
