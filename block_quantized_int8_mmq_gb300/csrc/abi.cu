@@ -78,6 +78,11 @@ int ensure_smem(const void* func, int bytes, SmemAttr& a) {
     return MMQ_OK;
 }
 
+// Time of the Q6_K tensor-core stream for M x N x K (us, measured on GB300: per wave of
+// CTAs, one per SM, ~1.9 us per two-super-block chunk of a CTA's share of K, plus ~3.5 us
+// until the first chunk is in), or -1 where the stream does not take the shape (gemm_small.cu).
+double q6_stream_cost_us(int64_t M, int64_t N, int64_t K);
+
 namespace {
 
 std::atomic<int> g_path{-1};

@@ -66,15 +66,11 @@ namespace mmq {
 int quantize_launch(const float* x, int64_t M, int64_t K, void* xq, cudaStream_t s);
 // which small-M kernel takes a shape with K % 256 == 0: the measured choice, the dp4a
 // weight stream (up to four rows per pass) or the tensor-core stream (eight rows per pass;
-// for Q6_K where K % 512 == 0 and N % 8 == 0).  small_set_route returns the previous setting.
+// not for Q6_K).  small_set_route returns the previous setting.
 enum SmallRoute { SMALL_ROUTE_AUTO = 0, SMALL_ROUTE_DP4A = 1, SMALL_ROUTE_MMA = 2 };
 int small_set_route(int route);
 int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                  int32_t* dots, cudaStream_t s);
-// Time of the Q6_K tensor-core stream for M x N x K (us, measured on GB300: per wave of
-// CTAs, one per SM, ~1.9 us per two-super-block chunk of a CTA's share of K, plus ~3.5 us
-// until the first chunk is in), or -1 where the stream does not take the shape.
-double q6_stream_cost_us(int64_t M, int64_t N, int64_t K);
 int tc_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
               int32_t* dots, cudaStream_t s);
 int tcx_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
@@ -142,28 +138,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-// launch_pdl with the grid's z dimension grouped into clusters of cz CTAs (cz <= 8; the
-// plain launch when cz == 1)
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_zcluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                unsigned cz, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = cz;
-    cfg.attrs = attr;
-    cfg.numAttrs = cz > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

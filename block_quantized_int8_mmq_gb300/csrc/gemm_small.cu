@@ -1342,6 +1342,51 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
 }
 
+// launch_pdl with the grid's z dimension grouped into clusters of cz CTAs (cz <= 8; the
+// plain launch when cz == 1)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_zcluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                unsigned cz, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = cz;
+    cfg.attrs = attr;
+    cfg.numAttrs = cz > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// cluster primitives of the Q6_K stream's K split
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives (release), then waits for all (acquire):
+// shared-memory writes before it are visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of the same shared-memory location in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // ------------------------------------------ Q6_K: k_mmq_q6_stream
 // The tensor-core stream for Q6_K: the weights are read once, and every block dot is taken
 // exactly on the tensor cores before its scales are applied ("13 . r7-r8 raw-byte MMQ
@@ -1749,17 +1794,17 @@ k_mmq_q6_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     if (splits > 1) {
         // the cluster's CTAs (ranks 0 .. splits - 1 in K order) hold partial tiles; rank 0
         // adds them in rank order and stores; nobody leaves while its tile may be read
-        ptx::cluster_sync();
-        if (!DOTS && !bad && ptx::cluster_ctarank() == 0) {
+        cluster_sync();
+        if (!DOTS && !bad && cluster_ctarank() == 0) {
             const uint32_t base = ptx::smem_u32(red);
             for (int e = threadIdx.x; e < 1024; e += Q6S_THREADS) {
                 const int tok = e >> 7, n = box * 128 + (e & 127);
                 float v = 0.f;
-                for (int r = 0; r < splits; ++r) v += ptx::ld_cluster_f32(ptx::cluster_map(base + 4 * e, r));
+                for (int r = 0; r < splits; ++r) v += ld_cluster_f32(cluster_map(base + 4 * e, r));
                 if (n < N && m0 + tok < M) out[(long long)(m0 + tok) * N + n] = v;
             }
         }
-        ptx::cluster_sync();
+        cluster_sync();
     } else {
         __syncthreads();
         if (!DOTS && !bad)
