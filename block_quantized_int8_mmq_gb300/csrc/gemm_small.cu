@@ -1997,11 +1997,14 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
             report(sfn, MMQ_ERR_K_MULTIPLE, "Q6_K needs K % 256 == 0");
             return MMQ_ERR_K_MULTIPLE;
         }
-        // the tensor-core stream from two rows on (where its shape rules hold); else the
-        // dp4a weight stream, 1, 2 or 4 activation rows per pass (one row per pass when four
-        // rows' activations do not fit in shared memory next to the ring)
+        // the tensor-core stream from two rows on (three on a long K through few rows:
+        // 3584 x 18944, two rows: 17.6 us on the dp4a stream against 22.3) where its shape
+        // rules hold; else the dp4a weight stream, 1, 2 or 4 activation rows per pass (one
+        // row per pass when four rows' activations do not fit in shared memory next to the ring)
         const int route = g_small_route.load();
-        if (q6_stream_fits(N, nb) && route != SMALL_ROUTE_DP4A && (M >= 2 || route == SMALL_ROUTE_MMA))
+        const bool q6_long_narrow = (N + 15) / 16 <= 2 * (int64_t)device_shape().sms && nb / 8 >= 32;
+        if (q6_stream_fits(N, nb) && route != SMALL_ROUTE_DP4A &&
+            (route == SMALL_ROUTE_MMA || M >= (q6_long_narrow ? 3 : 2)))
             return launch_q6_stream(x8, w8, M, N, nb, out, dots, s, sfn);
         const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
         if (ds_smem_bytes(fmt, mt, mt == 1 ? 2 : 4, nb) <= 220 * 1024 && (M + mt - 1) / mt <= 65535)

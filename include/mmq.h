@@ -302,7 +302,7 @@ int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* t
  *   0  the measured choice (default): the dp4a weight stream for one row; for two rows
  *      when the weight has at most two 16-row tiles per SM and K >= 8192 (a long K through
  *      few tiles), or for Q5_K; for three or four rows only Q5_K with such a long K; the
- *      tensor-core stream otherwise (Q6_K: from two rows on);
+ *      tensor-core stream otherwise (Q6_K: from two rows on, three on such a long K);
  *   1  the dp4a weight stream for up to four rows, the tensor-core stream beyond (Q6_K:
  *      the dp4a stream at every row count, four rows per pass);
  *   2  the tensor-core stream for every row count.
