@@ -159,8 +159,11 @@ int mmq_gemm_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
  *   out[m,n] = sum_b xd[m,b] * d * D[m,n,b],  D = sum_{k in b} xq[m,k] * (q[n,k] - 32) * sc
  * with sc the int8 scale of k's 16-value group and d that of the block's super-block (no
  * min term).  K % 256 == 0; alignment and accuracy as mmq_gemm_q8_0.  Runs on the
- * expanded-code tensor-core path and the small-M stream (4 activation rows per pass); the
- * converter kernel (MMQ_PATH_TC) refuses it with MMQ_ERR_ARG, and the small-M stream
+ * expanded-code tensor-core path and on two small-M kernels: the Q6_K tensor-core stream
+ * (8 activation rows per pass, for K % 512 == 0 and N % 8 == 0, from two rows on; the
+ * matrix copied as lines of eight rows, K split over a cluster for small N) and the dp4a
+ * stream (1, 2 or 4 rows per pass) for one row and the shapes the former does not take.
+ * The converter kernel (MMQ_PATH_TC) refuses it with MMQ_ERR_ARG, and the dp4a stream
  * refuses (MMQ_ERR_SHAPE) a K whose activation rows do not fit in shared memory (above
  * about 120000).
  */
