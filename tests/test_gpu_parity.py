@@ -284,6 +284,30 @@ def test_q6_k_tensor_core_stream_parity_and_dots(mmq, route):
     assert mmq.mmq_get_device_error() == 0
 
 
+# AUTO above eight Q6_K rows follows the Q6_K stream's cost model (waves of CTAs x chunks
+# per CTA) against the expanded path's; these are the measured sides of its crossovers on
+# GB300 (small / expanded, us): 16 x 18944 x 3584 31 / 106, 64 x 18944 x 3584 118 / 107,
+# 32 x 3584^2 15.1 / 23.7, 48 x 3584^2 29.0 / 24.4, 128 x 512 x 3584 11.1 / 15.3
+Q6_AUTO = [((16, 18944, 3584), "small"), ((64, 18944, 3584), "expand"), ((32, 3584, 3584), "small"),
+           ((48, 3584, 3584), "expand"), ((128, 512, 3584), "small")]
+
+
+def test_q6_k_auto_path_follows_the_stream_cost_model(mmq):
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the crossovers are those of a 152-SM GB300")
+    set_path(mmq, "auto")
+    for (M, N, K), want in Q6_AUTO:
+        x = synth.activations(M + N + K, M, K, True)
+        w = synth.weights("q6_k", N + 2 * K, N, K)
+        xq_ref = oracle.quantize_q8_1(x)
+        out = mmq.gemm("q6_k", mmq.mmq_quantize_q8_1(dev(x)), dev(w), M, N, K)
+        assert mmq.mmq_last_path() == PATH_IDS[want], f"{M}x{N}x{K}: path {mmq.mmq_last_path()}, expected {want}"
+        im, inn = sample_entries(M, N, 1000, M * 7 + N)
+        ref, norm = oracle.gemm_at("q6_k", xq_ref, w, M, N, K, im, inn)
+        check_close(out.cpu().numpy()[im, inn], ref, norm, f"q6_k auto {M}x{N}x{K}")
+    assert mmq.mmq_get_device_error() == 0
+
+
 # three to a hundred rows on the small path (the int8 tensor-core stream, 8 rows per pass):
 # passes with rows past M, weight tiles with rows past N, one to hundreds of tiles
 # (3, 5000, 512) and (4, 18944, 768): three or four rows of a wide weight, which the K-quants
