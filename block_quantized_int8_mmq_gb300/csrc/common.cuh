@@ -66,7 +66,7 @@ namespace mmq {
 int quantize_launch(const float* x, int64_t M, int64_t K, void* xq, cudaStream_t s);
 // which small-M kernel takes a shape with K % 256 == 0: the measured choice, the dp4a
 // weight stream (up to four rows per pass) or the tensor-core stream (eight rows per pass;
-// not for Q6_K).  small_set_route returns the previous setting.
+// for Q6_K where K % 512 == 0 and N % 8 == 0).  small_set_route returns the previous setting.
 enum SmallRoute { SMALL_ROUTE_AUTO = 0, SMALL_ROUTE_DP4A = 1, SMALL_ROUTE_MMA = 2 };
 int small_set_route(int route);
 int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,

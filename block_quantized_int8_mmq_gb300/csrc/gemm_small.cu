@@ -4,7 +4,9 @@
 //   k_mmq_dp4a_stream  one row (two for Q5_K and long K, up to four in a few cases, see
 //                      small_launch): per-warp weight streams, dp4a;
 //   k_mmq_i8_stream,   up to eight rows per pass on the tensor cores through mma.sync (Q8_0
-//   k_mmq_kq_stream    on s8, the K-quants on f16), per-warp rings of 2-D tensor copies;
+//   k_mmq_kq_stream    on s8, Q4_K and Q5_K on f16), per-warp rings of 2-D tensor copies;
+//   k_mmq_q6_stream    Q6_K, two to eight rows per pass on f16 (K % 512 == 0, N % 8 == 0):
+//                      the matrix copied as lines of eight rows, a CTA-wide chunk ring;
 //   k_mmq_small_mma, k_mmq_small  shapes the streams do not take (K % 256 != 0).
 // Each kernel's own comment describes it.
 //
