@@ -819,20 +819,23 @@ def run_moe(args):
     N=768 x K=2048, i.e. 16384 routed rows.  The grouping (count, scan, scatter) and the
     contraction are timed together, in CUDA-graph replays over rotating weight copies (> 3x
     L2).  The main line is Q4_K on the default (expanded) path; "lines" adds Q4_K on the
-    converter kernel and Q6_K experts, with each line's per-kernel device times."""
+    converter kernel and Q6_K experts, and a small batch (16 tokens: 128 routed rows, about
+    one per expert) where the automatic choice is the grouped weight stream, beside the
+    expanded path forced on the same call; each line with its per-kernel device times."""
     import torch
     import block_quantized_int8_mmq_gb300 as mmq
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
-    lines = [_moe_line(mmq, torch, dev, peaks, fmt, path, args)
-             for (fmt, path) in (("q4_k", "auto"), ("q4_k", "tc"), ("q6_k", "auto"))]
+    lines = [_moe_line(mmq, torch, dev, peaks, fmt, path, args, T)
+             for (fmt, path, T) in (("q4_k", "auto", 2048), ("q4_k", "tc", 2048), ("q6_k", "auto", 2048),
+                                    ("q4_k", "auto", 16), ("q4_k", "expand", 16), ("q6_k", "auto", 16))]
     main = dict(lines[0])
     main["lines"] = lines
     return main
 
 
-def _moe_line(mmq, torch, dev, peaks, fmt, path, args):
-    T, TOPK, E, N, K = 2048, 8, 128, 768, 2048
+def _moe_line(mmq, torch, dev, peaks, fmt, path, args, T=2048):
+    TOPK, E, N, K = 8, 128, 768, 2048
     R = T * TOPK
     rng = np.random.default_rng(synth.substream(synth.BASE_SEED + 6, 1))
     ids = np.stack([rng.permutation(E)[:TOPK] for _ in range(T)]).reshape(-1).astype(np.int32)
@@ -845,7 +848,8 @@ def _moe_line(mmq, torch, dev, peaks, fmt, path, args):
     idd = torch.from_numpy(ids).to(dev)
     out = torch.empty((R, N), device=dev)
     stream = torch.cuda.current_stream(dev)
-    prev_path = mmq.mmq_set_path(mmq.PATH_TC if path == "tc" else mmq.PATH_AUTO)
+    prev_path = mmq.mmq_set_path({"tc": mmq.PATH_TC, "expand": mmq.PATH_EXPAND, "small": mmq.PATH_SMALL,
+                                  "auto": mmq.PATH_AUTO}[path])
     try:
         for i in range(args.warmup):
             mmq.mmq_gemm_grouped(fmt, xq, idd, ws[i % copies], E, N, K, out=out, stream=stream)
@@ -899,7 +903,8 @@ def _moe_line(mmq, torch, dev, peaks, fmt, path, args):
     assert mmq.mmq_get_device_error(stream) == 0
     ms = statistics.median(x0.elapsed_time(x1) for (x0, x1) in ev) / iters
     ops = 2.0 * R * N * K
-    wbytes = w.nbytes
+    # the weights of the experts that received rows (each read at least once per call)
+    wbytes = w.nbytes // E * len(np.unique(ids))
     del ws
     return {"metric": "expert-grouped MMQ TOPS (2*R*N*K, R = routed rows)", "value": ops / (ms / 1e3) / 1e12,
             "unit": "TOPS", "ms_per_call": ms, "higher_is_better": True, "fmt": fmt, "path": used,
@@ -907,7 +912,8 @@ def _moe_line(mmq, torch, dev, peaks, fmt, path, args):
             "kernels_us": kernels,
             "weight_gbs": wbytes / (ms / 1e3) / 1e9, "frac_hbm_weights": wbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
             "n_gpus": 1, "steps": iters, "warmup": args.warmup, "data": "synthetic (seeded routing and weights)",
-            "config": {"workload": f"MoE prefill: 2048 tokens x top-8 of 128 experts, {fmt.upper()} experts 768x2048",
+            "config": {"workload": f"MoE {'prefill' if T >= 256 else 'small batch'}: {T} tokens x top-8 of 128 experts, "
+                                   f"{fmt.upper()} experts 768x2048" + (", forced path " + path if path != "auto" else ""),
                        "R": R, "E": E, "N": N, "K": K, "l2": f"rotating {copies} weight copies",
                        "cuda_graph": True},
             "clocks": clk}

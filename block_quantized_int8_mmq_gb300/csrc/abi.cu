@@ -78,6 +78,11 @@ int ensure_smem(const void* func, int bytes, SmemAttr& a) {
     return MMQ_OK;
 }
 
+// The expert-grouped call on the contraction `path` names (MMQ_PATH_AUTO: by the experts'
+// average fill); *taken: the one used (grouped.cu).
+int grouped_launch_path(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E,
+                        int64_t N, int64_t K, float* out, cudaStream_t s, int path, int* taken);
+
 // Time of the Q6_K tensor-core stream for M x N x K (us, measured on GB300: per wave of
 // CTAs, one per SM, ~1.9 us per two-super-block chunk of a CTA's share of K, plus ~3.5 us
 // until the first chunk is in), or -1 where the stream does not take the shape (gemm_small.cu).
@@ -238,8 +243,10 @@ int grouped(const char* fn, int fmt, const void* xq, const int32_t* row_expert, 
         report(fn, MMQ_ERR_ARG, "the converter tensor-core kernel takes Q8_0, Q4_K and Q5_K (Q6_K: the expanded path)");
         return MMQ_ERR_ARG;
     }
-    st = grouped_launch(fmt, xq, row_expert, R, wq, E, N, K, out, static_cast<cudaStream_t>(stream), use_tc);
-    if (st == MMQ_OK) t_last_path = use_tc ? MMQ_PATH_TC : MMQ_PATH_EXPAND;
+    int taken = MMQ_PATH_EXPAND;
+    st = grouped_launch_path(fmt, xq, row_expert, R, wq, E, N, K, out, static_cast<cudaStream_t>(stream),
+                             current_path(), &taken);
+    if (st == MMQ_OK) t_last_path = taken;
     return st;
 }
 

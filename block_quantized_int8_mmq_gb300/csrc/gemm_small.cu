@@ -399,11 +399,23 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// The expert-grouped form of the stream (GROUPED): CTA row y takes tile y of the grouping
+// kernels' list, up to MT rows of one expert in the sorted order: the weights of that
+// expert (wstride bytes apart), its activation rows and output rows through perm.
+struct DsGroup {
+    const int2* tiles;   // (first sorted row, expert), *ntiles of them
+    const int* ntiles;
+    const int* offsets;  // offsets[e + 1]: the end of expert e's rows in the sorted order
+    const int* perm;     // sorted row -> activation and output row
+    long long wstride;   // bytes of one expert's N x K weights
+    long long wend;      // bytes of all experts' weights
+};
+
 // S: slots per warp; 4 CTAs per SM with 2 slots, 2 CTAs per SM with 4 (64 copies in flight per SM)
-template <int FMT, int MT, int S>
+template <int FMT, int MT, int S, bool GROUPED>
 __global__ void __launch_bounds__(DS_WARPS * 32, S == 2 ? 4 : 2)
 k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq, int M, int N, int nb,
-                  float* __restrict__ out, int32_t* __restrict__ dots) {
+                  float* __restrict__ out, int32_t* __restrict__ dots, DsGroup grp) {
     constexpr int PU = ds_piece_units(FMT), UB = ds_unit_bytes(FMT), DS_SLOT = ds_slot(FMT);
     extern __shared__ __align__(128) uint8_t ds_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -416,8 +428,20 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
     // Q6_K keeps, in place of the block sums s, the integer code sums of each block's two
     // 16-value halves (int16 pairs) for the centring term
     uint32_t* xhs = reinterpret_cast<uint32_t*>(xsv);
-    const int m0 = blockIdx.y * MT;
-    const int ntok = min(MT, M - m0);
+    int m0 = blockIdx.y * MT, ntok = min(MT, M - m0);
+    long long woff = 0;  // byte offset of this CTA's weight matrix
+    if constexpr (GROUPED) {
+        // the tile list is the grouping kernels' output, and the tile names the expert: wait
+        // for them before anything (no weight prefetch ahead of the wait)
+        ptx::grid_dep_wait();
+        if ((int)blockIdx.y >= *grp.ntiles) return;
+        const int2 tl = grp.tiles[blockIdx.y];
+        m0 = tl.x;
+        ntok = min(MT, grp.offsets[tl.y + 1] - tl.x);
+        woff = (long long)tl.y * grp.wstride;
+    }
+    // activation / output row of the pass's token t
+    auto xrow_of = [&](int t) -> long long { return GROUPED ? (long long)grp.perm[m0 + t] : (long long)(m0 + t); };
     const int tw = gridDim.x * DS_WARPS, gw = blockIdx.x * DS_WARPS + warp;
     const int units = is_superblock(FMT) ? nb >> 3 : nb;  // super-blocks or blocks per row
     const int ppr = (units + PU - 1) / PU;             // pieces per row
@@ -434,7 +458,8 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
             // 210-byte super-blocks leave rows 2-byte aligned: copy the 16-byte granules that
             // hold the piece (the consumer starts at the piece's offset in the first one).
             // The buffer's bytes past its last whole granule come by plain loads instead.
-            const long long a = n * row_bytes + (long long)u0 * UB, end = (long long)N * row_bytes;
+            const long long a = woff + n * row_bytes + (long long)u0 * UB;
+            const long long end = GROUPED ? grp.wend : (long long)N * row_bytes;
             const long long a0 = a & ~15ll, lim = end & ~15ll;
             long long a1 = (a + (long long)nu * UB + 15) & ~15ll;
             uint8_t* slot = ring + (q % S) * DS_SLOT;
@@ -448,7 +473,7 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
             return;
         }
         ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nu * UB));
-        ptx::bulk_load(ptx::smem_u32(ring + (q % S) * DS_SLOT), wq + n * row_bytes + (long long)u0 * UB,
+        ptx::bulk_load(ptx::smem_u32(ring + (q % S) * DS_SLOT), wq + woff + n * row_bytes + (long long)u0 * UB,
                        (uint32_t)(nu * UB), bar);
     };
     int issued = 0;  // pieces whose copies were issued (kept by every lane)
@@ -470,7 +495,7 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
         const int t = e / nb, b = e - t * nb;
         uint32_t h = 0u, c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (t < ntok) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((long long)(m0 + t) * nb + b) * Q8_1_BYTES);
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + (xrow_of(t) * nb + b) * Q8_1_BYTES);
             h = __ldg(src);
 #pragma unroll
             for (int i = 0; i < 8; ++i) c[i] = __ldg(src + 1 + i);
@@ -512,7 +537,7 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
                 if (sl < nu) {
                     // the super-block starts at an even byte of the slot: read 4-byte words from
                     // the word boundary below it and funnel-shift by 0 or 16 bits
-                    const int bs = (int)((n * row_bytes + (long long)u0 * UB) & 15) + sl * Q6_K_BYTES;
+                    const int bs = (int)((woff + n * row_bytes + (long long)u0 * UB) & 15) + sl * Q6_K_BYTES;
                     const uint32_t* wa = reinterpret_cast<const uint32_t*>(pc + (bs & ~3));
                     const int fs = (bs & 2) * 8;
                     // half h: low-nibble bytes 64h .. 64h + 63, high-part bytes 128 + 32h ..
@@ -720,7 +745,7 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
                 float v = acc[t];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0 && t < ntok) out[(long long)(m0 + t) * N + n] = v;
+                if (lane == 0 && t < ntok) out[xrow_of(t) * N + n] = v;
             }
         }
     }
@@ -734,13 +759,16 @@ k_mmq_dp4a_stream(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ wq
     }
 }
 
-template <int FMT, int MT, int S>
+// GROUPED: grid row y takes tile y of the grouping's list (gtiles rows of CTAs, those past
+// the list's length return at once)
+template <int FMT, int MT, int S, bool GROUPED = false>
 int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
-                         int32_t* dots, cudaStream_t s, const char* fn) {
+                         int32_t* dots, cudaStream_t s, const char* fn, const DsGroup& grp = DsGroup{},
+                         int64_t gtiles = 0) {
     const int smem = ds_smem_bytes(FMT, MT, S, nb);
     static SmemAttr attr;
     if (smem > 48 * 1024) {
-        const int e = ensure_smem((const void*)k_mmq_dp4a_stream<FMT, MT, S>, smem, attr);
+        const int e = ensure_smem((const void*)k_mmq_dp4a_stream<FMT, MT, S, GROUPED>, smem, attr);
         if (e != MMQ_OK) {
             report(fn, e, "shared-memory request refused");
             return e;
@@ -752,15 +780,30 @@ int launch_dp4a_stream_s(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_
     const DeviceShape ds = device_shape();
     const int per_sm = std::max(1, std::min(S == 2 ? 4 : 2, ds.smem_per_sm / (smem + 1024)));
     const int64_t max_warps = (int64_t)ds.sms * per_sm * DS_WARPS;
-    const int64_t rpw = (N + max_warps - 1) / max_warps;
+    // grouped: 16 weight rows per warp (a CTA stages its tile's activations once for 128
+    // rows; measured against 4, 8 and 32 on 128 experts of 768 x 2048: the fastest or within
+    // 2 % at 1 to 16 rows per expert)
+    const int64_t rpw = GROUPED ? 16 : (N + max_warps - 1) / max_warps;
     const int64_t ctas = (N + DS_WARPS * rpw - 1) / (DS_WARPS * rpw);
-    dim3 grid((unsigned)ctas, (unsigned)((M + MT - 1) / MT));
+    dim3 grid((unsigned)ctas, (unsigned)(GROUPED ? gtiles : (M + MT - 1) / MT));
     {
         ProfScope ps("k_mmq_dp4a_stream", s);
-        return pdl_status(launch_pdl(k_mmq_dp4a_stream<FMT, MT, S>, grid, dim3(DS_WARPS * 32), (size_t)smem, s, x8, w8,
-                                     (int)M, (int)N, nb, out, dots),
+        return pdl_status(launch_pdl(k_mmq_dp4a_stream<FMT, MT, S, GROUPED>, grid, dim3(DS_WARPS * 32), (size_t)smem, s,
+                                     x8, w8, (int)M, (int)N, nb, out, dots, grp),
                           fn);
     }
+}
+
+// the grouped stream for tiles of mt rows (1, 2 or 4), slots as for that many dense rows
+template <int FMT>
+int launch_dp4a_grouped(const uint8_t* x8, const uint8_t* w8, int64_t R, int64_t N, int nb, int mt, float* out,
+                        cudaStream_t s, const char* fn, const DsGroup& g, int64_t gtiles) {
+    if (mt <= 1)
+        return FMT == FMT_Q6_K
+                   ? launch_dp4a_stream_s<FMT, 1, 4, true>(x8, w8, R, N, nb, out, nullptr, s, fn, g, gtiles)
+                   : launch_dp4a_stream_s<FMT, 1, 2, true>(x8, w8, R, N, nb, out, nullptr, s, fn, g, gtiles);
+    if (mt <= 2) return launch_dp4a_stream_s<FMT, 2, 4, true>(x8, w8, R, N, nb, out, nullptr, s, fn, g, gtiles);
+    return launch_dp4a_stream_s<FMT, 4, 4, true>(x8, w8, R, N, nb, out, nullptr, s, fn, g, gtiles);
 }
 
 // Two slots and four CTAs per SM (more warps to hide the math) for one activation row;
@@ -1965,6 +2008,31 @@ double q6_stream_cost_us(int64_t M, int64_t N, int64_t K) {
     const int64_t S = q6_stream_splits(boxes, passes, nch);
     const int64_t waves = (boxes * passes * S + sms - 1) / sms;
     return (double)(waves * ((nch + S - 1) / S)) * 1.9 + 3.5;
+}
+
+// The expert-grouped contraction on the dp4a weight stream (tiles of at most mt = 1, 2 or 4
+// rows of one expert, from the grouping kernels): for experts with few rows, where a
+// 128-row tensor-core tile would be almost empty and the expanded path would expand every
+// such expert's weights.  false from small_grouped_fits: not for this shape.
+bool small_grouped_fits(int fmt, int64_t K, int mt) {
+    const int nb = (int)(K / QK);
+    return nb % 8 == 0 && ds_smem_bytes(fmt, mt <= 1 ? 1 : mt <= 2 ? 2 : 4, mt <= 1 && fmt != FMT_Q6_K ? 2 : 4, nb) <=
+                              220 * 1024;
+}
+
+int small_grouped_launch(int fmt, const void* xq, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
+                         const int2* tiles, const int* ntiles, int64_t max_tiles, const int* offsets, const int* perm,
+                         int mt, float* out, cudaStream_t s, const char* fn) {
+    const int nb = (int)(K / QK);
+    const long long row_bytes =
+        is_superblock(fmt) ? (long long)(nb / 8) * kq_bytes(fmt) : (long long)nb * Q8_0_BYTES;
+    const DsGroup g{tiles, ntiles, offsets, perm, (long long)N * row_bytes, (long long)E * N * row_bytes};
+    const uint8_t* x8 = static_cast<const uint8_t*>(xq);
+    const uint8_t* w8 = static_cast<const uint8_t*>(wq);
+    return fmt == FMT_Q8_0   ? launch_dp4a_grouped<FMT_Q8_0>(x8, w8, R, N, nb, mt, out, s, fn, g, max_tiles)
+           : fmt == FMT_Q5_K ? launch_dp4a_grouped<FMT_Q5_K>(x8, w8, R, N, nb, mt, out, s, fn, g, max_tiles)
+           : fmt == FMT_Q6_K ? launch_dp4a_grouped<FMT_Q6_K>(x8, w8, R, N, nb, mt, out, s, fn, g, max_tiles)
+                             : launch_dp4a_grouped<FMT_Q4_K>(x8, w8, R, N, nb, mt, out, s, fn, g, max_tiles);
 }
 
 unsigned small_take_error() {

@@ -19,10 +19,14 @@
 //                    rows with an out-of-range id get an all-zero output row instead;
 //   k_group_copy     (the converter kernel only) one warp per sorted slot: the q8_1 row
 //                    copied there;
-// then a tensor-core contraction over the tile list, which stores each sorted row to its
-// original row: the converter kernel (gemm_tc.cu, GROUPED) on the sorted copy, or the
-// expanded path (gemm_expand.cu), whose expansion gathers each tile's rows from xq
-// through the permutation and expands the weights of every expert that has rows.  The order of rows within an expert depends on the
+// then a contraction over the tile list, which stores each sorted row to its original row:
+// the converter kernel (gemm_tc.cu, GROUPED) on the sorted copy, the expanded path
+// (gemm_expand.cu), whose expansion gathers each tile's rows from xq through the
+// permutation and expands the weights of every expert that has rows, or, for experts with
+// few rows, the dp4a weight stream (gemm_small.cu, GROUPED) over tiles of 2 or 4 rows: the
+// tile height follows the experts' fill ("Fused indexed-MoE prefill GEMM", dynamic M-tile),
+// 128-row tensor-core tiles where experts have many rows, weight-streaming tiles where a
+// 128-row tile would be almost empty.  The order of rows within an expert depends on the
 // atomics, but every row's result is computed by the same arithmetic wherever it lands, so
 // the output does not depend on it.
 #include "common.cuh"
@@ -30,7 +34,7 @@
 namespace mmq {
 namespace {
 
-constexpr int GT = 128;          // rows per tile (the contraction's BM)
+constexpr int GT = 128;          // rows per tile of the tensor-core contractions (their BM)
 constexpr int PLAN_THREADS = 1024;
 constexpr int SMEM_EXPERTS = 8192;  // per-expert counters in shared memory up to this many experts
 constexpr int GROUP_THREADS = 256;  // rows per counting / ranking CTA (one per thread)
@@ -58,7 +62,7 @@ constexpr int PLAN_COUNT_ROWS = 65536;
 
 // counts == nullptr: the CTA counts the R ids of row_expert itself (E <= SMEM_EXPERTS)
 __global__ void __launch_bounds__(PLAN_THREADS)
-k_group_plan(const int32_t* __restrict__ row_expert, int R, const int* __restrict__ counts, int E,
+k_group_plan(const int32_t* __restrict__ row_expert, int R, const int* __restrict__ counts, int E, int gt,
              int* __restrict__ offsets, int* __restrict__ cursor, int2* __restrict__ tiles, int* __restrict__ ntiles) {
     extern __shared__ int hist[];
     __shared__ int s_rows[PLAN_THREADS], s_tiles[PLAN_THREADS];
@@ -86,7 +90,7 @@ k_group_plan(const int32_t* __restrict__ row_expert, int R, const int* __restric
     for (int base = 0; base < E; base += PLAN_THREADS) {
         const int e = base + t;
         const int c = e < E ? (counts ? counts[e] : hist[e]) : 0;
-        const int nt = (c + GT - 1) / GT;
+        const int nt = (c + gt - 1) / gt;
         s_rows[t] = c;
         s_tiles[t] = nt;
         __syncthreads();
@@ -101,7 +105,7 @@ k_group_plan(const int32_t* __restrict__ row_expert, int R, const int* __restric
         if (e < E) {
             offsets[e] = row0;
             cursor[e] = row0;
-            for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int2(row0 + GT * j, e);
+            for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int2(row0 + gt * j, e);
         }
         __syncthreads();
         if (t == PLAN_THREADS - 1) {
@@ -165,15 +169,47 @@ __global__ void k_group_copy(const uint8_t* __restrict__ xq, const int* __restri
 
 }  // namespace
 
-int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
-                   int64_t K, float* out, cudaStream_t s, bool use_tc) {
+// the grouped dp4a stream (gemm_small.cu)
+bool small_grouped_fits(int fmt, int64_t K, int mt);
+int small_grouped_launch(int fmt, const void* xq, const void* wq, int64_t R, int64_t E, int64_t N, int64_t K,
+                         const int2* tiles, const int* ntiles, int64_t max_tiles, const int* offsets, const int* perm,
+                         int mt, float* out, cudaStream_t s, const char* fn);
+
+// Average rows per expert up to which MMQ_PATH_AUTO takes the grouped weight stream: it reads
+// an expert's weights once per tile of 2 or 4 rows, the expanded path writes and reads every
+// expert's expanded weights once.  Measured on 128 experts of 768 x 2048 (stream / expanded,
+// us): Q4_K 1 row per expert 48 / 166, 4 rows 126 / 255, 8 rows 218 / 257, 16 rows 377 /
+// 259; Q5_K 8 rows 229 / 261, 10 rows 264 / 261; Q6_K 1 row 62 / 233, 8 rows 357 / 353;
+// Q8_0 8 rows 165 / 249, 12 rows 220 / 250.
+static int64_t stream_rows_per_expert(int fmt) {
+    return fmt == FMT_Q8_0 ? 14 : fmt == FMT_Q4_K ? 10 : fmt == FMT_Q5_K ? 9 : 7;
+}
+
+// path: MMQ_PATH_TC (the converter kernel), MMQ_PATH_EXPAND, MMQ_PATH_SMALL (the grouped
+// weight stream) or MMQ_PATH_AUTO (the stream for up to stream_rows_per_expert rows per
+// expert on average, else the expanded path); *taken: the contraction used
+int grouped_launch_path(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E,
+                        int64_t N, int64_t K, float* out, cudaStream_t s, int path, int* taken) {
     const char* fn = fmt == FMT_Q8_0   ? "mmq_gemm_grouped_q8_0"
                      : fmt == FMT_Q5_K ? "mmq_gemm_grouped_q5_k"
                      : fmt == FMT_Q6_K ? "mmq_gemm_grouped_q6_k" : "mmq_gemm_grouped_q4_k";
+    const bool use_tc = path == MMQ_PATH_TC;
+    // the stream's tile height: 2 rows where experts hold about one row, else 4
+    const int mt = R <= 2 * E ? 2 : 4;
+    bool stream = path == MMQ_PATH_SMALL || (path == MMQ_PATH_AUTO && R <= stream_rows_per_expert(fmt) * E);
+    if (stream && !small_grouped_fits(fmt, K, mt)) {
+        if (path == MMQ_PATH_SMALL) {
+            report(fn, MMQ_ERR_SHAPE, "K too large for the grouped weight stream's shared memory");
+            return MMQ_ERR_SHAPE;
+        }
+        stream = false;
+    }
+    const int gt = stream ? mt : GT;
     const int64_t nb = K / QK, row_bytes = nb * Q8_1_BYTES;
-    const int64_t max_tiles = (R + GT - 1) / GT + (E < R ? E : R);  // each expert adds at most one partial tile
+    const int64_t max_tiles = (R + gt - 1) / gt + (E < R ? E : R);  // each expert adds at most one partial tile
     if (max_tiles > 65535) {
-        report(fn, MMQ_ERR_SHAPE, "too many row tiles for the grid (R / 128 + min(E, R) > 65535)");
+        report(fn, MMQ_ERR_SHAPE, stream ? "too many row tiles for the grid (R / tile rows + min(E, R) > 65535)"
+                                         : "too many row tiles for the grid (R / 128 + min(E, R) > 65535)");
         return MMQ_ERR_SHAPE;
     }
     // scratch: counts[E], offsets[E + 1], cursor[E], ntiles, tiles[max_tiles], perm[R], and for
@@ -209,7 +245,7 @@ int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R
     {
         ProfScope ps("k_group_plan", s);
         k_group_plan<<<1, PLAN_THREADS, count_in_plan ? hist_bytes : 0, s>>>(
-            row_expert, (int)R, count_in_plan ? nullptr : counts, (int)E, offsets, cursor, tiles, ntiles);
+            row_expert, (int)R, count_in_plan ? nullptr : counts, (int)E, gt, offsets, cursor, tiles, ntiles);
     }
     {
         ProfScope ps("k_group_scatter", s);
@@ -223,12 +259,21 @@ int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R
                                                                        offsets + E, (int)R, (int)(row_bytes / 16), xs);
     }
     st = launch_status(fn);
-    if (st == MMQ_OK && use_tc)
+    if (st == MMQ_OK && stream)
+        st = small_grouped_launch(fmt, xq, wq, R, E, N, K, tiles, ntiles, max_tiles, offsets, perm, mt, out, s, fn);
+    else if (st == MMQ_OK && use_tc)
         st = tc_grouped_launch(fmt, xs, wq, R, E, N, K, tiles, ntiles, max_tiles, offsets + 1, perm, out, s);
     else if (st == MMQ_OK)
         st = tcx_grouped_launch(fmt, xq, R, wq, E, N, K, tiles, ntiles, max_tiles, offsets, perm, out, s, fn);
     scratch_free(ws, s);  // stream-ordered: after the kernels above
+    if (st == MMQ_OK && taken) *taken = stream ? MMQ_PATH_SMALL : use_tc ? MMQ_PATH_TC : MMQ_PATH_EXPAND;
     return st;
+}
+
+int grouped_launch(int fmt, const void* xq, const int32_t* row_expert, int64_t R, const void* wq, int64_t E, int64_t N,
+                   int64_t K, float* out, cudaStream_t s, bool use_tc) {
+    return grouped_launch_path(fmt, xq, row_expert, R, wq, E, N, K, out, s, use_tc ? MMQ_PATH_TC : MMQ_PATH_EXPAND,
+                               nullptr);
 }
 
 }  // namespace mmq

@@ -198,20 +198,26 @@ int mmq_linear_q6_k(const float* x, int64_t M, int64_t K, const void* wq, int64_
  * Kernel Win Surface?", sec. "Fused indexed-MoE prefill GEMM": rows counting-sorted by
  * expert into tiles of at most 128 rows, each tile staging one expert's weights once).
  * The grouping runs on the device (no host round trip; capturable).  The contraction over
- * the tiles is the expanded-code tensor-core path (the activation tiles gathered from xq
- * in sorted order, the weights of every expert that has rows expanded once per call), or,
- * when mmq_set_path(MMQ_PATH_TC) is in force, the converter kernel (Q8_0, Q4_K, Q5_K; Q6_K
- * is then refused with MMQ_ERR_ARG).
+ * the tiles, by the path in force: MMQ_PATH_EXPAND, the expanded-code tensor-core path over
+ * 128-row tiles (the activation tiles gathered from xq in sorted order, the weights of
+ * every expert that has rows expanded once per call); MMQ_PATH_SMALL, the dp4a weight
+ * stream over tiles of 2 rows (R <= 2E) or 4 rows of one expert, each tile reading its
+ * expert's weights once; MMQ_PATH_TC, the converter kernel (Q8_0, Q4_K, Q5_K; Q6_K is then
+ * refused with MMQ_ERR_ARG); MMQ_PATH_AUTO (default), the tile height by the experts'
+ * fill (the same section's dynamic M-tile): the weight stream up to an average of 14 rows
+ * per expert for Q8_0, 10 for Q4_K, 9 for Q5_K, 7 for Q6_K (R <= that x E), the expanded
+ * path above (measured crossovers on 128 experts of 768 x 2048).
  *   xq: q8_1 [R][K/32] blocks, 16-byte aligned.  row_expert: int32 [R], 4-byte aligned.
  *   wq: E weight matrices stacked expert-major, expert e at row e*N ([E*N][K/32] Q8_0
  *   blocks or [E*N][K/256] Q4_K / Q5_K / Q6_K super-blocks), 16-byte aligned.  out: f32
  *   [R][N], 16-byte aligned, fully overwritten; a row whose expert id is outside [0, E)
  *   gets zeros.
  * Accuracy as mmq_gemm_q8_0 / mmq_gemm_q4_k / mmq_gemm_q5_k / mmq_gemm_q6_k, per row.  Needs
- * K % 256 == 0 and R / 128 + min(E, R) <= 65535.  Scratch (stream-ordered, as the expanded
- * path): about R*K*1.125 bytes on the converter kernel; on the expanded path 3 bytes per
- * activation value of up to R + 128*min(E, R) rows plus 2.25 bytes per weight value of the
- * E*N weight rows (Q6_K: 4.25).
+ * K % 256 == 0 and R / (tile rows) + min(E, R) <= 65535.  Scratch (stream-ordered, as the
+ * expanded path): about R*K*1.125 bytes on the converter kernel; on the expanded path 3
+ * bytes per activation value of up to R + 128*min(E, R) rows plus 2.25 bytes per weight
+ * value of the E*N weight rows (Q6_K: 4.25); on the weight stream only the grouping's
+ * tables (about 8 bytes per row and 12 per expert).
  * Errors: MMQ_ERR_SHAPE, MMQ_ERR_K_MULTIPLE, MMQ_ERR_NULL, MMQ_ERR_ALIGN, MMQ_ERR_ARG, MMQ_ERR_SMEM,
  * MMQ_ERR_NOMEM, MMQ_ERR_LAUNCH.
  */

@@ -97,7 +97,9 @@ def draw_grouped(i):
     """Case i: (fmt, path, R, E, N, K, invalid fraction, seed)."""
     rng = np.random.default_rng(9500 + i)
     fmt = FMTS[rng.integers(len(FMTS))]
-    path = "tc" if (fmt != "q6_k" and rng.integers(3) == 0) else "expand"
+    path = ["expand", "small", "tc"][rng.integers(3)]
+    if path == "tc" and fmt == "q6_k":
+        path = "expand"
     R = log_uniform(rng, 1, 3000)
     E = log_uniform(rng, 1, 64)
     N = log_uniform(rng, 1, 600)
@@ -125,10 +127,11 @@ def test_random_grouped_parity(mmq, case):
     xq_ref = oracle.quantize_q8_1(x)
     xq = mmq.mmq_quantize_q8_1(dev(x))
     out = torch.full((R, N), float("nan"), device="cuda")
-    mmq.mmq_set_path(mmq.PATH_TC if path == "tc" else mmq.PATH_AUTO)
+    pid = {"tc": mmq.PATH_TC, "small": mmq.PATH_SMALL, "expand": mmq.PATH_EXPAND}[path]
+    mmq.mmq_set_path(pid)
     try:
         mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K, out=out)
-        assert mmq.mmq_last_path() == (mmq.PATH_TC if path == "tc" else mmq.PATH_EXPAND)
+        assert mmq.mmq_last_path() == pid
     finally:
         mmq.mmq_set_path(mmq.PATH_AUTO)
     o = out.cpu().numpy()

@@ -762,12 +762,14 @@ GROUPED_CASES = [  # (R, E, N, K, routing)
 ]
 
 
-@pytest.mark.parametrize("path", ["expand", "tc"])
+@pytest.mark.parametrize("path", ["expand", "small", "tc"])
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("case", range(len(GROUPED_CASES)))
 def test_grouped_parity(mmq, fmt, case, path):
-    """Both contractions over the device-built grouping: the expanded path (the default)
-    and the converter kernel (MMQ_PATH_TC; not Q6_K, refused below)."""
+    """The three contractions over the device-built grouping, each forced: the expanded
+    path (128-row tiles), the grouped dp4a weight stream (tiles of 2 or 4 rows; the
+    automatic choice where experts hold few rows) and the converter kernel (MMQ_PATH_TC;
+    not Q6_K, refused below)."""
     if fmt in NO_TC and path == "tc":
         pytest.skip("the converter kernel takes Q8_0, Q4_K and Q5_K")
     R, E, N, K, routing = GROUPED_CASES[case]
@@ -783,7 +785,7 @@ def test_grouped_parity(mmq, fmt, case, path):
     w = synth.weights(fmt, 300 + case, E * N, K)
     xq = mmq.mmq_quantize_q8_1(dev(x))
     out = torch.full((R, N), float("nan"), device="cuda")
-    set_path(mmq, "tc" if path == "tc" else "auto")
+    set_path(mmq, path)
     try:
         mmq.mmq_gemm_grouped(fmt, xq, dev(ids), dev(w), E, N, K, out=out)
         assert mmq.mmq_last_path() == PATH_IDS[path]
@@ -796,7 +798,7 @@ def test_grouped_parity(mmq, fmt, case, path):
     check_close(out.cpu().numpy(), ref, norm, f"grouped {fmt} {GROUPED_CASES[case]}")
 
 
-@pytest.mark.parametrize("path", ["expand", "tc"])
+@pytest.mark.parametrize("path", ["expand", "small", "tc"])
 def test_grouped_graph_capture(mmq, path):
     R, E, N, K = 500, 12, 160, 512
     rng = np.random.default_rng(7)
@@ -809,7 +811,7 @@ def test_grouped_graph_capture(mmq, path):
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
-    set_path(mmq, "tc" if path == "tc" else "auto")
+    set_path(mmq, path)
     try:
         with torch.cuda.graph(g, stream=s):
             mmq.mmq_gemm_grouped("q4_k", xq, idd, wd, E, N, K, out=out, stream=s)
@@ -819,6 +821,26 @@ def test_grouped_graph_capture(mmq, path):
     torch.cuda.synchronize()
     ref, norm = grouped_reference("q4_k", oracle.quantize_q8_1(x), ids, w, E, N, K)
     check_close(out.cpu().numpy(), ref, norm, "captured grouped")
+    assert mmq.mmq_get_device_error() == 0
+
+
+# MMQ_PATH_AUTO takes the grouped weight stream up to 10 rows per expert on average for
+# Q4_K (Q8_0 14, Q5_K 9, Q6_K 7; every expert's weights read once per tile of 2 or 4 rows)
+# and the expanded path above (every expert's weights expanded once, 128-row tiles)
+@pytest.mark.parametrize("R,E,want", [(128, 128, "small"), (1280, 128, "small"), (1281, 128, "expand"),
+                                      (4096, 64, "expand")])
+def test_grouped_auto_follows_the_experts_fill(mmq, R, E, want):
+    N, K = 64, 512
+    rng = np.random.default_rng(R + E)
+    ids = rng.integers(0, E, R).astype(np.int32)
+    x = synth.activations(R + 11, R, K, True)
+    w = synth.weights("q4_k", E + 12, E * N, K)
+    xq = mmq.mmq_quantize_q8_1(dev(x))
+    set_path(mmq, "auto")
+    out = mmq.mmq_gemm_grouped("q4_k", xq, dev(ids), dev(w), E, N, K)
+    assert mmq.mmq_last_path() == PATH_IDS[want]
+    ref, norm = grouped_reference("q4_k", oracle.quantize_q8_1(x), ids, w, E, N, K)
+    check_close(out.cpu().numpy(), ref, norm, f"grouped auto R={R} E={E}")
     assert mmq.mmq_get_device_error() == 0
 
 
