@@ -107,6 +107,7 @@ KERNEL_SOURCES = {
     "k_mmq_i8_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_kq_stream": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_q6_stream": ("gemm_small.cu",) + _COMMON_SRC,
+    "k_stream_ksum": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small_mma": ("gemm_small.cu",) + _COMMON_SRC,
     "k_mmq_small": ("gemm_small.cu",) + _COMMON_SRC,
 }

@@ -88,6 +88,10 @@ int grouped_launch_path(int fmt, const void* xq, const int32_t* row_expert, int6
 // until the first chunk is in), or -1 where the stream does not take the shape (gemm_small.cu).
 double q6_stream_cost_us(int64_t M, int64_t N, int64_t K);
 
+// Test switch of the Q8_0 / Q4_K / Q5_K tensor-core streams' K splits (0: the measured rule,
+// n > 0: n splits) and boxes per CTA with a forced split (0: the launcher's) (gemm_small.cu).
+void small_set_ksplit(int splits, int boxes);
+
 namespace {
 
 std::atomic<int> g_path{-1};
@@ -428,6 +432,12 @@ int mmq_debug_refuse_smem(int on) { return g_refuse_smem.exchange(on ? 1 : 0); }
 int mmq_debug_small_route(int route) {
     if (route < SMALL_ROUTE_AUTO || route > SMALL_ROUTE_MMA) return MMQ_ERR_ARG;
     return small_set_route(route);
+}
+
+int mmq_debug_small_ksplit(int splits, int boxes) {
+    if (splits < 0 || splits > 8 || boxes < 0 || boxes > 4) return MMQ_ERR_ARG;
+    small_set_ksplit(splits, boxes);
+    return MMQ_OK;
 }
 
 int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* splits) {

@@ -898,11 +898,11 @@ constexpr int I8_SMEM = IS_WARPS * (I8_WARP_BYTES + 8 * (I8_SLOTS + I8_ASLOTS));
 static_assert(I8_SMEM <= 110 * 1024 && I8_SLOT % 128 == 0 && IS_ASLOT % 128 == 0, "two CTAs per SM");
 static_assert(IS_MAX_TPC * 16 * 8 * 4 <= I8_SLOTS * I8_SLOT, "a warp's partial sums fit in its weight ring");
 
-template <bool DOTS>
+template <bool DOTS, bool SPLIT = false>
 __global__ void __launch_bounds__(IS_WARPS * 32, 2)
 k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmXl, int M, int N,
-                int nb, int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
+                int nb, int tpc, float* __restrict__ out, long long pstride, int32_t* __restrict__ dots) {
     constexpr int S = I8_SLOTS, SA = I8_ASLOTS, SLOT = I8_SLOT, RB = 8 * Q8_0_BYTES, WB = I8_WARP_BYTES;
     extern __shared__ __align__(128) uint8_t is_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -912,7 +912,14 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const uint32_t abar0 = bar0 + 8 * S;
     const int ntiles = (N + 15) / 16;
     const int t0 = blockIdx.x * tpc, nt = min(tpc, ntiles - t0);
-    const int npieces = nb / 8;  // groups of 8 blocks
+    // SPLIT (K split over the grid's z): this CTA's groups of 8 blocks are pz0 .. pz0 +
+    // npieces - 1, its partial outputs go to slab z of `out` (pstride floats apart)
+    int pz0 = 0, npieces = nb / 8;
+    if constexpr (SPLIT) {
+        pz0 = (int)((long long)blockIdx.z * (nb / 8) / gridDim.z);
+        npieces = (int)((long long)(blockIdx.z + 1) * (nb / 8) / gridDim.z) - pz0;
+        out += blockIdx.z * pstride;
+    }
     const int my = warp < npieces ? (npieces - 1 - warp) / IS_WARPS + 1 : 0;  // this warp's pieces per tile
     const int total = nt * my;
     const int m0 = blockIdx.y * 8;
@@ -922,7 +929,7 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     auto issue = [&](int i) {  // lane 0: the copy of this warp's weight piece i into slot i % S
         const uint32_t bar = bar0 + 8 * (i % S);
         ptx::mbar_arrive_expect_tx(bar, SLOT);  // the whole box, zero-filled rows included
-        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, (warp + next.k * IS_WARPS) * (RB / 8),
+        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, (pz0 + warp + next.k * IS_WARPS) * (RB / 8),
                          (t0 + next.tl) * 16);
     };
     auto advance = [&]() {
@@ -936,7 +943,7 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         const uint32_t bar = abar0 + 8 * (k % SA);
         ptx::mbar_arrive_expect_tx(bar, abytes);
         ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), lastp ? &tmXl : &tmX, bar,
-                         (warp + k * IS_WARPS) * (IS_XROW / 8), m0);
+                         (pz0 + warp + k * IS_WARPS) * (IS_XROW / 8), m0);
     };
     int issued = 0, aissued = 0;
     if (lane == 0) {
@@ -962,7 +969,7 @@ k_mmq_i8_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 #pragma unroll
     for (int tl = 0; tl < IS_MAX_TPC; ++tl) acc[tl][0] = acc[tl][1] = 0ull;
     for (int k = 0; k < my && ok; ++k) {
-        const int b0 = 8 * (warp + k * IS_WARPS);  // first block of the piece
+        const int b0 = 8 * (pz0 + warp + k * IS_WARPS);  // first block of the piece
         if (!ds_wait(abar0 + 8 * (k % SA), (k / SA) & 1)) {
             ok = false;
             break;
@@ -1140,11 +1147,11 @@ __device__ __forceinline__ uint32_t ks_code_pair(uint32_t u, uint32_t sel) {
     return d;
 }
 
-template <int FMT, int BOXR, bool DOTS>
+template <int FMT, int BOXR, bool DOTS, bool SPLIT = false>
 __global__ void __launch_bounds__(ks_warps(FMT, BOXR) * 32, 2)
 k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmXl, int M, int N,
-                int nb, int tpc, float* __restrict__ out, int32_t* __restrict__ dots) {
+                int nb, int tpc, float* __restrict__ out, long long pstride, int32_t* __restrict__ dots) {
     constexpr int W = ks_warps(FMT, BOXR), S = ks_slots(FMT, BOXR), SLOT = ks_slot(FMT, BOXR), RB = kq_bytes(FMT);
     constexpr int SA = KS_ASLOTS, WB = ks_warp_bytes(FMT, BOXR), U = BOXR / 16, MB = ks_max_boxes(BOXR);
     extern __shared__ __align__(128) uint8_t is_smem[];
@@ -1155,7 +1162,14 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const uint32_t abar0 = bar0 + 8 * S;
     const int nboxes = (N + BOXR - 1) / BOXR;
     const int t0 = blockIdx.x * tpc, nt = min(tpc, nboxes - t0);  // this CTA's boxes
-    const int npieces = nb / 8;  // super-blocks
+    // SPLIT (K split over the grid's z): this CTA's super-blocks are pz0 .. pz0 + npieces - 1,
+    // its partial outputs go to slab z of `out` (pstride floats apart)
+    int pz0 = 0, npieces = nb / 8;
+    if constexpr (SPLIT) {
+        pz0 = (int)((long long)blockIdx.z * (nb / 8) / gridDim.z);
+        npieces = (int)((long long)(blockIdx.z + 1) * (nb / 8) / gridDim.z) - pz0;
+        out += blockIdx.z * pstride;
+    }
     const int my = warp < npieces ? (npieces - 1 - warp) / W + 1 : 0;  // this warp's pieces per box
     const int total = nt * my;
     const int m0 = blockIdx.y * 8;
@@ -1165,7 +1179,7 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     auto issue = [&](int i) {  // lane 0: the copy of this warp's weight piece i into slot i % S
         const uint32_t bar = bar0 + 8 * (i % S);
         ptx::mbar_arrive_expect_tx(bar, SLOT);  // the whole box, zero-filled rows included
-        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, (warp + next.k * W) * (RB / 8),
+        ptx::tma_load_2d(ptx::smem_u32(ring + (i % S) * SLOT), &tmW, bar, (pz0 + warp + next.k * W) * (RB / 8),
                          (t0 + next.tl) * BOXR);
     };
     auto advance = [&]() {
@@ -1179,7 +1193,7 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         const uint32_t bar = abar0 + 8 * (k % SA);
         ptx::mbar_arrive_expect_tx(bar, abytes);
         ptx::tma_load_2d(ptx::smem_u32(aring + (k % SA) * IS_ASLOT), lastp ? &tmXl : &tmX, bar,
-                         (warp + k * W) * (IS_XROW / 8), m0);
+                         (pz0 + warp + k * W) * (IS_XROW / 8), m0);
     };
     int issued = 0, aissued = 0;
     if (lane == 0) {
@@ -1217,7 +1231,7 @@ k_mmq_kq_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         for (int u = 0; u < U; ++u) acc[tl][u][0] = acc[tl][u][1] = 0ull;
     const uint32_t msel = 0x4140u + 0x0202u * (q & 1);  // bytes 2(q & 1), 2(q & 1) + 1 of a scale word
     for (int k = 0; k < my && ok; ++k) {
-        const int b0 = 8 * (warp + k * W);  // first block of the piece
+        const int b0 = 8 * (pz0 + warp + k * W);  // first block of the piece
         if (!ds_wait(abar0 + 8 * (k % SA), (k / SA) & 1)) {
             ok = false;
             break;
@@ -1691,11 +1705,11 @@ __device__ __forceinline__ bool q6s_wait1(uint32_t bar, uint32_t parity) {
     return true;
 }
 
-template <bool DOTS>
+template <bool DOTS, bool GSPLIT = false>
 __global__ void __launch_bounds__(Q6S_THREADS, 1)
 k_mmq_q6_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmXl, int M, int N, int nb, unsigned stagger_ns,
-                float* __restrict__ out, int32_t* __restrict__ dots) {
+                float* __restrict__ out, long long pstride, int32_t* __restrict__ dots) {
     extern __shared__ __align__(128) uint8_t is_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     const uint32_t full0 = ptx::smem_u32(is_smem + Q6S_SLOTS * Q6S_SLOT);
@@ -1836,7 +1850,7 @@ k_mmq_q6_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     __syncthreads();
     if (!DOTS && !bad)
         for (int e = threadIdx.x; e < 1024; e += Q6S_THREADS) red[e] += red[1024 + e];
-    if (splits > 1) {
+    if (!GSPLIT && splits > 1) {
         // the cluster's CTAs (ranks 0 .. splits - 1 in K order) hold partial tiles; rank 0
         // adds them in rank order and stores; nobody leaves while its tile may be read
         cluster_sync();
@@ -1851,7 +1865,10 @@ k_mmq_q6_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
         cluster_sync();
     } else {
+        // the whole K, or (GSPLIT: a split over the grid's z without clusters) this CTA's
+        // partial tile to slab z of `out`, pstride floats apart
         __syncthreads();
+        if (GSPLIT) out += z * pstride;
         if (!DOTS && !bad)
             for (int e = threadIdx.x; e < 1024; e += Q6S_THREADS) {
                 const int tok = e >> 7, n = box * 128 + (e & 127);
@@ -1878,13 +1895,165 @@ inline int64_t stream_tpc(int64_t nboxes, int max_boxes) {
     return tpc < 1 ? 1 : (tpc > max_boxes ? max_boxes : tpc);
 }
 
+// ------------------------------------------ K splits of the i8 / kq streams
+// A one-pass stream grid (up to eight rows) whose CTAs would load the SMs unevenly takes z
+// K splits (grid z) and, with them, tpc boxes per CTA: 3584 x 18944 is 224 one-box CTAs on
+// 152 SMs, 72 SMs with two boxes and 80 with one.  Each split writes its partial outputs
+// to a slab of scratch and k_stream_ksum adds the slabs in the order z = 0, 1, ... (the
+// same order at every call, so the output is deterministic).  (tpc, z) minimises a CTA's
+// work, tpc boxes x ceil(pieces / z) pieces, over grids resident in one wave (two CTAs per
+// SM: a second wave pays each CTA's start-up again) that leave each warp two pieces or
+// more, taken where that saves more than 15 %.  Measured (Q4_K, eight rows, graph
+// replays): 3584 x 18944 16.3 us unsplit, 13.25 with 3 boxes x 4 splits on 300 CTAs (57
+// pieces a CTA), 19.2 with 3 boxes x 2 splits on 150 (111 pieces, one CTA per SM), 15.2
+// with 2 x 2 or 4 x 4 (74 / 76), 18.5 with 4 x 8 (two waves); 512 x 18944 11.0 unsplit,
+// 5.5 with 4 splits.  Passes of more rows keep their grid (the path choice's cost model is
+// measured on it).
+std::atomic<int> g_small_ksplit{0};  // test switches: splits (0: the rule) and boxes per CTA (0: the launcher's)
+std::atomic<int> g_small_kboxes{0};
+
+struct StreamGrid {
+    int64_t tpc;
+    int z;
+};
+
+inline StreamGrid stream_grid(int64_t nboxes, int max_boxes, int64_t passes, int64_t pieces, int warps) {
+    const int64_t base = stream_tpc(nboxes, max_boxes);
+    const int forced = g_small_ksplit.load(), fboxes = g_small_kboxes.load();
+    if (forced > 0)
+        return {fboxes > 0 ? std::min<int64_t>(fboxes, max_boxes) : base,
+                (int)std::min<int64_t>(forced, std::max<int64_t>(pieces, 1))};
+    if (passes != 1) return {base, 1};
+    const int64_t sms = device_shape().sms;
+    auto ctas = [&](int64_t t, int64_t z) { return (nboxes + t - 1) / t * z; };
+    auto cost = [&](int64_t t, int64_t z) { return t * ((pieces + z - 1) / z); };
+    StreamGrid best{base, 1};
+    for (int z = 2; z <= 8 && pieces >= 2LL * warps * z; ++z)
+        for (int64_t t = 1; t <= max_boxes; ++t)
+            if (ctas(t, z) <= 2 * sms && cost(t, z) < cost(best.tpc, best.z)) best = {t, z};
+    return cost(best.tpc, best.z) * 20 < cost(base, 1) * 17 ? best : StreamGrid{base, 1};
+}
+
+// slab 0 + slab 1 + ... of a split stream's partial outputs, as a programmatic dependent of
+// the stream kernel; it releases the next kernel on the stream before its own wait (that
+// kernel's wait still covers this one's stores)
+__global__ void __launch_bounds__(256) k_stream_ksum(const float* __restrict__ part, int splits, long long pstride,
+                                                     long long n, float* __restrict__ out) {
+    ptx::grid_dep_launch_dependents();
+    ptx::grid_dep_wait();
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL) {
+        float v = __ldcs(part + i);
+        for (int z = 1; z < splits; ++z) v += __ldcs(part + z * pstride + i);
+        out[i] = v;
+    }
+}
+
+// Scratch for the partial outputs.  Outside stream capture: the library's stream-ordered
+// pool, allocated and freed on the call's stream like every other call's scratch.  Under
+// capture, the allocation is a root node of the graph with one edge, into the stream
+// kernel's node, and the free a leaf node after the sum: captured in stream order the two
+// would sit between this call's kernels and its neighbours' and end the programmatic
+// overlap of consecutive calls (measured ~4 us a call).
+struct SplitScratch {
+    float* p = nullptr;
+    cudaGraph_t graph = nullptr;  // set under capture
+    cudaGraphNode_t alloc = nullptr;
+};
+
+int split_scratch_alloc(size_t bytes, cudaStream_t s, SplitScratch* ss, const char* fn) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaGraph_t g = nullptr;
+    if (cudaStreamGetCaptureInfo(s, &cs, nullptr, &g) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "cudaStreamGetCaptureInfo failed");
+        return MMQ_ERR_CUDA;
+    }
+    if (cs == cudaStreamCaptureStatusNone) {
+        void* p = nullptr;
+        const int st = scratch_alloc(bytes, s, &p, fn);
+        ss->p = static_cast<float*>(p);
+        return st;
+    }
+    int dev = 0;
+    cudaMemAllocNodeParams prm = {};
+    prm.poolProps.allocType = cudaMemAllocationTypePinned;
+    prm.poolProps.location.type = cudaMemLocationTypeDevice;
+    prm.bytesize = bytes;
+    if (cs != cudaStreamCaptureStatusActive || cudaGetDevice(&dev) != cudaSuccess ||
+        (prm.poolProps.location.id = dev, cudaGraphAddMemAllocNode(&ss->alloc, g, nullptr, 0, &prm)) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_NOMEM, "scratch allocation node for the K split failed");
+        return MMQ_ERR_NOMEM;
+    }
+    ss->p = static_cast<float*>(prm.dptr);
+    ss->graph = g;
+    return MMQ_OK;
+}
+
+// under capture, right after the stream kernel's launch (the stream's one dependency is
+// then that kernel's node): the node depends on the allocation
+int split_scratch_bind(const SplitScratch& ss, cudaStream_t s, const char* fn) {
+    if (!ss.graph) return MMQ_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t* deps = nullptr;
+    const cudaGraphEdgeData* edata = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(s, &cs, nullptr, nullptr, &deps, &edata, &nd) != cudaSuccess || nd != 1 ||
+        cudaGraphAddDependencies(ss.graph, &ss.alloc, deps, nullptr, 1) != cudaSuccess) {
+        cudaGetLastError();
+        report(fn, MMQ_ERR_CUDA, "ordering the K split's scratch in the captured graph failed");
+        return MMQ_ERR_CUDA;
+    }
+    return MMQ_OK;
+}
+
+void split_scratch_free(const SplitScratch& ss, cudaStream_t s) {
+    if (!ss.p) return;
+    if (!ss.graph) {
+        scratch_free(ss.p, s);
+        return;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t* deps = nullptr;
+    const cudaGraphEdgeData* edata = nullptr;
+    size_t nd = 0;
+    cudaGraphNode_t fnode = nullptr;
+    if (cudaStreamGetCaptureInfo(s, &cs, nullptr, nullptr, &deps, &edata, &nd) != cudaSuccess ||
+        cudaGraphAddMemFreeNode(&fnode, ss.graph, deps, nd, ss.p) != cudaSuccess)
+        cudaGetLastError();
+}
+
+// A stream kernel's launch with z K splits: launch(out, pstride, z) launches it (with its
+// profiling scope) into `out` or the partial slabs and returns its status; the sum follows.
+template <typename Launch>
+int launch_stream_split(int z, int64_t M, int64_t N, float* out, cudaStream_t s, const char* fn, Launch&& launch,
+                        SplitScratch* ss) {
+    if (z <= 1) return launch(out, 0LL, 1u);
+    const long long pstride = (M * N + 63) / 64 * 64;  // 256-byte slabs
+    int st = split_scratch_alloc((size_t)z * pstride * sizeof(float), s, ss, fn);
+    if (st != MMQ_OK) return st;
+    st = launch(ss->p, pstride, (unsigned)z);
+    if (st == MMQ_OK) {
+        const long long n = M * N;
+        const unsigned blocks = (unsigned)std::min<long long>((n + 255) / 256, 4LL * device_shape().sms);
+        ProfScope ps("k_stream_ksum", s);
+        st = pdl_status(launch_pdl(k_stream_ksum, dim3(blocks), dim3(256), 0, s, (const float*)ss->p, z, pstride, n, out),
+                        fn);
+    }
+    split_scratch_free(*ss, s);
+    return st;
+}
+
 int launch_i8_stream_q8_0(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                           int32_t* dots, cudaStream_t s, const char* fn) {
     const int64_t ntiles = (N + 15) / 16;
-    const int64_t tpc = stream_tpc(ntiles, IS_MAX_TPC);
-    static SmemAttr attr, attr_d;
-    const int e = dots ? ensure_smem((const void*)k_mmq_i8_stream<true>, I8_SMEM, attr_d)
-                       : ensure_smem((const void*)k_mmq_i8_stream<false>, I8_SMEM, attr);
+    const StreamGrid sg = dots ? StreamGrid{stream_tpc(ntiles, IS_MAX_TPC), 1}
+                               : stream_grid(ntiles, IS_MAX_TPC, (M + 7) / 8, nb / 8, IS_WARPS);
+    const int64_t tpc = sg.tpc;
+    static SmemAttr attr, attr_d, attr_s;
+    const int e = dots       ? ensure_smem((const void*)k_mmq_i8_stream<true>, I8_SMEM, attr_d)
+                  : sg.z > 1 ? ensure_smem((const void*)k_mmq_i8_stream<false, true>, I8_SMEM, attr_s)
+                             : ensure_smem((const void*)k_mmq_i8_stream<false>, I8_SMEM, attr);
     if (e != MMQ_OK) {
         report(fn, e, "shared-memory request refused");
         return e;
@@ -1895,24 +2064,40 @@ int launch_i8_stream_q8_0(const uint8_t* x8, const uint8_t* w8, int64_t M, int64
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
     }
-    dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
-    ProfScope ps("k_mmq_i8_stream", s);
-    return pdl_status(dots ? launch_pdl(k_mmq_i8_stream<true>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx, txl,
-                                        (int)M, (int)N, nb, (int)tpc, out, dots)
-                           : launch_pdl(k_mmq_i8_stream<false>, grid, dim3(IS_WARPS * 32), (size_t)I8_SMEM, s, tw, tx, txl,
-                                        (int)M, (int)N, nb, (int)tpc, out, dots),
-                      fn);
+    const dim3 grid((unsigned)((ntiles + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
+    const int z = sg.z;
+    SplitScratch ss;
+    return launch_stream_split(
+        z, M, N, out, s, fn,
+        [&](float* o, long long pstride, unsigned gz) {
+            ProfScope ps("k_mmq_i8_stream", s);
+            const dim3 g3(grid.x, grid.y, gz);
+            const dim3 blk(IS_WARPS * 32);
+            const int st = pdl_status(
+                dots     ? launch_pdl(k_mmq_i8_stream<true>, g3, blk, (size_t)I8_SMEM, s, tw, tx, txl, (int)M, (int)N, nb,
+                                      (int)tpc, o, pstride, dots)
+                : gz > 1 ? launch_pdl(k_mmq_i8_stream<false, true>, g3, blk, (size_t)I8_SMEM, s, tw, tx, txl, (int)M,
+                                      (int)N, nb, (int)tpc, o, pstride, dots)
+                         : launch_pdl(k_mmq_i8_stream<false>, g3, blk, (size_t)I8_SMEM, s, tw, tx, txl, (int)M, (int)N,
+                                      nb, (int)tpc, o, pstride, dots),
+                fn);
+            return st == MMQ_OK ? split_scratch_bind(ss, s, fn) : st;
+        },
+        &ss);
 }
 
 template <int FMT, int BOXR>
 int launch_kq_stream_b(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                        int32_t* dots, cudaStream_t s, const char* fn) {
     const int64_t nboxes = (N + BOXR - 1) / BOXR;
-    const int64_t tpc = stream_tpc(nboxes, ks_max_boxes(BOXR));
+    const StreamGrid sg = dots ? StreamGrid{stream_tpc(nboxes, ks_max_boxes(BOXR)), 1}
+                               : stream_grid(nboxes, ks_max_boxes(BOXR), (M + 7) / 8, nb / 8, ks_warps(FMT, BOXR));
+    const int64_t tpc = sg.tpc;
     constexpr int smem = ks_smem_bytes(FMT, BOXR);
-    static SmemAttr attr, attr_d;
-    const int e = dots ? ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, true>, smem, attr_d)
-                       : ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, false>, smem, attr);
+    static SmemAttr attr, attr_d, attr_s;
+    const int e = dots       ? ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, true>, smem, attr_d)
+                  : sg.z > 1 ? ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, false, true>, smem, attr_s)
+                             : ensure_smem((const void*)k_mmq_kq_stream<FMT, BOXR, false>, smem, attr);
     if (e != MMQ_OK) {
         report(fn, e, "shared-memory request refused");
         return e;
@@ -1923,14 +2108,26 @@ int launch_kq_stream_b(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
     }
-    dim3 grid((unsigned)((nboxes + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
+    const dim3 grid((unsigned)((nboxes + tpc - 1) / tpc), (unsigned)((M + 7) / 8));
     const dim3 block(ks_warps(FMT, BOXR) * 32);
-    ProfScope ps("k_mmq_kq_stream", s);
-    return pdl_status(dots ? launch_pdl(k_mmq_kq_stream<FMT, BOXR, true>, grid, block, (size_t)smem, s, tw, tx, txl, (int)M,
-                                        (int)N, nb, (int)tpc, out, dots)
-                           : launch_pdl(k_mmq_kq_stream<FMT, BOXR, false>, grid, block, (size_t)smem, s, tw, tx, txl,
-                                        (int)M, (int)N, nb, (int)tpc, out, dots),
-                      fn);
+    const int z = sg.z;
+    SplitScratch ss;
+    return launch_stream_split(
+        z, M, N, out, s, fn,
+        [&](float* o, long long pstride, unsigned gz) {
+            ProfScope ps("k_mmq_kq_stream", s);
+            const dim3 g3(grid.x, grid.y, gz);
+            const int st = pdl_status(
+                dots     ? launch_pdl(k_mmq_kq_stream<FMT, BOXR, true>, g3, block, (size_t)smem, s, tw, tx, txl, (int)M,
+                                      (int)N, nb, (int)tpc, o, pstride, dots)
+                : gz > 1 ? launch_pdl(k_mmq_kq_stream<FMT, BOXR, false, true>, g3, block, (size_t)smem, s, tw, tx, txl,
+                                      (int)M, (int)N, nb, (int)tpc, o, pstride, dots)
+                         : launch_pdl(k_mmq_kq_stream<FMT, BOXR, false>, g3, block, (size_t)smem, s, tw, tx, txl,
+                                      (int)M, (int)N, nb, (int)tpc, o, pstride, dots),
+                fn);
+            return st == MMQ_OK ? split_scratch_bind(ss, s, fn) : st;
+        },
+        &ss);
 }
 
 // 32-row boxes when there are at least two of them per SM, else 16-row boxes
@@ -1956,13 +2153,29 @@ int q6_stream_splits(int64_t boxes, int64_t passes, int64_t nch) {
     return S;
 }
 
+// or over the grid's z without clusters, any count up to 16 while the grid fits the SMs,
+// each split's partial tile to a slab of scratch and k_stream_ksum adding the slabs: taken
+// where it leaves each CTA fewer chunks than the cluster split (3584 x 18944: 28 boxes x 5
+// splits, 8 chunks a CTA, against clusters of 4 and 10; five CTAs of a cluster would not
+// pack into the GPCs).  1: the cluster split.
+int q6_stream_gsplits(int64_t boxes, int64_t passes, int64_t nch) {
+    if (g_small_ksplit.load() == 1) return 1;  // the test switch's "never split"
+    const int64_t sms = device_shape().sms, S = q6_stream_splits(boxes, passes, nch);
+    int zg = 1;
+    for (int z = 2; z <= 16 && z <= nch && boxes * passes * z <= sms; ++z)
+        if ((nch + z - 1) / z < (nch + zg - 1) / zg) zg = z;
+    return (nch + zg - 1) / zg < (nch + S - 1) / S ? zg : 1;
+}
+
 template <bool DOTS>
 int launch_q6_stream_t(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out,
                        int32_t* dots, cudaStream_t s, const char* fn) {
     const int64_t nsb = nb / 8, nch = nsb / 2, boxes = (N + 127) / 128, passes = (M + 7) / 8;
     const int S = q6_stream_splits(boxes, passes, nch);
-    static SmemAttr attr;
-    const int e = ensure_smem((const void*)k_mmq_q6_stream<DOTS>, Q6S_SMEM, attr);
+    const int zg = DOTS ? 1 : q6_stream_gsplits(boxes, passes, nch);
+    static SmemAttr attr, attr_g;
+    const int e = zg > 1 ? ensure_smem((const void*)k_mmq_q6_stream<false, true>, Q6S_SMEM, attr_g)
+                         : ensure_smem((const void*)k_mmq_q6_stream<DOTS>, Q6S_SMEM, attr);
     if (e != MMQ_OK) {
         report(fn, e, "shared-memory request refused");
         return e;
@@ -1973,15 +2186,31 @@ int launch_q6_stream_t(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
         report(fn, MMQ_ERR_CUDA, "tensor map encoding failed");
         return MMQ_ERR_CUDA;
     }
-    const dim3 grid((unsigned)boxes, (unsigned)passes, (unsigned)S);
     // one chunk's transfer at this CTA's share of about 6 TB/s (bytes / (bytes per ns));
     // at most 2 us (a bounded wait)
-    const int64_t ctas = std::min<int64_t>(boxes * passes * S, device_shape().sms);
+    const int64_t ctas = std::min<int64_t>(boxes * passes * std::max(S, zg), device_shape().sms);
     const unsigned stagger = (unsigned)std::min<int64_t>(2000, (int64_t)(Q6S_WBYTES + 8 * Q6S_XROW) * ctas / 6000);
-    ProfScope ps("k_mmq_q6_stream", s);
-    return pdl_status(launch_pdl_zcluster(k_mmq_q6_stream<DOTS>, grid, dim3(Q6S_THREADS), (size_t)Q6S_SMEM, s,
-                                          (unsigned)S, tw, tx, txl, (int)M, (int)N, nb, stagger, out, dots),
-                      fn);
+    SplitScratch ss;
+    return launch_stream_split(
+        zg, M, N, out, s, fn,
+        [&](float* o, long long pstride, unsigned gz) {
+            ProfScope ps("k_mmq_q6_stream", s);
+            const dim3 blk(Q6S_THREADS);
+            if (gz > 1) {
+                const int st = pdl_status(launch_pdl(k_mmq_q6_stream<false, true>,
+                                                     dim3((unsigned)boxes, (unsigned)passes, gz), blk,
+                                                     (size_t)Q6S_SMEM, s, tw, tx, txl, (int)M, (int)N, nb, stagger, o,
+                                                     pstride, dots),
+                                          fn);
+                return st == MMQ_OK ? split_scratch_bind(ss, s, fn) : st;
+            }
+            return pdl_status(launch_pdl_zcluster(k_mmq_q6_stream<DOTS>, dim3((unsigned)boxes, (unsigned)passes,
+                                                                                (unsigned)S),
+                                                  blk, (size_t)Q6S_SMEM, s, (unsigned)S, tw, tx, txl, (int)M, (int)N,
+                                                  nb, stagger, o, pstride, dots),
+                              fn);
+        },
+        &ss);
 }
 
 int launch_q6_stream(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t N, int nb, float* out, int32_t* dots,
@@ -2005,7 +2234,8 @@ double q6_stream_cost_us(int64_t M, int64_t N, int64_t K) {
     const int nb = (int)(K / QK);
     if (K % QK_K != 0 || !q6_stream_fits(N, nb)) return -1.0;
     const int64_t nch = nb / 16, boxes = (N + 127) / 128, passes = (M + 7) / 8, sms = device_shape().sms;
-    const int64_t S = q6_stream_splits(boxes, passes, nch);
+    const int64_t zg = q6_stream_gsplits(boxes, passes, nch);
+    const int64_t S = zg > 1 ? zg : q6_stream_splits(boxes, passes, nch);
     const int64_t waves = (boxes * passes * S + sms - 1) / sms;
     return (double)(waves * ((nch + S - 1) / S)) * 1.9 + 3.5;
 }
@@ -2048,6 +2278,10 @@ unsigned small_take_error() {
 std::atomic<int> g_small_route{SMALL_ROUTE_AUTO};
 
 int small_set_route(int route) { return g_small_route.exchange(route); }
+void small_set_ksplit(int splits, int boxes) {
+    g_small_kboxes.store(boxes);
+    g_small_ksplit.store(splits);
+}
 
 int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, int64_t K, float* out,
                  int32_t* dots, cudaStream_t s) {
@@ -2085,17 +2319,16 @@ int small_launch(int fmt, const void* xq, const void* wq, int64_t M, int64_t N, 
         return MMQ_ERR_SHAPE;
     }
     // measured crossovers (GEMM alone, back-to-back graph launches, 7B projections): the dp4a
-    // weight stream for one row (Q4_K 18944 x 3584: 8.7 us against 9.9); for two rows when
-    // the tensor-core stream would run one 16-row tile per CTA through a long K (3584 x
-    // 18944: 12.0 us against 16.1) or for Q5_K (12.9 against 13.9); for three or four rows
-    // only Q5_K on such a long K (18.7 against 20.4); the tensor-core streams otherwise (Q4_K
-    // 4 x 18944 x 3584: 10.1 us against 17.8)
+    // weight stream for one row (Q4_K 18944 x 3584: 8.7 us against 9.9); for two rows of Q5_K
+    // (12.9 against 13.9), and of Q4_K when the tensor-core stream would run few 16-row tiles
+    // per SM through a long K (3584 x 18944: 11.9 us against 13.1 with its K split); the
+    // tensor-core streams otherwise (Q4_K 4 x 18944 x 3584: 10.1 us against 17.8; on 3584 x
+    // 18944 Q8_0 two rows 17.0 against 18.5, Q5_K four rows 16.9 against 18.6)
     const int route = g_small_route.load();
     const bool long_narrow = (N + 15) / 16 <= 2 * (int64_t)device_shape().sms && nb / 8 >= 32;
-    const int64_t auto_max = M <= 1                                  ? 1
-                             : (fmt == FMT_Q5_K || long_narrow) && M <= 2 ? 2
-                             : fmt == FMT_Q5_K && long_narrow         ? 4
-                                                                      : 0;
+    const int64_t auto_max = M <= 1                                                         ? 1
+                             : (fmt == FMT_Q5_K || (long_narrow && fmt == FMT_Q4_K)) && M <= 2 ? 2
+                                                                                             : 0;
     const int64_t dp4a_max_m = route == SMALL_ROUTE_DP4A ? 4 : route == SMALL_ROUTE_MMA ? 0 : auto_max;
     if (nb % 8 == 0 && M <= dp4a_max_m && ds_smem_bytes(fmt, M <= 1 ? 1 : M <= 2 ? 2 : 4, 4, nb) <= 220 * 1024)
         return fmt == FMT_Q8_0   ? launch_dp4a_stream<FMT_Q8_0>(x8, w8, M, N, nb, out, dots, s, sfn)

@@ -161,8 +161,10 @@ int mmq_gemm_q5_k(const void* xq, const void* wq, int64_t M, int64_t N, int64_t 
  * min term).  K % 256 == 0; alignment and accuracy as mmq_gemm_q8_0.  Runs on the
  * expanded-code tensor-core path and on two small-M kernels: the Q6_K tensor-core stream
  * (8 activation rows per pass, for K % 512 == 0 and N % 8 == 0, from two rows on; the
- * matrix copied as lines of eight rows, K split over a cluster for small N) and the dp4a
- * stream (1, 2 or 4 rows per pass) for one row and the shapes the former does not take.
+ * matrix copied as lines of eight rows; for small N, K split over a cluster of 2, 4 or 8
+ * CTAs, or over up to 16 independent CTAs whose partial tiles a summing kernel adds in
+ * split order where that leaves each CTA fewer chunks of K) and the dp4a stream (1, 2 or 4
+ * rows per pass) for one row and the shapes the former does not take.
  * The converter kernel (MMQ_PATH_TC) refuses it with MMQ_ERR_ARG, and the dp4a stream
  * refuses (MMQ_ERR_SHAPE) a K whose activation rows do not fit in shared memory (above
  * about 120000).
@@ -308,10 +310,10 @@ int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* t
 /*
  * Which small-M kernel takes a shape on MMQ_PATH_SMALL (or on MMQ_PATH_AUTO when the
  * automatic choice is the small path), for K % 256 == 0:
- *   0  the measured choice (default): the dp4a weight stream for one row; for two rows
- *      when the weight has at most two 16-row tiles per SM and K >= 8192 (a long K through
- *      few tiles), or for Q5_K; for three or four rows only Q5_K with such a long K; the
- *      tensor-core stream otherwise (Q6_K: from two rows on, three on such a long K);
+ *   0  the measured choice (default): the dp4a weight stream for one row; for two rows of
+ *      Q5_K, and of Q4_K when the weight has at most two 16-row tiles per SM and K >= 8192
+ *      (a long K through few tiles); the tensor-core stream otherwise (Q6_K: from two rows
+ *      on, three on such a long K);
  *   1  the dp4a weight stream for up to four rows, the tensor-core stream beyond (Q6_K:
  *      the dp4a stream at every row count, four rows per pass);
  *   2  the tensor-core stream for every row count.
@@ -322,6 +324,26 @@ int mmq_debug_expand_tiling(int fmt, int64_t M, int64_t N, int64_t K, int32_t* t
  * route outside 0..2 (nothing changed).  Process-wide.
  */
 int mmq_debug_small_route(int route);
+
+/*
+ * Test switch: the K splits of the Q8_0 / Q4_K / Q5_K tensor-core streams (the small-M
+ * kernels of route 2 above).  splits = 0 (the default): a one-pass grid (up to eight rows)
+ * whose CTAs would load the SMs unevenly is split — the boxes per CTA t and splits z that
+ * minimise a CTA's work, t boxes x ceil(K / 256 / z) super-blocks, among grids resident in
+ * one wave (two CTAs per SM) that leave every warp two super-blocks or more, taken where
+ * that saves more than 15 % (3584 x 18944 through up to eight rows: t = 3, z = 4, 300
+ * CTAs, against 224 one-box CTAs; 512 x 18944: t = 1, z = 4).  splits in 1..8: that many splits (at most K / 256) on
+ * every such call, with `boxes` boxes per CTA (1..4, at most the kernel's own maximum; 0:
+ * the unsplit grid's); splits = 1 never splits (and keeps the Q6_K tensor-core stream on
+ * its cluster split: see mmq_gemm_q6_k).  Each split writes its partial outputs to a
+ * slab of scratch (stream-ordered, like every other call's; under stream capture a graph
+ * allocation node outside the stream's chain of kernels) and a summing kernel adds the
+ * slabs in split order, the same order on every call: results are deterministic and within
+ * the same tolerance whatever the setting.  The block-dot hooks never split.  Returns
+ * MMQ_OK, or MMQ_ERR_ARG for splits outside 0..8 or boxes outside 0..4 (nothing changed).
+ * Process-wide.
+ */
+int mmq_debug_small_ksplit(int splits, int boxes);
 
 /*
  * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1), mmq_gemm_q5_k (fmt 2)

@@ -58,6 +58,13 @@ def test_small_route_round_trip():
     assert mmq.mmq_debug_small_route(prev) == prev
 
 
+def test_small_ksplit_switch_arguments():
+    mmq.mmq_debug_small_ksplit(8, 4)
+    mmq.mmq_debug_small_ksplit(0, 0)
+    for bad in ((9, 0), (-1, 0), (2, 5), (2, -1)):
+        assert mmq.lib().mmq_debug_small_ksplit(*bad) == -9
+
+
 def test_expand_tiling_rule():
     """The expanded path's tile width and K splits (host-only query; with no device it
     assumes 152 SMs, the count of the GPU the rule was measured on)."""

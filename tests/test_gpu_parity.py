@@ -339,6 +339,114 @@ def test_tens_of_rows_small_path_parity_and_dots(mmq, fmt):
     assert mmq.mmq_get_device_error() == 0
 
 
+# K splits of the Q8_0 / Q4_K / Q5_K tensor-core streams, forced to 2, 3, 5 and 8 splits
+# with 1 to 4 boxes per CTA: super-blocks dealt unevenly among the splits (K = 2048 under 8
+# splits: one each), passes with rows past M, boxes with rows past N, CTAs with fewer boxes
+# than the others.  Within the tolerance, the same bits on a
+# second call, and the summing kernel launched once per call.
+KSPLIT_SHAPES = [(1, 40, 2048), (3, 77, 4096), (8, 264, 4608), (13, 520, 2816), (9, 33, 7168)]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
+def test_stream_k_split_parity_and_determinism(mmq, fmt):
+    set_path(mmq, "small")
+    route = mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_MMA)
+    try:
+        for (M, N, K) in KSPLIT_SHAPES:
+            x = synth.activations(M * 13 + N, M, K, True)
+            w = synth.weights(fmt, N * 3 + K, N, K)
+            xq = mmq.mmq_quantize_q8_1(dev(x))
+            wd = dev(w)
+            ref, norm = oracle.gemm(fmt, oracle.quantize_q8_1(x), w, M, N, K)
+            mmq.mmq_debug_small_ksplit(1)
+            whole = mmq.gemm(fmt, xq, wd, M, N, K)
+            check_close(whole.cpu().numpy(), ref, norm, f"{fmt} {M}x{N}x{K} unsplit")
+            for z, boxes in ((2, 0), (3, 2), (5, 4), (8, 3)):
+                mmq.mmq_debug_small_ksplit(z, boxes)
+                torch.cuda.synchronize()
+                mmq.mmq_profile_read(reset=True)
+                was = mmq.mmq_profile_enable(True)
+                try:
+                    out = torch.full((M, N), float("nan"), device="cuda")
+                    mmq.gemm(fmt, xq, wd, M, N, K, out=out)
+                    torch.cuda.synchronize()
+                    prof = mmq.mmq_profile_read(reset=True)
+                finally:
+                    mmq.mmq_profile_enable(was)
+                assert prof.get("k_stream_ksum", (0, 0))[0] == 1, (fmt, M, N, K, z, prof)
+                o = out.cpu().numpy()
+                assert not np.isnan(o).any(), f"{fmt} {M}x{N}x{K} z={z}: output not fully written"
+                check_close(o, ref, norm, f"{fmt} {M}x{N}x{K} z={z}")
+                again = mmq.gemm(fmt, xq, wd, M, N, K)
+                assert torch.equal(again, out), f"{fmt} {M}x{N}x{K} z={z}: repeat differs"
+    finally:
+        mmq.mmq_debug_small_ksplit(0)
+        mmq.mmq_debug_small_route(route)
+    assert mmq.mmq_get_device_error() == 0
+
+
+# the measured rule: 3 boxes per CTA x 4 splits for 3584 x 18944 through eight rows (against
+# 224 one-box CTAs of 74 super-blocks on 152 SMs), none for 18944 x 3584 or for sixteen
+# rows; the split call in a
+# captured graph (its scratch a graph allocation outside the chain of kernels) replays to
+# the eager call's bits, next to an unsplit call captured after it
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
+def test_stream_k_split_rule_and_graph_capture(mmq, fmt):
+    set_path(mmq, "auto")
+    route = mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_AUTO)
+    mmq.mmq_debug_small_ksplit(0)
+    try:
+        def launches(M, N, K, xq, wd):
+            torch.cuda.synchronize()
+            mmq.mmq_profile_read(reset=True)
+            was = mmq.mmq_profile_enable(True)
+            try:
+                out = mmq.gemm(fmt, xq, wd, M, N, K)
+                torch.cuda.synchronize()
+                return out, mmq.mmq_profile_read(reset=True)
+            finally:
+                mmq.mmq_profile_enable(was)
+
+        M, N, K = 8, 3584, 18944
+        x = synth.activations(77, M, K, True)
+        w = synth.weights(fmt, 78, N, K)
+        xq, wd = mmq.mmq_quantize_q8_1(dev(x)), dev(w)
+        eager, prof = launches(M, N, K, xq, wd)
+        assert prof.get("k_stream_ksum", (0, 0))[0] == 1, prof
+        im, inn = sample_entries(M, N, 400, 5)
+        ref, norm = oracle.gemm_at(fmt, oracle.quantize_q8_1(x), w, M, N, K, im, inn)
+        check_close(eager.cpu().numpy()[im, inn], ref, norm, f"{fmt} {M}x{N}x{K} split")
+        for (m2, n2, k2) in [(8, 18944, 3584), (16, 3584, 18944)]:
+            x2 = synth.activations(m2 + n2, m2, k2, True)
+            w2 = synth.weights(fmt, n2 + k2, n2, k2)
+            _, p2 = launches(m2, n2, k2, mmq.mmq_quantize_q8_1(dev(x2)), dev(w2))
+            assert "k_stream_ksum" not in p2, (m2, n2, k2, p2)
+
+        x2 = synth.activations(79, 4, 3584, True)
+        w2 = synth.weights(fmt, 80, 512, 3584)
+        xq2, wd2 = mmq.mmq_quantize_q8_1(dev(x2)), dev(w2)
+        eager2 = mmq.gemm(fmt, xq2, wd2, 4, 512, 3584)
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        out = torch.full((M, N), float("nan"), device="cuda")
+        out2 = torch.full((4, 512), float("nan"), device="cuda")
+        with torch.cuda.graph(g, stream=s):
+            mmq.gemm(fmt, xq, wd, M, N, K, out=out, stream=s)
+            mmq.gemm(fmt, xq2, wd2, 4, 512, 3584, out=out2, stream=s)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager), f"{fmt}: captured split call differs from the eager one"
+        assert torch.equal(out2, eager2), f"{fmt}: captured call after the split differs"
+        del g
+    finally:
+        mmq.mmq_debug_small_ksplit(0)
+        mmq.mmq_debug_small_route(route)
+    assert mmq.mmq_get_device_error() == 0
+
+
 # quantize + contraction in one call: on the expanded path the quantize is fused into the
 # activation expansion.  xq must hold the q8_1 bytes of x and out must equal the separate
 # quantize + gemm calls on the same path bit for bit (same kernels downstream of the
