@@ -1908,7 +1908,10 @@ inline int64_t stream_tpc(int64_t nboxes, int max_boxes) {
 // pieces a CTA), 19.2 with 3 boxes x 2 splits on 150 (111 pieces, one CTA per SM), 15.2
 // with 2 x 2 or 4 x 4 (74 / 76), 18.5 with 4 x 8 (two waves); 512 x 18944 11.0 unsplit,
 // 5.5 with 4 splits.  Passes of more rows keep their grid (the path choice's cost model is
-// measured on it).
+// measured on it).  Outside stream capture a split call costs the host about 14 us (the
+// second launch, the scratch calls), more than the GPU time it saves on small weights:
+// eager calls split only weights of 32 MB and more (back to back, 512 x 18944 Q4_K 11.3 ->
+// 13.9 us split, 3584 x 18944 16.7 -> 14.5).
 std::atomic<int> g_small_ksplit{0};  // test switches: splits (0: the rule) and boxes per CTA (0: the launcher's)
 std::atomic<int> g_small_kboxes{0};
 
@@ -1917,13 +1920,26 @@ struct StreamGrid {
     int z;
 };
 
-inline StreamGrid stream_grid(int64_t nboxes, int max_boxes, int64_t passes, int64_t pieces, int warps) {
+constexpr int64_t EAGER_SPLIT_MIN_BYTES = (int64_t)32 << 20;
+
+// true when `s` is being captured (a split's host cost is then paid once, at capture)
+inline bool stream_captured(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
+inline StreamGrid stream_grid(int64_t nboxes, int max_boxes, int64_t passes, int64_t pieces, int warps,
+                              int64_t wbytes, cudaStream_t s) {
     const int64_t base = stream_tpc(nboxes, max_boxes);
     const int forced = g_small_ksplit.load(), fboxes = g_small_kboxes.load();
     if (forced > 0)
         return {fboxes > 0 ? std::min<int64_t>(fboxes, max_boxes) : base,
                 (int)std::min<int64_t>(forced, std::max<int64_t>(pieces, 1))};
-    if (passes != 1) return {base, 1};
+    if (passes != 1 || (wbytes < EAGER_SPLIT_MIN_BYTES && !stream_captured(s))) return {base, 1};
     const int64_t sms = device_shape().sms;
     auto ctas = [&](int64_t t, int64_t z) { return (nboxes + t - 1) / t * z; };
     auto cost = [&](int64_t t, int64_t z) { return t * ((pieces + z - 1) / z); };
@@ -2048,7 +2064,8 @@ int launch_i8_stream_q8_0(const uint8_t* x8, const uint8_t* w8, int64_t M, int64
                           int32_t* dots, cudaStream_t s, const char* fn) {
     const int64_t ntiles = (N + 15) / 16;
     const StreamGrid sg = dots ? StreamGrid{stream_tpc(ntiles, IS_MAX_TPC), 1}
-                               : stream_grid(ntiles, IS_MAX_TPC, (M + 7) / 8, nb / 8, IS_WARPS);
+                               : stream_grid(ntiles, IS_MAX_TPC, (M + 7) / 8, nb / 8, IS_WARPS,
+                                             N * (int64_t)nb * Q8_0_BYTES, s);
     const int64_t tpc = sg.tpc;
     static SmemAttr attr, attr_d, attr_s;
     const int e = dots       ? ensure_smem((const void*)k_mmq_i8_stream<true>, I8_SMEM, attr_d)
@@ -2091,7 +2108,8 @@ int launch_kq_stream_b(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
                        int32_t* dots, cudaStream_t s, const char* fn) {
     const int64_t nboxes = (N + BOXR - 1) / BOXR;
     const StreamGrid sg = dots ? StreamGrid{stream_tpc(nboxes, ks_max_boxes(BOXR)), 1}
-                               : stream_grid(nboxes, ks_max_boxes(BOXR), (M + 7) / 8, nb / 8, ks_warps(FMT, BOXR));
+                               : stream_grid(nboxes, ks_max_boxes(BOXR), (M + 7) / 8, nb / 8, ks_warps(FMT, BOXR),
+                                             N * (int64_t)(nb / 8) * kq_bytes(FMT), s);
     const int64_t tpc = sg.tpc;
     constexpr int smem = ks_smem_bytes(FMT, BOXR);
     static SmemAttr attr, attr_d, attr_s;
@@ -2159,7 +2177,8 @@ int q6_stream_splits(int64_t boxes, int64_t passes, int64_t nch) {
 // splits, 8 chunks a CTA, against clusters of 4 and 10; five CTAs of a cluster would not
 // pack into the GPCs).  1: the cluster split.
 int q6_stream_gsplits(int64_t boxes, int64_t passes, int64_t nch) {
-    if (g_small_ksplit.load() == 1) return 1;  // the test switch's "never split"
+    const int forced = g_small_ksplit.load();  // the test switch: 1 never, n > 1 n splits
+    if (forced > 0) return (int)std::min<int64_t>(forced, nch);
     const int64_t sms = device_shape().sms, S = q6_stream_splits(boxes, passes, nch);
     int zg = 1;
     for (int z = 2; z <= 16 && z <= nch && boxes * passes * z <= sms; ++z)
@@ -2172,7 +2191,10 @@ int launch_q6_stream_t(const uint8_t* x8, const uint8_t* w8, int64_t M, int64_t 
                        int32_t* dots, cudaStream_t s, const char* fn) {
     const int64_t nsb = nb / 8, nch = nsb / 2, boxes = (N + 127) / 128, passes = (M + 7) / 8;
     const int S = q6_stream_splits(boxes, passes, nch);
-    const int zg = DOTS ? 1 : q6_stream_gsplits(boxes, passes, nch);
+    const int zg = DOTS || (g_small_ksplit.load() == 0 && N * nsb * Q6_K_BYTES < EAGER_SPLIT_MIN_BYTES &&
+                            !stream_captured(s))
+                       ? 1
+                       : q6_stream_gsplits(boxes, passes, nch);
     static SmemAttr attr, attr_g;
     const int e = zg > 1 ? ensure_smem((const void*)k_mmq_q6_stream<false, true>, Q6S_SMEM, attr_g)
                          : ensure_smem((const void*)k_mmq_q6_stream<DOTS>, Q6S_SMEM, attr);

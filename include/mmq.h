@@ -334,8 +334,11 @@ int mmq_debug_small_route(int route);
  * that saves more than 15 % (3584 x 18944 through up to eight rows: t = 3, z = 4, 300
  * CTAs, against 224 one-box CTAs; 512 x 18944: t = 1, z = 4).  splits in 1..8: that many splits (at most K / 256) on
  * every such call, with `boxes` boxes per CTA (1..4, at most the kernel's own maximum; 0:
- * the unsplit grid's); splits = 1 never splits (and keeps the Q6_K tensor-core stream on
- * its cluster split: see mmq_gemm_q6_k).  Each split writes its partial outputs to a
+ * the unsplit grid's); splits = 1 never splits.  The Q6_K tensor-core stream follows the
+ * same switch for its split over independent CTAs (see mmq_gemm_q6_k): 1 keeps it on its
+ * cluster split, n > 1 takes n splits (at most K / 512).  Outside stream capture the rule
+ * splits only weights of 32 MB and more (a split call's host cost exceeds what it saves on
+ * smaller ones).  Each split writes its partial outputs to a
  * slab of scratch (stream-ordered, like every other call's; under stream capture a graph
  * allocation node outside the stream's chain of kernels) and a summing kernel adds the
  * slabs in split order, the same order on every call: results are deterministic and within

@@ -385,6 +385,42 @@ def test_stream_k_split_parity_and_determinism(mmq, fmt):
     assert mmq.mmq_get_device_error() == 0
 
 
+# the Q6_K tensor-core stream split over independent CTAs (forced 2, 3 and 5 splits: chunks
+# dealt unevenly, several passes, boxes with rows past N) against the oracle, the same bits
+# on a second call, and the summing kernel launched once
+@pytest.mark.parametrize("M,N,K", [(8, 128, 7168), (13, 264, 1536), (5, 1000, 5120), (3, 3584, 3584)])
+def test_q6_k_stream_split_parity(mmq, M, N, K):
+    set_path(mmq, "small")
+    route = mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_MMA)
+    try:
+        x = synth.activations(M * 17 + N, M, K, True)
+        w = synth.weights("q6_k", N * 11 + K, N, K)
+        xq, wd = mmq.mmq_quantize_q8_1(dev(x)), dev(w)
+        ref, norm = oracle.gemm("q6_k", oracle.quantize_q8_1(x), w, M, N, K)
+        for z in (2, 3, 5):
+            mmq.mmq_debug_small_ksplit(z, 0)
+            torch.cuda.synchronize()
+            mmq.mmq_profile_read(reset=True)
+            was = mmq.mmq_profile_enable(True)
+            try:
+                out = torch.full((M, N), float("nan"), device="cuda")
+                mmq.gemm("q6_k", xq, wd, M, N, K, out=out)
+                torch.cuda.synchronize()
+                prof = mmq.mmq_profile_read(reset=True)
+            finally:
+                mmq.mmq_profile_enable(was)
+            assert prof.get("k_mmq_q6_stream", (0, 0))[0] == 1, prof
+            assert prof.get("k_stream_ksum", (0, 0))[0] == 1, (M, N, K, z, prof)
+            o = out.cpu().numpy()
+            assert not np.isnan(o).any(), f"q6_k {M}x{N}x{K} z={z}: output not fully written"
+            check_close(o, ref, norm, f"q6_k {M}x{N}x{K} z={z}")
+            assert torch.equal(mmq.gemm("q6_k", xq, wd, M, N, K), out), f"q6_k {M}x{N}x{K} z={z}: repeat differs"
+    finally:
+        mmq.mmq_debug_small_ksplit(0)
+        mmq.mmq_debug_small_route(route)
+    assert mmq.mmq_get_device_error() == 0
+
+
 # the measured rule: 3 boxes per CTA x 4 splits for 3584 x 18944 through eight rows (against
 # 224 one-box CTAs of 74 super-blocks on 152 SMs), none for 18944 x 3584 or for sixteen
 # rows; the split call in a
