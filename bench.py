@@ -940,8 +940,10 @@ def run_sweep(args):
         cases += [(fmt, M, 3584, 3584, "q") for M in (512, 2048)]
     for fmt in ("q4_k", "q8_0"):  # a few tens of rows
         cases += [(fmt, M, 18944, 3584, "gate") for M in (16, 32, 64)]
-    # tens to hundreds of rows on the long-K projection: few output tiles, K split
-    cases += [("q4_k", M, 3584, 18944, "down") for M in (64, 128, 256)]
+    # tens to hundreds of rows on the long-K projection: few output tiles, K split (the
+    # small-M streams' grids reshaped into one wave up to 40 rows, the expanded path beyond)
+    cases += [("q4_k", M, 3584, 18944, "down") for M in (16, 24, 32, 64, 128, 256)]
+    cases += [("q8_0", 16, 3584, 18944, "down")]
     # three or four rows around 4864 weight rows (two 16-row tiles per SM), where the
     # automatic small-M choice changes kernel for the K-quants
     for fmt in ("q4_k", "q5_k"):
@@ -976,7 +978,8 @@ def run_sweep(args):
             "config": {"workload": "3584x3584 Q4_K projection, M in " + str(synth.M_SWEEP)
                                    + "; M in [1, 2, 4, 8] on 18944x3584 and 3584x18944, Q4_K, Q8_0, Q5_K"
                                    + " and Q6_K; Q5_K and Q6_K 3584x3584 at M = 512, 2048; Q4_K and Q5_K"
-                                   + " M = 3, 4 on N = 4096, 4864, 5632 (K = 3584); up to 8 rows: every"
+                                   + " M = 3, 4 on N = 4096, 4864, 5632 (K = 3584); Q4_K M = 16 ... 256 and"
+                                   + " Q8_0 M = 16 on 3584x18944; up to 8 rows: every"
                                    + " small-M kernel that takes the shape (route) besides the automatic one",
                        "l2": "rotating weight copies >= 3x L2", "cuda_graph": True}}
 

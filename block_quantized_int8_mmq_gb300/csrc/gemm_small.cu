@@ -1896,24 +1896,29 @@ inline int64_t stream_tpc(int64_t nboxes, int max_boxes) {
 }
 
 // ------------------------------------------ K splits of the i8 / kq streams
-// A one-pass stream grid (up to eight rows) whose CTAs would load the SMs unevenly takes z
-// K splits (grid z) and, with them, tpc boxes per CTA: 3584 x 18944 is 224 one-box CTAs on
-// 152 SMs, 72 SMs with two boxes and 80 with one.  Each split writes its partial outputs
-// to a slab of scratch and k_stream_ksum adds the slabs in the order z = 0, 1, ... (the
-// same order at every call, so the output is deterministic).  (tpc, z) minimises a CTA's
-// work, tpc boxes x ceil(pieces / z) pieces, over grids resident in one wave (two CTAs per
-// SM: a second wave pays each CTA's start-up again) that leave each warp two pieces or
-// more, taken where that saves more than 15 %.  Measured (Q4_K, eight rows, graph
-// replays): 3584 x 18944 16.3 us unsplit, 13.25 with 3 boxes x 4 splits on 300 CTAs (57
-// pieces a CTA), 19.2 with 3 boxes x 2 splits on 150 (111 pieces, one CTA per SM), 15.2
-// with 2 x 2 or 4 x 4 (74 / 76), 18.5 with 4 x 8 (two waves); 512 x 18944 11.0 unsplit,
-// 5.5 with 4 splits.  Passes of more rows keep their grid (the path choice's cost model is
-// measured on it).  Outside stream capture a split call costs the host about 14 us (the
-// second launch, the scratch calls), more than the GPU time it saves on small weights:
-// eager calls split only weights of 32 MB and more (back to back, 512 x 18944 Q4_K 11.3 ->
-// 13.9 us split, 3584 x 18944 16.7 -> 14.5).
+// A stream grid whose CTAs would load the SMs unevenly, or that needs a second wave, takes
+// z K splits (grid z) and, with them, tpc boxes per CTA: 3584 x 18944 through eight rows is
+// 224 one-box CTAs on 152 SMs, 72 SMs with two boxes and 80 with one; through sixteen rows,
+// 448 CTAs in two waves.  Each split writes its partial outputs to a slab of scratch and
+// k_stream_ksum adds the slabs in the order z = 0, 1, ... (the same order at every call, so
+// the output is deterministic).  Cost of a grid: its waves (two CTAs per SM resident) x
+// (KS_START + a CTA's pieces, tpc boxes x ceil(pieces / z)), KS_START pieces standing for a
+// CTA's start-up (~5 us, the first activations landing behind the SM's queued weight
+// copies, against ~0.17 us a piece).  The cheapest one-wave grid that leaves each warp two
+// pieces or more is taken where it saves more than 15 %; grids of several passes only for
+// a long K (32 pieces or more, the measured range).  Measured (Q4_K, graph replays):
+// 3584 x 18944, eight rows: 16.3 us unsplit, 13.25 with 3 boxes x 4 splits on 300 CTAs
+// (57 pieces a CTA), 19.2 with 3 x 2 on 150 (111 pieces, one CTA per SM), 15.2 with 2 x 2
+// or 4 x 4 (74 / 76), 18.5 with 4 x 8 (two waves); sixteen rows 25.6 -> 20.9 (3 x 2),
+// Q8_0 32.8 -> 24.7; 24 rows 39.2 -> 34.9 (3 boxes, no split); 4096 x 14336, sixteen rows,
+// 23.9 -> 19.4 (2 boxes, no split); 512 x 18944, eight rows, 11.0 -> 5.5 (4 splits).
+// Outside stream capture a split call costs the host about 14 us (the second launch, the
+// scratch calls), more than the GPU time it saves on small weights: eager calls split only
+// weights of 32 MB and more (back to back, 512 x 18944 Q4_K 11.3 -> 13.9 us split, 3584 x
+// 18944 16.7 -> 14.5); smaller ones may still take more boxes per CTA, unsplit.
 std::atomic<int> g_small_ksplit{0};  // test switches: splits (0: the rule) and boxes per CTA (0: the launcher's)
 std::atomic<int> g_small_kboxes{0};
+constexpr int64_t KS_START = 30;
 
 struct StreamGrid {
     int64_t tpc;
@@ -1939,14 +1944,17 @@ inline StreamGrid stream_grid(int64_t nboxes, int max_boxes, int64_t passes, int
     if (forced > 0)
         return {fboxes > 0 ? std::min<int64_t>(fboxes, max_boxes) : base,
                 (int)std::min<int64_t>(forced, std::max<int64_t>(pieces, 1))};
-    if (passes != 1 || (wbytes < EAGER_SPLIT_MIN_BYTES && !stream_captured(s))) return {base, 1};
-    const int64_t sms = device_shape().sms;
-    auto ctas = [&](int64_t t, int64_t z) { return (nboxes + t - 1) / t * z; };
-    auto cost = [&](int64_t t, int64_t z) { return t * ((pieces + z - 1) / z); };
+    if (passes != 1 && pieces < 32) return {base, 1};
+    const int zmax = wbytes < EAGER_SPLIT_MIN_BYTES && !stream_captured(s) ? 1 : 8;
+    const int64_t slots = 2 * (int64_t)device_shape().sms;
+    auto ctas = [&](int64_t t, int64_t z) { return (nboxes + t - 1) / t * z * passes; };
+    auto cost = [&](int64_t t, int64_t z) {
+        return (ctas(t, z) + slots - 1) / slots * (KS_START + t * ((pieces + z - 1) / z));
+    };
     StreamGrid best{base, 1};
-    for (int z = 2; z <= 8 && pieces >= 2LL * warps * z; ++z)
+    for (int z = 1; z <= zmax && (z == 1 || pieces >= 2LL * warps * z); ++z)
         for (int64_t t = 1; t <= max_boxes; ++t)
-            if (ctas(t, z) <= 2 * sms && cost(t, z) < cost(best.tpc, best.z)) best = {t, z};
+            if (ctas(t, z) <= slots && cost(t, z) < cost(best.tpc, best.z)) best = {t, z};
     return cost(best.tpc, best.z) * 20 < cost(base, 1) * 17 ? best : StreamGrid{base, 1};
 }
 

@@ -327,18 +327,20 @@ int mmq_debug_small_route(int route);
 
 /*
  * Test switch: the K splits of the Q8_0 / Q4_K / Q5_K tensor-core streams (the small-M
- * kernels of route 2 above).  splits = 0 (the default): a one-pass grid (up to eight rows)
- * whose CTAs would load the SMs unevenly is split — the boxes per CTA t and splits z that
- * minimise a CTA's work, t boxes x ceil(K / 256 / z) super-blocks, among grids resident in
- * one wave (two CTAs per SM) that leave every warp two super-blocks or more, taken where
- * that saves more than 15 % (3584 x 18944 through up to eight rows: t = 3, z = 4, 300
- * CTAs, against 224 one-box CTAs; 512 x 18944: t = 1, z = 4).  splits in 1..8: that many splits (at most K / 256) on
- * every such call, with `boxes` boxes per CTA (1..4, at most the kernel's own maximum; 0:
- * the unsplit grid's); splits = 1 never splits.  The Q6_K tensor-core stream follows the
+ * kernels of route 2 above).  splits = 0 (the default): a grid whose CTAs would load the
+ * SMs unevenly, or that would need a second wave, is reshaped — the boxes per CTA t and
+ * splits z of the cheapest grid resident in one wave (two CTAs per SM) that leaves every
+ * warp two super-blocks or more, a grid costing its waves x (a CTA's start-up + t boxes x
+ * ceil(K / 256 / z) super-blocks), taken where that saves more than 15 %; grids of several
+ * 8-row passes only for K >= 8192 (3584 x 18944: t = 3, z = 4 through eight rows, t = 3,
+ * z = 2 through sixteen, against one-box CTAs; 512 x 18944: t = 1, z = 4).  splits in 1..8:
+ * that many splits (at most K / 256) on every such call, with `boxes` boxes per CTA (1..4,
+ * at most the kernel's own maximum; 0: the launcher's own); splits = 1 keeps the launcher's
+ * grid, unsplit.  The Q6_K tensor-core stream follows the
  * same switch for its split over independent CTAs (see mmq_gemm_q6_k): 1 keeps it on its
  * cluster split, n > 1 takes n splits (at most K / 512).  Outside stream capture the rule
  * splits only weights of 32 MB and more (a split call's host cost exceeds what it saves on
- * smaller ones).  Each split writes its partial outputs to a
+ * smaller ones; those may still take more boxes per CTA, unsplit).  Each split writes its partial outputs to a
  * slab of scratch (stream-ordered, like every other call's; under stream capture a graph
  * allocation node outside the stream's chain of kernels) and a summing kernel adds the
  * slabs in split order, the same order on every call: results are deterministic and within

@@ -422,8 +422,8 @@ def test_q6_k_stream_split_parity(mmq, M, N, K):
 
 
 # the measured rule: 3 boxes per CTA x 4 splits for 3584 x 18944 through eight rows (against
-# 224 one-box CTAs of 74 super-blocks on 152 SMs), none for 18944 x 3584 or for sixteen
-# rows; the split call in a
+# 224 one-box CTAs of 74 super-blocks on 152 SMs) and 3 x 2 through sixteen, none for
+# 18944 x 3584 at eight or sixteen rows; the split call in a
 # captured graph (its scratch a graph allocation outside the chain of kernels) replays to
 # the eager call's bits, next to an unsplit call captured after it
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
@@ -452,11 +452,18 @@ def test_stream_k_split_rule_and_graph_capture(mmq, fmt):
         im, inn = sample_entries(M, N, 400, 5)
         ref, norm = oracle.gemm_at(fmt, oracle.quantize_q8_1(x), w, M, N, K, im, inn)
         check_close(eager.cpu().numpy()[im, inn], ref, norm, f"{fmt} {M}x{N}x{K} split")
-        for (m2, n2, k2) in [(8, 18944, 3584), (16, 3584, 18944)]:
+        for (m2, n2, k2) in [(8, 18944, 3584), (16, 18944, 3584)]:
             x2 = synth.activations(m2 + n2, m2, k2, True)
             w2 = synth.weights(fmt, n2 + k2, n2, k2)
             _, p2 = launches(m2, n2, k2, mmq.mmq_quantize_q8_1(dev(x2)), dev(w2))
             assert "k_stream_ksum" not in p2, (m2, n2, k2, p2)
+        # two passes through the long K: 3 boxes x 2 splits in one wave
+        x3 = synth.activations(81, 16, K, True)
+        out3, p3 = launches(16, N, K, mmq.mmq_quantize_q8_1(dev(x3)), wd)
+        assert p3.get("k_stream_ksum", (0, 0))[0] == 1, p3
+        im, inn = sample_entries(16, N, 400, 6)
+        ref, norm = oracle.gemm_at(fmt, oracle.quantize_q8_1(x3), w, 16, N, K, im, inn)
+        check_close(out3.cpu().numpy()[im, inn], ref, norm, f"{fmt} 16x{N}x{K} split")
 
         x2 = synth.activations(79, 4, 3584, True)
         w2 = synth.weights(fmt, 80, 512, 3584)
