@@ -379,8 +379,8 @@ def kernel_table(prof, steps):
 
 
 def measure_config(args, workload, rank, world, local, steps, with_e2e=True):
-    """One workload of BASELINE's configs: quantize + contraction per step (c1, c2, c3), or
-    the quantize alone (c3q).  Returns its bench entry."""
+    """One of the named projection workloads: quantize + contraction per step (c1, c2, c3),
+    or the quantize alone (c3q).  Returns its bench entry."""
     import torch
     import block_quantized_int8_mmq_gb300 as mmq
     dev = torch.device("cuda", local)
