@@ -428,6 +428,8 @@ def test_q6_k_stream_split_parity(mmq, M, N, K):
 # the eager call's bits, next to an unsplit call captured after it
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
 def test_stream_k_split_rule_and_graph_capture(mmq, fmt):
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the grids are those of a 152-SM GB300")
     set_path(mmq, "auto")
     route = mmq.mmq_debug_small_route(mmq.SMALL_ROUTE_AUTO)
     mmq.mmq_debug_small_ksplit(0)
