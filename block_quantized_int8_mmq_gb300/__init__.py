@@ -27,6 +27,7 @@ EXPORTED = (
     "mmq_gemm_q6_k", "mmq_linear_q6_k", "mmq_debug_block_dots_q6_k", "mmq_gemm_grouped_q5_k",
     "mmq_debug_product_dots", "mmq_debug_refuse_smem", "mmq_debug_set_wait_limit",
     "mmq_debug_small_route", "mmq_debug_expand_tiling", "mmq_gemm_grouped_q6_k", "mmq_debug_small_ksplit",
+    "mmq_debug_small_grid",
 )
 
 
@@ -67,6 +68,7 @@ def _load():
     L.mmq_debug_refuse_smem.argtypes = [I]
     L.mmq_debug_small_route.argtypes = [I]
     L.mmq_debug_small_ksplit.argtypes = [I, I]
+    L.mmq_debug_small_grid.argtypes = [I, I64, I64, I64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     L.mmq_debug_expand_tiling.argtypes = [I, I64, I64, I64, ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32)]
     L.mmq_debug_set_wait_limit.argtypes = [I64]
@@ -228,6 +230,16 @@ def mmq_debug_small_ksplit(splits: int, boxes: int = 0) -> None:
     """K splits of the Q8_0 / Q4_K / Q5_K tensor-core streams (0 the measured rule, n > 0 n
     splits, 1 never) and, with forced splits, boxes per CTA (0 the unsplit grid's)."""
     _check("mmq_debug_small_ksplit", _lib.mmq_debug_small_ksplit(int(splits), int(boxes)))
+
+
+def mmq_debug_small_grid(fmt, M: int, N: int, K: int) -> tuple:
+    """(boxes per CTA, K splits) of the Q8_0 / Q4_K / Q5_K tensor-core stream for this shape
+    under stream capture (host-only query)."""
+    b, z = ctypes.c_int32(0), ctypes.c_int32(0)
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check("mmq_debug_small_grid", _lib.mmq_debug_small_grid(f, int(M), int(N), int(K), ctypes.byref(b),
+                                                              ctypes.byref(z)))
+    return b.value, z.value
 
 
 def mmq_debug_expand_tiling(fmt, M: int, N: int, K: int) -> tuple:

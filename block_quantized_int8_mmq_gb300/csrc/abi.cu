@@ -91,6 +91,9 @@ double q6_stream_cost_us(int64_t M, int64_t N, int64_t K);
 // Test switch of the Q8_0 / Q4_K / Q5_K tensor-core streams' K splits (0: the measured rule,
 // n > 0: n splits) and boxes per CTA with a forced split (0: the launcher's) (gemm_small.cu).
 void small_set_ksplit(int splits, int boxes);
+// The Q8_0 / Q4_K / Q5_K tensor-core stream's grid for a shape under stream capture: boxes
+// per CTA and K splits (gemm_small.cu; host only).
+void small_stream_grid(int fmt, int64_t M, int64_t N, int64_t K, int32_t* boxes, int32_t* splits);
 
 namespace {
 
@@ -432,6 +435,22 @@ int mmq_debug_refuse_smem(int on) { return g_refuse_smem.exchange(on ? 1 : 0); }
 int mmq_debug_small_route(int route) {
     if (route < SMALL_ROUTE_AUTO || route > SMALL_ROUTE_MMA) return MMQ_ERR_ARG;
     return small_set_route(route);
+}
+
+int mmq_debug_small_grid(int fmt, int64_t M, int64_t N, int64_t K, int32_t* boxes, int32_t* splits) {
+    const char* fn = "mmq_debug_small_grid";
+    if (fmt != FMT_Q8_0 && fmt != FMT_Q4_K && fmt != FMT_Q5_K) {
+        report(fn, MMQ_ERR_ARG, "fmt must be 0 (Q8_0), 1 (Q4_K) or 2 (Q5_K)");
+        return MMQ_ERR_ARG;
+    }
+    const int st = check_mk(fn, M, N, K, QK_K);
+    if (st) return st;
+    if (!boxes || !splits) {
+        report(fn, MMQ_ERR_NULL, "boxes and splits must be non-NULL");
+        return MMQ_ERR_NULL;
+    }
+    small_stream_grid(fmt, M, N, K, boxes, splits);
+    return MMQ_OK;
 }
 
 int mmq_debug_small_ksplit(int splits, int boxes) {

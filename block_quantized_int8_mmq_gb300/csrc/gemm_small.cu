@@ -32,6 +32,7 @@
 // before any math, so the DRAM latency is paid once per batch; the warps reduce through
 // shared memory at the end.
 #include <algorithm>
+#include <cstdint>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -2308,6 +2309,23 @@ unsigned small_take_error() {
 std::atomic<int> g_small_route{SMALL_ROUTE_AUTO};
 
 int small_set_route(int route) { return g_small_route.exchange(route); }
+
+// The grid the Q8_0 / Q4_K / Q5_K tensor-core stream takes for M x N x K under stream
+// capture (no eager size floor): boxes per CTA and K splits.  Host only.
+void small_stream_grid(int fmt, int64_t M, int64_t N, int64_t K, int32_t* boxes, int32_t* splits) {
+    const int nb = (int)(K / QK);
+    StreamGrid g{1, 1};
+    if (fmt == FMT_Q8_0) {
+        g = stream_grid((N + 15) / 16, IS_MAX_TPC, (M + 7) / 8, nb / 8, IS_WARPS, INT64_MAX, nullptr);
+    } else {
+        const bool wide = (N + 31) / 32 >= 2 * (int64_t)device_shape().sms;
+        const int boxr = wide ? 32 : 16;
+        g = stream_grid((N + boxr - 1) / boxr, ks_max_boxes(boxr), (M + 7) / 8, nb / 8, ks_warps(fmt, boxr), INT64_MAX,
+                        nullptr);
+    }
+    *boxes = (int32_t)g.tpc;
+    *splits = g.z;
+}
 void small_set_ksplit(int splits, int boxes) {
     g_small_kboxes.store(boxes);
     g_small_ksplit.store(splits);

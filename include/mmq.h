@@ -351,6 +351,16 @@ int mmq_debug_small_route(int route);
 int mmq_debug_small_ksplit(int splits, int boxes);
 
 /*
+ * Host-only query: the grid the Q8_0 (fmt 0), Q4_K (1) or Q5_K (2) tensor-core stream takes
+ * for an M x N x K call made under stream capture (the rule and the test switch above; no
+ * eager size floor) on the current device, or on a 152-SM GB300 when no device is present:
+ * *boxes = weight boxes per CTA (16 rows each, 32 where N / 32 >= 2 x SMs), *splits = K
+ * splits.  Launches nothing.  MMQ_OK; MMQ_ERR_ARG for another fmt, MMQ_ERR_SHAPE /
+ * MMQ_ERR_K_MULTIPLE for a shape the stream does not take (K % 256 != 0), MMQ_ERR_NULL.
+ */
+int mmq_debug_small_grid(int fmt, int64_t M, int64_t N, int64_t K, int32_t* boxes, int32_t* splits);
+
+/*
  * The contraction of mmq_gemm_q8_0 (fmt 0), mmq_gemm_q4_k (fmt 1), mmq_gemm_q5_k (fmt 2)
  * or mmq_gemm_q6_k (fmt 3) on the expanded-code tensor-core path, with its scratch taken
  * from a fixed 64 MiB array in the library's device memory (one per device) instead of an

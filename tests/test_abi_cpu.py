@@ -65,6 +65,47 @@ def test_small_ksplit_switch_arguments():
         assert mmq.lib().mmq_debug_small_ksplit(*bad) == -9
 
 
+def test_small_stream_grid_rule():
+    """The small-M tensor-core streams' grids under capture (host-only query; with no device
+    it assumes 152 SMs, the count of the GPU the rule was measured on)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("checked against the device's own SM count in the GPU tests")
+    except ImportError:
+        pass
+    g = mmq.mmq_debug_small_grid
+    # 224 one-box CTAs of 74 super-blocks on 304 slots: 3 boxes x 4 splits on 300 CTAs
+    assert g("q4_k", 8, 3584, 18944) == (3, 4)
+    assert g("q8_0", 8, 3584, 18944) == (3, 4)
+    assert g("q5_k", 1, 3584, 18944) == (3, 4)
+    # two passes: 448 CTAs in two waves -> 3 x 2 on 300; three and four passes: 3 boxes, unsplit
+    assert g("q4_k", 16, 3584, 18944) == (3, 2)
+    assert g("q4_k", 24, 3584, 18944) == (3, 1)
+    assert g("q4_k", 32, 3584, 18944) == (3, 1)
+    # few boxes: 32 of them x 4 splits; 128 x 2
+    assert g("q4_k", 8, 512, 18944) == (1, 4)
+    assert g("q4_k", 8, 2048, 18944) == (1, 2)
+    # 4096 x 14336 through sixteen rows: 512 CTAs in two waves -> 2 boxes, one wave
+    assert g("q4_k", 16, 4096, 14336) == (2, 1)
+    # kept: short K (14 super-blocks), a grid already in one even wave, several passes of a short K
+    assert g("q4_k", 8, 3584, 3584) == (1, 1)
+    assert g("q4_k", 8, 18944, 3584) == (2, 1)      # 592 32-row boxes, two per CTA
+    assert g("q8_0", 8, 18944, 3584) == (4, 1)      # 1184 16-row boxes, four per CTA
+    assert g("q4_k", 16, 18944, 3584) == (2, 1)
+    assert g("q4_k", 8, 4096, 14336) == (1, 1)
+    # the test switch: forced splits and boxes, then back to the rule
+    mmq.mmq_debug_small_ksplit(5, 2)
+    try:
+        assert g("q4_k", 8, 3584, 3584) == (2, 5)
+        mmq.mmq_debug_small_ksplit(1, 0)
+        assert g("q4_k", 8, 3584, 18944) == (1, 1)
+    finally:
+        mmq.mmq_debug_small_ksplit(0, 0)
+    assert g("q4_k", 8, 3584, 18944) == (3, 4)
+    assert mmq.lib().mmq_debug_small_grid(3, 8, 3584, 18944, None, None) == -9  # Q6_K: not this stream
+
+
 def test_expand_tiling_rule():
     """The expanded path's tile width and K splits (host-only query; with no device it
     assumes 152 SMs, the count of the GPU the rule was measured on)."""
